@@ -1,0 +1,752 @@
+// C-ABI entry points: descriptors, algorithm table, dispatch, Fast-Run map,
+// device error word and TMA descriptor encoding.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+#define GBCONV_VERSION "gbconv-0.1"
+
+// ---------------------------------------------------------------------------
+// errors
+
+static thread_local char g_detail[512];
+
+conv_status_t gb_fail(conv_status_t st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_detail, sizeof(g_detail), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+static conv_status_t ok_status() {
+  g_detail[0] = 0;
+  return CONV_OK;
+}
+
+static conv_status_t cuda_fail(cudaError_t e, const char* what) {
+  return gb_fail(CONV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Device error word: one int per device in global memory, written by kernels
+// with atomicCAS(0 -> code) when a bounded wait runs out or a check fails.
+__device__ int g_device_error_word;
+
+static constexpr int kMaxDevices = 64;
+static std::mutex g_dev_mu;
+static int* g_err_ptr[kMaxDevices];
+static int g_num_sms[kMaxDevices];
+
+static int current_device() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return dev;
+}
+
+int* gb_device_error_word() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+int gb_num_sms() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return 1;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_num_sms[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    g_num_sms[dev] = n > 0 ? n : 1;
+  }
+  return g_num_sms[dev];
+}
+
+unsigned long long gb_wait_limit_ns() {
+  static unsigned long long v = [] {
+    const char* e = getenv("GBCONV_WAIT_LIMIT_MS");
+    long long ms = e ? atoll(e) : 2000;
+    if (ms <= 0) ms = 2000;
+    return (unsigned long long)ms * 1000000ull;
+  }();
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// TMA descriptor encoding through driver entry points (no -lcuda needed).
+
+typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+typedef CUresult (*PFN_encodeIm2col)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                     const cuuint64_t*, const cuuint64_t*, const int*,
+                                     const int*, cuuint32_t, cuuint32_t, const cuuint32_t*,
+                                     CUtensorMapInterleave, CUtensorMapSwizzle,
+                                     CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static void* driver_fn(const char* name) {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return fn;
+}
+
+CUresult gb_encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, cuuint32_t rank, void* addr,
+                         const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                         const cuuint32_t* estr, CUtensorMapSwizzle swz) {
+  static PFN_encodeTiled fn = (PFN_encodeTiled)driver_fn("cuTensorMapEncodeTiled");
+  if (!fn) return CUDA_ERROR_NOT_FOUND;
+  return fn(map, dt, rank, addr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+CUresult gb_encode_im2col(CUtensorMap* map, CUtensorMapDataType dt, cuuint32_t rank, void* addr,
+                          const cuuint64_t* dims, const cuuint64_t* strides, const int* lower,
+                          const int* upper, cuuint32_t channels, cuuint32_t pixels,
+                          const cuuint32_t* estr, CUtensorMapSwizzle swz) {
+  static PFN_encodeIm2col fn = (PFN_encodeIm2col)driver_fn("cuTensorMapEncodeIm2col");
+  if (!fn) return CUDA_ERROR_NOT_FOUND;
+  return fn(map, dt, rank, addr, dims, strides, lower, upper, channels, pixels, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+// ---------------------------------------------------------------------------
+// descriptor
+
+static int out_dim(int in, int k, int stride, int pad, int dil) {
+  return (int)(((long long)in + 2LL * pad - (long long)dil * (k - 1) - 1) / stride + 1);
+}
+
+extern "C" conv_status_t conv_desc_create(conv_desc_t* out, int N, int C, int H, int W, int K,
+                                          int R, int S, int stride, int pad, int dilation,
+                                          int groups, conv_dtype_t dtype) {
+  if (!out) return gb_fail(CONV_ERR_BAD_PARAM, "out is NULL");
+  *out = nullptr;
+  if (N <= 0 || C <= 0 || H <= 0 || W <= 0 || K <= 0 || R <= 0 || S <= 0)
+    return gb_fail(CONV_ERR_BAD_PARAM, "sizes must be positive");
+  if (stride <= 0 || dilation <= 0 || pad < 0 || groups <= 0)
+    return gb_fail(CONV_ERR_BAD_PARAM, "stride/dilation/groups must be > 0 and pad >= 0");
+  if (C % groups || K % groups)
+    return gb_fail(CONV_ERR_BAD_PARAM, "C and K must be multiples of groups");
+  if (dtype != CONV_BF16 && dtype != CONV_F32 && dtype != CONV_INT8)
+    return gb_fail(CONV_ERR_BAD_PARAM, "unknown dtype %d", (int)dtype);
+  const int OH = out_dim(H, R, stride, pad, dilation), OW = out_dim(W, S, stride, pad, dilation);
+  if (OH <= 0 || OW <= 0) return gb_fail(CONV_ERR_BAD_PARAM, "empty output (OH=%d OW=%d)", OH, OW);
+  if ((long long)N * H * W * C >= (1LL << 40) || (long long)N * OH * OW * K >= (1LL << 40))
+    return gb_fail(CONV_ERR_BAD_PARAM, "tensor too large");
+  gbconv_desc_s* d = new (std::nothrow) gbconv_desc_s{};
+  if (!d) return gb_fail(CONV_ERR_BAD_PARAM, "out of host memory");
+  d->N = N; d->C = C; d->H = H; d->W = W; d->K = K; d->R = R; d->S = S;
+  d->stride = stride; d->pad = pad; d->dil = dilation; d->groups = groups;
+  d->dtype = dtype;
+  d->layout = CONV_NHWC;
+  d->act = CONV_ACT_NONE;
+  d->has_residual = 0;
+  d->scale = nullptr;
+  d->OH = OH;
+  d->OW = OW;
+  *out = d;
+  return ok_status();
+}
+
+extern "C" conv_status_t conv_desc_destroy(conv_desc_t desc) {
+  delete desc;
+  return ok_status();
+}
+
+extern "C" conv_status_t conv_desc_set_layout(conv_desc_t d, conv_layout_t layout) {
+  if (!d) return gb_fail(CONV_ERR_BAD_PARAM, "desc is NULL");
+  if (layout != CONV_NHWC && layout != CONV_NCHW)
+    return gb_fail(CONV_ERR_BAD_PARAM, "unknown layout");
+  if (layout == CONV_NCHW && d->dtype != CONV_F32)
+    return gb_fail(CONV_ERR_UNSUPPORTED, "NCHW is accepted for CONV_F32 only");
+  d->layout = layout;
+  return ok_status();
+}
+
+extern "C" conv_status_t conv_desc_set_epilogue(conv_desc_t d, int act, int has_residual) {
+  if (!d) return gb_fail(CONV_ERR_BAD_PARAM, "desc is NULL");
+  if (act < 0 || act > 2) return gb_fail(CONV_ERR_BAD_PARAM, "act must be 0, 1 or 2");
+  if (d->dtype == CONV_INT8 && (act == CONV_ACT_RELU6 || has_residual))
+    return gb_fail(CONV_ERR_UNSUPPORTED, "int8 epilogue supports act NONE/RELU, no residual");
+  d->act = act;
+  d->has_residual = has_residual ? 1 : 0;
+  return ok_status();
+}
+
+extern "C" conv_status_t conv_desc_set_requant(conv_desc_t d, const float* scale_dev) {
+  if (!d) return gb_fail(CONV_ERR_BAD_PARAM, "desc is NULL");
+  if (d->dtype != CONV_INT8) return gb_fail(CONV_ERR_UNSUPPORTED, "requant is for CONV_INT8");
+  d->scale = scale_dev;
+  return ok_status();
+}
+
+extern "C" conv_status_t conv_desc_get_output_dims(conv_desc_t d, int* OH, int* OW) {
+  if (!d || !OH || !OW) return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
+  *OH = d->OH;
+  *OW = d->OW;
+  return ok_status();
+}
+
+// ---------------------------------------------------------------------------
+// algorithm table
+
+static const char* const kAlgoNames[CONV_ALGO_COUNT] = {
+    "direct", "igemm_tc_n64", "igemm_tc_n128", "igemm_tc_n256",
+    "winograd_f2x2_3x3", "winograd_f6x6_3x3", "depthwise3x3", "int8_igemm_mma"};
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Whether algo applies; on false, *why says which requirement failed.
+static bool applicable(const gbconv_desc_s& d, int algo, const char** why) {
+  const char* dummy;
+  if (!why) why = &dummy;
+  *why = "";
+  const bool nhwc = d.layout == CONV_NHWC;
+  switch (algo) {
+    case CONV_ALGO_DIRECT:
+      if (d.dtype == CONV_INT8 && !d.scale) return *why = "int8 needs a requant scale", false;
+      return true;
+    case CONV_ALGO_IGEMM_N64:
+    case CONV_ALGO_IGEMM_N128:
+    case CONV_ALGO_IGEMM_N256: {
+      if (d.dtype != CONV_BF16 || !nhwc) return *why = "needs bf16 NHWC", false;
+      if (d.groups != 1) return *why = "needs groups == 1", false;
+      if (d.R != d.S) return *why = "needs a square kernel", false;
+      if (d.C % 8 || d.K % 8) return *why = "needs C and K multiples of 8", false;
+      if (d.stride > 8) return *why = "stride > 8", false;
+      if (d.pad > 128 || d.pad - d.dil * (d.R - 1) < -128)
+        return *why = "padding/dilation outside the TMA im2col range", false;
+      if ((long long)d.N * d.OH * d.OW >= (1LL << 31)) return *why = "N*OH*OW >= 2^31", false;
+      if ((long long)d.H * d.W * d.C * 2 >= (1LL << 40)) return *why = "image too large", false;
+      const int bn = igemm_block_n(algo);
+      if (bn == 256 && d.K <= 128) return *why = "K <= 128: use a narrower tile", false;
+      if (bn == 128 && d.K <= 64) return *why = "K <= 64: use a narrower tile", false;
+      return true;
+    }
+    case CONV_ALGO_WINO_F2:
+    case CONV_ALGO_WINO_F6:
+      if (d.dtype != CONV_BF16 || !nhwc) return *why = "needs bf16 NHWC", false;
+      if (d.R != 3 || d.S != 3 || d.stride != 1 || d.dil != 1 || d.groups != 1)
+        return *why = "needs 3x3, stride 1, dilation 1, groups 1", false;
+      if (d.C % 8 || d.K % 8) return *why = "needs C and K multiples of 8", false;
+      return true;
+    case CONV_ALGO_DEPTHWISE:
+      if (d.dtype != CONV_BF16 || !nhwc) return *why = "needs bf16 NHWC", false;
+      if (!(d.groups == d.C && d.K == d.C)) return *why = "needs groups == C == K", false;
+      if (d.R != 3 || d.S != 3 || d.dil != 1 || d.stride > 2)
+        return *why = "needs 3x3, dilation 1, stride 1 or 2", false;
+      if (d.C % 8) return *why = "needs C multiple of 8", false;
+      return true;
+    case CONV_ALGO_INT8_MMA:
+      if (d.dtype != CONV_INT8 || !nhwc) return *why = "needs int8 NHWC", false;
+      if (!d.scale) return *why = "int8 needs a requant scale", false;
+      if (d.groups != 1) return *why = "needs groups == 1", false;
+      if (d.C % 16 || d.K % 16) return *why = "needs C and K multiples of 16", false;
+      return true;
+    default:
+      return *why = "unknown algorithm", false;
+  }
+}
+
+static bool implemented(int algo);
+
+extern "C" conv_status_t conv_algo_count(conv_desc_t d, int* count) {
+  if (!d || !count) return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
+  *count = CONV_ALGO_COUNT;
+  return ok_status();
+}
+
+extern "C" conv_status_t conv_algo_info(conv_desc_t d, int i, conv_algo_t* algo,
+                                        const char** name, int* is_applicable) {
+  if (!d) return gb_fail(CONV_ERR_BAD_PARAM, "desc is NULL");
+  if (i < 0 || i >= CONV_ALGO_COUNT) return gb_fail(CONV_ERR_BAD_PARAM, "index out of range");
+  if (algo) *algo = i;
+  if (name) *name = kAlgoNames[i];
+  if (is_applicable) *is_applicable = implemented(i) && applicable(*d, i, nullptr) ? 1 : 0;
+  return ok_status();
+}
+
+// Heuristic preference when no Fast-Run entry exists.  The MegEngine report's
+// table of preferences ("Fast-Run" section) is missing from the page; this is
+// the plain reading of its text: Winograd for 3x3 stride-1 layers with enough
+// channels, the depthwise kernel for depthwise layers, im2col-GEMM otherwise,
+// direct for what nothing else covers.
+static int heuristic(const gbconv_desc_s& d) {
+  if (d.dtype == CONV_INT8)
+    return implemented(CONV_ALGO_INT8_MMA) && applicable(d, CONV_ALGO_INT8_MMA, nullptr)
+               ? CONV_ALGO_INT8_MMA
+               : CONV_ALGO_DIRECT;
+  if (implemented(CONV_ALGO_DEPTHWISE) && applicable(d, CONV_ALGO_DEPTHWISE, nullptr))
+    return CONV_ALGO_DEPTHWISE;
+  const int order[] = {CONV_ALGO_IGEMM_N256, CONV_ALGO_IGEMM_N128, CONV_ALGO_IGEMM_N64};
+  for (int a : order)
+    if (implemented(a) && applicable(d, a, nullptr)) return a;
+  return CONV_ALGO_DIRECT;
+}
+
+// ---------------------------------------------------------------------------
+// Fast-Run map: key = descriptor + dtype/layout/epilogue; the file adds the
+// device name, SM count and library version.
+
+static std::mutex g_map_mu;
+static std::map<std::string, int> g_fastrun;
+
+static std::string desc_key(const gbconv_desc_s& d) {
+  char buf[256];
+  snprintf(buf, sizeof(buf), "N%d_C%d_H%d_W%d_K%d_R%d_S%d_st%d_p%d_d%d_g%d_t%d_l%d_a%d_r%d_q%d",
+           d.N, d.C, d.H, d.W, d.K, d.R, d.S, d.stride, d.pad, d.dil, d.groups, (int)d.dtype,
+           (int)d.layout, d.act, d.has_residual, d.scale ? 1 : 0);
+  return buf;
+}
+
+static int lookup_map(const gbconv_desc_s& d) {
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  auto it = g_fastrun.find(desc_key(d));
+  return it == g_fastrun.end() ? -1 : it->second;
+}
+
+static int resolve(const gbconv_desc_s& d, int algo) {
+  if (algo != CONV_ALGO_AUTO) return algo;
+  const int a = lookup_map(d);
+  if (a >= 0 && implemented(a) && applicable(d, a, nullptr)) return a;
+  return heuristic(d);
+}
+
+extern "C" conv_status_t conv_algo_resolve(conv_desc_t d, conv_algo_t* algo) {
+  if (!d || !algo) return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
+  *algo = resolve(*d, CONV_ALGO_AUTO);
+  return ok_status();
+}
+
+// ---------------------------------------------------------------------------
+// sizes and packing
+
+static size_t elem_bytes(conv_dtype_t t) { return t == CONV_F32 ? 4 : (t == CONV_BF16 ? 2 : 1); }
+
+static size_t user_weight_bytes(const gbconv_desc_s& d) {
+  return (size_t)d.K * (d.C / d.groups) * d.R * d.S * elem_bytes(d.dtype);
+}
+
+static conv_status_t check_algo(const gbconv_desc_s& d, int algo) {
+  if (algo < 0 || algo >= CONV_ALGO_COUNT)
+    return gb_fail(CONV_ERR_BAD_PARAM, "algorithm id %d out of range", algo);
+  if (!implemented(algo)) return gb_fail(CONV_ERR_UNSUPPORTED, "%s not built", kAlgoNames[algo]);
+  const char* why = "";
+  if (!applicable(d, algo, &why))
+    return gb_fail(CONV_ERR_UNSUPPORTED, "%s does not apply: %s", kAlgoNames[algo], why);
+  return CONV_OK;
+}
+
+extern "C" conv_status_t conv_workspace_size(conv_desc_t d, conv_algo_t algo, size_t* bytes) {
+  if (!d || !bytes) return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
+  const int a = resolve(*d, algo);
+  conv_status_t st = check_algo(*d, a);
+  if (st != CONV_OK) return st;
+  *bytes = 0;
+  if (a == CONV_ALGO_WINO_F2 || a == CONV_ALGO_WINO_F6)
+    *bytes = winograd_workspace_bytes(*d, a == CONV_ALGO_WINO_F2 ? 2 : 6);
+  return ok_status();
+}
+
+extern "C" conv_status_t conv_weights_packed_size(conv_desc_t d, conv_algo_t algo,
+                                                  size_t* bytes) {
+  if (!d || !bytes) return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
+  const int a = resolve(*d, algo);
+  conv_status_t st = check_algo(*d, a);
+  if (st != CONV_OK) return st;
+  const size_t Cp64 = (size_t)gb_ceil_div(d->C, 64) * 64;
+  switch (a) {
+    case CONV_ALGO_IGEMM_N64:
+    case CONV_ALGO_IGEMM_N128:
+    case CONV_ALGO_IGEMM_N256: *bytes = (size_t)d->K * d->R * d->S * Cp64 * 2; break;
+    case CONV_ALGO_INT8_MMA: *bytes = (size_t)d->K * d->R * d->S * Cp64; break;
+    case CONV_ALGO_WINO_F2: *bytes = winograd_packed_bytes(*d, 2); break;
+    case CONV_ALGO_WINO_F6: *bytes = winograd_packed_bytes(*d, 6); break;
+    default: *bytes = user_weight_bytes(*d); break;
+  }
+  return ok_status();
+}
+
+extern "C" conv_status_t conv_weights_prepack(conv_desc_t d, conv_algo_t algo, const void* w,
+                                              void* wpack, void* stream) {
+  if (!d || !w || !wpack) return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
+  const int a = resolve(*d, algo);
+  conv_status_t st = check_algo(*d, a);
+  if (st != CONV_OK) return st;
+  if (!aligned16(wpack)) return gb_fail(CONV_ERR_ALIGNMENT, "wpack not 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  switch (a) {
+    case CONV_ALGO_IGEMM_N64:
+    case CONV_ALGO_IGEMM_N128:
+    case CONV_ALGO_IGEMM_N256: e = launch_pack_igemm_weights(*d, w, wpack, s); break;
+    case CONV_ALGO_INT8_MMA: e = launch_pack_int8_weights(*d, w, wpack, s); break;
+    case CONV_ALGO_WINO_F2: e = launch_winograd_filter_transform(*d, 2, w, wpack, s); break;
+    case CONV_ALGO_WINO_F6: e = launch_winograd_filter_transform(*d, 6, w, wpack, s); break;
+    default:
+      e = cudaMemcpyAsync(wpack, w, user_weight_bytes(*d), cudaMemcpyDeviceToDevice, s);
+      break;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "weight prepack");
+  return ok_status();
+}
+
+// ---------------------------------------------------------------------------
+// forward
+
+static conv_status_t fwd_impl(const gbconv_desc_s& d, const void* x, const void* wpack,
+                              const void* bias, const void* res, void* y, int a, void* ws,
+                              size_t ws_bytes, cudaStream_t s) {
+  int* err = gb_device_error_word();
+  const unsigned long long wait_ns = gb_wait_limit_ns();
+  cudaError_t e = cudaSuccess;
+  switch (a) {
+    case CONV_ALGO_DIRECT: e = launch_direct(d, x, wpack, bias, res, y, s); break;
+    case CONV_ALGO_IGEMM_N64:
+    case CONV_ALGO_IGEMM_N128:
+    case CONV_ALGO_IGEMM_N256:
+      e = launch_igemm_bf16(d, igemm_block_n(a), x, wpack, static_cast<const float*>(bias), res,
+                            y, err, wait_ns, s);
+      break;
+    case CONV_ALGO_DEPTHWISE:
+      e = launch_dwconv3x3(d, x, wpack, static_cast<const float*>(bias), res, y, s);
+      break;
+    case CONV_ALGO_INT8_MMA:
+      e = launch_igemm_int8(d, x, wpack, static_cast<const int32_t*>(bias), y, s);
+      break;
+    case CONV_ALGO_WINO_F2:
+    case CONV_ALGO_WINO_F6: {
+      const int m = a == CONV_ALGO_WINO_F2 ? 2 : 6;
+      const size_t need = winograd_workspace_bytes(d, m);
+      if (need && (!ws || ws_bytes < need))
+        return gb_fail(CONV_ERR_WORKSPACE, "workspace of %zu bytes needed", need);
+      e = launch_winograd(d, m, x, wpack, static_cast<const float*>(bias), res, y, ws, err,
+                          wait_ns, s);
+      break;
+    }
+    default: return gb_fail(CONV_ERR_UNSUPPORTED, "algorithm %d", a);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, kAlgoNames[a]);
+  return ok_status();
+}
+
+extern "C" conv_status_t conv_fwd(conv_desc_t d, const void* x, const void* wpack,
+                                  const void* bias, const void* residual, void* y,
+                                  conv_algo_t algo, void* ws, size_t ws_bytes, void* stream) {
+  if (!d || !x || !wpack || !y) return gb_fail(CONV_ERR_BAD_PARAM, "NULL tensor argument");
+  if (d->has_residual && !residual)
+    return gb_fail(CONV_ERR_BAD_PARAM, "descriptor has a residual but residual is NULL");
+  if (!d->has_residual && residual)
+    return gb_fail(CONV_ERR_BAD_PARAM, "residual given but the descriptor has none");
+  const int a = resolve(*d, algo);
+  conv_status_t st = check_algo(*d, a);
+  if (st != CONV_OK) return st;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(wpack) || (residual && !aligned16(residual)) ||
+      (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)))
+    return gb_fail(CONV_ERR_ALIGNMENT, "tensors must be 16-byte aligned (bias 4-byte)");
+  if (d->dtype == CONV_INT8 && !d->scale)
+    return gb_fail(CONV_ERR_BAD_PARAM, "int8 descriptor has no requant scale");
+  return fwd_impl(*d, x, wpack, bias, residual, y, a, ws, ws_bytes,
+                  static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------------------
+// Fast-Run selection: time every applicable algorithm on scratch tensors.
+
+namespace {
+struct DevBuf {
+  void* p = nullptr;
+  ~DevBuf() {
+    if (p) cudaFree(p);
+  }
+  cudaError_t alloc(size_t n) { return cudaMalloc(&p, n ? n : 16); }
+};
+}  // namespace
+
+extern "C" conv_status_t conv_fastrun_select(conv_desc_t d, void* stream, conv_algo_t* best,
+                                             float* times_ms) {
+  if (!d || !best) return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t eb = elem_bytes(d->dtype);
+  const size_t xb = (size_t)d->N * d->C * d->H * d->W * eb;
+  const size_t yb = (size_t)d->N * d->K * d->OH * d->OW * eb;
+  const size_t bb = (size_t)d->K * 4;
+  DevBuf x, y, res, bias, w, scale;
+  cudaError_t e;
+  if ((e = x.alloc(xb)) != cudaSuccess || (e = y.alloc(yb)) != cudaSuccess ||
+      (e = bias.alloc(bb)) != cudaSuccess || (e = w.alloc(user_weight_bytes(*d))) != cudaSuccess)
+    return cuda_fail(e, "fastrun scratch");
+  if (d->has_residual && (e = res.alloc(yb)) != cudaSuccess) return cuda_fail(e, "fastrun");
+  gbconv_desc_s dd = *d;
+  if (d->dtype == CONV_INT8) {
+    if ((e = scale.alloc((size_t)d->K * 4)) != cudaSuccess) return cuda_fail(e, "fastrun");
+    std::vector<float> sc(d->K, 1e-4f);
+    cudaMemcpyAsync(scale.p, sc.data(), sc.size() * 4, cudaMemcpyHostToDevice, s);
+    dd.scale = static_cast<const float*>(scale.p);
+  }
+  const int esz = d->dtype == CONV_F32 ? 4 : (d->dtype == CONV_BF16 ? 2 : 1);
+  launch_fill_random(x.p, xb, esz, 1u, s);
+  launch_fill_random(w.p, user_weight_bytes(*d), esz, 2u, s);
+  cudaMemsetAsync(bias.p, 0, bb, s);
+  if (res.p) launch_fill_random(res.p, yb, esz, 3u, s);
+
+  float tms[CONV_ALGO_COUNT];
+  int best_a = -1;
+  float best_t = 0.f;
+  cudaEvent_t e0, e1;
+  cudaEventCreate(&e0);
+  cudaEventCreate(&e1);
+  for (int a = 0; a < CONV_ALGO_COUNT; ++a) {
+    tms[a] = -1.f;
+    if (!implemented(a) || !applicable(dd, a, nullptr)) continue;
+    size_t pb = 0, wsb = 0;
+    if (conv_weights_packed_size(&dd, a, &pb) != CONV_OK) continue;
+    if (conv_workspace_size(&dd, a, &wsb) != CONV_OK) continue;
+    DevBuf wp, ws;
+    if (wp.alloc(pb) != cudaSuccess || ws.alloc(wsb) != cudaSuccess) {
+      cudaGetLastError();
+      continue;
+    }
+    if (conv_weights_prepack(&dd, a, w.p, wp.p, s) != CONV_OK) continue;
+    // warm-up, then the median of `reps` timed runs
+    bool ok = true;
+    for (int i = 0; i < 3 && ok; ++i)
+      ok = fwd_impl(dd, x.p, wp.p, bias.p, res.p, y.p, a, ws.p, wsb, s) == CONV_OK;
+    if (!ok) continue;
+    std::vector<float> t;
+    const int reps = 15;
+    for (int i = 0; i < reps && ok; ++i) {
+      cudaEventRecord(e0, s);
+      ok = fwd_impl(dd, x.p, wp.p, bias.p, res.p, y.p, a, ws.p, wsb, s) == CONV_OK;
+      cudaEventRecord(e1, s);
+      cudaEventSynchronize(e1);
+      float ms = 0.f;
+      cudaEventElapsedTime(&ms, e0, e1);
+      t.push_back(ms);
+    }
+    if (!ok || cudaStreamSynchronize(s) != cudaSuccess) continue;
+    std::sort(t.begin(), t.end());
+    tms[a] = t[t.size() / 2];
+    // strictly faster by more than 1% wins; otherwise the lower id is kept
+    if (best_a < 0 || tms[a] < best_t * 0.99f) {
+      best_a = a;
+      best_t = tms[a];
+    }
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  int* err = gb_device_error_word();
+  int code = 0;
+  if (err) {
+    cudaMemcpy(&code, err, 4, cudaMemcpyDeviceToHost);
+    if (code) cudaMemset(err, 0, 4);
+  }
+  if (code) return gb_fail(code == DEV_ERR_TIMEOUT ? CONV_ERR_TIMEOUT : CONV_ERR_INTERNAL,
+                           "device error during Fast-Run timing");
+  if (best_a < 0) return gb_fail(CONV_ERR_UNSUPPORTED, "no applicable algorithm ran");
+  {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    g_fastrun[desc_key(*d)] = best_a;
+  }
+  *best = best_a;
+  if (times_ms) memcpy(times_ms, tms, sizeof(tms));
+  return ok_status();
+}
+
+extern "C" conv_status_t conv_fastrun_lookup(conv_desc_t d, conv_algo_t* algo) {
+  if (!d || !algo) return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
+  const int a = lookup_map(*d);
+  if (a < 0) return gb_fail(CONV_ERR_NOT_FOUND, "no Fast-Run entry");
+  *algo = a;
+  return ok_status();
+}
+
+static std::string device_tag() {
+  int dev = 0;
+  cudaDeviceProp prop;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return "nodevice";
+  }
+  std::string name = prop.name;
+  for (char& c : name)
+    if (c == ' ' || c == '\t') c = '_';
+  return name + "_sm" + std::to_string(prop.multiProcessorCount);
+}
+
+extern "C" conv_status_t conv_fastrun_save(const char* path) {
+  if (!path) return gb_fail(CONV_ERR_BAD_PARAM, "path is NULL");
+  FILE* f = fopen(path, "w");
+  if (!f) return gb_fail(CONV_ERR_FASTRUN_FILE, "cannot open %s for writing", path);
+  const std::string tag = device_tag();
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  fprintf(f, "# gbconv fastrun map\nversion %s\n", GBCONV_VERSION);
+  for (auto& kv : g_fastrun)
+    fprintf(f, "entry %s %s %s\n", tag.c_str(), kv.first.c_str(), kAlgoNames[kv.second]);
+  fprintf(f, "end %zu\n", g_fastrun.size());
+  const bool bad = ferror(f) != 0;
+  fclose(f);
+  if (bad) return gb_fail(CONV_ERR_FASTRUN_FILE, "write error on %s", path);
+  return ok_status();
+}
+
+extern "C" conv_status_t conv_fastrun_load(const char* path) {
+  if (!path) return gb_fail(CONV_ERR_BAD_PARAM, "path is NULL");
+  FILE* f = fopen(path, "r");
+  if (!f) return gb_fail(CONV_ERR_FASTRUN_FILE, "cannot open %s", path);
+  const std::string tag = device_tag();
+  std::map<std::string, int> fresh;
+  char line[1024];
+  bool saw_version = false, saw_end = false, version_ok = false;
+  size_t entries = 0, declared = 0;
+  bool corrupt = false;
+  while (fgets(line, sizeof(line), f)) {
+    if (line[0] == '#' || line[0] == '\n') continue;
+    char a[256], b[512], c[128];
+    if (!saw_version) {
+      if (sscanf(line, "version %255s", a) != 1) { corrupt = true; break; }
+      saw_version = true;
+      version_ok = strcmp(a, GBCONV_VERSION) == 0;
+      continue;
+    }
+    if (sscanf(line, "end %zu", &declared) == 1) { saw_end = true; break; }
+    if (sscanf(line, "entry %255s %511s %127s", a, b, c) != 3) { corrupt = true; break; }
+    ++entries;
+    int id = -1;
+    for (int i = 0; i < CONV_ALGO_COUNT; ++i)
+      if (strcmp(c, kAlgoNames[i]) == 0) id = i;
+    if (id < 0) { corrupt = true; break; }
+    if (version_ok && tag == a) fresh[b] = id;  // other devices/versions are skipped
+  }
+  fclose(f);
+  if (corrupt || !saw_version || !saw_end || declared != entries)
+    return gb_fail(CONV_ERR_FASTRUN_FILE, "corrupt Fast-Run file %s", path);
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  for (auto& kv : fresh) g_fastrun[kv.first] = kv.second;
+  return ok_status();
+}
+
+extern "C" conv_status_t conv_fastrun_clear(void) {
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  g_fastrun.clear();
+  return ok_status();
+}
+
+// ---------------------------------------------------------------------------
+// layout conversion and pooling
+
+extern "C" conv_status_t conv_nchw_f32_to_nhwc_bf16(const float* x, void* y, int N, int C, int H,
+                                                    int W, int C_out, void* stream) {
+  if (!x || !y) return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
+  if (N <= 0 || C <= 0 || H <= 0 || W <= 0 || C_out < C)
+    return gb_fail(CONV_ERR_BAD_PARAM, "bad sizes");
+  cudaError_t e =
+      launch_nchw_f32_to_nhwc_bf16(x, y, N, C, H, W, C_out, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok_status() : cuda_fail(e, "nchw->nhwc");
+}
+
+extern "C" conv_status_t conv_nhwc_bf16_to_nchw_f32(const void* x, float* y, int N, int C, int H,
+                                                    int W, int C_in, void* stream) {
+  if (!x || !y) return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
+  if (N <= 0 || C <= 0 || H <= 0 || W <= 0 || C_in < C)
+    return gb_fail(CONV_ERR_BAD_PARAM, "bad sizes");
+  cudaError_t e =
+      launch_nhwc_bf16_to_nchw_f32(x, y, N, C, H, W, C_in, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok_status() : cuda_fail(e, "nhwc->nchw");
+}
+
+extern "C" conv_status_t conv_maxpool2d_nhwc_bf16(const void* x, void* y, int N, int C, int H,
+                                                  int W, int k, int stride, int pad,
+                                                  void* stream) {
+  if (!x || !y) return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
+  if (N <= 0 || C <= 0 || H <= 0 || W <= 0 || k <= 0 || stride <= 0 || pad < 0 || pad >= k)
+    return gb_fail(CONV_ERR_BAD_PARAM, "bad sizes");
+  if (C % 8 || !aligned16(x) || !aligned16(y))
+    return gb_fail(CONV_ERR_ALIGNMENT, "needs C % 8 == 0 and 16-byte aligned tensors");
+  cudaError_t e =
+      launch_maxpool_nhwc_bf16(x, y, N, C, H, W, k, stride, pad, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok_status() : cuda_fail(e, "maxpool");
+}
+
+extern "C" conv_status_t conv_global_avgpool_nhwc_bf16(const void* x, void* y, int N, int C,
+                                                       int H, int W, void* stream) {
+  if (!x || !y) return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
+  if (N <= 0 || C <= 0 || H <= 0 || W <= 0) return gb_fail(CONV_ERR_BAD_PARAM, "bad sizes");
+  if (C % 8 || !aligned16(x) || !aligned16(y))
+    return gb_fail(CONV_ERR_ALIGNMENT, "needs C % 8 == 0 and 16-byte aligned tensors");
+  cudaError_t e = launch_avgpool_nhwc_bf16(x, y, N, C, H, W, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok_status() : cuda_fail(e, "avgpool");
+}
+
+// ---------------------------------------------------------------------------
+// status
+
+extern "C" conv_status_t conv_sync_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  int* err = gb_device_error_word();
+  if (!err) return gb_fail(CONV_ERR_CUDA, "device error word unavailable");
+  int code = 0;
+  e = cudaMemcpy(&code, err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+  if (code) {
+    cudaMemset(err, 0, sizeof(int));
+    return gb_fail(code == DEV_ERR_TIMEOUT ? CONV_ERR_TIMEOUT : CONV_ERR_INTERNAL,
+                   "device error word = %d", code);
+  }
+  return ok_status();
+}
+
+extern "C" const char* conv_status_string(conv_status_t s) {
+  switch (s) {
+    case CONV_OK: return "CONV_OK";
+    case CONV_ERR_BAD_PARAM: return "CONV_ERR_BAD_PARAM";
+    case CONV_ERR_UNSUPPORTED: return "CONV_ERR_UNSUPPORTED";
+    case CONV_ERR_ALIGNMENT: return "CONV_ERR_ALIGNMENT";
+    case CONV_ERR_WORKSPACE: return "CONV_ERR_WORKSPACE";
+    case CONV_ERR_CUDA: return "CONV_ERR_CUDA";
+    case CONV_ERR_TIMEOUT: return "CONV_ERR_TIMEOUT";
+    case CONV_ERR_INTERNAL: return "CONV_ERR_INTERNAL";
+    case CONV_ERR_FASTRUN_FILE: return "CONV_ERR_FASTRUN_FILE";
+    case CONV_ERR_NOT_FOUND: return "CONV_ERR_NOT_FOUND";
+    default: return "CONV_ERR_UNKNOWN";
+  }
+}
+
+extern "C" const char* conv_last_error_detail(void) { return g_detail; }
+
+extern "C" const char* conv_version(void) { return GBCONV_VERSION; }
+
+// Algorithms whose kernels are built into this library.
+static bool implemented(int algo) {
+  switch (algo) {
+    case CONV_ALGO_DIRECT:
+    case CONV_ALGO_IGEMM_N64:
+    case CONV_ALGO_IGEMM_N128:
+    case CONV_ALGO_IGEMM_N256:
+      return true;
+    default:
+      return false;
+  }
+}

@@ -1,0 +1,91 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gbconv.h"
+
+struct gbconv_desc_s {
+  int N, C, H, W, K, R, S, stride, pad, dil, groups;
+  conv_dtype_t dtype;
+  conv_layout_t layout;
+  int act;
+  int has_residual;
+  const float* scale;  // int8 requant scale [K] (device)
+  int OH, OW;
+};
+
+// Device-side error word codes (written by kernels, read by conv_sync_status).
+enum : int { DEV_ERR_NONE = 0, DEV_ERR_TIMEOUT = 1, DEV_ERR_INTERNAL = 2 };
+
+// Thread-local error detail; returns st for convenience.
+conv_status_t gb_fail(conv_status_t st, const char* fmt, ...);
+// Device error word of the current device (a __device__ int, address cached).
+int* gb_device_error_word();
+// Number of SMs of the current device (cached).
+int gb_num_sms();
+// Wait limit for device-side bounded waits, in nanoseconds (GBCONV_WAIT_LIMIT_MS).
+unsigned long long gb_wait_limit_ns();
+
+// Driver entry points for TMA descriptors (resolved once through the runtime).
+CUresult gb_encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, cuuint32_t rank, void* addr,
+                         const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                         const cuuint32_t* estr, CUtensorMapSwizzle swz);
+CUresult gb_encode_im2col(CUtensorMap* map, CUtensorMapDataType dt, cuuint32_t rank, void* addr,
+                          const cuuint64_t* dims, const cuuint64_t* strides, const int* lower,
+                          const int* upper, cuuint32_t channels, cuuint32_t pixels,
+                          const cuuint32_t* estr, CUtensorMapSwizzle swz);
+
+static inline int gb_ceil_div(int a, int b) { return (a + b - 1) / b; }
+static inline long long gb_ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
+
+// ---- launchers (each returns cudaSuccess or the launch error) --------------
+
+// Direct loop on CUDA cores (any groups / stride / dilation).  Weights in the
+// user layout (NHWC: [K][R][S][Cg]; NCHW: [K][Cg][R][S]).
+cudaError_t launch_direct(const gbconv_desc_s& d, const void* x, const void* w, const void* bias,
+                          const void* res, void* y, cudaStream_t st);
+
+// Implicit GEMM on tcgen05 (bf16 NHWC, groups 1).  wpack: [K][R*S][Cp] bf16,
+// Cp = C rounded up to 64, zero padded.
+int igemm_block_n(int algo);
+cudaError_t launch_igemm_bf16(const gbconv_desc_s& d, int block_n, const void* x,
+                              const void* wpack, const float* bias, const void* res, void* y,
+                              int* err, unsigned long long wait_ns, cudaStream_t st);
+cudaError_t launch_pack_igemm_weights(const gbconv_desc_s& d, const void* w, void* wpack,
+                                      cudaStream_t st);
+
+// Depthwise 3x3 (bf16 NHWC).  w: [C][3][3] bf16 (the user layout [K][R][S][1]).
+cudaError_t launch_dwconv3x3(const gbconv_desc_s& d, const void* x, const void* w,
+                             const float* bias, const void* res, void* y, cudaStream_t st);
+
+// int8 implicit GEMM (mma.sync s8, exact int32 accumulate).  wpack: [K][R*S][Cp] int8.
+cudaError_t launch_igemm_int8(const gbconv_desc_s& d, const void* x, const void* wpack,
+                              const int32_t* bias, void* y, cudaStream_t st);
+cudaError_t launch_pack_int8_weights(const gbconv_desc_s& d, const void* w, void* wpack,
+                                     cudaStream_t st);
+
+// Winograd F(m x m, 3 x 3), m in {2, 6}.
+size_t winograd_packed_bytes(const gbconv_desc_s& d, int m);
+size_t winograd_workspace_bytes(const gbconv_desc_s& d, int m);
+cudaError_t launch_winograd_filter_transform(const gbconv_desc_s& d, int m, const void* w,
+                                             void* wpack, cudaStream_t st);
+cudaError_t launch_winograd(const gbconv_desc_s& d, int m, const void* x, const void* wpack,
+                            const float* bias, const void* res, void* y, void* ws, int* err,
+                            unsigned long long wait_ns, cudaStream_t st);
+
+// Layout conversion and pooling.
+cudaError_t launch_nchw_f32_to_nhwc_bf16(const float* x, void* y, int N, int C, int H, int W,
+                                         int C_out, cudaStream_t st);
+cudaError_t launch_nhwc_bf16_to_nchw_f32(const void* x, float* y, int N, int C, int H, int W,
+                                         int C_in, cudaStream_t st);
+cudaError_t launch_maxpool_nhwc_bf16(const void* x, void* y, int N, int C, int H, int W, int k,
+                                     int stride, int pad, cudaStream_t st);
+cudaError_t launch_avgpool_nhwc_bf16(const void* x, void* y, int N, int C, int H, int W,
+                                     cudaStream_t st);
+// Fill a buffer with deterministic pseudo-random values (Fast-Run scratch).
+cudaError_t launch_fill_random(void* p, size_t bytes, int elem_bytes, uint32_t seed,
+                               cudaStream_t st);

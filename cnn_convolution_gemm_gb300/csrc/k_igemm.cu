@@ -1,0 +1,392 @@
+// Implicit-GEMM convolution on the 5th-generation tensor cores (tcgen05).
+//
+// The aminer.cn MegEngine report (section "Im2col+MatMul") unrolls input
+// patches into an im2col matrix [n, fh*fw*ic, oh*ow] and multiplies it by the
+// weight matrix; it then blocks the im2col matrix along oh*ow so a block stays
+// on chip, and fuses the "PACK" of the GEMM panels into the im2col step so the
+// unrolled data is written once instead of twice ("融合 PACK").  Here the
+// im2col matrix is never written at all: each 128-pixel block of the output
+// (flattened over n, oh, ow) is one GEMM M-tile, and for every filter tap
+// (r, s) and 64-channel slice a TMA load in im2col mode copies the matching
+// 128 x 64 input patch straight from the NHWC activation tensor into shared
+// memory, already in the 128-byte-swizzled K-major layout the tensor core
+// reads.  Zero padding comes from TMA's out-of-bounds fill.
+//
+//   GEMM:  Y[M = N*OH*OW][K] = A[M][R*S*Cp] * Wp[K][R*S*Cp]^T
+//   A[m][(r*S+s)*Cp + c] = x[n, oh*st - pad + r*dil, ow*st - pad + s*dil, c]
+//
+// Warp roles (192 threads, persistent over output tiles):
+//   warp 0      TMA producer (one elected lane) -> STAGES-deep smem ring
+//   warp 1      MMA issuer (one lane): tcgen05.mma 128 x BN x 16, fp32 in TMEM
+//   warps 2..5  epilogue: tcgen05.ld -> + bias (+ residual) -> activation ->
+//               bf16 store ("Graph層面" of the Momenta talk: bias and ReLU
+//               fused into the matrix product)
+// The accumulator is double-buffered in TMEM (2 x BN columns) so the
+// epilogue of tile i overlaps the MMAs of tile i+1.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace {
+
+constexpr int BM = 128;  // output pixels per tile (TMEM lanes)
+constexpr int BK = 64;   // channels per k-step: 64 bf16 = one 128-byte swizzle row
+
+struct IgemmParams {
+  int H, W, C, K, S, stride, pad, dil, OH, OW;
+  int cblocks;  // Cp / 64
+  int kiters;   // R * S * cblocks
+  int Kw;       // packed weight row length R*S*Cp
+  long long M;  // N*OH*OW
+  int m_tiles, n_tiles;
+  int act;
+  const float* bias;
+  const __nv_bfloat16* res;
+  __nv_bfloat16* y;
+  int* err;
+  unsigned long long wait_ns;
+};
+
+template <int BN>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (BN >= 256) ? 4 : (BN >= 128 ? 6 : 8);
+  static constexpr uint32_t TMEM_COLS = 2 * BN;  // double-buffered fp32 accumulator
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+};
+
+__device__ __forceinline__ float act_apply(float v, int act) {
+  if (act == 1) return fmaxf(v, 0.0f);
+  if (act == 2) return fminf(fmaxf(v, 0.0f), 6.0f);
+  return v;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(192, 1)
+    igemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
+                         const __grid_constant__ CUtensorMap tm_w, const IgemmParams p) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + C::STAGES * C::A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::STAGES;
+  uint64_t* tfull = bars + 2 * C::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      gb::mbar_init(&full[s], 1);
+      gb::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      gb::mbar_init(&tfull[b], 1);
+      gb::mbar_init(&tempty[b], 128);
+    }
+    gb::mbar_init(mma_done, 1);
+    gb::fence_barrier_init();
+    gb::tma_prefetch_desc(&tm_x);
+    gb::tma_prefetch_desc(&tm_w);
+  }
+  if (warp == 0) {
+    gb::tmem_alloc(tmem_slot, C::TMEM_COLS);
+    gb::tmem_relinquish();
+  }
+  gb::tc_fence_before();
+  __syncthreads();
+  gb::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_tiles = p.m_tiles * p.n_tiles;
+  const int ohow = p.OH * p.OW;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        const int mt = t / p.n_tiles, nt = t % p.n_tiles;
+        const long long m0 = (long long)mt * BM;
+        const int img = (int)(m0 / ohow);
+        const int rem = (int)(m0 % ohow);
+        const int h0 = (rem / p.OW) * p.stride - p.pad;
+        const int w0 = (rem % p.OW) * p.stride - p.pad;
+        int cb = 0, s = 0, r = 0;
+        for (int it = 0; it < p.kiters; ++it) {
+          if (!gb::mbar_wait_bounded(&empty[stage], phase ^ 1, p.wait_ns, p.err)) {
+            ok = false;
+            break;
+          }
+          gb::mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+          gb::tma_load_im2col_4d(sA + stage * C::A_BYTES, &tm_x, &full[stage], cb * BK, w0, h0,
+                                 img, (uint16_t)(s * p.dil), (uint16_t)(r * p.dil));
+          gb::tma_load_2d(sB + stage * C::B_BYTES, &tm_w, &full[stage],
+                          (r * p.S + s) * p.cblocks * BK + cb * BK, nt * BN);
+          ++issued;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+          if (++cb == p.cblocks) {
+            cb = 0;
+            if (++s == p.S) {
+              s = 0;
+              ++r;
+            }
+          }
+        }
+      }
+      // Drain: wait until the last loads this thread issued have landed, so no
+      // copy into shared memory is in flight when the block exits.
+      long long pending = issued < C::STAGES ? issued : C::STAGES;
+      int st = stage;
+      uint32_t ph = phase;
+      for (long long i = 0; i < pending; ++i) {
+        if (--st < 0) {
+          st = C::STAGES - 1;
+          ph ^= 1;
+        }
+        gb::mbar_wait_bounded(&full[st], ph, p.wait_ns, p.err);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t IDESC = gb::idesc_f16(BM, BN, 1);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        if (!gb::mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, p.wait_ns, p.err)) break;
+        gb::tc_fence_after();
+        const uint32_t d = tmem_base + acc * BN;
+        for (int it = 0; it < p.kiters; ++it) {
+          if (!gb::mbar_wait_bounded(&full[stage], phase, p.wait_ns, p.err)) {
+            ok = false;
+            break;
+          }
+          gb::tc_fence_after();
+          const uint32_t a0 = gb::smem_u32(sA + stage * C::A_BYTES);
+          const uint32_t b0 = gb::smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            gb::tc_mma_f16(d, gb::sw128_kmajor_desc(a0 + k * 32),
+                           gb::sw128_kmajor_desc(b0 + k * 32), IDESC, (it | k) != 0);
+          gb::tc_commit(&empty[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        gb::tc_commit(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      // All MMAs issued by this thread have completed once mma_done fires.
+      gb::tc_commit(mma_done);
+      gb::mbar_wait_bounded(mma_done, 0, p.wait_ns, p.err);
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      const int mt = t / p.n_tiles, nt = t % p.n_tiles;
+      if (!gb::mbar_wait_bounded(&tfull[acc], acc_phase, p.wait_ns, p.err)) break;
+      gb::tc_fence_after();
+      const long long m = (long long)mt * BM + q * 32 + lane;
+      const bool row_ok = m < p.M;
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        uint32_t r[16];
+        gb::tmem_ld_x16(tbase + c0, r);
+        gb::tmem_ld_wait();
+        const int n = nt * BN + c0;
+        if (row_ok && n < p.K) {
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+          const int nvalid = (p.K - n) >= 16 ? 16 : 8;  // K % 8 == 0
+          if (p.bias) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (j < nvalid) v[j] += __ldg(p.bias + n + j);
+          }
+          const size_t off = (size_t)m * p.K + n;
+          if (p.res) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              if (h * 8 < nvalid) {
+                uint4 rv = *reinterpret_cast<const uint4*>(p.res + off + h * 8);
+                const __nv_bfloat162* rp = reinterpret_cast<const __nv_bfloat162*>(&rv);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  float2 f = __bfloat1622float2(rp[j]);
+                  v[h * 8 + 2 * j] += f.x;
+                  v[h * 8 + 2 * j + 1] += f.y;
+                }
+              }
+            }
+          }
+          uint32_t packed[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(act_apply(v[2 * j], p.act),
+                                                      act_apply(v[2 * j + 1], p.act));
+            packed[j] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(p.y + off);
+          dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+          if (nvalid == 16) dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        }
+      }
+      gb::tc_fence_before();
+      gb::mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+
+  gb::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    gb::tc_fence_after();
+    gb::tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+__global__ void pack_igemm_weights_kernel(const __nv_bfloat16* __restrict__ w,
+                                          __nv_bfloat16* __restrict__ wp, int K, int RS, int C,
+                                          int Cp) {
+  const long long total = (long long)K * RS * Cp;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int c = (int)(i % Cp);
+    const long long krs = i / Cp;
+    wp[i] = c < C ? w[krs * C + c] : __float2bfloat16(0.0f);
+  }
+}
+
+template <int BN>
+cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, const float* bias,
+                      const void* res, void* y, int* err, unsigned long long wait_ns,
+                      cudaStream_t st) {
+  using Cf = Cfg<BN>;
+  const int Cp = gb_ceil_div(d.C, BK) * BK;
+  IgemmParams p{};
+  p.H = d.H;
+  p.W = d.W;
+  p.C = d.C;
+  p.K = d.K;
+  p.S = d.S;
+  p.stride = d.stride;
+  p.pad = d.pad;
+  p.dil = d.dil;
+  p.OH = d.OH;
+  p.OW = d.OW;
+  p.cblocks = Cp / BK;
+  p.kiters = d.R * d.S * p.cblocks;
+  p.Kw = d.R * d.S * Cp;
+  p.M = (long long)d.N * d.OH * d.OW;
+  p.m_tiles = (int)gb_ceil_div_ll(p.M, BM);
+  p.n_tiles = gb_ceil_div(d.K, BN);
+  p.act = d.act;
+  p.bias = bias;
+  p.res = static_cast<const __nv_bfloat16*>(res);
+  p.y = static_cast<__nv_bfloat16*>(y);
+  p.err = err;
+  p.wait_ns = wait_ns;
+
+  CUtensorMap tmx, tmw;
+  {
+    cuuint64_t dims[4] = {(cuuint64_t)d.C, (cuuint64_t)d.W, (cuuint64_t)d.H, (cuuint64_t)d.N};
+    cuuint64_t strides[3] = {(cuuint64_t)d.C * 2, (cuuint64_t)d.W * d.C * 2,
+                             (cuuint64_t)d.H * d.W * d.C * 2};
+    // Bounding box of the first filter tap's pixel: from -pad to
+    // (dim - 1) + pad - dil*(R-1) (R == S is required).
+    int lower[2] = {-d.pad, -d.pad};
+    int upper[2] = {d.pad - d.dil * (d.S - 1), d.pad - d.dil * (d.R - 1)};
+    cuuint32_t estr[4] = {1, (cuuint32_t)d.stride, (cuuint32_t)d.stride, 1};
+    CUresult r = gb_encode_im2col(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x),
+                                  dims, strides, lower, upper, BK, BM, estr,
+                                  CU_TENSOR_MAP_SWIZZLE_128B);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)p.Kw, (cuuint64_t)d.K};
+    cuuint64_t strides[1] = {(cuuint64_t)p.Kw * 2};
+    cuuint32_t box[2] = {BK, BN};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = gb_encode_tiled(&tmw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                                 const_cast<void*>(wpack), dims, strides, box, estr,
+                                 CU_TENSOR_MAP_SWIZZLE_128B);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(igemm_bf16_tc_kernel<BN>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+  if (e != cudaSuccess) return e;
+  const int tiles = p.m_tiles * p.n_tiles;
+  const int grid = tiles < gb_num_sms() ? tiles : gb_num_sms();
+  igemm_bf16_tc_kernel<BN><<<grid, 192, Cf::SMEM, st>>>(tmx, tmw, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int igemm_block_n(int algo) {
+  switch (algo) {
+    case CONV_ALGO_IGEMM_N64: return 64;
+    case CONV_ALGO_IGEMM_N128: return 128;
+    case CONV_ALGO_IGEMM_N256: return 256;
+    default: return 0;
+  }
+}
+
+cudaError_t launch_igemm_bf16(const gbconv_desc_s& d, int block_n, const void* x,
+                              const void* wpack, const float* bias, const void* res, void* y,
+                              int* err, unsigned long long wait_ns, cudaStream_t st) {
+  switch (block_n) {
+    case 64: return launch_bn<64>(d, x, wpack, bias, res, y, err, wait_ns, st);
+    case 128: return launch_bn<128>(d, x, wpack, bias, res, y, err, wait_ns, st);
+    case 256: return launch_bn<256>(d, x, wpack, bias, res, y, err, wait_ns, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_pack_igemm_weights(const gbconv_desc_s& d, const void* w, void* wpack,
+                                      cudaStream_t st) {
+  const int Cp = gb_ceil_div(d.C, BK) * BK;
+  const long long total = (long long)d.K * d.R * d.S * Cp;
+  const int block = 256;
+  const int grid = (int)std::min<long long>(gb_ceil_div_ll(total, block), 65535LL * 8);
+  pack_igemm_weights_kernel<<<grid, block, 0, st>>>(static_cast<const __nv_bfloat16*>(w),
+                                                    static_cast<__nv_bfloat16*>(wpack), d.K,
+                                                    d.R * d.S, d.C, Cp);
+  return cudaGetLastError();
+}

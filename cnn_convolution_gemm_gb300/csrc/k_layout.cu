@@ -1,0 +1,189 @@
+// Layout conversion (the MegEngine report's "Inference Layout": NCHW at the
+// boundary, a channel-innermost layout with the channel axis padded to the
+// vector width on the device), pooling for the ResNet-50 forward pass, and a
+// deterministic random fill for Fast-Run scratch tensors.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "internal.h"
+
+namespace {
+
+constexpr int kBlock = 256;
+
+int grid_for(long long work) {
+  return (int)std::min<long long>(gb_ceil_div_ll(work, kBlock), 148LL * 32);
+}
+
+// One thread per output pixel (n, h, w): reads C strided values (coalesced
+// across the warp along w) and writes C_out contiguous bf16 values.
+__global__ void nchw_f32_to_nhwc_bf16_kernel(const float* __restrict__ x,
+                                             __nv_bfloat16* __restrict__ y, int N, int C, int H,
+                                             int W, int C_out) {
+  const long long pixels = (long long)N * H * W;
+  const long long hw = (long long)H * W;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < pixels;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long n = i / hw, p = i % hw;
+    const float* src = x + n * C * hw + p;
+    __nv_bfloat16* dst = y + i * C_out;
+    int c = 0;
+    for (; c + 1 < C_out; c += 2) {
+      const float a = c < C ? src[(long long)c * hw] : 0.f;
+      const float b = c + 1 < C ? src[(long long)(c + 1) * hw] : 0.f;
+      *reinterpret_cast<__nv_bfloat162*>(dst + c) = __floats2bfloat162_rn(a, b);
+    }
+    if (c < C_out) dst[c] = __float2bfloat16_rn(c < C ? src[(long long)c * hw] : 0.f);
+  }
+}
+
+__global__ void nhwc_bf16_to_nchw_f32_kernel(const __nv_bfloat16* __restrict__ x,
+                                             float* __restrict__ y, int N, int C, int H, int W,
+                                             int C_in) {
+  const long long total = (long long)N * C * H * W;
+  const long long hw = (long long)H * W;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long p = i % hw;
+    const long long c = (i / hw) % C;
+    const long long n = i / (hw * C);
+    y[i] = __bfloat162float(x[(n * hw + p) * C_in + c]);
+  }
+}
+
+// Max pooling, NHWC bf16, 8 channels (16 bytes) per thread.
+__global__ void maxpool_nhwc_bf16_kernel(const __nv_bfloat16* __restrict__ x,
+                                         __nv_bfloat16* __restrict__ y, int N, int C, int H,
+                                         int W, int k, int stride, int pad, int OH, int OW) {
+  const int cv = C / 8;
+  const long long total = (long long)N * OH * OW * cv;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int c8 = (int)(i % cv);
+    long long t = i / cv;
+    const int ow = (int)(t % OW);
+    t /= OW;
+    const int oh = (int)(t % OH);
+    const int n = (int)(t / OH);
+    float m[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m[j] = -INFINITY;
+    for (int r = 0; r < k; ++r) {
+      const int ih = oh * stride - pad + r;
+      if (ih < 0 || ih >= H) continue;
+      for (int s = 0; s < k; ++s) {
+        const int iw = ow * stride - pad + s;
+        if (iw < 0 || iw >= W) continue;
+        const uint4 v =
+            *reinterpret_cast<const uint4*>(x + (((long long)n * H + ih) * W + iw) * C + c8 * 8);
+        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = __bfloat1622float2(b[j]);
+          m[2 * j] = fmaxf(m[2 * j], f.x);
+          m[2 * j + 1] = fmaxf(m[2 * j + 1], f.y);
+        }
+      }
+    }
+    uint4 o;
+    __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) ob[j] = __floats2bfloat162_rn(m[2 * j], m[2 * j + 1]);
+    *reinterpret_cast<uint4*>(y + i * 8) = o;
+  }
+}
+
+// Global average pooling: one thread per (n, 8-channel vector), fp32 sum.
+__global__ void avgpool_nhwc_bf16_kernel(const __nv_bfloat16* __restrict__ x,
+                                         __nv_bfloat16* __restrict__ y, int N, int C, int HW) {
+  const int cv = C / 8;
+  const long long total = (long long)N * cv;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int c8 = (int)(i % cv);
+    const long long n = i / cv;
+    float s[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int p = 0; p < HW; ++p) {
+      const uint4 v = *reinterpret_cast<const uint4*>(x + (n * HW + p) * C + c8 * 8);
+      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __bfloat1622float2(b[j]);
+        s[2 * j] += f.x;
+        s[2 * j + 1] += f.y;
+      }
+    }
+    const float inv = 1.0f / (float)HW;
+    uint4 o;
+    __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) ob[j] = __floats2bfloat162_rn(s[2 * j] * inv, s[2 * j + 1] * inv);
+    *reinterpret_cast<uint4*>(y + n * C + c8 * 8) = o;
+  }
+}
+
+__device__ __forceinline__ uint32_t hash32(uint32_t v) {
+  v ^= v >> 16;
+  v *= 0x7feb352dU;
+  v ^= v >> 15;
+  v *= 0x846ca68bU;
+  v ^= v >> 16;
+  return v;
+}
+
+// Values in [-1, 1) for float types, [-64, 63] for int8.
+__global__ void fill_random_kernel(uint8_t* p, long long n, int elem_bytes, uint32_t seed) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const uint32_t h = hash32((uint32_t)i * 2654435761u ^ seed);
+    if (elem_bytes == 4) {
+      reinterpret_cast<float*>(p)[i] = (float)(h >> 8) * (1.0f / 8388608.0f) - 1.0f;
+    } else if (elem_bytes == 2) {
+      reinterpret_cast<__nv_bfloat16*>(p)[i] =
+          __float2bfloat16_rn((float)(h >> 8) * (1.0f / 8388608.0f) - 1.0f);
+    } else {
+      reinterpret_cast<int8_t*>(p)[i] = (int8_t)((int)(h >> 25) - 64);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_nchw_f32_to_nhwc_bf16(const float* x, void* y, int N, int C, int H, int W,
+                                         int C_out, cudaStream_t st) {
+  nchw_f32_to_nhwc_bf16_kernel<<<grid_for((long long)N * H * W), kBlock, 0, st>>>(
+      x, static_cast<__nv_bfloat16*>(y), N, C, H, W, C_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nhwc_bf16_to_nchw_f32(const void* x, float* y, int N, int C, int H, int W,
+                                         int C_in, cudaStream_t st) {
+  nhwc_bf16_to_nchw_f32_kernel<<<grid_for((long long)N * C * H * W), kBlock, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(x), y, N, C, H, W, C_in);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_maxpool_nhwc_bf16(const void* x, void* y, int N, int C, int H, int W, int k,
+                                     int stride, int pad, cudaStream_t st) {
+  const int OH = (H + 2 * pad - k) / stride + 1, OW = (W + 2 * pad - k) / stride + 1;
+  maxpool_nhwc_bf16_kernel<<<grid_for((long long)N * OH * OW * (C / 8)), kBlock, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), N, C, H, W, k, stride,
+      pad, OH, OW);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_avgpool_nhwc_bf16(const void* x, void* y, int N, int C, int H, int W,
+                                     cudaStream_t st) {
+  avgpool_nhwc_bf16_kernel<<<grid_for((long long)N * (C / 8)), kBlock, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), N, C, H * W);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fill_random(void* p, size_t bytes, int elem_bytes, uint32_t seed,
+                               cudaStream_t st) {
+  const long long n = (long long)(bytes / elem_bytes);
+  fill_random_kernel<<<grid_for(n), kBlock, 0, st>>>(static_cast<uint8_t*>(p), n, elem_bytes,
+                                                     seed);
+  return cudaGetLastError();
+}

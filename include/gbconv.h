@@ -1,0 +1,198 @@
+/*
+ * gbconv — 2D convolution forward for CNN inference on GB300 (sm_103a).
+ *
+ * A C ABI over hand-written CUDA kernels.  Plain pointers and sizes only.
+ * All tensor pointers are caller-owned DEVICE memory unless a function says
+ * otherwise; the library never frees them.  Every call that launches work is
+ * stream-ordered on the given stream (a cudaStream_t passed as void*; NULL is
+ * the legacy default stream) and returns as soon as the work is enqueued.
+ *
+ * Passages cited below are from the four pages this library implements:
+ *   [MegEngine]  aminer.cn report on MegEngine's CPU convolution work
+ *                (sections "Inference Layout", "Im2col+MatMul", "Winograd",
+ *                "Fast-Run");
+ *   [Momenta]    getit01.com "Paper Reading | 讓深度學習更高效運行的兩個視角"
+ *                (roofline, FLOP/traffic accounting, depthwise, fusion);
+ *   [Beta]       96x.com.cn MegEngine Beta report (native int8 inference);
+ *   [卷积总结]   razer666.cn convolution-internals post (direct loop,
+ *                im2col -> GEMM).
+ *
+ * Error behaviour: every function returns a conv_status_t.  Host-side
+ * validation failures return before anything is enqueued.  Errors detected by
+ * a kernel on the device (a bounded wait that ran out, an internal check) are
+ * recorded in a device-side error word and reported by conv_sync_status().
+ * conv_last_error_detail() gives a human-readable reason for the last failure
+ * on the calling thread.
+ */
+#ifndef GBCONV_H_
+#define GBCONV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gbconv_desc_s* conv_desc_t;
+
+typedef enum {
+  CONV_OK = 0,
+  CONV_ERR_BAD_PARAM = 1,      /* invalid argument (null, negative size, ...)          */
+  CONV_ERR_UNSUPPORTED = 2,    /* the algorithm does not apply to this descriptor      */
+  CONV_ERR_ALIGNMENT = 3,      /* a pointer is not 16-byte aligned (TMA requirement)   */
+  CONV_ERR_WORKSPACE = 4,      /* workspace missing or smaller than conv_workspace_size */
+  CONV_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed                    */
+  CONV_ERR_TIMEOUT = 6,        /* a device-side bounded wait ran out                   */
+  CONV_ERR_INTERNAL = 7,       /* a device-side consistency check failed               */
+  CONV_ERR_FASTRUN_FILE = 8,   /* Fast-Run map file unreadable, corrupt or mismatched  */
+  CONV_ERR_NOT_FOUND = 9       /* no Fast-Run entry for this descriptor                */
+} conv_status_t;
+
+/* Element type of x, w and y.  CONV_BF16: bfloat16 tensors, fp32 bias,
+ * fp32 accumulation.  CONV_F32: fp32 tensors and bias.  CONV_INT8: int8
+ * tensors, int32 bias, exact int32 accumulation, fp32 per-channel requant. */
+typedef enum { CONV_BF16 = 0, CONV_F32 = 1, CONV_INT8 = 2 } conv_dtype_t;
+
+/* Activation layout ([MegEngine] "Inference Layout").  NHWC is the device
+ * layout of every fast kernel; NCHW is accepted for CONV_F32 only. */
+typedef enum { CONV_NHWC = 0, CONV_NCHW = 1 } conv_layout_t;
+
+typedef enum { CONV_ACT_NONE = 0, CONV_ACT_RELU = 1, CONV_ACT_RELU6 = 2 } conv_act_t;
+
+/* Algorithm ids ([MegEngine] "Fast-Run": Im2col, Direct and Winograd are the
+ * candidate implementations).  Ids are stable. */
+typedef int conv_algo_t;
+#define CONV_ALGO_AUTO (-1)        /* Fast-Run map entry if present, else the heuristic */
+#define CONV_ALGO_DIRECT 0         /* CUDA-core direct loop, any shape ([卷积总结])      */
+#define CONV_ALGO_IGEMM_N64 1      /* implicit GEMM on tcgen05, 128x64 output tiles     */
+#define CONV_ALGO_IGEMM_N128 2     /* implicit GEMM on tcgen05, 128x128 output tiles    */
+#define CONV_ALGO_IGEMM_N256 3     /* implicit GEMM on tcgen05, 128x256 output tiles    */
+#define CONV_ALGO_WINO_F2 4        /* Winograd F(2x2,3x3)                               */
+#define CONV_ALGO_WINO_F6 5        /* Winograd F(6x6,3x3)                               */
+#define CONV_ALGO_DEPTHWISE 6      /* depthwise 3x3 (groups == C == K)                  */
+#define CONV_ALGO_INT8_MMA 7       /* int8 implicit GEMM, exact int32 accumulate        */
+#define CONV_ALGO_COUNT 8
+
+/* ---- descriptor --------------------------------------------------------- */
+
+/* Create a convolution descriptor.
+ * Defines y[n,oh,ow,k] = act(b[k] + sum_{c in group(k), r, s}
+ *     w[k,r,s,c] * x[n, oh*stride - pad + r*dilation, ow*stride - pad + s*dilation, c]
+ *     (+ residual[n,oh,ow,k])), x = 0 outside the image: the direct loop of
+ * [卷积总结] "最原始的卷积实现" with the stride, dilation and padding it names,
+ * cross-correlation (no kernel flip) as in its "稀疏连接" example.
+ * OH = (H + 2*pad - dilation*(R-1) - 1)/stride + 1, likewise OW.
+ * Requirements: all sizes > 0, C % groups == 0, K % groups == 0, OH, OW > 0.
+ * The descriptor is owned by the caller and freed with conv_desc_destroy.
+ * Defaults: layout NHWC, no activation, no residual, no requant scale. */
+conv_status_t conv_desc_create(conv_desc_t* out, int N, int C, int H, int W, int K, int R, int S,
+                               int stride, int pad, int dilation, int groups, conv_dtype_t dtype);
+conv_status_t conv_desc_destroy(conv_desc_t desc);
+/* Activation layout of x, y and residual (weights follow: NHWC -> w is
+ * [K][R][S][C/groups], NCHW -> w is [K][C/groups][R][S]). NCHW: CONV_F32 only. */
+conv_status_t conv_desc_set_layout(conv_desc_t desc, conv_layout_t layout);
+/* Fused epilogue ([Momenta] "Graph層面": bias and ReLU fused into the matrix
+ * product).  act: conv_act_t; has_residual: conv_fwd reads a residual tensor
+ * shaped like y and adds it before the activation.  INT8 supports
+ * act in {NONE, RELU} and no residual. */
+conv_status_t conv_desc_set_epilogue(conv_desc_t desc, int act, int has_residual);
+/* INT8 only: per-output-channel requant scale, fp32 [K], DEVICE pointer that
+ * must stay valid while the descriptor is used.  Output int8 value:
+ * q = clamp(round_half_even(fp32(acc + bias[k]) * scale[k]), -128, 127), then
+ * the activation.  ([Beta] "推理：高效原生 int8 实现"; the pages print no
+ * formula, this is the library's definition.) */
+conv_status_t conv_desc_set_requant(conv_desc_t desc, const float* scale_dev);
+/* Output spatial size. */
+conv_status_t conv_desc_get_output_dims(conv_desc_t desc, int* OH, int* OW);
+
+/* ---- algorithms --------------------------------------------------------- */
+
+/* Number of algorithm ids (CONV_ALGO_COUNT). */
+conv_status_t conv_algo_count(conv_desc_t desc, int* count);
+/* Info for algorithm index i in [0, count): its id, a static name string and
+ * whether it applies to the descriptor (1) or not (0). */
+conv_status_t conv_algo_info(conv_desc_t desc, int i, conv_algo_t* algo, const char** name,
+                             int* applicable);
+/* The algorithm CONV_ALGO_AUTO resolves to (Fast-Run map, else heuristic). */
+conv_status_t conv_algo_resolve(conv_desc_t desc, conv_algo_t* algo);
+/* Bytes of device workspace conv_fwd needs for (desc, algo); 0 if none. */
+conv_status_t conv_workspace_size(conv_desc_t desc, conv_algo_t algo, size_t* bytes);
+/* Bytes of the packed weight buffer for (desc, algo). */
+conv_status_t conv_weights_packed_size(conv_desc_t desc, conv_algo_t algo, size_t* bytes);
+/* Pack weights once per layer ([MegEngine] "Winograd": the weights are
+ * transformed ahead; for implicit GEMM the reduction axis is padded to the
+ * tile).  w: device, layout per conv_desc_set_layout, dtype of the desc.
+ * wpack: device, conv_weights_packed_size bytes, 16-byte aligned, caller-owned.
+ * Stream-ordered. */
+conv_status_t conv_weights_prepack(conv_desc_t desc, conv_algo_t algo, const void* w,
+                                   void* wpack, void* stream);
+
+/* ---- forward ------------------------------------------------------------ */
+
+/* y = conv(x, w) + bias (+ residual), activation; per conv_desc_create.
+ * x, y, residual: device, layout of the desc, dtype of the desc, 16-byte
+ * aligned.  wpack: output of conv_weights_prepack for the SAME algo (after
+ * CONV_ALGO_AUTO resolution; use conv_algo_resolve).  bias: device fp32 [K]
+ * (int32 [K] for INT8) or NULL for zero.  residual: NULL unless the desc has
+ * has_residual.  ws: device workspace of at least conv_workspace_size bytes
+ * (NULL if 0).  Returns CONV_ERR_UNSUPPORTED if algo does not apply.
+ * Stream-ordered; x, wpack, bias, residual must stay valid until the work
+ * completes. */
+conv_status_t conv_fwd(conv_desc_t desc, const void* x, const void* wpack, const void* bias,
+                       const void* residual, void* y, conv_algo_t algo, void* ws,
+                       size_t ws_bytes, void* stream);
+
+/* ---- Fast-Run ([MegEngine] "Fast-Run") ----------------------------------- */
+
+/* Selection phase: time every applicable algorithm for this descriptor on the
+ * current device (scratch buffers allocated and freed inside the call;
+ * synchronizes the stream), keep the fastest in the process-wide map under
+ * the descriptor's key, and return it.  times_ms (optional, CONV_ALGO_COUNT
+ * entries) receives each algorithm's median time, or -1 where not applicable.
+ * Execution phase: CONV_ALGO_AUTO looks the map up. */
+conv_status_t conv_fastrun_select(conv_desc_t desc, void* stream, conv_algo_t* best,
+                                  float* times_ms);
+/* Map lookup only; CONV_ERR_NOT_FOUND if the descriptor was never selected. */
+conv_status_t conv_fastrun_lookup(conv_desc_t desc, conv_algo_t* algo);
+/* Persist / restore the map (text file; entries keyed by descriptor, device
+ * name, SM count and library version; entries for another device or version
+ * are skipped on load).  A corrupt file returns CONV_ERR_FASTRUN_FILE and
+ * leaves the map unchanged. */
+conv_status_t conv_fastrun_save(const char* path);
+conv_status_t conv_fastrun_load(const char* path);
+conv_status_t conv_fastrun_clear(void);
+
+/* ---- layout conversion and pooling -------------------------------------- */
+
+/* NCHW fp32 -> NHWC bf16 (round to nearest even), C_out >= C channels with
+ * the extra channels zero ([MegEngine] "Inference Layout": padding the
+ * channel axis to the vector width).  Stream-ordered. */
+conv_status_t conv_nchw_f32_to_nhwc_bf16(const float* x, void* y, int N, int C, int H, int W,
+                                         int C_out, void* stream);
+/* NHWC bf16 (C_in >= C channels, first C used) -> NCHW fp32. */
+conv_status_t conv_nhwc_bf16_to_nchw_f32(const void* x, float* y, int N, int C, int H, int W,
+                                         int C_in, void* stream);
+/* Max pooling, NHWC bf16, window k x k, stride, pad (outside = -inf). */
+conv_status_t conv_maxpool2d_nhwc_bf16(const void* x, void* y, int N, int C, int H, int W, int k,
+                                       int stride, int pad, void* stream);
+/* Global average pooling, NHWC bf16 [N][H][W][C] -> bf16 [N][C]. */
+conv_status_t conv_global_avgpool_nhwc_bf16(const void* x, void* y, int N, int C, int H, int W,
+                                            void* stream);
+
+/* ---- status ------------------------------------------------------------- */
+
+/* Synchronizes the stream, then reads and clears the device error word:
+ * CONV_OK, CONV_ERR_TIMEOUT or CONV_ERR_INTERNAL (or CONV_ERR_CUDA if the
+ * synchronization itself failed). */
+conv_status_t conv_sync_status(void* stream);
+const char* conv_status_string(conv_status_t status);
+/* Reason for the last non-OK status returned on this thread ("" if none). */
+const char* conv_last_error_detail(void);
+/* Library version string. */
+const char* conv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GBCONV_H_ */

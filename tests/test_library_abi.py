@@ -1,0 +1,111 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads,
+exports every symbol the header declares, and its pure-host calls validate
+arguments, report errors and persist the Fast-Run map."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def B():
+    from cnn_convolution_gemm_gb300 import build
+    build.build()
+    from cnn_convolution_gemm_gb300 import binding
+    binding.load_library()
+    return binding
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "gbconv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(conv_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported_and_bound(B):
+    import ctypes
+    names = _header_functions()
+    assert len(names) >= 25
+    lib = ctypes.CDLL(B.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(B.SIGNATURES), set(names) ^ set(B.SIGNATURES)
+
+
+def test_desc_validation(B):
+    with pytest.raises(B.GbconvError) as e:
+        B.conv_desc_create(1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 2, B.CONV_BF16)  # C % groups
+    assert e.value.status_name == "CONV_ERR_BAD_PARAM"
+    with pytest.raises(B.GbconvError):
+        B.conv_desc_create(1, 4, 2, 2, 4, 5, 5, 1, 0, 1, 1, B.CONV_BF16)  # empty output
+    d = B.conv_desc_create(2, 64, 56, 56, 64, 3, 3, 2, 1, 1, 1, B.CONV_BF16)
+    assert B.conv_desc_get_output_dims(d) == (28, 28)
+    with pytest.raises(B.GbconvError) as e:
+        B.conv_desc_set_layout(d, B.CONV_NCHW)
+    assert e.value.status_name == "CONV_ERR_UNSUPPORTED"
+    B.conv_desc_destroy(d)
+
+
+def test_algo_table_and_applicability(B):
+    d = B.conv_desc_create(32, 256, 56, 56, 256, 3, 3, 1, 1, 1, 1, B.CONV_BF16)
+    infos = [B.conv_algo_info(d, i) for i in range(B.conv_algo_count(d))]
+    names = {n: ok for _, n, ok in infos}
+    assert names["direct"] and names["igemm_tc_n256"]
+    dw = B.conv_desc_create(64, 144, 56, 56, 144, 3, 3, 1, 1, 1, 144, B.CONV_BF16)
+    dnames = {n: ok for _, n, ok in (B.conv_algo_info(dw, i) for i in range(B.CONV_ALGO_COUNT))}
+    assert not dnames["igemm_tc_n64"]  # grouped: implicit GEMM does not apply
+    with pytest.raises(B.GbconvError) as e:
+        B.conv_weights_packed_size(dw, B.CONV_ALGO_IGEMM_N64)
+    assert e.value.status_name == "CONV_ERR_UNSUPPORTED"
+    assert B.conv_weights_packed_size(d, B.CONV_ALGO_IGEMM_N128) == 256 * 9 * 256 * 2
+    # C = 24 pads to one 64-channel block per filter tap
+    e24 = B.conv_desc_create(64, 24, 56, 56, 144, 1, 1, 1, 0, 1, 1, B.CONV_BF16)
+    assert B.conv_weights_packed_size(e24, B.CONV_ALGO_IGEMM_N64) == 144 * 64 * 2
+    for h in (d, dw, e24):
+        B.conv_desc_destroy(h)
+
+
+def test_fwd_argument_errors(B):
+    d = B.conv_desc_create(1, 64, 8, 8, 64, 3, 3, 1, 1, 1, 1, B.CONV_BF16)
+    with pytest.raises(B.GbconvError) as e:
+        B.conv_fwd(d, 0, 0, 0, 0, 0, B.CONV_ALGO_DIRECT)
+    assert e.value.status_name == "CONV_ERR_BAD_PARAM"
+    with pytest.raises(B.GbconvError) as e:  # misaligned pointers are rejected before launch
+        B.conv_fwd(d, 0x1008, 0x2000, 0, 0, 0x3000, B.CONV_ALGO_IGEMM_N64)
+    assert e.value.status_name == "CONV_ERR_ALIGNMENT"
+    with pytest.raises(B.GbconvError) as e:
+        B.conv_fwd(d, 0x1000, 0x2000, 0, 0x4000, 0x3000, B.CONV_ALGO_IGEMM_N64)
+    assert e.value.status_name == "CONV_ERR_BAD_PARAM"  # residual without has_residual
+    B.conv_desc_destroy(d)
+
+
+def test_status_strings(B):
+    assert B.conv_status_string(0) == "CONV_OK"
+    assert B.conv_status_string(6) == "CONV_ERR_TIMEOUT"
+    assert B.conv_version().startswith("gbconv")
+
+
+def test_fastrun_file_roundtrip_and_corruption(B, tmp_path):
+    B.conv_fastrun_clear()
+    p = tmp_path / "map.txt"
+    B.conv_fastrun_save(str(p))
+    text = p.read_text()
+    assert "version" in text and "end 0" in text
+    B.conv_fastrun_load(str(p))
+    bad = tmp_path / "bad.txt"
+    bad.write_text(text.replace("end 0", "end 3"))
+    with pytest.raises(B.GbconvError) as e:
+        B.conv_fastrun_load(str(bad))
+    assert e.value.status_name == "CONV_ERR_FASTRUN_FILE"
+    bad.write_text("garbage\n")
+    with pytest.raises(B.GbconvError):
+        B.conv_fastrun_load(str(bad))
+    with pytest.raises(B.GbconvError):
+        B.conv_fastrun_load(str(tmp_path / "missing.txt"))
+    d = B.conv_desc_create(1, 8, 4, 4, 8, 3, 3, 1, 1, 1, 1, B.CONV_BF16)
+    with pytest.raises(B.GbconvError) as e:
+        B.conv_fastrun_lookup(d)
+    assert e.value.status_name == "CONV_ERR_NOT_FOUND"
+    B.conv_desc_destroy(d)
