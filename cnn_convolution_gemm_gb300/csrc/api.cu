@@ -512,13 +512,26 @@ extern "C" conv_status_t conv_fastrun_select(conv_desc_t d, void* stream, conv_a
   if (res.p) launch_fill_random(res.p, yb, esz, 3u, s);
 
   float tms[CONV_ALGO_COUNT];
+  for (int a = 0; a < CONV_ALGO_COUNT; ++a) tms[a] = -1.f;
   int best_a = -1;
   float best_t = 0.f;
   cudaEvent_t e0, e1;
   cudaEventCreate(&e0);
   cudaEventCreate(&e1);
-  for (int a = 0; a < CONV_ALGO_COUNT; ++a) {
-    tms[a] = -1.f;
+  // The heuristic's choice is timed first so that a clearly slower candidate
+  // can be measured with a single run instead of the full repetition count.
+  std::vector<int> order{heuristic(dd)};
+  for (int a = 0; a < CONV_ALGO_COUNT; ++a)
+    if (a != order[0]) order.push_back(a);
+  auto time_once = [&](int a, void* wp, void* wsp, size_t wsb, float* ms) {
+    cudaEventRecord(e0, s);
+    const bool ok = fwd_impl(dd, x.p, wp, bias.p, res.p, y.p, a, wsp, wsb, s) == CONV_OK;
+    cudaEventRecord(e1, s);
+    cudaEventSynchronize(e1);
+    cudaEventElapsedTime(ms, e0, e1);
+    return ok;
+  };
+  for (int a : order) {
     if (!implemented(a) || !applicable(dd, a, nullptr)) continue;
     size_t pb = 0, wsb = 0;
     if (conv_weights_packed_size(&dd, a, &pb) != CONV_OK) continue;
@@ -529,26 +542,30 @@ extern "C" conv_status_t conv_fastrun_select(conv_desc_t d, void* stream, conv_a
       continue;
     }
     if (conv_weights_prepack(&dd, a, w.p, wp.p, s) != CONV_OK) continue;
-    // warm-up, then the median of `reps` timed runs
+    float probe = 0.f;
+    if (fwd_impl(dd, x.p, wp.p, bias.p, res.p, y.p, a, ws.p, wsb, s) != CONV_OK) continue;
+    if (!time_once(a, wp.p, ws.p, wsb, &probe)) continue;
+    if (best_a >= 0 && probe > 5.f * best_t) {  // far slower: one measurement is enough
+      tms[a] = probe;
+      continue;
+    }
     bool ok = true;
-    for (int i = 0; i < 3 && ok; ++i)
+    for (int i = 0; i < 2 && ok; ++i)
       ok = fwd_impl(dd, x.p, wp.p, bias.p, res.p, y.p, a, ws.p, wsb, s) == CONV_OK;
-    if (!ok) continue;
     std::vector<float> t;
     const int reps = 15;
     for (int i = 0; i < reps && ok; ++i) {
-      cudaEventRecord(e0, s);
-      ok = fwd_impl(dd, x.p, wp.p, bias.p, res.p, y.p, a, ws.p, wsb, s) == CONV_OK;
-      cudaEventRecord(e1, s);
-      cudaEventSynchronize(e1);
       float ms = 0.f;
-      cudaEventElapsedTime(&ms, e0, e1);
+      ok = time_once(a, wp.p, ws.p, wsb, &ms);
       t.push_back(ms);
     }
     if (!ok || cudaStreamSynchronize(s) != cudaSuccess) continue;
     std::sort(t.begin(), t.end());
     tms[a] = t[t.size() / 2];
-    // strictly faster by more than 1% wins; otherwise the lower id is kept
+  }
+  // Fastest median wins; within 1% the lower id is kept (deterministic ties).
+  for (int a = 0; a < CONV_ALGO_COUNT; ++a) {
+    if (tms[a] < 0.f) continue;
     if (best_a < 0 || tms[a] < best_t * 0.99f) {
       best_a = a;
       best_t = tms[a];
