@@ -402,6 +402,7 @@ extern "C" conv_status_t conv_weights_prepack(conv_desc_t d, conv_algo_t algo, c
     case CONV_ALGO_IGEMM_N128:
     case CONV_ALGO_IGEMM_N256: e = launch_pack_igemm_weights(*d, w, wpack, s); break;
     case CONV_ALGO_INT8_MMA: e = launch_pack_int8_weights(*d, w, wpack, s); break;
+    case CONV_ALGO_DEPTHWISE: e = launch_pack_dw_weights(*d, w, wpack, s); break;
     case CONV_ALGO_WINO_F2: e = launch_winograd_filter_transform(*d, 2, w, wpack, s); break;
     case CONV_ALGO_WINO_F6: e = launch_winograd_filter_transform(*d, 6, w, wpack, s); break;
     default:
@@ -762,6 +763,10 @@ static bool implemented(int algo) {
     case CONV_ALGO_IGEMM_N64:
     case CONV_ALGO_IGEMM_N128:
     case CONV_ALGO_IGEMM_N256:
+    case CONV_ALGO_DEPTHWISE:
+    case CONV_ALGO_WINO_F2:
+    case CONV_ALGO_WINO_F6:
+    case CONV_ALGO_INT8_MMA:
       return true;
     default:
       return false;

@@ -57,10 +57,19 @@ cudaError_t launch_igemm_bf16(const gbconv_desc_s& d, int block_n, const void* x
                               int* err, unsigned long long wait_ns, cudaStream_t st);
 cudaError_t launch_pack_igemm_weights(const gbconv_desc_s& d, const void* w, void* wpack,
                                       cudaStream_t st);
+// Batched GEMM on the same tcgen05 pipeline: out[b][m][n] (fp32) =
+// sum_k A[b][m][k] * B[b][n][k]; A, B K-major fp16 (ab_type 0) or bf16 (1);
+// N and Kred multiples of 8.
+cudaError_t launch_batched_gemm_tc(int batch, int M, int N, int Kred, const void* A,
+                                   const void* B, float* out, int ab_type, int block_n, int* err,
+                                   unsigned long long wait_ns, cudaStream_t st);
 
-// Depthwise 3x3 (bf16 NHWC).  w: [C][3][3] bf16 (the user layout [K][R][S][1]).
+// Depthwise 3x3 (bf16 NHWC).  w: packed tap-major [9][C] bf16.
 cudaError_t launch_dwconv3x3(const gbconv_desc_s& d, const void* x, const void* w,
                              const float* bias, const void* res, void* y, cudaStream_t st);
+// [C][3][3] -> tap-major [9][C] bf16.
+cudaError_t launch_pack_dw_weights(const gbconv_desc_s& d, const void* w, void* wpack,
+                                   cudaStream_t st);
 
 // int8 implicit GEMM (mma.sync s8, exact int32 accumulate).  wpack: [K][R*S][Cp] int8.
 cudaError_t launch_igemm_int8(const gbconv_desc_s& d, const void* x, const void* wpack,

@@ -48,7 +48,13 @@ struct IgemmParams {
   __nv_bfloat16* y;
   int* err;
   unsigned long long wait_ns;
+  // batched-GEMM mode: `batch` independent [M x Kred] x [K x Kred]^T products
+  int batch;
+  int ab_type;  // 0 = fp16 operands, 1 = bf16
+  float* out_f32;
 };
+
+enum { MODE_CONV = 0, MODE_BATCHED = 1 };
 
 template <int BN>
 struct Cfg {
@@ -67,7 +73,7 @@ __device__ __forceinline__ float act_apply(float v, int act) {
   return v;
 }
 
-template <int BN>
+template <int BN, int MODE>
 __global__ void __launch_bounds__(192, 1)
     igemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                          const __grid_constant__ CUtensorMap tm_w, const IgemmParams p) {
@@ -111,7 +117,8 @@ __global__ void __launch_bounds__(192, 1)
   gb::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int num_tiles = p.m_tiles * p.n_tiles;
+  const int tiles_per_batch = p.m_tiles * p.n_tiles;
+  const int num_tiles = tiles_per_batch * (MODE == MODE_BATCHED ? p.batch : 1);
   const int ohow = p.OH * p.OW;
 
   if (warp == 0) {
@@ -122,12 +129,17 @@ __global__ void __launch_bounds__(192, 1)
       long long issued = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        const int mt = t / p.n_tiles, nt = t % p.n_tiles;
+        const int bt = t / tiles_per_batch;
+        const int tt = t % tiles_per_batch;
+        const int mt = tt / p.n_tiles, nt = tt % p.n_tiles;
         const long long m0 = (long long)mt * BM;
-        const int img = (int)(m0 / ohow);
-        const int rem = (int)(m0 % ohow);
-        const int h0 = (rem / p.OW) * p.stride - p.pad;
-        const int w0 = (rem % p.OW) * p.stride - p.pad;
+        int img = 0, h0 = 0, w0 = 0;
+        if (MODE == MODE_CONV) {
+          img = (int)(m0 / ohow);
+          const int rem = (int)(m0 % ohow);
+          h0 = (rem / p.OW) * p.stride - p.pad;
+          w0 = (rem % p.OW) * p.stride - p.pad;
+        }
         int cb = 0, s = 0, r = 0;
         for (int it = 0; it < p.kiters; ++it) {
           if (!gb::mbar_wait_bounded(&empty[stage], phase ^ 1, p.wait_ns, p.err)) {
@@ -135,10 +147,15 @@ __global__ void __launch_bounds__(192, 1)
             break;
           }
           gb::mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-          gb::tma_load_im2col_4d(sA + stage * C::A_BYTES, &tm_x, &full[stage], cb * BK, w0, h0,
-                                 img, (uint16_t)(s * p.dil), (uint16_t)(r * p.dil));
-          gb::tma_load_2d(sB + stage * C::B_BYTES, &tm_w, &full[stage],
-                          (r * p.S + s) * p.cblocks * BK + cb * BK, nt * BN);
+          if (MODE == MODE_CONV) {
+            gb::tma_load_im2col_4d(sA + stage * C::A_BYTES, &tm_x, &full[stage], cb * BK, w0, h0,
+                                   img, (uint16_t)(s * p.dil), (uint16_t)(r * p.dil));
+            gb::tma_load_2d(sB + stage * C::B_BYTES, &tm_w, &full[stage],
+                            (r * p.S + s) * p.cblocks * BK + cb * BK, nt * BN);
+          } else {
+            gb::tma_load_3d(sA + stage * C::A_BYTES, &tm_x, &full[stage], cb * BK, (int)m0, bt);
+            gb::tma_load_3d(sB + stage * C::B_BYTES, &tm_w, &full[stage], cb * BK, nt * BN, bt);
+          }
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -169,7 +186,7 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      constexpr uint32_t IDESC = gb::idesc_f16(BM, BN, 1);
+      const uint32_t IDESC = gb::idesc_f16(BM, BN, MODE == MODE_CONV ? 1 : p.ab_type);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -214,7 +231,9 @@ __global__ void __launch_bounds__(192, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-      const int mt = t / p.n_tiles, nt = t % p.n_tiles;
+      const int bt = t / tiles_per_batch;
+      const int tt = t % tiles_per_batch;
+      const int mt = tt / p.n_tiles, nt = tt % p.n_tiles;
       if (!gb::mbar_wait_bounded(&tfull[acc], acc_phase, p.wait_ns, p.err)) break;
       gb::tc_fence_after();
       const long long m = (long long)mt * BM + q * 32 + lane;
@@ -226,7 +245,18 @@ __global__ void __launch_bounds__(192, 1)
         gb::tmem_ld_x16(tbase + c0, r);
         gb::tmem_ld_wait();
         const int n = nt * BN + c0;
-        if (row_ok && n < p.K) {
+        if (MODE == MODE_BATCHED) {
+          if (row_ok && n < p.K) {
+            float4* dst = reinterpret_cast<float4*>(p.out_f32 +
+                                                    ((size_t)bt * p.M + m) * p.K + n);
+            const int nq = (p.K - n) >= 16 ? 4 : 2;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (q < nq)
+                dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                     __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+          }
+        } else if (row_ok && n < p.K) {
           float v[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
@@ -348,12 +378,61 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
                                  CU_TENSOR_MAP_SWIZZLE_128B);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(igemm_bf16_tc_kernel<BN>,
+  cudaError_t e = cudaFuncSetAttribute(igemm_bf16_tc_kernel<BN, MODE_CONV>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
   if (e != cudaSuccess) return e;
   const int tiles = p.m_tiles * p.n_tiles;
   const int grid = tiles < gb_num_sms() ? tiles : gb_num_sms();
-  igemm_bf16_tc_kernel<BN><<<grid, 192, Cf::SMEM, st>>>(tmx, tmw, p);
+  igemm_bf16_tc_kernel<BN, MODE_CONV><<<grid, 192, Cf::SMEM, st>>>(tmx, tmw, p);
+  return cudaGetLastError();
+}
+
+// out[b][m][n] = sum_k A[b][m][k] * B[b][n][k], fp32 out, fp16/bf16 operands.
+template <int BN>
+cudaError_t launch_batched_bn(int batch, int M, int N, int Kred, const void* A, const void* Bm,
+                              float* out, int ab_type, int* err, unsigned long long wait_ns,
+                              cudaStream_t st) {
+  using Cf = Cfg<BN>;
+  IgemmParams p{};
+  p.K = N;
+  p.cblocks = gb_ceil_div(Kred, BK);
+  p.kiters = p.cblocks;
+  p.M = M;
+  p.m_tiles = gb_ceil_div(M, BM);
+  p.n_tiles = gb_ceil_div(N, BN);
+  p.batch = batch;
+  p.ab_type = ab_type;
+  p.out_f32 = out;
+  p.err = err;
+  p.wait_ns = wait_ns;
+  p.OH = p.OW = 1;
+  const CUtensorMapDataType dt =
+      ab_type ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap tma, tmb;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)Kred, (cuuint64_t)M, (cuuint64_t)batch};
+    cuuint64_t strides[2] = {(cuuint64_t)Kred * 2, (cuuint64_t)M * Kred * 2};
+    cuuint32_t box[3] = {BK, BM, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (gb_encode_tiled(&tma, dt, 3, const_cast<void*>(A), dims, strides, box, estr,
+                        CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)Kred, (cuuint64_t)N, (cuuint64_t)batch};
+    cuuint64_t strides[2] = {(cuuint64_t)Kred * 2, (cuuint64_t)N * Kred * 2};
+    cuuint32_t box[3] = {BK, BN, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (gb_encode_tiled(&tmb, dt, 3, const_cast<void*>(Bm), dims, strides, box, estr,
+                        CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(igemm_bf16_tc_kernel<BN, MODE_BATCHED>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+  if (e != cudaSuccess) return e;
+  const long long tiles = (long long)p.m_tiles * p.n_tiles * batch;
+  const int grid = tiles < gb_num_sms() ? (int)tiles : gb_num_sms();
+  igemm_bf16_tc_kernel<BN, MODE_BATCHED><<<grid, 192, Cf::SMEM, st>>>(tma, tmb, p);
   return cudaGetLastError();
 }
 
@@ -375,6 +454,20 @@ cudaError_t launch_igemm_bf16(const gbconv_desc_s& d, int block_n, const void* x
     case 64: return launch_bn<64>(d, x, wpack, bias, res, y, err, wait_ns, st);
     case 128: return launch_bn<128>(d, x, wpack, bias, res, y, err, wait_ns, st);
     case 256: return launch_bn<256>(d, x, wpack, bias, res, y, err, wait_ns, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_batched_gemm_tc(int batch, int M, int N, int Kred, const void* A,
+                                   const void* B, float* out, int ab_type, int block_n, int* err,
+                                   unsigned long long wait_ns, cudaStream_t st) {
+  if (N % 8 || Kred % 8 || batch <= 0 || M <= 0) return cudaErrorInvalidValue;
+  switch (block_n) {
+    case 64: return launch_batched_bn<64>(batch, M, N, Kred, A, B, out, ab_type, err, wait_ns, st);
+    case 128:
+      return launch_batched_bn<128>(batch, M, N, Kred, A, B, out, ab_type, err, wait_ns, st);
+    case 256:
+      return launch_batched_bn<256>(batch, M, N, Kred, A, B, out, ab_type, err, wait_ns, st);
     default: return cudaErrorInvalidValue;
   }
 }

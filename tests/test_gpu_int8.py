@@ -1,0 +1,76 @@
+"""Bit-exact parity of the int8 implicit GEMM (mma.sync s8, exact int32
+accumulate, fp32 requant, ReLU) with the oracle."""
+import numpy as np
+import pytest
+
+from oracle import lib as ol
+from tests.gpu_util import need_gpu, nchw_to_nhwc, nhwc_to_nchw
+
+pytestmark = pytest.mark.gpu
+INT8_MMA = 7
+
+
+def _run(torch, N, C, H, W, K, R, stride, pad, relu=True, bias=True, seed=0, algo=INT8_MMA):
+    from cnn_convolution_gemm_gb300 import binding as B
+    from cnn_convolution_gemm_gb300 import synth
+    from cnn_convolution_gemm_gb300.layer import ConvLayer
+    dev = torch.device("cuda:0")
+    g = np.random.default_rng(seed)
+    x = synth.int8_uniform((N, H, W, C), seed)
+    w = synth.int8_uniform((K, R, R, C), seed + 1)
+    scale = synth.uniform((K,), 1e-4, 1e-3, seed + 2)
+    b = synth.int32_uniform((K,), seed + 3) if bias else None
+    sd = torch.from_numpy(scale).to(dev)
+    layer = ConvLayer(N, C, H, W, K, R, R, stride, pad, dtype=B.CONV_INT8,
+                      act=B.CONV_ACT_RELU if relu else B.CONV_ACT_NONE, scale=sd)
+    layer.prepack(torch.from_numpy(w).to(dev), algo)
+    y = layer(torch.from_numpy(x).to(dev), None if b is None else torch.from_numpy(b).to(dev))
+    B.conv_sync_status(torch.cuda.current_stream().cuda_stream)
+    ref = ol.conv2d_i8(nhwc_to_nchw(x), nhwc_to_nchw(w), b, scale, stride=stride, pad=pad,
+                       relu=relu)
+    del g
+    return y.cpu().numpy(), nchw_to_nhwc(ref)
+
+
+@pytest.mark.parametrize("C,HW", [(64, 56), (128, 28), (256, 14), (512, 7)])
+def test_int8_resnet_stage_shapes_full_batch(C, HW):
+    """The four ResNet-50 stage 3x3 layers at batch 32, every output compared."""
+    torch = need_gpu()
+    y, ref = _run(torch, 32, C, HW, HW, C, 3, 1, 1, seed=C)
+    assert np.array_equal(y, ref), int((y != ref).sum())
+
+
+@pytest.mark.parametrize("case", [
+    # N, C, H, W, K, R, stride, pad, relu, bias
+    (2, 16, 9, 7, 48, 3, 1, 1, True, True),      # C < 64 block, ragged K tile
+    (3, 32, 10, 10, 16, 3, 2, 1, False, True),   # stride 2, no ReLU
+    (2, 96, 6, 6, 80, 1, 1, 0, True, False),     # 1x1, no bias, C not a 64 multiple
+    (1, 64, 5, 5, 256, 3, 1, 2, True, True),     # pad 2 (many fully padded taps)
+])
+def test_int8_edge_cases(case):
+    torch = need_gpu()
+    N, C, H, W, K, R, st, pad, relu, bias = case
+    y, ref = _run(torch, N, C, H, W, K, R, st, pad, relu, bias, seed=N * C)
+    assert np.array_equal(y, ref)
+
+
+def test_int8_saturation_extremes():
+    """All +-127 inputs drive the accumulator to its largest magnitude and the
+    requant into saturation on both sides."""
+    torch = need_gpu()
+    from cnn_convolution_gemm_gb300 import binding as B
+    from cnn_convolution_gemm_gb300.layer import ConvLayer
+    dev = torch.device("cuda:0")
+    N, C, H, K = 1, 512, 7, 32
+    x = np.full((N, H, H, C), 127, np.int8)
+    w = np.where(np.arange(K)[:, None, None, None] % 2 == 0, 127, -127).astype(np.int8) * np.ones(
+        (K, 3, 3, C), np.int8)
+    scale = np.full(K, 1e-3, np.float32)
+    layer = ConvLayer(N, C, H, H, K, 3, 3, 1, 1, dtype=B.CONV_INT8,
+                      scale=torch.from_numpy(scale).to(dev))
+    layer.prepack(torch.from_numpy(w).to(dev), INT8_MMA)
+    y = layer(torch.from_numpy(x).to(dev))
+    B.conv_sync_status(torch.cuda.current_stream().cuda_stream)
+    ref = ol.conv2d_i8(nhwc_to_nchw(x), nhwc_to_nchw(w), None, scale, pad=1, relu=False)
+    assert np.array_equal(y.cpu().numpy(), nchw_to_nhwc(ref))
+    assert (ref == 127).any() and (ref == -128).any()
