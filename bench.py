@@ -1,22 +1,28 @@
 #!/usr/bin/env python3
-"""Benchmark: the ResNet 3x3 conv layer (N=32, C=K=256, 56x56, stride 1, pad 1,
-bf16 NHWC, fp32 bias) through the gbconv C ABI on one GB300 per rank.
+"""Benchmark of the gbconv C ABI on GB300, one JSON line per run (rank 0).
 
-A step is one forward pass of the layer over the batch: the algorithm Fast-Run
-picked for the shape (selection runs once before timing; execution looks the
-map up), with the bias fused into its epilogue.  The input is already
-resident in HBM when timing starts; the L2 cache (129 MB; the layer's tensors
-total 104 MB) is flushed between steps by writing a 256 MB buffer, outside the
-per-step CUDA-event window.
+Default workload (the headline): the ResNet 3x3 conv layer, N=32, C=K=256,
+56x56, stride 1, pad 1, bf16 NHWC, fp32 bias.  A step is one forward pass of
+the layer over the batch with the algorithm Fast-Run picked for the shape
+(selection runs once before timing; execution looks the map up).
 
-Prints ONE JSON line (rank 0).  `value` is direct-convolution-equivalent
-TFLOP/s over all ranks; `e2e` is the same metric through the same C-ABI call
-with the input copied from pinned host memory and the output copied back
-inside each timed step; `cpu_baseline` is the fp64 oracle on this host's
-cores over a bounded sample of the same layer.
+Other workloads (--workload):
+  single_layer  1 x 32 x 28 x 28 fp32 NCHW, 32 filters 3x3: boundary
+                conversion to NHWC bf16, conv, conversion back
+  mbv2_block    MobileNetV2 inverted residual, N=64, 56x56: 1x1 24->144 +
+                ReLU6, depthwise 3x3 + ReLU6, 1x1 144->24
+  int8_stages   int8 3x3 convs at the four ResNet-50 stage shapes, N=32
+  resnet50      full ResNet-50 forward, batch 64, 224x224x3 input
 
---impl reference times the oracle itself (the reference arm of this metric)
-on a bounded sample per step.
+Timing: W >= 3 untimed warm-up steps, then K steps; before every step the L2
+(129 MB) is flushed by writing a 256 MB buffer, outside the CUDA-event window
+that brackets the step's launches on the launching stream.  `value` is the
+workload's metric over all ranks; `e2e` is the same metric through the same
+calls with the step's input copied from pinned host memory and its output
+copied back inside the timed region; `cpu_baseline` is the fp64 / exact-int8
+oracle on this host's cores over a bounded sample of the same workload.
+
+--impl reference times the oracle itself (the reference arm of this metric).
 """
 from __future__ import annotations
 
@@ -33,40 +39,44 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOAD = dict(N=32, C=256, H=56, W=56, K=256, R=3, S=3, stride=1, pad=1)
-WORKLOAD_NAME = "resnet_conv3x3_c256_k256_56x56_n32_bf16_nhwc"
-METRIC = "conv TFLOP/s (direct-equivalent), ResNet 3x3 256->256 @56x56, batch 32"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 
-# DRAM traffic of one launch of each kernel, from an ncu capture of this
-# workload (profiles/igemm_tc_conv3x3_256_56x56_n32.md), keyed by the source
-# file's hash at capture time: a changed kernel reports null.
+# DRAM traffic of one launch (read + write) from an ncu capture of the named
+# kernel on this workload, keyed by the kernel source's hash at capture time:
+# a changed source reports null.  Captures are summarised under profiles/.
 NCU_TRAFFIC = {
-    # algo name: (dram bytes read + written per launch, sha256[:16] of the kernel source)
-    "igemm_tc_n256": (52_592_640 + 3_997_696, "686421d5724ef69b"),
+    # (workload, kernel): (bytes per launch, sha256[:16] of the source file)
 }
+KERNEL_SOURCE = {"igemm_tc_n64": "k_igemm.cu", "igemm_tc_n128": "k_igemm.cu",
+                 "igemm_tc_n256": "k_igemm.cu", "winograd_f2x2_3x3": "k_winograd.cu",
+                 "winograd_f6x6_3x3": "k_winograd.cu", "direct": "k_direct.cu",
+                 "depthwise3x3": "k_dwconv.cu", "int8_igemm_mma": "k_int8.cu"}
 
 
-def _src_hash(name: str) -> str:
+def src_hash(name: str) -> str:
     p = os.path.join(ROOT, "cnn_convolution_gemm_gb300", "csrc", name)
     with open(p, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-KERNEL_SOURCE = {"igemm_tc_n64": "k_igemm.cu", "igemm_tc_n128": "k_igemm.cu",
-                 "igemm_tc_n256": "k_igemm.cu", "winograd_f2x2_3x3": "k_winograd.cu",
-                 "winograd_f6x6_3x3": "k_winograd.cu", "direct": "k_direct.cu"}
-
-
 def load_peaks():
-    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
-        with open(p) as f:
-            d = json.load(f)
-        return d, "measured"
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
     except (OSError, ValueError):
         return dict(FALLBACK_PEAKS), "fallback"
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def threads():
+    return int(os.environ.get("OMP_NUM_THREADS", cpu_cores()))
 
 
 class ClockSampler:
@@ -76,11 +86,8 @@ class ClockSampler:
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int, period_ms: int = 100):
-        self.samples = []
-        self.proc = None
-        self.gpu = gpu_index
-        self.period = period_ms
-        self.t = None
+        self.samples, self.proc, self.t = [], None, None
+        self.gpu, self.period = gpu_index, period_ms
 
     def start(self):
         try:
@@ -89,7 +96,6 @@ class ClockSampler:
                  "--format=csv,noheader,nounits", f"-lms={self.period}"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
-            self.proc = None
             return
         self.t = threading.Thread(target=self._read, daemon=True)
         self.t.start()
@@ -130,67 +136,471 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(win)}
 
 
-def dist_setup():
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return world, rank, local
+# ---------------------------------------------------------------------------
+# workloads: each builds device state and exposes its launch groups
+
+class Workload:
+    name = ""
+    metric = ""
+    unit = "TFLOP/s"
+    dtype = "bf16"
+    algo_name = ""
+    fastrun_ms = None
+
+    def setup(self, dev, rank, args):
+        raise NotImplementedError
+
+    def groups(self):
+        """[(label, fn, work, bytes, bound)] launched in order each step; work is the
+        group's direct-equivalent FLOPs (int8 ops), bytes its algorithmic traffic."""
+        raise NotImplementedError
+
+    def value(self, ms):
+        return sum(g[2] for g in self.groups()) / (ms * 1e-3) / 1e12
+
+    def kernel_work(self, label, work):
+        return work
+
+    def h2d(self):
+        raise NotImplementedError
+
+    def d2h(self):
+        raise NotImplementedError
+
+    def cpu_baseline(self, args):
+        raise NotImplementedError
 
 
-def cpu_cores() -> int:
+def fastrun_pick(layer, sh, args, B):
+    """The forced algorithm (--algo NAME) if it applies to the layer, else Fast-Run's pick."""
+    if args.algo != "fastrun":
+        info = {B.conv_algo_info(layer.desc, i)[1]: (i, B.conv_algo_info(layer.desc, i)[2])
+                for i in range(B.CONV_ALGO_COUNT)}
+        if args.algo in info and info[args.algo][1]:
+            return info[args.algo][0], None
     try:
-        return len(os.sched_getaffinity(0))
-    except AttributeError:
-        return os.cpu_count() or 1
+        return B.conv_fastrun_lookup(layer.desc), None
+    except B.GbconvError:
+        a, times = layer.fastrun(sh)
+        return a, {B.conv_algo_info(layer.desc, i)[1]: round(t, 4)
+                   for i, t in enumerate(times) if t >= 0}
 
 
-def oracle_sample(images: int, seed: int = 0):
-    """Time the fp64 oracle on `images` images of the layer (all 256 output
-    channels).  Returns (seconds, flops)."""
+def oracle_resnet_layer(images, seed=0):
     import numpy as np
     from cnn_convolution_gemm_gb300 import synth
     from oracle import lib as ol
-    w = WORKLOAD
-    x, wt, b = synth.resnet_3x3_layer(seed=seed, N=images)
+    x, w, b = synth.resnet_3x3_layer(seed=seed, N=images)
     xn = np.ascontiguousarray(x.transpose(0, 3, 1, 2), dtype=np.float64)
-    wn = np.ascontiguousarray(wt.transpose(0, 3, 1, 2), dtype=np.float64)
+    wn = np.ascontiguousarray(w.transpose(0, 3, 1, 2), dtype=np.float64)
     t0 = time.perf_counter()
-    ol.conv2d_f64(xn, wn, b.astype(np.float64), stride=w["stride"], pad=w["pad"])
+    ol.conv2d_f64(xn, wn, b.astype(np.float64), stride=1, pad=1)
     dt = time.perf_counter() - t0
-    flops = 2 * images * 56 * 56 * w["K"] * w["C"] * 9
-    return dt, flops
+    return dt, 2 * images * 56 * 56 * 256 * 256 * 9, images
+
+
+class ResNetLayer(Workload):
+    name = "resnet_conv3x3_c256_k256_56x56_n32_bf16_nhwc"
+    metric = "conv TFLOP/s (direct-equivalent), ResNet 3x3 256->256 @56x56, batch 32"
+
+    def setup(self, dev, rank, args):
+        import torch
+        from cnn_convolution_gemm_gb300 import binding as B
+        from cnn_convolution_gemm_gb300 import synth
+        from cnn_convolution_gemm_gb300.layer import ConvLayer
+        from cnn_convolution_gemm_gb300.workload import ConvShape
+        self.shape = ConvShape(32, 256, 56, 56, 256, 3, 3, 1, 1)
+        x, w, b = synth.resnet_3x3_layer(seed=rank)
+        self.xh = torch.from_numpy(x).to(torch.bfloat16).pin_memory()
+        self.x = self.xh.to(dev)
+        self.b = torch.from_numpy(b).to(dev)
+        self.layer = ConvLayer(32, 256, 56, 56, 256, 3, 3, 1, 1)
+        self.sh = torch.cuda.current_stream().cuda_stream
+        a, self.fastrun_ms = fastrun_pick(self.layer, self.sh, args, B)
+        self.layer.prepack(torch.from_numpy(w).to(torch.bfloat16).to(dev), a)
+        self.algo_name = B.conv_algo_info(self.layer.desc, a)[1]
+        self.y = torch.empty(self.layer.output_shape, dtype=torch.bfloat16, device=dev)
+        self.yh = torch.empty(self.layer.output_shape, dtype=torch.bfloat16).pin_memory()
+
+    def groups(self):
+        return [(self.algo_name, lambda: self.layer.forward(self.x, self.b, out=self.y,
+                                                            stream=self.sh),
+                 self.shape.flops(), self.shape.traffic_bytes(2, 4), "tensor")]
+
+    def kernel_work(self, label, work):
+        if label.startswith("winograd"):  # the tensor cores run the GEMM FLOPs only
+            return self.shape.winograd_gemm_flops(2 if "f2x2" in label else 6)
+        return work
+
+    def h2d(self):
+        return [(self.xh, self.x)]
+
+    def d2h(self):
+        return [(self.y, self.yh)]
+
+    def cpu_baseline(self, args):
+        dt, f, n = oracle_resnet_layer(args.cpu_images)
+        return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": threads(), "kind": "oracle",
+                "sample": f"{n} of 32 images, all 256 output channels ({f / 1e9:.1f} GFLOP)",
+                "seconds": round(dt, 3)}
+
+
+class SingleLayer(Workload):
+    name = "single_conv3x3_c32_k32_28x28_n1_f32_nchw"
+    metric = "conv TFLOP/s (direct-equivalent), 1x32x28x28 fp32 NCHW, 32 filters 3x3"
+
+    def setup(self, dev, rank, args):
+        import numpy as np
+        import torch
+        from cnn_convolution_gemm_gb300 import binding as B
+        from cnn_convolution_gemm_gb300 import synth
+        from cnn_convolution_gemm_gb300.layer import ConvLayer
+        from cnn_convolution_gemm_gb300.workload import ConvShape
+        self.B = B
+        self.shape = ConvShape(1, 32, 28, 28, 32, 3, 3, 1, 1)
+        x, w, b = synth.single_layer_nchw(seed=rank)
+        self.xh = torch.from_numpy(x).pin_memory()
+        self.x = self.xh.to(dev)
+        self.b = torch.from_numpy(b).to(dev)
+        self.sh = sh = torch.cuda.current_stream().cuda_stream
+        # weights to NHWC bf16 through the same boundary kernel (one-time)
+        wd = torch.from_numpy(np.ascontiguousarray(w.transpose(0, 2, 3, 1))).to(dev)
+        wn = torch.empty((32, 3, 3, 32), dtype=torch.bfloat16, device=dev)
+        B.conv_nchw_f32_to_nhwc_bf16(wd.data_ptr(), wn.data_ptr(), 32 * 9, 32, 1, 1, 32, sh)
+        self.layer = ConvLayer(1, 32, 28, 28, 32, 3, 3, 1, 1)
+        a, self.fastrun_ms = fastrun_pick(self.layer, sh, args, B)
+        self.layer.prepack(wn, a)
+        self.algo_name = B.conv_algo_info(self.layer.desc, a)[1]
+        self.xn = torch.empty((1, 28, 28, 32), dtype=torch.bfloat16, device=dev)
+        self.yn = torch.empty((1, 28, 28, 32), dtype=torch.bfloat16, device=dev)
+        self.y = torch.empty((1, 32, 28, 28), dtype=torch.float32, device=dev)
+        self.yh = torch.empty((1, 32, 28, 28), dtype=torch.float32).pin_memory()
+
+    def groups(self):
+        B, sh = self.B, self.sh
+        return [
+            ("nchw_f32_to_nhwc_bf16", lambda: B.conv_nchw_f32_to_nhwc_bf16(
+                self.x.data_ptr(), self.xn.data_ptr(), 1, 32, 28, 28, 32, sh), 0,
+             32 * 28 * 28 * 6, "hbm"),
+            (self.algo_name, lambda: self.layer.forward(self.xn, self.b, out=self.yn, stream=sh),
+             self.shape.flops(), self.shape.traffic_bytes(2, 4), "tensor"),
+            ("nhwc_bf16_to_nchw_f32", lambda: B.conv_nhwc_bf16_to_nchw_f32(
+                self.yn.data_ptr(), self.y.data_ptr(), 1, 32, 28, 28, 32, sh), 0,
+             32 * 28 * 28 * 6, "hbm"),
+        ]
+
+    def h2d(self):
+        return [(self.xh, self.x)]
+
+    def d2h(self):
+        return [(self.y, self.yh)]
+
+    def cpu_baseline(self, args):
+        import numpy as np
+        from cnn_convolution_gemm_gb300 import synth
+        from oracle import lib as ol
+        x, w, b = synth.single_layer_nchw()
+        reps = 200
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            ol.conv2d_f64(x.astype(np.float64), w.astype(np.float64), b.astype(np.float64), pad=1)
+        dt = time.perf_counter() - t0
+        f = self.shape.flops() * reps
+        return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": threads(), "kind": "oracle",
+                "sample": f"the whole layer, {reps} times", "seconds": round(dt, 3)}
+
+
+class MBv2Block(Workload):
+    name = "mbv2_inverted_residual_24_144_56x56_n64_bf16_nhwc"
+    metric = "conv TFLOP/s (direct-equivalent), MobileNetV2 block 24->144->24 @56x56, batch 64"
+
+    def setup(self, dev, rank, args):
+        import torch
+        from cnn_convolution_gemm_gb300 import binding as B
+        from cnn_convolution_gemm_gb300 import synth
+        from cnn_convolution_gemm_gb300.layer import ConvLayer
+        from cnn_convolution_gemm_gb300.workload import ConvShape
+        d = synth.mbv2_block(seed=rank)
+        self.sh = sh = torch.cuda.current_stream().cuda_stream
+        N, H, W, C, E = 64, 56, 56, 24, 144
+        self.shapes = [ConvShape(N, C, H, W, E, 1, 1), ConvShape(N, E, H, W, E, 3, 3, 1, 1, 1, E),
+                       ConvShape(N, E, H, W, C, 1, 1)]
+        self.layers = [ConvLayer(N, C, H, W, E, 1, 1, act=B.CONV_ACT_RELU6),
+                       ConvLayer(N, E, H, W, E, 3, 3, 1, 1, 1, E, act=B.CONV_ACT_RELU6),
+                       ConvLayer(N, E, H, W, C, 1, 1)]
+        ws = [d["w_expand"], d["w_dw"], d["w_project"]]
+        bs = [d["b_expand"], d["b_dw"], d["b_project"]]
+        self.fastrun_ms, self.algo_names = {}, []
+        for i, (layer, w) in enumerate(zip(self.layers, ws)):
+            a, fr = fastrun_pick(layer, sh, args, B)
+            if fr:
+                self.fastrun_ms[f"layer{i}"] = fr
+            layer.prepack(torch.from_numpy(w).to(torch.bfloat16).to(dev), a)
+            self.algo_names.append(B.conv_algo_info(layer.desc, a)[1])
+        self.b = [torch.from_numpy(b).to(dev) for b in bs]
+        self.xh = torch.from_numpy(d["x"]).to(torch.bfloat16).pin_memory()
+        self.x = self.xh.to(dev)
+        self.t1 = torch.empty((N, H, W, E), dtype=torch.bfloat16, device=dev)
+        self.t2 = torch.empty((N, H, W, E), dtype=torch.bfloat16, device=dev)
+        self.y = torch.empty((N, H, W, C), dtype=torch.bfloat16, device=dev)
+        self.yh = torch.empty((N, H, W, C), dtype=torch.bfloat16).pin_memory()
+        self.algo_name = "+".join(self.algo_names)
+
+    def groups(self):
+        ins, outs = [self.x, self.t1, self.t2], [self.t1, self.t2, self.y]
+        return [(f"{['expand', 'depthwise', 'project'][i]}:{self.algo_names[i]}",
+                 (lambda l=layer, a=ins[i], o=outs[i], b=self.b[i]:
+                  l.forward(a, b, out=o, stream=self.sh)),
+                 sp.flops(), sp.traffic_bytes(2, 4), "hbm")
+                for i, (layer, sp) in enumerate(zip(self.layers, self.shapes))]
+
+    def h2d(self):
+        return [(self.xh, self.x)]
+
+    def d2h(self):
+        return [(self.y, self.yh)]
+
+    def cpu_baseline(self, args):
+        import numpy as np
+        from cnn_convolution_gemm_gb300 import synth
+        from oracle import lib as ol
+        n = 8
+        d = synth.mbv2_block(seed=0, N=n)
+        x = d["x"].transpose(0, 3, 1, 2).astype(np.float64)
+        t0 = time.perf_counter()
+        t1 = ol.conv2d_f64(x, d["w_expand"].transpose(0, 3, 1, 2), d["b_expand"], act=2)
+        t2 = ol.conv2d_f64(t1, d["w_dw"].transpose(0, 3, 1, 2), d["b_dw"], pad=1, groups=144,
+                           act=2)
+        ol.conv2d_f64(t2, d["w_project"].transpose(0, 3, 1, 2), d["b_project"])
+        dt = time.perf_counter() - t0
+        f = sum(s.flops() for s in self.shapes) * n // 64
+        return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": threads(), "kind": "oracle",
+                "sample": f"{n} of 64 images through the three layers", "seconds": round(dt, 3)}
+
+
+class Int8Stages(Workload):
+    name = "int8_conv3x3_resnet50_stages_n32"
+    metric = "int8 conv TOPS (direct-equivalent), ResNet-50 stage 3x3 layers, batch 32"
+    unit = "TOPS"
+    dtype = "int8 (int32 accumulate)"
+
+    def setup(self, dev, rank, args):
+        import torch
+        from cnn_convolution_gemm_gb300 import binding as B
+        from cnn_convolution_gemm_gb300 import synth
+        from cnn_convolution_gemm_gb300.layer import ConvLayer
+        from cnn_convolution_gemm_gb300.workload import ConvShape
+        self.sh = sh = torch.cuda.current_stream().cuda_stream
+        self.items, self.fastrun_ms, names = [], {}, []
+        for C, HW in synth.INT8_STAGES:
+            x, w, scale, bias = synth.int8_layer(seed=rank * 10 + C, N=32, C=C, H=HW, W=HW)
+            sd = torch.from_numpy(scale).to(dev)
+            layer = ConvLayer(32, C, HW, HW, C, 3, 3, 1, 1, dtype=B.CONV_INT8,
+                              act=B.CONV_ACT_RELU, scale=sd)
+            a, fr = fastrun_pick(layer, sh, args, B)
+            if fr:
+                self.fastrun_ms[f"{C}@{HW}"] = fr
+            layer.prepack(torch.from_numpy(w).to(dev), a)
+            names.append(B.conv_algo_info(layer.desc, a)[1])
+            xh = torch.from_numpy(x).pin_memory()
+            y = torch.empty(layer.output_shape, dtype=torch.int8, device=dev)
+            self.items.append(dict(layer=layer, xh=xh, x=xh.to(dev),
+                                   b=torch.from_numpy(bias).to(dev), s=sd, y=y,
+                                   yh=torch.empty(y.shape, dtype=torch.int8).pin_memory(),
+                                   shape=ConvShape(32, C, HW, HW, C, 3, 3, 1, 1),
+                                   name=f"{C}@{HW}", algo=names[-1]))
+        self.algo_name = "+".join(sorted(set(names)))
+
+    def groups(self):
+        return [(f"{it['name']}:{it['algo']}",
+                 (lambda it=it: it["layer"].forward(it["x"], it["b"], out=it["y"], stream=self.sh)),
+                 it["shape"].flops(), it["shape"].traffic_bytes(1, 4, out_bytes=1), "tensor")
+                for it in self.items]
+
+    def h2d(self):
+        return [(it["xh"], it["x"]) for it in self.items]
+
+    def d2h(self):
+        return [(it["y"], it["yh"]) for it in self.items]
+
+    def cpu_baseline(self, args):
+        from cnn_convolution_gemm_gb300 import synth
+        from oracle import lib as ol
+        t0 = time.perf_counter()
+        ops = 0
+        for C, HW in synth.INT8_STAGES:
+            x, w, scale, bias = synth.int8_layer(seed=C, N=4, C=C, H=HW, W=HW)
+            ol.conv2d_i8(x.transpose(0, 3, 1, 2), w.transpose(0, 3, 1, 2), bias, scale, pad=1)
+            ops += 2 * 4 * HW * HW * C * C * 9
+        dt = time.perf_counter() - t0
+        return {"value": ops / dt / 1e12, "unit": "TOPS", "cores": threads(), "kind": "oracle",
+                "sample": "4 of 32 images of each of the four layers", "seconds": round(dt, 3)}
+
+
+class ResNet50W(Workload):
+    name = "resnet50_forward_n64_224x224_bf16_nhwc"
+    metric = "ResNet-50 forward images/s (batch 64, 224x224, bf16)"
+    unit = "images/s"
+
+    def setup(self, dev, rank, args):
+        import torch
+        from cnn_convolution_gemm_gb300 import synth
+        from cnn_convolution_gemm_gb300.resnet50 import ResNet50
+        self.N = 64
+        self.net = ResNet50(self.N, dev, seed=rank,
+                            algo="fastrun" if args.algo == "fastrun" else "auto")
+        x = synth.normal((self.N, 3, 224, 224), 1.0, 100 + rank)
+        self.xh = torch.from_numpy(x).pin_memory()
+        self.x = self.xh.to(dev)
+        self.out = self.net.forward(self.x)
+        self.yh = torch.empty((self.N, 1000), dtype=torch.bfloat16).pin_memory()
+        self.algo_name = "Fast-Run per layer"
+        counts = {}
+        for a in self.net.algos.values():
+            counts[a] = counts.get(a, 0) + 1
+        self.algo_counts = counts
+
+    def groups(self):
+        def run():
+            self.out = self.net.forward(self.x)
+        return [("resnet50_forward", run, self.net.flops(), 0, "tensor")]
+
+    def layer_breakdown(self, reps=5):
+        """Per-layer device time from CUDA events between launch groups (median of
+        `reps` forwards), with each conv's direct-equivalent TFLOP/s and algorithm."""
+        import torch
+        stream = torch.cuda.current_stream()
+        names, runs = [], []
+        for _ in range(reps):
+            evs = []
+
+            def timer(name):
+                e = torch.cuda.Event(enable_timing=True)
+                e.record(stream)
+                evs.append((name, e))
+            self.net.forward(self.x, timer=timer)
+            end = torch.cuda.Event(enable_timing=True)
+            end.record(stream)
+            evs.append(("end", end))
+            torch.cuda.synchronize()
+            names = [n for n, _ in evs[:-1]]
+            runs.append([a[1].elapsed_time(b[1]) for a, b in zip(evs, evs[1:])])
+        med = [statistics.median(r[i] for r in runs) for i in range(len(names))]
+        flops = {sp.name: sp.shape(self.N).flops() for sp in self.net.specs}
+        out = {}
+        for n, ms in zip(names, med):
+            d = {"ms": round(ms, 5)}
+            if n in flops:
+                d["tflops"] = round(flops[n] / (ms * 1e-3) / 1e12, 1)
+                d["algo"] = self.net.algos[n]
+            out[n] = d
+        return out
+
+    def value(self, ms):
+        return self.N / (ms * 1e-3)
+
+    def h2d(self):
+        return [(self.xh, self.x)]
+
+    def d2h(self):
+        return [(self.out, self.yh)]
+
+    def cpu_baseline(self, args):
+        import numpy as np
+        from cnn_convolution_gemm_gb300 import synth
+        from cnn_convolution_gemm_gb300.resnet50 import conv_specs
+        from oracle import lib as ol
+        specs = conv_specs()
+        t0 = time.perf_counter()
+        flops = 0
+        x = synth.normal((1, 3, 224, 224), 1.0, 100).astype(np.float64)
+        t = {"input": np.concatenate([x, np.zeros((1, 5, 224, 224))], axis=1)}
+        for i, sp in enumerate(specs):
+            if sp.name == "fc":
+                t["pool5"] = ol.global_avgpool(t[specs[-2].dst]).reshape(1, 2048, 1, 1)
+            w = synth.kaiming((sp.K, sp.R, sp.R, sp.true_C or sp.C), 7 * i)
+            if sp.true_C:
+                w = np.concatenate([w, np.zeros((sp.K, sp.R, sp.R, sp.C - sp.true_C))], axis=3)
+            b = synth.uniform((sp.K,), -0.1, 0.1, 7 * i + 1)
+            t[sp.dst] = ol.conv2d_f64(t[sp.src], w.transpose(0, 3, 1, 2), b, stride=sp.stride,
+                                      pad=sp.pad, act=1 if sp.act else 0,
+                                      residual=t[sp.residual] if sp.residual else None)
+            flops += sp.shape(1).flops()
+            if sp.name == "conv1":
+                t["pool1"] = ol.maxpool2d(t["conv1"], 3, 2, 1)
+        dt = time.perf_counter() - t0
+        return {"value": 1 / dt, "unit": "images/s", "cores": threads(), "kind": "oracle",
+                "sample": f"1 of 64 images through all 53 convs, pools and the FC "
+                          f"({flops / 1e9:.2f} GFLOP)", "seconds": round(dt, 3)}
+
+
+WORKLOADS = {"resnet3x3": ResNetLayer, "single_layer": SingleLayer, "mbv2_block": MBv2Block,
+             "int8_stages": Int8Stages, "resnet50": ResNet50W}
+
+
+def dist_setup():
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
 
 
 def run_reference(args):
-    """Reference arm: the fp64 oracle on the host cores, one bounded sample
-    (one image of the layer) per step."""
+    """Reference arm: the oracle on the host cores, one bounded sample per step."""
     world, rank, _ = dist_setup()
     if rank != 0:
         return 0
     os.environ.setdefault("OMP_NUM_THREADS", str(cpu_cores()))
     from oracle import lib as ol
     ol.build()
+    wl = WORKLOADS[args.workload]()
+    if args.workload == "resnet3x3":
+        def sample():
+            dt, f, _ = oracle_resnet_layer(1)
+            return dt, f / 1e12
+        desc = "1 of 32 images (all 256 output channels) per step"
+    else:
+        def sample():
+            r = wl.cpu_baseline(args)
+            return r["seconds"], r["value"] * r["seconds"]
+        desc = "the workload's bounded CPU sample per step"
     for _ in range(args.warmup):
-        oracle_sample(1)
-    times, flops = [], 0
-    for i in range(args.steps):
-        dt, f = oracle_sample(1, seed=i)
-        times.append(dt)
-        flops += f
-    total = sum(times)
-    v = flops / total / 1e12
-    cores = int(os.environ["OMP_NUM_THREADS"])
+        sample()
+    tot_t = tot_w = 0.0
+    for _ in range(args.steps):
+        dt, w = sample()
+        tot_t += dt
+        tot_w += w
+    v = tot_w / tot_t
     line = {
-        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "impl": "reference", "metric": wl.metric, "value": v, "unit": wl.unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOAD_NAME, "sample": "1 image per step"},
-        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": "1 of 32 images (all 256 output channels) per step"},
-        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "data": "synthetic", "config": {"workload": wl.name, "sample": desc},
+        "cpu_baseline": {"value": v, "unit": wl.unit, "cores": threads(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": v, "unit": wl.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def launches_for(algo_name):
+    """Kernels of this library one conv_fwd call launches."""
+    if algo_name.startswith("winograd"):
+        return None  # 3 per chunk; counted by the caller
+    return 1
+
+
+def count_launches(wl, groups):
+    if isinstance(wl, ResNet50W):
+        return len(wl.net.algos) + 3  # 54 convs + layout conversion, max pool, avg pool
+    if isinstance(wl, ResNetLayer) and wl.algo_name.startswith("winograd"):
+        from cnn_convolution_gemm_gb300 import binding as B
+        ws = B.conv_workspace_size(wl.layer.desc, wl.layer.algo)
+        m = 2 if "f2x2" in wl.algo_name else 6
+        per_img = ((56 + m - 1) // m) ** 2 * (m + 2) ** 2 * (256 * 2 + 256 * 4)
+        nb = max(1, min(32, ws // per_img))
+        return 3 * -(-32 // nb)
+    return len(groups)
 
 
 def main():
@@ -199,6 +609,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gbconv", choices=["gbconv", "reference"])
+    ap.add_argument("--workload", default="resnet3x3", choices=sorted(WORKLOADS))
     ap.add_argument("--algo", default="fastrun",
                     help="fastrun (default) or an algorithm name to force")
     ap.add_argument("--fastrun-file", default=None,
@@ -212,7 +623,6 @@ def main():
         return run_reference(args)
 
     world, rank, local = dist_setup()
-    import numpy as np
     import torch
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU")
@@ -225,46 +635,23 @@ def main():
         pg = dist
 
     from cnn_convolution_gemm_gb300 import binding as B
-    from cnn_convolution_gemm_gb300 import synth
-    from cnn_convolution_gemm_gb300.layer import ConvLayer
-    from cnn_convolution_gemm_gb300.workload import ConvShape
     B.load_library()
-
-    w = WORKLOAD
-    shape = ConvShape(w["N"], w["C"], w["H"], w["W"], w["K"], w["R"], w["S"], w["stride"],
-                      w["pad"])
-    x, wt, b = synth.resnet_3x3_layer(seed=rank)
-    xt = torch.from_numpy(x).to(torch.bfloat16)
-    xd = xt.to(dev)
-    wd = torch.from_numpy(wt).to(torch.bfloat16).to(dev)
-    bd = torch.from_numpy(b).to(dev)
-    layer = ConvLayer(w["N"], w["C"], w["H"], w["W"], w["K"], w["R"], w["S"], w["stride"],
-                      w["pad"])
+    had_map = bool(args.fastrun_file and os.path.exists(args.fastrun_file))
+    if had_map:
+        B.conv_fastrun_load(args.fastrun_file)
+    wl = WORKLOADS[args.workload]()
+    wl.setup(dev, rank, args)
+    if args.fastrun_file and not had_map and rank == 0:
+        B.conv_fastrun_save(args.fastrun_file)
+    groups = wl.groups()
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
-    fastrun_ms = None
-    if args.algo == "fastrun":
-        if args.fastrun_file and os.path.exists(args.fastrun_file):
-            B.conv_fastrun_load(args.fastrun_file)
-            algo = B.conv_fastrun_lookup(layer.desc)
-        else:
-            algo, times = layer.fastrun(sh)
-            fastrun_ms = {B.conv_algo_info(layer.desc, i)[1]: round(t, 4)
-                          for i, t in enumerate(times) if t >= 0}
-            if args.fastrun_file:
-                B.conv_fastrun_save(args.fastrun_file)
-    else:
-        names = {B.conv_algo_info(layer.desc, i)[1]: i for i in range(B.CONV_ALGO_COUNT)}
-        algo = names[args.algo]
-    layer.prepack(wd, algo)
-    algo_name = B.conv_algo_info(layer.desc, algo)[1]
-    y = torch.empty(layer.output_shape, dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def step():
-        layer.forward(xd, bd, out=y, stream=sh)
+        for g in groups:
+            g[1]()
 
-    # warm-up
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -273,7 +660,8 @@ def main():
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    ng = len(groups)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(ng + 1)]
           for _ in range(args.steps)]
     if pg:
         pg.barrier()
@@ -282,30 +670,34 @@ def main():
     for i in range(args.steps):
         flush.zero_()
         ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
+        for j, g in enumerate(groups):
+            g[1]()
+            ev[i][j + 1].record(stream)
     torch.cuda.synchronize()
     if pg:
         pg.barrier()
     t_wall1 = time.time()
     B.conv_sync_status(sh)
-    per_step = [a.elapsed_time(e) for a, e in ev]
+    per_step = [e[0].elapsed_time(e[ng]) for e in ev]
+    per_group = [[e[j].elapsed_time(e[j + 1]) for e in ev] for j in range(ng)]
     dev_ms = sum(per_step)
-    # end-to-end through the same call with host buffers
-    xh = xt.pin_memory()
-    yh = torch.empty(layer.output_shape, dtype=torch.bfloat16).pin_memory()
+
+    # end-to-end: the step's input host -> device, the step, its result -> host
     e2e_steps = max(3, min(args.steps, 50))
-    for _ in range(2):
-        xd.copy_(xh, non_blocking=True)
+
+    def e2e_step():
+        for hsrc, ddst in wl.h2d():
+            ddst.copy_(hsrc, non_blocking=True)
         step()
-        yh.copy_(y, non_blocking=True)
+        for dsrc, hdst in wl.d2h():
+            hdst.copy_(dsrc, non_blocking=True)
+    for _ in range(2):
+        e2e_step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
-        xd.copy_(xh, non_blocking=True)
-        step()
-        yh.copy_(y, non_blocking=True)
+        e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
@@ -313,60 +705,80 @@ def main():
     sampler.stop()
     clocks = sampler.summary(t_wall0 - 0.15, t_wall1 + 0.15)
 
-    # max over ranks of the timed region
     ms_tensor = torch.tensor([dev_ms, e2e_ms], dtype=torch.float64, device=dev)
     if pg:
         pg.all_reduce(ms_tensor, op=pg.ReduceOp.MAX)
     dev_ms, e2e_ms = float(ms_tensor[0]), float(ms_tensor[1])
-    flops = shape.flops()
-    value = flops * args.steps * world / (dev_ms * 1e-3) / 1e12
-    e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
+    step_ms = dev_ms / args.steps
+    value = wl.value(step_ms) * world
+    e2e_value = wl.value(e2e_ms) * world
 
     if rank == 0:
         peaks, peak_src = load_peaks()
-        avg_launch_ms = dev_ms / args.steps
-        is_wino = algo_name.startswith("winograd")
-        kflops = shape.winograd_gemm_flops(2 if "f2x2" in algo_name else 6) if is_wino else flops
-        achieved = kflops / (avg_launch_ms * 1e-3) / 1e12
-        peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        tot = [sum(t) for t in per_group]
+        k = max(range(ng), key=lambda j: tot[j])  # dominant launch group
+        label, _, work, nbytes, bound = groups[k]
+        avg_ms = tot[k] / args.steps
+        kname = label.split(":")[-1]
+        if bound == "tensor":
+            achieved = wl.kernel_work(kname, work) / (avg_ms * 1e-3) / 1e12
+            peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+            unit = "TFLOP/s"
+        else:
+            achieved = nbytes / (avg_ms * 1e-3) / 1e9
+            peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+            unit = "GB/s"
         traffic = None
-        if algo_name in NCU_TRAFFIC:
-            tb, h = NCU_TRAFFIC[algo_name]
-            if h == _src_hash(KERNEL_SOURCE.get(algo_name, "k_igemm.cu")):
+        key = (args.workload, kname)
+        if key in NCU_TRAFFIC and KERNEL_SOURCE.get(kname):
+            tb, h = NCU_TRAFFIC[key]
+            if h == src_hash(KERNEL_SOURCE[kname]):
                 traffic = tb
-        roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
-                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                    "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)"
-                    if peak_src == "measured" else "fallback 1.9 PFLOP/s bf16",
-                    "kernel": algo_name, "algorithmic_flops_per_launch": kflops,
-                    "algorithmic_bytes_per_launch": shape.traffic_bytes(2, 4)}
+        kind = "bf16 burst" if bound == "tensor" else "HBM copy"
+        roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                    "frac": round(achieved / peak, 4), "traffic": traffic,
+                    "peak_source": f"measured {kind} (MEASURED_PEAKS.json)"
+                    if peak_src == "measured" else "fallback", "kernel": label,
+                    "algorithmic_work_per_launch": wl.kernel_work(kname, work),
+                    "algorithmic_bytes_per_launch": nbytes}
+        if args.workload == "int8_stages":
+            roofline["note"] = ("int8 runs on mma.sync (sm_103a has no tcgen05 int8 kind); the "
+                                "fraction is against the measured bf16 tensor peak")
         cpu = None
         if not args.no_cpu_baseline:
             os.environ.setdefault("OMP_NUM_THREADS", str(cpu_cores()))
-            dt, f = oracle_sample(args.cpu_images)
-            cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s",
-                   "cores": int(os.environ["OMP_NUM_THREADS"]), "kind": "oracle",
-                   "sample": f"{args.cpu_images} of 32 images, all 256 output channels "
-                             f"({f / 1e9:.1f} GFLOP, {dt:.1f} s)"}
+            cpu = wl.cpu_baseline(args)
+        groups_out = {}
+        for j, g in enumerate(groups):
+            ms = tot[j] / args.steps
+            groups_out[g[0]] = {"ms": round(ms, 5), "work": g[2], "bytes": g[3],
+                                "tflops": round(g[2] / (ms * 1e-3) / 1e12, 2),
+                                "gbs": round(g[3] / (ms * 1e-3) / 1e9, 1)}
+        h2d_bytes = sum(h.numel() * h.element_size() for h, _ in wl.h2d())
+        d2h_bytes = sum(d.numel() * d.element_size() for d, _ in wl.d2h())
         line = {
-            "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(dev_ms / args.steps, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded N(0,1) activations, Kaiming weights)",
-            "config": {"workload": WORKLOAD_NAME, "algo": algo_name,
+            "metric": wl.metric, "value": round(value, 3), "unit": wl.unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+            "data": "synthetic (seeded; N(0,1)/U activations, Kaiming weights)",
+            "config": {"workload": wl.name, "algo": wl.algo_name,
                        "l2": "flushed between steps (256 MB write outside the event window)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-            "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": xt.numel() * 2, "d2h_bytes_per_step": y.numel() * 2,
+            "e2e": {"value": round(e2e_value, 3), "unit": wl.unit,
+                    "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
                     "ms_per_step": round(e2e_ms, 4)},
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * count_launches(wl, groups),
             "roofline": roofline,
             "cpu_baseline": cpu,
             "clocks": clocks,
-            "fastrun_ms": fastrun_ms,
+            "groups": groups_out,
+            "fastrun_ms": wl.fastrun_ms,
             "step_ms_min_median": [round(min(per_step), 5), round(statistics.median(per_step), 5)],
         }
+        if hasattr(wl, "algo_counts"):
+            line["config"]["algos"] = wl.algo_counts
+        if hasattr(wl, "layer_breakdown"):
+            line["layers"] = wl.layer_breakdown()
         print(json.dumps(line), flush=True)
     if pg:
         pg.barrier()

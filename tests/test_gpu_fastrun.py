@@ -1,0 +1,62 @@
+"""Fast-Run: the selection phase keeps the algorithm that an independent
+re-timing finds fastest (within a 3% noise band), the execution phase (AUTO)
+uses the map, and the map survives a save / load round trip."""
+import statistics
+
+import pytest
+
+from tests.gpu_util import need_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _retime(torch, layer, algo, x, b, reps=25):
+    layer.prepack(layer._w, algo)
+    y = torch.empty(layer.output_shape, dtype=x.dtype, device=x.device)
+    for _ in range(3):
+        layer(x, b, out=y)
+    ts = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        layer(x, b, out=y)
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+@pytest.mark.parametrize("shape", [
+    (8, 256, 56, 56, 256, 3, 1, 1, 1),     # 3x3 layer, several algorithms apply
+    (16, 64, 56, 56, 256, 1, 1, 0, 1),     # 1x1 expand
+    (16, 144, 28, 28, 144, 3, 1, 1, 144),  # depthwise
+])
+def test_fastrun_picks_measured_fastest(shape, tmp_path):
+    torch = need_gpu()
+    from cnn_convolution_gemm_gb300 import binding as B
+    from cnn_convolution_gemm_gb300.layer import ConvLayer
+    dev = torch.device("cuda:0")
+    N, C, H, W, K, R, st, pad, g = shape
+    B.conv_fastrun_clear()
+    layer = ConvLayer(N, C, H, W, K, R, R, st, pad, 1, g)
+    best, times = layer.fastrun()
+    assert times[best] >= 0
+    x = torch.randn((N, H, W, C), device=dev).to(torch.bfloat16)
+    layer._w = torch.randn((K, R, R, C // g), device=dev).to(torch.bfloat16) * 0.05
+    b = torch.zeros(K, device=dev)
+    cands = [a for a, _ in layer.applicable_algos() if a != B.CONV_ALGO_DIRECT]
+    cands = cands or [B.CONV_ALGO_DIRECT]
+    retimed = {a: _retime(torch, layer, a, x, b) for a in cands}
+    fastest = min(retimed.values())
+    assert best in retimed or best == B.CONV_ALGO_DIRECT
+    assert retimed.get(best, float("inf")) <= 1.03 * fastest + 0.002, (best, retimed, times)
+    # execution phase: AUTO resolves to the map entry
+    assert B.conv_fastrun_lookup(layer.desc) == best
+    assert B.conv_algo_resolve(layer.desc) == best
+    p = tmp_path / "fastrun.map"
+    B.conv_fastrun_save(str(p))
+    B.conv_fastrun_clear()
+    with pytest.raises(B.GbconvError):
+        B.conv_fastrun_lookup(layer.desc)
+    B.conv_fastrun_load(str(p))
+    assert B.conv_fastrun_lookup(layer.desc) == best
