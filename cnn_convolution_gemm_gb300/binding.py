@@ -57,6 +57,7 @@ SIGNATURES = {
     "conv_weights_packed_size": (_i, [_p, _i, ctypes.POINTER(_sz)]),
     "conv_weights_prepack": (_i, [_p, _i, _p, _p, _p]),
     "conv_fwd": (_i, [_p, _p, _p, _p, _p, _p, _i, _p, _sz, _p]),
+    "conv_fwd_noalloc": (_i, [_p, _p, _p, _p, _p, _p, _i, _p]),
     "conv_fastrun_select": (_i, [_p, _p, ctypes.POINTER(_i), ctypes.POINTER(_f)]),
     "conv_fastrun_lookup": (_i, [_p, ctypes.POINTER(_i)]),
     "conv_fastrun_save": (_i, [_cp]),
@@ -189,6 +190,12 @@ def conv_fwd(desc, x_ptr, wpack_ptr, bias_ptr, residual_ptr, y_ptr, algo=CONV_AL
     _check(load_library().conv_fwd(desc, _ptr(x_ptr), _ptr(wpack_ptr), _ptr(bias_ptr),
                                    _ptr(residual_ptr), _ptr(y_ptr), algo, _ptr(ws_ptr), ws_bytes,
                                    _stream(stream)), "conv_fwd")
+
+
+def conv_fwd_noalloc(desc, x_ptr, wpack_ptr, bias_ptr, residual_ptr, y_ptr, algo, stream=None):
+    _check(load_library().conv_fwd_noalloc(desc, _ptr(x_ptr), _ptr(wpack_ptr), _ptr(bias_ptr),
+                                           _ptr(residual_ptr), _ptr(y_ptr), algo, _stream(stream)),
+           "conv_fwd_noalloc")
 
 
 def conv_fastrun_select(desc, stream=None):

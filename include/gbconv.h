@@ -143,6 +143,27 @@ conv_status_t conv_fwd(conv_desc_t desc, const void* x, const void* wpack, const
                        const void* residual, void* y, conv_algo_t algo, void* ws,
                        size_t ws_bytes, void* stream);
 
+/* Winograd forward (algo CONV_ALGO_WINO_F2 or CONV_ALGO_WINO_F6) that
+ * allocates nothing and takes no workspace.  The pages have no counterpart:
+ * this entry point exists for callers that cannot allocate device memory when
+ * they run a layer — a plugin inside a host framework whose memory manager
+ * owns all device allocations, a latency-critical path where a cudaMalloc or a
+ * growing allocator pool would stall or synchronize the GPU, or a deployment
+ * whose memory budget is fixed at load time.  They pass inputs and outputs only
+ * (same meaning, layout and alignment rules as conv_fwd; wpack from
+ * conv_weights_prepack with the same algo).
+ * Scratch: a fixed 24 MiB array in device global memory, held by every GPU
+ * that loads the library until the process exits.  The batch is processed in
+ * slices of as many images as fit; if a single image needs more, the call
+ * returns CONV_ERR_WORKSPACE before launching anything.  All calls on a device
+ * share the array: calls that can overlap on the GPU race on it, so order them
+ * (one stream, or events).  The first call on a device looks up the array's
+ * device address with that device current; make it before any stream capture.
+ * Other algorithms return CONV_ERR_UNSUPPORTED.  Stream-ordered. */
+conv_status_t conv_fwd_noalloc(conv_desc_t desc, const void* x, const void* wpack,
+                               const void* bias, const void* residual, void* y,
+                               conv_algo_t algo, void* stream);
+
 /* ---- Fast-Run ([MegEngine] "Fast-Run") ----------------------------------- */
 
 /* Selection phase: time every applicable algorithm for this descriptor on the
