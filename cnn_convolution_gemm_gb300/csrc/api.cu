@@ -379,7 +379,10 @@ extern "C" conv_status_t conv_weights_packed_size(conv_desc_t d, conv_algo_t alg
   switch (a) {
     case CONV_ALGO_IGEMM_N64:
     case CONV_ALGO_IGEMM_N128:
-    case CONV_ALGO_IGEMM_N256: *bytes = (size_t)d->K * d->R * d->S * Cp64 * 2; break;
+    case CONV_ALGO_IGEMM_N256:
+      *bytes = d->C == 8 ? (size_t)d->K * gb_ceil_div(d->R * d->S, 8) * 64 * 2  // 8 taps x 8 ch
+                         : (size_t)d->K * d->R * d->S * Cp64 * 2;
+      break;
     case CONV_ALGO_INT8_MMA: *bytes = (size_t)d->K * d->R * d->S * Cp64; break;
     case CONV_ALGO_WINO_F2: *bytes = winograd_packed_bytes(*d, 2); break;
     case CONV_ALGO_WINO_F6: *bytes = winograd_packed_bytes(*d, 6); break;
@@ -431,7 +434,7 @@ static conv_status_t fwd_impl(const gbconv_desc_s& d, const void* x, const void*
                             y, err, wait_ns, s);
       break;
     case CONV_ALGO_DEPTHWISE:
-      e = launch_dwconv3x3(d, x, wpack, static_cast<const float*>(bias), res, y, s);
+      e = launch_dwconv3x3(d, x, wpack, static_cast<const float*>(bias), res, y, err, wait_ns, s);
       break;
     case CONV_ALGO_INT8_MMA:
       e = launch_igemm_int8(d, x, wpack, static_cast<const int32_t*>(bias), y, s);

@@ -66,7 +66,8 @@ cudaError_t launch_batched_gemm_tc(int batch, int M, int N, int Kred, const void
 
 // Depthwise 3x3 (bf16 NHWC).  w: packed tap-major [9][C] bf16.
 cudaError_t launch_dwconv3x3(const gbconv_desc_s& d, const void* x, const void* w,
-                             const float* bias, const void* res, void* y, cudaStream_t st);
+                             const float* bias, const void* res, void* y, int* err,
+                             unsigned long long wait_ns, cudaStream_t st);
 // [C][3][3] -> tap-major [9][C] bf16.
 cudaError_t launch_pack_dw_weights(const gbconv_desc_s& d, const void* w, void* wpack,
                                    cudaStream_t st);

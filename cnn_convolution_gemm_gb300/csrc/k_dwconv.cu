@@ -2,150 +2,218 @@
 // fused bias / residual / ReLU / ReLU6.
 //
 // The Momenta talk ("優化2：Depthwise卷積") splits a 3x3 conv into a per-channel
-// spatial filter and a 1x1 channel mix; the spatial part loads each input
-// value for only 9 multiply-adds, so it is bound by memory bandwidth, not
-// arithmetic.  The kernel is therefore built to move each input byte from
-// DRAM once:
-//   * a thread owns 8 channels (one 16-byte vector) of one output column ow
-//     and walks down a strip of TH output rows, keeping the 3 x 3 input window
-//     in registers (fp32) and loading only the new input row(s) per step;
-//   * consecutive threads of a warp own consecutive channel vectors, then
-//     consecutive columns, so every load and store is a contiguous 16-byte
-//     run of the NHWC row;
-//   * weights are prepacked tap-major ([9][C] bf16) so one 16-byte load
-//     fetches a tap for the thread's 8 channels; they stay in registers.
+// spatial filter and a 1x1 channel mix; the spatial part does only 9
+// multiply-adds per loaded value, so it is bound by memory bandwidth.  The
+// kernel is built so HBM streams at full rate with few threads:
+//   * persistent CTAs walk a list of blocks (image, channel slice of up to 256
+//     channels — all of C for the usual widths, so a block reads whole
+//     contiguous pixel runs —, block of RB output rows, block of output
+//     columns sized to fill a buffer); for each, one 4-D TMA load
+//     brings the input rows/columns the block needs (its halo included) into
+//     shared memory, and out-of-bounds elements arrive as zeros, which is the
+//     padding;
+//   * two shared-memory buffers: the load of the next block is in flight while
+//     the current one is computed, so bytes in flight do not depend on
+//     registers or occupancy;
+//   * a thread owns 4 channels of one output column and walks down the block's
+//     rows keeping a 3 x 3 window in registers (3 new 8-byte shared loads per
+//     output row); operands stay packed as fp32 pairs for fma.rn.f32x2;
+//   * weights are prepacked tap-major ([9][C] bf16): one 16-byte load per tap.
 #include <cuda_bf16.h>
 
 #include <algorithm>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace {
 
-constexpr int TH = 8;  // output rows per thread
+constexpr int MAX_THREADS = 512;
+constexpr int BUF_MAX = 100 * 1024;  // bytes per shared-memory buffer (two buffers)
 
-struct DwParams {
-  int N, C, H, W, OH, OW, pad, CV, strips, act;
+template <int ST>
+struct DwCfg {
+  static constexpr int RB = ST == 1 ? 8 : 4;      // output rows per block
+  static constexpr int IH = (RB - 1) * ST + 3;    // input rows per block
+  static constexpr int SMEM = 2 * BUF_MAX + 1024 + 64;
 };
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
-  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    f[2 * j] = __uint_as_float(u[j] << 16);
-    f[2 * j + 1] = __uint_as_float(u[j] & 0xffff0000u);
-  }
+struct DwParams {
+  int N, C, H, W, OH, OW, pad, act;
+  int cb;                  // channels per block (all of C when C <= 256)
+  int owt, iw, buf_bytes;  // output columns per block, input columns, bytes per buffer
+  int cslices, rblocks, cblocks;
+  long long nblocks;
+  int* err;
+  unsigned long long wait_ns;
+};
+
+// two fp32 values in one 64-bit register pair (the operand of fma.rn.f32x2)
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 unpack2(f32x2 v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+// bf16x2 (one 32-bit word) -> two fp32 in a register pair
+__device__ __forceinline__ f32x2 bf16x2_to_f32x2(uint32_t u) {
+  return pack2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+__device__ __forceinline__ void ffma2(f32x2& d, f32x2 a, f32x2 b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
 }
 
 template <int ST>
-__global__ void __launch_bounds__(128)
-    dwconv3x3_kernel(const DwParams p, const __nv_bfloat16* __restrict__ x,
-                     const __nv_bfloat16* __restrict__ w9c, const float* __restrict__ bias,
-                     const __nv_bfloat16* __restrict__ res, __nv_bfloat16* __restrict__ y) {
-  long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  const long long total = (long long)p.N * p.strips * p.OW * p.CV;
-  if (t >= total) return;
-  const int cv = (int)(t % p.CV);
-  t /= p.CV;
-  const int ow = (int)(t % p.OW);
-  t /= p.OW;
-  const int strip = (int)(t % p.strips);
-  const int n = (int)(t / p.strips);
-  const int c = cv * 8;
+__global__ void __launch_bounds__(MAX_THREADS, 1)
+    dwconv3x3_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const DwParams p,
+                         const __nv_bfloat16* __restrict__ w9c, const float* __restrict__ bias,
+                         const __nv_bfloat16* __restrict__ res, __nv_bfloat16* __restrict__ y) {
+  using Cf = DwCfg<ST>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + 2 * BUF_MAX);
 
-  float wr[9][8];
-#pragma unroll
-  for (int k = 0; k < 9; ++k)
-    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(w9c + (size_t)k * p.C + c)), wr[k]);
-  float b[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) b[j] = bias ? __ldg(bias + c + j) : 0.f;
+  if (threadIdx.x == 0) {
+    gb::mbar_init(&full[0], 1);
+    gb::mbar_init(&full[1], 1);
+    gb::fence_barrier_init();
+    gb::tma_prefetch_desc(&tm_x);
+  }
+  __syncthreads();
 
-  const int oh0 = strip * TH;
-  const int iw0 = ow * ST - p.pad;
-  const __nv_bfloat16* xn = x + (size_t)n * p.H * p.W * p.C + c;
-
-  // load one input row (3 columns) of the window as raw bf16 vectors
-  auto load_row = [&](int ih, uint4 (&dst)[3]) {
-#pragma unroll
-    for (int j = 0; j < 3; ++j) {
-      const int iw = iw0 + j;
-      if (ih >= 0 && ih < p.H && iw >= 0 && iw < p.W)
-        dst[j] = __ldg(reinterpret_cast<const uint4*>(xn + ((size_t)ih * p.W + iw) * p.C));
-      else
-        dst[j] = make_uint4(0, 0, 0, 0);
-    }
+  auto block_coords = [&](long long b, int& n, int& cs, int& rb, int& cb) {
+    cb = (int)(b % p.cblocks);
+    b /= p.cblocks;
+    rb = (int)(b % p.rblocks);
+    b /= p.rblocks;
+    cs = (int)(b % p.cslices);
+    n = (int)(b / p.cslices);
+  };
+  auto issue = [&](long long b, int buf) {
+    int n, cs, rb, cb;
+    block_coords(b, n, cs, rb, cb);
+    gb::fence_proxy_async_smem();
+    gb::mbar_arrive_expect_tx(&full[buf], p.buf_bytes);
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(gb::smem_u32(smem + buf * BUF_MAX)),
+        "l"(reinterpret_cast<uint64_t>(&tm_x)), "r"(cs * p.cb), "r"(cb * p.owt * ST - p.pad),
+        "r"(rb * Cf::RB * ST - p.pad), "r"(n), "r"(gb::smem_u32(&full[buf]))
+        : "memory");
   };
 
-  // window rows win[slot][col][ch]; slot rotates with the unrolled row index
-  constexpr int SLOTS = 3;
-  float win[SLOTS][3][8];
-  {
-    uint4 raw[3];
-#pragma unroll
-    for (int i = 0; i < 3; ++i) {
-      load_row(oh0 * ST - p.pad + i, raw);
-#pragma unroll
-      for (int j = 0; j < 3; ++j) bf16x8_to_f32(raw[j], win[i][j]);
+  long long b = blockIdx.x;
+  if (threadIdx.x == 0 && b < p.nblocks) issue(b, 0);
+  int it = 0;
+  bool ok = true;
+  const int groups = p.cb / 4;
+  const int items = p.owt * groups;
+  for (; b < p.nblocks; b += gridDim.x, ++it) {
+    const int buf = it & 1;
+    const long long nb = b + gridDim.x;
+    if (threadIdx.x == 0 && nb < p.nblocks) issue(nb, buf ^ 1);
+    if (!gb::mbar_wait_bounded(&full[buf], (it >> 1) & 1, p.wait_ns, p.err)) ok = false;
+    if (!__syncthreads_and(ok)) {
+      // a wait ran out: let the loads this CTA issued land before it exits
+      if (threadIdx.x == 0) {
+        gb::mbar_wait_bounded(&full[buf], (it >> 1) & 1, p.wait_ns, p.err);
+        if (nb < p.nblocks)
+          gb::mbar_wait_bounded(&full[buf ^ 1], ((it + 1) >> 1) & 1, p.wait_ns, p.err);
+      }
+      break;
     }
+    int n, cs, rb, cb;
+    block_coords(b, n, cs, rb, cb);
+    const uint8_t* tile = smem + buf * BUF_MAX;
+    // work items: (4-channel group g, output column j), g fastest
+    for (int item = threadIdx.x; item < items; item += blockDim.x) {
+      const int g = item % groups;
+      const int j = item / groups;
+      const int c = cs * p.cb + g * 4;
+      const int ow = cb * p.owt + j;
+      if (c >= p.C || ow >= p.OW) continue;
+      f32x2 wr[9][2];
+#pragma unroll
+      for (int k = 0; k < 9; ++k) {
+        const uint2 v = __ldg(reinterpret_cast<const uint2*>(w9c + (size_t)k * p.C + c));
+        wr[k][0] = bf16x2_to_f32x2(v.x);
+        wr[k][1] = bf16x2_to_f32x2(v.y);
+      }
+      f32x2 bz[2];
+      bz[0] = bias ? pack2(__ldg(bias + c), __ldg(bias + c + 1)) : pack2(0.f, 0.f);
+      bz[1] = bias ? pack2(__ldg(bias + c + 2), __ldg(bias + c + 3)) : pack2(0.f, 0.f);
+      const int lc = j * ST;  // tile-local input column of tap s = 0
+      auto ld = [&](int row, int s, f32x2* f) {
+        const uint2 v = *reinterpret_cast<const uint2*>(
+            tile + ((size_t)(row * p.iw + lc + s) * p.cb + g * 4) * 2);
+        f[0] = bf16x2_to_f32x2(v.x);
+        f[1] = bf16x2_to_f32x2(v.y);
+      };
+      f32x2 win[3][3][2];  // [slot][s][pair]; input row rho lives in slot rho % 3
+#pragma unroll
+      for (int i = 0; i < 3; ++i)
+#pragma unroll
+        for (int s = 0; s < 3; ++s) ld(i, s, win[i][s]);
+#pragma unroll
+      for (int k = 0; k < Cf::RB; ++k) {
+        const int oh = rb * Cf::RB + k;
+        if (oh >= p.OH) break;
+        if (k > 0) {  // the ST new input rows of this output row's window
+#pragma unroll
+          for (int q = 0; q < ST; ++q) {
+            const int rho = (k - 1) * ST + 3 + q;
+#pragma unroll
+            for (int s = 0; s < 3; ++s) ld(rho, s, win[rho % 3][s]);
+          }
+        }
+        f32x2 acc[2] = {bz[0], bz[1]};
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+          const int sl = (k * ST + i) % 3;
+#pragma unroll
+          for (int s = 0; s < 3; ++s) {
+            ffma2(acc[0], win[sl][s][0], wr[i * 3 + s][0]);
+            ffma2(acc[1], win[sl][s][1], wr[i * 3 + s][1]);
+          }
+        }
+        float a[4];
+        const float2 a01 = unpack2(acc[0]), a23 = unpack2(acc[1]);
+        a[0] = a01.x;
+        a[1] = a01.y;
+        a[2] = a23.x;
+        a[3] = a23.y;
+        const size_t off = (((size_t)n * p.OH + oh) * p.OW + ow) * p.C + c;
+        if (res) {
+          const uint2 rv = __ldg(reinterpret_cast<const uint2*>(res + off));
+          a[0] += __uint_as_float(rv.x << 16);
+          a[1] += __uint_as_float(rv.x & 0xffff0000u);
+          a[2] += __uint_as_float(rv.y << 16);
+          a[3] += __uint_as_float(rv.y & 0xffff0000u);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (p.act >= 1) a[q] = fmaxf(a[q], 0.f);
+          if (p.act == 2) a[q] = fminf(a[q], 6.f);
+        }
+        __nv_bfloat162 h0 = __floats2bfloat162_rn(a[0], a[1]);
+        __nv_bfloat162 h1 = __floats2bfloat162_rn(a[2], a[3]);
+        uint2 o;
+        o.x = *reinterpret_cast<uint32_t*>(&h0);
+        o.y = *reinterpret_cast<uint32_t*>(&h1);
+        *reinterpret_cast<uint2*>(y + off) = o;
+      }
+    }
+    __syncthreads();  // the buffer is free for the load issued next iteration
   }
-
-#pragma unroll
-  for (int k = 0; k < TH; ++k) {
-    const int oh = oh0 + k;
-    if (oh >= p.OH) break;
-    // prefetch the rows the next output needs (ST new rows)
-    uint4 nxt[ST][3];
-    if (k + 1 < TH && oh + 1 < p.OH) {
-#pragma unroll
-      for (int q = 0; q < ST; ++q) load_row((oh + 1) * ST - p.pad + (3 - ST) + q, nxt[q]);
-    }
-    // slots: row i of the current window lives in slot (k*ST + i) % 3
-    float acc[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = b[j];
-#pragma unroll
-    for (int i = 0; i < 3; ++i) {
-      const int sl = (k * ST + i) % SLOTS;
-#pragma unroll
-      for (int jj = 0; jj < 3; ++jj)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = fmaf(win[sl][jj][j], wr[i * 3 + jj][j], acc[j]);
-    }
-    const size_t off = (((size_t)n * p.OH + oh) * p.OW + ow) * p.C + c;
-    if (res) {
-      float r[8];
-      bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(res + off)), r);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc[j] += r[j];
-    }
-    uint4 o;
-    uint32_t* ou = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float a0 = acc[2 * j], a1 = acc[2 * j + 1];
-      if (p.act >= 1) {
-        a0 = fmaxf(a0, 0.f);
-        a1 = fmaxf(a1, 0.f);
-      }
-      if (p.act == 2) {
-        a0 = fminf(a0, 6.f);
-        a1 = fminf(a1, 6.f);
-      }
-      __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
-      ou[j] = *reinterpret_cast<uint32_t*>(&h);
-    }
-    *reinterpret_cast<uint4*>(y + off) = o;
-    // retire the oldest ST rows, install the prefetched ones
-    if (k + 1 < TH && oh + 1 < p.OH) {
-#pragma unroll
-      for (int q = 0; q < ST; ++q) {
-        const int sl = (k * ST + 3 + q) % SLOTS;
-#pragma unroll
-        for (int j = 0; j < 3; ++j) bf16x8_to_f32(nxt[q][j], win[sl][j]);
-      }
-    }
-  }
+  // On normal exit every issued load has been waited for: the last iteration
+  // issues none, because its successor index is past the block list.
 }
 
 // [C][3][3] -> [9][C]
@@ -155,6 +223,64 @@ __global__ void pack_dw_weights_kernel(const __nv_bfloat16* __restrict__ w,
   if (i >= 9 * C) return;
   const int k = i / C, c = i % C;
   wp[i] = w[c * 9 + k];
+}
+
+template <int ST>
+cudaError_t launch_st(const gbconv_desc_s& d, const void* x, const void* w, const float* bias,
+                      const void* res, void* y, int* err, unsigned long long wait_ns,
+                      cudaStream_t st) {
+  using Cf = DwCfg<ST>;
+  DwParams p{};
+  p.N = d.N;
+  p.C = d.C;
+  p.H = d.H;
+  p.W = d.W;
+  p.OH = d.OH;
+  p.OW = d.OW;
+  p.pad = d.pad;
+  p.act = d.act;
+  // channel slices of <= 256 channels (the TMA box limit), as few as possible,
+  // so each block reads whole contiguous pixel rows
+  p.cslices = gb_ceil_div(d.C, 256);
+  p.cb = gb_ceil_div(gb_ceil_div(d.C, p.cslices), 8) * 8;
+  // widest column block whose input tile fits one buffer
+  const int px_bytes = p.cb * 2;
+  int iw_max = BUF_MAX / (Cf::IH * px_bytes);
+  int owt = (iw_max - 3) / ST + 1;
+  if (owt > d.OW) owt = d.OW;
+  if (owt > 256 / ST - 2) owt = 256 / ST - 2;  // TMA box dimension <= 256
+  if (owt < 1) return cudaErrorInvalidConfiguration;
+  owt = gb_ceil_div(d.OW, gb_ceil_div(d.OW, owt));  // equal-width column blocks
+  p.owt = owt;
+  p.iw = (p.owt - 1) * ST + 3;
+  p.buf_bytes = Cf::IH * p.iw * px_bytes;
+  p.rblocks = gb_ceil_div(d.OH, Cf::RB);
+  p.cblocks = gb_ceil_div(d.OW, p.owt);
+  p.nblocks = (long long)d.N * p.cslices * p.rblocks * p.cblocks;
+  p.err = err;
+  p.wait_ns = wait_ns;
+  CUtensorMap tm;
+  cuuint64_t dims[4] = {(cuuint64_t)d.C, (cuuint64_t)d.W, (cuuint64_t)d.H, (cuuint64_t)d.N};
+  cuuint64_t strides[3] = {(cuuint64_t)d.C * 2, (cuuint64_t)d.W * d.C * 2,
+                           (cuuint64_t)d.H * d.W * d.C * 2};
+  cuuint32_t box[4] = {(cuuint32_t)p.cb, (cuuint32_t)p.iw, Cf::IH, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  if (gb_encode_tiled(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims,
+                      strides, box, estr, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(dwconv3x3_tma_kernel<ST>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+  if (e != cudaSuccess) return e;
+  const long long grid = std::min<long long>(p.nblocks, gb_num_sms());
+  // threads: the block's work items split into equal rounds of <= MAX_THREADS
+  const int groups = p.cb / 4;
+  const int items = p.owt * groups;
+  const int rounds = gb_ceil_div(items, MAX_THREADS);
+  const int threads = gb_ceil_div(gb_ceil_div(items, rounds), 32) * 32;
+  dwconv3x3_tma_kernel<ST><<<(unsigned)grid, threads, Cf::SMEM, st>>>(
+      tm, p, static_cast<const __nv_bfloat16*>(w), bias, static_cast<const __nv_bfloat16*>(res),
+      static_cast<__nv_bfloat16*>(y));
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -168,19 +294,8 @@ cudaError_t launch_pack_dw_weights(const gbconv_desc_s& d, const void* w, void* 
 }
 
 cudaError_t launch_dwconv3x3(const gbconv_desc_s& d, const void* x, const void* w,
-                             const float* bias, const void* res, void* y, cudaStream_t st) {
-  DwParams p{d.N, d.C, d.H, d.W, d.OH, d.OW, d.pad, d.C / 8, gb_ceil_div(d.OH, TH), d.act};
-  const long long total = (long long)p.N * p.strips * p.OW * p.CV;
-  const int block = 128;
-  const long long grid = gb_ceil_div_ll(total, block);
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  auto xb = static_cast<const __nv_bfloat16*>(x);
-  auto wb = static_cast<const __nv_bfloat16*>(w);
-  auto rb = static_cast<const __nv_bfloat16*>(res);
-  auto yb = static_cast<__nv_bfloat16*>(y);
-  if (d.stride == 1)
-    dwconv3x3_kernel<1><<<(unsigned)grid, block, 0, st>>>(p, xb, wb, bias, rb, yb);
-  else
-    dwconv3x3_kernel<2><<<(unsigned)grid, block, 0, st>>>(p, xb, wb, bias, rb, yb);
-  return cudaGetLastError();
+                             const float* bias, const void* res, void* y, int* err,
+                             unsigned long long wait_ns, cudaStream_t st) {
+  if (d.stride == 1) return launch_st<1>(d, x, w, bias, res, y, err, wait_ns, st);
+  return launch_st<2>(d, x, w, bias, res, y, err, wait_ns, st);
 }

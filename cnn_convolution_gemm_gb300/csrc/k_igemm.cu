@@ -52,6 +52,10 @@ struct IgemmParams {
   int batch;
   int ab_type;  // 0 = fp16 operands, 1 = bf16
   float* out_f32;
+  // narrow-channel mode (C == 8): each 64-wide k-step holds 8 filter taps x 8
+  // channels, loaded as 8 im2col boxes of 128 pixels x 16 bytes
+  int narrow;
+  int taps;  // R * S
 };
 
 enum { MODE_CONV = 0, MODE_BATCHED = 1 };
@@ -147,7 +151,18 @@ __global__ void __launch_bounds__(192, 1)
             break;
           }
           gb::mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-          if (MODE == MODE_CONV) {
+          if (MODE == MODE_CONV && p.narrow) {
+#pragma unroll 1
+            for (int t = 0; t < 8; ++t) {
+              int tap = it * 8 + t;
+              if (tap >= p.taps) tap = 0;  // its packed weights are zero
+              const int tr = tap / p.S, ts = tap % p.S;
+              gb::tma_load_im2col_4d(sA + stage * C::A_BYTES + t * (BM * 16), &tm_x, &full[stage],
+                                     0, w0, h0, img, (uint16_t)(ts * p.dil),
+                                     (uint16_t)(tr * p.dil));
+            }
+            gb::tma_load_2d(sB + stage * C::B_BYTES, &tm_w, &full[stage], it * BK, nt * BN);
+          } else if (MODE == MODE_CONV) {
             gb::tma_load_im2col_4d(sA + stage * C::A_BYTES, &tm_x, &full[stage], cb * BK, w0, h0,
                                    img, (uint16_t)(s * p.dil), (uint16_t)(r * p.dil));
             gb::tma_load_2d(sB + stage * C::B_BYTES, &tm_w, &full[stage],
@@ -205,9 +220,15 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t a0 = gb::smem_u32(sA + stage * C::A_BYTES);
           const uint32_t b0 = gb::smem_u32(sB + stage * C::B_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            gb::tc_mma_f16(d, gb::sw128_kmajor_desc(a0 + k * 32),
-                           gb::sw128_kmajor_desc(b0 + k * 32), IDESC, (it | k) != 0);
+          for (int k = 0; k < BK / 16; ++k) {
+            // narrow mode: two taps (2 x 2 KB boxes) per 16-wide k; core matrices
+            // are 128 bytes apart along M and one box (2 KB) apart along K
+            const uint64_t adesc =
+                (MODE == MODE_CONV && p.narrow)
+                    ? gb::noswz_kmajor_desc(a0 + k * 2 * (BM * 16), BM * 16, 128)
+                    : gb::sw128_kmajor_desc(a0 + k * 32);
+            gb::tc_mma_f16(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), IDESC, (it | k) != 0);
+          }
           gb::tc_commit(&empty[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
@@ -311,15 +332,18 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
+// wp[k][rs][c] (rs < RS, c < Cp) = w[k][rs][c] for rs < RS_valid and c < C, else 0
 __global__ void pack_igemm_weights_kernel(const __nv_bfloat16* __restrict__ w,
                                           __nv_bfloat16* __restrict__ wp, int K, int RS, int C,
-                                          int Cp) {
+                                          int Cp, int RS_valid) {
   const long long total = (long long)K * RS * Cp;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
     const int c = (int)(i % Cp);
     const long long krs = i / Cp;
-    wp[i] = c < C ? w[krs * C + c] : __float2bfloat16(0.0f);
+    const int rs = (int)(krs % RS);
+    const long long k = krs / RS;
+    wp[i] = (c < C && rs < RS_valid) ? w[(k * RS_valid + rs) * C + c] : __float2bfloat16(0.0f);
   }
 }
 
@@ -328,8 +352,11 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
                       const void* res, void* y, int* err, unsigned long long wait_ns,
                       cudaStream_t st) {
   using Cf = Cfg<BN>;
+  const bool narrow = d.C == 8;
   const int Cp = gb_ceil_div(d.C, BK) * BK;
   IgemmParams p{};
+  p.narrow = narrow ? 1 : 0;
+  p.taps = d.R * d.S;
   p.H = d.H;
   p.W = d.W;
   p.C = d.C;
@@ -340,9 +367,9 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   p.dil = d.dil;
   p.OH = d.OH;
   p.OW = d.OW;
-  p.cblocks = Cp / BK;
-  p.kiters = d.R * d.S * p.cblocks;
-  p.Kw = d.R * d.S * Cp;
+  p.cblocks = narrow ? 1 : Cp / BK;
+  p.kiters = narrow ? gb_ceil_div(d.R * d.S, 8) : d.R * d.S * p.cblocks;
+  p.Kw = narrow ? p.kiters * BK : d.R * d.S * Cp;
   p.M = (long long)d.N * d.OH * d.OW;
   p.m_tiles = (int)gb_ceil_div_ll(p.M, BM);
   p.n_tiles = gb_ceil_div(d.K, BN);
@@ -364,8 +391,8 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
     int upper[2] = {d.pad - d.dil * (d.S - 1), d.pad - d.dil * (d.R - 1)};
     cuuint32_t estr[4] = {1, (cuuint32_t)d.stride, (cuuint32_t)d.stride, 1};
     CUresult r = gb_encode_im2col(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x),
-                                  dims, strides, lower, upper, BK, BM, estr,
-                                  CU_TENSOR_MAP_SWIZZLE_128B);
+                                  dims, strides, lower, upper, narrow ? 8 : BK, BM, estr,
+                                  narrow ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
   {
@@ -474,12 +501,21 @@ cudaError_t launch_batched_gemm_tc(int batch, int M, int N, int Kred, const void
 
 cudaError_t launch_pack_igemm_weights(const gbconv_desc_s& d, const void* w, void* wpack,
                                       cudaStream_t st) {
+  if (d.C == 8) {  // narrow mode: [K][taps rounded up to 8][8], zero taps at the end
+    const int taps8 = gb_ceil_div(d.R * d.S, 8) * 8;
+    const long long total = (long long)d.K * taps8 * 8;
+    const int grid = (int)std::min<long long>(gb_ceil_div_ll(total, 256), 65535LL * 8);
+    pack_igemm_weights_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(w),
+                                                    static_cast<__nv_bfloat16*>(wpack), d.K,
+                                                    taps8, 8, 8, d.R * d.S);
+    return cudaGetLastError();
+  }
   const int Cp = gb_ceil_div(d.C, BK) * BK;
   const long long total = (long long)d.K * d.R * d.S * Cp;
   const int block = 256;
   const int grid = (int)std::min<long long>(gb_ceil_div_ll(total, block), 65535LL * 8);
   pack_igemm_weights_kernel<<<grid, block, 0, st>>>(static_cast<const __nv_bfloat16*>(w),
                                                     static_cast<__nv_bfloat16*>(wpack), d.K,
-                                                    d.R * d.S, d.C, Cp);
+                                                    d.R * d.S, d.C, Cp, d.R * d.S);
   return cudaGetLastError();
 }

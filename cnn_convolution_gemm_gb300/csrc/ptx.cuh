@@ -190,6 +190,19 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory matrix descriptor for a K-major operand tile without swizzle,
+// built from 8-row x 16-byte core matrices: `lbo` bytes between core matrices
+// adjacent along K, `sbo` bytes between core matrices adjacent along M/N.
+__device__ __forceinline__ uint64_t noswz_kmajor_desc(uint32_t smem_addr, uint32_t lbo,
+                                                      uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFF) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version; swizzle field 0 = none
+  return d;
+}
+
 // Instruction descriptor for kind::f16: fp32 accumulate, both operands K-major.
 // ab_type: 0 = f16, 1 = bf16.
 __host__ __device__ constexpr uint32_t idesc_f16(int m, int n, int ab_type) {
