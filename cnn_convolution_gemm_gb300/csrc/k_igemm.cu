@@ -19,8 +19,11 @@
 //   warp 0      TMA producer (one elected lane) -> STAGES-deep smem ring
 //   warp 1      MMA issuer (one lane): tcgen05.mma 128 x BN x 16, fp32 in TMEM
 //   warps 2..5  epilogue: tcgen05.ld -> + bias (+ residual) -> activation ->
-//               bf16 store ("Graph層面" of the Momenta talk: bias and ReLU
-//               fused into the matrix product)
+//               bf16 ("Graph層面" of the Momenta talk: bias and ReLU fused into
+//               the matrix product), staged per warp in a 128-byte-swizzled
+//               32 x 64 shared-memory box and written by a TMA store, so the
+//               output (and the residual, read row-coalesced into the same
+//               box) moves in full 128-byte lines
 // The accumulator is double-buffered in TMEM (2 x BN columns) so the
 // epilogue of tile i overlaps the MMAs of tile i+1.
 #include <cuda_bf16.h>
@@ -67,8 +70,12 @@ struct Cfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (BN >= 256) ? 4 : (BN >= 128 ? 6 : 8);
   static constexpr uint32_t TMEM_COLS = 2 * BN;  // double-buffered fp32 accumulator
+  // epilogue staging: per epilogue warp two 32-row x 64-column bf16 boxes
+  // (128-byte swizzle), written by the warp and stored by TMA
+  static constexpr int EPI_BOX = 32 * 128;
+  static constexpr int EPI_BYTES = 4 * 2 * EPI_BOX;
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES + 1024;
 };
 
 __device__ __forceinline__ float act_apply(float v, int act) {
@@ -80,20 +87,24 @@ __device__ __forceinline__ float act_apply(float v, int act) {
 template <int BN, int MODE>
 __global__ void __launch_bounds__(192, 1)
     igemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
-                         const __grid_constant__ CUtensorMap tm_w, const IgemmParams p) {
+                         const __grid_constant__ CUtensorMap tm_w,
+                         const __grid_constant__ CUtensorMap tm_y,
+                         const __grid_constant__ CUtensorMap tm_r, const IgemmParams p) {
   using C = Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + C::STAGES * C::A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint8_t* sEpi = smem + C::STAGES * C::STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + C::EPI_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + C::STAGES;
   uint64_t* tfull = bars + 2 * C::STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* mma_done = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* rbar = mma_done + 1;  // [4 epilogue warps][2 boxes]: residual box landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rbar + 8);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -108,9 +119,12 @@ __global__ void __launch_bounds__(192, 1)
       gb::mbar_init(&tempty[b], 128);
     }
     gb::mbar_init(mma_done, 1);
+    for (int i = 0; i < 8; ++i) gb::mbar_init(&rbar[i], 1);
     gb::fence_barrier_init();
     gb::tma_prefetch_desc(&tm_x);
     gb::tma_prefetch_desc(&tm_w);
+    if (MODE == MODE_CONV) gb::tma_prefetch_desc(&tm_y);
+    if (MODE == MODE_CONV && p.res) gb::tma_prefetch_desc(&tm_r);
   }
   if (warp == 0) {
     gb::tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -251,6 +265,34 @@ __global__ void __launch_bounds__(192, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int acc = 0;
     uint32_t acc_phase = 0;
+    uint32_t epi_count = 0;  // staging boxes used by this warp (alternating pair)
+    uint32_t rphase = 0;     // bit b: parity of the next completion of box b's barrier
+    // number of 64-column sub-blocks of tile t that hold output columns
+    auto nsub = [&](int t) {
+      const int ntt = (t % tiles_per_batch) % p.n_tiles;
+      const int rem = p.K - ntt * BN;
+      const int s64 = (rem + 63) / 64;
+      return s64 < BN / 64 ? s64 : BN / 64;
+    };
+    // residual box (64 columns x 32 rows) for sub-block j of tile t -> box b
+    auto fetch_res = [&](int t, int j, int b) {
+      const int tt = t % tiles_per_batch;
+      const int mt2 = tt / p.n_tiles, nt2 = tt % p.n_tiles;
+      uint64_t* bar = &rbar[q * 2 + b];
+      gb::mbar_arrive_expect_tx(bar, C::EPI_BOX);
+      asm volatile(
+          "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+          " [%0], [%1, {%2, %3}], [%4];" ::"r"(gb::smem_u32(sEpi + (q * 2 + b) * C::EPI_BOX)),
+          "l"(reinterpret_cast<uint64_t>(&tm_r)), "r"(nt2 * BN + j * 64),
+          "r"(mt2 * BM + q * 32), "r"(gb::smem_u32(bar))
+          : "memory");
+    };
+    const bool has_res = MODE == MODE_CONV && p.res != nullptr;
+    int pending = -1;  // box with a residual load not yet waited for
+    if (has_res && (int)blockIdx.x < num_tiles) {
+      if (lane == 0) fetch_res(blockIdx.x, 0, 0);
+      pending = 0;
+    }
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       const int bt = t / tiles_per_batch;
       const int tt = t % tiles_per_batch;
@@ -260,60 +302,106 @@ __global__ void __launch_bounds__(192, 1)
       const long long m = (long long)mt * BM + q * 32 + lane;
       const bool row_ok = m < p.M;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      if (MODE == MODE_BATCHED) {
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        uint32_t r[16];
-        gb::tmem_ld_x16(tbase + c0, r);
-        gb::tmem_ld_wait();
-        const int n = nt * BN + c0;
-        if (MODE == MODE_BATCHED) {
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          uint32_t r[16];
+          gb::tmem_ld_x16(tbase + c0, r);
+          gb::tmem_ld_wait();
+          const int n = nt * BN + c0;
           if (row_ok && n < p.K) {
-            float4* dst = reinterpret_cast<float4*>(p.out_f32 +
-                                                    ((size_t)bt * p.M + m) * p.K + n);
+            float4* dst = reinterpret_cast<float4*>(p.out_f32 + ((size_t)bt * p.M + m) * p.K + n);
             const int nq = (p.K - n) >= 16 ? 4 : 2;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              if (q < nq)
-                dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                     __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+            for (int qq = 0; qq < 4; ++qq)
+              if (qq < nq)
+                dst[qq] = make_float4(__uint_as_float(r[4 * qq]), __uint_as_float(r[4 * qq + 1]),
+                                      __uint_as_float(r[4 * qq + 2]),
+                                      __uint_as_float(r[4 * qq + 3]));
           }
-        } else if (row_ok && n < p.K) {
-          float v[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-          const int nvalid = (p.K - n) >= 16 ? 16 : 8;  // K % 8 == 0
-          if (p.bias) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (j < nvalid) v[j] += __ldg(p.bias + n + j);
-          }
-          const size_t off = (size_t)m * p.K + n;
-          if (p.res) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              if (h * 8 < nvalid) {
-                uint4 rv = *reinterpret_cast<const uint4*>(p.res + off + h * 8);
-                const __nv_bfloat162* rp = reinterpret_cast<const __nv_bfloat162*>(&rv);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  float2 f = __bfloat1622float2(rp[j]);
-                  v[h * 8 + 2 * j] += f.x;
-                  v[h * 8 + 2 * j + 1] += f.y;
-                }
+        }
+      } else {
+        // 64-column sub-blocks: TMEM -> registers (+ bias, residual, act) ->
+        // swizzled staging box in shared memory -> TMA store of 32 rows x 64 cols
+        const long long m_warp = (long long)mt * BM + q * 32;
+        const int ns = nsub(t);
+#pragma unroll 1
+        for (int j = 0; j < ns; ++j) {
+          const int cur = epi_count & 1;
+          uint8_t* box = sEpi + (q * 2 + cur) * C::EPI_BOX;
+          const int nb0 = nt * BN + j * 64;
+          if (has_res) {
+            // prefetch the next sub-block's residual into the other box once the
+            // store that last read that box is done with it
+            int tn = t, jn = j + 1;
+            if (jn >= ns) {
+              tn = t + gridDim.x;
+              jn = 0;
+            }
+            if (tn < num_tiles) {
+              if (lane == 0) {
+                gb::bulk_wait_read<0>();
+                fetch_res(tn, jn, cur ^ 1);
               }
             }
+            if (!gb::mbar_wait_bounded(&rbar[q * 2 + cur], (rphase >> cur) & 1, p.wait_ns, p.err))
+              break;
+            rphase ^= 1u << cur;
+            pending = tn < num_tiles ? (cur ^ 1) : -1;
+          } else {
+            if (lane == 0) gb::bulk_wait_read<1>();  // the store that last used this box
+            __syncwarp();
           }
-          uint32_t packed[8];
+          uint32_t r[64];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(act_apply(v[2 * j], p.act),
-                                                      act_apply(v[2 * j + 1], p.act));
-            packed[j] = *reinterpret_cast<uint32_t*>(&b2);
+          for (int c16 = 0; c16 < 4; ++c16) {
+            uint32_t (&rr)[16] = *reinterpret_cast<uint32_t(*)[16]>(&r[c16 * 16]);
+            gb::tmem_ld_x16(tbase + j * 64 + c16 * 16, rr);
           }
-          uint4* dst = reinterpret_cast<uint4*>(p.y + off);
-          dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-          if (nvalid == 16) dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+          gb::tmem_ld_wait();
+#pragma unroll
+          for (int c16 = 0; c16 < 4; ++c16) {
+            const int n = nb0 + c16 * 16;
+            float v[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(r[c16 * 16 + k]);
+            if (p.bias) {
+#pragma unroll
+              for (int k = 0; k < 16; ++k)
+                if (n + k < p.K) v[k] += __ldg(p.bias + n + k);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint8_t* chunk = box + lane * 128 + (((c16 * 2 + h) ^ (lane & 7)) << 4);
+              if (has_res) {
+                const uint4 rv = *reinterpret_cast<const uint4*>(chunk);
+                const __nv_bfloat162* rp = reinterpret_cast<const __nv_bfloat162*>(&rv);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const float2 f = __bfloat1622float2(rp[k]);
+                  v[h * 8 + 2 * k] += f.x;
+                  v[h * 8 + 2 * k + 1] += f.y;
+                }
+              }
+              uint32_t pk[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(act_apply(v[h * 8 + 2 * k], p.act),
+                                                          act_apply(v[h * 8 + 2 * k + 1], p.act));
+                pk[k] = *reinterpret_cast<uint32_t*>(&b2);
+              }
+              *reinterpret_cast<uint4*>(chunk) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+          }
+          gb::fence_proxy_async_smem();  // staging writes -> visible to the TMA engine
+          __syncwarp();
+          if (lane == 0) {
+            gb::tma_store_2d(&tm_y, box, nb0, (int)m_warp);
+            gb::bulk_commit();
+          }
+          ++epi_count;
         }
+        (void)row_ok;
       }
       gb::tc_fence_before();
       gb::mbar_arrive(&tempty[acc]);
@@ -321,6 +409,12 @@ __global__ void __launch_bounds__(192, 1)
         acc = 0;
         acc_phase ^= 1;
       }
+    }
+    if (MODE == MODE_CONV && lane == 0) {
+      gb::bulk_wait_all();  // stores done before exit
+      // after a wait ran out, a residual load may still be landing
+      if (pending >= 0)
+        gb::mbar_wait_bounded(&rbar[q * 2 + pending], (rphase >> pending) & 1, p.wait_ns, p.err);
     }
   }
 
@@ -405,12 +499,32 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
                                  CU_TENSOR_MAP_SWIZZLE_128B);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
+  CUtensorMap tmy;  // output [M][K] bf16, 64-column x 32-row boxes, 128-byte swizzle
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)d.K, (cuuint64_t)p.M};
+    cuuint64_t strides[1] = {(cuuint64_t)d.K * 2};
+    cuuint32_t box[2] = {64, 32};
+    cuuint32_t estr[2] = {1, 1};
+    if (gb_encode_tiled(&tmy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, dims, strides, box, estr,
+                        CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  CUtensorMap tmr = tmy;  // residual, same shape and boxes as the output
+  if (res) {
+    cuuint64_t dims[2] = {(cuuint64_t)d.K, (cuuint64_t)p.M};
+    cuuint64_t strides[1] = {(cuuint64_t)d.K * 2};
+    cuuint32_t box[2] = {64, 32};
+    cuuint32_t estr[2] = {1, 1};
+    if (gb_encode_tiled(&tmr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(res), dims,
+                        strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   cudaError_t e = cudaFuncSetAttribute(igemm_bf16_tc_kernel<BN, MODE_CONV>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
   if (e != cudaSuccess) return e;
   const int tiles = p.m_tiles * p.n_tiles;
   const int grid = tiles < gb_num_sms() ? tiles : gb_num_sms();
-  igemm_bf16_tc_kernel<BN, MODE_CONV><<<grid, 192, Cf::SMEM, st>>>(tmx, tmw, p);
+  igemm_bf16_tc_kernel<BN, MODE_CONV><<<grid, 192, Cf::SMEM, st>>>(tmx, tmw, tmy, tmr, p);
   return cudaGetLastError();
 }
 
@@ -459,7 +573,7 @@ cudaError_t launch_batched_bn(int batch, int M, int N, int Kred, const void* A, 
   if (e != cudaSuccess) return e;
   const long long tiles = (long long)p.m_tiles * p.n_tiles * batch;
   const int grid = tiles < gb_num_sms() ? (int)tiles : gb_num_sms();
-  igemm_bf16_tc_kernel<BN, MODE_BATCHED><<<grid, 192, Cf::SMEM, st>>>(tma, tmb, p);
+  igemm_bf16_tc_kernel<BN, MODE_BATCHED><<<grid, 192, Cf::SMEM, st>>>(tma, tmb, tma, tma, p);
   return cudaGetLastError();
 }
 

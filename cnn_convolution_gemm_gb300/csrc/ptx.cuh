@@ -116,6 +116,28 @@ __device__ __forceinline__ void tma_load_im2col_4d(void* smem, const void* map, 
       : "memory");
 }
 
+// 2-D tiled store from shared memory (bulk-group completion).  Elements
+// outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const void* map, const void* smem, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(smem)), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most N committed bulk groups of this thread still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until all committed bulk groups of this thread have completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // ---- tcgen05 ------------------------------------------------------------------
 
 // Allocate ncols TMEM columns (power of two >= 32); the base address is written
