@@ -63,17 +63,20 @@ struct IgemmParams {
 
 enum { MODE_CONV = 0, MODE_BATCHED = 1 };
 
-template <int BN>
+// LIGHT: a shallow ring (for short reductions) so two CTAs fit on one SM and
+// the epilogue, which bounds memory-bound layers, gets twice the warps.
+template <int BN, bool LIGHT = false>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (BN >= 256) ? 4 : (BN >= 128 ? 6 : 8);
+  static constexpr int STAGES =
+      LIGHT ? (BN >= 128 ? 2 : 3) : ((BN >= 256) ? 4 : (BN >= 128 ? 6 : 8));
   static constexpr uint32_t TMEM_COLS = 2 * BN;  // double-buffered fp32 accumulator
   // epilogue staging: per epilogue warp two 32-row x 64-column bf16 boxes
   // (128-byte swizzle), written by the warp and stored by TMA
   static constexpr int EPI_BOX = 32 * 128;
-  static constexpr int EPI_BYTES = 4 * 2 * EPI_BOX;
+  static constexpr int EPI_BYTES = 4 * 2 * EPI_BOX + 4 * 256;  // + per-warp bias slice
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES + 1024;
 };
@@ -84,13 +87,13 @@ __device__ __forceinline__ float act_apply(float v, int act) {
   return v;
 }
 
-template <int BN, int MODE>
+template <int BN, int MODE, bool LIGHT = false>
 __global__ void __launch_bounds__(192, 1)
     igemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                          const __grid_constant__ CUtensorMap tm_w,
                          const __grid_constant__ CUtensorMap tm_y,
                          const __grid_constant__ CUtensorMap tm_r, const IgemmParams p) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, LIGHT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -358,18 +361,29 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t (&rr)[16] = *reinterpret_cast<uint32_t(*)[16]>(&r[c16 * 16]);
             gb::tmem_ld_x16(tbase + j * 64 + c16 * 16, rr);
           }
+          // this sub-block's 64 bias values: two per lane, then broadcast reads
+          float* sbias = reinterpret_cast<float*>(sEpi + 4 * 2 * C::EPI_BOX + q * 256);
+          {
+            const int nc = nb0 + 2 * lane;
+            float2 bv = make_float2(0.f, 0.f);
+            if (p.bias && nc < p.K) bv = make_float2(__ldg(p.bias + nc), __ldg(p.bias + nc + 1));
+            reinterpret_cast<float2*>(sbias)[lane] = bv;
+          }
+          __syncwarp();
           gb::tmem_ld_wait();
 #pragma unroll
           for (int c16 = 0; c16 < 4; ++c16) {
             const int n = nb0 + c16 * 16;
             float v[16];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(r[c16 * 16 + k]);
-            if (p.bias) {
-#pragma unroll
-              for (int k = 0; k < 16; ++k)
-                if (n + k < p.K) v[k] += __ldg(p.bias + n + k);
+            for (int k = 0; k < 16; k += 4) {
+              const float4 bq = reinterpret_cast<const float4*>(sbias)[c16 * 4 + k / 4];
+              v[k] = __uint_as_float(r[c16 * 16 + k]) + bq.x;
+              v[k + 1] = __uint_as_float(r[c16 * 16 + k + 1]) + bq.y;
+              v[k + 2] = __uint_as_float(r[c16 * 16 + k + 2]) + bq.z;
+              v[k + 3] = __uint_as_float(r[c16 * 16 + k + 3]) + bq.w;
             }
+            (void)n;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               uint8_t* chunk = box + lane * 128 + (((c16 * 2 + h) ^ (lane & 7)) << 4);
@@ -441,11 +455,11 @@ __global__ void pack_igemm_weights_kernel(const __nv_bfloat16* __restrict__ w,
   }
 }
 
-template <int BN>
+template <int BN, bool LIGHT>
 cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, const float* bias,
                       const void* res, void* y, int* err, unsigned long long wait_ns,
                       cudaStream_t st) {
-  using Cf = Cfg<BN>;
+  using Cf = Cfg<BN, LIGHT>;
   const bool narrow = d.C == 8;
   const int Cp = gb_ceil_div(d.C, BK) * BK;
   IgemmParams p{};
@@ -519,12 +533,13 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
                         strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(igemm_bf16_tc_kernel<BN, MODE_CONV>,
+  cudaError_t e = cudaFuncSetAttribute(igemm_bf16_tc_kernel<BN, MODE_CONV, LIGHT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
   if (e != cudaSuccess) return e;
   const int tiles = p.m_tiles * p.n_tiles;
-  const int grid = tiles < gb_num_sms() ? tiles : gb_num_sms();
-  igemm_bf16_tc_kernel<BN, MODE_CONV><<<grid, 192, Cf::SMEM, st>>>(tmx, tmw, tmy, tmr, p);
+  const int slots = gb_num_sms() * (LIGHT ? 2 : 1);
+  const int grid = tiles < slots ? tiles : slots;
+  igemm_bf16_tc_kernel<BN, MODE_CONV, LIGHT><<<grid, 192, Cf::SMEM, st>>>(tmx, tmw, tmy, tmr, p);
   return cudaGetLastError();
 }
 
@@ -591,10 +606,17 @@ int igemm_block_n(int algo) {
 cudaError_t launch_igemm_bf16(const gbconv_desc_s& d, int block_n, const void* x,
                               const void* wpack, const float* bias, const void* res, void* y,
                               int* err, unsigned long long wait_ns, cudaStream_t st) {
+  // short reductions (1x1 layers up to 512 channels) are bound by the epilogue
+  // and memory, not by the operand pipeline: run two shallow CTAs per SM
+  const bool light = d.C != 8 && d.R * d.S * gb_ceil_div(d.C, BK) <= 8;
   switch (block_n) {
-    case 64: return launch_bn<64>(d, x, wpack, bias, res, y, err, wait_ns, st);
-    case 128: return launch_bn<128>(d, x, wpack, bias, res, y, err, wait_ns, st);
-    case 256: return launch_bn<256>(d, x, wpack, bias, res, y, err, wait_ns, st);
+    case 64:
+      return light ? launch_bn<64, true>(d, x, wpack, bias, res, y, err, wait_ns, st)
+                   : launch_bn<64, false>(d, x, wpack, bias, res, y, err, wait_ns, st);
+    case 128:
+      return light ? launch_bn<128, true>(d, x, wpack, bias, res, y, err, wait_ns, st)
+                   : launch_bn<128, false>(d, x, wpack, bias, res, y, err, wait_ns, st);
+    case 256: return launch_bn<256, false>(d, x, wpack, bias, res, y, err, wait_ns, st);
     default: return cudaErrorInvalidValue;
   }
 }
