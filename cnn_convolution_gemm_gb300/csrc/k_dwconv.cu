@@ -15,9 +15,10 @@
 //   * two shared-memory buffers: the load of the next block is in flight while
 //     the current one is computed, so bytes in flight do not depend on
 //     registers or occupancy;
-//   * a thread owns 4 channels of one output column and walks down the block's
-//     rows keeping a 3 x 3 window in registers (3 new 8-byte shared loads per
-//     output row); operands stay packed as fp32 pairs for fma.rn.f32x2;
+//   * a thread owns 4 channels of two adjacent output columns and walks down
+//     the block's rows keeping the bf16 input window in registers (4 new
+//     8-byte shared loads per output row), multiplying bf16 operands into fp32
+//     accumulators with fma.rn.f32.bf16;
 //   * weights are prepacked tap-major ([9][C] bf16): one 16-byte load per tap.
 #include <cuda_bf16.h>
 
@@ -28,14 +29,15 @@
 
 namespace {
 
-constexpr int MAX_THREADS = 512;
-constexpr int BUF_MAX = 100 * 1024;  // bytes per shared-memory buffer (two buffers)
+constexpr int MAX_THREADS = 384;
+constexpr int NBUF = 3;              // shared-memory ring depth: two loads in flight
+constexpr int BUF_MAX = 66 * 1024;   // bytes per buffer
 
 template <int ST>
 struct DwCfg {
   static constexpr int RB = ST == 1 ? 8 : 4;      // output rows per block
   static constexpr int IH = (RB - 1) * ST + 3;    // input rows per block
-  static constexpr int SMEM = 2 * BUF_MAX + 1024 + 64;
+  static constexpr int SMEM = NBUF * BUF_MAX + 1024 + 64;
 };
 
 struct DwParams {
@@ -47,6 +49,9 @@ struct DwParams {
   int* err;
   unsigned long long wait_ns;
 };
+
+// work items of one block: (4-channel group, pair of output columns)
+__host__ __device__ inline int gb_items(const DwParams& p) { return ((p.owt + 1) / 2) * (p.cb / 4); }
 
 // two fp32 values in one 64-bit register pair (the operand of fma.rn.f32x2)
 typedef unsigned long long f32x2;
@@ -69,6 +74,17 @@ __device__ __forceinline__ void ffma2(f32x2& d, f32x2 a, f32x2 b) {
   asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
 }
 
+// d += a * w with bf16 operands and an fp32 accumulator, one rounding (the same
+// result as converting both operands to fp32 first)
+__device__ __forceinline__ void fma_bf16(float& d, unsigned short a, unsigned short w) {
+  asm("fma.rn.f32.bf16 %0, %1, %2, %0;" : "+f"(d) : "h"(a), "h"(w));
+}
+// four bf16 values of an 8-byte load, one per 16-bit register
+__device__ __forceinline__ void split4(const uint2 v, unsigned short (&h)[4]) {
+  asm("mov.b32 {%0, %1}, %2;" : "=h"(h[0]), "=h"(h[1]) : "r"(v.x));
+  asm("mov.b32 {%0, %1}, %2;" : "=h"(h[2]), "=h"(h[3]) : "r"(v.y));
+}
+
 template <int ST>
 __global__ void __launch_bounds__(MAX_THREADS, 1)
     dwconv3x3_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const DwParams p,
@@ -78,11 +94,10 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + 2 * BUF_MAX);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NBUF * BUF_MAX);
 
   if (threadIdx.x == 0) {
-    gb::mbar_init(&full[0], 1);
-    gb::mbar_init(&full[1], 1);
+    for (int i = 0; i < NBUF; ++i) gb::mbar_init(&full[i], 1);
     gb::fence_barrier_init();
     gb::tma_prefetch_desc(&tm_x);
   }
@@ -109,58 +124,68 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
         : "memory");
   };
 
-  long long b = blockIdx.x;
-  if (threadIdx.x == 0 && b < p.nblocks) issue(b, 0);
+  // ring of NBUF buffers: block i of this CTA lives in buffer i % NBUF; the
+  // load of block i + NBUF - 1 is issued before block i is computed
+  const long long first = blockIdx.x, step = gridDim.x;
+  if (threadIdx.x == 0)
+    for (int i = 0; i < NBUF - 1; ++i)
+      if (first + i * step < p.nblocks) issue(first + i * step, i);
   int it = 0;
   bool ok = true;
   const int groups = p.cb / 4;
-  const int items = p.owt * groups;
-  for (; b < p.nblocks; b += gridDim.x, ++it) {
-    const int buf = it & 1;
-    const long long nb = b + gridDim.x;
-    if (threadIdx.x == 0 && nb < p.nblocks) issue(nb, buf ^ 1);
-    if (!gb::mbar_wait_bounded(&full[buf], (it >> 1) & 1, p.wait_ns, p.err)) ok = false;
+  const int items = gb_items(p);
+  unsigned short wr[9][4];  // this thread's weights (kept while its work item is unchanged)
+  float bz[4];
+  int w_item = -1, w_cs = -1;
+  for (long long b = first; b < p.nblocks; b += step, ++it) {
+    const int buf = it % NBUF;
+    const long long nb = b + (NBUF - 1) * step;
+    if (threadIdx.x == 0 && nb < p.nblocks) issue(nb, (it + NBUF - 1) % NBUF);
+    const uint32_t parity = (uint32_t)((it / NBUF) & 1);
+    if (!gb::mbar_wait_bounded(&full[buf], parity, p.wait_ns, p.err)) ok = false;
     if (!__syncthreads_and(ok)) {
-      // a wait ran out: let the loads this CTA issued land before it exits
-      if (threadIdx.x == 0) {
-        gb::mbar_wait_bounded(&full[buf], (it >> 1) & 1, p.wait_ns, p.err);
-        if (nb < p.nblocks)
-          gb::mbar_wait_bounded(&full[buf ^ 1], ((it + 1) >> 1) & 1, p.wait_ns, p.err);
-      }
+      // a wait ran out: let every load this CTA issued land before it exits
+      if (threadIdx.x == 0)
+        for (int i = 0; i < NBUF; ++i) {
+          const int k = it + i;
+          if (first + (long long)k * step < p.nblocks)
+            gb::mbar_wait_bounded(&full[k % NBUF], (uint32_t)((k / NBUF) & 1), p.wait_ns, p.err);
+        }
       break;
     }
     int n, cs, rb, cb;
     block_coords(b, n, cs, rb, cb);
     const uint8_t* tile = smem + buf * BUF_MAX;
-    // work items: (4-channel group g, output column j), g fastest
+    // work items: (4-channel group g, pair of output columns j0, j0 + 1), g fastest
     for (int item = threadIdx.x; item < items; item += blockDim.x) {
       const int g = item % groups;
-      const int j = item / groups;
+      const int j0 = 2 * (item / groups);
       const int c = cs * p.cb + g * 4;
-      const int ow = cb * p.owt + j;
-      if (c >= p.C || ow >= p.OW) continue;
-      f32x2 wr[9][2];
+      const int ow0 = cb * p.owt + j0;
+      if (c >= p.C || ow0 >= p.OW || j0 >= p.owt) continue;
+      const bool two = j0 + 1 < p.owt && ow0 + 1 < p.OW;
+      if (item != w_item || cs != w_cs) {  // weights and bias of these 4 channels
 #pragma unroll
-      for (int k = 0; k < 9; ++k) {
-        const uint2 v = __ldg(reinterpret_cast<const uint2*>(w9c + (size_t)k * p.C + c));
-        wr[k][0] = bf16x2_to_f32x2(v.x);
-        wr[k][1] = bf16x2_to_f32x2(v.y);
+        for (int k = 0; k < 9; ++k)
+          split4(__ldg(reinterpret_cast<const uint2*>(w9c + (size_t)k * p.C + c)), wr[k]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) bz[q] = bias ? __ldg(bias + c + q) : 0.f;
+        w_item = item;
+        w_cs = cs;
       }
-      f32x2 bz[2];
-      bz[0] = bias ? pack2(__ldg(bias + c), __ldg(bias + c + 1)) : pack2(0.f, 0.f);
-      bz[1] = bias ? pack2(__ldg(bias + c + 2), __ldg(bias + c + 3)) : pack2(0.f, 0.f);
-      const int lc = j * ST;  // tile-local input column of tap s = 0
-      auto ld = [&](int row, int s, f32x2* f) {
-        const uint2 v = *reinterpret_cast<const uint2*>(
-            tile + ((size_t)(row * p.iw + lc + s) * p.cb + g * 4) * 2);
-        f[0] = bf16x2_to_f32x2(v.x);
-        f[1] = bf16x2_to_f32x2(v.y);
+      // tile-local input columns of the pair: j0*ST + s (first), (j0+1)*ST + s (second)
+      constexpr int NC = ST + 3;  // distinct input columns the two outputs read
+      const int lc = j0 * ST;
+      auto ld = [&](int row, int col, unsigned short (&h)[4]) {
+        split4(*reinterpret_cast<const uint2*>(
+                   tile + ((size_t)(row * p.iw + lc + col) * p.cb + g * 4) * 2),
+               h);
       };
-      f32x2 win[3][3][2];  // [slot][s][pair]; input row rho lives in slot rho % 3
+      unsigned short win[3][NC][4];  // bf16 window; input row rho lives in slot rho % 3
 #pragma unroll
       for (int i = 0; i < 3; ++i)
 #pragma unroll
-        for (int s = 0; s < 3; ++s) ld(i, s, win[i][s]);
+        for (int cc = 0; cc < NC; ++cc) ld(i, cc, win[i][cc]);
 #pragma unroll
       for (int k = 0; k < Cf::RB; ++k) {
         const int oh = rb * Cf::RB + k;
@@ -170,50 +195,61 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
           for (int q = 0; q < ST; ++q) {
             const int rho = (k - 1) * ST + 3 + q;
 #pragma unroll
-            for (int s = 0; s < 3; ++s) ld(rho, s, win[rho % 3][s]);
+            for (int cc = 0; cc < NC; ++cc) ld(rho, cc, win[rho % 3][cc]);
           }
         }
-        f32x2 acc[2] = {bz[0], bz[1]};
+        float acc[2][4];
+#pragma unroll
+        for (int o = 0; o < 2; ++o)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[o][q] = bz[q];
 #pragma unroll
         for (int i = 0; i < 3; ++i) {
           const int sl = (k * ST + i) % 3;
 #pragma unroll
           for (int s = 0; s < 3; ++s) {
-            ffma2(acc[0], win[sl][s][0], wr[i * 3 + s][0]);
-            ffma2(acc[1], win[sl][s][1], wr[i * 3 + s][1]);
+#pragma unroll
+            for (int o = 0; o < 2; ++o)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) fma_bf16(acc[o][q], win[sl][o * ST + s][q], wr[i * 3 + s][q]);
           }
         }
-        float a[4];
-        const float2 a01 = unpack2(acc[0]), a23 = unpack2(acc[1]);
-        a[0] = a01.x;
-        a[1] = a01.y;
-        a[2] = a23.x;
-        a[3] = a23.y;
-        const size_t off = (((size_t)n * p.OH + oh) * p.OW + ow) * p.C + c;
-        if (res) {
-          const uint2 rv = __ldg(reinterpret_cast<const uint2*>(res + off));
-          a[0] += __uint_as_float(rv.x << 16);
-          a[1] += __uint_as_float(rv.x & 0xffff0000u);
-          a[2] += __uint_as_float(rv.y << 16);
-          a[3] += __uint_as_float(rv.y & 0xffff0000u);
-        }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (p.act >= 1) a[q] = fmaxf(a[q], 0.f);
-          if (p.act == 2) a[q] = fminf(a[q], 6.f);
+        for (int o = 0; o < 2; ++o) {
+          if (o == 1 && !two) break;
+          float* a = acc[o];
+          const size_t off = (((size_t)n * p.OH + oh) * p.OW + ow0 + o) * p.C + c;
+          if (res) {
+            const uint2 rv = __ldg(reinterpret_cast<const uint2*>(res + off));
+            a[0] += __uint_as_float(rv.x << 16);
+            a[1] += __uint_as_float(rv.x & 0xffff0000u);
+            a[2] += __uint_as_float(rv.y << 16);
+            a[3] += __uint_as_float(rv.y & 0xffff0000u);
+          }
+          __nv_bfloat162 h0 = __floats2bfloat162_rn(a[0], a[1]);
+          __nv_bfloat162 h1 = __floats2bfloat162_rn(a[2], a[3]);
+          // the activation commutes with the (monotone) rounding to bf16
+          if (p.act >= 1) {
+            const __nv_bfloat162 z = __float2bfloat162_rn(0.f);
+            h0 = __hmax2(h0, z);
+            h1 = __hmax2(h1, z);
+          }
+          if (p.act == 2) {
+            const __nv_bfloat162 six = __float2bfloat162_rn(6.f);
+            h0 = __hmin2(h0, six);
+            h1 = __hmin2(h1, six);
+          }
+          uint2 ov;
+          ov.x = *reinterpret_cast<uint32_t*>(&h0);
+          ov.y = *reinterpret_cast<uint32_t*>(&h1);
+          *reinterpret_cast<uint2*>(y + off) = ov;
         }
-        __nv_bfloat162 h0 = __floats2bfloat162_rn(a[0], a[1]);
-        __nv_bfloat162 h1 = __floats2bfloat162_rn(a[2], a[3]);
-        uint2 o;
-        o.x = *reinterpret_cast<uint32_t*>(&h0);
-        o.y = *reinterpret_cast<uint32_t*>(&h1);
-        *reinterpret_cast<uint2*>(y + off) = o;
       }
     }
     __syncthreads();  // the buffer is free for the load issued next iteration
   }
-  // On normal exit every issued load has been waited for: the last iteration
-  // issues none, because its successor index is past the block list.
+  // On normal exit every issued load has been waited for: a load is issued
+  // only for a block index inside the list, and every such block is processed.
 }
 
 // [C][3][3] -> [9][C]
@@ -273,8 +309,7 @@ cudaError_t launch_st(const gbconv_desc_s& d, const void* x, const void* w, cons
   if (e != cudaSuccess) return e;
   const long long grid = std::min<long long>(p.nblocks, gb_num_sms());
   // threads: the block's work items split into equal rounds of <= MAX_THREADS
-  const int groups = p.cb / 4;
-  const int items = p.owt * groups;
+  const int items = gb_items(p);
   const int rounds = gb_ceil_div(items, MAX_THREADS);
   const int threads = gb_ceil_div(gb_ceil_div(items, rounds), 32) * 32;
   dwconv3x3_tma_kernel<ST><<<(unsigned)grid, threads, Cf::SMEM, st>>>(
