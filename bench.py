@@ -453,8 +453,11 @@ class ResNet50W(Workload):
         self.xh = torch.from_numpy(x).pin_memory()
         self.x = self.xh.to(dev)
         self.out = self.net.forward(self.x)
+        self.graph = not getattr(args, "no_graph", False)
+        if self.graph:  # one CUDA-graph launch per forward (57 kernels inside)
+            self.out = self.net.capture(self.x)
         self.yh = torch.empty((self.N, 1000), dtype=torch.bfloat16).pin_memory()
-        self.algo_name = "Fast-Run per layer"
+        self.algo_name = "Fast-Run per layer" + (", CUDA graph" if self.graph else "")
         counts = {}
         for a in self.net.algos.values():
             counts[a] = counts.get(a, 0) + 1
@@ -462,7 +465,7 @@ class ResNet50W(Workload):
 
     def groups(self):
         def run():
-            self.out = self.net.forward(self.x)
+            self.out = self.net.replay() if self.graph else self.net.forward(self.x)
         return [("resnet50_forward", run, self.net.flops(), 0, "tensor")]
 
     def layer_breakdown(self, reps=5):
@@ -616,6 +619,8 @@ def main():
                     help="load the Fast-Run map from this file if it exists (skipping "
                          "selection), else select and save it there")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="resnet50: launch layer by layer instead of replaying a CUDA graph")
     ap.add_argument("--cpu-images", type=int, default=8)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

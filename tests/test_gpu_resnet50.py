@@ -51,3 +51,27 @@ def test_resnet50_layerwise_parity():
     ap = ol.global_avgpool(nhwc_to_nchw(t[net.specs[-2].dst]))
     np.testing.assert_allclose(t["pool5"].reshape(N, 2048), ap, rtol=1e-2, atol=1e-2)
     assert logits.shape == (N, 1000) and torch.isfinite(logits.float()).all()
+
+
+def test_resnet50_cuda_graph_replay_matches_eager():
+    """A captured forward replays to the same logits as the eager forward, and
+    picks up new input values written into the captured input buffer."""
+    torch = need_gpu()
+    from cnn_convolution_gemm_gb300 import synth
+    from cnn_convolution_gemm_gb300.resnet50 import ResNet50
+    dev = torch.device("cuda:0")
+    net = ResNet50(2, dev, seed=4, algo="auto")
+    x = torch.from_numpy(synth.normal((2, 3, 224, 224), 1.0, 6)).to(dev)
+    eager = net.forward(x).clone()
+    out = net.capture(x.clone())
+    net._graph_x.copy_(x)
+    got = net.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(got, eager)
+    x2 = torch.from_numpy(synth.normal((2, 3, 224, 224), 1.0, 7)).to(dev)
+    eager2 = net.forward(x2).clone()
+    net._graph_x.copy_(x2)
+    got2 = net.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(got2, eager2) and not torch.equal(got2, eager)
+    del out
