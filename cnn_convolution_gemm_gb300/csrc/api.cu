@@ -213,7 +213,8 @@ extern "C" conv_status_t conv_desc_get_output_dims(conv_desc_t d, int* OH, int* 
 
 static const char* const kAlgoNames[CONV_ALGO_COUNT] = {
     "direct", "igemm_tc_n64", "igemm_tc_n128", "igemm_tc_n256",
-    "winograd_f2x2_3x3", "winograd_f6x6_3x3", "depthwise3x3", "int8_igemm_mma"};
+    "winograd_f2x2_3x3", "winograd_f6x6_3x3", "depthwise3x3", "int8_igemm_mma",
+    "int8_igemm_tc"};
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -264,6 +265,15 @@ static bool applicable(const gbconv_desc_s& d, int algo, const char** why) {
       if (d.groups != 1) return *why = "needs groups == 1", false;
       if (d.C % 16 || d.K % 16) return *why = "needs C and K multiples of 16", false;
       return true;
+    case CONV_ALGO_INT8_TC:
+      if (d.dtype != CONV_INT8 || !nhwc) return *why = "needs int8 NHWC", false;
+      if (!d.scale) return *why = "int8 needs a requant scale", false;
+      if (d.groups != 1 || d.R != d.S) return *why = "needs groups == 1, square kernel", false;
+      if (d.C % 16 || d.K % 8) return *why = "needs C % 16 == 0 and K % 8 == 0", false;
+      if (d.stride > 8 || d.pad > 128 || d.pad - d.dil * (d.R - 1) < -128)
+        return *why = "stride/padding outside the TMA im2col range", false;
+      if ((long long)d.N * d.OH * d.OW >= (1LL << 31)) return *why = "N*OH*OW >= 2^31", false;
+      return true;
     default:
       return *why = "unknown algorithm", false;
   }
@@ -293,10 +303,13 @@ extern "C" conv_status_t conv_algo_info(conv_desc_t d, int i, conv_algo_t* algo,
 // channels, the depthwise kernel for depthwise layers, im2col-GEMM otherwise,
 // direct for what nothing else covers.
 static int heuristic(const gbconv_desc_s& d) {
-  if (d.dtype == CONV_INT8)
+  if (d.dtype == CONV_INT8) {
+    if (implemented(CONV_ALGO_INT8_TC) && applicable(d, CONV_ALGO_INT8_TC, nullptr))
+      return CONV_ALGO_INT8_TC;
     return implemented(CONV_ALGO_INT8_MMA) && applicable(d, CONV_ALGO_INT8_MMA, nullptr)
                ? CONV_ALGO_INT8_MMA
                : CONV_ALGO_DIRECT;
+  }
   if (implemented(CONV_ALGO_DEPTHWISE) && applicable(d, CONV_ALGO_DEPTHWISE, nullptr))
     return CONV_ALGO_DEPTHWISE;
   const int order[] = {CONV_ALGO_IGEMM_N256, CONV_ALGO_IGEMM_N128, CONV_ALGO_IGEMM_N64};
@@ -366,6 +379,7 @@ extern "C" conv_status_t conv_workspace_size(conv_desc_t d, conv_algo_t algo, si
   *bytes = 0;
   if (a == CONV_ALGO_WINO_F2 || a == CONV_ALGO_WINO_F6)
     *bytes = winograd_workspace_bytes(*d, a == CONV_ALGO_WINO_F2 ? 2 : 6);
+  if (a == CONV_ALGO_INT8_TC) *bytes = int8_tc_workspace_bytes(*d);
   return ok_status();
 }
 
@@ -384,6 +398,7 @@ extern "C" conv_status_t conv_weights_packed_size(conv_desc_t d, conv_algo_t alg
                          : (size_t)d->K * d->R * d->S * Cp64 * 2;
       break;
     case CONV_ALGO_INT8_MMA: *bytes = (size_t)d->K * d->R * d->S * Cp64; break;
+    case CONV_ALGO_INT8_TC: *bytes = int8_tc_packed_bytes(*d); break;
     case CONV_ALGO_WINO_F2: *bytes = winograd_packed_bytes(*d, 2); break;
     case CONV_ALGO_WINO_F6: *bytes = winograd_packed_bytes(*d, 6); break;
     default: *bytes = user_weight_bytes(*d); break;
@@ -405,6 +420,7 @@ extern "C" conv_status_t conv_weights_prepack(conv_desc_t d, conv_algo_t algo, c
     case CONV_ALGO_IGEMM_N128:
     case CONV_ALGO_IGEMM_N256: e = launch_pack_igemm_weights(*d, w, wpack, s); break;
     case CONV_ALGO_INT8_MMA: e = launch_pack_int8_weights(*d, w, wpack, s); break;
+    case CONV_ALGO_INT8_TC: e = launch_pack_int8_tc_weights(*d, w, wpack, s); break;
     case CONV_ALGO_DEPTHWISE: e = launch_pack_dw_weights(*d, w, wpack, s); break;
     case CONV_ALGO_WINO_F2: e = launch_winograd_filter_transform(*d, 2, w, wpack, s); break;
     case CONV_ALGO_WINO_F6: e = launch_winograd_filter_transform(*d, 6, w, wpack, s); break;
@@ -439,6 +455,15 @@ static conv_status_t fwd_impl(const gbconv_desc_s& d, const void* x, const void*
     case CONV_ALGO_INT8_MMA:
       e = launch_igemm_int8(d, x, wpack, static_cast<const int32_t*>(bias), y, s);
       break;
+    case CONV_ALGO_INT8_TC: {
+      const size_t need = int8_tc_workspace_bytes(d);
+      if (!ws || ws_bytes < need)
+        return gb_fail(CONV_ERR_WORKSPACE, "workspace of %zu bytes needed", need);
+      if (reinterpret_cast<uintptr_t>(ws) & 255u)
+        return gb_fail(CONV_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+      e = launch_int8_tc(d, x, wpack, static_cast<const int32_t*>(bias), y, ws, err, wait_ns, s);
+      break;
+    }
     case CONV_ALGO_WINO_F2:
     case CONV_ALGO_WINO_F6: {
       const int m = a == CONV_ALGO_WINO_F2 ? 2 : 6;
@@ -770,6 +795,7 @@ static bool implemented(int algo) {
     case CONV_ALGO_WINO_F2:
     case CONV_ALGO_WINO_F6:
     case CONV_ALGO_INT8_MMA:
+    case CONV_ALGO_INT8_TC:
       return true;
     default:
       return false;

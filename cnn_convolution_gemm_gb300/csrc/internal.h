@@ -52,9 +52,19 @@ cudaError_t launch_direct(const gbconv_desc_s& d, const void* x, const void* w, 
 // Implicit GEMM on tcgen05 (bf16 NHWC, groups 1).  wpack: [K][R*S][Cp] bf16,
 // Cp = C rounded up to 64, zero padded.
 int igemm_block_n(int algo);
+// Split-K request: ksplit > 1 cuts the reduction into ranges of kchunk k-steps
+// (64 channels of one filter tap each) and writes fp32 partial sums to
+// part[ksplit][N*OH*OW][K] instead of running the epilogue.
+struct IgemmSplit {
+  int ksplit = 1;
+  int kchunk = 0;
+  float* part = nullptr;
+};
+int igemm_kiters(const gbconv_desc_s& d);
 cudaError_t launch_igemm_bf16(const gbconv_desc_s& d, int block_n, const void* x,
                               const void* wpack, const float* bias, const void* res, void* y,
-                              int* err, unsigned long long wait_ns, cudaStream_t st);
+                              int* err, unsigned long long wait_ns, cudaStream_t st,
+                              const IgemmSplit& split = IgemmSplit());
 cudaError_t launch_pack_igemm_weights(const gbconv_desc_s& d, const void* w, void* wpack,
                                       cudaStream_t st);
 // Batched GEMM on the same tcgen05 pipeline: out[b][m][n] (fp32) =
@@ -77,6 +87,16 @@ cudaError_t launch_igemm_int8(const gbconv_desc_s& d, const void* x, const void*
                               const int32_t* bias, void* y, cudaStream_t st);
 cudaError_t launch_pack_int8_weights(const gbconv_desc_s& d, const void* w, void* wpack,
                                      cudaStream_t st);
+
+// int8 on tcgen05 with bf16 as the carrier (exact split-K, see k_int8_tc.cu).
+// wpack: [K][R*S][Cp] bf16.
+size_t int8_tc_workspace_bytes(const gbconv_desc_s& d);
+size_t int8_tc_packed_bytes(const gbconv_desc_s& d);
+cudaError_t launch_pack_int8_tc_weights(const gbconv_desc_s& d, const void* w, void* wpack,
+                                        cudaStream_t st);
+cudaError_t launch_int8_tc(const gbconv_desc_s& d, const void* x, const void* wpack,
+                           const int32_t* bias, void* y, void* ws, int* err,
+                           unsigned long long wait_ns, cudaStream_t st);
 
 // Winograd F(m x m, 3 x 3), m in {2, 6}.
 size_t winograd_packed_bytes(const gbconv_desc_s& d, int m);

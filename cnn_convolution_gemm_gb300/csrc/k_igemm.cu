@@ -59,6 +59,10 @@ struct IgemmParams {
   // channels, loaded as 8 im2col boxes of 128 pixels x 16 bytes
   int narrow;
   int taps;  // R * S
+  // split-K (conv mode): the reduction is cut into ksplit ranges of kchunk
+  // k-steps; range b writes fp32 partial sums to part[b][M][K] (no epilogue)
+  int ksplit, kchunk;
+  float* part;
 };
 
 enum { MODE_CONV = 0, MODE_BATCHED = 1 };
@@ -139,7 +143,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const int tiles_per_batch = p.m_tiles * p.n_tiles;
-  const int num_tiles = tiles_per_batch * (MODE == MODE_BATCHED ? p.batch : 1);
+  const int num_tiles = tiles_per_batch * (MODE == MODE_BATCHED ? p.batch : p.ksplit);
   const int ohow = p.OH * p.OW;
 
   if (warp == 0) {
@@ -161,8 +165,10 @@ __global__ void __launch_bounds__(192, 1)
           h0 = (rem / p.OW) * p.stride - p.pad;
           w0 = (rem % p.OW) * p.stride - p.pad;
         }
-        int cb = 0, s = 0, r = 0;
-        for (int it = 0; it < p.kiters; ++it) {
+        const int kbeg = MODE == MODE_CONV ? bt * p.kchunk : 0;
+        const int kend = MODE == MODE_CONV ? min(p.kiters, kbeg + p.kchunk) : p.kiters;
+        int cb = kbeg % p.cblocks, s = (kbeg / p.cblocks) % p.S, r = (kbeg / p.cblocks) / p.S;
+        for (int it = kbeg; it < kend; ++it) {
           if (!gb::mbar_wait_bounded(&empty[stage], phase ^ 1, p.wait_ns, p.err)) {
             ok = false;
             break;
@@ -228,7 +234,10 @@ __global__ void __launch_bounds__(192, 1)
         if (!gb::mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, p.wait_ns, p.err)) break;
         gb::tc_fence_after();
         const uint32_t d = tmem_base + acc * BN;
-        for (int it = 0; it < p.kiters; ++it) {
+        const int bt = t / tiles_per_batch;
+        const int kbeg = MODE == MODE_CONV ? bt * p.kchunk : 0;
+        const int kend = MODE == MODE_CONV ? min(p.kiters, kbeg + p.kchunk) : p.kiters;
+        for (int it = kbeg; it < kend; ++it) {
           if (!gb::mbar_wait_bounded(&full[stage], phase, p.wait_ns, p.err)) {
             ok = false;
             break;
@@ -244,7 +253,8 @@ __global__ void __launch_bounds__(192, 1)
                 (MODE == MODE_CONV && p.narrow)
                     ? gb::noswz_kmajor_desc(a0 + k * 2 * (BM * 16), BM * 16, 128)
                     : gb::sw128_kmajor_desc(a0 + k * 32);
-            gb::tc_mma_f16(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), IDESC, (it | k) != 0);
+            gb::tc_mma_f16(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), IDESC,
+                           (it > kbeg || k > 0) ? 1u : 0u);
           }
           gb::tc_commit(&empty[stage]);
           if (++stage == C::STAGES) {
@@ -290,7 +300,7 @@ __global__ void __launch_bounds__(192, 1)
           "r"(mt2 * BM + q * 32), "r"(gb::smem_u32(bar))
           : "memory");
     };
-    const bool has_res = MODE == MODE_CONV && p.res != nullptr;
+    const bool has_res = MODE == MODE_CONV && p.res != nullptr && p.part == nullptr;
     int pending = -1;  // box with a residual load not yet waited for
     if (has_res && (int)blockIdx.x < num_tiles) {
       if (lane == 0) fetch_res(blockIdx.x, 0, 0);
@@ -305,7 +315,8 @@ __global__ void __launch_bounds__(192, 1)
       const long long m = (long long)mt * BM + q * 32 + lane;
       const bool row_ok = m < p.M;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-      if (MODE == MODE_BATCHED) {
+      if (MODE == MODE_BATCHED || p.part) {
+        float* outp = MODE == MODE_BATCHED ? p.out_f32 : p.part;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 16) {
           uint32_t r[16];
@@ -313,7 +324,7 @@ __global__ void __launch_bounds__(192, 1)
           gb::tmem_ld_wait();
           const int n = nt * BN + c0;
           if (row_ok && n < p.K) {
-            float4* dst = reinterpret_cast<float4*>(p.out_f32 + ((size_t)bt * p.M + m) * p.K + n);
+            float4* dst = reinterpret_cast<float4*>(outp + ((size_t)bt * p.M + m) * p.K + n);
             const int nq = (p.K - n) >= 16 ? 4 : 2;
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq)
@@ -425,7 +436,7 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
     if (MODE == MODE_CONV && lane == 0) {
-      gb::bulk_wait_all();  // stores done before exit
+      gb::bulk_wait_all();  // stores done before exit (none were issued in partial mode)
       // after a wait ran out, a residual load may still be landing
       if (pending >= 0)
         gb::mbar_wait_bounded(&rbar[q * 2 + pending], (rphase >> pending) & 1, p.wait_ns, p.err);
@@ -458,7 +469,7 @@ __global__ void pack_igemm_weights_kernel(const __nv_bfloat16* __restrict__ w,
 template <int BN, bool LIGHT>
 cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, const float* bias,
                       const void* res, void* y, int* err, unsigned long long wait_ns,
-                      cudaStream_t st) {
+                      cudaStream_t st, const IgemmSplit& split) {
   using Cf = Cfg<BN, LIGHT>;
   const bool narrow = d.C == 8;
   const int Cp = gb_ceil_div(d.C, BK) * BK;
@@ -487,6 +498,9 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   p.y = static_cast<__nv_bfloat16*>(y);
   p.err = err;
   p.wait_ns = wait_ns;
+  p.ksplit = split.ksplit > 1 ? split.ksplit : 1;
+  p.kchunk = split.ksplit > 1 ? split.kchunk : p.kiters;
+  p.part = split.part;
 
   CUtensorMap tmx, tmw;
   {
@@ -536,7 +550,7 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   cudaError_t e = cudaFuncSetAttribute(igemm_bf16_tc_kernel<BN, MODE_CONV, LIGHT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
   if (e != cudaSuccess) return e;
-  const int tiles = p.m_tiles * p.n_tiles;
+  const int tiles = p.m_tiles * p.n_tiles * p.ksplit;
   const int slots = gb_num_sms() * (LIGHT ? 2 : 1);
   const int grid = tiles < slots ? tiles : slots;
   igemm_bf16_tc_kernel<BN, MODE_CONV, LIGHT><<<grid, 192, Cf::SMEM, st>>>(tmx, tmw, tmy, tmr, p);
@@ -605,20 +619,27 @@ int igemm_block_n(int algo) {
 
 cudaError_t launch_igemm_bf16(const gbconv_desc_s& d, int block_n, const void* x,
                               const void* wpack, const float* bias, const void* res, void* y,
-                              int* err, unsigned long long wait_ns, cudaStream_t st) {
+                              int* err, unsigned long long wait_ns, cudaStream_t st,
+                              const IgemmSplit& split) {
   // short reductions (1x1 layers up to 512 channels) are bound by the epilogue
   // and memory, not by the operand pipeline: run two shallow CTAs per SM
-  const bool light = d.C != 8 && d.R * d.S * gb_ceil_div(d.C, BK) <= 8;
+  const int kiters = d.C == 8 ? gb_ceil_div(d.R * d.S, 8) : d.R * d.S * gb_ceil_div(d.C, BK);
+  const int kper = split.ksplit > 1 ? split.kchunk : kiters;
+  const bool light = d.C != 8 && kper <= 8;
   switch (block_n) {
     case 64:
-      return light ? launch_bn<64, true>(d, x, wpack, bias, res, y, err, wait_ns, st)
-                   : launch_bn<64, false>(d, x, wpack, bias, res, y, err, wait_ns, st);
+      return light ? launch_bn<64, true>(d, x, wpack, bias, res, y, err, wait_ns, st, split)
+                   : launch_bn<64, false>(d, x, wpack, bias, res, y, err, wait_ns, st, split);
     case 128:
-      return light ? launch_bn<128, true>(d, x, wpack, bias, res, y, err, wait_ns, st)
-                   : launch_bn<128, false>(d, x, wpack, bias, res, y, err, wait_ns, st);
-    case 256: return launch_bn<256, false>(d, x, wpack, bias, res, y, err, wait_ns, st);
+      return light ? launch_bn<128, true>(d, x, wpack, bias, res, y, err, wait_ns, st, split)
+                   : launch_bn<128, false>(d, x, wpack, bias, res, y, err, wait_ns, st, split);
+    case 256: return launch_bn<256, false>(d, x, wpack, bias, res, y, err, wait_ns, st, split);
     default: return cudaErrorInvalidValue;
   }
+}
+
+int igemm_kiters(const gbconv_desc_s& d) {
+  return d.C == 8 ? gb_ceil_div(d.R * d.S, 8) : d.R * d.S * gb_ceil_div(d.C, BK);
 }
 
 cudaError_t launch_batched_gemm_tc(int batch, int M, int N, int Kred, const void* A,

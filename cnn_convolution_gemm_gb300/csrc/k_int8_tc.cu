@@ -1,0 +1,158 @@
+// Exact int8 convolution on the tcgen05 tensor cores, bf16 as the carrier.
+//
+// sm_103a's tcgen05.mma has no int8 kind.  Every int8 value (|v| <= 128) is
+// exact in bf16 and every product of two of them (|p| <= 16384) is exact in the
+// fp32 accumulator, and a sum of integers stays exact in fp32 while its
+// magnitude is below 2^24.  So the reduction is cut into chunks of at most
+// 1024 products per output (16 k-steps of 64 channels: 1024 * 127^2 < 2^24),
+// each chunk runs on the bf16 tcgen05 pipeline (split-K mode of the implicit
+// GEMM kernel) and writes its exact fp32 partial sums, and a final pass sums the
+// chunks in int32 and applies the int8 epilogue of the MegEngine Beta report's
+// native int8 inference: + int32 bias, fp32 requantisation
+// q = clamp(rne(fp32(acc + bias) * scale[k]), -128, 127), ReLU.
+//
+// Steps per call: int8 -> bf16 copy of the activations (workspace), split-K
+// implicit GEMM into fp32 partials (workspace), reduction + requant -> int8.
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "internal.h"
+
+namespace {
+
+constexpr int KCHUNK_MAX = 16;  // k-steps of 64 products per exact fp32 chunk
+
+// bf16 has 8 significant bits: every int8 value converts exactly.
+__global__ void int8_to_bf16_kernel(const int8_t* __restrict__ x, __nv_bfloat16* __restrict__ y,
+                                    long long n16) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n16;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int4 v = reinterpret_cast<const int4*>(x)[i];
+    const int8_t* b = reinterpret_cast<const int8_t*>(&v);
+    uint4 o[2];
+    uint32_t* ou = reinterpret_cast<uint32_t*>(o);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      __nv_bfloat162 h = __floats2bfloat162_rn((float)b[2 * j], (float)b[2 * j + 1]);
+      ou[j] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    reinterpret_cast<uint4*>(y)[2 * i] = o[0];
+    reinterpret_cast<uint4*>(y)[2 * i + 1] = o[1];
+  }
+}
+
+// int8 [K][RS][C] -> bf16 [K][RS][Cp], zero padded channels
+__global__ void pack_int8_as_bf16_kernel(const int8_t* __restrict__ w,
+                                         __nv_bfloat16* __restrict__ wp, int K, int RS, int C,
+                                         int Cp) {
+  const long long total = (long long)K * RS * Cp;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int c = (int)(i % Cp);
+    const long long krs = i / Cp;
+    wp[i] = __float2bfloat16_rn(c < C ? (float)w[krs * C + c] : 0.f);
+  }
+}
+
+// y[m][n] = requant(sum_b part[b][m][n] + bias[n]); 4 channels per thread
+__global__ void reduce_requant_kernel(const float* __restrict__ part, int ksplit, long long MK,
+                                      int K, const int32_t* __restrict__ bias,
+                                      const float* __restrict__ scale, int relu,
+                                      int8_t* __restrict__ y) {
+  const long long n4 = MK / 4;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
+       i += (long long)gridDim.x * blockDim.x) {
+    int acc[4] = {0, 0, 0, 0};
+    for (int b = 0; b < ksplit; ++b) {
+      const float4 v = reinterpret_cast<const float4*>(part + (size_t)b * MK)[i];
+      acc[0] += __float2int_rn(v.x);  // exact: each partial is an integer below 2^24
+      acc[1] += __float2int_rn(v.y);
+      acc[2] += __float2int_rn(v.z);
+      acc[3] += __float2int_rn(v.w);
+    }
+    const int n0 = (int)((i * 4) % K);
+    char4 o;
+    int8_t* ob = reinterpret_cast<int8_t*>(&o);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int t = acc[j] + (bias ? bias[n0 + j] : 0);
+      int q = __float2int_rn(__fmul_rn(__int2float_rn(t), scale[n0 + j]));
+      q = q > 127 ? 127 : (q < -128 ? -128 : q);
+      if (relu && q < 0) q = 0;
+      ob[j] = (int8_t)q;
+    }
+    reinterpret_cast<char4*>(y)[i] = o;
+  }
+}
+
+struct Plan {
+  int block_n, kiters, ksplit, kchunk;
+  size_t x_bytes, part_bytes;
+};
+
+Plan make_plan(const gbconv_desc_s& d) {
+  Plan p{};
+  p.block_n = d.K > 128 ? 256 : (d.K > 64 ? 128 : 64);
+  p.kiters = igemm_kiters(d);
+  const long long M = (long long)d.N * d.OH * d.OW;
+  const long long tiles = gb_ceil_div_ll(M, 128) * gb_ceil_div(d.K, p.block_n);
+  int ks = gb_ceil_div(p.kiters, KCHUNK_MAX);  // exactness bound
+  // more ranges when the tile grid alone would leave SMs idle
+  while ((long long)ks * tiles < gb_num_sms() && gb_ceil_div(p.kiters, ks + 1) >= 4) ++ks;
+  p.kchunk = gb_ceil_div(p.kiters, ks);
+  p.ksplit = gb_ceil_div(p.kiters, p.kchunk);
+  p.x_bytes = ((size_t)d.N * d.H * d.W * d.C * 2 + 255) / 256 * 256;
+  p.part_bytes = (size_t)p.ksplit * M * d.K * 4;
+  return p;
+}
+
+int grid_for(long long n) { return (int)std::min<long long>(gb_ceil_div_ll(n, 256), 148LL * 32); }
+
+}  // namespace
+
+size_t int8_tc_workspace_bytes(const gbconv_desc_s& d) {
+  const Plan p = make_plan(d);
+  return p.x_bytes + p.part_bytes;
+}
+
+size_t int8_tc_packed_bytes(const gbconv_desc_s& d) {
+  return (size_t)d.K * d.R * d.S * gb_ceil_div(d.C, 64) * 64 * 2;
+}
+
+cudaError_t launch_pack_int8_tc_weights(const gbconv_desc_s& d, const void* w, void* wpack,
+                                        cudaStream_t st) {
+  const int Cp = gb_ceil_div(d.C, 64) * 64;
+  const long long total = (long long)d.K * d.R * d.S * Cp;
+  pack_int8_as_bf16_kernel<<<grid_for(total), 256, 0, st>>>(
+      static_cast<const int8_t*>(w), static_cast<__nv_bfloat16*>(wpack), d.K, d.R * d.S, d.C, Cp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_int8_tc(const gbconv_desc_s& d, const void* x, const void* wpack,
+                           const int32_t* bias, void* y, void* ws, int* err,
+                           unsigned long long wait_ns, cudaStream_t st) {
+  const Plan pl = make_plan(d);
+  __nv_bfloat16* xb = static_cast<__nv_bfloat16*>(ws);
+  float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.x_bytes);
+  const long long n16 = (long long)d.N * d.H * d.W * d.C / 16;
+  int8_to_bf16_kernel<<<grid_for(n16), 256, 0, st>>>(static_cast<const int8_t*>(x), xb, n16);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  gbconv_desc_s db = d;  // the same convolution over the bf16 copy
+  db.dtype = CONV_BF16;
+  db.act = CONV_ACT_NONE;
+  db.has_residual = 0;
+  IgemmSplit sp;
+  sp.ksplit = pl.ksplit;
+  sp.kchunk = pl.kchunk;
+  sp.part = part;
+  e = launch_igemm_bf16(db, pl.block_n, xb, wpack, nullptr, nullptr, y, err, wait_ns, st, sp);
+  if (e != cudaSuccess) return e;
+  const long long MK = (long long)d.N * d.OH * d.OW * d.K;
+  reduce_requant_kernel<<<grid_for(MK / 4), 256, 0, st>>>(part, pl.ksplit, MK, d.K, bias, d.scale,
+                                                          d.act == CONV_ACT_RELU ? 1 : 0,
+                                                          static_cast<int8_t*>(y));
+  return cudaGetLastError();
+}

@@ -71,8 +71,9 @@ typedef int conv_algo_t;
 #define CONV_ALGO_WINO_F2 4        /* Winograd F(2x2,3x3)                               */
 #define CONV_ALGO_WINO_F6 5        /* Winograd F(6x6,3x3)                               */
 #define CONV_ALGO_DEPTHWISE 6      /* depthwise 3x3 (groups == C == K)                  */
-#define CONV_ALGO_INT8_MMA 7       /* int8 implicit GEMM, exact int32 accumulate        */
-#define CONV_ALGO_COUNT 8
+#define CONV_ALGO_INT8_MMA 7       /* int8 implicit GEMM on mma.sync, exact int32 acc.  */
+#define CONV_ALGO_INT8_TC 8        /* int8 on tcgen05 via exact bf16 chunks (workspace) */
+#define CONV_ALGO_COUNT 9
 
 /* ---- descriptor --------------------------------------------------------- */
 

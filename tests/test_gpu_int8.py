@@ -8,6 +8,8 @@ from tests.gpu_util import need_gpu, nchw_to_nhwc, nhwc_to_nchw
 
 pytestmark = pytest.mark.gpu
 INT8_MMA = 7
+INT8_TC = 8
+ALGOS = [INT8_MMA, INT8_TC]
 
 
 def _run(torch, N, C, H, W, K, R, stride, pad, relu=True, bias=True, seed=0, algo=INT8_MMA):
@@ -32,11 +34,12 @@ def _run(torch, N, C, H, W, K, R, stride, pad, relu=True, bias=True, seed=0, alg
     return y.cpu().numpy(), nchw_to_nhwc(ref)
 
 
+@pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("C,HW", [(64, 56), (128, 28), (256, 14), (512, 7)])
-def test_int8_resnet_stage_shapes_full_batch(C, HW):
+def test_int8_resnet_stage_shapes_full_batch(C, HW, algo):
     """The four ResNet-50 stage 3x3 layers at batch 32, every output compared."""
     torch = need_gpu()
-    y, ref = _run(torch, 32, C, HW, HW, C, 3, 1, 1, seed=C)
+    y, ref = _run(torch, 32, C, HW, HW, C, 3, 1, 1, seed=C, algo=algo)
     assert np.array_equal(y, ref), int((y != ref).sum())
 
 
@@ -47,16 +50,19 @@ def test_int8_resnet_stage_shapes_full_batch(C, HW):
     (2, 96, 6, 6, 80, 1, 1, 0, True, False),     # 1x1, no bias, C not a 64 multiple
     (1, 64, 5, 5, 256, 3, 1, 2, True, True),     # pad 2 (many fully padded taps)
 ])
-def test_int8_edge_cases(case):
+@pytest.mark.parametrize("algo", ALGOS)
+def test_int8_edge_cases(case, algo):
     torch = need_gpu()
     N, C, H, W, K, R, st, pad, relu, bias = case
-    y, ref = _run(torch, N, C, H, W, K, R, st, pad, relu, bias, seed=N * C)
+    y, ref = _run(torch, N, C, H, W, K, R, st, pad, relu, bias, seed=N * C, algo=algo)
     assert np.array_equal(y, ref)
 
 
-def test_int8_saturation_extremes():
+@pytest.mark.parametrize("algo", ALGOS)
+def test_int8_saturation_extremes(algo):
     """All +-127 inputs drive the accumulator to its largest magnitude and the
-    requant into saturation on both sides."""
+    requant into saturation on both sides; for the tcgen05 path this is also the
+    worst case of the exact-fp32-chunk bound (every chunk partial near 2^24)."""
     torch = need_gpu()
     from cnn_convolution_gemm_gb300 import binding as B
     from cnn_convolution_gemm_gb300.layer import ConvLayer
@@ -68,7 +74,7 @@ def test_int8_saturation_extremes():
     scale = np.full(K, 1e-3, np.float32)
     layer = ConvLayer(N, C, H, H, K, 3, 3, 1, 1, dtype=B.CONV_INT8,
                       scale=torch.from_numpy(scale).to(dev))
-    layer.prepack(torch.from_numpy(w).to(dev), INT8_MMA)
+    layer.prepack(torch.from_numpy(w).to(dev), algo)
     y = layer(torch.from_numpy(x).to(dev))
     B.conv_sync_status(torch.cuda.current_stream().cuda_stream)
     ref = ol.conv2d_i8(nhwc_to_nchw(x), nhwc_to_nchw(w), None, scale, pad=1, relu=False)
