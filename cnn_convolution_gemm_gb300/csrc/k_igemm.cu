@@ -316,24 +316,34 @@ __global__ void __launch_bounds__(192, 1)
       const bool row_ok = m < p.M;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
       if (MODE == MODE_BATCHED || p.part) {
-        float* outp = MODE == MODE_BATCHED ? p.out_f32 : p.part;
+        // fp32 outputs (batched products, split-K partials): 32-column boxes of
+        // 32 rows staged with the 128-byte swizzle and written by TMA stores
+        // through the fp32 map passed in the tm_r slot
+        const long long m_warp = (long long)mt * BM + q * 32;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 16) {
-          uint32_t r[16];
-          gb::tmem_ld_x16(tbase + c0, r);
+        for (int j = 0; j < BN / 32; ++j) {
+          const int nb0 = nt * BN + j * 32;
+          if (nb0 >= p.K) break;
+          uint8_t* box = sEpi + (q * 2 + (epi_count & 1)) * C::EPI_BOX;
+          if (lane == 0) gb::bulk_wait_read<1>();
+          __syncwarp();
+          uint32_t r[32];
+          gb::tmem_ld_x16(tbase + j * 32, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
+          gb::tmem_ld_x16(tbase + j * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
           gb::tmem_ld_wait();
-          const int n = nt * BN + c0;
-          if (row_ok && n < p.K) {
-            float4* dst = reinterpret_cast<float4*>(outp + ((size_t)bt * p.M + m) * p.K + n);
-            const int nq = (p.K - n) >= 16 ? 4 : 2;
 #pragma unroll
-            for (int qq = 0; qq < 4; ++qq)
-              if (qq < nq)
-                dst[qq] = make_float4(__uint_as_float(r[4 * qq]), __uint_as_float(r[4 * qq + 1]),
-                                      __uint_as_float(r[4 * qq + 2]),
-                                      __uint_as_float(r[4 * qq + 3]));
+          for (int h = 0; h < 8; ++h)
+            *reinterpret_cast<uint4*>(box + lane * 128 + ((h ^ (lane & 7)) << 4)) =
+                make_uint4(r[4 * h], r[4 * h + 1], r[4 * h + 2], r[4 * h + 3]);
+          gb::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            gb::tma_store_3d(&tm_r, box, nb0, (int)m_warp, bt);
+            gb::bulk_commit();
           }
+          ++epi_count;
         }
+        (void)row_ok;
       } else {
         // 64-column sub-blocks: TMEM -> registers (+ bias, residual, act) ->
         // swizzled staging box in shared memory -> TMA store of 32 rows x 64 cols
@@ -435,8 +445,8 @@ __global__ void __launch_bounds__(192, 1)
         acc_phase ^= 1;
       }
     }
-    if (MODE == MODE_CONV && lane == 0) {
-      gb::bulk_wait_all();  // stores done before exit (none were issued in partial mode)
+    if (lane == 0) {
+      gb::bulk_wait_all();  // TMA stores done before exit
       // after a wait ran out, a residual load may still be landing
       if (pending >= 0)
         gb::mbar_wait_bounded(&rbar[q * 2 + pending], (rphase >> pending) & 1, p.wait_ns, p.err);
@@ -537,8 +547,17 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
                         CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  CUtensorMap tmr = tmy;  // residual, same shape and boxes as the output
-  if (res) {
+  CUtensorMap tmr = tmy;  // residual (same shape and boxes as the output), or the
+                          // fp32 partial-sum map in split-K mode
+  if (p.part) {
+    cuuint64_t dims[3] = {(cuuint64_t)d.K, (cuuint64_t)p.M, (cuuint64_t)p.ksplit};
+    cuuint64_t strides[2] = {(cuuint64_t)d.K * 4, (cuuint64_t)p.M * d.K * 4};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (gb_encode_tiled(&tmr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.part, dims, strides, box,
+                        estr, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  } else if (res) {
     cuuint64_t dims[2] = {(cuuint64_t)d.K, (cuuint64_t)p.M};
     cuuint64_t strides[1] = {(cuuint64_t)d.K * 2};
     cuuint32_t box[2] = {64, 32};
@@ -602,7 +621,17 @@ cudaError_t launch_batched_bn(int batch, int M, int N, int Kred, const void* A, 
   if (e != cudaSuccess) return e;
   const long long tiles = (long long)p.m_tiles * p.n_tiles * batch;
   const int grid = tiles < gb_num_sms() ? (int)tiles : gb_num_sms();
-  igemm_bf16_tc_kernel<BN, MODE_BATCHED><<<grid, 192, Cf::SMEM, st>>>(tma, tmb, tma, tma, p);
+  CUtensorMap tmo;  // fp32 products out[b][m][n], 32 x 32 boxes
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)M, (cuuint64_t)batch};
+    cuuint64_t strides[2] = {(cuuint64_t)N * 4, (cuuint64_t)M * N * 4};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (gb_encode_tiled(&tmo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, out, dims, strides, box, estr,
+                        CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  igemm_bf16_tc_kernel<BN, MODE_BATCHED><<<grid, 192, Cf::SMEM, st>>>(tma, tmb, tma, tmo, p);
   return cudaGetLastError();
 }
 

@@ -31,6 +31,7 @@
 #include <algorithm>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace {
 
@@ -159,109 +160,143 @@ __global__ void filter_transform_kernel(const __nv_bfloat16* __restrict__ w, voi
     }
 }
 
-// ---- input transform: V[xi][t][c] = (B^T d B)[xi], two channels per thread -------
+// ---- input transform: V[xi][t][c] = (B^T d B)[xi] ---------------------------------
+//
+// A CTA transforms one strip: image n, tile row ti, up to TWC tiles along the
+// row starting at tile tj0, 64 channels.  One 4-D TMA load brings the strip's
+// alpha input rows x (TWC*m + 2) columns x 64 channels into shared memory, with
+// zeros outside the image (the padding).  A thread then owns one (tile,
+// channel): column transform of the 8 x 8 (4 x 4) patch into registers, row
+// transform, and alpha^2 two-byte stores of V (a warp writes 32 consecutive
+// channels of one V row).
 
-template <typename TT, bool F16>
-__global__ void __launch_bounds__(128)
-    input_transform_kernel(const WinoParams p, const __nv_bfloat16* __restrict__ x,
-                           void* __restrict__ V) {
-  constexpr int A = TT::a, Mo = TT::m;
-  const int cp_per = p.C / 2;
-  const long long T = (long long)p.nb * p.th * p.tw;
-  const long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  if (i >= T * cp_per) return;
-  const int cp = (int)(i % cp_per);
-  const long long t = i / cp_per;
-  const int tj = (int)(t % p.tw);
-  const int ti = (int)((t / p.tw) % p.th);
-  const int n = p.n0 + (int)(t / ((long long)p.tw * p.th));
-  const int h0 = ti * Mo - p.pad, w0 = tj * Mo - p.pad;
-  const __nv_bfloat16* xn = x + (size_t)n * p.H * p.W * p.C + 2 * cp;
-
-  // tmp = B^T d, built column by column
-  float2 tmp[A][A];
-#pragma unroll
-  for (int l = 0; l < A; ++l) {
-    float2 col[A];
-    const int iw = w0 + l;
-#pragma unroll
-    for (int k = 0; k < A; ++k) {
-      const int ih = h0 + k;
-      if (ih >= 0 && ih < p.H && iw >= 0 && iw < p.W) {
-        const __nv_bfloat162 v =
-            *reinterpret_cast<const __nv_bfloat162*>(xn + ((size_t)ih * p.W + iw) * p.C);
-        col[k] = __bfloat1622float2(v);
-      } else {
-        col[k] = make_float2(0.f, 0.f);
-      }
-    }
-#pragma unroll
-    for (int a = 0; a < A; ++a) {
-      float2 v = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int k = 0; k < A; ++k) {
-        v.x = madd(v.x, TT::BT(a, k), col[k].x);
-        v.y = madd(v.y, TT::BT(a, k), col[k].y);
-      }
-      tmp[a][l] = v;
-    }
-  }
-  using Op = OpT<F16>;
-  using T2 = typename Op::T2;
-  T2* out = reinterpret_cast<T2*>(V);
-#pragma unroll
-  for (int a = 0; a < A; ++a)
-#pragma unroll
-    for (int b = 0; b < A; ++b) {
-      float2 v = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int l = 0; l < A; ++l) {
-        v.x = madd(v.x, TT::BT(b, l), tmp[a][l].x);
-        v.y = madd(v.y, TT::BT(b, l), tmp[a][l].y);
-      }
-      out[((size_t)(a * A + b) * T + t) * cp_per + cp] = Op::make(v.x, v.y);
-    }
-}
-
-// ---- output transform: Y = A^T M A (+ bias, residual, act), two channels/thread --
+constexpr int WCB = 64;   // channels per strip
+constexpr int TWC = 16;   // tiles per strip along the row (max)
 
 template <typename TT>
-__global__ void __launch_bounds__(128)
+struct InCfg {
+  static constexpr int IW = TWC * TT::m + 2;                // strip columns
+  static constexpr int BYTES = TT::a * IW * WCB * 2;        // strip bytes
+  static constexpr int SMEM = BYTES + 64 + 128;
+};
+
+template <typename TT, bool F16>
+__global__ void __launch_bounds__(256)
+    input_transform_kernel(const __grid_constant__ CUtensorMap tm_x, const WinoParams p,
+                           void* __restrict__ V, int* err, unsigned long long wait_ns) {
+  constexpr int A = TT::a, Mo = TT::m;
+  using Cf = InCfg<TT>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + Cf::BYTES);
+  const int tblocks = (p.tw + TWC - 1) / TWC;
+  int b = blockIdx.x;
+  const int cblk = b % (p.C / WCB + (p.C % WCB ? 1 : 0));
+  b /= (p.C / WCB + (p.C % WCB ? 1 : 0));
+  const int tjb = b % tblocks;
+  b /= tblocks;
+  const int ti = b % p.th;
+  const int nl = b / p.th;  // image within the chunk
+  const int n = p.n0 + nl;
+  if (threadIdx.x == 0) {
+    gb::mbar_init(bar, 1);
+    gb::fence_barrier_init();
+    gb::mbar_arrive_expect_tx(bar, Cf::BYTES);
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(gb::smem_u32(smem)),
+        "l"(reinterpret_cast<uint64_t>(&tm_x)), "r"(cblk * WCB), "r"(tjb * TWC * Mo - p.pad),
+        "r"(ti * Mo - p.pad), "r"(n), "r"(gb::smem_u32(bar))
+        : "memory");
+  }
+  __syncthreads();
+  const bool ok = gb::mbar_wait_bounded(bar, 0, wait_ns, err);
+  if (!__syncthreads_and(ok)) return;  // the load either landed or the wait ran out
+  const __nv_bfloat16* strip = reinterpret_cast<const __nv_bfloat16*>(smem);
+  const long long T = (long long)p.nb * p.th * p.tw;
+  using Op = OpT<F16>;
+  auto* out = reinterpret_cast<decltype(Op::one(0.f))*>(V);
+  for (int item = threadIdx.x; item < TWC * WCB; item += blockDim.x) {
+    const int c = item % WCB;
+    const int j = item / WCB;
+    const int tj = tjb * TWC + j;
+    const int cg = cblk * WCB + c;
+    if (tj >= p.tw || cg >= p.C) continue;
+    // V = B^T d B accumulated one input row at a time:
+    //   u[i][b] = sum_l d[i][l] BT[b][l];   V[a][b] += BT[a][i] u[i][b]
+    float acc[A][A];
+#pragma unroll
+    for (int a = 0; a < A; ++a)
+#pragma unroll
+      for (int bb = 0; bb < A; ++bb) acc[a][bb] = 0.f;
+#pragma unroll
+    for (int i = 0; i < A; ++i) {
+      asm volatile("" ::: "memory");  // keep one row of loads live at a time
+      float row[A];
+#pragma unroll
+      for (int l = 0; l < A; ++l)
+        row[l] = __bfloat162float(strip[((size_t)i * Cf::IW + j * Mo + l) * WCB + c]);
+      float u[A];
+#pragma unroll
+      for (int bb = 0; bb < A; ++bb) {
+        float v = 0.f;
+#pragma unroll
+        for (int l = 0; l < A; ++l) v = madd(v, TT::BT(bb, l), row[l]);
+        u[bb] = v;
+      }
+#pragma unroll
+      for (int a = 0; a < A; ++a)
+#pragma unroll
+        for (int bb = 0; bb < A; ++bb) acc[a][bb] = madd(acc[a][bb], TT::BT(a, i), u[bb]);
+    }
+    const long long tg = ((long long)nl * p.th + ti) * p.tw + tj;
+    auto* o = out + (size_t)tg * p.C + cg;  // V[0][tg][cg]; one xi plane is T*C apart
+    const size_t plane = (size_t)T * p.C;
+#pragma unroll
+    for (int a = 0; a < A; ++a) {
+      asm volatile("" ::: "memory");
+#pragma unroll
+      for (int bb = 0; bb < A; ++bb) {
+        *o = Op::one(acc[a][bb]);
+        o += plane;
+      }
+    }
+  }
+}
+
+// ---- output transform: Y = A^T M A (+ bias, residual, act), one channel per thread
+
+template <typename TT>
+__global__ void __launch_bounds__(256)
     output_transform_kernel(const WinoParams p, const float* __restrict__ Mws,
                             const float* __restrict__ bias, const __nv_bfloat16* __restrict__ res,
                             __nv_bfloat16* __restrict__ y) {
   constexpr int A = TT::a, Mo = TT::m;
-  const int kp_per = p.K / 2;
   const long long T = (long long)p.nb * p.th * p.tw;
   const long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  if (i >= T * kp_per) return;
-  const int kp = (int)(i % kp_per);
-  const long long t = i / kp_per;
+  if (i >= T * p.K) return;
+  const int k = (int)(i % p.K);
+  const long long t = i / p.K;
   const int tj = (int)(t % p.tw);
   const int ti = (int)((t / p.tw) % p.th);
   const int n = p.n0 + (int)(t / ((long long)p.tw * p.th));
-  const float2* M2 = reinterpret_cast<const float2*>(Mws);
 
   // tmp[a][l] = sum_xi1 A^T[a][xi1] M[xi1][l]
-  float2 tmp[Mo][A];
+  float tmp[Mo][A];
 #pragma unroll
   for (int a = 0; a < Mo; ++a)
 #pragma unroll
-    for (int l = 0; l < A; ++l) tmp[a][l] = make_float2(0.f, 0.f);
+    for (int l = 0; l < A; ++l) tmp[a][l] = 0.f;
 #pragma unroll
   for (int r = 0; r < A; ++r) {
-    float2 row[A];
+    float row[A];
 #pragma unroll
-    for (int l = 0; l < A; ++l) row[l] = M2[((size_t)(r * A + l) * T + t) * kp_per + kp];
+    for (int l = 0; l < A; ++l) row[l] = __ldg(Mws + ((size_t)(r * A + l) * T + t) * p.K + k);
 #pragma unroll
     for (int a = 0; a < Mo; ++a)
 #pragma unroll
-      for (int l = 0; l < A; ++l) {
-        tmp[a][l].x = madd(tmp[a][l].x, TT::AT(a, r), row[l].x);
-        tmp[a][l].y = madd(tmp[a][l].y, TT::AT(a, r), row[l].y);
-      }
+      for (int l = 0; l < A; ++l) tmp[a][l] = madd(tmp[a][l], TT::AT(a, r), row[l]);
   }
-  const float b0 = bias ? bias[2 * kp] : 0.f, b1 = bias ? bias[2 * kp + 1] : 0.f;
+  const float bk = bias ? __ldg(bias + k) : 0.f;
 #pragma unroll
   for (int a = 0; a < Mo; ++a) {
     const int oh = ti * Mo + a;
@@ -270,32 +305,19 @@ __global__ void __launch_bounds__(128)
     for (int b = 0; b < Mo; ++b) {
       const int ow = tj * Mo + b;
       if (ow >= p.OW) break;
-      float2 v = make_float2(b0, b1);
+      float v = bk;
 #pragma unroll
-      for (int l = 0; l < A; ++l) {
-        v.x = madd(v.x, TT::AT(b, l), tmp[a][l].x);
-        v.y = madd(v.y, TT::AT(b, l), tmp[a][l].y);
-      }
-      const size_t off = (((size_t)n * p.OH + oh) * p.OW + ow) * p.K + 2 * kp;
-      if (res) {
-        const float2 rv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(res + off));
-        v.x += rv.x;
-        v.y += rv.y;
-      }
-      if (p.act >= 1) {
-        v.x = fmaxf(v.x, 0.f);
-        v.y = fmaxf(v.y, 0.f);
-      }
-      if (p.act == 2) {
-        v.x = fminf(v.x, 6.f);
-        v.y = fminf(v.y, 6.f);
-      }
-      *reinterpret_cast<__nv_bfloat162*>(y + off) = __floats2bfloat162_rn(v.x, v.y);
+      for (int l = 0; l < A; ++l) v = madd(v, TT::AT(b, l), tmp[a][l]);
+      const size_t off = (((size_t)n * p.OH + oh) * p.OW + ow) * p.K + k;
+      if (res) v += __bfloat162float(res[off]);
+      if (p.act >= 1) v = fmaxf(v, 0.f);
+      if (p.act == 2) v = fminf(v, 6.f);
+      y[off] = __float2bfloat16_rn(v);
     }
   }
 }
 
-constexpr size_t kChunkBudget = 48ull << 20;  // V + M bytes per chunk (L2-resident)
+constexpr size_t kChunkBudget = 64ull << 20;  // V + M bytes per chunk (L2-resident)
 
 int tiles_h(const gbconv_desc_s& d, int m) { return gb_ceil_div(d.OH, m); }
 int tiles_w(const gbconv_desc_s& d, int m) { return gb_ceil_div(d.OW, m); }
@@ -306,12 +328,25 @@ size_t bytes_per_image(const gbconv_desc_s& d, int m) {
   return tiles * a2 * ((size_t)d.C * 2 + (size_t)d.K * 4);
 }
 
+// Images per chunk: within the L2 budget, the count whose tile total fills the
+// GEMM's 128-row tiles best (ties: the larger chunk).
 int images_per_chunk(const gbconv_desc_s& d, int m) {
   const size_t per = bytes_per_image(d, m);
-  size_t nb = per ? kChunkBudget / per : 1;
-  if (nb < 1) nb = 1;
-  if (nb > (size_t)d.N) nb = d.N;
-  return (int)nb;
+  long long nbmax = per ? (long long)(kChunkBudget / per) : 1;
+  if (nbmax < 1) nbmax = 1;
+  if (nbmax > d.N) nbmax = d.N;
+  const long long tiles_img = (long long)tiles_h(d, m) * tiles_w(d, m);
+  long long best = 1;
+  double best_eff = 0.0;
+  for (long long nb = 1; nb <= nbmax; ++nb) {
+    const long long T = nb * tiles_img;
+    const double eff = (double)T / (double)(gb_ceil_div_ll(T, 128) * 128);
+    if (eff >= best_eff - 1e-9) {
+      best_eff = eff;
+      best = nb;
+    }
+  }
+  return (int)best;
 }
 
 template <typename TT, bool F16>
@@ -327,20 +362,36 @@ cudaError_t run_winograd(const gbconv_desc_s& d, const void* x, const void* wpac
   float* Mws = reinterpret_cast<float*>(static_cast<char*>(ws) +
                                         ((size_t)A * A * Tmax * d.C * 2 + 255) / 256 * 256);
   const int block_n = d.K > 128 ? 256 : (d.K > 64 ? 128 : 64);
+  // input strips: 4-D tiled map over x, box {64 ch, TWC*m + 2 cols, alpha rows, 1}
+  CUtensorMap tmx;
+  {
+    cuuint64_t dims[4] = {(cuuint64_t)d.C, (cuuint64_t)d.W, (cuuint64_t)d.H, (cuuint64_t)d.N};
+    cuuint64_t strides[3] = {(cuuint64_t)d.C * 2, (cuuint64_t)d.W * d.C * 2,
+                             (cuuint64_t)d.H * d.W * d.C * 2};
+    cuuint32_t box[4] = {WCB, (cuuint32_t)InCfg<TT>::IW, (cuuint32_t)A, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (gb_encode_tiled(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims,
+                        strides, box, estr, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(input_transform_kernel<TT, F16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         InCfg<TT>::SMEM);
+    if (e != cudaSuccess) return e;
+  }
   for (int n0 = 0; n0 < d.N; n0 += nb_max) {
     p.n0 = n0;
     p.nb = std::min(nb_max, d.N - n0);
     const long long T = (long long)p.nb * p.th * p.tw;
-    const long long in_threads = T * (d.C / 2);
-    input_transform_kernel<TT, F16><<<(unsigned)gb_ceil_div_ll(in_threads, 128), 128, 0, st>>>(
-        p, static_cast<const __nv_bfloat16*>(x), V);
+    const int strips = p.nb * p.th * gb_ceil_div(p.tw, TWC) * gb_ceil_div(d.C, WCB);
+    input_transform_kernel<TT, F16><<<strips, 256, InCfg<TT>::SMEM, st>>>(tmx, p, V, err,
+                                                                            wait_ns);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     e = launch_batched_gemm_tc(A * A, (int)T, d.K, d.C, V, wpack, Mws, F16 ? 0 : 1, block_n, err,
                                wait_ns, st);
     if (e != cudaSuccess) return e;
-    const long long out_threads = T * (d.K / 2);
-    output_transform_kernel<TT><<<(unsigned)gb_ceil_div_ll(out_threads, 128), 128, 0, st>>>(
+    const long long out_threads = T * d.K;
+    output_transform_kernel<TT><<<(unsigned)gb_ceil_div_ll(out_threads, 256), 256, 0, st>>>(
         p, Mws, bias, static_cast<const __nv_bfloat16*>(res), static_cast<__nv_bfloat16*>(y));
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
