@@ -63,6 +63,9 @@ struct IgemmParams {
   // k-steps; range b writes fp32 partial sums to part[b][M][K] (no epilogue)
   int ksplit, kchunk;
   float* part;
+  // tail rebalancing: work units from tail_start on cover the last partial
+  // wave's tiles as two half-width (BN/2) units each
+  int tail_start;
 };
 
 enum { MODE_CONV = 0, MODE_BATCHED = 1 };
@@ -145,6 +148,21 @@ __global__ void __launch_bounds__(192, 1)
   const int tiles_per_batch = p.m_tiles * p.n_tiles;
   const int num_tiles = tiles_per_batch * (MODE == MODE_BATCHED ? p.batch : p.ksplit);
   const int ohow = p.OH * p.OW;
+  // work unit u -> tile t, first output column offset within the tile, width
+  const int num_units =
+      p.tail_start < num_tiles ? p.tail_start + 2 * (num_tiles - p.tail_start) : num_tiles;
+  auto decode = [&](int u, int& t, int& noff, int& width) {
+    if (u < p.tail_start) {
+      t = u;
+      noff = 0;
+      width = BN;
+    } else {
+      const int h = u - p.tail_start;
+      t = p.tail_start + (h >> 1);
+      noff = (h & 1) * (BN / 2);
+      width = BN / 2;
+    }
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -153,7 +171,9 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t phase = 0;
       long long issued = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        int t, noff, width;
+        decode(u, t, noff, width);
         const int bt = t / tiles_per_batch;
         const int tt = t % tiles_per_batch;
         const int mt = tt / p.n_tiles, nt = tt % p.n_tiles;
@@ -184,12 +204,13 @@ __global__ void __launch_bounds__(192, 1)
                                      0, w0, h0, img, (uint16_t)(ts * p.dil),
                                      (uint16_t)(tr * p.dil));
             }
-            gb::tma_load_2d(sB + stage * C::B_BYTES, &tm_w, &full[stage], it * BK, nt * BN);
+            gb::tma_load_2d(sB + stage * C::B_BYTES, &tm_w, &full[stage], it * BK,
+                            nt * BN + noff);
           } else if (MODE == MODE_CONV) {
             gb::tma_load_im2col_4d(sA + stage * C::A_BYTES, &tm_x, &full[stage], cb * BK, w0, h0,
                                    img, (uint16_t)(s * p.dil), (uint16_t)(r * p.dil));
             gb::tma_load_2d(sB + stage * C::B_BYTES, &tm_w, &full[stage],
-                            (r * p.S + s) * p.cblocks * BK + cb * BK, nt * BN);
+                            (r * p.S + s) * p.cblocks * BK + cb * BK, nt * BN + noff);
           } else {
             gb::tma_load_3d(sA + stage * C::A_BYTES, &tm_x, &full[stage], cb * BK, (int)m0, bt);
             gb::tma_load_3d(sB + stage * C::B_BYTES, &tm_w, &full[stage], cb * BK, nt * BN, bt);
@@ -230,7 +251,10 @@ __global__ void __launch_bounds__(192, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        int t, noff, width;
+        decode(u, t, noff, width);
+        const uint32_t idesc_u = width == BN ? IDESC : gb::idesc_f16(BM, BN / 2, 1);
         if (!gb::mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, p.wait_ns, p.err)) break;
         gb::tc_fence_after();
         const uint32_t d = tmem_base + acc * BN;
@@ -253,7 +277,7 @@ __global__ void __launch_bounds__(192, 1)
                 (MODE == MODE_CONV && p.narrow)
                     ? gb::noswz_kmajor_desc(a0 + k * 2 * (BM * 16), BM * 16, 128)
                     : gb::sw128_kmajor_desc(a0 + k * 32);
-            gb::tc_mma_f16(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), IDESC,
+            gb::tc_mma_f16(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), idesc_u,
                            (it > kbeg || k > 0) ? 1u : 0u);
           }
           gb::tc_commit(&empty[stage]);
@@ -280,15 +304,19 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t acc_phase = 0;
     uint32_t epi_count = 0;  // staging boxes used by this warp (alternating pair)
     uint32_t rphase = 0;     // bit b: parity of the next completion of box b's barrier
-    // number of 64-column sub-blocks of tile t that hold output columns
-    auto nsub = [&](int t) {
+    // number of 64-column sub-blocks of work unit u that hold output columns
+    auto nsub = [&](int u) {
+      int t, noff, width;
+      decode(u, t, noff, width);
       const int ntt = (t % tiles_per_batch) % p.n_tiles;
-      const int rem = p.K - ntt * BN;
-      const int s64 = (rem + 63) / 64;
-      return s64 < BN / 64 ? s64 : BN / 64;
+      const int rem = p.K - (ntt * BN + noff);
+      const int s64 = rem > 0 ? (rem + 63) / 64 : 0;
+      return s64 < width / 64 ? s64 : width / 64;
     };
-    // residual box (64 columns x 32 rows) for sub-block j of tile t -> box b
-    auto fetch_res = [&](int t, int j, int b) {
+    // residual box (64 columns x 32 rows) for sub-block j of work unit u -> box b
+    auto fetch_res = [&](int u, int j, int b) {
+      int t, noff, width;
+      decode(u, t, noff, width);
       const int tt = t % tiles_per_batch;
       const int mt2 = tt / p.n_tiles, nt2 = tt % p.n_tiles;
       uint64_t* bar = &rbar[q * 2 + b];
@@ -296,17 +324,19 @@ __global__ void __launch_bounds__(192, 1)
       asm volatile(
           "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
           " [%0], [%1, {%2, %3}], [%4];" ::"r"(gb::smem_u32(sEpi + (q * 2 + b) * C::EPI_BOX)),
-          "l"(reinterpret_cast<uint64_t>(&tm_r)), "r"(nt2 * BN + j * 64),
+          "l"(reinterpret_cast<uint64_t>(&tm_r)), "r"(nt2 * BN + noff + j * 64),
           "r"(mt2 * BM + q * 32), "r"(gb::smem_u32(bar))
           : "memory");
     };
     const bool has_res = MODE == MODE_CONV && p.res != nullptr && p.part == nullptr;
     int pending = -1;  // box with a residual load not yet waited for
-    if (has_res && (int)blockIdx.x < num_tiles) {
+    if (has_res && (int)blockIdx.x < num_units) {
       if (lane == 0) fetch_res(blockIdx.x, 0, 0);
       pending = 0;
     }
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+      int t, noff, width;
+      decode(u, t, noff, width);
       const int bt = t / tiles_per_batch;
       const int tt = t % tiles_per_batch;
       const int mt = tt / p.n_tiles, nt = tt % p.n_tiles;
@@ -348,21 +378,21 @@ __global__ void __launch_bounds__(192, 1)
         // 64-column sub-blocks: TMEM -> registers (+ bias, residual, act) ->
         // swizzled staging box in shared memory -> TMA store of 32 rows x 64 cols
         const long long m_warp = (long long)mt * BM + q * 32;
-        const int ns = nsub(t);
+        const int ns = nsub(u);
 #pragma unroll 1
         for (int j = 0; j < ns; ++j) {
           const int cur = epi_count & 1;
           uint8_t* box = sEpi + (q * 2 + cur) * C::EPI_BOX;
-          const int nb0 = nt * BN + j * 64;
+          const int nb0 = nt * BN + noff + j * 64;
           if (has_res) {
             // prefetch the next sub-block's residual into the other box once the
             // store that last read that box is done with it
-            int tn = t, jn = j + 1;
+            int tn = u, jn = j + 1;
             if (jn >= ns) {
-              tn = t + gridDim.x;
+              tn = u + gridDim.x;
               jn = 0;
             }
-            if (tn < num_tiles) {
+            if (tn < num_units) {
               if (lane == 0) {
                 gb::bulk_wait_read<0>();
                 fetch_res(tn, jn, cur ^ 1);
@@ -371,7 +401,7 @@ __global__ void __launch_bounds__(192, 1)
             if (!gb::mbar_wait_bounded(&rbar[q * 2 + cur], (rphase >> cur) & 1, p.wait_ns, p.err))
               break;
             rphase ^= 1u << cur;
-            pending = tn < num_tiles ? (cur ^ 1) : -1;
+            pending = tn < num_units ? (cur ^ 1) : -1;
           } else {
             if (lane == 0) gb::bulk_wait_read<1>();  // the store that last used this box
             __syncwarp();
@@ -380,7 +410,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int c16 = 0; c16 < 4; ++c16) {
             uint32_t (&rr)[16] = *reinterpret_cast<uint32_t(*)[16]>(&r[c16 * 16]);
-            gb::tmem_ld_x16(tbase + j * 64 + c16 * 16, rr);
+            gb::tmem_ld_x16(tbase + j * 64 + c16 * 16, rr);  // accumulator column = nb0 - tile n0
           }
           // this sub-block's 64 bias values: two per lane, then broadcast reads
           float* sbias = reinterpret_cast<float*>(sEpi + 4 * 2 * C::EPI_BOX + q * 256);
@@ -572,6 +602,12 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   const int tiles = p.m_tiles * p.n_tiles * p.ksplit;
   const int slots = gb_num_sms() * (LIGHT ? 2 : 1);
   const int grid = tiles < slots ? tiles : slots;
+  // a last wave that would leave most SMs idle runs as half-width units
+  p.tail_start = tiles;
+  if (BN == 256 && p.ksplit == 1 && !LIGHT && tiles > grid) {
+    const int rem = tiles % grid;
+    if (rem > 0 && rem <= grid / 2) p.tail_start = tiles - rem;
+  }
   igemm_bf16_tc_kernel<BN, MODE_CONV, LIGHT><<<grid, 192, Cf::SMEM, st>>>(tmx, tmw, tmy, tmr, p);
   return cudaGetLastError();
 }
@@ -595,6 +631,7 @@ cudaError_t launch_batched_bn(int batch, int M, int N, int Kred, const void* A, 
   p.err = err;
   p.wait_ns = wait_ns;
   p.OH = p.OW = 1;
+  p.tail_start = 1 << 30;
   const CUtensorMapDataType dt =
       ab_type ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap tma, tmb;

@@ -81,3 +81,14 @@ def test_igemm_full_resnet_layer_sampled():
         got = yh[idx[:, 0], idx[:, 2], idx[:, 3], idx[:, 1]]
         err = np.max(np.abs(got - ref)) / np.max(np.abs(ref))
         assert err <= TOL, (algo, err)
+
+
+@pytest.mark.parametrize("residual", [False, True])
+def test_igemm_tail_wave_half_width_units(residual):
+    """196 full-width tiles on a 152-SM grid: the last partial wave runs as
+    half-width (128-column) work units; with a residual, its prefetch crosses
+    from full to half units."""
+    torch = need_gpu()
+    y, ref = run_bf16_layer(torch, 3, 8, 64, 56, 56, 256, 3, 3, 1, 1, act=1, residual=residual,
+                            seed=9)
+    assert ol.normalized_max_error(y, ref) <= TOL
