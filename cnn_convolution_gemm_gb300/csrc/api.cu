@@ -214,7 +214,7 @@ extern "C" conv_status_t conv_desc_get_output_dims(conv_desc_t d, int* OH, int* 
 static const char* const kAlgoNames[CONV_ALGO_COUNT] = {
     "direct", "igemm_tc_n64", "igemm_tc_n128", "igemm_tc_n256",
     "winograd_f2x2_3x3", "winograd_f6x6_3x3", "depthwise3x3", "int8_igemm_mma",
-    "int8_igemm_tc"};
+    "int8_igemm_tc", "im2col_gemm"};
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -273,6 +273,14 @@ static bool applicable(const gbconv_desc_s& d, int algo, const char** why) {
       if (d.stride > 8 || d.pad > 128 || d.pad - d.dil * (d.R - 1) < -128)
         return *why = "stride/padding outside the TMA im2col range", false;
       if ((long long)d.N * d.OH * d.OW >= (1LL << 31)) return *why = "N*OH*OW >= 2^31", false;
+      return true;
+    case CONV_ALGO_IM2COL_GEMM:
+      if (d.dtype != CONV_BF16 || !nhwc) return *why = "needs bf16 NHWC", false;
+      if (d.groups != 1) return *why = "needs groups == 1", false;
+      if (d.C % 8 || d.K % 8) return *why = "needs C and K multiples of 8", false;
+      if ((long long)d.N * d.OH * d.OW >= (1LL << 31)) return *why = "N*OH*OW >= 2^31", false;
+      if (im2col_workspace_bytes(d) > (8ull << 30))
+        return *why = "im2col matrix above 8 GiB", false;
       return true;
     default:
       return *why = "unknown algorithm", false;
@@ -380,6 +388,7 @@ extern "C" conv_status_t conv_workspace_size(conv_desc_t d, conv_algo_t algo, si
   if (a == CONV_ALGO_WINO_F2 || a == CONV_ALGO_WINO_F6)
     *bytes = winograd_workspace_bytes(*d, a == CONV_ALGO_WINO_F2 ? 2 : 6);
   if (a == CONV_ALGO_INT8_TC) *bytes = int8_tc_workspace_bytes(*d);
+  if (a == CONV_ALGO_IM2COL_GEMM) *bytes = im2col_workspace_bytes(*d);
   return ok_status();
 }
 
@@ -399,6 +408,7 @@ extern "C" conv_status_t conv_weights_packed_size(conv_desc_t d, conv_algo_t alg
       break;
     case CONV_ALGO_INT8_MMA: *bytes = (size_t)d->K * d->R * d->S * Cp64; break;
     case CONV_ALGO_INT8_TC: *bytes = int8_tc_packed_bytes(*d); break;
+    case CONV_ALGO_IM2COL_GEMM: *bytes = im2col_packed_bytes(*d); break;
     case CONV_ALGO_WINO_F2: *bytes = winograd_packed_bytes(*d, 2); break;
     case CONV_ALGO_WINO_F6: *bytes = winograd_packed_bytes(*d, 6); break;
     default: *bytes = user_weight_bytes(*d); break;
@@ -421,6 +431,7 @@ extern "C" conv_status_t conv_weights_prepack(conv_desc_t d, conv_algo_t algo, c
     case CONV_ALGO_IGEMM_N256: e = launch_pack_igemm_weights(*d, w, wpack, s); break;
     case CONV_ALGO_INT8_MMA: e = launch_pack_int8_weights(*d, w, wpack, s); break;
     case CONV_ALGO_INT8_TC: e = launch_pack_int8_tc_weights(*d, w, wpack, s); break;
+    case CONV_ALGO_IM2COL_GEMM: e = launch_pack_im2col_weights(*d, w, wpack, s); break;
     case CONV_ALGO_DEPTHWISE: e = launch_pack_dw_weights(*d, w, wpack, s); break;
     case CONV_ALGO_WINO_F2: e = launch_winograd_filter_transform(*d, 2, w, wpack, s); break;
     case CONV_ALGO_WINO_F6: e = launch_winograd_filter_transform(*d, 6, w, wpack, s); break;
@@ -455,6 +466,16 @@ static conv_status_t fwd_impl(const gbconv_desc_s& d, const void* x, const void*
     case CONV_ALGO_INT8_MMA:
       e = launch_igemm_int8(d, x, wpack, static_cast<const int32_t*>(bias), y, s);
       break;
+    case CONV_ALGO_IM2COL_GEMM: {
+      const size_t need = im2col_workspace_bytes(d);
+      if (!ws || ws_bytes < need)
+        return gb_fail(CONV_ERR_WORKSPACE, "workspace of %zu bytes needed", need);
+      if (reinterpret_cast<uintptr_t>(ws) & 15u)
+        return gb_fail(CONV_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
+      e = launch_im2col_gemm(d, x, wpack, static_cast<const float*>(bias), res, y, ws, err,
+                             wait_ns, s);
+      break;
+    }
     case CONV_ALGO_INT8_TC: {
       const size_t need = int8_tc_workspace_bytes(d);
       if (!ws || ws_bytes < need)
@@ -796,6 +817,7 @@ static bool implemented(int algo) {
     case CONV_ALGO_WINO_F6:
     case CONV_ALGO_INT8_MMA:
     case CONV_ALGO_INT8_TC:
+    case CONV_ALGO_IM2COL_GEMM:
       return true;
     default:
       return false;

@@ -98,6 +98,15 @@ cudaError_t launch_int8_tc(const gbconv_desc_s& d, const void* x, const void* wp
                            const int32_t* bias, void* y, void* ws, int* err,
                            unsigned long long wait_ns, cudaStream_t st);
 
+// Explicit im2col matrix in the workspace, then the tcgen05 GEMM (1x1 path).
+size_t im2col_workspace_bytes(const gbconv_desc_s& d);
+size_t im2col_packed_bytes(const gbconv_desc_s& d);
+cudaError_t launch_pack_im2col_weights(const gbconv_desc_s& d, const void* w, void* wpack,
+                                       cudaStream_t st);
+cudaError_t launch_im2col_gemm(const gbconv_desc_s& d, const void* x, const void* wpack,
+                               const float* bias, const void* res, void* y, void* ws, int* err,
+                               unsigned long long wait_ns, cudaStream_t st);
+
 // Winograd F(m x m, 3 x 3), m in {2, 6}.
 size_t winograd_packed_bytes(const gbconv_desc_s& d, int m);
 size_t winograd_workspace_bytes(const gbconv_desc_s& d, int m);

@@ -73,7 +73,8 @@ typedef int conv_algo_t;
 #define CONV_ALGO_DEPTHWISE 6      /* depthwise 3x3 (groups == C == K)                  */
 #define CONV_ALGO_INT8_MMA 7       /* int8 implicit GEMM on mma.sync, exact int32 acc.  */
 #define CONV_ALGO_INT8_TC 8        /* int8 on tcgen05 via exact bf16 chunks (workspace) */
-#define CONV_ALGO_COUNT 9
+#define CONV_ALGO_IM2COL_GEMM 9    /* materialised im2col matrix + GEMM (workspace)     */
+#define CONV_ALGO_COUNT 10
 
 /* ---- descriptor --------------------------------------------------------- */
 

@@ -92,3 +92,12 @@ def test_igemm_tail_wave_half_width_units(residual):
     y, ref = run_bf16_layer(torch, 3, 8, 64, 56, 56, 256, 3, 3, 1, 1, act=1, residual=residual,
                             seed=9)
     assert ol.normalized_max_error(y, ref) <= TOL
+
+
+@pytest.mark.parametrize("case", CASES[:8], ids=lambda c: "x".join(map(str, c)))
+def test_explicit_im2col_gemm_matches_oracle(case):
+    """The materialised im2col matrix + GEMM comparator (algorithm 9)."""
+    torch = need_gpu()
+    N, C, H, W, K, R, S, st, pad, dil = case
+    y, ref = run_bf16_layer(torch, 9, N, C, H, W, K, R, S, st, pad, dil, act=2, seed=13)
+    assert ol.normalized_max_error(y, ref) <= TOL
