@@ -47,6 +47,7 @@ L2_FLUSH_BYTES = 256 << 20
 # a changed source reports null.  Captures are summarised under profiles/.
 NCU_TRAFFIC = {
     # (workload, kernel): (bytes per launch, sha256[:16] of the source file)
+    ("resnet3x3", "igemm_tc_n256"): (52_613_632 + 8_057_600, "3e6bb3c0021f6e14"),
 }
 KERNEL_SOURCE = {"igemm_tc_n64": "k_igemm.cu", "igemm_tc_n128": "k_igemm.cu",
                  "igemm_tc_n256": "k_igemm.cu", "winograd_f2x2_3x3": "k_winograd.cu",
