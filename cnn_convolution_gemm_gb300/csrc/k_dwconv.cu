@@ -8,18 +8,25 @@
 //   * persistent CTAs walk a list of blocks (image, channel slice of up to 256
 //     channels — all of C for the usual widths, so a block reads whole
 //     contiguous pixel runs —, block of RB output rows, block of output
-//     columns sized to fill a buffer); for each, one 4-D TMA load
-//     brings the input rows/columns the block needs (its halo included) into
-//     shared memory, and out-of-bounds elements arrive as zeros, which is the
-//     padding;
-//   * two shared-memory buffers: the load of the next block is in flight while
-//     the current one is computed, so bytes in flight do not depend on
-//     registers or occupancy;
+//     columns sized to fill a buffer); for each, one 4-D TMA load per input
+//     row brings the columns the block needs (its halo included) into that
+//     row's slot in shared memory (a fixed pitch, so shared loads take
+//     constant offsets), and out-of-bounds elements arrive as zeros, which is
+//     the padding;
+//   * a ring of three shared-memory buffers: the loads of the next two blocks
+//     are in flight while the current one is computed, so bytes in flight do
+//     not depend on registers or occupancy;
 //   * a thread owns 4 channels of two adjacent output columns and walks down
-//     the block's rows keeping the bf16 input window in registers (4 new
-//     8-byte shared loads per output row), multiplying bf16 operands into fp32
-//     accumulators with fma.rn.f32.bf16;
-//   * weights are prepacked tap-major ([9][C] bf16): one 16-byte load per tap.
+//     the block's input rows: each row's values (4 or 5 columns, one 8-byte
+//     shared load each) are converted to fp32 once and added into the
+//     accumulators of the up to three output rows they reach (fp32 weights in
+//     registers); a finished output row gets bias / residual / activation and
+//     is stored as bf16;
+//   * a warp releases a buffer through an mbarrier when it is done with it,
+//     and the loading thread refills it once every warp has, so warps are not
+//     held to a common pace by block-wide barriers;
+//   * weights are prepacked tap-major ([9][C] bf16): one 8-byte load per tap
+//     gives a thread its 4 channels.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -37,13 +44,16 @@ template <int ST>
 struct DwCfg {
   static constexpr int RB = ST == 1 ? 8 : 4;      // output rows per block
   static constexpr int IH = (RB - 1) * ST + 3;    // input rows per block
-  static constexpr int SMEM = NBUF * BUF_MAX + 1024 + 64;
+  // input row r of a block sits at r * ROWP in its buffer: a compile-time,
+  // 128-byte aligned pitch, so every shared-memory load has a constant offset
+  static constexpr int ROWP = BUF_MAX / IH / 128 * 128;
+  static constexpr int SMEM = NBUF * BUF_MAX + 1024 + 2 * NBUF * 8;
 };
 
 struct DwParams {
-  int N, C, H, W, OH, OW, pad, act;
+  int N, C, H, W, OH, OW, pad;
   int cb;                  // channels per block (all of C when C <= 256)
-  int owt, iw, buf_bytes;  // output columns per block, input columns, bytes per buffer
+  int owt, iw, buf_bytes;  // output columns per block, input columns, bytes per block
   int cslices, rblocks, cblocks;
   long long nblocks;
   int* err;
@@ -53,39 +63,133 @@ struct DwParams {
 // work items of one block: (4-channel group, pair of output columns)
 __host__ __device__ inline int gb_items(const DwParams& p) { return ((p.owt + 1) / 2) * (p.cb / 4); }
 
-// two fp32 values in one 64-bit register pair (the operand of fma.rn.f32x2)
+// Two fp32 values in one 64-bit register pair: the operand of fma.rn.f32x2,
+// which does two fp32 fused multiply-adds (each rounded once) per instruction.
+// Pairs here are channels (c, c + 1).
 typedef unsigned long long f32x2;
 
-__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
+__device__ __forceinline__ f32x2 f2_pack(float lo, float hi) {
   f32x2 r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
   return r;
 }
-__device__ __forceinline__ float2 unpack2(f32x2 v) {
-  float2 r;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+__device__ __forceinline__ void f2_unpack(f32x2 v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// a bf16x2 word -> its two values in fp32 (exact: a bf16 is the top half of an fp32)
+__device__ __forceinline__ f32x2 bf16x2_to_f2(uint32_t u) {
+  return f2_pack(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+// an fp32 pair -> one bf16x2 word (round to nearest even), negative results set
+// to zero when RELU; the activation commutes with the monotone rounding
+template <bool RELU>
+__device__ __forceinline__ uint32_t f2_to_bf16x2(f32x2 v) {
+  float lo, hi;
+  f2_unpack(v, lo, hi);
+  uint32_t r;
+  if (RELU)
+    asm("cvt.rn.relu.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  else
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
-// bf16x2 (one 32-bit word) -> two fp32 in a register pair
-__device__ __forceinline__ f32x2 bf16x2_to_f32x2(uint32_t u) {
-  return pack2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+__device__ __forceinline__ uint32_t min6_bf16x2(uint32_t v) {
+  const __nv_bfloat162 six = __float2bfloat162_rn(6.f);
+  __nv_bfloat162 h = __hmin2(*reinterpret_cast<__nv_bfloat162*>(&v), six);
+  return *reinterpret_cast<uint32_t*>(&h);
 }
-__device__ __forceinline__ void ffma2(f32x2& d, f32x2 a, f32x2 b) {
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
-}
-
-// d += a * w with bf16 operands and an fp32 accumulator, one rounding (the same
-// result as converting both operands to fp32 first)
-__device__ __forceinline__ void fma_bf16(float& d, unsigned short a, unsigned short w) {
-  asm("fma.rn.f32.bf16 %0, %1, %2, %0;" : "+f"(d) : "h"(a), "h"(w));
-}
-// four bf16 values of an 8-byte load, one per 16-bit register
-__device__ __forceinline__ void split4(const uint2 v, unsigned short (&h)[4]) {
-  asm("mov.b32 {%0, %1}, %2;" : "=h"(h[0]), "=h"(h[1]) : "r"(v.x));
-  asm("mov.b32 {%0, %1}, %2;" : "=h"(h[2]), "=h"(h[3]) : "r"(v.y));
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
 }
 
-template <int ST>
+// bias / residual / activation of 4 channels, rounding to bf16, one 8-byte store
+template <int ACT, bool RES>
+__device__ __forceinline__ void store4(f32x2 a0, f32x2 a1, __nv_bfloat16* yp,
+                                       const __nv_bfloat16* rp) {
+  if (RES) {
+    const uint2 rv = __ldg(reinterpret_cast<const uint2*>(rp));
+    float v0, v1, v2, v3;
+    f2_unpack(a0, v0, v1);
+    f2_unpack(a1, v2, v3);
+    a0 = f2_pack(v0 + __uint_as_float(rv.x << 16), v1 + __uint_as_float(rv.x & 0xffff0000u));
+    a1 = f2_pack(v2 + __uint_as_float(rv.y << 16), v3 + __uint_as_float(rv.y & 0xffff0000u));
+  }
+  uint2 ov;
+  ov.x = f2_to_bf16x2<(ACT >= 1)>(a0);
+  ov.y = f2_to_bf16x2<(ACT >= 1)>(a1);
+  if (ACT == 2) {
+    ov.x = min6_bf16x2(ov.x);
+    ov.y = min6_bf16x2(ov.y);
+  }
+  *reinterpret_cast<uint2*>(yp) = ov;
+}
+
+// One work item of one block: 4 channels x 2 output columns x RB output rows.
+// Input row rho feeds output row (rho - i) / ST through filter row i; each input
+// value is converted once and added into the accumulators of the (up to three)
+// output rows it reaches.  Output row o lives in slot o % 3 and is stored once
+// its last input row, o * ST + 2, has been added.  FULL: all RB rows and both
+// columns exist (no per-row tests).
+template <int ST, int ACT, bool RES, bool FULL>
+__device__ __forceinline__ void dw_item(uint32_t src, uint32_t col_b, const f32x2 (&wf)[9][2],
+                                        const f32x2 (&bz)[2], __nv_bfloat16* y0,
+                                        const __nv_bfloat16* r0, size_t y_row, int C, int nrows,
+                                        bool two) {
+  using Cf = DwCfg<ST>;
+  constexpr int NC = ST + 3;  // distinct input columns the two outputs read
+  uint32_t sc[NC];            // shared address of input column cc of the pair, row 0
+#pragma unroll
+  for (int cc = 0; cc < NC; ++cc) sc[cc] = src + cc * col_b;
+  __nv_bfloat16* y1 = y0 + C;
+  const __nv_bfloat16* r1 = RES ? r0 + C : nullptr;
+  f32x2 acc[3][2][2];  // [slot][output column][channel pair]
+#pragma unroll
+  for (int rho = 0; rho < Cf::IH; ++rho) {
+    f32x2 xin[NC][2];
+#pragma unroll
+    for (int cc = 0; cc < NC; ++cc) {
+      const uint2 v = lds64(sc[cc] + rho * Cf::ROWP);
+      xin[cc][0] = bf16x2_to_f2(v.x);
+      xin[cc][1] = bf16x2_to_f2(v.y);
+    }
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      if (rho < i || (rho - i) % ST != 0 || (rho - i) / ST >= Cf::RB) continue;
+      f32x2(&a)[2][2] = acc[((rho - i) / ST) % 3];
+#pragma unroll
+      for (int s = 0; s < 3; ++s)
+#pragma unroll
+        for (int o = 0; o < 2; ++o)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            a[o][h] = f2_fma(xin[o * ST + s][h], wf[i * 3 + s][h],
+                             (i == 0 && s == 0) ? bz[h] : a[o][h]);
+    }
+    if (rho < 2 || (rho - 2) % ST != 0 || (rho - 2) / ST >= Cf::RB) continue;
+    const int orow = (rho - 2) / ST;
+    const f32x2(&a)[2][2] = acc[orow % 3];
+    if (FULL || orow < nrows) {
+      store4<ACT, RES>(a[0][0], a[0][1], y0, r0);
+      if (FULL || two) store4<ACT, RES>(a[1][0], a[1][1], y1, r1);
+    }
+    y0 += y_row;
+    y1 += y_row;
+    if (RES) {
+      r0 += y_row;
+      r1 += y_row;
+    }
+  }
+}
+
+// Persistent CTAs walk the block list; see the file comment.
+template <int ST, int ACT, bool RES>
 __global__ void __launch_bounds__(MAX_THREADS, 1)
     dwconv3x3_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const DwParams p,
                          const __nv_bfloat16* __restrict__ w9c, const float* __restrict__ bias,
@@ -94,162 +198,159 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NBUF * BUF_MAX);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NBUF * BUF_MAX);  // tile landed
+  uint64_t* empty = full + NBUF;  // every warp is done reading the tile
+  const int nwarps = blockDim.x / 32;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NBUF; ++i) gb::mbar_init(&full[i], 1);
+    for (int i = 0; i < NBUF; ++i) {
+      gb::mbar_init(&full[i], 1);
+      gb::mbar_init(&empty[i], nwarps);
+    }
     gb::fence_barrier_init();
     gb::tma_prefetch_desc(&tm_x);
   }
   __syncthreads();
 
-  auto block_coords = [&](long long b, int& n, int& cs, int& rb, int& cb) {
-    cb = (int)(b % p.cblocks);
-    b /= p.cblocks;
-    rb = (int)(b % p.rblocks);
-    b /= p.rblocks;
-    cs = (int)(b % p.cslices);
-    n = (int)(b / p.cslices);
-  };
-  auto issue = [&](long long b, int buf) {
+  // A block index is a mixed-radix number (image n, channel slice cs, row block
+  // rb, column block cb; cb fastest).  The CTA's blocks are first, first + step,
+  // ..., so both cursors below (the block being computed and the one thread 0
+  // loads next) advance by adding the digits of step with carries: no division
+  // inside the loop.
+  struct Cursor {
     int n, cs, rb, cb;
-    block_coords(b, n, cs, rb, cb);
+  };
+  auto digits = [&](long long b) {
+    Cursor c;
+    c.cb = (int)(b % p.cblocks);
+    b /= p.cblocks;
+    c.rb = (int)(b % p.rblocks);
+    b /= p.rblocks;
+    c.cs = (int)(b % p.cslices);
+    c.n = (int)(b / p.cslices);
+    return c;
+  };
+  const Cursor sd = digits(gridDim.x);
+  auto advance = [&](Cursor& c) {
+    // each digit + step digit + carry < 2 * radix: one subtraction suffices
+    c.cb += sd.cb;
+    int k = c.cb >= p.cblocks;
+    c.cb -= k ? p.cblocks : 0;
+    c.rb += sd.rb + k;
+    k = c.rb >= p.rblocks;
+    c.rb -= k ? p.rblocks : 0;
+    c.cs += sd.cs + k;
+    k = c.cs >= p.cslices;
+    c.cs -= k ? p.cslices : 0;
+    c.n += sd.n + k;
+  };
+  // one TMA load per input row (a box one row high) into its slot at r * ROWP;
+  // rows and columns outside the image arrive as zeros, which is the padding
+  auto issue = [&](const Cursor& c, int buf) {
     gb::fence_proxy_async_smem();
     gb::mbar_arrive_expect_tx(&full[buf], p.buf_bytes);
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(gb::smem_u32(smem + buf * BUF_MAX)),
-        "l"(reinterpret_cast<uint64_t>(&tm_x)), "r"(cs * p.cb), "r"(cb * p.owt * ST - p.pad),
-        "r"(rb * Cf::RB * ST - p.pad), "r"(n), "r"(gb::smem_u32(&full[buf]))
-        : "memory");
+    const uint32_t dst = gb::smem_u32(smem + buf * BUF_MAX);
+    const int c0 = c.cs * p.cb, w0 = c.cb * p.owt * ST - p.pad, h0 = c.rb * Cf::RB * ST - p.pad;
+#pragma unroll 1
+    for (int r = 0; r < Cf::IH; ++r)
+      asm volatile(
+          "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+          " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst + r * Cf::ROWP),
+          "l"(reinterpret_cast<uint64_t>(&tm_x)), "r"(c0), "r"(w0), "r"(h0 + r), "r"(c.n),
+          "r"(gb::smem_u32(&full[buf]))
+          : "memory");
   };
 
-  // ring of NBUF buffers: block i of this CTA lives in buffer i % NBUF; the
-  // load of block i + NBUF - 1 is issued before block i is computed
+  // The CTA's k-th block (k = 0, 1, ...) is block first + k * step and lives in
+  // buffer k % NBUF.  Thread 0 keeps NBUF - 1 loads ahead of its own warp; it
+  // refills a buffer once all warps have released it, so the other warps never
+  // wait on one another.
   const long long first = blockIdx.x, step = gridDim.x;
+  const int nmine = p.nblocks > first ? (int)((p.nblocks - first + step - 1) / step) : 0;
+  Cursor cur = digits(first), ld = cur;
+  int issued = 0;  // blocks thread 0 has issued
   if (threadIdx.x == 0)
-    for (int i = 0; i < NBUF - 1; ++i)
-      if (first + i * step < p.nblocks) issue(first + i * step, i);
-  int it = 0;
-  bool ok = true;
+    for (; issued < NBUF - 1 && issued < nmine; ++issued) {
+      issue(ld, issued);
+      advance(ld);
+    }
+  // this thread's work items: (4-channel group g, pair jp of output columns
+  // 2jp, 2jp + 1), item = jp * groups + g, items threadIdx.x + r * blockDim.x
   const int groups = p.cb / 4;
-  const int items = gb_items(p);
-  unsigned short wr[9][4];  // this thread's weights (kept while its work item is unchanged)
-  float bz[4];
-  int w_item = -1, w_cs = -1;
-  for (long long b = first; b < p.nblocks; b += step, ++it) {
+  const int npairs = (p.owt + 1) / 2;
+  const int g_first = threadIdx.x % groups, jp_first = threadIdx.x / groups;
+  const int g_step = blockDim.x % groups, jp_step = blockDim.x / groups;
+  f32x2 wf[9][2];  // this thread's weights (kept while its channels are unchanged)
+  f32x2 bz[2];
+  int w_c = -1;
+  const uint32_t col_b = (uint32_t)p.cb * 2;  // bytes between input columns in a row slot
+  const size_t y_row = (size_t)p.OW * p.C;    // elements between output rows
+  int it = 0;
+  for (; it < nmine; ++it, advance(cur)) {
     const int buf = it % NBUF;
-    const long long nb = b + (NBUF - 1) * step;
-    if (threadIdx.x == 0 && nb < p.nblocks) issue(nb, (it + NBUF - 1) % NBUF);
-    const uint32_t parity = (uint32_t)((it / NBUF) & 1);
-    if (!gb::mbar_wait_bounded(&full[buf], parity, p.wait_ns, p.err)) ok = false;
-    if (!__syncthreads_and(ok)) {
-      // a wait ran out: let every load this CTA issued land before it exits
-      if (threadIdx.x == 0)
-        for (int i = 0; i < NBUF; ++i) {
-          const int k = it + i;
-          if (first + (long long)k * step < p.nblocks)
-            gb::mbar_wait_bounded(&full[k % NBUF], (uint32_t)((k / NBUF) & 1), p.wait_ns, p.err);
-        }
-      break;
-    }
-    int n, cs, rb, cb;
-    block_coords(b, n, cs, rb, cb);
-    const uint8_t* tile = smem + buf * BUF_MAX;
-    // work items: (4-channel group g, pair of output columns j0, j0 + 1), g fastest
-    for (int item = threadIdx.x; item < items; item += blockDim.x) {
-      const int g = item % groups;
-      const int j0 = 2 * (item / groups);
-      const int c = cs * p.cb + g * 4;
-      const int ow0 = cb * p.owt + j0;
-      if (c >= p.C || ow0 >= p.OW || j0 >= p.owt) continue;
-      const bool two = j0 + 1 < p.owt && ow0 + 1 < p.OW;
-      if (item != w_item || cs != w_cs) {  // weights and bias of these 4 channels
-#pragma unroll
-        for (int k = 0; k < 9; ++k)
-          split4(__ldg(reinterpret_cast<const uint2*>(w9c + (size_t)k * p.C + c)), wr[k]);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) bz[q] = bias ? __ldg(bias + c + q) : 0.f;
-        w_item = item;
-        w_cs = cs;
-      }
-      // tile-local input columns of the pair: j0*ST + s (first), (j0+1)*ST + s (second)
-      constexpr int NC = ST + 3;  // distinct input columns the two outputs read
-      const int lc = j0 * ST;
-      auto ld = [&](int row, int col, unsigned short (&h)[4]) {
-        split4(*reinterpret_cast<const uint2*>(
-                   tile + ((size_t)(row * p.iw + lc + col) * p.cb + g * 4) * 2),
-               h);
-      };
-      unsigned short win[3][NC][4];  // bf16 window; input row rho lives in slot rho % 3
-#pragma unroll
-      for (int i = 0; i < 3; ++i)
-#pragma unroll
-        for (int cc = 0; cc < NC; ++cc) ld(i, cc, win[i][cc]);
-#pragma unroll
-      for (int k = 0; k < Cf::RB; ++k) {
-        const int oh = rb * Cf::RB + k;
-        if (oh >= p.OH) break;
-        if (k > 0) {  // the ST new input rows of this output row's window
-#pragma unroll
-          for (int q = 0; q < ST; ++q) {
-            const int rho = (k - 1) * ST + 3 + q;
-#pragma unroll
-            for (int cc = 0; cc < NC; ++cc) ld(rho, cc, win[rho % 3][cc]);
-          }
-        }
-        float acc[2][4];
-#pragma unroll
-        for (int o = 0; o < 2; ++o)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) acc[o][q] = bz[q];
-#pragma unroll
-        for (int i = 0; i < 3; ++i) {
-          const int sl = (k * ST + i) % 3;
-#pragma unroll
-          for (int s = 0; s < 3; ++s) {
-#pragma unroll
-            for (int o = 0; o < 2; ++o)
-#pragma unroll
-              for (int q = 0; q < 4; ++q) fma_bf16(acc[o][q], win[sl][o * ST + s][q], wr[i * 3 + s][q]);
-          }
-        }
-#pragma unroll
-        for (int o = 0; o < 2; ++o) {
-          if (o == 1 && !two) break;
-          float* a = acc[o];
-          const size_t off = (((size_t)n * p.OH + oh) * p.OW + ow0 + o) * p.C + c;
-          if (res) {
-            const uint2 rv = __ldg(reinterpret_cast<const uint2*>(res + off));
-            a[0] += __uint_as_float(rv.x << 16);
-            a[1] += __uint_as_float(rv.x & 0xffff0000u);
-            a[2] += __uint_as_float(rv.y << 16);
-            a[3] += __uint_as_float(rv.y & 0xffff0000u);
-          }
-          __nv_bfloat162 h0 = __floats2bfloat162_rn(a[0], a[1]);
-          __nv_bfloat162 h1 = __floats2bfloat162_rn(a[2], a[3]);
-          // the activation commutes with the (monotone) rounding to bf16
-          if (p.act >= 1) {
-            const __nv_bfloat162 z = __float2bfloat162_rn(0.f);
-            h0 = __hmax2(h0, z);
-            h1 = __hmax2(h1, z);
-          }
-          if (p.act == 2) {
-            const __nv_bfloat162 six = __float2bfloat162_rn(6.f);
-            h0 = __hmin2(h0, six);
-            h1 = __hmin2(h1, six);
-          }
-          uint2 ov;
-          ov.x = *reinterpret_cast<uint32_t*>(&h0);
-          ov.y = *reinterpret_cast<uint32_t*>(&h1);
-          *reinterpret_cast<uint2*>(y + off) = ov;
-        }
+    bool ok = true;
+    if (threadIdx.x == 0 && issued < nmine) {
+      // refill: block `issued` goes where block issued - NBUF was
+      if (issued >= NBUF)
+        ok = gb::mbar_wait_bounded(&empty[issued % NBUF], (uint32_t)((issued / NBUF - 1) & 1),
+                                   p.wait_ns, p.err);
+      if (ok) {
+        issue(ld, issued % NBUF);
+        advance(ld);
+        ++issued;
       }
     }
-    __syncthreads();  // the buffer is free for the load issued next iteration
+    if (ok) ok = gb::mbar_wait_bounded(&full[buf], (uint32_t)((it / NBUF) & 1), p.wait_ns, p.err);
+    if (!__all_sync(0xffffffffu, ok)) break;  // a wait ran out: leave (the drain is below)
+
+    const uint32_t tile = gb::smem_u32(smem + buf * BUF_MAX);
+    const int nrows = min(Cf::RB, p.OH - cur.rb * Cf::RB);  // output rows of this block
+    for (int g = g_first, jp = jp_first; jp < npairs;) {
+      const int j0 = 2 * jp;
+      const int c = cur.cs * p.cb + g * 4;
+      const int ow0 = cur.cb * p.owt + j0;
+      if (c < p.C && ow0 < p.OW) {
+        const bool two = j0 + 1 < p.owt && ow0 + 1 < p.OW;
+        if (c != w_c) {  // weights and bias of these 4 channels, in fp32
+#pragma unroll
+          for (int k = 0; k < 9; ++k) {
+            const uint2 v = __ldg(reinterpret_cast<const uint2*>(w9c + (size_t)k * p.C + c));
+            wf[k][0] = bf16x2_to_f2(v.x);
+            wf[k][1] = bf16x2_to_f2(v.y);
+          }
+          if (bias) {  // scalar loads: the caller's bias need not be 16-byte aligned
+            bz[0] = f2_pack(__ldg(bias + c), __ldg(bias + c + 1));
+            bz[1] = f2_pack(__ldg(bias + c + 2), __ldg(bias + c + 3));
+          } else {
+            bz[0] = bz[1] = f2_pack(0.f, 0.f);
+          }
+          w_c = c;
+        }
+        // tile-local input columns of the pair: j0*ST + s (first), (j0+1)*ST + s (second)
+        const uint32_t src = tile + (uint32_t)(j0 * ST) * col_b + (uint32_t)g * 8;
+        const size_t yoff = (((size_t)cur.n * p.OH + cur.rb * Cf::RB) * p.OW + ow0) * p.C + c;
+        const __nv_bfloat16* r0 = RES ? res + yoff : nullptr;
+        if (nrows == Cf::RB && two)
+          dw_item<ST, ACT, RES, true>(src, col_b, wf, bz, y + yoff, r0, y_row, p.C, nrows, two);
+        else
+          dw_item<ST, ACT, RES, false>(src, col_b, wf, bz, y + yoff, r0, y_row, p.C, nrows, two);
+      }
+      g += g_step;  // next item: + blockDim.x
+      jp += jp_step;
+      if (g >= groups) {
+        g -= groups;
+        ++jp;
+      }
+    }
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) gb::mbar_arrive(&empty[buf]);
   }
-  // On normal exit every issued load has been waited for: a load is issued
-  // only for a block index inside the list, and every such block is processed.
+  // Every load thread 0 issued must land before the CTA's shared memory goes
+  // away.  On normal exit all of them were consumed (it == issued); after a
+  // timeout the ones still in flight are waited for here (bounded).
+  if (threadIdx.x == 0)
+    for (int k = it; k < issued; ++k)
+      gb::mbar_wait_bounded(&full[k % NBUF], (uint32_t)((k / NBUF) & 1), p.wait_ns, p.err);
 }
 
 // [C][3][3] -> [9][C]
@@ -259,6 +360,11 @@ __global__ void pack_dw_weights_kernel(const __nv_bfloat16* __restrict__ w,
   if (i >= 9 * C) return;
   const int k = i / C, c = i % C;
   wp[i] = w[c * 9 + k];
+}
+
+template <int ST, int ACT>
+auto pick_kernel(bool res) {
+  return res ? dwconv3x3_tma_kernel<ST, ACT, true> : dwconv3x3_tma_kernel<ST, ACT, false>;
 }
 
 template <int ST>
@@ -274,14 +380,13 @@ cudaError_t launch_st(const gbconv_desc_s& d, const void* x, const void* w, cons
   p.OH = d.OH;
   p.OW = d.OW;
   p.pad = d.pad;
-  p.act = d.act;
   // channel slices of <= 256 channels (the TMA box limit), as few as possible,
   // so each block reads whole contiguous pixel rows
   p.cslices = gb_ceil_div(d.C, 256);
   p.cb = gb_ceil_div(gb_ceil_div(d.C, p.cslices), 8) * 8;
-  // widest column block whose input tile fits one buffer
+  // widest column block whose input row fits one row slot
   const int px_bytes = p.cb * 2;
-  int iw_max = BUF_MAX / (Cf::IH * px_bytes);
+  int iw_max = Cf::ROWP / px_bytes;
   int owt = (iw_max - 3) / ST + 1;
   if (owt > d.OW) owt = d.OW;
   if (owt > 256 / ST - 2) owt = 256 / ST - 2;  // TMA box dimension <= 256
@@ -289,30 +394,34 @@ cudaError_t launch_st(const gbconv_desc_s& d, const void* x, const void* w, cons
   owt = gb_ceil_div(d.OW, gb_ceil_div(d.OW, owt));  // equal-width column blocks
   p.owt = owt;
   p.iw = (p.owt - 1) * ST + 3;
-  p.buf_bytes = Cf::IH * p.iw * px_bytes;
+  p.buf_bytes = Cf::IH * p.iw * px_bytes;  // transaction bytes of one block's IH row loads
   p.rblocks = gb_ceil_div(d.OH, Cf::RB);
   p.cblocks = gb_ceil_div(d.OW, p.owt);
   p.nblocks = (long long)d.N * p.cslices * p.rblocks * p.cblocks;
+  if (p.nblocks >= (1LL << 31)) return cudaErrorInvalidValue;  // block counters are 32-bit
   p.err = err;
   p.wait_ns = wait_ns;
   CUtensorMap tm;
   cuuint64_t dims[4] = {(cuuint64_t)d.C, (cuuint64_t)d.W, (cuuint64_t)d.H, (cuuint64_t)d.N};
   cuuint64_t strides[3] = {(cuuint64_t)d.C * 2, (cuuint64_t)d.W * d.C * 2,
                            (cuuint64_t)d.H * d.W * d.C * 2};
-  cuuint32_t box[4] = {(cuuint32_t)p.cb, (cuuint32_t)p.iw, Cf::IH, 1};
+  cuuint32_t box[4] = {(cuuint32_t)p.cb, (cuuint32_t)p.iw, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   if (gb_encode_tiled(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims,
                       strides, box, estr, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(dwconv3x3_tma_kernel<ST>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
-  if (e != cudaSuccess) return e;
   const long long grid = std::min<long long>(p.nblocks, gb_num_sms());
   // threads: the block's work items split into equal rounds of <= MAX_THREADS
   const int items = gb_items(p);
   const int rounds = gb_ceil_div(items, MAX_THREADS);
   const int threads = gb_ceil_div(gb_ceil_div(items, rounds), 32) * 32;
-  dwconv3x3_tma_kernel<ST><<<(unsigned)grid, threads, Cf::SMEM, st>>>(
+  const bool has_res = res != nullptr;
+  auto kern = d.act == CONV_ACT_RELU6  ? pick_kernel<ST, 2>(has_res)
+              : d.act == CONV_ACT_RELU ? pick_kernel<ST, 1>(has_res)
+                                       : pick_kernel<ST, 0>(has_res);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)grid, threads, Cf::SMEM, st>>>(
       tm, p, static_cast<const __nv_bfloat16*>(w), bias, static_cast<const __nv_bfloat16*>(res),
       static_cast<__nv_bfloat16*>(y));
   return cudaGetLastError();

@@ -16,6 +16,10 @@ DW = 6  # CONV_ALGO_DEPTHWISE
     (3, 32, 8, 9, 1, 1, True),        # residual + ReLU
     (1, 96, 56, 56, 2, 2, False),     # MobileNetV2 stride-2 depthwise shape
     (4, 144, 56, 56, 1, 2, False),    # the inverted-residual block's depthwise (4 of 64 images)
+    (2, 384, 14, 14, 1, 2, False),    # two 192-channel slices per pixel
+    (1, 576, 14, 14, 2, 2, True),     # stride 2, three slices, residual
+    (1, 960, 7, 7, 1, 2, False),      # four 240-channel slices
+    (2, 64, 20, 60, 1, 1, True),      # 400 work items: two rounds per thread, weights reloaded
 ])
 def test_depthwise_matches_oracle(case):
     torch = need_gpu()
