@@ -13,9 +13,10 @@
 //     row's slot in shared memory (a fixed pitch, so shared loads take
 //     constant offsets), and out-of-bounds elements arrive as zeros, which is
 //     the padding;
-//   * a ring of three shared-memory buffers: the loads of the next two blocks
-//     are in flight while the current one is computed, so bytes in flight do
-//     not depend on registers or occupancy;
+//   * a ring of four shared-memory buffers: the loads of the next three
+//     blocks are in flight while the current one is computed, so bytes in
+//     flight do not depend on registers or occupancy, and warps that run
+//     ahead of the slowest one still find their next tiles loaded;
 //   * a thread owns 4 channels of two adjacent output columns and walks down
 //     the block's input rows: each row's values (4 or 5 columns, one 8-byte
 //     shared load each) are converted to fp32 once and added into the
@@ -37,8 +38,8 @@
 namespace {
 
 constexpr int MAX_THREADS = 384;
-constexpr int NBUF = 3;              // shared-memory ring depth: two loads in flight
-constexpr int BUF_MAX = 66 * 1024;   // bytes per buffer
+constexpr int NBUF = 4;              // shared-memory ring depth: three loads in flight
+constexpr int BUF_MAX = 55 * 1024;   // bytes per buffer (4 x 55 KB + barriers fit 227 KB)
 
 template <int ST>
 struct DwCfg {
