@@ -52,7 +52,8 @@ NCU_TRAFFIC = {
 KERNEL_SOURCE = {"igemm_tc_n64": "k_igemm.cu", "igemm_tc_n128": "k_igemm.cu",
                  "igemm_tc_n256": "k_igemm.cu", "winograd_f2x2_3x3": "k_winograd.cu",
                  "winograd_f6x6_3x3": "k_winograd.cu", "direct": "k_direct.cu",
-                 "depthwise3x3": "k_dwconv.cu", "int8_igemm_mma": "k_int8.cu"}
+                 "depthwise3x3": "k_dwconv.cu", "int8_igemm_mma": "k_int8.cu",
+                 "int8_igemm_tc": "k_int8_tc.cu", "im2col_gemm": "k_im2col.cu"}
 
 
 def src_hash(name: str) -> str:
@@ -747,7 +748,12 @@ def main():
                     if peak_src == "measured" else "fallback", "kernel": label,
                     "algorithmic_work_per_launch": wl.kernel_work(kname, work),
                     "algorithmic_bytes_per_launch": nbytes}
-        if args.workload == "int8_stages":
+        if kname == "int8_igemm_tc":
+            roofline["note"] = ("int8 runs exactly on the bf16 tcgen05 pipe (sm_103a has no "
+                                "tcgen05 int8 kind; int8 values are exact in bf16 and chunks of "
+                                "<= 1024 products are exact in fp32): the fraction is against "
+                                "the measured bf16 tensor peak")
+        elif kname == "int8_igemm_mma":
             roofline["note"] = ("int8 runs on mma.sync (sm_103a has no tcgen05 int8 kind); the "
                                 "fraction is against the measured bf16 tensor peak")
         cpu = None

@@ -60,6 +60,9 @@ SIGNATURES = {
     "conv_weights_prepack": (_i, [_p, _i, _p, _p, _p]),
     "conv_fwd": (_i, [_p, _p, _p, _p, _p, _p, _i, _p, _sz, _p]),
     "conv_fwd_noalloc": (_i, [_p, _p, _p, _p, _p, _p, _i, _p]),
+    "conv_mbv2_block_packed_size": (_i, [_i, _i, _i, ctypes.POINTER(_sz)]),
+    "conv_mbv2_block_prepack": (_i, [_i, _i, _i, _p, _p, _p, _p, _p]),
+    "conv_mbv2_block_fwd": (_i, [_i] * 6 + [_p, _p, _p, _p, _p, _i, _p, _p]),
     "conv_fastrun_select": (_i, [_p, _p, ctypes.POINTER(_i), ctypes.POINTER(_f)]),
     "conv_fastrun_lookup": (_i, [_p, ctypes.POINTER(_i)]),
     "conv_fastrun_save": (_i, [_cp]),
@@ -198,6 +201,30 @@ def conv_fwd_noalloc(desc, x_ptr, wpack_ptr, bias_ptr, residual_ptr, y_ptr, algo
     _check(load_library().conv_fwd_noalloc(desc, _ptr(x_ptr), _ptr(wpack_ptr), _ptr(bias_ptr),
                                            _ptr(residual_ptr), _ptr(y_ptr), algo, _stream(stream)),
            "conv_fwd_noalloc")
+
+
+def conv_mbv2_block_packed_size(C_in, E, C_out):
+    n = ctypes.c_size_t()
+    _check(load_library().conv_mbv2_block_packed_size(C_in, E, C_out, ctypes.byref(n)),
+           "conv_mbv2_block_packed_size")
+    return n.value
+
+
+def conv_mbv2_block_prepack(C_in, E, C_out, w_expand_ptr, w_dw_ptr, w_project_ptr, wpack_ptr,
+                            stream=None):
+    _check(load_library().conv_mbv2_block_prepack(C_in, E, C_out, _ptr(w_expand_ptr),
+                                                  _ptr(w_dw_ptr), _ptr(w_project_ptr),
+                                                  _ptr(wpack_ptr), _stream(stream)),
+           "conv_mbv2_block_prepack")
+
+
+def conv_mbv2_block_fwd(N, H, W, C_in, E, C_out, x_ptr, wpack_ptr, b_expand_ptr, b_dw_ptr,
+                        b_project_ptr, has_residual, y_ptr, stream=None):
+    _check(load_library().conv_mbv2_block_fwd(N, H, W, C_in, E, C_out, _ptr(x_ptr),
+                                              _ptr(wpack_ptr), _ptr(b_expand_ptr),
+                                              _ptr(b_dw_ptr), _ptr(b_project_ptr),
+                                              1 if has_residual else 0, _ptr(y_ptr),
+                                              _stream(stream)), "conv_mbv2_block_fwd")
 
 
 def conv_fastrun_select(desc, stream=None):

@@ -522,6 +522,62 @@ extern "C" conv_status_t conv_fwd(conv_desc_t d, const void* x, const void* wpac
 }
 
 // ---------------------------------------------------------------------------
+// fused MobileNetV2 block
+
+static conv_status_t mbv2_check(int C_in, int E, int C_out) {
+  if (C_in <= 0 || E <= 0 || C_out <= 0) return gb_fail(CONV_ERR_BAD_PARAM, "bad channel counts");
+  if (!mbv2_block_supported(C_in, E, C_out))
+    return gb_fail(CONV_ERR_UNSUPPORTED,
+                   "fused block supports E = 144, C_in and C_out multiples of 8 in [8, 32]");
+  return CONV_OK;
+}
+
+extern "C" conv_status_t conv_mbv2_block_packed_size(int C_in, int E, int C_out, size_t* bytes) {
+  if (!bytes) return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
+  conv_status_t st = mbv2_check(C_in, E, C_out);
+  if (st != CONV_OK) return st;
+  *bytes = mbv2_block_packed_bytes(E);
+  return ok_status();
+}
+
+extern "C" conv_status_t conv_mbv2_block_prepack(int C_in, int E, int C_out, const void* w_expand,
+                                                 const void* w_dw, const void* w_project,
+                                                 void* wpack, void* stream) {
+  if (!w_expand || !w_dw || !w_project || !wpack)
+    return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
+  conv_status_t st = mbv2_check(C_in, E, C_out);
+  if (st != CONV_OK) return st;
+  if (!aligned16(wpack)) return gb_fail(CONV_ERR_ALIGNMENT, "wpack not 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(w_expand) | reinterpret_cast<uintptr_t>(w_dw) |
+       reinterpret_cast<uintptr_t>(w_project)) & 1u)
+    return gb_fail(CONV_ERR_ALIGNMENT, "bf16 weights must be 2-byte aligned");
+  cudaError_t e = launch_pack_mbv2(C_in, E, C_out, w_expand, w_dw, w_project, wpack,
+                                   static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok_status() : cuda_fail(e, "mbv2 prepack");
+}
+
+extern "C" conv_status_t conv_mbv2_block_fwd(int N, int H, int W, int C_in, int E, int C_out,
+                                             const void* x, const void* wpack,
+                                             const float* b_expand, const float* b_dw,
+                                             const float* b_project, int has_residual, void* y,
+                                             void* stream) {
+  if (!x || !wpack || !y) return gb_fail(CONV_ERR_BAD_PARAM, "NULL tensor argument");
+  if (N <= 0 || H <= 0 || W <= 0) return gb_fail(CONV_ERR_BAD_PARAM, "bad sizes");
+  conv_status_t st = mbv2_check(C_in, E, C_out);
+  if (st != CONV_OK) return st;
+  if (has_residual && C_in != C_out)
+    return gb_fail(CONV_ERR_BAD_PARAM, "the residual needs C_in == C_out");
+  if (!aligned16(x) || !aligned16(y) || !aligned16(wpack) ||
+      ((reinterpret_cast<uintptr_t>(b_expand) | reinterpret_cast<uintptr_t>(b_dw) |
+        reinterpret_cast<uintptr_t>(b_project)) & 3u))
+    return gb_fail(CONV_ERR_ALIGNMENT, "tensors must be 16-byte aligned (biases 4-byte)");
+  cudaError_t e = launch_mbv2_block(N, H, W, C_in, E, C_out, x, wpack, b_expand, b_dw, b_project,
+                                    has_residual, y, gb_device_error_word(), gb_wait_limit_ns(),
+                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok_status() : cuda_fail(e, "mbv2 block");
+}
+
+// ---------------------------------------------------------------------------
 // Fast-Run selection: time every applicable algorithm on scratch tensors.
 
 namespace {

@@ -128,3 +128,14 @@ cudaError_t launch_avgpool_nhwc_bf16(const void* x, void* y, int N, int C, int H
 // Fill a buffer with deterministic pseudo-random values (Fast-Run scratch).
 cudaError_t launch_fill_random(void* p, size_t bytes, int elem_bytes, uint32_t seed,
                                cudaStream_t st);
+
+// Fused MobileNetV2 block (stride 1): expand 1x1 + ReLU6, depthwise 3x3 + ReLU6,
+// project 1x1 (+ residual) in one kernel.
+bool mbv2_block_supported(int cin, int E, int cout);
+size_t mbv2_block_packed_bytes(int E);
+cudaError_t launch_pack_mbv2(int cin, int E, int cout, const void* we, const void* wd,
+                             const void* wp, void* out, cudaStream_t st);
+cudaError_t launch_mbv2_block(int N, int H, int W, int cin, int E, int cout, const void* x,
+                              const void* wpack, const float* b_exp, const float* b_dw,
+                              const float* b_proj, int has_res, void* y, int* err,
+                              unsigned long long wait_ns, cudaStream_t st);
