@@ -61,8 +61,8 @@ SIGNATURES = {
     "conv_fwd": (_i, [_p, _p, _p, _p, _p, _p, _i, _p, _sz, _p]),
     "conv_fwd_noalloc": (_i, [_p, _p, _p, _p, _p, _p, _i, _p]),
     "conv_mbv2_block_packed_size": (_i, [_i, _i, _i, ctypes.POINTER(_sz)]),
-    "conv_mbv2_block_prepack": (_i, [_i, _i, _i, _p, _p, _p, _p, _p]),
-    "conv_mbv2_block_fwd": (_i, [_i] * 6 + [_p, _p, _p, _p, _p, _i, _p, _p]),
+    "conv_mbv2_block_prepack": (_i, [_i, _i, _i, _p, _p, _p, _p, _p, _p]),
+    "conv_mbv2_block_fwd": (_i, [_i] * 6 + [_p, _p, _p, _p, _i, _p, _p]),
     "conv_fastrun_select": (_i, [_p, _p, ctypes.POINTER(_i), ctypes.POINTER(_f)]),
     "conv_fastrun_lookup": (_i, [_p, ctypes.POINTER(_i)]),
     "conv_fastrun_save": (_i, [_cp]),
@@ -210,21 +210,21 @@ def conv_mbv2_block_packed_size(C_in, E, C_out):
     return n.value
 
 
-def conv_mbv2_block_prepack(C_in, E, C_out, w_expand_ptr, w_dw_ptr, w_project_ptr, wpack_ptr,
-                            stream=None):
+def conv_mbv2_block_prepack(C_in, E, C_out, w_expand_ptr, b_expand_ptr, w_dw_ptr, w_project_ptr,
+                            wpack_ptr, stream=None):
     _check(load_library().conv_mbv2_block_prepack(C_in, E, C_out, _ptr(w_expand_ptr),
-                                                  _ptr(w_dw_ptr), _ptr(w_project_ptr),
-                                                  _ptr(wpack_ptr), _stream(stream)),
-           "conv_mbv2_block_prepack")
+                                                  _ptr(b_expand_ptr), _ptr(w_dw_ptr),
+                                                  _ptr(w_project_ptr), _ptr(wpack_ptr),
+                                                  _stream(stream)), "conv_mbv2_block_prepack")
 
 
-def conv_mbv2_block_fwd(N, H, W, C_in, E, C_out, x_ptr, wpack_ptr, b_expand_ptr, b_dw_ptr,
-                        b_project_ptr, has_residual, y_ptr, stream=None):
+def conv_mbv2_block_fwd(N, H, W, C_in, E, C_out, x_ptr, wpack_ptr, b_dw_ptr, b_project_ptr,
+                        has_residual, y_ptr, stream=None):
     _check(load_library().conv_mbv2_block_fwd(N, H, W, C_in, E, C_out, _ptr(x_ptr),
-                                              _ptr(wpack_ptr), _ptr(b_expand_ptr),
-                                              _ptr(b_dw_ptr), _ptr(b_project_ptr),
-                                              1 if has_residual else 0, _ptr(y_ptr),
-                                              _stream(stream)), "conv_mbv2_block_fwd")
+                                              _ptr(wpack_ptr), _ptr(b_dw_ptr),
+                                              _ptr(b_project_ptr), 1 if has_residual else 0,
+                                              _ptr(y_ptr), _stream(stream)),
+           "conv_mbv2_block_fwd")
 
 
 def conv_fastrun_select(desc, stream=None):

@@ -528,7 +528,8 @@ static conv_status_t mbv2_check(int C_in, int E, int C_out) {
   if (C_in <= 0 || E <= 0 || C_out <= 0) return gb_fail(CONV_ERR_BAD_PARAM, "bad channel counts");
   if (!mbv2_block_supported(C_in, E, C_out))
     return gb_fail(CONV_ERR_UNSUPPORTED,
-                   "fused block supports E = 144, C_in and C_out multiples of 8 in [8, 32]");
+                   "fused block supports E = 144, C_in in {8, 16, 24}, C_out a multiple of 8 "
+                   "in [8, 32]");
   return CONV_OK;
 }
 
@@ -541,8 +542,9 @@ extern "C" conv_status_t conv_mbv2_block_packed_size(int C_in, int E, int C_out,
 }
 
 extern "C" conv_status_t conv_mbv2_block_prepack(int C_in, int E, int C_out, const void* w_expand,
-                                                 const void* w_dw, const void* w_project,
-                                                 void* wpack, void* stream) {
+                                                 const float* b_expand, const void* w_dw,
+                                                 const void* w_project, void* wpack,
+                                                 void* stream) {
   if (!w_expand || !w_dw || !w_project || !wpack)
     return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
   conv_status_t st = mbv2_check(C_in, E, C_out);
@@ -551,14 +553,15 @@ extern "C" conv_status_t conv_mbv2_block_prepack(int C_in, int E, int C_out, con
   if ((reinterpret_cast<uintptr_t>(w_expand) | reinterpret_cast<uintptr_t>(w_dw) |
        reinterpret_cast<uintptr_t>(w_project)) & 1u)
     return gb_fail(CONV_ERR_ALIGNMENT, "bf16 weights must be 2-byte aligned");
-  cudaError_t e = launch_pack_mbv2(C_in, E, C_out, w_expand, w_dw, w_project, wpack,
+  if (reinterpret_cast<uintptr_t>(b_expand) & 3u)
+    return gb_fail(CONV_ERR_ALIGNMENT, "b_expand must be 4-byte aligned");
+  cudaError_t e = launch_pack_mbv2(C_in, E, C_out, w_expand, b_expand, w_dw, w_project, wpack,
                                    static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ok_status() : cuda_fail(e, "mbv2 prepack");
 }
 
 extern "C" conv_status_t conv_mbv2_block_fwd(int N, int H, int W, int C_in, int E, int C_out,
-                                             const void* x, const void* wpack,
-                                             const float* b_expand, const float* b_dw,
+                                             const void* x, const void* wpack, const float* b_dw,
                                              const float* b_project, int has_residual, void* y,
                                              void* stream) {
   if (!x || !wpack || !y) return gb_fail(CONV_ERR_BAD_PARAM, "NULL tensor argument");
@@ -568,10 +571,9 @@ extern "C" conv_status_t conv_mbv2_block_fwd(int N, int H, int W, int C_in, int 
   if (has_residual && C_in != C_out)
     return gb_fail(CONV_ERR_BAD_PARAM, "the residual needs C_in == C_out");
   if (!aligned16(x) || !aligned16(y) || !aligned16(wpack) ||
-      ((reinterpret_cast<uintptr_t>(b_expand) | reinterpret_cast<uintptr_t>(b_dw) |
-        reinterpret_cast<uintptr_t>(b_project)) & 3u))
+      ((reinterpret_cast<uintptr_t>(b_dw) | reinterpret_cast<uintptr_t>(b_project)) & 3u))
     return gb_fail(CONV_ERR_ALIGNMENT, "tensors must be 16-byte aligned (biases 4-byte)");
-  cudaError_t e = launch_mbv2_block(N, H, W, C_in, E, C_out, x, wpack, b_expand, b_dw, b_project,
+  cudaError_t e = launch_mbv2_block(N, H, W, C_in, E, C_out, x, wpack, b_dw, b_project,
                                     has_residual, y, gb_device_error_word(), gb_wait_limit_ns(),
                                     static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ok_status() : cuda_fail(e, "mbv2 block");

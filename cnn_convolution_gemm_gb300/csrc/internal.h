@@ -133,9 +133,10 @@ cudaError_t launch_fill_random(void* p, size_t bytes, int elem_bytes, uint32_t s
 // project 1x1 (+ residual) in one kernel.
 bool mbv2_block_supported(int cin, int E, int cout);
 size_t mbv2_block_packed_bytes(int E);
-cudaError_t launch_pack_mbv2(int cin, int E, int cout, const void* we, const void* wd,
-                             const void* wp, void* out, cudaStream_t st);
+// The expand bias is packed into wpack (it rides in the expand MMA).
+cudaError_t launch_pack_mbv2(int cin, int E, int cout, const void* we, const float* be,
+                             const void* wd, const void* wp, void* out, cudaStream_t st);
 cudaError_t launch_mbv2_block(int N, int H, int W, int cin, int E, int cout, const void* x,
-                              const void* wpack, const float* b_exp, const float* b_dw,
-                              const float* b_proj, int has_res, void* y, int* err,
-                              unsigned long long wait_ns, cudaStream_t st);
+                              const void* wpack, const float* b_dw, const float* b_proj,
+                              int has_res, void* y, int* err, unsigned long long wait_ns,
+                              cudaStream_t st);

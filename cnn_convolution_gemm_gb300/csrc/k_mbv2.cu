@@ -12,10 +12,13 @@
 //      outside the image) into shared memory, laid out as 8-row x 16-byte core
 //      matrices (the next tile's halo is loaded while this one is computed);
 //   2. the expand is two M=128 tcgen05 MMAs per 16-channel k-step, N = E,
-//      accumulating in TMEM;
-//   3. each thread reads one halo pixel's E accumulators back, adds the bias,
-//      applies ReLU6 and stores bf16 to shared memory — zeros for pixels
-//      outside the image, which is the depthwise conv's zero padding of t1;
+//      accumulating in TMEM.  Its bias rides in the MMA: two padded input
+//      channels hold 1 for pixels inside the image and 0 outside, and their
+//      weights are the bias split into two bf16 terms (hi + lo, 16 significant
+//      bits), so the accumulator is x.W + b inside the image and exactly 0
+//      outside — the depthwise conv's zero padding of t1;
+//   3. each thread reads one halo pixel's E accumulators back, applies ReLU6
+//      and stores bf16 to shared memory;
 //   4. the depthwise 3x3 runs on CUDA cores (a thread owns 4 channels x 2
 //      columns x 14 rows; each t1 value is converted once and added into up to
 //      three output rows with fma.rn.f32x2) and writes ReLU6(.) as bf16
@@ -36,7 +39,7 @@ namespace {
 constexpr int TS = 14;            // output tile side
 constexpr int HS = TS + 2;        // halo tile side
 constexpr int NPIX = HS * HS;     // 256 halo pixels = two M=128 tiles
-constexpr int KX = 32;            // expand reduction (C_in padded)
+constexpr int KX = 32;            // expand reduction: C_in, two bias channels, zero padding
 constexpr int XCHUNK = NPIX * 16; // one 8-channel chunk of the halo tile: 256 rows x 16 B
 constexpr int X_BYTES = (KX / 8) * XCHUNK;
 constexpr int NP = 32;            // project N (C_out padded)
@@ -57,8 +60,8 @@ struct Cfg {
   static constexpr int OFF_T2 = OFF_T1 + NPIX * T1_PITCH;
   static constexpr int OFF_WE = OFF_T2 + (E / 8) * T2_CHUNK;
   static constexpr int OFF_WP = OFF_WE + WE_BYTES;
-  static constexpr int OFF_B = OFF_WP + WP_BYTES;     // b_expand[E], b_project[NP] fp32
-  static constexpr int OFF_BAR = OFF_B + (E + NP) * 4;
+  static constexpr int OFF_B = OFF_WP + WP_BYTES;     // b_project[NP] fp32
+  static constexpr int OFF_BAR = OFF_B + NP * 4;
   static constexpr int SMEM = OFF_BAR + 64 + 1024;    // barriers, TMEM slot, 1 KB alignment
   // TMEM columns: expand M-tile mt at mt * ECOL, project M-tile mt at PCOL + mt * NP
   static constexpr int ECOL = (E + 31) / 32 * 32;
@@ -99,9 +102,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
-// ReLU6 then bf16: clamping before the monotone rounding equals clamping after
+// ReLU6 then bf16: the conversion clamps negatives to zero, then a packed min
+// with 6 (exact in bf16); clamping after the monotone rounding equals clamping
+// before it
 __device__ __forceinline__ uint32_t relu6_bf16(float lo, float hi) {
-  return pack_bf16(fminf(fmaxf(lo, 0.f), 6.f), fminf(fmaxf(hi, 0.f), 6.f));
+  uint32_t r;
+  asm("cvt.rn.relu.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  const __nv_bfloat162 six = __float2bfloat162_rn(6.f);
+  __nv_bfloat162 h = __hmin2(*reinterpret_cast<__nv_bfloat162*>(&r), six);
+  return *reinterpret_cast<uint32_t*>(&h);
 }
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
@@ -171,30 +180,31 @@ __device__ __forceinline__ void dw_tile(uint32_t t1, uint32_t t2, int g, int jp,
 template <int E>
 __global__ void __launch_bounds__(THREADS, 1)
     mbv2_block_kernel(const __grid_constant__ CUtensorMap tm_x, const Mbv2Params p,
-                      const uint8_t* __restrict__ wpack, const float* __restrict__ b_exp,
-                      const float* __restrict__ b_dw, const float* __restrict__ b_proj,
+                      const uint8_t* __restrict__ wpack, const float* __restrict__ b_dw,
+                      const float* __restrict__ b_proj,
                       const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ y) {
   using C = Cfg<E>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* xfull = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);  // [2]
-  uint64_t* mma_bar = xfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_bar + 1);
-  float* sb_exp = reinterpret_cast<float*>(smem + C::OFF_B);
-  float* sb_proj = sb_exp + E;
+  uint64_t* xfull = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);  // [2] halo landed
+  uint64_t* ebar = xfull + 2;  // expand MMAs done
+  uint64_t* pbar = xfull + 3;  // project MMAs done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xfull + 4);
+  float* sb_proj = reinterpret_cast<float*>(smem + C::OFF_B);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t s_x = gb::smem_u32(smem + C::OFF_X);
   const uint32_t s_t1 = gb::smem_u32(smem + C::OFF_T1);
   const uint32_t s_t2 = gb::smem_u32(smem + C::OFF_T2);
   const uint32_t s_we = gb::smem_u32(smem + C::OFF_WE);
   const uint32_t s_wp = gb::smem_u32(smem + C::OFF_WP);
-  const int xchunks = p.cin / 8;  // chunks loaded by TMA; the rest of the 32 stay zero
+  const int xchunks = p.cin / 8;  // chunks loaded by TMA; chunk xchunks holds the bias channels
 
   if (tid == 0) {
     gb::mbar_init(&xfull[0], 1);
     gb::mbar_init(&xfull[1], 1);
-    gb::mbar_init(mma_bar, 1);
+    gb::mbar_init(ebar, 1);
+    gb::mbar_init(pbar, 1);
     gb::fence_barrier_init();
     gb::tma_prefetch_desc(&tm_x);
   }
@@ -210,7 +220,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int i = tid; i < (C::WE_BYTES + C::WP_BYTES) / 16; i += THREADS) dwe[i] = __ldg(src + i);
     uint4* dx = reinterpret_cast<uint4*>(smem + C::OFF_X);
     for (int i = tid; i < 2 * X_BYTES / 16; i += THREADS) dx[i] = make_uint4(0, 0, 0, 0);
-    for (int i = tid; i < E; i += THREADS) sb_exp[i] = b_exp ? __ldg(b_exp + i) : 0.f;
     for (int i = tid; i < NP; i += THREADS)
       sb_proj[i] = (b_proj && i < p.cout) ? __ldg(b_proj + i) : 0.f;
   }
@@ -263,18 +272,67 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   constexpr uint32_t IDESC_E = gb::idesc_f16(128, E, 1);
   constexpr uint32_t IDESC_P = gb::idesc_f16(128, NP, 1);
-  uint32_t mma_phase = 0;
-  bool mma_pending = false;
-  const int q = warp & 3, mt = warp >> 2;  // TMEM lane quarter and M-tile of this warp
+  uint32_t ephase = 0, pphase = 0;
+  bool e_pending = false, p_pending = false;  // MMAs issued and not yet waited for
+  const int q = warp & 3, mt = warp >> 2;    // TMEM lane quarter and M-tile of this warp
   const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-  int it = 0;
+
+  // project epilogue of a finished tile: output pixel m = oh * 14 + ow
+  auto project_epilogue = [&](int n, int h0, int w0) {
+    const int m = mt * 128 + q * 32 + lane;
+    const int oh = m / TS, ow = m % TS;
+    const int hh = h0 + oh, ww = w0 + ow;
+    const bool store = m < TS * TS && hh < p.H && ww < p.W;
+    uint32_t r[32];
+    const uint32_t tl = tmem_base + lane_off + C::PCOL + mt * NP;
+    gb::tmem_ld_x16(tl, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
+    gb::tmem_ld_x16(tl + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
+    gb::tmem_ld_wait();
+    if (store) {
+      const size_t off = (((size_t)n * p.H + hh) * p.W + ww) * p.cout;
+      uint4* yo = reinterpret_cast<uint4*>(y + off);
+      const uint4* xr = reinterpret_cast<const uint4*>(x + off);  // residual: C_in == C_out
+#pragma unroll
+      for (int c8 = 0; c8 < NP / 8; ++c8) {
+        if (c8 * 8 >= p.cout) break;
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[c8 * 8 + i]) + sb_proj[c8 * 8 + i];
+        if (p.res) {
+          const uint4 rv = __ldg(xr + c8);
+          const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            v[2 * i] += __uint_as_float(rw[i] << 16);
+            v[2 * i + 1] += __uint_as_float(rw[i] & 0xffff0000u);
+          }
+        }
+        yo[c8] = make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
+                            pack_bf16(v[6], v[7]));
+      }
+    }
+    gb::tc_fence_before();
+  };
+
+  // Software pipeline over the CTA's tiles: the project MMAs of tile i run
+  // while tile i+1's halo wait and expand MMAs are issued, and tile i's project
+  // epilogue overlaps tile i+1's expand MMAs.
+  int it = 0, pn = 0, ph0 = 0, pw0 = 0;  // coordinates of the tile whose project is in flight
+  bool ok = true;
   for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++it) {
     const int buf = it & 1;
     int n, h0, w0;
     tile_coords(t, n, h0, w0);
     // the other buffer's last tile finished its expand MMA: load the next halo there
     if (tid == 0 && t + (int)gridDim.x < p.ntiles) issue_x(t + gridDim.x, buf ^ 1);
-    bool ok = gb::mbar_wait_bounded(&xfull[buf], (uint32_t)((it >> 1) & 1), p.wait_ns, p.err);
+    {  // bias channels C_in, C_in+1 of halo pixel tid: 1 inside the image, 0 outside
+      const int hh = h0 - 1 + (tid >> 4), ww = w0 - 1 + (tid & 15);
+      const bool inside = hh >= 0 && hh < p.H && ww >= 0 && ww < p.W;
+      *reinterpret_cast<uint32_t*>(smem + C::OFF_X + buf * X_BYTES + xchunks * XCHUNK + tid * 16) =
+          inside ? 0x3F803F80u : 0u;  // two bf16 ones
+      gb::fence_proxy_async_smem();
+    }
+    ok = gb::mbar_wait_bounded(&xfull[buf], (uint32_t)((it >> 1) & 1), p.wait_ns, p.err);
     if (!__syncthreads_and(ok)) break;
     if (tid == 0) {
       if (buf) ++xdone1; else ++xdone0;
@@ -291,47 +349,63 @@ __global__ void __launch_bounds__(THREADS, 1)
               tmem_base + m2 * C::ECOL,
               gb::noswz_kmajor_desc(s_x + buf * X_BYTES + m2 * 2048 + ks * 2 * XCHUNK, XCHUNK, 128),
               gb::noswz_kmajor_desc(s_we + ks * 2 * (E * 16), E * 16, 128), IDESC_E, ks > 0);
-      gb::tc_commit(mma_bar);
+      gb::tc_commit(ebar);
     }
-    mma_pending = true;
-    ok = gb::mbar_wait_bounded(mma_bar, mma_phase, p.wait_ns, p.err);
+    e_pending = true;
+
+    // previous tile's project epilogue while the expand runs
+    if (p_pending) {
+      ok = gb::mbar_wait_bounded(pbar, pphase, p.wait_ns, p.err);
+      if (!__syncthreads_and(ok)) break;
+      p_pending = false;
+      pphase ^= 1;
+      gb::tc_fence_after();
+      project_epilogue(pn, ph0, pw0);
+    }
+
+    ok = gb::mbar_wait_bounded(ebar, ephase, p.wait_ns, p.err);
     if (!__syncthreads_and(ok)) break;
-    mma_pending = false;
-    mma_phase ^= 1;
+    e_pending = false;
+    ephase ^= 1;
     gb::tc_fence_after();
 
-    // 3. expand epilogue: halo pixel pix -> t1 row (zeros outside the image)
+    // 3. expand epilogue: halo pixel pix -> t1 row (the accumulator is already
+    //    0 outside the image)
     {
       const int pix = mt * 128 + q * 32 + lane;
-      const int hh = h0 - 1 + (pix >> 4), ww = w0 - 1 + (pix & 15);
-      const bool inside = hh >= 0 && hh < p.H && ww >= 0 && ww < p.W;
       const uint32_t tl = tmem_base + lane_off + mt * C::ECOL;
       const uint32_t row = s_t1 + (uint32_t)pix * C::T1_PITCH;
+      constexpr int G = 3;  // 16-column chunks per TMEM wait
+      static_assert((E / 16) % G == 0, "chunk grouping");
 #pragma unroll 1
-      for (int j = 0; j < E / 16; ++j) {
-        uint32_t r[16];
-        gb::tmem_ld_x16(tl + j * 16, r);
-        gb::tmem_ld_wait();
-        uint32_t o[8];
+      for (int j0 = 0; j0 < E / 16; j0 += G) {
+        uint32_t r[G][16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float v0 = __uint_as_float(r[2 * i]) + sb_exp[j * 16 + 2 * i];
-          const float v1 = __uint_as_float(r[2 * i + 1]) + sb_exp[j * 16 + 2 * i + 1];
-          o[i] = inside ? relu6_bf16(v0, v1) : 0u;
+        for (int g2 = 0; g2 < G; ++g2) gb::tmem_ld_x16(tl + (j0 + g2) * 16, r[g2]);
+        gb::tmem_ld_wait();
+#pragma unroll
+        for (int g2 = 0; g2 < G; ++g2) {
+          uint32_t o[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            o[i] = relu6_bf16(__uint_as_float(r[g2][2 * i]), __uint_as_float(r[g2][2 * i + 1]));
+          const uint32_t a = row + (j0 + g2) * 32;
+          sts128(a, o[0], o[1], o[2], o[3]);
+          sts128(a + 16, o[4], o[5], o[6], o[7]);
         }
-        sts128(row + j * 32, o[0], o[1], o[2], o[3]);
-        sts128(row + j * 32 + 16, o[4], o[5], o[6], o[7]);
       }
     }
     gb::tc_fence_before();
     __syncthreads();
 
-    // 4. depthwise into t2
+    // 4. depthwise into t2 (the previous tile's project MMAs, t2's last reader, are done)
     if (dw_item) dw_tile<E>(s_t1, s_t2, dg, djp, wf, bz);
     gb::fence_proxy_async_smem();  // t2's generic writes before the MMA reads them
+    gb::tc_fence_before();
     __syncthreads();
 
-    // 5. project: D[mt] = T2[mt] (128 x E) * WP^T (E x 32)
+    // 5. project: D[mt] = T2[mt] (128 x E) * WP^T (E x 32); its epilogue runs
+    //    next iteration (or after the loop)
     if (tid == 0) {
       gb::tc_fence_after();
 #pragma unroll
@@ -343,51 +417,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                                                C::T2_CHUNK, 128),
                          gb::noswz_kmajor_desc(s_wp + ks * 2 * (NP * 16), NP * 16, 128), IDESC_P,
                          ks > 0);
-      gb::tc_commit(mma_bar);
+      gb::tc_commit(pbar);
     }
-    mma_pending = true;
-    ok = gb::mbar_wait_bounded(mma_bar, mma_phase, p.wait_ns, p.err);
-    if (!__syncthreads_and(ok)) break;
-    mma_pending = false;
-    mma_phase ^= 1;
-    gb::tc_fence_after();
-
-    // project epilogue: output pixel m = oh * 14 + ow of this tile
-    {
-      const int m = mt * 128 + q * 32 + lane;
-      const int oh = m / TS, ow = m % TS;
-      const int hh = h0 + oh, ww = w0 + ow;
-      const bool store = m < TS * TS && hh < p.H && ww < p.W;
-      uint32_t r[32];
-      const uint32_t tl = tmem_base + lane_off + C::PCOL + mt * NP;
-      gb::tmem_ld_x16(tl, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
-      gb::tmem_ld_x16(tl + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
-      gb::tmem_ld_wait();
-      if (store) {
-        const size_t off = (((size_t)n * p.H + hh) * p.W + ww) * p.cout;
-        uint4* yo = reinterpret_cast<uint4*>(y + off);
-        const uint4* xr = reinterpret_cast<const uint4*>(x + off);  // residual: C_in == C_out
-#pragma unroll
-        for (int c8 = 0; c8 < NP / 8; ++c8) {
-          if (c8 * 8 >= p.cout) break;
-          float v[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[c8 * 8 + i]) + sb_proj[c8 * 8 + i];
-          if (p.res) {
-            const uint4 rv = __ldg(xr + c8);
-            const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              v[2 * i] += __uint_as_float(rw[i] << 16);
-              v[2 * i + 1] += __uint_as_float(rw[i] & 0xffff0000u);
-            }
-          }
-          yo[c8] = make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
-                              pack_bf16(v[6], v[7]));
-        }
-      }
+    p_pending = true;
+    pn = n;
+    ph0 = h0;
+    pw0 = w0;
+  }
+  if (ok && p_pending) {  // the last tile's project epilogue
+    ok = gb::mbar_wait_bounded(pbar, pphase, p.wait_ns, p.err);
+    if (__syncthreads_and(ok)) {
+      p_pending = false;
+      gb::tc_fence_after();
+      project_epilogue(pn, ph0, pw0);
     }
-    gb::tc_fence_before();
   }
 
   // Teardown.  On normal exit every halo load was consumed and every MMA waited
@@ -398,7 +441,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       gb::mbar_wait_bounded(&xfull[0], (uint32_t)((xissued0 - 1) & 1), p.wait_ns, p.err);
     if (xissued1 > xdone1)
       gb::mbar_wait_bounded(&xfull[1], (uint32_t)((xissued1 - 1) & 1), p.wait_ns, p.err);
-    if (mma_pending) gb::mbar_wait_bounded(mma_bar, mma_phase, p.wait_ns, p.err);
+    if (e_pending) gb::mbar_wait_bounded(ebar, ephase, p.wait_ns, p.err);
+    if (p_pending) gb::mbar_wait_bounded(pbar, pphase, p.wait_ns, p.err);
   }
   gb::tc_fence_before();
   __syncthreads();
@@ -409,10 +453,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // wpack = [WE: 4 chunks][E][8] | [WP: E/8 chunks][32][8] | [WD: 9][E], bf16
-//   WE[k][e][i] = w_expand[e][8k + i] (0 past C_in), WP[j][r][i] = w_project[r][8j + i]
-//   (0 for r >= C_out), WD[tap][e] = w_dw[e][tap]
+//   WE[k][e][i] = w_expand[e][c] for c = 8k + i < C_in; at c = C_in and C_in + 1 the
+//   bias b_expand[e] as hi = bf16(b) and lo = bf16(b - hi); 0 beyond.
+//   WP[j][r][i] = w_project[r][8j + i] (0 for r >= C_out), WD[tap][e] = w_dw[e][tap]
 template <int E>
 __global__ void pack_mbv2_kernel(const __nv_bfloat16* __restrict__ we,
+                                 const float* __restrict__ be,
                                  const __nv_bfloat16* __restrict__ wd,
                                  const __nv_bfloat16* __restrict__ wp, int cin, int cout,
                                  __nv_bfloat16* __restrict__ out) {
@@ -424,7 +470,16 @@ __global__ void pack_mbv2_kernel(const __nv_bfloat16* __restrict__ we,
     __nv_bfloat16 v;
     if (i < nwe) {
       const int k = i / (E * 8), e = (i / 8) % E, c = k * 8 + i % 8;
-      v = c < cin ? we[e * cin + c] : z;
+      const float b = be ? be[e] : 0.f;
+      const __nv_bfloat16 bhi = __float2bfloat16_rn(b);
+      if (c < cin)
+        v = we[e * cin + c];
+      else if (c == cin)  // bias, high part
+        v = bhi;
+      else if (c == cin + 1)  // bias, low part: b - hi rounded
+        v = __float2bfloat16_rn(b - __bfloat162float(bhi));
+      else
+        v = z;
     } else if (i < nwe + nwp) {
       const int j = (i - nwe) / (NP * 8), r = ((i - nwe) / 8) % NP, c = j * 8 + (i - nwe) % 8;
       v = r < cout ? wp[r * E + c] : z;
@@ -439,16 +494,17 @@ __global__ void pack_mbv2_kernel(const __nv_bfloat16* __restrict__ we,
 }  // namespace
 
 bool mbv2_block_supported(int cin, int E, int cout) {
-  return E == 144 && cin % 8 == 0 && cin >= 8 && cin <= KX && cout % 8 == 0 && cout >= 8 &&
+  // C_in + 2 bias channels must fit the padded reduction
+  return E == 144 && cin % 8 == 0 && cin >= 8 && cin + 2 <= KX && cout % 8 == 0 && cout >= 8 &&
          cout <= NP;
 }
 
 size_t mbv2_block_packed_bytes(int E) { return E == 144 ? (size_t)Cfg<144>::PACKED : 0; }
 
-cudaError_t launch_pack_mbv2(int cin, int E, int cout, const void* we, const void* wd,
-                             const void* wp, void* out, cudaStream_t st) {
+cudaError_t launch_pack_mbv2(int cin, int E, int cout, const void* we, const float* be,
+                             const void* wd, const void* wp, void* out, cudaStream_t st) {
   if (E != 144) return cudaErrorInvalidValue;
-  pack_mbv2_kernel<144><<<32, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(we),
+  pack_mbv2_kernel<144><<<32, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(we), be,
                                             static_cast<const __nv_bfloat16*>(wd),
                                             static_cast<const __nv_bfloat16*>(wp), cin, cout,
                                             static_cast<__nv_bfloat16*>(out));
@@ -456,8 +512,8 @@ cudaError_t launch_pack_mbv2(int cin, int E, int cout, const void* we, const voi
 }
 
 cudaError_t launch_mbv2_block(int N, int H, int W, int cin, int E, int cout, const void* x,
-                              const void* wpack, const float* b_exp, const float* b_dw,
-                              const float* b_proj, int has_res, void* y, int* err,
+                              const void* wpack, const float* b_dw, const float* b_proj,
+                              int has_res, void* y, int* err,
                               unsigned long long wait_ns, cudaStream_t st) {
   if (E != 144) return cudaErrorInvalidValue;
   using C = Cfg<144>;
@@ -489,7 +545,7 @@ cudaError_t launch_mbv2_block(int N, int H, int W, int cin, int E, int cout, con
   if (e != cudaSuccess) return e;
   const int grid = std::min(p.ntiles, gb_num_sms());
   mbv2_block_kernel<144><<<grid, THREADS, C::SMEM, st>>>(
-      tm, p, static_cast<const uint8_t*>(wpack), b_exp, b_dw, b_proj,
+      tm, p, static_cast<const uint8_t*>(wpack), b_dw, b_proj,
       static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y));
   return cudaGetLastError();
 }

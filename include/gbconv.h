@@ -176,26 +176,28 @@ conv_status_t conv_fwd_noalloc(conv_desc_t desc, const void* x, const void* wpac
  * intermediates make four passes through memory; here they stay in shared
  * memory per 14x14 output tile (halo recomputed), so HBM sees x, y and the
  * weights only.  t1 and t2 are rounded to bf16 where the three-layer chain
- * stores them.  Supported: E = 144, C_in and C_out multiples of 8 in [8, 32]
- * (the 24 -> 144 -> 24 blocks); has_residual needs C_in == C_out.  Anything
- * else returns CONV_ERR_UNSUPPORTED. */
+ * stores them; b_expand enters the expand's fp32 accumulation as two bf16 terms
+ * (16 significant bits).  Supported: E = 144, C_in in {8, 16, 24}, C_out a
+ * multiple of 8 in [8, 32] (the 24 -> 144 -> 24 blocks); has_residual needs
+ * C_in == C_out.  Anything else returns CONV_ERR_UNSUPPORTED. */
 /* Bytes of the packed weight buffer. */
 conv_status_t conv_mbv2_block_packed_size(int C_in, int E, int C_out, size_t* bytes);
-/* Pack the three weights once.  w_expand: device bf16 [E][C_in] (the [K][1][1][C]
- * layout of conv_desc NHWC weights); w_dw: device bf16 [E][3][3]; w_project:
- * device bf16 [C_out][E].  wpack: device, conv_mbv2_block_packed_size bytes,
- * 16-byte aligned, caller-owned.  Stream-ordered. */
+/* Pack the weights and the expand bias once.  w_expand: device bf16 [E][C_in]
+ * (the [K][1][1][C] layout of conv_desc NHWC weights); b_expand: device fp32
+ * [E] or NULL for zero; w_dw: device bf16 [E][3][3]; w_project: device bf16
+ * [C_out][E].  wpack: device, conv_mbv2_block_packed_size bytes, 16-byte
+ * aligned, caller-owned.  Stream-ordered. */
 conv_status_t conv_mbv2_block_prepack(int C_in, int E, int C_out, const void* w_expand,
-                                      const void* w_dw, const void* w_project, void* wpack,
-                                      void* stream);
+                                      const float* b_expand, const void* w_dw,
+                                      const void* w_project, void* wpack, void* stream);
 /* x: device bf16 NHWC [N][H][W][C_in]; y: device bf16 NHWC [N][H][W][C_out]
- * (both 16-byte aligned, not overlapping); biases: device fp32 [E], [E],
- * [C_out] or NULL for zero (4-byte aligned).  Device-side waits are bounded;
- * a timeout is reported by conv_sync_status.  Stream-ordered. */
+ * (both 16-byte aligned, not overlapping); wpack from conv_mbv2_block_prepack
+ * with the same channel counts; b_dw, b_project: device fp32 [E], [C_out] or
+ * NULL for zero (4-byte aligned).  Device-side waits are bounded; a timeout is
+ * reported by conv_sync_status.  Stream-ordered. */
 conv_status_t conv_mbv2_block_fwd(int N, int H, int W, int C_in, int E, int C_out, const void* x,
-                                  const void* wpack, const float* b_expand, const float* b_dw,
-                                  const float* b_project, int has_residual, void* y,
-                                  void* stream);
+                                  const void* wpack, const float* b_dw, const float* b_project,
+                                  int has_residual, void* y, void* stream);
 
 /* ---- Fast-Run ([MegEngine] "Fast-Run") ----------------------------------- */
 

@@ -37,11 +37,11 @@ def run_fused(torch, d, N, H, W, cin, E, cout, res):
     nbytes = B.conv_mbv2_block_packed_size(cin, E, cout)
     wpack = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     sh = torch.cuda.current_stream().cuda_stream
-    B.conv_mbv2_block_prepack(cin, E, cout, we.data_ptr(), wd.data_ptr(), wp.data_ptr(),
-                              wpack.data_ptr(), sh)
+    B.conv_mbv2_block_prepack(cin, E, cout, we.data_ptr(), be.data_ptr(), wd.data_ptr(),
+                              wp.data_ptr(), wpack.data_ptr(), sh)
     y = torch.full((N, H, W, cout), float("nan"), dtype=torch.bfloat16, device=dev)
-    B.conv_mbv2_block_fwd(N, H, W, cin, E, cout, x.data_ptr(), wpack.data_ptr(), be.data_ptr(),
-                          bd.data_ptr(), bp.data_ptr(), res, y.data_ptr(), sh)
+    B.conv_mbv2_block_fwd(N, H, W, cin, E, cout, x.data_ptr(), wpack.data_ptr(), bd.data_ptr(),
+                          bp.data_ptr(), res, y.data_ptr(), sh)
     B.conv_sync_status(sh)
     return y.double().cpu().numpy()
 
@@ -65,7 +65,7 @@ def oracle_block(torch, d, E, res, images=None):
     (1, 56, 56, 24, 144, 24, False),   # the block's spatial size: 4x4 tiles
     (3, 9, 30, 16, 144, 32, False),    # C_in 16 (two chunks zero), C_out 32, one partial tile row
     (1, 5, 5, 8, 144, 8, True),        # image smaller than a tile; C_in = C_out = 8
-    (4, 28, 28, 32, 144, 16, False),   # C_in 32 (all four chunks loaded), C_out 16
+    (4, 28, 28, 24, 144, 16, False),   # C_out 16
 ])
 def test_fused_block_matches_oracle(case):
     torch = need_gpu()
@@ -96,11 +96,11 @@ def test_fused_block_rejects_unsupported():
     with pytest.raises(B.GbconvError):
         B.conv_mbv2_block_packed_size(24, 192, 24)   # E other than 144
     with pytest.raises(B.GbconvError):
-        B.conv_mbv2_block_packed_size(40, 144, 24)   # C_in above 32
+        B.conv_mbv2_block_packed_size(32, 144, 24)   # C_in 32: no room for the bias channels
     with pytest.raises(B.GbconvError):
         B.conv_mbv2_block_packed_size(20, 144, 24)   # C_in not a multiple of 8
     dev = torch.device("cuda:0")
     buf = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
     with pytest.raises(B.GbconvError):              # residual with C_in != C_out
         B.conv_mbv2_block_fwd(1, 14, 14, 16, 144, 24, buf.data_ptr(), buf.data_ptr(), None, None,
-                              None, True, buf.data_ptr())
+                              True, buf.data_ptr())

@@ -85,18 +85,18 @@ def test_fused_block_argument_errors(B):
     # the fused MobileNetV2 block validates shapes and pointers before any launch
     n = B.conv_mbv2_block_packed_size(24, 144, 24)
     assert n == 4 * 144 * 16 + 18 * 32 * 16 + 9 * 144 * 2  # [4][E][8] + [E/8][32][8] + [9][E]
-    for bad in [(24, 192, 24), (40, 144, 24), (20, 144, 24), (24, 144, 36)]:
+    for bad in [(24, 192, 24), (32, 144, 24), (20, 144, 24), (24, 144, 36)]:
         with pytest.raises(B.GbconvError) as e:
             B.conv_mbv2_block_packed_size(*bad)
         assert e.value.status_name == "CONV_ERR_UNSUPPORTED"
     with pytest.raises(B.GbconvError) as e:
-        B.conv_mbv2_block_fwd(1, 14, 14, 24, 144, 24, 0, 0x2000, 0, 0, 0, False, 0x3000)
+        B.conv_mbv2_block_fwd(1, 14, 14, 24, 144, 24, 0, 0x2000, 0, 0, False, 0x3000)
     assert e.value.status_name == "CONV_ERR_BAD_PARAM"  # NULL x
     with pytest.raises(B.GbconvError) as e:
-        B.conv_mbv2_block_fwd(1, 14, 14, 16, 144, 24, 0x1000, 0x2000, 0, 0, 0, True, 0x3000)
+        B.conv_mbv2_block_fwd(1, 14, 14, 16, 144, 24, 0x1000, 0x2000, 0, 0, True, 0x3000)
     assert e.value.status_name == "CONV_ERR_BAD_PARAM"  # residual needs C_in == C_out
     with pytest.raises(B.GbconvError) as e:
-        B.conv_mbv2_block_fwd(1, 14, 14, 24, 144, 24, 0x1008, 0x2000, 0, 0, 0, False, 0x3000)
+        B.conv_mbv2_block_fwd(1, 14, 14, 24, 144, 24, 0x1008, 0x2000, 0, 0, False, 0x3000)
     assert e.value.status_name == "CONV_ERR_ALIGNMENT"
 
 
