@@ -10,7 +10,10 @@ Other workloads (--workload):
   single_layer  1 x 32 x 28 x 28 fp32 NCHW, 32 filters 3x3: boundary
                 conversion to NHWC bf16, conv, conversion back
   mbv2_block    MobileNetV2 inverted residual, N=64, 56x56: 1x1 24->144 +
-                ReLU6, depthwise 3x3 + ReLU6, 1x1 144->24
+                ReLU6, depthwise 3x3 + ReLU6, 1x1 144->24.  By default the
+                fused one-kernel block and the three-layer chain (each layer's
+                Fast-Run pick) are both timed and the faster runs; --algo fused
+                forces the fused kernel, any layer algorithm name the chain
   int8_stages   int8 3x3 convs at the four ResNet-50 stage shapes, N=32
   resnet50      full ResNet-50 forward, batch 64, 224x224x3 input
 
@@ -53,7 +56,8 @@ KERNEL_SOURCE = {"igemm_tc_n64": "k_igemm.cu", "igemm_tc_n128": "k_igemm.cu",
                  "igemm_tc_n256": "k_igemm.cu", "winograd_f2x2_3x3": "k_winograd.cu",
                  "winograd_f6x6_3x3": "k_winograd.cu", "direct": "k_direct.cu",
                  "depthwise3x3": "k_dwconv.cu", "int8_igemm_mma": "k_int8.cu",
-                 "int8_igemm_tc": "k_int8_tc.cu", "im2col_gemm": "k_im2col.cu"}
+                 "int8_igemm_tc": "k_int8_tc.cu", "im2col_gemm": "k_im2col.cu",
+                 "mbv2_fused": "k_mbv2.cu"}
 
 
 def src_hash(name: str) -> str:
@@ -171,6 +175,29 @@ class Workload:
 
     def cpu_baseline(self, args):
         raise NotImplementedError
+
+
+def x_bytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+def time_groups(groups, stream_handle, reps=7):
+    """Median device time (ms) of one pass over the groups, launched on the current
+    stream after two warm-up passes (used for block-level Fast-Run choices)."""
+    import torch
+    for _ in range(2):
+        for g in groups:
+            g[1]()
+    ts = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for g in groups:
+            g[1]()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return sorted(ts)[len(ts) // 2]
 
 
 def fastrun_pick(layer, sh, args, B):
@@ -307,7 +334,8 @@ class SingleLayer(Workload):
         for _ in range(reps):
             ol.conv2d_f64(x.astype(np.float64), w.astype(np.float64), b.astype(np.float64), pad=1)
         dt = time.perf_counter() - t0
-        f = self.shape.flops() * reps
+        from cnn_convolution_gemm_gb300.workload import ConvShape
+        f = ConvShape(1, 32, 28, 28, 32, 3, 3, 1, 1).flops() * reps  # no setup() needed
         return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": threads(), "kind": "oracle",
                 "sample": f"the whole layer, {reps} times", "seconds": round(dt, 3)}
 
@@ -346,15 +374,51 @@ class MBv2Block(Workload):
         self.t2 = torch.empty((N, H, W, E), dtype=torch.bfloat16, device=dev)
         self.y = torch.empty((N, H, W, C), dtype=torch.bfloat16, device=dev)
         self.yh = torch.empty((N, H, W, C), dtype=torch.bfloat16).pin_memory()
-        self.algo_name = "+".join(self.algo_names)
+        # the whole block as one kernel (t1, t2 stay on chip)
+        self.dims = (N, H, W, C, E, C)
+        self.fpack = torch.empty(B.conv_mbv2_block_packed_size(C, E, C), dtype=torch.uint8,
+                                 device=dev)
+        wt = [torch.from_numpy(w).to(torch.bfloat16).to(dev) for w in ws]
+        B.conv_mbv2_block_prepack(C, E, C, wt[0].data_ptr(), self.b[0].data_ptr(),
+                                  wt[1].data_ptr(), wt[2].data_ptr(), self.fpack.data_ptr(), sh)
+        self.fused_bytes = 2 * x_bytes(self.x) + self.fpack.numel() + 4 * (E + C)
+        self.mode = "fused"
+        if args.algo == "fastrun":  # block-level Fast-Run: the fused kernel vs the layer chain
+            times = {}
+            for mode in ("fused", "layers"):
+                self.mode = mode
+                times[mode] = time_groups(self.groups(), sh)
+            self.mode = min(times, key=times.get)
+            self.fastrun_ms["block"] = {"mbv2_fused": round(times["fused"], 4),
+                                        "+".join(self.algo_names): round(times["layers"], 4)}
+        elif args.algo != "fused":
+            self.mode = "layers"
+        self.algo_name = "mbv2_fused" if self.mode == "fused" else "+".join(self.algo_names)
 
     def groups(self):
+        if self.mode == "fused":
+            from cnn_convolution_gemm_gb300 import binding as B
+            N, H, W, C, E, Co = self.dims
+            return [("block:mbv2_fused",
+                     lambda: B.conv_mbv2_block_fwd(N, H, W, C, E, Co, self.x.data_ptr(),
+                                                   self.fpack.data_ptr(), self.b[1].data_ptr(),
+                                                   self.b[2].data_ptr(), False, self.y.data_ptr(),
+                                                   self.sh),
+                     sum(sp.flops() for sp in self.shapes), self.fused_bytes, "alu")]
         ins, outs = [self.x, self.t1, self.t2], [self.t1, self.t2, self.y]
         return [(f"{['expand', 'depthwise', 'project'][i]}:{self.algo_names[i]}",
                  (lambda l=layer, a=ins[i], o=outs[i], b=self.b[i]:
                   l.forward(a, b, out=o, stream=self.sh)),
                  sp.flops(), sp.traffic_bytes(2, 4), "hbm")
                 for i, (layer, sp) in enumerate(zip(self.layers, self.shapes))]
+
+    def kernel_work(self, label, work):
+        # the fused kernel is bound by its CUDA-core depthwise arithmetic: 9 FMAs
+        # (18 FLOPs) per t2 element; the 1x1 convolutions run on the tensor cores
+        if label == "mbv2_fused":
+            N, H, W, C, E, Co = self.dims
+            return 18 * N * H * W * E
+        return work
 
     def h2d(self):
         return [(self.xh, self.x)]
@@ -375,7 +439,10 @@ class MBv2Block(Workload):
                            act=2)
         ol.conv2d_f64(t2, d["w_project"].transpose(0, 3, 1, 2), d["b_project"])
         dt = time.perf_counter() - t0
-        f = sum(s.flops() for s in self.shapes) * n // 64
+        from cnn_convolution_gemm_gb300.workload import ConvShape
+        f = sum(s.flops() for s in (ConvShape(n, 24, 56, 56, 144, 1, 1),
+                                    ConvShape(n, 144, 56, 56, 144, 3, 3, 1, 1, 1, 144),
+                                    ConvShape(n, 144, 56, 56, 24, 1, 1)))  # no setup() needed
         return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": threads(), "kind": "oracle",
                 "sample": f"{n} of 64 images through the three layers", "seconds": round(dt, 3)}
 
@@ -731,6 +798,13 @@ def main():
             achieved = wl.kernel_work(kname, work) / (avg_ms * 1e-3) / 1e12
             peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
             unit = "TFLOP/s"
+        elif bound == "alu":
+            # CUDA-core fp32 FMA peak: SMs x 128 lanes x 2 FLOP x the maximum SM clock
+            achieved = wl.kernel_work(kname, work) / (avg_ms * 1e-3) / 1e12
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            mhz = peaks.get("sm_max_mhz", 2070.0)
+            peak = round(sms * 128 * 2 * mhz * 1e6 / 1e12, 2)
+            unit = "TFLOP/s"
         else:
             achieved = nbytes / (avg_ms * 1e-3) / 1e9
             peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
@@ -742,10 +816,14 @@ def main():
             if h == src_hash(KERNEL_SOURCE[kname]):
                 traffic = tb
         kind = "bf16 burst" if bound == "tensor" else "HBM copy"
+        psrc = (f"measured {kind} (MEASURED_PEAKS.json)" if peak_src == "measured"
+                else "fallback")
+        if bound == "alu":
+            psrc = ("derived: SMs x 128 fp32 lanes x 2 FLOP x max SM clock "
+                    f"({'MEASURED_PEAKS.json sm_max_mhz' if peak_src == 'measured' else 'fallback'})")
         roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-                    "frac": round(achieved / peak, 4), "traffic": traffic,
-                    "peak_source": f"measured {kind} (MEASURED_PEAKS.json)"
-                    if peak_src == "measured" else "fallback", "kernel": label,
+                    "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": psrc,
+                    "kernel": label,
                     "algorithmic_work_per_launch": wl.kernel_work(kname, work),
                     "algorithmic_bytes_per_launch": nbytes}
         if kname == "int8_igemm_tc":
