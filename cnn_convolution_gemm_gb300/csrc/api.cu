@@ -78,6 +78,18 @@ int gb_num_sms() {
   return g_num_sms[dev];
 }
 
+cudaError_t gb_set_smem_once(const void* func, int bytes) {
+  const int dev = current_device();
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> done;  // (kernel, device) -> bytes set
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = done.find({func, dev});
+  if (it != done.end() && it->second >= bytes) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[{func, dev}] = bytes;
+  return e;
+}
+
 unsigned long long gb_wait_limit_ns() {
   static unsigned long long v = [] {
     const char* e = getenv("GBCONV_WAIT_LIMIT_MS");

@@ -27,6 +27,9 @@ conv_status_t gb_fail(conv_status_t st, const char* fmt, ...);
 int* gb_device_error_word();
 // Number of SMs of the current device (cached).
 int gb_num_sms();
+// Raise a kernel's dynamic shared-memory limit, once per (kernel, device): the
+// attribute call costs host time on every launch otherwise.
+cudaError_t gb_set_smem_once(const void* func, int bytes);
 // Wait limit for device-side bounded waits, in nanoseconds (GBCONV_WAIT_LIMIT_MS).
 unsigned long long gb_wait_limit_ns();
 
@@ -55,10 +58,22 @@ int igemm_block_n(int algo);
 // Split-K request: ksplit > 1 cuts the reduction into ranges of kchunk k-steps
 // (64 channels of one filter tap each) and writes fp32 partial sums to
 // part[ksplit][N*OH*OW][K] instead of running the epilogue.
+//
+// Exact int8 output mode (i8_y set): the GEMM's N = 2 * i8_kout columns hold, per
+// 64 output channels, 64 columns of sums against the low weight nibbles
+// (w & 15) then 64 against the high parts (w - (w & 15)) / 16; the epilogue
+// forms t = 16 * hi + lo + i8_bias[k] in int32, requantises with i8_scale[k]
+// (fp32, round to nearest even), clamps to int8, optional ReLU, and stores
+// int8 [M][i8_kout].  Needs BN a multiple of 128 and no split.
 struct IgemmSplit {
   int ksplit = 1;
   int kchunk = 0;
   float* part = nullptr;
+  int8_t* i8_y = nullptr;
+  const int32_t* i8_bias = nullptr;
+  const float* i8_scale = nullptr;
+  int i8_kout = 0;
+  int i8_relu = 0;
 };
 int igemm_kiters(const gbconv_desc_s& d);
 cudaError_t launch_igemm_bf16(const gbconv_desc_s& d, int block_n, const void* x,

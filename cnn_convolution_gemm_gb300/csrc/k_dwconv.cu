@@ -420,7 +420,7 @@ cudaError_t launch_st(const gbconv_desc_s& d, const void* x, const void* w, cons
   auto kern = d.act == CONV_ACT_RELU6  ? pick_kernel<ST, 2>(has_res)
               : d.act == CONV_ACT_RELU ? pick_kernel<ST, 1>(has_res)
                                        : pick_kernel<ST, 0>(has_res);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+  cudaError_t e = gb_set_smem_once(reinterpret_cast<const void*>(kern), Cf::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<(unsigned)grid, threads, Cf::SMEM, st>>>(
       tm, p, static_cast<const __nv_bfloat16*>(w), bias, static_cast<const __nv_bfloat16*>(res),

@@ -66,6 +66,11 @@ struct IgemmParams {
   // tail rebalancing: work units from tail_start on cover the last partial
   // wave's tiles as two half-width (BN/2) units each
   int tail_start;
+  // exact int8 output (see IgemmSplit): y8[M][i8_kout]
+  int8_t* i8_y;
+  const int32_t* i8_bias;
+  const float* i8_scale;
+  int i8_kout, i8_relu;
 };
 
 enum { MODE_CONV = 0, MODE_BATCHED = 1 };
@@ -345,7 +350,50 @@ __global__ void __launch_bounds__(192, 1)
       const long long m = (long long)mt * BM + q * 32 + lane;
       const bool row_ok = m < p.M;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-      if (MODE == MODE_BATCHED || p.part) {
+      if (MODE == MODE_CONV && p.i8_y) {
+        // exact int8: each 128-column group of the tile holds 64 sums against
+        // the low weight nibbles, then 64 against the high parts, all exact
+        // integers in fp32; t = 16 * hi + lo + bias, requantised to int8 (the
+        // MegEngine Beta report's native int8 epilogue)
+#pragma unroll 1
+        // this group's 64 biases and scales, staged once in the warp's (here
+        // unused) staging box and read back as broadcasts
+        int32_t* sbi = reinterpret_cast<int32_t*>(sEpi + q * 2 * C::EPI_BOX);
+        float* ssc = reinterpret_cast<float*>(sbi + 64);
+        for (int g = 0; g < BN / 128; ++g) {
+          const int k0 = (nt * BN + g * 128) / 2;  // first output channel of the group
+          if (k0 >= p.i8_kout) break;
+          __syncwarp();  // the previous group's reads of the slice are done
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int kk = k0 + h * 32 + lane;
+            sbi[h * 32 + lane] = p.i8_bias ? __ldg(p.i8_bias + kk) : 0;
+            ssc[h * 32 + lane] = __ldg(p.i8_scale + kk);
+          }
+          __syncwarp();
+#pragma unroll 1
+          for (int c16 = 0; c16 < 4; ++c16) {
+            uint32_t lo[16], hi[16];
+            gb::tmem_ld_x16(tbase + g * 128 + c16 * 16, lo);
+            gb::tmem_ld_x16(tbase + g * 128 + 64 + c16 * 16, hi);
+            gb::tmem_ld_wait();
+            const int kb = k0 + c16 * 16;
+            uint32_t pk[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int tv = 16 * __float2int_rn(__uint_as_float(hi[i])) +
+                             __float2int_rn(__uint_as_float(lo[i])) + sbi[c16 * 16 + i];
+              int qv = __float2int_rn(__fmul_rn(__int2float_rn(tv), ssc[c16 * 16 + i]));
+              qv = qv > 127 ? 127 : (qv < -128 ? -128 : qv);
+              if (p.i8_relu && qv < 0) qv = 0;
+              pk[i >> 2] |= (uint32_t)(qv & 0xff) << (8 * (i & 3));
+            }
+            if (row_ok)
+              *reinterpret_cast<uint4*>(p.i8_y + m * p.i8_kout + kb) =
+                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+        }
+      } else if (MODE == MODE_BATCHED || p.part) {
         // fp32 outputs (batched products, split-K partials): 32-column boxes of
         // 32 rows staged with the 128-byte swizzle and written by TMA stores
         // through the fp32 map passed in the tm_r slot
@@ -541,6 +589,13 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   p.ksplit = split.ksplit > 1 ? split.ksplit : 1;
   p.kchunk = split.ksplit > 1 ? split.kchunk : p.kiters;
   p.part = split.part;
+  p.i8_y = split.i8_y;
+  p.i8_bias = split.i8_bias;
+  p.i8_scale = split.i8_scale;
+  p.i8_kout = split.i8_kout;
+  p.i8_relu = split.i8_relu;
+  if (p.i8_y && (BN % 128 != 0 || p.ksplit != 1 || p.i8_kout * 2 != d.K || p.i8_kout % 16))
+    return cudaErrorInvalidValue;
 
   CUtensorMap tmx, tmw;
   {
@@ -596,15 +651,15 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
                         strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(igemm_bf16_tc_kernel<BN, MODE_CONV, LIGHT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+  cudaError_t e = gb_set_smem_once(
+      reinterpret_cast<const void*>(igemm_bf16_tc_kernel<BN, MODE_CONV, LIGHT>), Cf::SMEM);
   if (e != cudaSuccess) return e;
   const int tiles = p.m_tiles * p.n_tiles * p.ksplit;
   const int slots = gb_num_sms() * (LIGHT ? 2 : 1);
   const int grid = tiles < slots ? tiles : slots;
   // a last wave that would leave most SMs idle runs as half-width units
   p.tail_start = tiles;
-  if (BN == 256 && p.ksplit == 1 && !LIGHT && tiles > grid) {
+  if (BN == 256 && p.ksplit == 1 && !LIGHT && !p.i8_y && tiles > grid) {
     const int rem = tiles % grid;
     if (rem > 0 && rem <= grid / 2) p.tail_start = tiles - rem;
   }
@@ -653,8 +708,8 @@ cudaError_t launch_batched_bn(int batch, int M, int N, int Kred, const void* A, 
                         CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(igemm_bf16_tc_kernel<BN, MODE_BATCHED>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+  cudaError_t e = gb_set_smem_once(
+      reinterpret_cast<const void*>(igemm_bf16_tc_kernel<BN, MODE_BATCHED>), Cf::SMEM);
   if (e != cudaSuccess) return e;
   const long long tiles = (long long)p.m_tiles * p.n_tiles * batch;
   const int grid = tiles < gb_num_sms() ? (int)tiles : gb_num_sms();
@@ -691,7 +746,8 @@ cudaError_t launch_igemm_bf16(const gbconv_desc_s& d, int block_n, const void* x
   // and memory, not by the operand pipeline: run two shallow CTAs per SM
   const int kiters = d.C == 8 ? gb_ceil_div(d.R * d.S, 8) : d.R * d.S * gb_ceil_div(d.C, BK);
   const int kper = split.ksplit > 1 ? split.kchunk : kiters;
-  const bool light = d.C != 8 && kper <= 8;
+  // (the exact int8 epilogue does more per output: two CTAs per SM up to 16 k-steps)
+  const bool light = d.C != 8 && (kper <= 8 || (split.i8_y && kper <= 16));
   switch (block_n) {
     case 64:
       return light ? launch_bn<64, true>(d, x, wpack, bias, res, y, err, wait_ns, st, split)

@@ -229,15 +229,13 @@ cudaError_t launch_igemm_int8(const gbconv_desc_s& d, const void* x, const void*
   auto yb = static_cast<int8_t*>(y);
   if (d.K > 64) {
     constexpr int smem = STAGES * (BM * BK + 128 * BK);
-    cudaError_t e = cudaFuncSetAttribute(igemm_int8_kernel<128>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = gb_set_smem_once(reinterpret_cast<const void*>(igemm_int8_kernel<128>), smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)mt, gb_ceil_div(d.K, 128));
     igemm_int8_kernel<128><<<grid, THREADS, smem, st>>>(p, xb, wb, yb);
   } else {
     constexpr int smem = STAGES * (BM * BK + 64 * BK);
-    cudaError_t e = cudaFuncSetAttribute(igemm_int8_kernel<64>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = gb_set_smem_once(reinterpret_cast<const void*>(igemm_int8_kernel<64>), smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)mt, gb_ceil_div(d.K, 64));
     igemm_int8_kernel<64><<<grid, THREADS, smem, st>>>(p, xb, wb, yb);

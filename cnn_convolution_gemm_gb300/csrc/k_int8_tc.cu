@@ -13,6 +13,16 @@
 //
 // Steps per call: int8 -> bf16 copy of the activations (workspace), split-K
 // implicit GEMM into fp32 partials (workspace), reduction + requant -> int8.
+//
+// Split-weight path (used whenever K % 64 == 0 and R*S*C <= 8704): each weight
+// is cut at prepack into w = 16 * wh + wl, wl = w & 15 in [0, 15] and wh in
+// [-8, 7].  Products x * wl are at most 128 * 15 = 1920 and x * wh at most
+// 128 * 8 = 1024 in magnitude, so an fp32 accumulator stays exact over
+// 8704 products (8704 * 1920 < 2^24): every ResNet int8 layer (at most 4608)
+// needs no split at all.  One implicit GEMM over 2K columns (per 64 output
+// channels: 64 low-part columns, 64 high-part columns) then finishes in its
+// own epilogue — t = 16 * hi + lo + bias, requant, ReLU, int8 store — so the
+// fp32 partials and the reduction pass disappear, at twice the tensor work.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -23,6 +33,16 @@
 namespace {
 
 constexpr int KCHUNK_MAX = 16;  // k-steps of 64 products per exact fp32 chunk
+constexpr int SPLITW_MAX = 8704;  // products per output that stay exact with split weights
+
+// the split-weight path applies (see the file comment) and its unsplit tile
+// grid fills the SMs; smaller grids keep split-K, which spreads the reduction
+bool split_weights(const gbconv_desc_s& d) {
+  if (d.K % 64 || (long long)d.R * d.S * (gb_ceil_div(d.C, 64) * 64) > SPLITW_MAX) return false;
+  const long long m_tiles = gb_ceil_div_ll((long long)d.N * d.OH * d.OW, 128);
+  const int n_tiles = d.K == 64 ? 1 : 2 * d.K / 256;
+  return m_tiles * n_tiles >= gb_num_sms();
+}
 
 // bf16 has 8 significant bits: every int8 value converts exactly.
 __global__ void int8_to_bf16_kernel(const int8_t* __restrict__ x, __nv_bfloat16* __restrict__ y,
@@ -53,6 +73,31 @@ __global__ void pack_int8_as_bf16_kernel(const int8_t* __restrict__ w,
     const int c = (int)(i % Cp);
     const long long krs = i / Cp;
     wp[i] = __float2bfloat16_rn(c < C ? (float)w[krs * C + c] : 0.f);
+  }
+}
+
+// int8 [K][RS][C] -> bf16 [2K][RS][Cp]: per 64 output channels, 64 rows of low
+// nibbles (w & 15) then 64 rows of high parts ((w - (w & 15)) / 16), zero
+// padded channels
+__global__ void pack_int8_split_kernel(const int8_t* __restrict__ w,
+                                       __nv_bfloat16* __restrict__ wp, int K, int RS, int C,
+                                       int Cp) {
+  const long long total = (long long)2 * K * RS * Cp;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int c = (int)(i % Cp);
+    const long long rowrs = i / Cp;
+    const int rs = (int)(rowrs % RS);
+    const int row = (int)(rowrs / RS);
+    const int k = (row >> 7) * 64 + (row & 63);  // output channel of this row
+    const bool high = (row & 64) != 0;
+    float v = 0.f;
+    if (c < C) {
+      const int wv = w[((long long)k * RS + rs) * C + c];
+      const int lo = wv & 15;
+      v = high ? (float)((wv - lo) / 16) : (float)lo;
+    }
+    wp[i] = __float2bfloat16_rn(v);  // |v| <= 15: exact
   }
 }
 
@@ -114,16 +159,23 @@ int grid_for(long long n) { return (int)std::min<long long>(gb_ceil_div_ll(n, 25
 
 size_t int8_tc_workspace_bytes(const gbconv_desc_s& d) {
   const Plan p = make_plan(d);
-  return p.x_bytes + p.part_bytes;
+  return split_weights(d) ? p.x_bytes : p.x_bytes + p.part_bytes;
 }
 
 size_t int8_tc_packed_bytes(const gbconv_desc_s& d) {
-  return (size_t)d.K * d.R * d.S * gb_ceil_div(d.C, 64) * 64 * 2;
+  return (size_t)(split_weights(d) ? 2 : 1) * d.K * d.R * d.S * gb_ceil_div(d.C, 64) * 64 * 2;
 }
 
 cudaError_t launch_pack_int8_tc_weights(const gbconv_desc_s& d, const void* w, void* wpack,
                                         cudaStream_t st) {
   const int Cp = gb_ceil_div(d.C, 64) * 64;
+  if (split_weights(d)) {
+    const long long total = (long long)2 * d.K * d.R * d.S * Cp;
+    pack_int8_split_kernel<<<grid_for(total), 256, 0, st>>>(
+        static_cast<const int8_t*>(w), static_cast<__nv_bfloat16*>(wpack), d.K, d.R * d.S, d.C,
+        Cp);
+    return cudaGetLastError();
+  }
   const long long total = (long long)d.K * d.R * d.S * Cp;
   pack_int8_as_bf16_kernel<<<grid_for(total), 256, 0, st>>>(
       static_cast<const int8_t*>(w), static_cast<__nv_bfloat16*>(wpack), d.K, d.R * d.S, d.C, Cp);
@@ -144,6 +196,17 @@ cudaError_t launch_int8_tc(const gbconv_desc_s& d, const void* x, const void* wp
   db.dtype = CONV_BF16;
   db.act = CONV_ACT_NONE;
   db.has_residual = 0;
+  if (split_weights(d)) {  // one GEMM over 2K columns, int8 written by its epilogue
+    db.K = 2 * d.K;
+    IgemmSplit sp;
+    sp.i8_y = static_cast<int8_t*>(y);
+    sp.i8_bias = bias;
+    sp.i8_scale = d.scale;
+    sp.i8_kout = d.K;
+    sp.i8_relu = d.act == CONV_ACT_RELU ? 1 : 0;
+    return launch_igemm_bf16(db, d.K == 64 ? 128 : 256, xb, wpack, nullptr, nullptr, y, err,
+                             wait_ns, st, sp);
+  }
   IgemmSplit sp;
   sp.ksplit = pl.ksplit;
   sp.kchunk = pl.kchunk;

@@ -540,8 +540,7 @@ cudaError_t launch_mbv2_block(int N, int H, int W, int cin, int E, int cout, con
   if (gb_encode_tiled(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims,
                       strides, box, estr, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(mbv2_block_kernel<144>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = gb_set_smem_once(reinterpret_cast<const void*>(mbv2_block_kernel<144>), C::SMEM);
   if (e != cudaSuccess) return e;
   const int grid = std::min(p.ntiles, gb_num_sms());
   mbv2_block_kernel<144><<<grid, THREADS, C::SMEM, st>>>(

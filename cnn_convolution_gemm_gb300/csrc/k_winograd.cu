@@ -373,9 +373,8 @@ cudaError_t run_winograd(const gbconv_desc_s& d, const void* x, const void* wpac
     if (gb_encode_tiled(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims,
                         strides, box, estr, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(input_transform_kernel<TT, F16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         InCfg<TT>::SMEM);
+    cudaError_t e = gb_set_smem_once(reinterpret_cast<const void*>(input_transform_kernel<TT, F16>),
+                                     InCfg<TT>::SMEM);
     if (e != cudaSuccess) return e;
   }
   for (int n0 = 0; n0 < d.N; n0 += nb_max) {

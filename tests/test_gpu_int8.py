@@ -49,6 +49,7 @@ def test_int8_resnet_stage_shapes_full_batch(C, HW, algo):
     (3, 32, 10, 10, 16, 3, 2, 1, False, True),   # stride 2, no ReLU
     (2, 96, 6, 6, 80, 1, 1, 0, True, False),     # 1x1, no bias, C not a 64 multiple
     (1, 64, 5, 5, 256, 3, 1, 2, True, True),     # pad 2 (many fully padded taps)
+    (1, 1024, 4, 5, 64, 3, 1, 1, True, True),    # 9216 products > the split-weight bound: chunked
 ])
 @pytest.mark.parametrize("algo", ALGOS)
 def test_int8_edge_cases(case, algo):
@@ -80,3 +81,27 @@ def test_int8_saturation_extremes(algo):
     ref = ol.conv2d_i8(nhwc_to_nchw(x), nhwc_to_nchw(w), None, scale, pad=1, relu=False)
     assert np.array_equal(y.cpu().numpy(), nchw_to_nhwc(ref))
     assert (ref == 127).any() and (ref == -128).any()
+
+
+def test_int8_split_weight_bound_extremes():
+    """The split-weight path at its largest exact sums: x = -128 everywhere and
+    w alternating 127 / -128 over C = 512 (4608 products per output), so the
+    low-nibble sums reach -128 * 15 * 4608 and the high-part sums -128 * 7 * 4608
+    (and +128 * 8 * 4608 for w = -128); requant into saturation both ways."""
+    torch = need_gpu()
+    from cnn_convolution_gemm_gb300 import binding as B
+    from cnn_convolution_gemm_gb300.layer import ConvLayer
+    dev = torch.device("cuda:0")
+    N, C, H, K = 2, 512, 7, 64
+    x = np.full((N, H, H, C), -128, np.int8)
+    w = np.where(np.arange(K)[:, None, None, None] % 2 == 0, 127, -128).astype(np.int8) * np.ones(
+        (K, 3, 3, C), np.int8)
+    scale = np.full(K, 1e-5, np.float32)
+    layer = ConvLayer(N, C, H, H, K, 3, 3, 1, 1, dtype=B.CONV_INT8,
+                      scale=torch.from_numpy(scale).to(dev))
+    layer.prepack(torch.from_numpy(w).to(dev), INT8_TC)
+    y = layer(torch.from_numpy(x).to(dev))
+    B.conv_sync_status(torch.cuda.current_stream().cuda_stream)
+    ref = ol.conv2d_i8(nhwc_to_nchw(x), nhwc_to_nchw(w), None, scale, pad=1, relu=False)
+    assert np.array_equal(y.cpu().numpy(), nchw_to_nhwc(ref))
+    assert (nchw_to_nhwc(ref) == -128).any() and (nchw_to_nhwc(ref) == 127).any()
