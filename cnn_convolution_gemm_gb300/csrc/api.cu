@@ -226,7 +226,7 @@ extern "C" conv_status_t conv_desc_get_output_dims(conv_desc_t d, int* OH, int* 
 static const char* const kAlgoNames[CONV_ALGO_COUNT] = {
     "direct", "igemm_tc_n64", "igemm_tc_n128", "igemm_tc_n256",
     "winograd_f2x2_3x3", "winograd_f6x6_3x3", "depthwise3x3", "int8_igemm_mma",
-    "int8_igemm_tc", "im2col_gemm"};
+    "int8_igemm_tc", "im2col_gemm", "stem_s2d_igemm"};
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -294,6 +294,9 @@ static bool applicable(const gbconv_desc_s& d, int algo, const char** why) {
       if (im2col_workspace_bytes(d) > (8ull << 30))
         return *why = "im2col matrix above 8 GiB", false;
       return true;
+    case CONV_ALGO_STEM_S2D:
+      if (d.dtype != CONV_BF16 || !nhwc) return *why = "needs bf16 NHWC", false;
+      return stem_s2d_applicable(d, why);
     default:
       return *why = "unknown algorithm", false;
   }
@@ -401,6 +404,7 @@ extern "C" conv_status_t conv_workspace_size(conv_desc_t d, conv_algo_t algo, si
     *bytes = winograd_workspace_bytes(*d, a == CONV_ALGO_WINO_F2 ? 2 : 6);
   if (a == CONV_ALGO_INT8_TC) *bytes = int8_tc_workspace_bytes(*d);
   if (a == CONV_ALGO_IM2COL_GEMM) *bytes = im2col_workspace_bytes(*d);
+  if (a == CONV_ALGO_STEM_S2D) *bytes = stem_s2d_workspace_bytes(*d);
   return ok_status();
 }
 
@@ -421,6 +425,7 @@ extern "C" conv_status_t conv_weights_packed_size(conv_desc_t d, conv_algo_t alg
     case CONV_ALGO_INT8_MMA: *bytes = (size_t)d->K * d->R * d->S * Cp64; break;
     case CONV_ALGO_INT8_TC: *bytes = int8_tc_packed_bytes(*d); break;
     case CONV_ALGO_IM2COL_GEMM: *bytes = im2col_packed_bytes(*d); break;
+    case CONV_ALGO_STEM_S2D: *bytes = stem_s2d_packed_bytes(*d); break;
     case CONV_ALGO_WINO_F2: *bytes = winograd_packed_bytes(*d, 2); break;
     case CONV_ALGO_WINO_F6: *bytes = winograd_packed_bytes(*d, 6); break;
     default: *bytes = user_weight_bytes(*d); break;
@@ -444,6 +449,7 @@ extern "C" conv_status_t conv_weights_prepack(conv_desc_t d, conv_algo_t algo, c
     case CONV_ALGO_INT8_MMA: e = launch_pack_int8_weights(*d, w, wpack, s); break;
     case CONV_ALGO_INT8_TC: e = launch_pack_int8_tc_weights(*d, w, wpack, s); break;
     case CONV_ALGO_IM2COL_GEMM: e = launch_pack_im2col_weights(*d, w, wpack, s); break;
+    case CONV_ALGO_STEM_S2D: e = launch_pack_stem_weights(*d, w, wpack, s); break;
     case CONV_ALGO_DEPTHWISE: e = launch_pack_dw_weights(*d, w, wpack, s); break;
     case CONV_ALGO_WINO_F2: e = launch_winograd_filter_transform(*d, 2, w, wpack, s); break;
     case CONV_ALGO_WINO_F6: e = launch_winograd_filter_transform(*d, 6, w, wpack, s); break;
@@ -486,6 +492,16 @@ static conv_status_t fwd_impl(const gbconv_desc_s& d, const void* x, const void*
         return gb_fail(CONV_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
       e = launch_im2col_gemm(d, x, wpack, static_cast<const float*>(bias), res, y, ws, err,
                              wait_ns, s);
+      break;
+    }
+    case CONV_ALGO_STEM_S2D: {
+      const size_t need = stem_s2d_workspace_bytes(d);
+      if (!ws || ws_bytes < need)
+        return gb_fail(CONV_ERR_WORKSPACE, "workspace of %zu bytes needed", need);
+      if (reinterpret_cast<uintptr_t>(ws) & 255u)
+        return gb_fail(CONV_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+      e = launch_stem_s2d(d, x, wpack, static_cast<const float*>(bias), res, y, ws, err, wait_ns,
+                          s);
       break;
     }
     case CONV_ALGO_INT8_TC: {
@@ -888,6 +904,7 @@ static bool implemented(int algo) {
     case CONV_ALGO_INT8_MMA:
     case CONV_ALGO_INT8_TC:
     case CONV_ALGO_IM2COL_GEMM:
+    case CONV_ALGO_STEM_S2D:
       return true;
     default:
       return false;

@@ -16,6 +16,7 @@ struct gbconv_desc_s {
   int has_residual;
   const float* scale;  // int8 requant scale [K] (device)
   int OH, OW;
+  int pad_hi_delta;    // padding after minus padding before (internal rewrites only; 0 = symmetric)
 };
 
 // Device-side error word codes (written by kernels, read by conv_sync_status).
@@ -155,3 +156,14 @@ cudaError_t launch_mbv2_block(int N, int H, int W, int cin, int E, int cout, con
                               const void* wpack, const float* b_dw, const float* b_proj,
                               int has_res, void* y, int* err, unsigned long long wait_ns,
                               cudaStream_t st);
+
+// Stride-2 convolutions over 8 channels as space-to-depth (32 channels) + a
+// stride-1 implicit GEMM with asymmetric padding; workspace = the rewritten input.
+bool stem_s2d_applicable(const gbconv_desc_s& d, const char** why);
+size_t stem_s2d_workspace_bytes(const gbconv_desc_s& d);
+size_t stem_s2d_packed_bytes(const gbconv_desc_s& d);
+cudaError_t launch_pack_stem_weights(const gbconv_desc_s& d, const void* w, void* wpack,
+                                     cudaStream_t st);
+cudaError_t launch_stem_s2d(const gbconv_desc_s& d, const void* x, const void* wpack,
+                            const float* bias, const void* res, void* y, void* ws, int* err,
+                            unsigned long long wait_ns, cudaStream_t st);

@@ -605,7 +605,8 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
     // Bounding box of the first filter tap's pixel: from -pad to
     // (dim - 1) + pad - dil*(R-1) (R == S is required).
     int lower[2] = {-d.pad, -d.pad};
-    int upper[2] = {d.pad - d.dil * (d.S - 1), d.pad - d.dil * (d.R - 1)};
+    const int pad_hi = d.pad + d.pad_hi_delta;  // padding after (equal to pad unless rewritten)
+    int upper[2] = {pad_hi - d.dil * (d.S - 1), pad_hi - d.dil * (d.R - 1)};
     cuuint32_t estr[4] = {1, (cuuint32_t)d.stride, (cuuint32_t)d.stride, 1};
     CUresult r = gb_encode_im2col(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x),
                                   dims, strides, lower, upper, narrow ? 8 : BK, BM, estr,

@@ -74,7 +74,9 @@ typedef int conv_algo_t;
 #define CONV_ALGO_INT8_MMA 7       /* int8 implicit GEMM on mma.sync, exact int32 acc.  */
 #define CONV_ALGO_INT8_TC 8        /* int8 on tcgen05 via exact bf16 chunks (workspace) */
 #define CONV_ALGO_IM2COL_GEMM 9    /* materialised im2col matrix + GEMM (workspace)     */
-#define CONV_ALGO_COUNT 10
+#define CONV_ALGO_STEM_S2D 10      /* stride-2 conv over 8 channels (the image stem) as
+                                      space-to-depth + stride-1 implicit GEMM (workspace) */
+#define CONV_ALGO_COUNT 11
 
 /* ---- descriptor --------------------------------------------------------- */
 

@@ -63,7 +63,16 @@ def test_algo_table_and_applicability(B):
     # C = 24 pads to one 64-channel block per filter tap
     e24 = B.conv_desc_create(64, 24, 56, 56, 144, 1, 1, 1, 0, 1, 1, B.CONV_BF16)
     assert B.conv_weights_packed_size(e24, B.CONV_ALGO_IGEMM_N64) == 144 * 64 * 2
-    for h in (d, dw, e24):
+    # the space-to-depth stem applies to stride-2 convs over 8 channels only
+    stem = B.conv_desc_create(64, 8, 224, 224, 64, 7, 7, 2, 3, 1, 1, B.CONV_BF16)
+    assert B.conv_algo_info(stem, B.CONV_ALGO_STEM_S2D)[2]
+    assert B.conv_algo_info(stem, B.CONV_ALGO_STEM_S2D)[1] == "stem_s2d_igemm"
+    assert B.conv_weights_packed_size(stem, B.CONV_ALGO_STEM_S2D) == 64 * 16 * 64 * 2
+    assert B.conv_workspace_size(stem, B.CONV_ALGO_STEM_S2D) == 64 * 112 * 112 * 32 * 2
+    assert not B.conv_algo_info(d, B.CONV_ALGO_STEM_S2D)[2]  # C = 256, stride 1
+    odd = B.conv_desc_create(1, 8, 15, 16, 64, 7, 7, 2, 3, 1, 1, B.CONV_BF16)
+    assert not B.conv_algo_info(odd, B.CONV_ALGO_STEM_S2D)[2]  # odd height
+    for h in (d, dw, e24, stem, odd):
         B.conv_desc_destroy(h)
 
 
