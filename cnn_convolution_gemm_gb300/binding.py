@@ -20,7 +20,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libgbconv.so")
 
 CONV_BF16, CONV_F32, CONV_INT8 = 0, 1, 2
-CONV_NHWC, CONV_NCHW = 0, 1
+CONV_NHWC, CONV_NCHW, CONV_NC32HW32 = 0, 1, 2
 CONV_ACT_NONE, CONV_ACT_RELU, CONV_ACT_RELU6 = 0, 1, 2
 
 CONV_ALGO_AUTO = -1
@@ -70,6 +70,8 @@ SIGNATURES = {
     "conv_fastrun_load": (_i, [_cp]),
     "conv_fastrun_clear": (_i, []),
     "conv_nchw_f32_to_nhwc_bf16": (_i, [_p, _p, _i, _i, _i, _i, _i, _p]),
+    "conv_nchw_i8_to_nc32hw32": (_i, [_p, _p, _i, _i, _i, _i, _p]),
+    "conv_nc32hw32_to_nchw_i8": (_i, [_p, _p, _i, _i, _i, _i, _p]),
     "conv_nhwc_bf16_to_nchw_f32": (_i, [_p, _p, _i, _i, _i, _i, _i, _p]),
     "conv_maxpool2d_nhwc_bf16": (_i, [_p, _p, _i, _i, _i, _i, _i, _i, _i, _p]),
     "conv_global_avgpool_nhwc_bf16": (_i, [_p, _p, _i, _i, _i, _i, _p]),
@@ -252,6 +254,16 @@ def conv_fastrun_load(path):
 
 def conv_fastrun_clear():
     _check(load_library().conv_fastrun_clear(), "conv_fastrun_clear")
+
+
+def conv_nchw_i8_to_nc32hw32(x_ptr, y_ptr, N, C, H, W, stream=None):
+    _check(load_library().conv_nchw_i8_to_nc32hw32(_ptr(x_ptr), _ptr(y_ptr), N, C, H, W,
+                                                   _stream(stream)), "conv_nchw_i8_to_nc32hw32")
+
+
+def conv_nc32hw32_to_nchw_i8(x_ptr, y_ptr, N, C, H, W, stream=None):
+    _check(load_library().conv_nc32hw32_to_nchw_i8(_ptr(x_ptr), _ptr(y_ptr), N, C, H, W,
+                                                   _stream(stream)), "conv_nc32hw32_to_nchw_i8")
 
 
 def conv_nchw_f32_to_nhwc_bf16(x_ptr, y_ptr, N, C, H, W, C_out, stream=None):

@@ -188,10 +188,14 @@ extern "C" conv_status_t conv_desc_destroy(conv_desc_t desc) {
 
 extern "C" conv_status_t conv_desc_set_layout(conv_desc_t d, conv_layout_t layout) {
   if (!d) return gb_fail(CONV_ERR_BAD_PARAM, "desc is NULL");
-  if (layout != CONV_NHWC && layout != CONV_NCHW)
+  if (layout != CONV_NHWC && layout != CONV_NCHW && layout != CONV_NC32HW32)
     return gb_fail(CONV_ERR_BAD_PARAM, "unknown layout");
   if (layout == CONV_NCHW && d->dtype != CONV_F32)
     return gb_fail(CONV_ERR_UNSUPPORTED, "NCHW is accepted for CONV_F32 only");
+  if (layout == CONV_NC32HW32 &&
+      (d->dtype != CONV_INT8 || d->C % 32 || d->K % 32 || d->groups != 1))
+    return gb_fail(CONV_ERR_UNSUPPORTED,
+                   "NC32HW32 is accepted for CONV_INT8 with C, K multiples of 32, groups 1");
   d->layout = layout;
   return ok_status();
 }
@@ -278,7 +282,8 @@ static bool applicable(const gbconv_desc_s& d, int algo, const char** why) {
       if (d.C % 16 || d.K % 16) return *why = "needs C and K multiples of 16", false;
       return true;
     case CONV_ALGO_INT8_TC:
-      if (d.dtype != CONV_INT8 || !nhwc) return *why = "needs int8 NHWC", false;
+      if (d.dtype != CONV_INT8 || !(nhwc || d.layout == CONV_NC32HW32))
+        return *why = "needs int8 NHWC or NC32HW32", false;
       if (!d.scale) return *why = "int8 needs a requant scale", false;
       if (d.groups != 1 || d.R != d.S) return *why = "needs groups == 1, square kernel", false;
       if (d.C % 16 || d.K % 8) return *why = "needs C % 16 == 0 and K % 8 == 0", false;
@@ -827,6 +832,22 @@ extern "C" conv_status_t conv_nhwc_bf16_to_nchw_f32(const void* x, float* y, int
   cudaError_t e =
       launch_nhwc_bf16_to_nchw_f32(x, y, N, C, H, W, C_in, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ok_status() : cuda_fail(e, "nhwc->nchw");
+}
+
+extern "C" conv_status_t conv_nchw_i8_to_nc32hw32(const void* x, void* y, int N, int C, int H,
+                                                  int W, void* stream) {
+  if (!x || !y) return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
+  if (N <= 0 || C <= 0 || H <= 0 || W <= 0) return gb_fail(CONV_ERR_BAD_PARAM, "bad sizes");
+  cudaError_t e = launch_nc32_convert(x, y, N, C, H, W, 1, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok_status() : cuda_fail(e, "nchw->nc32hw32");
+}
+
+extern "C" conv_status_t conv_nc32hw32_to_nchw_i8(const void* x, void* y, int N, int C, int H,
+                                                  int W, void* stream) {
+  if (!x || !y) return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
+  if (N <= 0 || C <= 0 || H <= 0 || W <= 0) return gb_fail(CONV_ERR_BAD_PARAM, "bad sizes");
+  cudaError_t e = launch_nc32_convert(x, y, N, C, H, W, 0, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok_status() : cuda_fail(e, "nc32hw32->nchw");
 }
 
 extern "C" conv_status_t conv_maxpool2d_nhwc_bf16(const void* x, void* y, int N, int C, int H,

@@ -75,6 +75,7 @@ struct IgemmSplit {
   const float* i8_scale = nullptr;
   int i8_kout = 0;
   int i8_relu = 0;
+  int i8_nc32 = 0;  // int8 output in NC32HW32 (else NHWC)
 };
 int igemm_kiters(const gbconv_desc_s& d);
 cudaError_t launch_igemm_bf16(const gbconv_desc_s& d, int block_n, const void* x,
@@ -167,3 +168,7 @@ cudaError_t launch_pack_stem_weights(const gbconv_desc_s& d, const void* w, void
 cudaError_t launch_stem_s2d(const gbconv_desc_s& d, const void* x, const void* wpack,
                             const float* bias, const void* res, void* y, void* ws, int* err,
                             unsigned long long wait_ns, cudaStream_t st);
+
+// NCHW int8 <-> NC32HW32 int8 (to_nc32: 1 = NCHW -> NC32HW32, 0 = back).
+cudaError_t launch_nc32_convert(const void* x, void* y, int N, int C, int H, int W, int to_nc32,
+                                cudaStream_t st);

@@ -30,9 +30,19 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
   return __float2bfloat16_rn(v);
 }
 
+// p.nhwc: 1 NHWC, 0 NCHW, 2 NC32HW32 (int8 only)
 __device__ __forceinline__ void decompose(long long i, const DirectParams& p, int& n, int& k,
                                           int& oh, int& ow) {
-  if (p.nhwc) {
+  if (p.nhwc == 2) {
+    const int klo = (int)(i % 32);
+    i /= 32;
+    ow = (int)(i % p.OW);
+    i /= p.OW;
+    oh = (int)(i % p.OH);
+    i /= p.OH;
+    k = (int)(i % (p.K / 32)) * 32 + klo;
+    n = (int)(i / (p.K / 32));
+  } else if (p.nhwc) {
     k = (int)(i % p.K);
     i /= p.K;
     ow = (int)(i % p.OW);
@@ -110,8 +120,11 @@ __global__ void direct_conv_int8_kernel(DirectParams p, const int8_t* __restrict
         if (iw < 0 || iw >= p.W) continue;
         for (int cc = 0; cc < p.Cg; ++cc) {
           const int c = g * p.Cg + cc;
-          acc += (int)x[(((long long)n * p.H + ih) * p.W + iw) * p.C + c] *
-                 (int)w[(((long long)k * p.R + r) * p.S + s) * p.Cg + cc];
+          const long long xi =
+              p.nhwc == 2 ? ((((long long)n * (p.C / 32) + c / 32) * p.H + ih) * p.W + iw) * 32 +
+                                (c & 31)
+                          : (((long long)n * p.H + ih) * p.W + iw) * p.C + c;
+          acc += (int)x[xi] * (int)w[(((long long)k * p.R + r) * p.S + s) * p.Cg + cc];
         }
       }
     }
@@ -129,7 +142,8 @@ __global__ void direct_conv_int8_kernel(DirectParams p, const int8_t* __restrict
 cudaError_t launch_direct(const gbconv_desc_s& d, const void* x, const void* w, const void* bias,
                           const void* res, void* y, cudaStream_t st) {
   DirectParams p{d.N, d.C, d.H, d.W, d.K, d.R, d.S, d.stride, d.pad, d.dil, d.OH, d.OW,
-                 d.C / d.groups, d.K / d.groups, d.act, d.layout == CONV_NHWC ? 1 : 0};
+                 d.C / d.groups, d.K / d.groups, d.act,
+                 d.layout == CONV_NHWC ? 1 : (d.layout == CONV_NC32HW32 ? 2 : 0)};
   const long long total = (long long)d.N * d.K * d.OH * d.OW;
   const int block = 256;
   const int grid = (int)std::min<long long>(gb_ceil_div_ll(total, block), 148LL * 64);

@@ -70,7 +70,7 @@ struct IgemmParams {
   int8_t* i8_y;
   const int32_t* i8_bias;
   const float* i8_scale;
-  int i8_kout, i8_relu;
+  int i8_kout, i8_relu, i8_nc32;
 };
 
 enum { MODE_CONV = 0, MODE_BATCHED = 1 };
@@ -388,9 +388,15 @@ __global__ void __launch_bounds__(192, 1)
               if (p.i8_relu && qv < 0) qv = 0;
               pk[i >> 2] |= (uint32_t)(qv & 0xff) << (8 * (i & 3));
             }
-            if (row_ok)
-              *reinterpret_cast<uint4*>(p.i8_y + m * p.i8_kout + kb) =
-                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            if (row_ok) {
+              // NHWC: row m, channel kb; NC32HW32: block kb/32 of image m / (OH*OW)
+              long long off = m * p.i8_kout + kb;
+              if (p.i8_nc32) {
+                const long long ohw = (long long)p.OH * p.OW, img = m / ohw;
+                off = ((img * (p.i8_kout / 32) + kb / 32) * ohw + (m - img * ohw)) * 32 + (kb & 31);
+              }
+              *reinterpret_cast<uint4*>(p.i8_y + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
           }
         }
       } else if (MODE == MODE_BATCHED || p.part) {
@@ -594,6 +600,7 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   p.i8_scale = split.i8_scale;
   p.i8_kout = split.i8_kout;
   p.i8_relu = split.i8_relu;
+  p.i8_nc32 = split.i8_nc32;
   if (p.i8_y && (BN % 128 != 0 || p.ksplit != 1 || p.i8_kout * 2 != d.K || p.i8_kout % 16))
     return cudaErrorInvalidValue;
 

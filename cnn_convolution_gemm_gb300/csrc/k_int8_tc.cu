@@ -44,12 +44,20 @@ bool split_weights(const gbconv_desc_s& d) {
   return m_tiles * n_tiles >= gb_num_sms();
 }
 
-// bf16 has 8 significant bits: every int8 value converts exactly.
+// bf16 has 8 significant bits: every int8 value converts exactly.  Output NHWC
+// bf16, 16 channels per thread; the int8 input is NHWC, or NC32HW32 (nc32 = 1:
+// the same 16 channels are one 16-byte half of a 32-channel block vector).
 __global__ void int8_to_bf16_kernel(const int8_t* __restrict__ x, __nv_bfloat16* __restrict__ y,
-                                    long long n16) {
+                                    long long n16, int C, long long HW, int nc32) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n16;
        i += (long long)gridDim.x * blockDim.x) {
-    const int4 v = reinterpret_cast<const int4*>(x)[i];
+    long long src = i;  // in 16-byte units
+    if (nc32) {
+      const int j = (int)(i % (C / 16));  // 16-channel group of the pixel
+      const long long pix = i / (C / 16), n = pix / HW;
+      src = ((n * (C / 32) + j / 2) * HW + (pix - n * HW)) * 2 + (j & 1);
+    }
+    const int4 v = reinterpret_cast<const int4*>(x)[src];
     const int8_t* b = reinterpret_cast<const int8_t*>(&v);
     uint4 o[2];
     uint32_t* ou = reinterpret_cast<uint32_t*>(o);
@@ -102,10 +110,11 @@ __global__ void pack_int8_split_kernel(const int8_t* __restrict__ w,
 }
 
 // y[m][n] = requant(sum_b part[b][m][n] + bias[n]); 4 channels per thread
+// (y in NHWC, or NC32HW32 when nc32 = 1; ohw = OH * OW)
 __global__ void reduce_requant_kernel(const float* __restrict__ part, int ksplit, long long MK,
                                       int K, const int32_t* __restrict__ bias,
                                       const float* __restrict__ scale, int relu,
-                                      int8_t* __restrict__ y) {
+                                      int8_t* __restrict__ y, long long ohw, int nc32) {
   const long long n4 = MK / 4;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
        i += (long long)gridDim.x * blockDim.x) {
@@ -128,7 +137,12 @@ __global__ void reduce_requant_kernel(const float* __restrict__ part, int ksplit
       if (relu && q < 0) q = 0;
       ob[j] = (int8_t)q;
     }
-    reinterpret_cast<char4*>(y)[i] = o;
+    long long dst = i;  // in 4-byte units
+    if (nc32) {
+      const long long m = (i * 4) / K, img = m / ohw;
+      dst = (((img * (K / 32) + n0 / 32) * ohw + (m - img * ohw)) * 32 + (n0 & 31)) / 4;
+    }
+    reinterpret_cast<char4*>(y)[dst] = o;
   }
 }
 
@@ -189,7 +203,9 @@ cudaError_t launch_int8_tc(const gbconv_desc_s& d, const void* x, const void* wp
   __nv_bfloat16* xb = static_cast<__nv_bfloat16*>(ws);
   float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.x_bytes);
   const long long n16 = (long long)d.N * d.H * d.W * d.C / 16;
-  int8_to_bf16_kernel<<<grid_for(n16), 256, 0, st>>>(static_cast<const int8_t*>(x), xb, n16);
+  const int nc32 = d.layout == CONV_NC32HW32 ? 1 : 0;
+  int8_to_bf16_kernel<<<grid_for(n16), 256, 0, st>>>(static_cast<const int8_t*>(x), xb, n16, d.C,
+                                                     (long long)d.H * d.W, nc32);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   gbconv_desc_s db = d;  // the same convolution over the bf16 copy
@@ -204,6 +220,7 @@ cudaError_t launch_int8_tc(const gbconv_desc_s& d, const void* x, const void* wp
     sp.i8_scale = d.scale;
     sp.i8_kout = d.K;
     sp.i8_relu = d.act == CONV_ACT_RELU ? 1 : 0;
+    sp.i8_nc32 = nc32;
     return launch_igemm_bf16(db, d.K == 64 ? 128 : 256, xb, wpack, nullptr, nullptr, y, err,
                              wait_ns, st, sp);
   }
@@ -216,6 +233,7 @@ cudaError_t launch_int8_tc(const gbconv_desc_s& d, const void* x, const void* wp
   const long long MK = (long long)d.N * d.OH * d.OW * d.K;
   reduce_requant_kernel<<<grid_for(MK / 4), 256, 0, st>>>(part, pl.ksplit, MK, d.K, bias, d.scale,
                                                           d.act == CONV_ACT_RELU ? 1 : 0,
-                                                          static_cast<int8_t*>(y));
+                                                          static_cast<int8_t*>(y),
+                                                          (long long)d.OH * d.OW, nc32);
   return cudaGetLastError();
 }

@@ -187,3 +187,39 @@ cudaError_t launch_fill_random(void* p, size_t bytes, int elem_bytes, uint32_t s
                                                      seed);
   return cudaGetLastError();
 }
+
+namespace {
+// NCHW int8 [N][C][H][W] <-> NC32HW32 int8 [N][ceil(C/32)][H][W][32]; one byte
+// per thread, indexed by the NC32HW32 element (channels past C read as 0 going
+// in, are skipped going out)
+__global__ void nc32_convert_kernel(const int8_t* __restrict__ x, int8_t* __restrict__ y, int N,
+                                    int C, long long HW, int to_nc32) {
+  const int CB = (C + 31) / 32;
+  const long long total = (long long)N * CB * HW * 32;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int cl = (int)(i % 32);
+    const long long t = i / 32;
+    const long long hw = t % HW;
+    const long long nb = t / HW;
+    const int cb = (int)(nb % CB);
+    const long long n = nb / CB;
+    const int c = cb * 32 + cl;
+    const long long nchw = (n * C + c) * HW + hw;
+    if (to_nc32)
+      y[i] = c < C ? x[nchw] : (int8_t)0;
+    else if (c < C)
+      y[nchw] = x[i];
+  }
+}
+}  // namespace
+
+cudaError_t launch_nc32_convert(const void* x, void* y, int N, int C, int H, int W, int to_nc32,
+                                cudaStream_t st) {
+  const long long total = (long long)N * ((C + 31) / 32) * H * W * 32;
+  const int grid = (int)std::min<long long>((total + 255) / 256, 152LL * 32);
+  nc32_convert_kernel<<<grid, 256, 0, st>>>(static_cast<const int8_t*>(x),
+                                            static_cast<int8_t*>(y), N, C, (long long)H * W,
+                                            to_nc32);
+  return cudaGetLastError();
+}

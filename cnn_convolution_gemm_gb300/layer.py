@@ -54,6 +54,8 @@ class ConvLayer:
         N, K = self.shape[0], self.shape[4]
         if self.layout == B.CONV_NHWC:
             return (N, self.OH, self.OW, K)
+        if self.layout == B.CONV_NC32HW32:
+            return (N, K // 32, self.OH, self.OW, 32)
         return (N, K, self.OH, self.OW)
 
     def applicable_algos(self):

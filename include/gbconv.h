@@ -56,7 +56,12 @@ typedef enum { CONV_BF16 = 0, CONV_F32 = 1, CONV_INT8 = 2 } conv_dtype_t;
 
 /* Activation layout ([MegEngine] "Inference Layout").  NHWC is the device
  * layout of every fast kernel; NCHW is accepted for CONV_F32 only. */
-typedef enum { CONV_NHWC = 0, CONV_NCHW = 1 } conv_layout_t;
+/* NC32HW32 (int8 only): channel blocks of 32, element (n, c, h, w) at
+ * (((n * C/32 + c/32) * H + h) * W + w) * 32 + c % 32 — the GPU counterpart of
+ * the pages' NCHWX layouts ([MegEngine] "Inference Layout"; [Beta] NCHW44):
+ * each pixel's 32 channels of a block are one 32-byte vector.  Needs C and K
+ * multiples of 32; weights stay [K][R][S][C]. */
+typedef enum { CONV_NHWC = 0, CONV_NCHW = 1, CONV_NC32HW32 = 2 } conv_layout_t;
 
 typedef enum { CONV_ACT_NONE = 0, CONV_ACT_RELU = 1, CONV_ACT_RELU6 = 2 } conv_act_t;
 
@@ -231,6 +236,12 @@ conv_status_t conv_nchw_f32_to_nhwc_bf16(const float* x, void* y, int N, int C, 
 /* NHWC bf16 (C_in >= C channels, first C used) -> NCHW fp32. */
 conv_status_t conv_nhwc_bf16_to_nchw_f32(const void* x, float* y, int N, int C, int H, int W,
                                          int C_in, void* stream);
+/* NCHW int8 -> NC32HW32 int8 with ceil(C/32) channel blocks, channels past C
+ * zero; and back (the first C channels).  Stream-ordered. */
+conv_status_t conv_nchw_i8_to_nc32hw32(const void* x, void* y, int N, int C, int H, int W,
+                                       void* stream);
+conv_status_t conv_nc32hw32_to_nchw_i8(const void* x, void* y, int N, int C, int H, int W,
+                                       void* stream);
 /* Max pooling, NHWC bf16, window k x k, stride, pad (outside = -inf). */
 conv_status_t conv_maxpool2d_nhwc_bf16(const void* x, void* y, int N, int C, int H, int W, int k,
                                        int stride, int pad, void* stream);

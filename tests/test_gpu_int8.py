@@ -105,3 +105,58 @@ def test_int8_split_weight_bound_extremes():
     ref = ol.conv2d_i8(nhwc_to_nchw(x), nhwc_to_nchw(w), None, scale, pad=1, relu=False)
     assert np.array_equal(y.cpu().numpy(), nchw_to_nhwc(ref))
     assert (nchw_to_nhwc(ref) == -128).any() and (nchw_to_nhwc(ref) == 127).any()
+
+
+def _to_nc32(a_nchw):
+    """NCHW -> NC32HW32 by the layout's definition (numpy reshape), channels padded."""
+    N, C, H, W = a_nchw.shape
+    cb = (C + 31) // 32
+    p = np.zeros((N, cb * 32, H, W), a_nchw.dtype)
+    p[:, :C] = a_nchw
+    return np.ascontiguousarray(p.reshape(N, cb, 32, H, W).transpose(0, 1, 3, 4, 2))
+
+
+def test_nc32hw32_conversion_roundtrip():
+    torch = need_gpu()
+    from cnn_convolution_gemm_gb300 import binding as B
+    from cnn_convolution_gemm_gb300 import synth
+    dev = torch.device("cuda:0")
+    N, C, H, W = 3, 40, 5, 7  # C not a multiple of 32: the second block is padded
+    x = synth.int8_uniform((N, C, H, W), 11)
+    xd = torch.from_numpy(x).to(dev)
+    nc = torch.full((N, 2, H, W, 32), 77, dtype=torch.int8, device=dev)
+    back = torch.zeros((N, C, H, W), dtype=torch.int8, device=dev)
+    sh = torch.cuda.current_stream().cuda_stream
+    B.conv_nchw_i8_to_nc32hw32(xd.data_ptr(), nc.data_ptr(), N, C, H, W, sh)
+    B.conv_nc32hw32_to_nchw_i8(nc.data_ptr(), back.data_ptr(), N, C, H, W, sh)
+    torch.cuda.synchronize()
+    assert np.array_equal(nc.cpu().numpy(), _to_nc32(x))
+    assert np.array_equal(back.cpu().numpy(), x)
+
+
+@pytest.mark.parametrize("case", [
+    # N, C, H, W, K, algo — tcgen05 split-weight path (grid >= SMs), its split-K
+    # fallback (K not a multiple of 64), and the direct kernel
+    (32, 64, 28, 28, 64, INT8_TC),
+    (2, 64, 14, 14, 96, INT8_TC),
+    (2, 32, 6, 5, 64, 0),
+])
+def test_int8_nc32hw32_layout(case):
+    """int8 conv with NC32HW32 input and output: bit-exact against the oracle."""
+    torch = need_gpu()
+    from cnn_convolution_gemm_gb300 import binding as B
+    from cnn_convolution_gemm_gb300 import synth
+    from cnn_convolution_gemm_gb300.layer import ConvLayer
+    N, C, H, W, K, algo = case
+    dev = torch.device("cuda:0")
+    x = synth.int8_uniform((N, C, H, W), 21)  # NCHW
+    w = synth.int8_uniform((K, 3, 3, C), 22)
+    scale = synth.uniform((K,), 1e-4, 1e-3, 23)
+    b = synth.int32_uniform((K,), 24)
+    layer = ConvLayer(N, C, H, W, K, 3, 3, 1, 1, dtype=B.CONV_INT8, layout=B.CONV_NC32HW32,
+                      act=B.CONV_ACT_RELU, scale=torch.from_numpy(scale).to(dev))
+    layer.prepack(torch.from_numpy(w).to(dev), algo)
+    y = layer(torch.from_numpy(_to_nc32(x)).to(dev), torch.from_numpy(b).to(dev))
+    B.conv_sync_status(torch.cuda.current_stream().cuda_stream)
+    ref = ol.conv2d_i8(x, nhwc_to_nchw(w), b, scale, pad=1, relu=True)
+    assert np.array_equal(y.cpu().numpy(), _to_nc32(ref))

@@ -109,6 +109,24 @@ def test_fused_block_argument_errors(B):
     assert e.value.status_name == "CONV_ERR_ALIGNMENT"
 
 
+def test_nc32hw32_layout_validation(B):
+    # the blocked int8 layout: int8 only, C and K multiples of 32, groups 1
+    bf = B.conv_desc_create(1, 64, 8, 8, 64, 3, 3, 1, 1, 1, 1, B.CONV_BF16)
+    with pytest.raises(B.GbconvError) as e:
+        B.conv_desc_set_layout(bf, B.CONV_NC32HW32)
+    assert e.value.status_name == "CONV_ERR_UNSUPPORTED"
+    i48 = B.conv_desc_create(1, 48, 8, 8, 64, 3, 3, 1, 1, 1, 1, B.CONV_INT8)
+    with pytest.raises(B.GbconvError):
+        B.conv_desc_set_layout(i48, B.CONV_NC32HW32)
+    i64 = B.conv_desc_create(1, 64, 8, 8, 64, 3, 3, 1, 1, 1, 1, B.CONV_INT8)
+    B.conv_desc_set_layout(i64, B.CONV_NC32HW32)
+    B.conv_desc_set_requant(i64, 0x1000)  # a device address stand-in: no call runs here
+    ok = {n: a for _, n, a in (B.conv_algo_info(i64, i) for i in range(B.CONV_ALGO_COUNT))}
+    assert ok["int8_igemm_tc"] and ok["direct"] and not ok["int8_igemm_mma"]
+    for h in (bf, i48, i64):
+        B.conv_desc_destroy(h)
+
+
 def test_status_strings(B):
     assert B.conv_status_string(0) == "CONV_OK"
     assert B.conv_status_string(6) == "CONV_ERR_TIMEOUT"
