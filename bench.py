@@ -9,6 +9,7 @@ the layer over the batch with the algorithm Fast-Run picked for the shape
 Other workloads (--workload):
   single_layer  1 x 32 x 28 x 28 fp32 NCHW, 32 filters 3x3: boundary
                 conversion to NHWC bf16, conv, conversion back
+  resnet3x3_tf32  the headline layer with fp32 NHWC tensors on the tf32 path
   mbv2_block    MobileNetV2 inverted residual, N=64, 56x56: 1x1 24->144 +
                 ReLU6, depthwise 3x3 + ReLU6, 1x1 144->24.  By default the
                 fused one-kernel block and the three-layer chain (each layer's
@@ -273,6 +274,38 @@ class ResNetLayer(Workload):
         return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": threads(), "kind": "oracle",
                 "sample": f"{n} of 32 images, all 256 output channels ({f / 1e9:.1f} GFLOP)",
                 "seconds": round(dt, 3)}
+
+
+class ResNetLayerTF32(ResNetLayer):
+    """The same layer with fp32 tensors on the tf32 implicit GEMM."""
+    name = "resnet_conv3x3_c256_k256_56x56_n32_f32_nhwc"
+    metric = "conv TFLOP/s (direct-equivalent), ResNet 3x3 256->256 @56x56, batch 32, fp32 (tf32)"
+    dtype = "tf32"
+
+    def setup(self, dev, rank, args):
+        import torch
+        from cnn_convolution_gemm_gb300 import binding as B
+        from cnn_convolution_gemm_gb300 import synth
+        from cnn_convolution_gemm_gb300.layer import ConvLayer
+        from cnn_convolution_gemm_gb300.workload import ConvShape
+        self.shape = ConvShape(32, 256, 56, 56, 256, 3, 3, 1, 1)
+        x, w, b = synth.resnet_3x3_layer(seed=rank)
+        self.xh = torch.from_numpy(x).pin_memory()
+        self.x = self.xh.to(dev)
+        self.b = torch.from_numpy(b).to(dev)
+        self.layer = ConvLayer(32, 256, 56, 56, 256, 3, 3, 1, 1, dtype=B.CONV_F32)
+        self.sh = torch.cuda.current_stream().cuda_stream
+        a, self.fastrun_ms = fastrun_pick(self.layer, self.sh, args, B)
+        self.layer.prepack(torch.from_numpy(w).to(dev), a)
+        self.algo_name = B.conv_algo_info(self.layer.desc, a)[1]
+        self.y = torch.empty(self.layer.output_shape, dtype=torch.float32, device=dev)
+        self.yh = torch.empty(self.layer.output_shape, dtype=torch.float32).pin_memory()
+
+    def groups(self):
+        return [(self.algo_name, lambda: self.layer.forward(self.x, self.b, out=self.y,
+                                                            stream=self.sh),
+                 self.shape.flops(), self.shape.traffic_bytes(4, 4),
+                 "tf32" if self.algo_name == "igemm_tf32" else "alu")]
 
 
 class SingleLayer(Workload):
@@ -607,7 +640,8 @@ class ResNet50W(Workload):
                           f"({flops / 1e9:.2f} GFLOP)", "seconds": round(dt, 3)}
 
 
-WORKLOADS = {"resnet3x3": ResNetLayer, "single_layer": SingleLayer, "mbv2_block": MBv2Block,
+WORKLOADS = {"resnet3x3": ResNetLayer, "resnet3x3_tf32": ResNetLayerTF32,
+             "single_layer": SingleLayer, "mbv2_block": MBv2Block,
              "int8_stages": Int8Stages, "resnet50": ResNet50W}
 
 
@@ -799,6 +833,11 @@ def main():
             achieved = wl.kernel_work(kname, work) / (avg_ms * 1e-3) / 1e12
             peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
             unit = "TFLOP/s"
+        elif bound == "tf32":
+            # tf32 peak = the measured bf16 peak x the nominal tf32 / bf16 ratio (1.1 / 2.25)
+            achieved = wl.kernel_work(kname, work) / (avg_ms * 1e-3) / 1e12
+            peak = round(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) * 1.1 / 2.25, 1)
+            unit = "TFLOP/s"
         elif bound == "alu":
             # CUDA-core fp32 FMA peak: SMs x 128 lanes x 2 FLOP x the maximum SM clock
             achieved = wl.kernel_work(kname, work) / (avg_ms * 1e-3) / 1e12
@@ -819,6 +858,10 @@ def main():
         kind = "bf16 burst" if bound == "tensor" else "HBM copy"
         psrc = (f"measured {kind} (MEASURED_PEAKS.json)" if peak_src == "measured"
                 else "fallback")
+        if bound == "tf32":
+            psrc = ("measured bf16 burst (MEASURED_PEAKS.json) x nominal tf32/bf16 1.1/2.25"
+                    if peak_src == "measured" else "fallback bf16 x 1.1/2.25")
+            bound = "tensor"
         if bound == "alu":
             psrc = ("derived: SMs x 128 fp32 lanes x 2 FLOP x max SM clock "
                     f"({'MEASURED_PEAKS.json sm_max_mhz' if peak_src == 'measured' else 'fallback'})")

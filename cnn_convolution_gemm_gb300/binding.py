@@ -35,7 +35,8 @@ CONV_ALGO_INT8_MMA = 7
 CONV_ALGO_INT8_TC = 8
 CONV_ALGO_IM2COL_GEMM = 9
 CONV_ALGO_STEM_S2D = 10
-CONV_ALGO_COUNT = 11
+CONV_ALGO_IGEMM_TF32 = 11
+CONV_ALGO_COUNT = 12
 
 STATUS_NAMES = {
     0: "CONV_OK", 1: "CONV_ERR_BAD_PARAM", 2: "CONV_ERR_UNSUPPORTED", 3: "CONV_ERR_ALIGNMENT",

@@ -230,7 +230,7 @@ extern "C" conv_status_t conv_desc_get_output_dims(conv_desc_t d, int* OH, int* 
 static const char* const kAlgoNames[CONV_ALGO_COUNT] = {
     "direct", "igemm_tc_n64", "igemm_tc_n128", "igemm_tc_n256",
     "winograd_f2x2_3x3", "winograd_f6x6_3x3", "depthwise3x3", "int8_igemm_mma",
-    "int8_igemm_tc", "im2col_gemm", "stem_s2d_igemm"};
+    "int8_igemm_tc", "im2col_gemm", "stem_s2d_igemm", "igemm_tf32"};
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -302,6 +302,14 @@ static bool applicable(const gbconv_desc_s& d, int algo, const char** why) {
     case CONV_ALGO_STEM_S2D:
       if (d.dtype != CONV_BF16 || !nhwc) return *why = "needs bf16 NHWC", false;
       return stem_s2d_applicable(d, why);
+    case CONV_ALGO_IGEMM_TF32:
+      if (d.dtype != CONV_F32 || !nhwc) return *why = "needs fp32 NHWC", false;
+      if (d.groups != 1 || d.R != d.S) return *why = "needs groups == 1, square kernel", false;
+      if (d.C % 4 || d.K % 4) return *why = "needs C and K multiples of 4", false;
+      if (d.stride > 8 || d.pad > 128 || d.pad - d.dil * (d.R - 1) < -128)
+        return *why = "stride/padding outside the TMA im2col range", false;
+      if ((long long)d.N * d.OH * d.OW >= (1LL << 31)) return *why = "N*OH*OW >= 2^31", false;
+      return true;
     default:
       return *why = "unknown algorithm", false;
   }
@@ -340,6 +348,10 @@ static int heuristic(const gbconv_desc_s& d) {
   }
   if (implemented(CONV_ALGO_DEPTHWISE) && applicable(d, CONV_ALGO_DEPTHWISE, nullptr))
     return CONV_ALGO_DEPTHWISE;
+  if (d.dtype == CONV_F32)
+    return implemented(CONV_ALGO_IGEMM_TF32) && applicable(d, CONV_ALGO_IGEMM_TF32, nullptr)
+               ? CONV_ALGO_IGEMM_TF32
+               : CONV_ALGO_DIRECT;
   const int order[] = {CONV_ALGO_IGEMM_N256, CONV_ALGO_IGEMM_N128, CONV_ALGO_IGEMM_N64};
   for (int a : order)
     if (implemented(a) && applicable(d, a, nullptr)) return a;
@@ -431,6 +443,7 @@ extern "C" conv_status_t conv_weights_packed_size(conv_desc_t d, conv_algo_t alg
     case CONV_ALGO_INT8_TC: *bytes = int8_tc_packed_bytes(*d); break;
     case CONV_ALGO_IM2COL_GEMM: *bytes = im2col_packed_bytes(*d); break;
     case CONV_ALGO_STEM_S2D: *bytes = stem_s2d_packed_bytes(*d); break;
+    case CONV_ALGO_IGEMM_TF32: *bytes = igemm_tf32_packed_bytes(*d); break;
     case CONV_ALGO_WINO_F2: *bytes = winograd_packed_bytes(*d, 2); break;
     case CONV_ALGO_WINO_F6: *bytes = winograd_packed_bytes(*d, 6); break;
     default: *bytes = user_weight_bytes(*d); break;
@@ -455,6 +468,7 @@ extern "C" conv_status_t conv_weights_prepack(conv_desc_t d, conv_algo_t algo, c
     case CONV_ALGO_INT8_TC: e = launch_pack_int8_tc_weights(*d, w, wpack, s); break;
     case CONV_ALGO_IM2COL_GEMM: e = launch_pack_im2col_weights(*d, w, wpack, s); break;
     case CONV_ALGO_STEM_S2D: e = launch_pack_stem_weights(*d, w, wpack, s); break;
+    case CONV_ALGO_IGEMM_TF32: e = launch_pack_tf32_weights(*d, w, wpack, s); break;
     case CONV_ALGO_DEPTHWISE: e = launch_pack_dw_weights(*d, w, wpack, s); break;
     case CONV_ALGO_WINO_F2: e = launch_winograd_filter_transform(*d, 2, w, wpack, s); break;
     case CONV_ALGO_WINO_F6: e = launch_winograd_filter_transform(*d, 6, w, wpack, s); break;
@@ -499,6 +513,10 @@ static conv_status_t fwd_impl(const gbconv_desc_s& d, const void* x, const void*
                              wait_ns, s);
       break;
     }
+    case CONV_ALGO_IGEMM_TF32:
+      e = launch_igemm_bf16(d, d.K <= 64 ? 64 : (d.K <= 128 ? 128 : 256), x, wpack,
+                            static_cast<const float*>(bias), res, y, err, wait_ns, s);
+      break;
     case CONV_ALGO_STEM_S2D: {
       const size_t need = stem_s2d_workspace_bytes(d);
       if (!ws || ws_bytes < need)
@@ -926,6 +944,7 @@ static bool implemented(int algo) {
     case CONV_ALGO_INT8_TC:
     case CONV_ALGO_IM2COL_GEMM:
     case CONV_ALGO_STEM_S2D:
+    case CONV_ALGO_IGEMM_TF32:
       return true;
     default:
       return false;

@@ -172,3 +172,9 @@ cudaError_t launch_stem_s2d(const gbconv_desc_s& d, const void* x, const void* w
 // NCHW int8 <-> NC32HW32 int8 (to_nc32: 1 = NCHW -> NC32HW32, 0 = back).
 cudaError_t launch_nc32_convert(const void* x, void* y, int N, int C, int H, int W, int to_nc32,
                                 cudaStream_t st);
+
+// Implicit GEMM over fp32 NHWC tensors on kind::tf32 (launch_igemm_bf16 with a
+// CONV_F32 desc).  wpack: [K][R*S][Cp] fp32, Cp = C rounded up to 32.
+size_t igemm_tf32_packed_bytes(const gbconv_desc_s& d);
+cudaError_t launch_pack_tf32_weights(const gbconv_desc_s& d, const void* w, void* wpack,
+                                     cudaStream_t st);

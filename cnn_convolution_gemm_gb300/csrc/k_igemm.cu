@@ -71,6 +71,8 @@ struct IgemmParams {
   const int32_t* i8_bias;
   const float* i8_scale;
   int i8_kout, i8_relu, i8_nc32;
+  // tf32 mode: fp32 residual [M][K] (the fp32 output goes through tm_y)
+  const float* res_f32;
 };
 
 enum { MODE_CONV = 0, MODE_BATCHED = 1 };
@@ -99,13 +101,16 @@ __device__ __forceinline__ float act_apply(float v, int act) {
   return v;
 }
 
-template <int BN, int MODE, bool LIGHT = false>
+// TF32: fp32 NHWC tensors, kind::tf32 MMAs; a 128-byte swizzle row then holds
+// 32 channels (BKE) instead of 64 and each MMA still advances 32 bytes of K.
+template <int BN, int MODE, bool LIGHT = false, bool TF32 = false>
 __global__ void __launch_bounds__(192, 1)
     igemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                          const __grid_constant__ CUtensorMap tm_w,
                          const __grid_constant__ CUtensorMap tm_y,
                          const __grid_constant__ CUtensorMap tm_r, const IgemmParams p) {
   using C = Cfg<BN, LIGHT>;
+  constexpr int BKE = TF32 ? 32 : BK;  // channels per k-step (one 128-byte row)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -212,10 +217,10 @@ __global__ void __launch_bounds__(192, 1)
             gb::tma_load_2d(sB + stage * C::B_BYTES, &tm_w, &full[stage], it * BK,
                             nt * BN + noff);
           } else if (MODE == MODE_CONV) {
-            gb::tma_load_im2col_4d(sA + stage * C::A_BYTES, &tm_x, &full[stage], cb * BK, w0, h0,
-                                   img, (uint16_t)(s * p.dil), (uint16_t)(r * p.dil));
+            gb::tma_load_im2col_4d(sA + stage * C::A_BYTES, &tm_x, &full[stage], cb * BKE, w0,
+                                   h0, img, (uint16_t)(s * p.dil), (uint16_t)(r * p.dil));
             gb::tma_load_2d(sB + stage * C::B_BYTES, &tm_w, &full[stage],
-                            (r * p.S + s) * p.cblocks * BK + cb * BK, nt * BN + noff);
+                            (r * p.S + s) * p.cblocks * BKE + cb * BKE, nt * BN + noff);
           } else {
             gb::tma_load_3d(sA + stage * C::A_BYTES, &tm_x, &full[stage], cb * BK, (int)m0, bt);
             gb::tma_load_3d(sB + stage * C::B_BYTES, &tm_w, &full[stage], cb * BK, nt * BN, bt);
@@ -250,7 +255,7 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      const uint32_t IDESC = gb::idesc_f16(BM, BN, MODE == MODE_CONV ? 1 : p.ab_type);
+      const uint32_t IDESC = gb::idesc_f16(BM, BN, TF32 ? 2 : (MODE == MODE_CONV ? 1 : p.ab_type));
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -259,7 +264,7 @@ __global__ void __launch_bounds__(192, 1)
       for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
         int t, noff, width;
         decode(u, t, noff, width);
-        const uint32_t idesc_u = width == BN ? IDESC : gb::idesc_f16(BM, BN / 2, 1);
+        const uint32_t idesc_u = width == BN ? IDESC : gb::idesc_f16(BM, BN / 2, TF32 ? 2 : 1);
         if (!gb::mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, p.wait_ns, p.err)) break;
         gb::tc_fence_after();
         const uint32_t d = tmem_base + acc * BN;
@@ -275,15 +280,19 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t a0 = gb::smem_u32(sA + stage * C::A_BYTES);
           const uint32_t b0 = gb::smem_u32(sB + stage * C::B_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
+          for (int k = 0; k < 4; ++k) {  // 4 MMAs of 32 bytes of K per 128-byte row
             // narrow mode: two taps (2 x 2 KB boxes) per 16-wide k; core matrices
             // are 128 bytes apart along M and one box (2 KB) apart along K
             const uint64_t adesc =
                 (MODE == MODE_CONV && p.narrow)
                     ? gb::noswz_kmajor_desc(a0 + k * 2 * (BM * 16), BM * 16, 128)
                     : gb::sw128_kmajor_desc(a0 + k * 32);
-            gb::tc_mma_f16(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), idesc_u,
-                           (it > kbeg || k > 0) ? 1u : 0u);
+            if constexpr (TF32)
+              gb::tc_mma_tf32(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), idesc_u,
+                              (it > kbeg || k > 0) ? 1u : 0u);
+            else
+              gb::tc_mma_f16(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), idesc_u,
+                             (it > kbeg || k > 0) ? 1u : 0u);
           }
           gb::tc_commit(&empty[stage]);
           if (++stage == C::STAGES) {
@@ -350,7 +359,55 @@ __global__ void __launch_bounds__(192, 1)
       const long long m = (long long)mt * BM + q * 32 + lane;
       const bool row_ok = m < p.M;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-      if (MODE == MODE_CONV && p.i8_y) {
+      if constexpr (TF32) {
+        // fp32 NHWC output: 32-column sub-blocks -> + bias (+ residual) ->
+        // activation -> a 128-byte-swizzled 32 x 32 fp32 box per warp -> TMA store
+        const long long m_warp = (long long)mt * BM + q * 32;
+        const int remk = p.K - (nt * BN + noff);
+        int ns32 = remk > 0 ? (remk + 31) / 32 : 0;
+        if (ns32 > width / 32) ns32 = width / 32;
+        float* sbias = reinterpret_cast<float*>(sEpi + 4 * 2 * C::EPI_BOX + q * 256);
+#pragma unroll 1
+        for (int j = 0; j < ns32; ++j) {
+          const int nb0 = nt * BN + noff + j * 32;
+          uint8_t* box = sEpi + (q * 2 + (epi_count & 1)) * C::EPI_BOX;
+          if (lane == 0) gb::bulk_wait_read<1>();  // the store that last used this box
+          __syncwarp();
+          uint32_t r[32];
+          gb::tmem_ld_x16(tbase + j * 32, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
+          gb::tmem_ld_x16(tbase + j * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
+          sbias[lane] = (p.bias && nb0 + lane < p.K) ? __ldg(p.bias + nb0 + lane) : 0.f;
+          __syncwarp();
+          gb::tmem_ld_wait();
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) + sbias[i];
+          if (p.res_f32 && row_ok) {
+            const float4* rp = reinterpret_cast<const float4*>(p.res_f32 + m * p.K + nb0);
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+              if (nb0 + 4 * h >= p.K) break;
+              const float4 rv = __ldg(rp + h);
+              v[4 * h] += rv.x;
+              v[4 * h + 1] += rv.y;
+              v[4 * h + 2] += rv.z;
+              v[4 * h + 3] += rv.w;
+            }
+          }
+#pragma unroll
+          for (int h = 0; h < 8; ++h)
+            *reinterpret_cast<float4*>(box + lane * 128 + ((h ^ (lane & 7)) << 4)) =
+                make_float4(act_apply(v[4 * h], p.act), act_apply(v[4 * h + 1], p.act),
+                            act_apply(v[4 * h + 2], p.act), act_apply(v[4 * h + 3], p.act));
+          gb::fence_proxy_async_smem();  // staging writes -> visible to the TMA engine
+          __syncwarp();
+          if (lane == 0) {
+            gb::tma_store_2d(&tm_y, box, nb0, (int)m_warp);
+            gb::bulk_commit();
+          }
+          ++epi_count;
+        }
+      } else if (MODE == MODE_CONV && p.i8_y) {
         // exact int8: each 128-column group of the tile holds 64 sums against
         // the low weight nibbles, then 64 against the high parts, all exact
         // integers in fp32; t = 16 * hi + lo + bias, requantised to int8 (the
@@ -560,13 +617,17 @@ __global__ void pack_igemm_weights_kernel(const __nv_bfloat16* __restrict__ w,
   }
 }
 
-template <int BN, bool LIGHT>
+template <int BN, bool LIGHT, bool TF32 = false>
 cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, const float* bias,
                       const void* res, void* y, int* err, unsigned long long wait_ns,
                       cudaStream_t st, const IgemmSplit& split) {
   using Cf = Cfg<BN, LIGHT>;
-  const bool narrow = d.C == 8;
-  const int Cp = gb_ceil_div(d.C, BK) * BK;
+  constexpr int BKE = TF32 ? 32 : BK;  // channels per k-step
+  constexpr int ES = TF32 ? 4 : 2;     // element bytes
+  const CUtensorMapDataType DT =
+      TF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const bool narrow = !TF32 && d.C == 8;
+  const int Cp = gb_ceil_div(d.C, BKE) * BKE;
   IgemmParams p{};
   p.narrow = narrow ? 1 : 0;
   p.taps = d.R * d.S;
@@ -580,7 +641,7 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   p.dil = d.dil;
   p.OH = d.OH;
   p.OW = d.OW;
-  p.cblocks = narrow ? 1 : Cp / BK;
+  p.cblocks = narrow ? 1 : Cp / BKE;
   p.kiters = narrow ? gb_ceil_div(d.R * d.S, 8) : d.R * d.S * p.cblocks;
   p.Kw = narrow ? p.kiters * BK : d.R * d.S * Cp;
   p.M = (long long)d.N * d.OH * d.OW;
@@ -588,7 +649,8 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   p.n_tiles = gb_ceil_div(d.K, BN);
   p.act = d.act;
   p.bias = bias;
-  p.res = static_cast<const __nv_bfloat16*>(res);
+  p.res = TF32 ? nullptr : static_cast<const __nv_bfloat16*>(res);
+  p.res_f32 = TF32 ? static_cast<const float*>(res) : nullptr;
   p.y = static_cast<__nv_bfloat16*>(y);
   p.err = err;
   p.wait_ns = wait_ns;
@@ -607,37 +669,37 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   CUtensorMap tmx, tmw;
   {
     cuuint64_t dims[4] = {(cuuint64_t)d.C, (cuuint64_t)d.W, (cuuint64_t)d.H, (cuuint64_t)d.N};
-    cuuint64_t strides[3] = {(cuuint64_t)d.C * 2, (cuuint64_t)d.W * d.C * 2,
-                             (cuuint64_t)d.H * d.W * d.C * 2};
+    cuuint64_t strides[3] = {(cuuint64_t)d.C * ES, (cuuint64_t)d.W * d.C * ES,
+                             (cuuint64_t)d.H * d.W * d.C * ES};
     // Bounding box of the first filter tap's pixel: from -pad to
     // (dim - 1) + pad - dil*(R-1) (R == S is required).
     int lower[2] = {-d.pad, -d.pad};
     const int pad_hi = d.pad + d.pad_hi_delta;  // padding after (equal to pad unless rewritten)
     int upper[2] = {pad_hi - d.dil * (d.S - 1), pad_hi - d.dil * (d.R - 1)};
     cuuint32_t estr[4] = {1, (cuuint32_t)d.stride, (cuuint32_t)d.stride, 1};
-    CUresult r = gb_encode_im2col(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x),
-                                  dims, strides, lower, upper, narrow ? 8 : BK, BM, estr,
+    CUresult r = gb_encode_im2col(&tmx, DT, 4, const_cast<void*>(x),
+                                  dims, strides, lower, upper, narrow ? 8 : BKE, BM, estr,
                                   narrow ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
   {
     cuuint64_t dims[2] = {(cuuint64_t)p.Kw, (cuuint64_t)d.K};
-    cuuint64_t strides[1] = {(cuuint64_t)p.Kw * 2};
-    cuuint32_t box[2] = {BK, BN};
+    cuuint64_t strides[1] = {(cuuint64_t)p.Kw * ES};
+    cuuint32_t box[2] = {BKE, BN};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = gb_encode_tiled(&tmw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                                 const_cast<void*>(wpack), dims, strides, box, estr,
+    CUresult r = gb_encode_tiled(&tmw, DT, 2, const_cast<void*>(wpack), dims, strides, box, estr,
                                  CU_TENSOR_MAP_SWIZZLE_128B);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-  CUtensorMap tmy;  // output [M][K] bf16, 64-column x 32-row boxes, 128-byte swizzle
+  CUtensorMap tmy;  // output [M][K]: bf16 64-column (fp32: 32-column) x 32-row boxes,
+                    // 128-byte swizzle
   {
     cuuint64_t dims[2] = {(cuuint64_t)d.K, (cuuint64_t)p.M};
-    cuuint64_t strides[1] = {(cuuint64_t)d.K * 2};
-    cuuint32_t box[2] = {64, 32};
+    cuuint64_t strides[1] = {(cuuint64_t)d.K * ES};
+    cuuint32_t box[2] = {TF32 ? 32u : 64u, 32};
     cuuint32_t estr[2] = {1, 1};
-    if (gb_encode_tiled(&tmy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, dims, strides, box, estr,
-                        CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+    if (gb_encode_tiled(&tmy, DT, 2, y, dims, strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B) !=
+        CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
   CUtensorMap tmr = tmy;  // residual (same shape and boxes as the output), or the
@@ -650,7 +712,7 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
     if (gb_encode_tiled(&tmr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.part, dims, strides, box,
                         estr, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-  } else if (res) {
+  } else if (res && !TF32) {
     cuuint64_t dims[2] = {(cuuint64_t)d.K, (cuuint64_t)p.M};
     cuuint64_t strides[1] = {(cuuint64_t)d.K * 2};
     cuuint32_t box[2] = {64, 32};
@@ -660,7 +722,7 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
       return cudaErrorInvalidValue;
   }
   cudaError_t e = gb_set_smem_once(
-      reinterpret_cast<const void*>(igemm_bf16_tc_kernel<BN, MODE_CONV, LIGHT>), Cf::SMEM);
+      reinterpret_cast<const void*>(igemm_bf16_tc_kernel<BN, MODE_CONV, LIGHT, TF32>), Cf::SMEM);
   if (e != cudaSuccess) return e;
   const int tiles = p.m_tiles * p.n_tiles * p.ksplit;
   const int slots = gb_num_sms() * (LIGHT ? 2 : 1);
@@ -671,7 +733,8 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
     const int rem = tiles % grid;
     if (rem > 0 && rem <= grid / 2) p.tail_start = tiles - rem;
   }
-  igemm_bf16_tc_kernel<BN, MODE_CONV, LIGHT><<<grid, 192, Cf::SMEM, st>>>(tmx, tmw, tmy, tmr, p);
+  igemm_bf16_tc_kernel<BN, MODE_CONV, LIGHT, TF32><<<grid, 192, Cf::SMEM, st>>>(tmx, tmw, tmy,
+                                                                               tmr, p);
   return cudaGetLastError();
 }
 
@@ -750,6 +813,22 @@ cudaError_t launch_igemm_bf16(const gbconv_desc_s& d, int block_n, const void* x
                               const void* wpack, const float* bias, const void* res, void* y,
                               int* err, unsigned long long wait_ns, cudaStream_t st,
                               const IgemmSplit& split) {
+  if (d.dtype == CONV_F32) {  // fp32 tensors: kind::tf32, 32 channels per k-step
+    const int kt = d.R * d.S * gb_ceil_div(d.C, 32);
+    const bool lt = kt <= 8;
+    switch (block_n) {
+      case 64:
+        return lt ? launch_bn<64, true, true>(d, x, wpack, bias, res, y, err, wait_ns, st, split)
+                  : launch_bn<64, false, true>(d, x, wpack, bias, res, y, err, wait_ns, st, split);
+      case 128:
+        return lt ? launch_bn<128, true, true>(d, x, wpack, bias, res, y, err, wait_ns, st, split)
+                  : launch_bn<128, false, true>(d, x, wpack, bias, res, y, err, wait_ns, st,
+                                                split);
+      case 256:
+        return launch_bn<256, false, true>(d, x, wpack, bias, res, y, err, wait_ns, st, split);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   // short reductions (1x1 layers up to 512 channels) are bound by the epilogue
   // and memory, not by the operand pipeline: run two shallow CTAs per SM
   const int kiters = d.C == 8 ? gb_ceil_div(d.R * d.S, 8) : d.R * d.S * gb_ceil_div(d.C, BK);
@@ -784,6 +863,35 @@ cudaError_t launch_batched_gemm_tc(int batch, int M, int N, int Kred, const void
       return launch_batched_bn<256>(batch, M, N, Kred, A, B, out, ab_type, err, wait_ns, st);
     default: return cudaErrorInvalidValue;
   }
+}
+
+namespace {
+// fp32 weights [K][R][S][C] -> [K][R*S][Cp], Cp = C rounded up to 32, zero padded
+__global__ void pack_tf32_weights_kernel(const float* __restrict__ w, float* __restrict__ wp,
+                                         int K, int RS, int C, int Cp) {
+  const long long total = (long long)K * RS * Cp;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int c = (int)(i % Cp);
+    const long long krs = i / Cp;
+    wp[i] = c < C ? w[krs * C + c] : 0.f;
+  }
+}
+}  // namespace
+
+size_t igemm_tf32_packed_bytes(const gbconv_desc_s& d) {
+  return (size_t)d.K * d.R * d.S * gb_ceil_div(d.C, 32) * 32 * 4;
+}
+
+cudaError_t launch_pack_tf32_weights(const gbconv_desc_s& d, const void* w, void* wpack,
+                                     cudaStream_t st) {
+  const int Cp = gb_ceil_div(d.C, 32) * 32;
+  const long long total = (long long)d.K * d.R * d.S * Cp;
+  const int grid = (int)std::min<long long>((total + 255) / 256, 152LL * 16);
+  pack_tf32_weights_kernel<<<grid, 256, 0, st>>>(static_cast<const float*>(w),
+                                                  static_cast<float*>(wpack), d.K, d.R * d.S,
+                                                  d.C, Cp);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_pack_igemm_weights(const gbconv_desc_s& d, const void* w, void* wpack,

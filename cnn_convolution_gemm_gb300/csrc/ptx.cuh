@@ -185,6 +185,17 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::tf32 (fp32 operands read as tf32, fp32 acc).
+__device__ __forceinline__ void tc_mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on bar once all previously issued tcgen05 async ops of this thread complete.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile(
@@ -242,8 +253,8 @@ __device__ __forceinline__ uint64_t noswz_kmajor_desc(uint32_t smem_addr, uint32
   return d;
 }
 
-// Instruction descriptor for kind::f16: fp32 accumulate, both operands K-major.
-// ab_type: 0 = f16, 1 = bf16.
+// Instruction descriptor for kind::f16 / kind::tf32: fp32 accumulate, both
+// operands K-major.  ab_type: 0 = f16, 1 = bf16 (kind::f16); 2 = tf32 (kind::tf32).
 __host__ __device__ constexpr uint32_t idesc_f16(int m, int n, int ab_type) {
   return (1u << 4)                              // D format fp32
          | ((uint32_t)ab_type << 7)             // A format

@@ -81,7 +81,9 @@ typedef int conv_algo_t;
 #define CONV_ALGO_IM2COL_GEMM 9    /* materialised im2col matrix + GEMM (workspace)     */
 #define CONV_ALGO_STEM_S2D 10      /* stride-2 conv over 8 channels (the image stem) as
                                       space-to-depth + stride-1 implicit GEMM (workspace) */
-#define CONV_ALGO_COUNT 11
+#define CONV_ALGO_IGEMM_TF32 11    /* implicit GEMM over fp32 NHWC tensors on kind::tf32
+                                      (inputs read with tf32's 10-bit mantissa)          */
+#define CONV_ALGO_COUNT 12
 
 /* ---- descriptor --------------------------------------------------------- */
 
