@@ -10,6 +10,8 @@ Other workloads (--workload):
   single_layer  1 x 32 x 28 x 28 fp32 NCHW, 32 filters 3x3: boundary
                 conversion to NHWC bf16, conv, conversion back
   resnet3x3_tf32  the headline layer with fp32 NHWC tensors on the tf32 path
+  shuffle_dw    ShuffleNet v1 depthwise (240 ch, 28x28, batch 64) reading its
+                input channel-shuffled (g = 3), the shuffle fused into the kernel
   mbv2_block    MobileNetV2 inverted residual, N=64, 56x56: 1x1 24->144 +
                 ReLU6, depthwise 3x3 + ReLU6, 1x1 144->24.  By default the
                 fused one-kernel block and the three-layer chain (each layer's
@@ -306,6 +308,75 @@ class ResNetLayerTF32(ResNetLayer):
                                                             stream=self.sh),
                  self.shape.flops(), self.shape.traffic_bytes(4, 4),
                  "tf32" if self.algo_name == "igemm_tf32" else "alu")]
+
+
+class ShuffleDepthwise(Workload):
+    """ShuffleNet v1 (g = 3) stage-2 depthwise 3x3 over 240 channels at 28x28,
+    batch 64, reading its input channel-shuffled (the shuffle fused into the
+    depthwise: no shuffled tensor is written)."""
+    name = "shufflenet_dw3x3_c240_g3_28x28_n64_bf16_nhwc"
+    metric = "depthwise GB/s (algorithmic), channel shuffle g=3 fused, 240ch @28x28, batch 64"
+    unit = "GB/s"
+
+    def setup(self, dev, rank, args):
+        import torch
+        from cnn_convolution_gemm_gb300 import binding as B
+        from cnn_convolution_gemm_gb300 import synth
+        from cnn_convolution_gemm_gb300.layer import ConvLayer
+        from cnn_convolution_gemm_gb300.workload import ConvShape
+        N, C, H = 64, 240, 28
+        self.shape = ConvShape(N, C, H, H, C, 3, 3, 1, 1, 1, C)
+        x = synth.normal((N, H, H, C), 1.0, rank)
+        w = synth.kaiming((C, 3, 3, 1), rank + 1)
+        b = synth.uniform((C,), -0.1, 0.1, rank + 2)
+        self.sh = torch.cuda.current_stream().cuda_stream
+        self.xh = torch.from_numpy(x).to(torch.bfloat16).pin_memory()
+        self.x = self.xh.to(dev)
+        self.b = torch.from_numpy(b).to(dev)
+        wt = torch.from_numpy(w).to(torch.bfloat16).to(dev)
+        self.layer = ConvLayer(N, C, H, H, C, 3, 3, 1, 1, 1, C, input_shuffle=3)
+        self.layer.prepack(wt, B.CONV_ALGO_DEPTHWISE)
+        self.plain = ConvLayer(N, C, H, H, C, 3, 3, 1, 1, 1, C)
+        self.plain.prepack(wt, B.CONV_ALGO_DEPTHWISE)
+        self.algo_name = "depthwise3x3+shuffle"
+        self.y = torch.empty((N, H, H, C), dtype=torch.bfloat16, device=dev)
+        self.yh = torch.empty((N, H, H, C), dtype=torch.bfloat16).pin_memory()
+        # the same depthwise without the shuffle, for the cost of the gather
+        self.fastrun_ms = {"depthwise3x3 (no shuffle)": round(time_groups(
+            [("plain", lambda: self.plain.forward(self.x, self.b, out=self.y, stream=self.sh))],
+            self.sh), 4),
+            "depthwise3x3+shuffle": round(time_groups(self.groups(), self.sh), 4)}
+
+    def groups(self):
+        return [(self.algo_name, lambda: self.layer.forward(self.x, self.b, out=self.y,
+                                                            stream=self.sh),
+                 self.shape.traffic_bytes(2, 4), self.shape.traffic_bytes(2, 4), "hbm")]
+
+    def value(self, ms):
+        return self.shape.traffic_bytes(2, 4) / (ms * 1e-3) / 1e9
+
+    def h2d(self):
+        return [(self.xh, self.x)]
+
+    def d2h(self):
+        return [(self.y, self.yh)]
+
+    def cpu_baseline(self, args):
+        import numpy as np
+        from cnn_convolution_gemm_gb300 import synth
+        from cnn_convolution_gemm_gb300.workload import ConvShape
+        from oracle import lib as ol
+        n = 8
+        x = synth.normal((n, 28, 28, 240), 1.0, 0)
+        x = x.reshape(n, 28, 28, 3, 80).transpose(0, 1, 2, 4, 3).reshape(n, 28, 28, 240)
+        w = synth.kaiming((240, 3, 3, 1), 1)
+        t0 = time.perf_counter()
+        ol.conv2d_f64(np.ascontiguousarray(x.transpose(0, 3, 1, 2)), w.transpose(0, 3, 1, 2),
+                      pad=1, groups=240)
+        dt = time.perf_counter() - t0
+        byts = ConvShape(n, 240, 28, 28, 240, 3, 3, 1, 1, 1, 240).traffic_bytes(2, 4)
+        return {"value": byts / dt / 1e9, "unit": "GB/s", "cores": threads(), "kind": "oracle",
+                "sample": f"{n} of 64 images", "seconds": round(dt, 3)}
 
 
 class SingleLayer(Workload):
@@ -641,6 +712,7 @@ class ResNet50W(Workload):
 
 
 WORKLOADS = {"resnet3x3": ResNetLayer, "resnet3x3_tf32": ResNetLayerTF32,
+             "shuffle_dw": ShuffleDepthwise,
              "single_layer": SingleLayer, "mbv2_block": MBv2Block,
              "int8_stages": Int8Stages, "resnet50": ResNet50W}
 

@@ -52,6 +52,7 @@ SIGNATURES = {
     "conv_desc_destroy": (_i, [_p]),
     "conv_desc_set_layout": (_i, [_p, _i]),
     "conv_desc_set_epilogue": (_i, [_p, _i, _i]),
+    "conv_desc_set_input_shuffle": (_i, [_p, _i]),
     "conv_desc_set_requant": (_i, [_p, _p]),
     "conv_desc_get_output_dims": (_i, [_p, ctypes.POINTER(_i), ctypes.POINTER(_i)]),
     "conv_algo_count": (_i, [_p, ctypes.POINTER(_i)]),
@@ -144,6 +145,10 @@ def conv_desc_set_layout(desc, layout):
 def conv_desc_set_epilogue(desc, act, has_residual):
     _check(load_library().conv_desc_set_epilogue(desc, act, 1 if has_residual else 0),
            "conv_desc_set_epilogue")
+
+
+def conv_desc_set_input_shuffle(desc, groups):
+    _check(load_library().conv_desc_set_input_shuffle(desc, groups), "conv_desc_set_input_shuffle")
 
 
 def conv_desc_set_requant(desc, scale_ptr):

@@ -210,6 +210,14 @@ extern "C" conv_status_t conv_desc_set_epilogue(conv_desc_t d, int act, int has_
   return ok_status();
 }
 
+extern "C" conv_status_t conv_desc_set_input_shuffle(conv_desc_t d, int groups) {
+  if (!d) return gb_fail(CONV_ERR_BAD_PARAM, "desc is NULL");
+  if (groups < 1 || d->C % groups)
+    return gb_fail(CONV_ERR_BAD_PARAM, "shuffle groups must divide C");
+  d->shuffle_groups = groups > 1 ? groups : 0;
+  return ok_status();
+}
+
 extern "C" conv_status_t conv_desc_set_requant(conv_desc_t d, const float* scale_dev) {
   if (!d) return gb_fail(CONV_ERR_BAD_PARAM, "desc is NULL");
   if (d->dtype != CONV_INT8) return gb_fail(CONV_ERR_UNSUPPORTED, "requant is for CONV_INT8");
@@ -240,6 +248,8 @@ static bool applicable(const gbconv_desc_s& d, int algo, const char** why) {
   if (!why) why = &dummy;
   *why = "";
   const bool nhwc = d.layout == CONV_NHWC;
+  if (d.shuffle_groups > 1 && algo != CONV_ALGO_DIRECT && algo != CONV_ALGO_DEPTHWISE)
+    return *why = "an input shuffle is honoured by depthwise3x3 and direct only", false;
   switch (algo) {
     case CONV_ALGO_DIRECT:
       if (d.dtype == CONV_INT8 && !d.scale) return *why = "int8 needs a requant scale", false;
@@ -274,6 +284,8 @@ static bool applicable(const gbconv_desc_s& d, int algo, const char** why) {
       if (d.R != 3 || d.S != 3 || d.dil != 1 || d.stride > 2)
         return *why = "needs 3x3, dilation 1, stride 1 or 2", false;
       if (d.C % 8) return *why = "needs C multiple of 8", false;
+      if (d.shuffle_groups > 1 && (d.C > 256 || d.has_residual))
+        return *why = "an input shuffle needs C <= 256 and no residual", false;
       return true;
     case CONV_ALGO_INT8_MMA:
       if (d.dtype != CONV_INT8 || !nhwc) return *why = "needs int8 NHWC", false;
@@ -367,9 +379,10 @@ static std::map<std::string, int> g_fastrun;
 
 static std::string desc_key(const gbconv_desc_s& d) {
   char buf[256];
-  snprintf(buf, sizeof(buf), "N%d_C%d_H%d_W%d_K%d_R%d_S%d_st%d_p%d_d%d_g%d_t%d_l%d_a%d_r%d_q%d",
+  snprintf(buf, sizeof(buf), "N%d_C%d_H%d_W%d_K%d_R%d_S%d_st%d_p%d_d%d_g%d_t%d_l%d_a%d_r%d_q%d%s",
            d.N, d.C, d.H, d.W, d.K, d.R, d.S, d.stride, d.pad, d.dil, d.groups, (int)d.dtype,
-           (int)d.layout, d.act, d.has_residual, d.scale ? 1 : 0);
+           (int)d.layout, d.act, d.has_residual, d.scale ? 1 : 0,
+           d.shuffle_groups > 1 ? ("_sh" + std::to_string(d.shuffle_groups)).c_str() : "");
   return buf;
 }
 

@@ -17,6 +17,7 @@ struct gbconv_desc_s {
   const float* scale;  // int8 requant scale [K] (device)
   int OH, OW;
   int pad_hi_delta;    // padding after minus padding before (internal rewrites only; 0 = symmetric)
+  int shuffle_groups;  // > 1: the input is read channel-shuffled with this many groups
 };
 
 // Device-side error word codes (written by kernels, read by conv_sync_status).

@@ -15,7 +15,12 @@ struct DirectParams {
   int N, C, H, W, K, R, S, stride, pad, dil, OH, OW, Cg, Kg;
   int act;
   int nhwc;
+  int shuf;  // > 1: input channel c is read from (c mod shuf) * (C / shuf) + c div shuf
 };
+
+__device__ __forceinline__ int in_channel(const DirectParams& p, int c) {
+  return p.shuf > 1 ? (c % p.shuf) * (p.C / p.shuf) + c / p.shuf : c;
+}
 
 __device__ __forceinline__ float to_f(float v) { return v; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
@@ -77,7 +82,7 @@ __global__ void direct_conv_kernel(DirectParams p, const T* __restrict__ x,
         const int iw = ow * p.stride - p.pad + s * p.dil;
         if (iw < 0 || iw >= p.W) continue;
         for (int cc = 0; cc < p.Cg; ++cc) {
-          const int c = g * p.Cg + cc;
+          const int c = in_channel(p, g * p.Cg + cc);
           float xv, wv;
           if (p.nhwc) {
             xv = to_f(x[(((long long)n * p.H + ih) * p.W + iw) * p.C + c]);
@@ -119,7 +124,7 @@ __global__ void direct_conv_int8_kernel(DirectParams p, const int8_t* __restrict
         const int iw = ow * p.stride - p.pad + s * p.dil;
         if (iw < 0 || iw >= p.W) continue;
         for (int cc = 0; cc < p.Cg; ++cc) {
-          const int c = g * p.Cg + cc;
+          const int c = in_channel(p, g * p.Cg + cc);
           const long long xi =
               p.nhwc == 2 ? ((((long long)n * (p.C / 32) + c / 32) * p.H + ih) * p.W + iw) * 32 +
                                 (c & 31)
@@ -143,7 +148,8 @@ cudaError_t launch_direct(const gbconv_desc_s& d, const void* x, const void* w, 
                           const void* res, void* y, cudaStream_t st) {
   DirectParams p{d.N, d.C, d.H, d.W, d.K, d.R, d.S, d.stride, d.pad, d.dil, d.OH, d.OW,
                  d.C / d.groups, d.K / d.groups, d.act,
-                 d.layout == CONV_NHWC ? 1 : (d.layout == CONV_NC32HW32 ? 2 : 0)};
+                 d.layout == CONV_NHWC ? 1 : (d.layout == CONV_NC32HW32 ? 2 : 0),
+                 d.shuffle_groups};
   const long long total = (long long)d.N * d.K * d.OH * d.OW;
   const int block = 256;
   const int grid = (int)std::min<long long>(gb_ceil_div_ll(total, block), 148LL * 64);

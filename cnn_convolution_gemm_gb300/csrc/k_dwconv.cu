@@ -53,6 +53,7 @@ struct DwCfg {
 
 struct DwParams {
   int N, C, H, W, OH, OW, pad;
+  int shuf_g;              // input channel shuffle groups (SHUF kernels)
   int cb;                  // channels per block (all of C when C <= 256)
   int owt, iw, buf_bytes;  // output columns per block, input columns, bytes per block
   int cslices, rblocks, cblocks;
@@ -137,12 +138,13 @@ __device__ __forceinline__ void store4(f32x2 a0, f32x2 a1, __nv_bfloat16* yp,
 // value is converted once and added into the accumulators of the (up to three)
 // output rows it reaches.  Output row o lives in slot o % 3 and is stored once
 // its last input row, o * ST + 2, has been added.  FULL: all RB rows and both
-// columns exist (no per-row tests).
-template <int ST, int ACT, bool RES, bool FULL>
+// columns exist (no per-row tests).  SHUF: the 4 input channels are gathered
+// one by one at byte offsets choff[] within the pixel (channel shuffle).
+template <int ST, int ACT, bool RES, bool FULL, bool SHUF = false>
 __device__ __forceinline__ void dw_item(uint32_t src, uint32_t col_b, const f32x2 (&wf)[9][2],
                                         const f32x2 (&bz)[2], __nv_bfloat16* y0,
                                         const __nv_bfloat16* r0, size_t y_row, int C, int nrows,
-                                        bool two) {
+                                        bool two, const uint32_t (&choff)[4]) {
   using Cf = DwCfg<ST>;
   constexpr int NC = ST + 3;  // distinct input columns the two outputs read
   uint32_t sc[NC];            // shared address of input column cc of the pair, row 0
@@ -156,9 +158,20 @@ __device__ __forceinline__ void dw_item(uint32_t src, uint32_t col_b, const f32x
     f32x2 xin[NC][2];
 #pragma unroll
     for (int cc = 0; cc < NC; ++cc) {
-      const uint2 v = lds64(sc[cc] + rho * Cf::ROWP);
-      xin[cc][0] = bf16x2_to_f2(v.x);
-      xin[cc][1] = bf16x2_to_f2(v.y);
+      if constexpr (SHUF) {
+        uint32_t u[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          asm volatile("ld.shared.u16 %0, [%1];"
+                       : "=r"(u[q])
+                       : "r"(sc[cc] + rho * Cf::ROWP + choff[q]));
+        xin[cc][0] = f2_pack(__uint_as_float(u[0] << 16), __uint_as_float(u[1] << 16));
+        xin[cc][1] = f2_pack(__uint_as_float(u[2] << 16), __uint_as_float(u[3] << 16));
+      } else {
+        const uint2 v = lds64(sc[cc] + rho * Cf::ROWP);
+        xin[cc][0] = bf16x2_to_f2(v.x);
+        xin[cc][1] = bf16x2_to_f2(v.y);
+      }
     }
 #pragma unroll
     for (int i = 0; i < 3; ++i) {
@@ -190,7 +203,7 @@ __device__ __forceinline__ void dw_item(uint32_t src, uint32_t col_b, const f32x
 }
 
 // Persistent CTAs walk the block list; see the file comment.
-template <int ST, int ACT, bool RES>
+template <int ST, int ACT, bool RES, bool SHUF = false>
 __global__ void __launch_bounds__(MAX_THREADS, 1)
     dwconv3x3_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const DwParams p,
                          const __nv_bfloat16* __restrict__ w9c, const float* __restrict__ bias,
@@ -328,13 +341,25 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
           w_c = c;
         }
         // tile-local input columns of the pair: j0*ST + s (first), (j0+1)*ST + s (second)
-        const uint32_t src = tile + (uint32_t)(j0 * ST) * col_b + (uint32_t)g * 8;
+        uint32_t choff[4] = {0, 0, 0, 0};
+        uint32_t src = tile + (uint32_t)(j0 * ST) * col_b;
+        if constexpr (SHUF) {
+          // output channel j reads channel (j mod G) * (C / G) + j div G of the
+          // input (the whole channel range is in the tile: one slice)
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            choff[q] = (uint32_t)(((c + q) % p.shuf_g) * (p.C / p.shuf_g) + (c + q) / p.shuf_g) * 2;
+        } else {
+          src += (uint32_t)g * 8;
+        }
         const size_t yoff = (((size_t)cur.n * p.OH + cur.rb * Cf::RB) * p.OW + ow0) * p.C + c;
         const __nv_bfloat16* r0 = RES ? res + yoff : nullptr;
         if (nrows == Cf::RB && two)
-          dw_item<ST, ACT, RES, true>(src, col_b, wf, bz, y + yoff, r0, y_row, p.C, nrows, two);
+          dw_item<ST, ACT, RES, true, SHUF>(src, col_b, wf, bz, y + yoff, r0, y_row, p.C, nrows,
+                                            two, choff);
         else
-          dw_item<ST, ACT, RES, false>(src, col_b, wf, bz, y + yoff, r0, y_row, p.C, nrows, two);
+          dw_item<ST, ACT, RES, false, SHUF>(src, col_b, wf, bz, y + yoff, r0, y_row, p.C, nrows,
+                                             two, choff);
       }
       g += g_step;  // next item: + blockDim.x
       jp += jp_step;
@@ -364,8 +389,11 @@ __global__ void pack_dw_weights_kernel(const __nv_bfloat16* __restrict__ w,
 }
 
 template <int ST, int ACT>
-auto pick_kernel(bool res) {
-  return res ? dwconv3x3_tma_kernel<ST, ACT, true> : dwconv3x3_tma_kernel<ST, ACT, false>;
+auto pick_kernel(bool res, bool shuf) {
+  // (a shuffled input with a residual is not a combination networks use: the
+  // shuffle variants are built without the residual)
+  return shuf ? dwconv3x3_tma_kernel<ST, ACT, false, true>
+              : (res ? dwconv3x3_tma_kernel<ST, ACT, true> : dwconv3x3_tma_kernel<ST, ACT, false>);
 }
 
 template <int ST>
@@ -417,9 +445,12 @@ cudaError_t launch_st(const gbconv_desc_s& d, const void* x, const void* w, cons
   const int rounds = gb_ceil_div(items, MAX_THREADS);
   const int threads = gb_ceil_div(gb_ceil_div(items, rounds), 32) * 32;
   const bool has_res = res != nullptr;
-  auto kern = d.act == CONV_ACT_RELU6  ? pick_kernel<ST, 2>(has_res)
-              : d.act == CONV_ACT_RELU ? pick_kernel<ST, 1>(has_res)
-                                       : pick_kernel<ST, 0>(has_res);
+  const bool shuf = d.shuffle_groups > 1;
+  if (shuf && (has_res || p.cslices != 1)) return cudaErrorInvalidValue;
+  p.shuf_g = shuf ? d.shuffle_groups : 1;
+  auto kern = d.act == CONV_ACT_RELU6  ? pick_kernel<ST, 2>(has_res, shuf)
+              : d.act == CONV_ACT_RELU ? pick_kernel<ST, 1>(has_res, shuf)
+                                       : pick_kernel<ST, 0>(has_res, shuf);
   cudaError_t e = gb_set_smem_once(reinterpret_cast<const void*>(kern), Cf::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<(unsigned)grid, threads, Cf::SMEM, st>>>(

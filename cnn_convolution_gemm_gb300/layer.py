@@ -25,7 +25,7 @@ class ConvLayer:
 
     def __init__(self, N, C, H, W, K, R, S, stride=1, pad=0, dilation=1, groups=1,
                  dtype=B.CONV_BF16, layout=B.CONV_NHWC, act=B.CONV_ACT_NONE,
-                 has_residual=False, scale=None):
+                 has_residual=False, scale=None, input_shuffle=1):
         self.shape = (N, C, H, W, K, R, S, stride, pad, dilation, groups)
         self.dtype, self.layout = dtype, layout
         self.desc = B.conv_desc_create(N, C, H, W, K, R, S, stride, pad, dilation, groups, dtype)
@@ -33,6 +33,8 @@ class ConvLayer:
             B.conv_desc_set_layout(self.desc, layout)
         if act or has_residual:
             B.conv_desc_set_epilogue(self.desc, act, has_residual)
+        if input_shuffle > 1:
+            B.conv_desc_set_input_shuffle(self.desc, input_shuffle)
         self.scale = scale
         if scale is not None:
             B.conv_desc_set_requant(self.desc, scale.data_ptr())

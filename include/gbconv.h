@@ -108,6 +108,13 @@ conv_status_t conv_desc_set_layout(conv_desc_t desc, conv_layout_t layout);
  * shaped like y and adds it before the activation.  INT8 supports
  * act in {NONE, RELU} and no residual. */
 conv_status_t conv_desc_set_epilogue(conv_desc_t desc, int act, int has_residual);
+/* Read the input channel-shuffled ([Momenta] Graph層面: "shuffle-channel +
+ * depthwise" fused): with g groups, channel c of the shuffled input is channel
+ * (c mod g) * (C / g) + c div g of x — ShuffleNet's shuffle (view C as g x C/g,
+ * transpose) applied while loading, so the shuffled tensor is never written.
+ * g = 1 turns it off.  Needs C % g == 0.  Honoured by CONV_ALGO_DEPTHWISE (C <=
+ * 256, no residual) and CONV_ALGO_DIRECT; other algorithms do not apply. */
+conv_status_t conv_desc_set_input_shuffle(conv_desc_t desc, int groups);
 /* INT8 only: per-output-channel requant scale, fp32 [K], DEVICE pointer that
  * must stay valid while the descriptor is used.  Output int8 value:
  * q = clamp(round_half_even(fp32(acc + bias[k]) * scale[k]), -128, 127), then

@@ -127,6 +127,24 @@ def test_nc32hw32_layout_validation(B):
         B.conv_desc_destroy(h)
 
 
+def test_input_shuffle_validation(B):
+    d = B.conv_desc_create(1, 240, 28, 28, 240, 3, 3, 1, 1, 1, 240, B.CONV_BF16)
+    with pytest.raises(B.GbconvError) as e:
+        B.conv_desc_set_input_shuffle(d, 7)  # 7 does not divide 240
+    assert e.value.status_name == "CONV_ERR_BAD_PARAM"
+    B.conv_desc_set_input_shuffle(d, 3)
+    ok = {n: a for _, n, a in (B.conv_algo_info(d, i) for i in range(B.CONV_ALGO_COUNT))}
+    assert ok["depthwise3x3"] and ok["direct"]
+    assert not any(a for n, a in ok.items() if n not in ("depthwise3x3", "direct"))
+    g = B.conv_desc_create(1, 64, 8, 8, 64, 3, 3, 1, 1, 1, 1, B.CONV_BF16)
+    B.conv_desc_set_input_shuffle(g, 4)
+    assert not B.conv_algo_info(g, B.CONV_ALGO_IGEMM_N64)[2]
+    B.conv_desc_set_input_shuffle(g, 1)  # off again
+    assert B.conv_algo_info(g, B.CONV_ALGO_IGEMM_N64)[2]
+    for h in (d, g):
+        B.conv_desc_destroy(h)
+
+
 def test_status_strings(B):
     assert B.conv_status_string(0) == "CONV_OK"
     assert B.conv_status_string(6) == "CONV_ERR_TIMEOUT"
