@@ -10,6 +10,7 @@ Other workloads (--workload):
   single_layer  1 x 32 x 28 x 28 fp32 NCHW, 32 filters 3x3: boundary
                 conversion to NHWC bf16, conv, conversion back
   resnet3x3_tf32  the headline layer with fp32 NHWC tensors on the tf32 path
+  gconv_g3      ShuffleNet v1 grouped 1x1 conv (240 -> 240, g = 3, 28x28, batch 64)
   shuffle_dw    ShuffleNet v1 depthwise (240 ch, 28x28, batch 64) reading its
                 input channel-shuffled (g = 3), the shuffle fused into the kernel
   mbv2_block    MobileNetV2 inverted residual, N=64, 56x56: 1x1 24->144 +
@@ -379,6 +380,63 @@ class ShuffleDepthwise(Workload):
                 "sample": f"{n} of 64 images", "seconds": round(dt, 3)}
 
 
+class GroupedConv(Workload):
+    """ShuffleNet v1 (g = 3) grouped 1x1 convolution, 240 -> 240 channels
+    (80 per group) at 28x28, batch 64: one implicit GEMM per group over
+    strided channel views (memory-bound: judged against HBM)."""
+    name = "shufflenet_gconv1x1_c240_g3_28x28_n64_bf16_nhwc"
+    metric = "conv TFLOP/s (direct-equivalent), grouped 1x1 240->240 g=3 @28x28, batch 64"
+
+    def setup(self, dev, rank, args):
+        import torch
+        from cnn_convolution_gemm_gb300 import binding as B
+        from cnn_convolution_gemm_gb300 import synth
+        from cnn_convolution_gemm_gb300.layer import ConvLayer
+        from cnn_convolution_gemm_gb300.workload import ConvShape
+        N, C, H, G = 64, 240, 28, 3
+        self.shape = ConvShape(N, C, H, H, C, 1, 1, 1, 0, 1, G)
+        x = synth.normal((N, H, H, C), 1.0, rank)
+        w = synth.kaiming((C, 1, 1, C // G), rank + 1)
+        b = synth.uniform((C,), -0.1, 0.1, rank + 2)
+        self.sh = torch.cuda.current_stream().cuda_stream
+        self.xh = torch.from_numpy(x).to(torch.bfloat16).pin_memory()
+        self.x = self.xh.to(dev)
+        self.b = torch.from_numpy(b).to(dev)
+        self.layer = ConvLayer(N, C, H, H, C, 1, 1, 1, 0, 1, G, act=B.CONV_ACT_RELU)
+        a, self.fastrun_ms = fastrun_pick(self.layer, self.sh, args, B)
+        self.layer.prepack(torch.from_numpy(w).to(torch.bfloat16).to(dev), a)
+        self.algo_name = B.conv_algo_info(self.layer.desc, a)[1]
+        self.y = torch.empty((N, H, H, C), dtype=torch.bfloat16, device=dev)
+        self.yh = torch.empty((N, H, H, C), dtype=torch.bfloat16).pin_memory()
+
+    def groups(self):
+        return [(self.algo_name, lambda: self.layer.forward(self.x, self.b, out=self.y,
+                                                            stream=self.sh),
+                 self.shape.flops(), self.shape.traffic_bytes(2, 4), "hbm")]
+
+    def h2d(self):
+        return [(self.xh, self.x)]
+
+    def d2h(self):
+        return [(self.y, self.yh)]
+
+    def cpu_baseline(self, args):
+        import numpy as np
+        from cnn_convolution_gemm_gb300 import synth
+        from cnn_convolution_gemm_gb300.workload import ConvShape
+        from oracle import lib as ol
+        n = 8
+        x = synth.normal((n, 28, 28, 240), 1.0, 0)
+        w = synth.kaiming((240, 1, 1, 80), 1)
+        t0 = time.perf_counter()
+        ol.conv2d_f64(np.ascontiguousarray(x.transpose(0, 3, 1, 2)), w.transpose(0, 3, 1, 2),
+                      groups=3)
+        dt = time.perf_counter() - t0
+        f = ConvShape(n, 240, 28, 28, 240, 1, 1, 1, 0, 1, 3).flops()
+        return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": threads(), "kind": "oracle",
+                "sample": f"{n} of 64 images", "seconds": round(dt, 3)}
+
+
 class SingleLayer(Workload):
     name = "single_conv3x3_c32_k32_28x28_n1_f32_nchw"
     metric = "conv TFLOP/s (direct-equivalent), 1x32x28x28 fp32 NCHW, 32 filters 3x3"
@@ -712,7 +770,7 @@ class ResNet50W(Workload):
 
 
 WORKLOADS = {"resnet3x3": ResNetLayer, "resnet3x3_tf32": ResNetLayerTF32,
-             "shuffle_dw": ShuffleDepthwise,
+             "shuffle_dw": ShuffleDepthwise, "gconv_g3": GroupedConv,
              "single_layer": SingleLayer, "mbv2_block": MBv2Block,
              "int8_stages": Int8Stages, "resnet50": ResNet50W}
 

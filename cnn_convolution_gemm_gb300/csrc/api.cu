@@ -258,17 +258,18 @@ static bool applicable(const gbconv_desc_s& d, int algo, const char** why) {
     case CONV_ALGO_IGEMM_N128:
     case CONV_ALGO_IGEMM_N256: {
       if (d.dtype != CONV_BF16 || !nhwc) return *why = "needs bf16 NHWC", false;
-      if (d.groups != 1) return *why = "needs groups == 1", false;
       if (d.R != d.S) return *why = "needs a square kernel", false;
-      if (d.C % 8 || d.K % 8) return *why = "needs C and K multiples of 8", false;
+      // grouped convs run one GEMM per group over strided channel views
+      const int Cg = d.C / d.groups, Kg = d.K / d.groups;
+      if (Cg % 8 || Kg % 8) return *why = "needs C/groups and K/groups multiples of 8", false;
       if (d.stride > 8) return *why = "stride > 8", false;
       if (d.pad > 128 || d.pad - d.dil * (d.R - 1) < -128)
         return *why = "padding/dilation outside the TMA im2col range", false;
       if ((long long)d.N * d.OH * d.OW >= (1LL << 31)) return *why = "N*OH*OW >= 2^31", false;
       if ((long long)d.H * d.W * d.C * 2 >= (1LL << 40)) return *why = "image too large", false;
       const int bn = igemm_block_n(algo);
-      if (bn == 256 && d.K <= 128) return *why = "K <= 128: use a narrower tile", false;
-      if (bn == 128 && d.K <= 64) return *why = "K <= 64: use a narrower tile", false;
+      if (bn == 256 && Kg <= 128) return *why = "K/groups <= 128: use a narrower tile", false;
+      if (bn == 128 && Kg <= 64) return *why = "K/groups <= 64: use a narrower tile", false;
       return true;
     }
     case CONV_ALGO_WINO_F2:
@@ -438,6 +439,25 @@ extern "C" conv_status_t conv_workspace_size(conv_desc_t d, conv_algo_t algo, si
   return ok_status();
 }
 
+// One group of a (possibly) grouped conv as a plain conv over strided channel
+// views: x channels [g*Cg, (g+1)*Cg) with pixel stride C, y / residual
+// channels [g*Kg, (g+1)*Kg) with pixel stride K.
+static gbconv_desc_s group_view(const gbconv_desc_s& d) {
+  gbconv_desc_s e = d;
+  e.C = d.C / d.groups;
+  e.K = d.K / d.groups;
+  e.groups = 1;
+  e.x_cstride = d.C;
+  e.y_kstride = d.K;
+  return e;
+}
+
+// packed implicit-GEMM weights of one group (the layout launch_pack_igemm_weights writes)
+static size_t igemm_group_packed_bytes(const gbconv_desc_s& e) {
+  return e.C == 8 ? (size_t)e.K * gb_ceil_div(e.R * e.S, 8) * 64 * 2  // 8 taps x 8 ch
+                  : (size_t)e.K * e.R * e.S * gb_ceil_div(e.C, 64) * 64 * 2;
+}
+
 extern "C" conv_status_t conv_weights_packed_size(conv_desc_t d, conv_algo_t algo,
                                                   size_t* bytes) {
   if (!d || !bytes) return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
@@ -449,8 +469,7 @@ extern "C" conv_status_t conv_weights_packed_size(conv_desc_t d, conv_algo_t alg
     case CONV_ALGO_IGEMM_N64:
     case CONV_ALGO_IGEMM_N128:
     case CONV_ALGO_IGEMM_N256:
-      *bytes = d->C == 8 ? (size_t)d->K * gb_ceil_div(d->R * d->S, 8) * 64 * 2  // 8 taps x 8 ch
-                         : (size_t)d->K * d->R * d->S * Cp64 * 2;
+      *bytes = igemm_group_packed_bytes(group_view(*d)) * d->groups;
       break;
     case CONV_ALGO_INT8_MMA: *bytes = (size_t)d->K * d->R * d->S * Cp64; break;
     case CONV_ALGO_INT8_TC: *bytes = int8_tc_packed_bytes(*d); break;
@@ -476,7 +495,14 @@ extern "C" conv_status_t conv_weights_prepack(conv_desc_t d, conv_algo_t algo, c
   switch (a) {
     case CONV_ALGO_IGEMM_N64:
     case CONV_ALGO_IGEMM_N128:
-    case CONV_ALGO_IGEMM_N256: e = launch_pack_igemm_weights(*d, w, wpack, s); break;
+    case CONV_ALGO_IGEMM_N256: {  // per group: weights [Kg][R][S][Cg] -> the group's slice
+      const gbconv_desc_s v = group_view(*d);
+      const size_t in_g = (size_t)v.K * v.R * v.S * v.C * 2, out_g = igemm_group_packed_bytes(v);
+      for (int g = 0; g < d->groups && e == cudaSuccess; ++g)
+        e = launch_pack_igemm_weights(v, static_cast<const char*>(w) + g * in_g,
+                                      static_cast<char*>(wpack) + g * out_g, s);
+      break;
+    }
     case CONV_ALGO_INT8_MMA: e = launch_pack_int8_weights(*d, w, wpack, s); break;
     case CONV_ALGO_INT8_TC: e = launch_pack_int8_tc_weights(*d, w, wpack, s); break;
     case CONV_ALGO_IM2COL_GEMM: e = launch_pack_im2col_weights(*d, w, wpack, s); break;
@@ -506,10 +532,18 @@ static conv_status_t fwd_impl(const gbconv_desc_s& d, const void* x, const void*
     case CONV_ALGO_DIRECT: e = launch_direct(d, x, wpack, bias, res, y, s); break;
     case CONV_ALGO_IGEMM_N64:
     case CONV_ALGO_IGEMM_N128:
-    case CONV_ALGO_IGEMM_N256:
-      e = launch_igemm_bf16(d, igemm_block_n(a), x, wpack, static_cast<const float*>(bias), res,
-                            y, err, wait_ns, s);
+    case CONV_ALGO_IGEMM_N256: {  // one launch per group over strided channel views
+      const gbconv_desc_s v = group_view(d);
+      const size_t wg = igemm_group_packed_bytes(v);
+      for (int g = 0; g < d.groups && e == cudaSuccess; ++g)
+        e = launch_igemm_bf16(
+            v, igemm_block_n(a), static_cast<const __nv_bfloat16*>(x) + (size_t)g * v.C,
+            static_cast<const char*>(wpack) + g * wg,
+            bias ? static_cast<const float*>(bias) + (size_t)g * v.K : nullptr,
+            res ? static_cast<const __nv_bfloat16*>(res) + (size_t)g * v.K : nullptr,
+            static_cast<__nv_bfloat16*>(y) + (size_t)g * v.K, err, wait_ns, s);
       break;
+    }
     case CONV_ALGO_DEPTHWISE:
       e = launch_dwconv3x3(d, x, wpack, static_cast<const float*>(bias), res, y, err, wait_ns, s);
       break;

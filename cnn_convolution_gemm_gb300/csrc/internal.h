@@ -18,6 +18,9 @@ struct gbconv_desc_s {
   int OH, OW;
   int pad_hi_delta;    // padding after minus padding before (internal rewrites only; 0 = symmetric)
   int shuffle_groups;  // > 1: the input is read channel-shuffled with this many groups
+  // channel strides of strided views (one group of a grouped conv): elements
+  // between pixels of x and of y / residual; 0 = contiguous (C, K)
+  int x_cstride, y_kstride;
 };
 
 // Device-side error word codes (written by kernels, read by conv_sync_status).

@@ -669,8 +669,9 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   CUtensorMap tmx, tmw;
   {
     cuuint64_t dims[4] = {(cuuint64_t)d.C, (cuuint64_t)d.W, (cuuint64_t)d.H, (cuuint64_t)d.N};
-    cuuint64_t strides[3] = {(cuuint64_t)d.C * ES, (cuuint64_t)d.W * d.C * ES,
-                             (cuuint64_t)d.H * d.W * d.C * ES};
+    const cuuint64_t xcs = d.x_cstride ? d.x_cstride : d.C;  // elements between pixels
+    cuuint64_t strides[3] = {xcs * ES, (cuuint64_t)d.W * xcs * ES,
+                             (cuuint64_t)d.H * d.W * xcs * ES};
     // Bounding box of the first filter tap's pixel: from -pad to
     // (dim - 1) + pad - dil*(R-1) (R == S is required).
     int lower[2] = {-d.pad, -d.pad};
@@ -695,7 +696,7 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
                     // 128-byte swizzle
   {
     cuuint64_t dims[2] = {(cuuint64_t)d.K, (cuuint64_t)p.M};
-    cuuint64_t strides[1] = {(cuuint64_t)d.K * ES};
+    cuuint64_t strides[1] = {(cuuint64_t)(d.y_kstride ? d.y_kstride : d.K) * ES};
     cuuint32_t box[2] = {TF32 ? 32u : 64u, 32};
     cuuint32_t estr[2] = {1, 1};
     if (gb_encode_tiled(&tmy, DT, 2, y, dims, strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B) !=
@@ -714,7 +715,7 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
       return cudaErrorInvalidValue;
   } else if (res && !TF32) {
     cuuint64_t dims[2] = {(cuuint64_t)d.K, (cuuint64_t)p.M};
-    cuuint64_t strides[1] = {(cuuint64_t)d.K * 2};
+    cuuint64_t strides[1] = {(cuuint64_t)(d.y_kstride ? d.y_kstride : d.K) * 2};
     cuuint32_t box[2] = {64, 32};
     cuuint32_t estr[2] = {1, 1};
     if (gb_encode_tiled(&tmr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(res), dims,
