@@ -238,7 +238,8 @@ extern "C" conv_status_t conv_desc_get_output_dims(conv_desc_t d, int* OH, int* 
 static const char* const kAlgoNames[CONV_ALGO_COUNT] = {
     "direct", "igemm_tc_n64", "igemm_tc_n128", "igemm_tc_n256",
     "winograd_f2x2_3x3", "winograd_f6x6_3x3", "depthwise3x3", "int8_igemm_mma",
-    "int8_igemm_tc", "im2col_gemm", "stem_s2d_igemm", "igemm_tf32"};
+    "int8_igemm_tc", "im2col_gemm", "stem_s2d_igemm", "igemm_tf32",
+    "int8_winograd_f2x2_3x3"};
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -315,6 +316,10 @@ static bool applicable(const gbconv_desc_s& d, int algo, const char** why) {
     case CONV_ALGO_STEM_S2D:
       if (d.dtype != CONV_BF16 || !nhwc) return *why = "needs bf16 NHWC", false;
       return stem_s2d_applicable(d, why);
+    case CONV_ALGO_INT8_WINO_F2:
+      if (d.dtype != CONV_INT8 || !nhwc) return *why = "needs int8 NHWC", false;
+      if (!d.scale) return *why = "int8 needs a requant scale", false;
+      return int8_wino_applicable(d, why);
     case CONV_ALGO_IGEMM_TF32:
       if (d.dtype != CONV_F32 || !nhwc) return *why = "needs fp32 NHWC", false;
       if (d.groups != 1 || d.R != d.S) return *why = "needs groups == 1, square kernel", false;
@@ -436,6 +441,7 @@ extern "C" conv_status_t conv_workspace_size(conv_desc_t d, conv_algo_t algo, si
   if (a == CONV_ALGO_INT8_TC) *bytes = int8_tc_workspace_bytes(*d);
   if (a == CONV_ALGO_IM2COL_GEMM) *bytes = im2col_workspace_bytes(*d);
   if (a == CONV_ALGO_STEM_S2D) *bytes = stem_s2d_workspace_bytes(*d);
+  if (a == CONV_ALGO_INT8_WINO_F2) *bytes = int8_wino_workspace_bytes(*d);
   return ok_status();
 }
 
@@ -476,6 +482,7 @@ extern "C" conv_status_t conv_weights_packed_size(conv_desc_t d, conv_algo_t alg
     case CONV_ALGO_IM2COL_GEMM: *bytes = im2col_packed_bytes(*d); break;
     case CONV_ALGO_STEM_S2D: *bytes = stem_s2d_packed_bytes(*d); break;
     case CONV_ALGO_IGEMM_TF32: *bytes = igemm_tf32_packed_bytes(*d); break;
+    case CONV_ALGO_INT8_WINO_F2: *bytes = int8_wino_packed_bytes(*d); break;
     case CONV_ALGO_WINO_F2: *bytes = winograd_packed_bytes(*d, 2); break;
     case CONV_ALGO_WINO_F6: *bytes = winograd_packed_bytes(*d, 6); break;
     default: *bytes = user_weight_bytes(*d); break;
@@ -508,6 +515,7 @@ extern "C" conv_status_t conv_weights_prepack(conv_desc_t d, conv_algo_t algo, c
     case CONV_ALGO_IM2COL_GEMM: e = launch_pack_im2col_weights(*d, w, wpack, s); break;
     case CONV_ALGO_STEM_S2D: e = launch_pack_stem_weights(*d, w, wpack, s); break;
     case CONV_ALGO_IGEMM_TF32: e = launch_pack_tf32_weights(*d, w, wpack, s); break;
+    case CONV_ALGO_INT8_WINO_F2: e = launch_pack_int8_wino(*d, w, wpack, s); break;
     case CONV_ALGO_DEPTHWISE: e = launch_pack_dw_weights(*d, w, wpack, s); break;
     case CONV_ALGO_WINO_F2: e = launch_winograd_filter_transform(*d, 2, w, wpack, s); break;
     case CONV_ALGO_WINO_F6: e = launch_winograd_filter_transform(*d, 6, w, wpack, s); break;
@@ -558,6 +566,16 @@ static conv_status_t fwd_impl(const gbconv_desc_s& d, const void* x, const void*
         return gb_fail(CONV_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
       e = launch_im2col_gemm(d, x, wpack, static_cast<const float*>(bias), res, y, ws, err,
                              wait_ns, s);
+      break;
+    }
+    case CONV_ALGO_INT8_WINO_F2: {
+      const size_t need = int8_wino_workspace_bytes(d);
+      if (!ws || ws_bytes < need)
+        return gb_fail(CONV_ERR_WORKSPACE, "workspace of %zu bytes needed", need);
+      if (reinterpret_cast<uintptr_t>(ws) & 255u)
+        return gb_fail(CONV_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+      e = launch_int8_wino(d, x, wpack, static_cast<const int32_t*>(bias), y, ws, err, wait_ns,
+                           s);
       break;
     }
     case CONV_ALGO_IGEMM_TF32:
@@ -992,6 +1010,7 @@ static bool implemented(int algo) {
     case CONV_ALGO_IM2COL_GEMM:
     case CONV_ALGO_STEM_S2D:
     case CONV_ALGO_IGEMM_TF32:
+    case CONV_ALGO_INT8_WINO_F2:
       return true;
     default:
       return false;

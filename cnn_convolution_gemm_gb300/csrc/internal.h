@@ -182,3 +182,14 @@ cudaError_t launch_nc32_convert(const void* x, void* y, int N, int C, int H, int
 size_t igemm_tf32_packed_bytes(const gbconv_desc_s& d);
 cudaError_t launch_pack_tf32_weights(const gbconv_desc_s& d, const void* w, void* wpack,
                                      cudaStream_t st);
+
+// Exact int8 Winograd F(2x2,3x3) with float intermediates: wpack [16][2K][Cp]
+// fp16 (the split 4U), workspace V [16][T][Cp] fp16 + M [16][T][2K] fp32.
+bool int8_wino_applicable(const gbconv_desc_s& d, const char** why);
+size_t int8_wino_packed_bytes(const gbconv_desc_s& d);
+size_t int8_wino_workspace_bytes(const gbconv_desc_s& d);
+cudaError_t launch_pack_int8_wino(const gbconv_desc_s& d, const void* w, void* wpack,
+                                  cudaStream_t st);
+cudaError_t launch_int8_wino(const gbconv_desc_s& d, const void* x, const void* wpack,
+                             const int32_t* bias, void* y, void* ws, int* err,
+                             unsigned long long wait_ns, cudaStream_t st);

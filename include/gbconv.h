@@ -83,7 +83,10 @@ typedef int conv_algo_t;
                                       space-to-depth + stride-1 implicit GEMM (workspace) */
 #define CONV_ALGO_IGEMM_TF32 11    /* implicit GEMM over fp32 NHWC tensors on kind::tf32
                                       (inputs read with tf32's 10-bit mantissa)          */
-#define CONV_ALGO_COUNT 12
+#define CONV_ALGO_INT8_WINO_F2 12  /* int8 Winograd F(2x2,3x3) with float intermediates
+                                      ([Beta]), exact: integer transforms, split filter
+                                      transform, fp32 sums below 2^24 (C <= 896; workspace) */
+#define CONV_ALGO_COUNT 13
 
 /* ---- descriptor --------------------------------------------------------- */
 

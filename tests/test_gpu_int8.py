@@ -160,3 +160,51 @@ def test_int8_nc32hw32_layout(case):
     B.conv_sync_status(torch.cuda.current_stream().cuda_stream)
     ref = ol.conv2d_i8(x, nhwc_to_nchw(w), b, scale, pad=1, relu=True)
     assert np.array_equal(y.cpu().numpy(), _to_nc32(ref))
+
+
+INT8_WINO = 12  # CONV_ALGO_INT8_WINO_F2
+
+
+@pytest.mark.parametrize("C,HW", [(64, 56), (128, 28), (256, 14), (512, 7)])
+def test_int8_winograd_resnet_stage_shapes_full_batch(C, HW):
+    """int8 Winograd F(2x2,3x3) with float intermediates equals the direct int8
+    convolution bit for bit on the four stage shapes, batch 32."""
+    torch = need_gpu()
+    y, ref = _run(torch, 32, C, HW, HW, C, 3, 1, 1, seed=C + 1, algo=INT8_WINO)
+    assert np.array_equal(y, ref), int((y != ref).sum())
+
+
+@pytest.mark.parametrize("case", [
+    # N, C, H, W, K, pad, relu, bias
+    (2, 16, 9, 7, 20, 1, True, True),     # odd output: partial 2x2 tiles; K % 16 != 0
+    (3, 32, 10, 11, 64, 0, False, True),  # no padding (8 x 9 output), no ReLU
+    (1, 48, 5, 5, 8, 1, True, False),     # no bias
+])
+def test_int8_winograd_edge_cases(case):
+    torch = need_gpu()
+    N, C, H, W, K, pad, relu, bias = case
+    y, ref = _run(torch, N, C, H, W, K, 3, 1, pad, relu, bias, seed=N + C, algo=INT8_WINO)
+    assert np.array_equal(y, ref)
+
+
+def test_int8_winograd_exactness_bound_extremes():
+    """896 channels (the largest exact case) with x = -128 and filters of +-128/127
+    extremes: the fp32 Winograd-domain sums reach their largest magnitudes."""
+    torch = need_gpu()
+    from cnn_convolution_gemm_gb300 import binding as B
+    from cnn_convolution_gemm_gb300.layer import ConvLayer
+    dev = torch.device("cuda:0")
+    N, C, H, K = 1, 896, 6, 8
+    x = np.full((N, H, H, C), -128, np.int8)
+    pat = np.array([[127, -128, 127], [-128, 127, -128], [127, -128, 127]], np.int8)
+    w = np.empty((K, 3, 3, C), np.int8)
+    for k in range(K):
+        w[k] = (pat if k % 2 == 0 else -pat - 1)[:, :, None]
+    scale = np.full(K, 2e-6, np.float32)
+    layer = ConvLayer(N, C, H, H, K, 3, 3, 1, 1, dtype=B.CONV_INT8,
+                      scale=torch.from_numpy(scale).to(dev))
+    layer.prepack(torch.from_numpy(w).to(dev), INT8_WINO)
+    y = layer(torch.from_numpy(x).to(dev))
+    B.conv_sync_status(torch.cuda.current_stream().cuda_stream)
+    ref = ol.conv2d_i8(nhwc_to_nchw(x), nhwc_to_nchw(w), None, scale, pad=1, relu=False)
+    assert np.array_equal(y.cpu().numpy(), nchw_to_nhwc(ref))
