@@ -642,12 +642,32 @@ class Int8Stages(Workload):
                                    shape=ConvShape(32, C, HW, HW, C, 3, 3, 1, 1),
                                    name=f"{C}@{HW}", algo=names[-1]))
         self.algo_name = "+".join(sorted(set(names)))
+        # each stage's launches (int8 -> bf16 copy, GEMM, ...) as one CUDA graph:
+        # a replay costs one launch on the host, so the stages are not waiting
+        # on the host between kernels (--no-graph: launch call by call)
+        self.graphs = None
+        if not args.no_graph:
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                for it in self.items:
+                    it["layer"].forward(it["x"], it["b"], out=it["y"])
+            torch.cuda.current_stream().wait_stream(side)
+            self.graphs = []
+            c0 = B.conv_launch_count()
+            for it in self.items:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    it["layer"].forward(it["x"], it["b"], out=it["y"])
+                self.graphs.append(g)
+            self.launches_per_step = B.conv_launch_count() - c0
 
     def groups(self):
         return [(f"{it['name']}:{it['algo']}",
-                 (lambda it=it: it["layer"].forward(it["x"], it["b"], out=it["y"], stream=self.sh)),
+                 (lambda it=it: it["layer"].forward(it["x"], it["b"], out=it["y"], stream=self.sh))
+                 if self.graphs is None else self.graphs[i].replay,
                  it["shape"].flops(), it["shape"].traffic_bytes(1, 4, out_bytes=1), "tensor")
-                for it in self.items]
+                for i, it in enumerate(self.items)]
 
     def h2d(self):
         return [(it["xh"], it["x"]) for it in self.items]
@@ -684,7 +704,10 @@ class ResNet50W(Workload):
         x = synth.normal((self.N, 3, 224, 224), 1.0, 100 + rank)
         self.xh = torch.from_numpy(x).pin_memory()
         self.x = self.xh.to(dev)
+        from cnn_convolution_gemm_gb300 import binding as B
+        c0 = B.conv_launch_count()
         self.out = self.net.forward(self.x)
+        self.launches_per_step = B.conv_launch_count() - c0
         self.graph = not getattr(args, "no_graph", False)
         if self.graph:  # one CUDA-graph launch per forward (57 kernels inside)
             self.out = self.net.capture(self.x)
@@ -828,16 +851,20 @@ def launches_for(algo_name):
 
 
 def count_launches(wl, groups):
-    if isinstance(wl, ResNet50W):
-        return len(wl.net.algos) + 3  # 54 convs + layout conversion, max pool, avg pool
-    if isinstance(wl, ResNetLayer) and wl.algo_name.startswith("winograd"):
-        from cnn_convolution_gemm_gb300 import binding as B
-        ws = B.conv_workspace_size(wl.layer.desc, wl.layer.algo)
-        m = 2 if "f2x2" in wl.algo_name else 6
-        per_img = ((56 + m - 1) // m) ** 2 * (m + 2) ** 2 * (256 * 2 + 256 * 4)
-        nb = max(1, min(32, ws // per_img))
-        return 3 * -(-32 // nb)
-    return len(groups)
+    """Kernels of this library one step enqueues, read from the library's own
+    launch counter: around one untimed eager step, or, for a workload that
+    replays CUDA graphs, around its capture (a replay does not pass through the
+    library)."""
+    import torch
+    from cnn_convolution_gemm_gb300 import binding as B
+    n = getattr(wl, "launches_per_step", None)
+    if n is not None:
+        return n
+    c0 = B.conv_launch_count()
+    for g in groups:
+        g[1]()
+    torch.cuda.synchronize()
+    return B.conv_launch_count() - c0
 
 
 def main():
@@ -854,7 +881,8 @@ def main():
                          "selection), else select and save it there")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
-                    help="resnet50: launch layer by layer instead of replaying a CUDA graph")
+                    help="resnet50, int8_stages: launch call by call instead of replaying CUDA "
+                         "graphs")
     ap.add_argument("--cpu-images", type=int, default=8)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

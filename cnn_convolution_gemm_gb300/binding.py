@@ -82,6 +82,7 @@ SIGNATURES = {
     "conv_status_string": (_cp, [_i]),
     "conv_last_error_detail": (_cp, []),
     "conv_version": (_cp, []),
+    "conv_launch_count": (_i, [ctypes.POINTER(ctypes.c_ulonglong)]),
 }
 
 
@@ -311,3 +312,10 @@ def conv_last_error_detail():
 
 def conv_version():
     return load_library().conv_version().decode()
+
+
+def conv_launch_count():
+    """Kernels the library has enqueued since it was loaded."""
+    n = ctypes.c_ulonglong(0)
+    _check(load_library().conv_launch_count(ctypes.byref(n)), "conv_launch_count")
+    return n.value

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -992,6 +993,16 @@ extern "C" const char* conv_status_string(conv_status_t s) {
 }
 
 extern "C" const char* conv_last_error_detail(void) { return g_detail; }
+
+static std::atomic<unsigned long long> g_launches{0};
+
+void gb_count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+extern "C" conv_status_t conv_launch_count(unsigned long long* count) {
+  if (!count) return gb_fail(CONV_ERR_BAD_PARAM, "count is NULL");
+  *count = g_launches.load(std::memory_order_relaxed);
+  return ok_status();
+}
 
 extern "C" const char* conv_version(void) { return GBCONV_VERSION; }
 

@@ -32,6 +32,8 @@ conv_status_t gb_fail(conv_status_t st, const char* fmt, ...);
 int* gb_device_error_word();
 // Number of SMs of the current device (cached).
 int gb_num_sms();
+// Called after each kernel launch: counts the kernels the library enqueues.
+void gb_count_launch();
 // Raise a kernel's dynamic shared-memory limit, once per (kernel, device): the
 // attribute call costs host time on every launch otherwise.
 cudaError_t gb_set_smem_once(const void* func, int bytes);

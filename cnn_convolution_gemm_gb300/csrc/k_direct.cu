@@ -159,17 +159,20 @@ cudaError_t launch_direct(const gbconv_desc_s& d, const void* x, const void* w, 
           p, static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w),
           static_cast<const float*>(bias), static_cast<const __nv_bfloat16*>(res),
           static_cast<__nv_bfloat16*>(y));
+      gb_count_launch();
       break;
     case CONV_F32:
       direct_conv_kernel<float><<<grid, block, 0, st>>>(
           p, static_cast<const float*>(x), static_cast<const float*>(w),
           static_cast<const float*>(bias), static_cast<const float*>(res),
           static_cast<float*>(y));
+      gb_count_launch();
       break;
     case CONV_INT8:
       direct_conv_int8_kernel<<<grid, block, 0, st>>>(
           p, static_cast<const int8_t*>(x), static_cast<const int8_t*>(w),
           static_cast<const int32_t*>(bias), d.scale, static_cast<int8_t*>(y));
+      gb_count_launch();
       break;
   }
   return cudaGetLastError();

@@ -456,6 +456,7 @@ cudaError_t launch_st(const gbconv_desc_s& d, const void* x, const void* w, cons
   kern<<<(unsigned)grid, threads, Cf::SMEM, st>>>(
       tm, p, static_cast<const __nv_bfloat16*>(w), bias, static_cast<const __nv_bfloat16*>(res),
       static_cast<__nv_bfloat16*>(y));
+  gb_count_launch();
   return cudaGetLastError();
 }
 
@@ -466,6 +467,7 @@ cudaError_t launch_pack_dw_weights(const gbconv_desc_s& d, const void* w, void* 
   const int n = 9 * d.C;
   pack_dw_weights_kernel<<<gb_ceil_div(n, 256), 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(w), static_cast<__nv_bfloat16*>(wpack), d.C);
+  gb_count_launch();
   return cudaGetLastError();
 }
 

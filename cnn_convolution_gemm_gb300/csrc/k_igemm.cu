@@ -736,6 +736,7 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   }
   igemm_bf16_tc_kernel<BN, MODE_CONV, LIGHT, TF32><<<grid, 192, Cf::SMEM, st>>>(tmx, tmw, tmy,
                                                                                tmr, p);
+  gb_count_launch();
   return cudaGetLastError();
 }
 
@@ -796,6 +797,7 @@ cudaError_t launch_batched_bn(int batch, int M, int N, int Kred, const void* A, 
       return cudaErrorInvalidValue;
   }
   igemm_bf16_tc_kernel<BN, MODE_BATCHED><<<grid, 192, Cf::SMEM, st>>>(tma, tmb, tma, tmo, p);
+  gb_count_launch();
   return cudaGetLastError();
 }
 
@@ -892,6 +894,7 @@ cudaError_t launch_pack_tf32_weights(const gbconv_desc_s& d, const void* w, void
   pack_tf32_weights_kernel<<<grid, 256, 0, st>>>(static_cast<const float*>(w),
                                                   static_cast<float*>(wpack), d.K, d.R * d.S,
                                                   d.C, Cp);
+  gb_count_launch();
   return cudaGetLastError();
 }
 
@@ -904,6 +907,7 @@ cudaError_t launch_pack_igemm_weights(const gbconv_desc_s& d, const void* w, voi
     pack_igemm_weights_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(w),
                                                     static_cast<__nv_bfloat16*>(wpack), d.K,
                                                     taps8, 8, 8, d.R * d.S);
+    gb_count_launch();
     return cudaGetLastError();
   }
   const int Cp = gb_ceil_div(d.C, BK) * BK;
@@ -913,5 +917,6 @@ cudaError_t launch_pack_igemm_weights(const gbconv_desc_s& d, const void* w, voi
   pack_igemm_weights_kernel<<<grid, block, 0, st>>>(static_cast<const __nv_bfloat16*>(w),
                                                     static_cast<__nv_bfloat16*>(wpack), d.K,
                                                     d.R * d.S, d.C, Cp, d.R * d.S);
+  gb_count_launch();
   return cudaGetLastError();
 }

@@ -78,6 +78,7 @@ cudaError_t launch_im2col_gemm(const gbconv_desc_s& d, const void* x, const void
   im2col_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x),
                                       static_cast<__nv_bfloat16*>(ws), d.H, d.W, d.C, d.S,
                                       d.R * d.S, d.stride, d.pad, d.dil, d.OH, d.OW, M);
+  gb_count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const gbconv_desc_s g = as_gemm(d);

@@ -233,12 +233,14 @@ cudaError_t launch_igemm_int8(const gbconv_desc_s& d, const void* x, const void*
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)mt, gb_ceil_div(d.K, 128));
     igemm_int8_kernel<128><<<grid, THREADS, smem, st>>>(p, xb, wb, yb);
+    gb_count_launch();
   } else {
     constexpr int smem = STAGES * (BM * BK + 64 * BK);
     cudaError_t e = gb_set_smem_once(reinterpret_cast<const void*>(igemm_int8_kernel<64>), smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)mt, gb_ceil_div(d.K, 64));
     igemm_int8_kernel<64><<<grid, THREADS, smem, st>>>(p, xb, wb, yb);
+    gb_count_launch();
   }
   return cudaGetLastError();
 }
@@ -251,5 +253,6 @@ cudaError_t launch_pack_int8_weights(const gbconv_desc_s& d, const void* w, void
   pack_int8_weights_kernel<<<grid, 256, 0, st>>>(static_cast<const int8_t*>(w),
                                                  static_cast<int8_t*>(wpack), d.K, d.R * d.S, d.C,
                                                  Cp);
+  gb_count_launch();
   return cudaGetLastError();
 }

@@ -188,11 +188,13 @@ cudaError_t launch_pack_int8_tc_weights(const gbconv_desc_s& d, const void* w, v
     pack_int8_split_kernel<<<grid_for(total), 256, 0, st>>>(
         static_cast<const int8_t*>(w), static_cast<__nv_bfloat16*>(wpack), d.K, d.R * d.S, d.C,
         Cp);
+    gb_count_launch();
     return cudaGetLastError();
   }
   const long long total = (long long)d.K * d.R * d.S * Cp;
   pack_int8_as_bf16_kernel<<<grid_for(total), 256, 0, st>>>(
       static_cast<const int8_t*>(w), static_cast<__nv_bfloat16*>(wpack), d.K, d.R * d.S, d.C, Cp);
+  gb_count_launch();
   return cudaGetLastError();
 }
 
@@ -206,6 +208,7 @@ cudaError_t launch_int8_tc(const gbconv_desc_s& d, const void* x, const void* wp
   const int nc32 = d.layout == CONV_NC32HW32 ? 1 : 0;
   int8_to_bf16_kernel<<<grid_for(n16), 256, 0, st>>>(static_cast<const int8_t*>(x), xb, n16, d.C,
                                                      (long long)d.H * d.W, nc32);
+  gb_count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   gbconv_desc_s db = d;  // the same convolution over the bf16 copy
@@ -235,5 +238,6 @@ cudaError_t launch_int8_tc(const gbconv_desc_s& d, const void* x, const void* wp
                                                           d.act == CONV_ACT_RELU ? 1 : 0,
                                                           static_cast<int8_t*>(y),
                                                           (long long)d.OH * d.OW, nc32);
+  gb_count_launch();
   return cudaGetLastError();
 }

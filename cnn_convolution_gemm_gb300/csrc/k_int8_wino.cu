@@ -216,6 +216,7 @@ cudaError_t launch_pack_int8_wino(const gbconv_desc_s& d, const void* w, void* w
   const Geo g = geo(d);
   i8w_filter_kernel<<<grid_for((long long)d.K * g.Cp), 256, 0, st>>>(
       static_cast<const int8_t*>(w), static_cast<__half*>(wpack), d.K, d.C, g.Cp);
+  gb_count_launch();
   return cudaGetLastError();
 }
 
@@ -228,6 +229,7 @@ cudaError_t launch_int8_wino(const gbconv_desc_s& d, const void* x, const void* 
                                       ((size_t)16 * g.T * g.Cp * 2 + 255) / 256 * 256);
   i8w_input_kernel<<<grid_for(g.T * (g.Cp / 4)), 256, 0, st>>>(
       static_cast<const int8_t*>(x), v, d.H, d.W, d.C, g.Cp, d.pad, g.TH, g.TW, g.T);
+  gb_count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int n2 = 2 * d.K;
@@ -237,5 +239,6 @@ cudaError_t launch_int8_wino(const gbconv_desc_s& d, const void* x, const void* 
   i8w_output_kernel<<<grid_for(g.T * d.K), 256, 0, st>>>(
       m, static_cast<int8_t*>(y), bias, d.scale, d.act == CONV_ACT_RELU ? 1 : 0, d.K, g.T, g.TH,
       g.TW, d.OH, d.OW);
+  gb_count_launch();
   return cudaGetLastError();
 }

@@ -154,6 +154,7 @@ cudaError_t launch_nchw_f32_to_nhwc_bf16(const float* x, void* y, int N, int C, 
                                          int C_out, cudaStream_t st) {
   nchw_f32_to_nhwc_bf16_kernel<<<grid_for((long long)N * H * W), kBlock, 0, st>>>(
       x, static_cast<__nv_bfloat16*>(y), N, C, H, W, C_out);
+  gb_count_launch();
   return cudaGetLastError();
 }
 
@@ -161,6 +162,7 @@ cudaError_t launch_nhwc_bf16_to_nchw_f32(const void* x, float* y, int N, int C, 
                                          int C_in, cudaStream_t st) {
   nhwc_bf16_to_nchw_f32_kernel<<<grid_for((long long)N * C * H * W), kBlock, 0, st>>>(
       static_cast<const __nv_bfloat16*>(x), y, N, C, H, W, C_in);
+  gb_count_launch();
   return cudaGetLastError();
 }
 
@@ -170,6 +172,7 @@ cudaError_t launch_maxpool_nhwc_bf16(const void* x, void* y, int N, int C, int H
   maxpool_nhwc_bf16_kernel<<<grid_for((long long)N * OH * OW * (C / 8)), kBlock, 0, st>>>(
       static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), N, C, H, W, k, stride,
       pad, OH, OW);
+  gb_count_launch();
   return cudaGetLastError();
 }
 
@@ -177,6 +180,7 @@ cudaError_t launch_avgpool_nhwc_bf16(const void* x, void* y, int N, int C, int H
                                      cudaStream_t st) {
   avgpool_nhwc_bf16_kernel<<<grid_for((long long)N * (C / 8)), kBlock, 0, st>>>(
       static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), N, C, H * W);
+  gb_count_launch();
   return cudaGetLastError();
 }
 
@@ -185,6 +189,7 @@ cudaError_t launch_fill_random(void* p, size_t bytes, int elem_bytes, uint32_t s
   const long long n = (long long)(bytes / elem_bytes);
   fill_random_kernel<<<grid_for(n), kBlock, 0, st>>>(static_cast<uint8_t*>(p), n, elem_bytes,
                                                      seed);
+  gb_count_launch();
   return cudaGetLastError();
 }
 
@@ -221,5 +226,6 @@ cudaError_t launch_nc32_convert(const void* x, void* y, int N, int C, int H, int
   nc32_convert_kernel<<<grid, 256, 0, st>>>(static_cast<const int8_t*>(x),
                                             static_cast<int8_t*>(y), N, C, (long long)H * W,
                                             to_nc32);
+  gb_count_launch();
   return cudaGetLastError();
 }

@@ -508,6 +508,7 @@ cudaError_t launch_pack_mbv2(int cin, int E, int cout, const void* we, const flo
                                             static_cast<const __nv_bfloat16*>(wd),
                                             static_cast<const __nv_bfloat16*>(wp), cin, cout,
                                             static_cast<__nv_bfloat16*>(out));
+  gb_count_launch();
   return cudaGetLastError();
 }
 
@@ -546,5 +547,6 @@ cudaError_t launch_mbv2_block(int N, int H, int W, int cin, int E, int cout, con
   mbv2_block_kernel<144><<<grid, THREADS, C::SMEM, st>>>(
       tm, p, static_cast<const uint8_t*>(wpack), b_dw, b_proj,
       static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y));
+  gb_count_launch();
   return cudaGetLastError();
 }

@@ -129,6 +129,7 @@ cudaError_t launch_pack_stem_weights(const gbconv_desc_s& d, const void* w, void
   pack_stem_weights_kernel<<<grid_for(total), 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(w), static_cast<__nv_bfloat16*>(wpack), d.K, d.R, d.pad,
       g.a_min, g.R2);
+  gb_count_launch();
   return cudaGetLastError();
 }
 
@@ -138,6 +139,7 @@ cudaError_t launch_stem_s2d(const gbconv_desc_s& d, const void* x, const void* w
   const long long pixels = (long long)d.N * (d.H / 2) * (d.W / 2);
   space_to_depth8_kernel<<<grid_for(pixels), 256, 0, st>>>(static_cast<const uint4*>(x),
                                                            static_cast<uint4*>(ws), d.N, d.H, d.W);
+  gb_count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const gbconv_desc_s e2 = stem_desc(d);

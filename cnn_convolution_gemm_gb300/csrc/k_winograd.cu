@@ -384,6 +384,7 @@ cudaError_t run_winograd(const gbconv_desc_s& d, const void* x, const void* wpac
     const int strips = p.nb * p.th * gb_ceil_div(p.tw, TWC) * gb_ceil_div(d.C, WCB);
     input_transform_kernel<TT, F16><<<strips, 256, InCfg<TT>::SMEM, st>>>(tmx, p, V, err,
                                                                             wait_ns);
+    gb_count_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     e = launch_batched_gemm_tc(A * A, (int)T, d.K, d.C, V, wpack, Mws, F16 ? 0 : 1, block_n, err,
@@ -392,6 +393,7 @@ cudaError_t run_winograd(const gbconv_desc_s& d, const void* x, const void* wpac
     const long long out_threads = T * d.K;
     output_transform_kernel<TT><<<(unsigned)gb_ceil_div_ll(out_threads, 256), 256, 0, st>>>(
         p, Mws, bias, static_cast<const __nv_bfloat16*>(res), static_cast<__nv_bfloat16*>(y));
+    gb_count_launch();
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -420,6 +422,7 @@ cudaError_t launch_winograd_filter_transform(const gbconv_desc_s& d, int m, cons
     filter_transform_kernel<F2T, false><<<grid, 128, 0, st>>>(wb, wpack, d.K, d.C);
   else
     filter_transform_kernel<F6T, true><<<grid, 128, 0, st>>>(wb, wpack, d.K, d.C);
+  gb_count_launch();
   return cudaGetLastError();
 }
 

@@ -272,6 +272,12 @@ const char* conv_status_string(conv_status_t status);
 const char* conv_last_error_detail(void);
 /* Library version string. */
 const char* conv_version(void);
+/* Number of kernels this library has enqueued, on any stream and from any host
+ * thread, since it was loaded: forward, prepack and layout kernels alike.  The
+ * difference across a call is the number of kernels that call launched (also
+ * while a stream is being captured into a CUDA graph, where it is the number of
+ * kernel nodes the call added).  count must not be NULL. */
+conv_status_t conv_launch_count(unsigned long long* count);
 
 #ifdef __cplusplus
 }

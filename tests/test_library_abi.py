@@ -151,6 +151,18 @@ def test_status_strings(B):
     assert B.conv_version().startswith("gbconv")
 
 
+def test_launch_counter_does_not_move_on_rejected_calls(B):
+    # calls that fail validation on the host launch nothing
+    n0 = B.conv_launch_count()
+    h = B.conv_desc_create(2, 64, 8, 8, 64, 3, 3, 1, 1)
+    try:
+        with pytest.raises(B.GbconvError):
+            B.conv_fwd(h, 0, 0, None, None, 0, B.CONV_ALGO_IGEMM_N64, None, 0, None)
+    finally:
+        B.conv_desc_destroy(h)
+    assert B.conv_launch_count() == n0
+
+
 def test_fastrun_file_roundtrip_and_corruption(B, tmp_path):
     B.conv_fastrun_clear()
     p = tmp_path / "map.txt"
