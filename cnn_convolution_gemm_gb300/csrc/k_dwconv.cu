@@ -13,16 +13,19 @@
 //     row's slot in shared memory (a fixed pitch, so shared loads take
 //     constant offsets), and out-of-bounds elements arrive as zeros, which is
 //     the padding;
-//   * a ring of four shared-memory buffers: the loads of the next three
-//     blocks are in flight while the current one is computed, so bytes in
-//     flight do not depend on registers or occupancy, and warps that run
-//     ahead of the slowest one still find their next tiles loaded;
+//   * two CTAs per SM, each with a ring of two shared-memory buffers: the
+//     loads of a CTA's next block are in flight while it computes the current
+//     one, so bytes in flight do not depend on registers, and the two CTAs'
+//     warps hide each other's latencies;
 //   * a thread owns 4 channels of two adjacent output columns and walks down
 //     the block's input rows: each row's values (4 or 5 columns, one 8-byte
-//     shared load each) are converted to fp32 once and added into the
-//     accumulators of the up to three output rows they reach (fp32 weights in
-//     registers); a finished output row gets bias / residual / activation and
-//     is stored as bf16;
+//     shared load each) are added into the accumulators of the up to three
+//     output rows they reach; a finished output row gets bias / residual /
+//     activation and is stored as bf16;
+//   * the multiply-adds take the bf16 input and weight straight from their
+//     packed 32-bit words (fma.rn.f32.bf16: bf16 x bf16 + fp32 -> fp32, the
+//     product exact, one rounding), so no instruction widens the operands and
+//     the result equals the fp32 FMA of the widened values;
 //   * a warp releases a buffer through an mbarrier when it is done with it,
 //     and the loading thread refills it once every warp has, so warps are not
 //     held to a common pace by block-wide barriers;
@@ -37,9 +40,14 @@
 
 namespace {
 
-constexpr int MAX_THREADS = 384;
-constexpr int NBUF = 4;              // shared-memory ring depth: three loads in flight
-constexpr int BUF_MAX = 55 * 1024;   // bytes per buffer (4 x 55 KB + barriers fit 227 KB)
+// Two CTAs of up to 256 threads share an SM (registers: 2 x 256 x 128), each
+// with a ring of two shared-memory buffers: while a CTA computes one block, the
+// loads of its next block are in flight, and the other CTA's warps cover the
+// latencies of this one's.
+constexpr int MAX_THREADS = 256;
+constexpr int CTAS_PER_SM = 2;
+constexpr int NBUF = 2;              // shared-memory ring depth per CTA
+constexpr int BUF_MAX = 54 * 1024;   // bytes per buffer (2 CTAs x 2 x 54 KB fit 228 KB)
 
 template <int ST>
 struct DwCfg {
@@ -65,9 +73,8 @@ struct DwParams {
 // work items of one block: (4-channel group, pair of output columns)
 __host__ __device__ inline int gb_items(const DwParams& p) { return ((p.owt + 1) / 2) * (p.cb / 4); }
 
-// Two fp32 values in one 64-bit register pair: the operand of fma.rn.f32x2,
-// which does two fp32 fused multiply-adds (each rounded once) per instruction.
-// Pairs here are channels (c, c + 1).
+// Two fp32 values in one 64-bit register pair: channels (c, c + 1) of an
+// output on their way to one bf16x2 word.
 typedef unsigned long long f32x2;
 
 __device__ __forceinline__ f32x2 f2_pack(float lo, float hi) {
@@ -77,15 +84,6 @@ __device__ __forceinline__ f32x2 f2_pack(float lo, float hi) {
 }
 __device__ __forceinline__ void f2_unpack(f32x2 v, float& lo, float& hi) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
-  f32x2 d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-// a bf16x2 word -> its two values in fp32 (exact: a bf16 is the top half of an fp32)
-__device__ __forceinline__ f32x2 bf16x2_to_f2(uint32_t u) {
-  return f2_pack(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 // an fp32 pair -> one bf16x2 word (round to nearest even), negative results set
 // to zero when RELU; the activation commutes with the monotone rounding
@@ -109,6 +107,18 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
   return v;
+}
+
+// a * b + c for bf16 a, b (bit patterns) and fp32 c: the product of two bf16
+// values is exact in fp32, so this is the fp32 FMA of the widened operands
+__device__ __forceinline__ float fma_bf16(unsigned short a, unsigned short b, float c) {
+  float d;
+  asm("fma.rn.f32.bf16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+  return d;
+}
+// the two bf16 halves of a packed word (lo: the element at the lower address)
+__device__ __forceinline__ void halves(uint32_t u, unsigned short& lo, unsigned short& hi) {
+  asm("mov.b32 {%0, %1}, %2;" : "=h"(lo), "=h"(hi) : "r"(u));
 }
 
 // bias / residual / activation of 4 channels, rounding to bf16, one 8-byte store
@@ -135,16 +145,16 @@ __device__ __forceinline__ void store4(f32x2 a0, f32x2 a1, __nv_bfloat16* yp,
 
 // One work item of one block: 4 channels x 2 output columns x RB output rows.
 // Input row rho feeds output row (rho - i) / ST through filter row i; each input
-// value is converted once and added into the accumulators of the (up to three)
+// value is loaded once and added into the accumulators of the (up to three)
 // output rows it reaches.  Output row o lives in slot o % 3 and is stored once
 // its last input row, o * ST + 2, has been added.  FULL: all RB rows and both
 // columns exist (no per-row tests).  SHUF: the 4 input channels are gathered
 // one by one at byte offsets choff[] within the pixel (channel shuffle).
 template <int ST, int ACT, bool RES, bool FULL, bool SHUF = false>
-__device__ __forceinline__ void dw_item(uint32_t src, uint32_t col_b, const f32x2 (&wf)[9][2],
-                                        const f32x2 (&bz)[2], __nv_bfloat16* y0,
-                                        const __nv_bfloat16* r0, size_t y_row, int C, int nrows,
-                                        bool two, const uint32_t (&choff)[4]) {
+__device__ __forceinline__ void dw_item(uint32_t src, uint32_t col_b,
+                                        const unsigned short (&wh)[9][4], const float (&bz)[4],
+                                        __nv_bfloat16* y0, const __nv_bfloat16* r0, size_t y_row,
+                                        int C, int nrows, bool two, const uint32_t (&choff)[4]) {
   using Cf = DwCfg<ST>;
   constexpr int NC = ST + 3;  // distinct input columns the two outputs read
   uint32_t sc[NC];            // shared address of input column cc of the pair, row 0
@@ -152,46 +162,44 @@ __device__ __forceinline__ void dw_item(uint32_t src, uint32_t col_b, const f32x
   for (int cc = 0; cc < NC; ++cc) sc[cc] = src + cc * col_b;
   __nv_bfloat16* y1 = y0 + C;
   const __nv_bfloat16* r1 = RES ? r0 + C : nullptr;
-  f32x2 acc[3][2][2];  // [slot][output column][channel pair]
+  float acc[3][2][4];  // [slot][output column][channel]
 #pragma unroll
   for (int rho = 0; rho < Cf::IH; ++rho) {
-    f32x2 xin[NC][2];
+    unsigned short xh[NC][4];  // bf16 inputs of this row: [column][channel]
 #pragma unroll
     for (int cc = 0; cc < NC; ++cc) {
       if constexpr (SHUF) {
-        uint32_t u[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           asm volatile("ld.shared.u16 %0, [%1];"
-                       : "=r"(u[q])
+                       : "=h"(xh[cc][q])
                        : "r"(sc[cc] + rho * Cf::ROWP + choff[q]));
-        xin[cc][0] = f2_pack(__uint_as_float(u[0] << 16), __uint_as_float(u[1] << 16));
-        xin[cc][1] = f2_pack(__uint_as_float(u[2] << 16), __uint_as_float(u[3] << 16));
       } else {
         const uint2 v = lds64(sc[cc] + rho * Cf::ROWP);
-        xin[cc][0] = bf16x2_to_f2(v.x);
-        xin[cc][1] = bf16x2_to_f2(v.y);
+        halves(v.x, xh[cc][0], xh[cc][1]);
+        halves(v.y, xh[cc][2], xh[cc][3]);
       }
     }
 #pragma unroll
     for (int i = 0; i < 3; ++i) {
       if (rho < i || (rho - i) % ST != 0 || (rho - i) / ST >= Cf::RB) continue;
-      f32x2(&a)[2][2] = acc[((rho - i) / ST) % 3];
+      float(&a)[2][4] = acc[((rho - i) / ST) % 3];
 #pragma unroll
       for (int s = 0; s < 3; ++s)
 #pragma unroll
         for (int o = 0; o < 2; ++o)
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-            a[o][h] = f2_fma(xin[o * ST + s][h], wf[i * 3 + s][h],
-                             (i == 0 && s == 0) ? bz[h] : a[o][h]);
+          for (int q = 0; q < 4; ++q)
+            a[o][q] = fma_bf16(xh[o * ST + s][q], wh[i * 3 + s][q],
+                               (i == 0 && s == 0) ? bz[q] : a[o][q]);
     }
     if (rho < 2 || (rho - 2) % ST != 0 || (rho - 2) / ST >= Cf::RB) continue;
     const int orow = (rho - 2) / ST;
-    const f32x2(&a)[2][2] = acc[orow % 3];
+    const float(&a)[2][4] = acc[orow % 3];
     if (FULL || orow < nrows) {
-      store4<ACT, RES>(a[0][0], a[0][1], y0, r0);
-      if (FULL || two) store4<ACT, RES>(a[1][0], a[1][1], y1, r1);
+      store4<ACT, RES>(f2_pack(a[0][0], a[0][1]), f2_pack(a[0][2], a[0][3]), y0, r0);
+      if (FULL || two)
+        store4<ACT, RES>(f2_pack(a[1][0], a[1][1]), f2_pack(a[1][2], a[1][3]), y1, r1);
     }
     y0 += y_row;
     y1 += y_row;
@@ -204,7 +212,7 @@ __device__ __forceinline__ void dw_item(uint32_t src, uint32_t col_b, const f32x
 
 // Persistent CTAs walk the block list; see the file comment.
 template <int ST, int ACT, bool RES, bool SHUF = false>
-__global__ void __launch_bounds__(MAX_THREADS, 1)
+__global__ void __launch_bounds__(MAX_THREADS, CTAS_PER_SM)
     dwconv3x3_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const DwParams p,
                          const __nv_bfloat16* __restrict__ w9c, const float* __restrict__ bias,
                          const __nv_bfloat16* __restrict__ res, __nv_bfloat16* __restrict__ y) {
@@ -294,8 +302,8 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
   const int npairs = (p.owt + 1) / 2;
   const int g_first = threadIdx.x % groups, jp_first = threadIdx.x / groups;
   const int g_step = blockDim.x % groups, jp_step = blockDim.x / groups;
-  f32x2 wf[9][2];  // this thread's weights (kept while its channels are unchanged)
-  f32x2 bz[2];
+  unsigned short wf[9][4];  // this thread's bf16 weights [tap][channel] (kept while its
+  float bz[4];              // channels are unchanged) and fp32 bias
   int w_c = -1;
   const uint32_t col_b = (uint32_t)p.cb * 2;  // bytes between input columns in a row slot
   const size_t y_row = (size_t)p.OW * p.C;    // elements between output rows
@@ -329,14 +337,13 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
 #pragma unroll
           for (int k = 0; k < 9; ++k) {
             const uint2 v = __ldg(reinterpret_cast<const uint2*>(w9c + (size_t)k * p.C + c));
-            wf[k][0] = bf16x2_to_f2(v.x);
-            wf[k][1] = bf16x2_to_f2(v.y);
+            halves(v.x, wf[k][0], wf[k][1]);
+            halves(v.y, wf[k][2], wf[k][3]);
           }
           if (bias) {  // scalar loads: the caller's bias need not be 16-byte aligned
-            bz[0] = f2_pack(__ldg(bias + c), __ldg(bias + c + 1));
-            bz[1] = f2_pack(__ldg(bias + c + 2), __ldg(bias + c + 3));
+            for (int q = 0; q < 4; ++q) bz[q] = __ldg(bias + c + q);
           } else {
-            bz[0] = bz[1] = f2_pack(0.f, 0.f);
+            for (int q = 0; q < 4; ++q) bz[q] = 0.f;
           }
           w_c = c;
         }
@@ -439,7 +446,7 @@ cudaError_t launch_st(const gbconv_desc_s& d, const void* x, const void* w, cons
   if (gb_encode_tiled(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims,
                       strides, box, estr, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  const long long grid = std::min<long long>(p.nblocks, gb_num_sms());
+  const long long grid = std::min<long long>(p.nblocks, (long long)CTAS_PER_SM * gb_num_sms());
   // threads: the block's work items split into equal rounds of <= MAX_THREADS
   const int items = gb_items(p);
   const int rounds = gb_ceil_div(items, MAX_THREADS);
