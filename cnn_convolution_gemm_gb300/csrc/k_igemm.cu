@@ -417,8 +417,8 @@ __global__ void __launch_bounds__(192, 1)
         // unused) staging box and read back as broadcasts
         int32_t* sbi = reinterpret_cast<int32_t*>(sEpi + q * 2 * C::EPI_BOX);
         float* ssc = reinterpret_cast<float*>(sbi + 64);
-        for (int g = 0; g < BN / 128; ++g) {
-          const int k0 = (nt * BN + g * 128) / 2;  // first output channel of the group
+        for (int g = 0; g < width / 128; ++g) {
+          const int k0 = (nt * BN + noff + g * 128) / 2;  // first output channel of the group
           if (k0 >= p.i8_kout) break;
           __syncwarp();  // the previous group's reads of the slice are done
 #pragma unroll
@@ -730,7 +730,8 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   const int grid = tiles < slots ? tiles : slots;
   // a last wave that would leave most SMs idle runs as half-width units
   p.tail_start = tiles;
-  if (BN == 256 && p.ksplit == 1 && !LIGHT && !p.i8_y && tiles > grid) {
+  // (a half-width unit of the exact int8 path is one whole 128-column lo/hi group)
+  if (BN == 256 && p.ksplit == 1 && !LIGHT && tiles > grid) {
     const int rem = tiles % grid;
     if (rem > 0 && rem <= grid / 2) p.tail_start = tiles - rem;
   }

@@ -36,12 +36,14 @@ constexpr int KCHUNK_MAX = 16;  // k-steps of 64 products per exact fp32 chunk
 constexpr int SPLITW_MAX = 8704;  // products per output that stay exact with split weights
 
 // the split-weight path applies (see the file comment) and its unsplit tile
-// grid fills the SMs; smaller grids keep split-K, which spreads the reduction
+// grid fills at least half the SMs; smaller grids keep split-K, which spreads the
+// reduction (measured on the ResNet-50 stage shapes at batch 32: 256@14 with 98
+// tiles runs faster split-weight, 512@7 with 52 tiles faster split-K)
 bool split_weights(const gbconv_desc_s& d) {
   if (d.K % 64 || (long long)d.R * d.S * (gb_ceil_div(d.C, 64) * 64) > SPLITW_MAX) return false;
   const long long m_tiles = gb_ceil_div_ll((long long)d.N * d.OH * d.OW, 128);
   const int n_tiles = d.K == 64 ? 1 : 2 * d.K / 256;
-  return m_tiles * n_tiles >= gb_num_sms();
+  return 2 * m_tiles * n_tiles >= gb_num_sms();
 }
 
 // bf16 has 8 significant bits: every int8 value converts exactly.  Output NHWC

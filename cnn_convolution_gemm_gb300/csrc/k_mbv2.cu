@@ -20,8 +20,8 @@
 //   3. each thread reads one halo pixel's E accumulators back, applies ReLU6
 //      and stores bf16 to shared memory;
 //   4. the depthwise 3x3 runs on CUDA cores (a thread owns 4 channels x 2
-//      columns x 14 rows; each t1 value is converted once and added into up to
-//      three output rows with fma.rn.f32x2) and writes ReLU6(.) as bf16
+//      columns x 14 rows; each t1 value is loaded once and added into up to
+//      three output rows with fma.rn.f32.bf16) and writes ReLU6(.) as bf16
 //      straight into the project GEMM's A-operand layout;
 //   5. the project is M=128 MMAs over K = E (N = C_out padded to 32), then bias,
 //      the optional residual and a bf16 store of the 14x14 x C_out tile.
@@ -78,23 +78,16 @@ struct Mbv2Params {
   unsigned long long wait_ns;
 };
 
-typedef unsigned long long f32x2;  // two fp32 in a 64-bit register pair
-
-__device__ __forceinline__ f32x2 f2_pack(float lo, float hi) {
-  f32x2 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void f2_unpack(f32x2 v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
-  f32x2 d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+// a * b + c for bf16 a, b (bit patterns) and fp32 c: the product of two bf16
+// values is exact in fp32, so this is the fp32 FMA of the widened operands
+__device__ __forceinline__ float fma_bf16(unsigned short a, unsigned short b, float c) {
+  float d;
+  asm("fma.rn.f32.bf16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
   return d;
 }
-__device__ __forceinline__ f32x2 bf16x2_to_f2(uint32_t u) {
-  return f2_pack(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+// the two bf16 halves of a packed word (lo: the element at the lower address)
+__device__ __forceinline__ void halves(uint32_t u, unsigned short& lo, unsigned short& hi) {
+  asm("mov.b32 {%0, %1}, %2;" : "=h"(lo), "=h"(hi) : "r"(u));
 }
 // two fp32 -> bf16x2 (round to nearest even), lo in the low half
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -129,51 +122,50 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
 
 // Depthwise 3x3 + bias + ReLU6 for one work item: channels 4g..4g+3 of output
 // columns 2jp, 2jp+1, all 14 rows of the tile.  Input row rho of the halo feeds
-// output row rho - i through filter row i; each t1 value is converted once and
-// added into the accumulators of the (up to three) output rows it reaches;
+// output row rho - i through filter row i; each t1 value is loaded once and
+// added (fma.rn.f32.bf16 on the packed words: no widening instructions) into
+// the accumulators of the (up to three) output rows it reaches;
 // output row o lives in slot o % 3 and is stored once row o + 2 has been added.
 // The result goes to t2 in the project GEMM's K-major core-matrix layout:
 // channel chunk c/8 at chunk * T2_CHUNK, pixel m at m * 16, (c % 8) * 2 within.
 template <int E>
 __device__ __forceinline__ void dw_tile(uint32_t t1, uint32_t t2, int g, int jp,
-                                        const f32x2 (&wf)[9][2], const f32x2 (&bz)[2]) {
+                                        const unsigned short (&wf)[9][4],
+                                        const float (&bz)[4]) {
   using C = Cfg<E>;
   const uint32_t src = t1 + (uint32_t)(2 * jp) * C::T1_PITCH + (uint32_t)g * 8;
   const uint32_t dst = t2 + (uint32_t)(g >> 1) * C::T2_CHUNK + (uint32_t)(g & 1) * 8 +
                        (uint32_t)(2 * jp) * 16;
-  f32x2 acc[3][2][2];  // [slot][output column][channel pair]
+  float acc[3][2][4];  // [slot][output column][channel]
 #pragma unroll
   for (int rho = 0; rho < HS; ++rho) {
-    f32x2 xin[4][2];
+    unsigned short xh[4][4];  // bf16 t1 values of this row: [column][channel]
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc) {
       const uint2 v = lds64(src + rho * (HS * C::T1_PITCH) + cc * C::T1_PITCH);
-      xin[cc][0] = bf16x2_to_f2(v.x);
-      xin[cc][1] = bf16x2_to_f2(v.y);
+      halves(v.x, xh[cc][0], xh[cc][1]);
+      halves(v.y, xh[cc][2], xh[cc][3]);
     }
 #pragma unroll
     for (int i = 0; i < 3; ++i) {
       if (rho < i || rho - i >= TS) continue;
-      f32x2(&a)[2][2] = acc[(rho - i) % 3];
+      float(&a)[2][4] = acc[(rho - i) % 3];
 #pragma unroll
       for (int s = 0; s < 3; ++s)
 #pragma unroll
         for (int o = 0; o < 2; ++o)
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-            a[o][h] = f2_fma(xin[o + s][h], wf[i * 3 + s][h],
-                             (i == 0 && s == 0) ? bz[h] : a[o][h]);
+          for (int q = 0; q < 4; ++q)
+            a[o][q] = fma_bf16(xh[o + s][q], wf[i * 3 + s][q],
+                               (i == 0 && s == 0) ? bz[q] : a[o][q]);
     }
     if (rho < 2) continue;
     const int orow = rho - 2;
-    const f32x2(&a)[2][2] = acc[orow % 3];
+    const float(&a)[2][4] = acc[orow % 3];
 #pragma unroll
-    for (int o = 0; o < 2; ++o) {
-      float v0, v1, v2, v3;
-      f2_unpack(a[o][0], v0, v1);
-      f2_unpack(a[o][1], v2, v3);
-      sts64(dst + (uint32_t)(orow * TS + o) * 16, relu6_bf16(v0, v1), relu6_bf16(v2, v3));
-    }
+    for (int o = 0; o < 2; ++o)
+      sts64(dst + (uint32_t)(orow * TS + o) * 16, relu6_bf16(a[o][0], a[o][1]),
+            relu6_bf16(a[o][2], a[o][3]));
   }
 }
 
@@ -226,19 +218,19 @@ __global__ void __launch_bounds__(THREADS, 1)
   // this thread's depthwise item and its weights (fixed for the whole launch)
   const int dg = tid % (E / 4), djp = tid / (E / 4);
   const bool dw_item = tid < C::ITEMS;
-  f32x2 wf[9][2], bz[2];
+  unsigned short wf[9][4];  // bf16 weights [tap][channel]
+  float bz[4];
   if (dw_item) {
     const __nv_bfloat16* wd =
         reinterpret_cast<const __nv_bfloat16*>(wpack + C::WE_BYTES + C::WP_BYTES);
 #pragma unroll
     for (int k = 0; k < 9; ++k) {
       const uint2 v = __ldg(reinterpret_cast<const uint2*>(wd + k * E + dg * 4));
-      wf[k][0] = bf16x2_to_f2(v.x);
-      wf[k][1] = bf16x2_to_f2(v.y);
+      halves(v.x, wf[k][0], wf[k][1]);
+      halves(v.y, wf[k][2], wf[k][3]);
     }
     const int c = dg * 4;
-    bz[0] = b_dw ? f2_pack(__ldg(b_dw + c), __ldg(b_dw + c + 1)) : f2_pack(0.f, 0.f);
-    bz[1] = b_dw ? f2_pack(__ldg(b_dw + c + 2), __ldg(b_dw + c + 3)) : f2_pack(0.f, 0.f);
+    for (int q = 0; q < 4; ++q) bz[q] = b_dw ? __ldg(b_dw + c + q) : 0.f;
   }
   gb::fence_proxy_async_smem();  // generic writes (weights, zeros) before async-proxy use
   gb::tc_fence_before();

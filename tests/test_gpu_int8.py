@@ -83,16 +83,20 @@ def test_int8_saturation_extremes(algo):
     assert (ref == 127).any() and (ref == -128).any()
 
 
-def test_int8_split_weight_bound_extremes():
-    """The split-weight path at its largest exact sums: x = -128 everywhere and
-    w alternating 127 / -128 over C = 512 (4608 products per output), so the
+@pytest.mark.parametrize("N", [2, 200])
+def test_int8_split_weight_bound_extremes(N):
+    """The largest exact sums: x = -128 everywhere and w alternating 127 / -128
+    over C = 512 (4608 products per output), so on the split-weight path the
     low-nibble sums reach -128 * 15 * 4608 and the high-part sums -128 * 7 * 4608
-    (and +128 * 8 * 4608 for w = -128); requant into saturation both ways."""
+    (and +128 * 8 * 4608 for w = -128); requant into saturation both ways.
+    N = 200 (77 tiles of 128 pixels) takes the split-weight path, N = 2 (one
+    tile) the chunked split-K path; every image is the same, so the oracle
+    computes one and each image is compared with it."""
     torch = need_gpu()
     from cnn_convolution_gemm_gb300 import binding as B
     from cnn_convolution_gemm_gb300.layer import ConvLayer
     dev = torch.device("cuda:0")
-    N, C, H, K = 2, 512, 7, 64
+    C, H, K = 512, 7, 64
     x = np.full((N, H, H, C), -128, np.int8)
     w = np.where(np.arange(K)[:, None, None, None] % 2 == 0, 127, -128).astype(np.int8) * np.ones(
         (K, 3, 3, C), np.int8)
@@ -100,11 +104,18 @@ def test_int8_split_weight_bound_extremes():
     layer = ConvLayer(N, C, H, H, K, 3, 3, 1, 1, dtype=B.CONV_INT8,
                       scale=torch.from_numpy(scale).to(dev))
     layer.prepack(torch.from_numpy(w).to(dev), INT8_TC)
+    # the split-weight path needs no fp32 partials: its workspace is the bf16 copy alone
+    bf16_copy = (N * H * H * C * 2 + 255) // 256 * 256
+    split_weight = B.conv_workspace_size(layer.desc, INT8_TC) == bf16_copy
+    assert split_weight == (N == 200)
     y = layer(torch.from_numpy(x).to(dev))
     B.conv_sync_status(torch.cuda.current_stream().cuda_stream)
-    ref = ol.conv2d_i8(nhwc_to_nchw(x), nhwc_to_nchw(w), None, scale, pad=1, relu=False)
-    assert np.array_equal(y.cpu().numpy(), nchw_to_nhwc(ref))
-    assert (nchw_to_nhwc(ref) == -128).any() and (nchw_to_nhwc(ref) == 127).any()
+    ref = nchw_to_nhwc(ol.conv2d_i8(nhwc_to_nchw(x[:1]), nhwc_to_nchw(w), None, scale, pad=1,
+                                    relu=False))
+    yn = y.cpu().numpy()
+    for n in range(N):
+        assert np.array_equal(yn[n:n + 1], ref), n
+    assert (ref == -128).any() and (ref == 127).any()
 
 
 def _to_nc32(a_nchw):
@@ -135,7 +146,7 @@ def test_nc32hw32_conversion_roundtrip():
 
 
 @pytest.mark.parametrize("case", [
-    # N, C, H, W, K, algo — tcgen05 split-weight path (grid >= SMs), its split-K
+    # N, C, H, W, K, algo — tcgen05 split-weight path (grid >= half the SMs), its split-K
     # fallback (K not a multiple of 64), and the direct kernel
     (32, 64, 28, 28, 64, INT8_TC),
     (2, 64, 14, 14, 96, INT8_TC),
