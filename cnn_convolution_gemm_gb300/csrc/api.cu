@@ -240,7 +240,7 @@ static const char* const kAlgoNames[CONV_ALGO_COUNT] = {
     "direct", "igemm_tc_n64", "igemm_tc_n128", "igemm_tc_n256",
     "winograd_f2x2_3x3", "winograd_f6x6_3x3", "depthwise3x3", "int8_igemm_mma",
     "int8_igemm_tc", "im2col_gemm", "stem_s2d_igemm", "igemm_tf32",
-    "int8_winograd_f2x2_3x3"};
+    "int8_winograd_f2x2_3x3", "stem_s2d4_igemm"};
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -317,6 +317,9 @@ static bool applicable(const gbconv_desc_s& d, int algo, const char** why) {
     case CONV_ALGO_STEM_S2D:
       if (d.dtype != CONV_BF16 || !nhwc) return *why = "needs bf16 NHWC", false;
       return stem_s2d_applicable(d, why);
+    case CONV_ALGO_STEM_S2D4:
+      if (d.dtype != CONV_BF16 || !nhwc) return *why = "needs bf16 NHWC", false;
+      return stem_s2d4_applicable(d, why);
     case CONV_ALGO_INT8_WINO_F2:
       if (d.dtype != CONV_INT8 || !nhwc) return *why = "needs int8 NHWC", false;
       if (!d.scale) return *why = "int8 needs a requant scale", false;
@@ -367,6 +370,9 @@ static int heuristic(const gbconv_desc_s& d) {
   }
   if (implemented(CONV_ALGO_DEPTHWISE) && applicable(d, CONV_ALGO_DEPTHWISE, nullptr))
     return CONV_ALGO_DEPTHWISE;
+  // narrow stride-2 stems: the space-to-depth rewrites
+  for (int a : {CONV_ALGO_STEM_S2D4, CONV_ALGO_STEM_S2D})
+    if (implemented(a) && applicable(d, a, nullptr)) return a;
   if (d.dtype == CONV_F32)
     return implemented(CONV_ALGO_IGEMM_TF32) && applicable(d, CONV_ALGO_IGEMM_TF32, nullptr)
                ? CONV_ALGO_IGEMM_TF32
@@ -442,6 +448,7 @@ extern "C" conv_status_t conv_workspace_size(conv_desc_t d, conv_algo_t algo, si
   if (a == CONV_ALGO_INT8_TC) *bytes = int8_tc_workspace_bytes(*d);
   if (a == CONV_ALGO_IM2COL_GEMM) *bytes = im2col_workspace_bytes(*d);
   if (a == CONV_ALGO_STEM_S2D) *bytes = stem_s2d_workspace_bytes(*d);
+  if (a == CONV_ALGO_STEM_S2D4) *bytes = stem_s2d4_workspace_bytes(*d);
   if (a == CONV_ALGO_INT8_WINO_F2) *bytes = int8_wino_workspace_bytes(*d);
   return ok_status();
 }
@@ -482,6 +489,7 @@ extern "C" conv_status_t conv_weights_packed_size(conv_desc_t d, conv_algo_t alg
     case CONV_ALGO_INT8_TC: *bytes = int8_tc_packed_bytes(*d); break;
     case CONV_ALGO_IM2COL_GEMM: *bytes = im2col_packed_bytes(*d); break;
     case CONV_ALGO_STEM_S2D: *bytes = stem_s2d_packed_bytes(*d); break;
+    case CONV_ALGO_STEM_S2D4: *bytes = stem_s2d4_packed_bytes(*d); break;
     case CONV_ALGO_IGEMM_TF32: *bytes = igemm_tf32_packed_bytes(*d); break;
     case CONV_ALGO_INT8_WINO_F2: *bytes = int8_wino_packed_bytes(*d); break;
     case CONV_ALGO_WINO_F2: *bytes = winograd_packed_bytes(*d, 2); break;
@@ -515,6 +523,7 @@ extern "C" conv_status_t conv_weights_prepack(conv_desc_t d, conv_algo_t algo, c
     case CONV_ALGO_INT8_TC: e = launch_pack_int8_tc_weights(*d, w, wpack, s); break;
     case CONV_ALGO_IM2COL_GEMM: e = launch_pack_im2col_weights(*d, w, wpack, s); break;
     case CONV_ALGO_STEM_S2D: e = launch_pack_stem_weights(*d, w, wpack, s); break;
+    case CONV_ALGO_STEM_S2D4: e = launch_pack_stem4_weights(*d, w, wpack, s); break;
     case CONV_ALGO_IGEMM_TF32: e = launch_pack_tf32_weights(*d, w, wpack, s); break;
     case CONV_ALGO_INT8_WINO_F2: e = launch_pack_int8_wino(*d, w, wpack, s); break;
     case CONV_ALGO_DEPTHWISE: e = launch_pack_dw_weights(*d, w, wpack, s); break;
@@ -591,6 +600,15 @@ static conv_status_t fwd_impl(const gbconv_desc_s& d, const void* x, const void*
         return gb_fail(CONV_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
       e = launch_stem_s2d(d, x, wpack, static_cast<const float*>(bias), res, y, ws, err, wait_ns,
                           s);
+      break;
+    }
+    case CONV_ALGO_STEM_S2D4: {
+      const size_t need = stem_s2d4_workspace_bytes(d);
+      if (!ws || ws_bytes < need)
+        return gb_fail(CONV_ERR_WORKSPACE, "workspace of %zu bytes needed", need);
+      if (reinterpret_cast<uintptr_t>(ws) & 255u)
+        return gb_fail(CONV_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+      e = launch_stem_s2d4(d, x, wpack, static_cast<const float*>(bias), y, ws, err, wait_ns, s);
       break;
     }
     case CONV_ALGO_INT8_TC: {
@@ -1020,6 +1038,7 @@ static bool implemented(int algo) {
     case CONV_ALGO_INT8_TC:
     case CONV_ALGO_IM2COL_GEMM:
     case CONV_ALGO_STEM_S2D:
+    case CONV_ALGO_STEM_S2D4:
     case CONV_ALGO_IGEMM_TF32:
     case CONV_ALGO_INT8_WINO_F2:
       return true;

@@ -82,6 +82,11 @@ struct IgemmSplit {
   int i8_kout = 0;
   int i8_relu = 0;
   int i8_nc32 = 0;  // int8 output in NC32HW32 (else NHWC)
+  // space-to-depth-by-4 stem: the GEMM runs over the 4x4-block grid and its
+  // 4K columns are (py, px, k) of the 2x2 output pixels of each block; the
+  // epilogue writes them to the stride-2 conv's NHWC output [N][2BH][2BW][K]
+  // (s2d4_k = K; 0: off)
+  int s2d4_k = 0;
 };
 int igemm_kiters(const gbconv_desc_s& d);
 cudaError_t launch_igemm_bf16(const gbconv_desc_s& d, int block_n, const void* x,
@@ -166,6 +171,14 @@ cudaError_t launch_mbv2_block(int N, int H, int W, int cin, int E, int cout, con
 
 // Stride-2 convolutions over 8 channels as space-to-depth (32 channels) + a
 // stride-1 implicit GEMM with asymmetric padding; workspace = the rewritten input.
+bool stem_s2d4_applicable(const gbconv_desc_s& d, const char** why);
+size_t stem_s2d4_workspace_bytes(const gbconv_desc_s& d);
+size_t stem_s2d4_packed_bytes(const gbconv_desc_s& d);
+cudaError_t launch_pack_stem4_weights(const gbconv_desc_s& d, const void* w, void* wpack,
+                                      cudaStream_t st);
+cudaError_t launch_stem_s2d4(const gbconv_desc_s& d, const void* x, const void* wpack,
+                             const float* bias, void* y, void* ws, int* err,
+                             unsigned long long wait_ns, cudaStream_t st);
 bool stem_s2d_applicable(const gbconv_desc_s& d, const char** why);
 size_t stem_s2d_workspace_bytes(const gbconv_desc_s& d);
 size_t stem_s2d_packed_bytes(const gbconv_desc_s& d);

@@ -73,6 +73,10 @@ struct IgemmParams {
   int i8_kout, i8_relu, i8_nc32;
   // tf32 mode: fp32 residual [M][K] (the fp32 output goes through tm_y)
   const float* res_f32;
+  // space-to-depth-by-4 stem output (see IgemmSplit): column c of the GEMM is
+  // channel c % s2d4_k of output pixel (2 bh + py, 2 bw + px), (py, px) = the
+  // bits of c / s2d4_k; stored through the 5-D map in the tm_y slot
+  int s2d4_k;
 };
 
 enum { MODE_CONV = 0, MODE_BATCHED = 1 };
@@ -527,8 +531,9 @@ __global__ void __launch_bounds__(192, 1)
           float* sbias = reinterpret_cast<float*>(sEpi + 4 * 2 * C::EPI_BOX + q * 256);
           {
             const int nc = nb0 + 2 * lane;
+            const int bc = p.s2d4_k ? nc % p.s2d4_k : nc;  // (s2d4: bias of channel c % K)
             float2 bv = make_float2(0.f, 0.f);
-            if (p.bias && nc < p.K) bv = make_float2(__ldg(p.bias + nc), __ldg(p.bias + nc + 1));
+            if (p.bias && nc < p.K) bv = make_float2(__ldg(p.bias + bc), __ldg(p.bias + bc + 1));
             reinterpret_cast<float2*>(sbias)[lane] = bv;
           }
           __syncwarp();
@@ -572,7 +577,22 @@ __global__ void __launch_bounds__(192, 1)
           gb::fence_proxy_async_smem();  // staging writes -> visible to the TMA engine
           __syncwarp();
           if (lane == 0) {
-            gb::tma_store_2d(&tm_y, box, nb0, (int)m_warp);
+            if (p.s2d4_k) {
+              // rows are 4x4 blocks (n, bh, bw), bw fastest; 8-row pieces of the
+              // box (8 divides the block-grid width, so a piece stays in one block
+              // row and starts on a swizzle-atom boundary) go to output pixels
+              // (2 bh + py, 2 bw + px) for bw = bw0 .. bw0 + 7
+              const int g = nb0 / p.s2d4_k;
+#pragma unroll 1
+              for (int r8 = 0; r8 < 4; ++r8) {
+                const long long row = m_warp + r8 * 8;
+                if (row >= p.M) break;
+                gb::tma_store_5d(&tm_y, box + r8 * 1024, 0, g & 1, (int)(row % p.OW), g >> 1,
+                                 (int)(row / p.OW));
+              }
+            } else {
+              gb::tma_store_2d(&tm_y, box, nb0, (int)m_warp);
+            }
             gb::bulk_commit();
           }
           ++epi_count;
@@ -665,6 +685,10 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   p.i8_nc32 = split.i8_nc32;
   if (p.i8_y && (BN % 128 != 0 || p.ksplit != 1 || p.i8_kout * 2 != d.K || p.i8_kout % 16))
     return cudaErrorInvalidValue;
+  p.s2d4_k = split.s2d4_k;
+  if (p.s2d4_k && (TF32 || res || p.i8_y || p.ksplit != 1 || p.s2d4_k != 64 ||
+                   d.K != 4 * p.s2d4_k || d.OW % 8))
+    return cudaErrorInvalidValue;
 
   CUtensorMap tmx, tmw;
   {
@@ -699,9 +723,23 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
     cuuint64_t strides[1] = {(cuuint64_t)(d.y_kstride ? d.y_kstride : d.K) * ES};
     cuuint32_t box[2] = {TF32 ? 32u : 64u, 32};
     cuuint32_t estr[2] = {1, 1};
-    if (gb_encode_tiled(&tmy, DT, 2, y, dims, strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B) !=
-        CUDA_SUCCESS)
+    if (p.s2d4_k) {
+      // the stride-2 conv's NHWC output [N][2 OH][2 OW][k] seen as
+      // (k, px, bw, py, (n, bh)): pixel (2 bh + py, 2 bw + px); 8-row boxes
+      const cuuint64_t kb = (cuuint64_t)p.s2d4_k * 2;  // bytes per output pixel
+      cuuint64_t dims5[5] = {(cuuint64_t)p.s2d4_k, 2, (cuuint64_t)d.OW, 2,
+                             (cuuint64_t)d.N * d.OH};
+      cuuint64_t strides5[4] = {kb, 2 * kb, 2 * (cuuint64_t)d.OW * kb,
+                                4 * (cuuint64_t)d.OW * kb};
+      cuuint32_t box5[5] = {64, 1, 8, 1, 1};
+      cuuint32_t estr5[5] = {1, 1, 1, 1, 1};
+      if (gb_encode_tiled(&tmy, DT, 5, y, dims5, strides5, box5, estr5,
+                          CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    } else if (gb_encode_tiled(&tmy, DT, 2, y, dims, strides, box, estr,
+                               CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS) {
       return cudaErrorInvalidValue;
+    }
   }
   CUtensorMap tmr = tmy;  // residual (same shape and boxes as the output), or the
                           // fp32 partial-sum map in split-K mode

@@ -29,7 +29,7 @@ from .layer import ConvLayer, current_stream_handle
 from .workload import ConvShape
 
 STAGES = [(3, 64, 256, 1), (4, 128, 512, 2), (6, 256, 1024, 2), (3, 512, 2048, 2)]
-STEM_CHANNELS = 8  # 3 input channels padded to 8
+STEM_CHANNELS = 4  # 3 input channels padded to 4
 
 
 @dataclass

@@ -86,7 +86,11 @@ typedef int conv_algo_t;
 #define CONV_ALGO_INT8_WINO_F2 12  /* int8 Winograd F(2x2,3x3) with float intermediates
                                       ([Beta]), exact: integer transforms, split filter
                                       transform, fp32 sums below 2^24 (C <= 896; workspace) */
-#define CONV_ALGO_COUNT 13
+#define CONV_ALGO_STEM_S2D4 13     /* stride-2 conv over 4 or 8 channels as a 4x4
+                                      space-to-depth + implicit GEMM whose columns are
+                                      the 2x2 output pixels of each block (K == 64;
+                                      workspace)                                         */
+#define CONV_ALGO_COUNT 14
 
 /* ---- descriptor --------------------------------------------------------- */
 

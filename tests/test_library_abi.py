@@ -72,7 +72,22 @@ def test_algo_table_and_applicability(B):
     assert not B.conv_algo_info(d, B.CONV_ALGO_STEM_S2D)[2]  # C = 256, stride 1
     odd = B.conv_desc_create(1, 8, 15, 16, 64, 7, 7, 2, 3, 1, 1, B.CONV_BF16)
     assert not B.conv_algo_info(odd, B.CONV_ALGO_STEM_S2D)[2]  # odd height
-    for h in (d, dw, e24, stem, odd):
+    # the space-to-depth-by-4 stem: 4 (or 8) channels, W % 32 == 0, K == 64;
+    # 7x7 / 2 is a 3x3 conv over 4x4 blocks of 64 channels with 256 columns
+    stem4 = B.conv_desc_create(64, 4, 224, 224, 64, 7, 7, 2, 3, 1, 1, B.CONV_BF16)
+    assert B.conv_algo_info(stem4, B.CONV_ALGO_STEM_S2D4)[1:] == ("stem_s2d4_igemm", 1)
+    assert B.conv_weights_packed_size(stem4, B.CONV_ALGO_STEM_S2D4) == 256 * 9 * 64 * 2
+    assert B.conv_workspace_size(stem4, B.CONV_ALGO_STEM_S2D4) == 64 * 56 * 56 * 64 * 2
+    assert not B.conv_algo_info(stem4, B.CONV_ALGO_STEM_S2D)[2]  # C = 4
+    assert not B.conv_algo_info(stem4, B.CONV_ALGO_IGEMM_N64)[2]  # C % 8
+    assert B.conv_algo_resolve(stem4) == B.CONV_ALGO_STEM_S2D4
+    assert B.conv_algo_info(stem, B.CONV_ALGO_STEM_S2D4)[2]  # 8 channels: 128 per block
+    assert B.conv_weights_packed_size(stem, B.CONV_ALGO_STEM_S2D4) == 256 * 9 * 128 * 2
+    narrow_w = B.conv_desc_create(2, 4, 32, 48, 64, 7, 7, 2, 3, 1, 1, B.CONV_BF16)
+    assert not B.conv_algo_info(narrow_w, B.CONV_ALGO_STEM_S2D4)[2]  # W % 32
+    k32 = B.conv_desc_create(2, 4, 32, 32, 32, 7, 7, 2, 3, 1, 1, B.CONV_BF16)
+    assert not B.conv_algo_info(k32, B.CONV_ALGO_STEM_S2D4)[2]  # K != 64
+    for h in (d, dw, e24, stem, odd, stem4, narrow_w, k32):
         B.conv_desc_destroy(h)
 
 
