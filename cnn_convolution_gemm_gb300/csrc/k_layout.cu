@@ -16,25 +16,36 @@ int grid_for(long long work) {
   return (int)std::min<long long>(gb_ceil_div_ll(work, kBlock), 148LL * 32);
 }
 
-// One thread per output pixel (n, h, w): reads C strided values (coalesced
-// across the warp along w) and writes C_out contiguous bf16 values.
+// One thread per output pixel: blockIdx.y walks the image rows (n, h), the
+// threads of a block the columns w, so no index needs a division.  A thread
+// reads C strided values (coalesced across the warp along w) and writes C_out
+// contiguous bf16 values (one 8-byte store when C_out == 4).
 __global__ void nchw_f32_to_nhwc_bf16_kernel(const float* __restrict__ x,
                                              __nv_bfloat16* __restrict__ y, int N, int C, int H,
                                              int W, int C_out) {
-  const long long pixels = (long long)N * H * W;
+  const int w = blockIdx.x * blockDim.x + threadIdx.x;
+  if (w >= W) return;
   const long long hw = (long long)H * W;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < pixels;
-       i += (long long)gridDim.x * blockDim.x) {
-    const long long n = i / hw, p = i % hw;
-    const float* src = x + n * C * hw + p;
-    __nv_bfloat16* dst = y + i * C_out;
+  for (int nh = blockIdx.y; nh < N * H; nh += gridDim.y) {
+    const int n = nh / H, h = nh - n * H;
+    const float* src = x + (long long)n * C * hw + (long long)h * W + w;
+    __nv_bfloat16* dst = y + ((long long)nh * W + w) * C_out;
+    if (C_out == 4) {
+      float v[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) v[c] = c < C ? __ldg(src + c * hw) : 0.f;
+      __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]), hi = __floats2bfloat162_rn(v[2], v[3]);
+      *reinterpret_cast<uint2*>(dst) =
+          make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+      continue;
+    }
     int c = 0;
     for (; c + 1 < C_out; c += 2) {
-      const float a = c < C ? src[(long long)c * hw] : 0.f;
-      const float b = c + 1 < C ? src[(long long)(c + 1) * hw] : 0.f;
+      const float a = c < C ? __ldg(src + c * hw) : 0.f;
+      const float b = c + 1 < C ? __ldg(src + (c + 1) * hw) : 0.f;
       *reinterpret_cast<__nv_bfloat162*>(dst + c) = __floats2bfloat162_rn(a, b);
     }
-    if (c < C_out) dst[c] = __float2bfloat16_rn(c < C ? src[(long long)c * hw] : 0.f);
+    if (c < C_out) dst[c] = __float2bfloat16_rn(c < C ? __ldg(src + c * hw) : 0.f);
   }
 }
 
@@ -52,20 +63,19 @@ __global__ void nhwc_bf16_to_nchw_f32_kernel(const __nv_bfloat16* __restrict__ x
   }
 }
 
-// Max pooling, NHWC bf16, 8 channels (16 bytes) per thread.
+// Max pooling, NHWC bf16, 8 channels (16 bytes) per thread: blockIdx.y walks
+// the output rows (n, oh), the threads of a block x cover (ow, 8-channel group)
+// of the row with ow outermost, so a warp reads contiguous pixels.
 __global__ void maxpool_nhwc_bf16_kernel(const __nv_bfloat16* __restrict__ x,
                                          __nv_bfloat16* __restrict__ y, int N, int C, int H,
                                          int W, int k, int stride, int pad, int OH, int OW) {
   const int cv = C / 8;
-  const long long total = (long long)N * OH * OW * cv;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int c8 = (int)(i % cv);
-    long long t = i / cv;
-    const int ow = (int)(t % OW);
-    t /= OW;
-    const int oh = (int)(t % OH);
-    const int n = (int)(t / OH);
+  const int item = blockIdx.x * blockDim.x + threadIdx.x;
+  if (item >= OW * cv) return;
+  const int ow = item / cv, c8 = item - ow * cv;
+  for (int row = blockIdx.y; row < N * OH; row += gridDim.y) {
+    const int n = row / OH, oh = row - n * OH;
+    const long long i = (long long)row * OW * cv + item;  // output vector index
     float m[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) m[j] = -INFINITY;
@@ -152,8 +162,10 @@ __global__ void fill_random_kernel(uint8_t* p, long long n, int elem_bytes, uint
 
 cudaError_t launch_nchw_f32_to_nhwc_bf16(const float* x, void* y, int N, int C, int H, int W,
                                          int C_out, cudaStream_t st) {
-  nchw_f32_to_nhwc_bf16_kernel<<<grid_for((long long)N * H * W), kBlock, 0, st>>>(
-      x, static_cast<__nv_bfloat16*>(y), N, C, H, W, C_out);
+  if ((long long)N * H >= (1LL << 31)) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)gb_ceil_div(W, 128), (unsigned)std::min(N * H, 65535));
+  nchw_f32_to_nhwc_bf16_kernel<<<grid, 128, 0, st>>>(x, static_cast<__nv_bfloat16*>(y), N, C, H,
+                                                     W, C_out);
   gb_count_launch();
   return cudaGetLastError();
 }
@@ -169,7 +181,10 @@ cudaError_t launch_nhwc_bf16_to_nchw_f32(const void* x, float* y, int N, int C, 
 cudaError_t launch_maxpool_nhwc_bf16(const void* x, void* y, int N, int C, int H, int W, int k,
                                      int stride, int pad, cudaStream_t st) {
   const int OH = (H + 2 * pad - k) / stride + 1, OW = (W + 2 * pad - k) / stride + 1;
-  maxpool_nhwc_bf16_kernel<<<grid_for((long long)N * OH * OW * (C / 8)), kBlock, 0, st>>>(
+  if ((long long)N * OH >= (1LL << 31) || (long long)OW * (C / 8) >= (1LL << 31))
+    return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)gb_ceil_div(OW * (C / 8), kBlock), (unsigned)std::min(N * OH, 65535));
+  maxpool_nhwc_bf16_kernel<<<grid, kBlock, 0, st>>>(
       static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), N, C, H, W, k, stride,
       pad, OH, OW);
   gb_count_launch();

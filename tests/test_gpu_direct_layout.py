@@ -100,6 +100,23 @@ def test_layout_conversion_bit_exact():
     assert np.array_equal(back.cpu().numpy(), ol.round_bf16(x))
 
 
+@pytest.mark.parametrize("C,C_out,W", [(3, 4, 224), (3, 4, 130), (4, 4, 9), (3, 8, 300)])
+def test_layout_conversion_image_channels(C, C_out, W):
+    """An RGB image padded to 4 (the 4x4 space-to-depth stem's input) or 8
+    channels, rows wider than one 128-thread block included."""
+    torch = need_gpu()
+    from cnn_convolution_gemm_gb300 import binding as B
+    dev = torch.device("cuda:0")
+    x = (np.random.default_rng(C_out + W).standard_normal((2, C, 5, W)) * 4).astype(np.float32)
+    y = torch.full((2, 5, W, C_out), 3.0, dtype=torch.bfloat16, device=dev)
+    B.conv_nchw_f32_to_nhwc_bf16(torch.from_numpy(x).to(dev).data_ptr(), y.data_ptr(), 2, C, 5,
+                                 W, C_out, None)
+    torch.cuda.synchronize()
+    yh = y.float().cpu().numpy()
+    assert np.array_equal(yh[..., :C], nchw_to_nhwc(ol.round_bf16(x)))
+    assert np.all(yh[..., C:] == 0)
+
+
 def test_pooling():
     torch = need_gpu()
     from cnn_convolution_gemm_gb300 import binding as B
@@ -114,5 +131,14 @@ def test_pooling():
     torch.cuda.synchronize()
     ref = nchw_to_nhwc(ol.maxpool2d(nhwc_to_nchw(x.double().numpy()), 3, 2, 1))
     assert np.array_equal(y.double().cpu().numpy(), ref)
+    # the ResNet-50 shape's row layout (56 output columns x 8 channel groups per row)
+    x2 = torch.from_numpy(g.standard_normal((3, 112, 112, 64)).astype(np.float32)).to(
+        torch.bfloat16)
+    y2 = torch.empty((3, 56, 56, 64), dtype=torch.bfloat16, device=dev)
+    B.conv_maxpool2d_nhwc_bf16(x2.to(dev).data_ptr(), y2.data_ptr(), 3, 64, 112, 112, 3, 2, 1,
+                               None)
+    torch.cuda.synchronize()
+    ref2 = nchw_to_nhwc(ol.maxpool2d(nhwc_to_nchw(x2.double().numpy()), 3, 2, 1))
+    assert np.array_equal(y2.double().cpu().numpy(), ref2)
     aref = ol.global_avgpool(nhwc_to_nchw(x.double().numpy()))
     np.testing.assert_allclose(a.double().cpu().numpy(), aref, rtol=1e-2, atol=1e-2)
