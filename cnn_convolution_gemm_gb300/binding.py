@@ -64,6 +64,8 @@ SIGNATURES = {
     "conv_weights_packed_size": (_i, [_p, _i, ctypes.POINTER(_sz)]),
     "conv_weights_prepack": (_i, [_p, _i, _p, _p, _p]),
     "conv_fwd": (_i, [_p, _p, _p, _p, _p, _p, _i, _p, _sz, _p]),
+    "conv_fwd_host_scratch_size": (_i, [_p, _i, _i, ctypes.POINTER(_sz)]),
+    "conv_fwd_host": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _p, _sz, _p]),
     "conv_fwd_noalloc": (_i, [_p, _p, _p, _p, _p, _p, _i, _p]),
     "conv_mbv2_block_packed_size": (_i, [_i, _i, _i, ctypes.POINTER(_sz)]),
     "conv_mbv2_block_prepack": (_i, [_i, _i, _i, _p, _p, _p, _p, _p, _p]),
@@ -207,6 +209,23 @@ def conv_fwd(desc, x_ptr, wpack_ptr, bias_ptr, residual_ptr, y_ptr, algo=CONV_AL
     _check(load_library().conv_fwd(desc, _ptr(x_ptr), _ptr(wpack_ptr), _ptr(bias_ptr),
                                    _ptr(residual_ptr), _ptr(y_ptr), algo, _ptr(ws_ptr), ws_bytes,
                                    _stream(stream)), "conv_fwd")
+
+
+def conv_fwd_host_scratch_size(desc, algo=CONV_ALGO_AUTO, n_chunk=0):
+    n = ctypes.c_size_t()
+    _check(load_library().conv_fwd_host_scratch_size(desc, algo, n_chunk, ctypes.byref(n)),
+           "conv_fwd_host_scratch_size")
+    return n.value
+
+
+def conv_fwd_host(desc, x_host_ptr, wpack_ptr, bias_ptr, residual_host_ptr, y_host_ptr,
+                  algo=CONV_ALGO_AUTO, n_chunk=0, scratch_ptr=None, scratch_bytes=0, stream=None):
+    """x, residual and y in host memory (page-locked for overlap); wpack, bias on
+    the device.  Stream-ordered like conv_fwd."""
+    _check(load_library().conv_fwd_host(desc, _ptr(x_host_ptr), _ptr(wpack_ptr), _ptr(bias_ptr),
+                                        _ptr(residual_host_ptr), _ptr(y_host_ptr), algo, n_chunk,
+                                        _ptr(scratch_ptr), scratch_bytes, _stream(stream)),
+           "conv_fwd_host")
 
 
 def conv_fwd_noalloc(desc, x_ptr, wpack_ptr, bias_ptr, residual_ptr, y_ptr, algo, stream=None):

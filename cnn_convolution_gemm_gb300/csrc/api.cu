@@ -660,6 +660,171 @@ extern "C" conv_status_t conv_fwd(conv_desc_t d, const void* x, const void* wpac
 }
 
 // ---------------------------------------------------------------------------
+// forward pass on host tensors: chunked copies overlapping the convolution
+
+// bytes of one image of the input (or output) tensor in the descriptor's layout
+static size_t image_bytes(const gbconv_desc_s& d, bool input) {
+  const size_t c = input ? d.C : d.K;
+  const size_t hw = input ? (size_t)d.H * d.W : (size_t)d.OH * d.OW;
+  const size_t cp = d.layout == CONV_NC32HW32 ? (c + 31) / 32 * 32 : c;
+  return cp * hw * elem_bytes(d.dtype);
+}
+
+static size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+struct HostPlan {
+  int a, n_chunk;
+  size_t xb, yb, rb, ws;  // per-chunk buffer bytes (rounded) and the chunk workspace
+  size_t total;
+};
+
+// the algorithm and chunking for conv_fwd_host; chunks fall back to the whole
+// batch when the packed weights of a chunk-sized problem would differ
+static conv_status_t host_plan(const gbconv_desc_s& d, conv_algo_t algo, int n_chunk,
+                               HostPlan* hp) {
+  const int a = resolve(d, algo);
+  conv_status_t st = check_algo(d, a);
+  if (st != CONV_OK) return st;
+  int nc = (n_chunk <= 0 || n_chunk > d.N) ? d.N : n_chunk;
+  if (nc < d.N) {
+    gbconv_desc_s e = d;
+    e.N = nc;
+    size_t pf = 0, pc = 0;
+    if (!applicable(e, a, nullptr) ||
+        conv_weights_packed_size(const_cast<gbconv_desc_s*>(&d), a, &pf) != CONV_OK ||
+        conv_weights_packed_size(&e, a, &pc) != CONV_OK || pf != pc)
+      nc = d.N;
+  }
+  gbconv_desc_s e = d;
+  e.N = nc;
+  size_t ws = 0;
+  st = conv_workspace_size(&e, a, &ws);
+  if (st != CONV_OK) return st;
+  hp->a = a;
+  hp->n_chunk = nc;
+  hp->xb = round256(image_bytes(d, true) * nc);
+  hp->yb = round256(image_bytes(d, false) * nc);
+  hp->rb = d.has_residual ? hp->yb : 0;
+  hp->ws = round256(ws);
+  hp->total = 2 * (hp->xb + hp->yb + hp->rb) + hp->ws;
+  return ok_status();
+}
+
+extern "C" conv_status_t conv_fwd_host_scratch_size(conv_desc_t d, conv_algo_t algo, int n_chunk,
+                                                    size_t* bytes) {
+  if (!d || !bytes) return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
+  HostPlan hp;
+  conv_status_t st = host_plan(*d, algo, n_chunk, &hp);
+  if (st != CONV_OK) return st;
+  *bytes = hp.total;
+  return ok_status();
+}
+
+namespace {
+// the copy streams and the events that order chunks (one set per device)
+struct HostPipe {
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  cudaEvent_t start = nullptr, in[2] = {}, cv[2] = {}, out[2] = {};
+};
+std::mutex g_pipe_mu;
+std::map<int, HostPipe> g_pipes;
+
+cudaError_t host_pipe(HostPipe** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  HostPipe& p = g_pipes[dev];
+  if (!p.s_in) {
+    if ((e = cudaStreamCreateWithFlags(&p.s_in, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithFlags(&p.s_out, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    cudaEvent_t* evs[] = {&p.start, &p.in[0], &p.in[1], &p.cv[0], &p.cv[1], &p.out[0], &p.out[1]};
+    for (cudaEvent_t* ev : evs)
+      if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) return e;
+  }
+  *out = &p;
+  return cudaSuccess;
+}
+}  // namespace
+
+extern "C" conv_status_t conv_fwd_host(conv_desc_t d, const void* x_host, const void* wpack,
+                                       const void* bias, const void* residual_host, void* y_host,
+                                       conv_algo_t algo, int n_chunk, void* scratch,
+                                       size_t scratch_bytes, void* stream) {
+  if (!d || !x_host || !wpack || !y_host || !scratch)
+    return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
+  if (d->has_residual != (residual_host != nullptr))
+    return gb_fail(CONV_ERR_BAD_PARAM, "residual_host must be given exactly when the "
+                                       "descriptor has a residual");
+  if (d->dtype == CONV_INT8 && !d->scale)
+    return gb_fail(CONV_ERR_BAD_PARAM, "int8 descriptor has no requant scale");
+  if (reinterpret_cast<uintptr_t>(scratch) & 255u)
+    return gb_fail(CONV_ERR_ALIGNMENT, "scratch must be 256-byte aligned");
+  if (!aligned16(wpack) || (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)))
+    return gb_fail(CONV_ERR_ALIGNMENT, "wpack must be 16-byte aligned (bias 4-byte)");
+  HostPlan hp;
+  conv_status_t st = host_plan(*d, algo, n_chunk, &hp);
+  if (st != CONV_OK) return st;
+  if (scratch_bytes < hp.total)
+    return gb_fail(CONV_ERR_WORKSPACE, "scratch of %zu bytes needed", hp.total);
+  char* base = static_cast<char*>(scratch);
+  char* xbuf[2] = {base, base + hp.xb};
+  char* ybuf[2] = {base + 2 * hp.xb, base + 2 * hp.xb + hp.yb};
+  char* rbuf[2] = {base + 2 * (hp.xb + hp.yb), base + 2 * (hp.xb + hp.yb) + hp.rb};
+  char* ws = base + 2 * (hp.xb + hp.yb + hp.rb);
+  const size_t xi = image_bytes(*d, true), yi = image_bytes(*d, false);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  std::lock_guard<std::mutex> lk(g_pipe_mu);
+  HostPipe* pp = nullptr;
+  cudaError_t e = host_pipe(&pp);
+  if (e != cudaSuccess) return cuda_fail(e, "conv_fwd_host streams");
+  HostPipe& p = *pp;
+  // the copies start after whatever `stream` holds before this call
+  if ((e = cudaEventRecord(p.start, s)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(p.s_in, p.start, 0)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(p.s_out, p.start, 0)) != cudaSuccess)
+    return cuda_fail(e, "conv_fwd_host ordering");
+  const int nch = gb_ceil_div(d->N, hp.n_chunk);
+  for (int i = 0; i < nch; ++i) {
+    const int slot = i & 1;
+    const int n0 = i * hp.n_chunk, nc = std::min(hp.n_chunk, d->N - n0);
+    // input copies: slot free once the convolution of chunk i - 2 has read it
+    if (i >= 2 && (e = cudaStreamWaitEvent(p.s_in, p.cv[slot], 0)) != cudaSuccess) break;
+    if ((e = cudaMemcpyAsync(xbuf[slot], static_cast<const char*>(x_host) + n0 * xi, nc * xi,
+                             cudaMemcpyHostToDevice, p.s_in)) != cudaSuccess)
+      break;
+    if (residual_host &&
+        (e = cudaMemcpyAsync(rbuf[slot], static_cast<const char*>(residual_host) + n0 * yi,
+                             nc * yi, cudaMemcpyHostToDevice, p.s_in)) != cudaSuccess)
+      break;
+    if ((e = cudaEventRecord(p.in[slot], p.s_in)) != cudaSuccess) break;
+    // the convolution of chunk i on `stream`: after its input landed and after
+    // the output copy of chunk i - 2 has drained the output slot
+    if ((e = cudaStreamWaitEvent(s, p.in[slot], 0)) != cudaSuccess) break;
+    if (i >= 2 && (e = cudaStreamWaitEvent(s, p.out[slot], 0)) != cudaSuccess) break;
+    gbconv_desc_s c = *d;
+    c.N = nc;
+    st = fwd_impl(c, xbuf[slot], wpack, bias, residual_host ? rbuf[slot] : nullptr, ybuf[slot],
+                  hp.a, ws, hp.ws, s);
+    if (st != CONV_OK) return st;
+    if ((e = cudaEventRecord(p.cv[slot], s)) != cudaSuccess) break;
+    // output copy of chunk i
+    if ((e = cudaStreamWaitEvent(p.s_out, p.cv[slot], 0)) != cudaSuccess) break;
+    if ((e = cudaMemcpyAsync(static_cast<char*>(y_host) + n0 * yi, ybuf[slot], nc * yi,
+                             cudaMemcpyDeviceToHost, p.s_out)) != cudaSuccess)
+      break;
+    if ((e = cudaEventRecord(p.out[slot], p.s_out)) != cudaSuccess) break;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "conv_fwd_host");
+  // `stream` continues after every output copy (the last one of each slot)
+  for (int slot = 0; slot < 2 && slot < nch; ++slot)
+    if ((e = cudaStreamWaitEvent(s, p.out[slot], 0)) != cudaSuccess)
+      return cuda_fail(e, "conv_fwd_host ordering");
+  return ok_status();
+}
+
+
+// ---------------------------------------------------------------------------
 // fused MobileNetV2 block
 
 static conv_status_t mbv2_check(int C_in, int E, int C_out) {

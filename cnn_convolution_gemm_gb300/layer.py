@@ -97,3 +97,26 @@ class ConvLayer:
         return out
 
     __call__ = forward
+
+    def forward_host(self, x_host: torch.Tensor, bias=None, residual_host=None, out_host=None,
+                     n_chunk=0, stream=None):
+        """The same forward pass on host tensors (x, residual, y page-locked in host
+        memory; weights and bias on the device): the batch runs in chunks of
+        n_chunk images whose copies overlap the convolution (conv_fwd_host).
+        Stream-ordered: out_host is complete once the stream has caught up."""
+        if self.wpack is None:
+            raise RuntimeError("prepack() the weights first")
+        if out_host is None:
+            out_host = torch.empty(self.output_shape, dtype=x_host.dtype).pin_memory()
+        need = B.conv_fwd_host_scratch_size(self.desc, self.algo, n_chunk)
+        sc = getattr(self, "_host_scratch", None)
+        if sc is None or sc.numel() < need:
+            dev = self.wpack.device
+            sc = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+            self._host_scratch = sc
+        B.conv_fwd_host(self.desc, x_host.data_ptr(), self.wpack.data_ptr(),
+                        None if bias is None else bias.data_ptr(),
+                        None if residual_host is None else residual_host.data_ptr(),
+                        out_host.data_ptr(), self.algo, n_chunk, sc.data_ptr(), sc.numel(),
+                        current_stream_handle() if stream is None else stream)
+        return out_host

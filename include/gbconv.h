@@ -189,6 +189,39 @@ conv_status_t conv_fwd_noalloc(conv_desc_t desc, const void* x, const void* wpac
                                const void* bias, const void* residual, void* y,
                                conv_algo_t algo, void* stream);
 
+/* ---- forward pass on host tensors ---------------------------------------- */
+
+/* conv_fwd with the activations in HOST memory: x_host (and residual_host when
+ * the descriptor has a residual) are copied to the device, convolved, and the
+ * result copied back to y_host.  The batch is cut into chunks of n_chunk
+ * images (n_chunk <= 0 or >= N: one chunk) and the copies run on two streams
+ * the library owns, so chunk i+1's input copy and chunk i-1's output copy
+ * overlap chunk i's convolution, which runs on `stream`.  Images are
+ * independent, so the result equals conv_fwd on the whole batch.
+ *   x_host, residual_host, y_host: the same layouts and sizes as conv_fwd's
+ *     device tensors, in host memory (page-locked memory lets the copies
+ *     overlap; pageable memory works but serialises them).
+ *   wpack, bias: DEVICE pointers, as for conv_fwd (weights stay resident).
+ *   algo: as for conv_fwd (AUTO resolves on the whole-batch descriptor).  An
+ *     algorithm whose packed-weight layout depends on the batch size (the int8
+ *     split-weight choice) runs the batch as one chunk.
+ *   scratch: device memory of conv_fwd_host_scratch_size() bytes, 256-byte
+ *     aligned, caller-owned: two input, two output (and two residual) chunk
+ *     buffers plus the algorithm's workspace for one chunk.
+ * Stream-ordered: the call enqueues and returns; y_host is complete when
+ * `stream` reaches the point after the call (e.g. after
+ * cudaStreamSynchronize(stream) or conv_sync_status(stream)).  Host threads
+ * calling it at the same time are serialised while they enqueue.
+ * Errors: CONV_ERR_BAD_PARAM (NULL tensor, residual mismatch), the algorithm's
+ * CONV_ERR_UNSUPPORTED, CONV_ERR_WORKSPACE (scratch too small),
+ * CONV_ERR_ALIGNMENT, CONV_ERR_CUDA. */
+conv_status_t conv_fwd_host_scratch_size(conv_desc_t desc, conv_algo_t algo, int n_chunk,
+                                         size_t* bytes);
+conv_status_t conv_fwd_host(conv_desc_t desc, const void* x_host, const void* wpack,
+                            const void* bias, const void* residual_host, void* y_host,
+                            conv_algo_t algo, int n_chunk, void* scratch, size_t scratch_bytes,
+                            void* stream);
+
 /* ---- fused MobileNetV2 block ([Momenta] "Graph層面" and "優化2") ----------- */
 
 /* The inverted-residual block of MobileNetV2 at stride 1 as ONE kernel:

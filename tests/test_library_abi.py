@@ -166,6 +166,29 @@ def test_status_strings(B):
     assert B.conv_version().startswith("gbconv")
 
 
+def test_fwd_host_scratch_and_argument_errors(B):
+    # scratch = 2 x (input chunk + output chunk) + the chunk's workspace, each 256-rounded
+    d = B.conv_desc_create(8, 64, 10, 10, 128, 3, 3, 1, 1, 1, 1, B.CONV_BF16)
+    xi, yi = 64 * 100 * 2, 128 * 100 * 2
+    r256 = lambda b: (b + 255) // 256 * 256
+    assert B.conv_fwd_host_scratch_size(d, B.CONV_ALGO_IGEMM_N128, 3) == 2 * (
+        r256(3 * xi) + r256(3 * yi))
+    assert B.conv_fwd_host_scratch_size(d, B.CONV_ALGO_IGEMM_N128, 0) == 2 * (8 * xi + 8 * yi)
+    assert B.conv_fwd_host_scratch_size(d, B.CONV_ALGO_IGEMM_N128, 99) == 2 * (8 * xi + 8 * yi)
+    n0 = B.conv_launch_count()
+    for args, status in [
+        ((d, 0, 16, None, None, 16, 2, 2, 256, 1 << 20, None), "CONV_ERR_BAD_PARAM"),  # NULL x
+        ((d, 16, 16, None, 16, 16, 2, 2, 256, 1 << 20, None), "CONV_ERR_BAD_PARAM"),  # residual
+        ((d, 16, 16, None, None, 16, 2, 2, 272, 1 << 20, None), "CONV_ERR_ALIGNMENT"),  # scratch
+        ((d, 16, 16, None, None, 16, 2, 2, 256, 1024, None), "CONV_ERR_WORKSPACE"),
+    ]:
+        with pytest.raises(B.GbconvError) as e:
+            B.conv_fwd_host(*args)
+        assert e.value.status_name == status
+    assert B.conv_launch_count() == n0
+    B.conv_desc_destroy(d)
+
+
 def test_launch_counter_does_not_move_on_rejected_calls(B):
     # calls that fail validation on the host launch nothing
     n0 = B.conv_launch_count()
