@@ -19,6 +19,7 @@ Other workloads (--workload):
                 Fast-Run pick) are both timed and the faster runs; --algo fused
                 forces the fused kernel, any layer algorithm name the chain
   int8_stages   int8 3x3 convs at the four ResNet-50 stage shapes, N=32
+  stem7x7       ResNet-50's stem alone (7x7/2, 3 -> 64, 224x224, batch 64)
   resnet50      full ResNet-50 forward, batch 64, 224x224x3 input
 
 Timing: W >= 3 untimed warm-up steps, then K steps; before every step the L2
@@ -443,6 +444,67 @@ class GroupedConv(Workload):
                 "sample": f"{n} of 64 images", "seconds": round(dt, 3)}
 
 
+class Stem7x7(Workload):
+    """ResNet-50's stem alone: 7x7 / 2, pad 3, 3 -> 64 channels + ReLU on a batch
+    of 64 224x224 images (NHWC bf16, the RGB channels padded to 4 for the 4x4
+    space-to-depth algorithm); FLOPs counted over the 3 real channels."""
+    name = "resnet50_stem_conv7x7s2_c3_k64_224x224_n64_bf16_nhwc"
+    metric = "conv TFLOP/s (direct-equivalent), ResNet-50 stem 7x7/2 3->64 @224x224, batch 64"
+
+    def setup(self, dev, rank, args):
+        import torch
+        from cnn_convolution_gemm_gb300 import binding as B
+        from cnn_convolution_gemm_gb300 import synth
+        from cnn_convolution_gemm_gb300.layer import ConvLayer
+        from cnn_convolution_gemm_gb300.workload import ConvShape
+        N, C, H, K = 64, 4, 224, 64
+        self.shape = ConvShape(N, 3, H, H, K, 7, 7, 2, 3)
+        x = synth.normal((N, H, H, C), 1.0, rank)
+        x[..., 3:] = 0.0
+        w = synth.kaiming((K, 7, 7, C), rank + 1, fan_in=3 * 49)
+        w[..., 3:] = 0.0
+        b = synth.uniform((K,), -0.1, 0.1, rank + 2)
+        self.sh = torch.cuda.current_stream().cuda_stream
+        self.xh = torch.from_numpy(x).to(torch.bfloat16).pin_memory()
+        self.x = self.xh.to(dev)
+        self.b = torch.from_numpy(b).to(dev)
+        self.layer = ConvLayer(N, C, H, H, K, 7, 7, 2, 3, act=B.CONV_ACT_RELU)
+        a, self.fastrun_ms = fastrun_pick(self.layer, self.sh, args, B)
+        self.layer.prepack(torch.from_numpy(w).to(torch.bfloat16).to(dev), a)
+        self.algo_name = B.conv_algo_info(self.layer.desc, a)[1]
+        self.y = torch.empty(self.layer.output_shape, dtype=torch.bfloat16, device=dev)
+        self.yh = torch.empty(self.layer.output_shape, dtype=torch.bfloat16).pin_memory()
+
+    def groups(self):
+        # algorithmic bytes: the 4-channel input, the output, weights and bias
+        nbytes = 64 * 224 * 224 * 4 * 2 + 64 * 112 * 112 * 64 * 2 + 64 * 49 * 4 * 2 + 64 * 4
+        return [(self.algo_name, lambda: self.layer.forward(self.x, self.b, out=self.y,
+                                                            stream=self.sh),
+                 self.shape.flops(), nbytes, "tensor")]
+
+    def h2d(self):
+        return [(self.xh, self.x)]
+
+    def d2h(self):
+        return [(self.y, self.yh)]
+
+    def cpu_baseline(self, args):
+        import numpy as np
+        from cnn_convolution_gemm_gb300 import synth
+        from cnn_convolution_gemm_gb300.workload import ConvShape
+        from oracle import lib as ol
+        n = 2
+        x = synth.normal((n, 224, 224, 3), 1.0, 0)
+        w = synth.kaiming((64, 7, 7, 3), 1)
+        t0 = time.perf_counter()
+        ol.conv2d_f64(np.ascontiguousarray(x.transpose(0, 3, 1, 2)), w.transpose(0, 3, 1, 2),
+                      stride=2, pad=3)
+        dt = time.perf_counter() - t0
+        f = ConvShape(n, 3, 224, 224, 64, 7, 7, 2, 3).flops()
+        return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": threads(), "kind": "oracle",
+                "sample": f"{n} of 64 images", "seconds": round(dt, 3)}
+
+
 class SingleLayer(Workload):
     name = "single_conv3x3_c32_k32_28x28_n1_f32_nchw"
     metric = "conv TFLOP/s (direct-equivalent), 1x32x28x28 fp32 NCHW, 32 filters 3x3"
@@ -801,7 +863,7 @@ class ResNet50W(Workload):
 WORKLOADS = {"resnet3x3": ResNetLayer, "resnet3x3_tf32": ResNetLayerTF32,
              "shuffle_dw": ShuffleDepthwise, "gconv_g3": GroupedConv,
              "single_layer": SingleLayer, "mbv2_block": MBv2Block,
-             "int8_stages": Int8Stages, "resnet50": ResNet50W}
+             "int8_stages": Int8Stages, "resnet50": ResNet50W, "stem7x7": Stem7x7}
 
 
 def dist_setup():

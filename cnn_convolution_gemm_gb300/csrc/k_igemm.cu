@@ -875,8 +875,11 @@ cudaError_t launch_igemm_bf16(const gbconv_desc_s& d, int block_n, const void* x
   // and memory, not by the operand pipeline: run two shallow CTAs per SM
   const int kiters = d.C == 8 ? gb_ceil_div(d.R * d.S, 8) : d.R * d.S * gb_ceil_div(d.C, BK);
   const int kper = split.ksplit > 1 ? split.kchunk : kiters;
-  // (the exact int8 epilogue does more per output: two CTAs per SM up to 16 k-steps)
-  const bool light = d.C != 8 && (kper <= 8 || (split.i8_y && kper <= 16));
+  // (the exact int8 epilogue does more per output: two CTAs per SM up to 16 k-steps;
+  // the space-to-depth stem's 9 or 18 k-steps per tile leave its epilogue, which
+  // scatters 8-row pieces, as the bound: two CTAs per SM)
+  const bool light =
+      d.C != 8 && (kper <= 8 || (split.i8_y && kper <= 16) || (split.s2d4_k && kper <= 18));
   switch (block_n) {
     case 64:
       return light ? launch_bn<64, true>(d, x, wpack, bias, res, y, err, wait_ns, st, split)
