@@ -99,6 +99,44 @@ struct Cfg {
   static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES + 1024;
 };
 
+// Two fp32 values in one 64-bit register pair (channels n, n + 1) for the packed
+// fp32 add of the bf16 epilogue.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 f2_pack(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+// two IEEE fp32 additions (each rounded to nearest even) in one instruction
+__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// a bf16x2 word -> its two values in fp32 (exact: a bf16 is the top half of an fp32)
+__device__ __forceinline__ f32x2 bf16x2_to_f2(uint32_t u) {
+  return f2_pack(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+// activation, then rounding to a bf16x2 word (lo channel in the low half): the
+// conversion's relu clamps negatives to zero, ReLU6 then takes a packed min
+// with 6 (exact in bf16); activation and the monotone rounding commute
+__device__ __forceinline__ uint32_t act_to_bf16x2(f32x2 v, int act) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  uint32_t r;
+  if (act == 0) {
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+  }
+  asm("cvt.rn.relu.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  if (act == 2) {
+    const __nv_bfloat162 six = __float2bfloat162_rn(6.f);
+    __nv_bfloat162 h = __hmin2(*reinterpret_cast<__nv_bfloat162*>(&r), six);
+    r = *reinterpret_cast<uint32_t*>(&h);
+  }
+  return r;
+}
+
 __device__ __forceinline__ float act_apply(float v, int act) {
   if (act == 1) return fmaxf(v, 0.0f);
   if (act == 2) return fminf(fmaxf(v, 0.0f), 6.0f);
@@ -538,38 +576,28 @@ __global__ void __launch_bounds__(192, 1)
           }
           __syncwarp();
           gb::tmem_ld_wait();
+          // per channel pair: fp32 accumulator + bias (+ residual), each an IEEE
+          // fp32 add (packed two per instruction), then activation and bf16
+          // rounding in one conversion
 #pragma unroll
           for (int c16 = 0; c16 < 4; ++c16) {
-            const int n = nb0 + c16 * 16;
-            float v[16];
-#pragma unroll
-            for (int k = 0; k < 16; k += 4) {
-              const float4 bq = reinterpret_cast<const float4*>(sbias)[c16 * 4 + k / 4];
-              v[k] = __uint_as_float(r[c16 * 16 + k]) + bq.x;
-              v[k + 1] = __uint_as_float(r[c16 * 16 + k + 1]) + bq.y;
-              v[k + 2] = __uint_as_float(r[c16 * 16 + k + 2]) + bq.z;
-              v[k + 3] = __uint_as_float(r[c16 * 16 + k + 3]) + bq.w;
-            }
-            (void)n;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               uint8_t* chunk = box + lane * 128 + (((c16 * 2 + h) ^ (lane & 7)) << 4);
-              if (has_res) {
-                const uint4 rv = *reinterpret_cast<const uint4*>(chunk);
-                const __nv_bfloat162* rp = reinterpret_cast<const __nv_bfloat162*>(&rv);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  const float2 f = __bfloat1622float2(rp[k]);
-                  v[h * 8 + 2 * k] += f.x;
-                  v[h * 8 + 2 * k + 1] += f.y;
-                }
-              }
+              uint4 rv = make_uint4(0, 0, 0, 0);
+              if (has_res) rv = *reinterpret_cast<const uint4*>(chunk);
+              const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+              const float4 b0 = reinterpret_cast<const float4*>(sbias)[c16 * 4 + h * 2];
+              const float4 b1 = reinterpret_cast<const float4*>(sbias)[c16 * 4 + h * 2 + 1];
+              const f32x2 bp[4] = {f2_pack(b0.x, b0.y), f2_pack(b0.z, b0.w), f2_pack(b1.x, b1.y),
+                                   f2_pack(b1.z, b1.w)};
               uint32_t pk[4];
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
-                __nv_bfloat162 b2 = __floats2bfloat162_rn(act_apply(v[h * 8 + 2 * k], p.act),
-                                                          act_apply(v[h * 8 + 2 * k + 1], p.act));
-                pk[k] = *reinterpret_cast<uint32_t*>(&b2);
+                const int i = c16 * 16 + h * 8 + 2 * k;
+                f32x2 v = f2_add(f2_pack(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), bp[k]);
+                if (has_res) v = f2_add(v, bf16x2_to_f2(rw[k]));
+                pk[k] = act_to_bf16x2(v, p.act);
               }
               *reinterpret_cast<uint4*>(chunk) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
