@@ -120,21 +120,55 @@ __device__ __forceinline__ f32x2 bf16x2_to_f2(uint32_t u) {
 // activation, then rounding to a bf16x2 word (lo channel in the low half): the
 // conversion's relu clamps negatives to zero, ReLU6 then takes a packed min
 // with 6 (exact in bf16); activation and the monotone rounding commute
-__device__ __forceinline__ uint32_t act_to_bf16x2(f32x2 v, int act) {
+template <int ACT>
+__device__ __forceinline__ uint32_t act_to_bf16x2(f32x2 v) {
   float lo, hi;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
   uint32_t r;
-  if (act == 0) {
+  if (ACT == 0) {
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
   }
   asm("cvt.rn.relu.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  if (act == 2) {
+  if (ACT == 2) {
     const __nv_bfloat162 six = __float2bfloat162_rn(6.f);
     __nv_bfloat162 h = __hmin2(*reinterpret_cast<__nv_bfloat162*>(&r), six);
     r = *reinterpret_cast<uint32_t*>(&h);
   }
   return r;
+}
+
+// One 32-row x 64-column bf16 epilogue sub-block of a warp: fp32 accumulator
+// (r) + bias (sbias, 64 values) (+ the residual already staged in the box),
+// activation, bf16, written to the 128-byte-swizzled staging box.  Per channel
+// pair: each add an IEEE fp32 add (packed two per instruction), then the
+// activation and the bf16 rounding in one conversion.
+template <int ACT>
+__device__ __forceinline__ void epi_bf16_subblock(const uint32_t (&r)[64], const float* sbias,
+                                                  uint8_t* box, int lane, bool has_res) {
+#pragma unroll
+  for (int c16 = 0; c16 < 4; ++c16) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint8_t* chunk = box + lane * 128 + (((c16 * 2 + h) ^ (lane & 7)) << 4);
+      uint4 rv = make_uint4(0, 0, 0, 0);
+      if (has_res) rv = *reinterpret_cast<const uint4*>(chunk);
+      const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+      const float4 b0 = reinterpret_cast<const float4*>(sbias)[c16 * 4 + h * 2];
+      const float4 b1 = reinterpret_cast<const float4*>(sbias)[c16 * 4 + h * 2 + 1];
+      const f32x2 bp[4] = {f2_pack(b0.x, b0.y), f2_pack(b0.z, b0.w), f2_pack(b1.x, b1.y),
+                           f2_pack(b1.z, b1.w)};
+      uint32_t pk[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = c16 * 16 + h * 8 + 2 * k;
+        f32x2 v = f2_add(f2_pack(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), bp[k]);
+        if (has_res) v = f2_add(v, bf16x2_to_f2(rw[k]));
+        pk[k] = act_to_bf16x2<ACT>(v);
+      }
+      *reinterpret_cast<uint4*>(chunk) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+  }
 }
 
 __device__ __forceinline__ float act_apply(float v, int act) {
@@ -229,13 +263,14 @@ __global__ void __launch_bounds__(192, 1)
         const int bt = t / tiles_per_batch;
         const int tt = t % tiles_per_batch;
         const int mt = tt / p.n_tiles, nt = tt % p.n_tiles;
-        const long long m0 = (long long)mt * BM;
+        const int m0 = mt * BM;  // M < 2^31 (checked on the host): 32-bit index math
         int img = 0, h0 = 0, w0 = 0;
         if (MODE == MODE_CONV) {
-          img = (int)(m0 / ohow);
-          const int rem = (int)(m0 % ohow);
-          h0 = (rem / p.OW) * p.stride - p.pad;
-          w0 = (rem % p.OW) * p.stride - p.pad;
+          img = m0 / ohow;
+          const int rem = m0 - img * ohow;
+          const int oh = rem / p.OW;
+          h0 = oh * p.stride - p.pad;
+          w0 = (rem - oh * p.OW) * p.stride - p.pad;
         }
         const int kbeg = MODE == MODE_CONV ? bt * p.kchunk : 0;
         const int kend = MODE == MODE_CONV ? min(p.kiters, kbeg + p.kchunk) : p.kiters;
@@ -385,6 +420,21 @@ __global__ void __launch_bounds__(192, 1)
           : "memory");
     };
     const bool has_res = MODE == MODE_CONV && p.res != nullptr && p.part == nullptr;
+    // bias of output columns (2 lane, 2 lane + 1) of sub-block j of work unit u
+    // (bf16 epilogue; s2d4: bias of channel c % K)
+    auto bias_pair = [&](int uu, int j) {
+      int t2, noff2, width2;
+      decode(uu, t2, noff2, width2);
+      const int nt2 = (t2 % tiles_per_batch) % p.n_tiles;
+      const int nc = nt2 * BN + noff2 + j * 64 + 2 * lane;
+      const int bc = p.s2d4_k ? nc % p.s2d4_k : nc;
+      float2 bv = make_float2(0.f, 0.f);
+      if (p.bias && nc < p.K) bv = make_float2(__ldg(p.bias + bc), __ldg(p.bias + bc + 1));
+      return bv;
+    };
+    float2 bias_next = make_float2(0.f, 0.f);
+    if (!TF32 && MODE == MODE_CONV && !p.i8_y && !p.part && (int)blockIdx.x < num_units)
+      bias_next = bias_pair(blockIdx.x, 0);
     int pending = -1;  // box with a residual load not yet waited for
     if (has_res && (int)blockIdx.x < num_units) {
       if (lane == 0) fetch_res(blockIdx.x, 0, 0);
@@ -565,43 +615,26 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t (&rr)[16] = *reinterpret_cast<uint32_t(*)[16]>(&r[c16 * 16]);
             gb::tmem_ld_x16(tbase + j * 64 + c16 * 16, rr);  // accumulator column = nb0 - tile n0
           }
-          // this sub-block's 64 bias values: two per lane, then broadcast reads
+          // this sub-block's 64 bias values (loaded one sub-block ahead, two per
+          // lane) staged for broadcast reads; then the next sub-block's are loaded
           float* sbias = reinterpret_cast<float*>(sEpi + 4 * 2 * C::EPI_BOX + q * 256);
+          reinterpret_cast<float2*>(sbias)[lane] = bias_next;
           {
-            const int nc = nb0 + 2 * lane;
-            const int bc = p.s2d4_k ? nc % p.s2d4_k : nc;  // (s2d4: bias of channel c % K)
-            float2 bv = make_float2(0.f, 0.f);
-            if (p.bias && nc < p.K) bv = make_float2(__ldg(p.bias + bc), __ldg(p.bias + bc + 1));
-            reinterpret_cast<float2*>(sbias)[lane] = bv;
+            int tn = u, jn = j + 1;
+            if (jn >= ns) {
+              tn = u + gridDim.x;
+              jn = 0;
+            }
+            if (tn < num_units) bias_next = bias_pair(tn, jn);
           }
           __syncwarp();
           gb::tmem_ld_wait();
-          // per channel pair: fp32 accumulator + bias (+ residual), each an IEEE
-          // fp32 add (packed two per instruction), then activation and bf16
-          // rounding in one conversion
-#pragma unroll
-          for (int c16 = 0; c16 < 4; ++c16) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              uint8_t* chunk = box + lane * 128 + (((c16 * 2 + h) ^ (lane & 7)) << 4);
-              uint4 rv = make_uint4(0, 0, 0, 0);
-              if (has_res) rv = *reinterpret_cast<const uint4*>(chunk);
-              const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
-              const float4 b0 = reinterpret_cast<const float4*>(sbias)[c16 * 4 + h * 2];
-              const float4 b1 = reinterpret_cast<const float4*>(sbias)[c16 * 4 + h * 2 + 1];
-              const f32x2 bp[4] = {f2_pack(b0.x, b0.y), f2_pack(b0.z, b0.w), f2_pack(b1.x, b1.y),
-                                   f2_pack(b1.z, b1.w)};
-              uint32_t pk[4];
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const int i = c16 * 16 + h * 8 + 2 * k;
-                f32x2 v = f2_add(f2_pack(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), bp[k]);
-                if (has_res) v = f2_add(v, bf16x2_to_f2(rw[k]));
-                pk[k] = act_to_bf16x2(v, p.act);
-              }
-              *reinterpret_cast<uint4*>(chunk) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            }
-          }
+          if (p.act == 0)
+            epi_bf16_subblock<0>(r, sbias, box, lane, has_res);
+          else if (p.act == 1)
+            epi_bf16_subblock<1>(r, sbias, box, lane, has_res);
+          else
+            epi_bf16_subblock<2>(r, sbias, box, lane, has_res);
           gb::fence_proxy_async_smem();  // staging writes -> visible to the TMA engine
           __syncwarp();
           if (lane == 0) {
