@@ -230,6 +230,11 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   gb::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Programmatic dependent launch: the next kernel on the stream may start its
+  // own set-up (this one's above) while this grid drains, and this grid reads
+  // or writes global memory only once the kernel before it has completed.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const int tiles_per_batch = p.m_tiles * p.n_tiles;
   const int num_tiles = tiles_per_batch * (MODE == MODE_BATCHED ? p.batch : p.ksplit);
@@ -834,8 +839,19 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
     const int rem = tiles % grid;
     if (rem > 0 && rem <= grid / 2) p.tail_start = tiles - rem;
   }
-  igemm_bf16_tc_kernel<BN, MODE_CONV, LIGHT, TF32><<<grid, 192, Cf::SMEM, st>>>(tmx, tmw, tmy,
-                                                                               tmr, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = Cf::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t le = cudaLaunchKernelEx(&cfg, igemm_bf16_tc_kernel<BN, MODE_CONV, LIGHT, TF32>, tmx,
+                                      tmw, tmy, tmr, p);
+  if (le != cudaSuccess) return le;
   gb_count_launch();
   return cudaGetLastError();
 }
