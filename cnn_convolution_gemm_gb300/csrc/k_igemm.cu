@@ -832,10 +832,11 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   const int tiles = p.m_tiles * p.n_tiles * p.ksplit;
   const int slots = gb_num_sms() * (LIGHT ? 2 : 1);
   const int grid = tiles < slots ? tiles : slots;
-  // a last wave that would leave most SMs idle runs as half-width units
+  // a last wave that would leave most SMs idle runs as half-width units (at
+  // least 64 columns: the epilogue's sub-block; the exact int8 path needs a whole
+  // 128-column lo/hi group per unit)
   p.tail_start = tiles;
-  // (a half-width unit of the exact int8 path is one whole 128-column lo/hi group)
-  if (BN == 256 && p.ksplit == 1 && !LIGHT && tiles > grid) {
+  if ((BN == 256 || (BN == 128 && !p.i8_y)) && p.ksplit == 1 && tiles > grid) {
     const int rem = tiles % grid;
     if (rem > 0 && rem <= grid / 2) p.tail_start = tiles - rem;
   }

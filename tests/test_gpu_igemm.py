@@ -94,6 +94,20 @@ def test_igemm_tail_wave_half_width_units(residual):
     assert ol.normalized_max_error(y, ref) <= TOL
 
 
+@pytest.mark.parametrize("case", [
+    # N, C, H, R, pad, residual: 128-column tiles whose last partial wave runs as
+    # 64-column units
+    (16, 128, 56, 1, 0, True),   # 1x1, two CTAs per SM: 392 tiles on 304 slots
+    (8, 128, 56, 3, 1, False),   # 3x3, one CTA per SM: 196 tiles on 152
+])
+def test_igemm_n128_tail_wave_half_width_units(case):
+    torch = need_gpu()
+    N, C, H, R, pad, res = case
+    y, ref = run_bf16_layer(torch, 2, N, C, H, H, 128, R, R, 1, pad, act=2, residual=res,
+                            seed=10)
+    assert ol.normalized_max_error(y, ref) <= TOL
+
+
 @pytest.mark.parametrize("case", CASES[:8], ids=lambda c: "x".join(map(str, c)))
 def test_explicit_im2col_gemm_matches_oracle(case):
     """The materialised im2col matrix + GEMM comparator (algorithm 9)."""
