@@ -48,6 +48,31 @@ def test_desc_validation(B):
     B.conv_desc_destroy(d)
 
 
+def test_size_limits_and_degenerate_shapes(B):
+    # zero-sized dimensions are rejected at creation
+    for dims in [(0, 8, 8, 8, 8), (1, 0, 8, 8, 8), (1, 8, 0, 8, 8), (1, 8, 8, 8, 0)]:
+        N, C, H, W, K = dims
+        with pytest.raises(B.GbconvError) as e:
+            B.conv_desc_create(N, C, H, W, K, 3, 3, 1, 1, 1, 1, B.CONV_BF16)
+        assert e.value.status_name == "CONV_ERR_BAD_PARAM", dims
+    # N*OH*OW at 2^31: the implicit GEMMs (32-bit GEMM row indices) step aside;
+    # direct and Winograd (which runs chunks of images) still apply
+    big = B.conv_desc_create(1 << 19, 64, 64, 64, 64, 3, 3, 1, 1, 1, 1, B.CONV_BF16)
+    names = {n: ok for _, n, ok in (B.conv_algo_info(big, i) for i in range(B.CONV_ALGO_COUNT))}
+    for n in ("igemm_tc_n64", "igemm_tc_n128", "igemm_tc_n256", "im2col_gemm"):
+        assert not names[n], n
+    assert names["direct"] and names["winograd_f2x2_3x3"]
+    B.conv_desc_destroy(big)
+    # just below: the implicit GEMM applies
+    edge = B.conv_desc_create((1 << 19) - 1, 64, 64, 64, 64, 3, 3, 1, 1, 1, 1, B.CONV_BF16)
+    assert B.conv_algo_info(edge, B.CONV_ALGO_IGEMM_N64)[2]
+    B.conv_desc_destroy(edge)
+    # a 1x1 output (kernel as large as the padded image) and a 1x1 kernel
+    one = B.conv_desc_create(1, 8, 5, 5, 8, 5, 5, 1, 0, 1, 1, B.CONV_BF16)
+    assert B.conv_desc_get_output_dims(one) == (1, 1)
+    B.conv_desc_destroy(one)
+
+
 def test_algo_table_and_applicability(B):
     d = B.conv_desc_create(32, 256, 56, 56, 256, 3, 3, 1, 1, 1, 1, B.CONV_BF16)
     infos = [B.conv_algo_info(d, i) for i in range(B.conv_algo_count(d))]
