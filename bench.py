@@ -535,9 +535,32 @@ class SingleLayer(Workload):
         self.yn = torch.empty((1, 28, 28, 32), dtype=torch.bfloat16, device=dev)
         self.y = torch.empty((1, 32, 28, 28), dtype=torch.float32, device=dev)
         self.yh = torch.empty((1, 32, 28, 28), dtype=torch.float32).pin_memory()
+        # the step's three launches as one CUDA graph (a replay is one launch on
+        # the host; --no-graph launches and times them one by one)
+        self.graph = None
+        if not args.no_graph:
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                for g in self.launches(torch.cuda.current_stream().cuda_stream):
+                    g[1]()
+            torch.cuda.current_stream().wait_stream(side)
+            c0 = B.conv_launch_count()
+            self.graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.graph):
+                for g in self.launches(torch.cuda.current_stream().cuda_stream):
+                    g[1]()
+            self.launches_per_step = B.conv_launch_count() - c0
 
     def groups(self):
-        B, sh = self.B, self.sh
+        if self.graph is not None:
+            return [("layout+" + self.algo_name + "+layout (CUDA graph)", self.graph.replay,
+                     self.shape.flops(), self.shape.traffic_bytes(2, 4) + 2 * 32 * 28 * 28 * 6,
+                     "tensor")]
+        return self.launches(self.sh)
+
+    def launches(self, sh):
+        B = self.B
         return [
             ("nchw_f32_to_nhwc_bf16", lambda: B.conv_nchw_f32_to_nhwc_bf16(
                 self.x.data_ptr(), self.xn.data_ptr(), 1, 32, 28, 28, 32, sh), 0,
@@ -958,8 +981,8 @@ def main():
                          "selection), else select and save it there")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
-                    help="resnet50, int8_stages: launch call by call instead of replaying CUDA "
-                         "graphs")
+                    help="resnet50, int8_stages, single_layer: launch call by call instead of "
+                         "replaying CUDA graphs")
     ap.add_argument("--cpu-images", type=int, default=32)
     ap.add_argument("--e2e-chunk", type=int, default=4,
                     help="images per chunk of the host-tensor forward pass (e2e of resnet3x3)")
