@@ -82,6 +82,7 @@ SIGNATURES = {
     "conv_maxpool2d_nhwc_bf16": (_i, [_p, _p, _i, _i, _i, _i, _i, _i, _i, _p]),
     "conv_global_avgpool_nhwc_bf16": (_i, [_p, _p, _i, _i, _i, _i, _p]),
     "conv_sync_status": (_i, [_p]),
+    "conv_selftest_wait_timeout": (_i, [ctypes.c_uint, _p]),
     "conv_status_string": (_cp, [_i]),
     "conv_last_error_detail": (_cp, []),
     "conv_version": (_cp, []),
@@ -320,6 +321,11 @@ def conv_global_avgpool_nhwc_bf16(x_ptr, y_ptr, N, C, H, W, stream=None):
 
 def conv_sync_status(stream=None):
     _check(load_library().conv_sync_status(_stream(stream)), "conv_sync_status")
+
+
+def conv_selftest_wait_timeout(limit_us, stream=None):
+    _check(load_library().conv_selftest_wait_timeout(limit_us, _stream(stream)),
+           "conv_selftest_wait_timeout")
 
 
 def conv_status_string(st):

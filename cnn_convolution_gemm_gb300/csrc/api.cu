@@ -1146,6 +1146,17 @@ extern "C" conv_status_t conv_global_avgpool_nhwc_bf16(const void* x, void* y, i
 // ---------------------------------------------------------------------------
 // status
 
+extern "C" conv_status_t conv_selftest_wait_timeout(unsigned int limit_us, void* stream) {
+  if (limit_us == 0 || limit_us > 10u * 1000u * 1000u)
+    return gb_fail(CONV_ERR_BAD_PARAM, "limit_us must be in (0, 10 s]");
+  int* err = gb_device_error_word();
+  if (!err) return gb_fail(CONV_ERR_CUDA, "device error word unavailable");
+  cudaError_t e = launch_selftest_wait_timeout(err, (unsigned long long)limit_us * 1000ull,
+                                               static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return ok_status();
+}
+
 extern "C" conv_status_t conv_sync_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");

@@ -34,6 +34,9 @@ int* gb_device_error_word();
 int gb_num_sms();
 // Called after each kernel launch: counts the kernels the library enqueues.
 void gb_count_launch();
+// Diagnostic: a kernel whose bounded wait on an mbarrier nothing arrives at runs
+// out after limit_ns and records DEV_ERR_TIMEOUT in err.
+cudaError_t launch_selftest_wait_timeout(int* err, unsigned long long limit_ns, cudaStream_t st);
 // Raise a kernel's dynamic shared-memory limit, once per (kernel, device): the
 // attribute call costs host time on every launch otherwise.
 cudaError_t gb_set_smem_once(const void* func, int bytes);

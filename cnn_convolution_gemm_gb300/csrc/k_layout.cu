@@ -7,6 +7,7 @@
 #include <algorithm>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace {
 
@@ -241,6 +242,26 @@ cudaError_t launch_nc32_convert(const void* x, void* y, int N, int C, int H, int
   nc32_convert_kernel<<<grid, 256, 0, st>>>(static_cast<const int8_t*>(x),
                                             static_cast<int8_t*>(y), N, C, (long long)H * W,
                                             to_nc32);
+  gb_count_launch();
+  return cudaGetLastError();
+}
+
+namespace {
+// One thread waits on an mbarrier that nothing arrives at, through the bounded
+// wait every tcgen05 kernel uses: the wait runs out after limit_ns, the thread
+// records the timeout in the device error word, and the kernel returns.
+__global__ void selftest_wait_timeout_kernel(int* err, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    gb::mbar_init(&bar, 1);
+    gb::fence_barrier_init();
+    gb::mbar_wait_bounded(&bar, 0, limit_ns, err);
+  }
+}
+}  // namespace
+
+cudaError_t launch_selftest_wait_timeout(int* err, unsigned long long limit_ns, cudaStream_t st) {
+  selftest_wait_timeout_kernel<<<1, 32, 0, st>>>(err, limit_ns);
   gb_count_launch();
   return cudaGetLastError();
 }

@@ -304,6 +304,13 @@ conv_status_t conv_global_avgpool_nhwc_bf16(const void* x, void* y, int N, int C
  * CONV_OK, CONV_ERR_TIMEOUT or CONV_ERR_INTERNAL (or CONV_ERR_CUDA if the
  * synchronization itself failed). */
 conv_status_t conv_sync_status(void* stream);
+/* Diagnostic of the failure path: enqueues a one-thread kernel that waits on an
+ * mbarrier nothing arrives at, through the same bounded wait every tensor-core
+ * kernel uses, with a limit of limit_us microseconds (0 < limit_us <= 10 s).
+ * The wait runs out, the kernel records a timeout in the device error word and
+ * returns (the context stays usable); the next conv_sync_status(stream) then
+ * returns CONV_ERR_TIMEOUT and clears the word.  Stream-ordered. */
+conv_status_t conv_selftest_wait_timeout(unsigned int limit_us, void* stream);
 const char* conv_status_string(conv_status_t status);
 /* Reason for the last non-OK status returned on this thread ("" if none). */
 const char* conv_last_error_detail(void);

@@ -185,6 +185,13 @@ def test_input_shuffle_validation(B):
         B.conv_desc_destroy(h)
 
 
+def test_selftest_argument_checks(B):
+    for bad in (0, 10_000_001):
+        with pytest.raises(B.GbconvError) as e:
+            B.conv_selftest_wait_timeout(bad, None)
+        assert e.value.status_name == "CONV_ERR_BAD_PARAM"
+
+
 def test_status_strings(B):
     assert B.conv_status_string(0) == "CONV_OK"
     assert B.conv_status_string(6) == "CONV_ERR_TIMEOUT"
