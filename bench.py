@@ -894,6 +894,17 @@ def dist_setup():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(vals, pg=None, device=None):
+    """Element-wise maximum of per-rank timings over the process group (the
+    slowest replica sets the step time); the values themselves without one."""
+    if pg is None:
+        return [float(v) for v in vals]
+    import torch
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
 def run_reference(args):
     """Reference arm: the oracle on the host cores, one bounded sample per step."""
     world, rank, _ = dist_setup()
@@ -1077,10 +1088,9 @@ def main():
     sampler.stop()
     clocks = sampler.summary(t_wall0 - 0.15, t_wall1 + 0.15)
 
-    ms_tensor = torch.tensor([dev_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if pg:
-        pg.all_reduce(ms_tensor, op=pg.ReduceOp.MAX)
-    dev_ms, e2e_ms = float(ms_tensor[0]), float(ms_tensor[1])
+    # replicas: every rank ran its own batch; the job's rate is all ranks' work
+    # over the slowest rank's time
+    dev_ms, e2e_ms = max_over_ranks([dev_ms, e2e_ms], pg, dev)
     step_ms = dev_ms / args.steps
     value = wl.value(step_ms) * world
     e2e_value = wl.value(e2e_ms) * world
