@@ -273,6 +273,10 @@ class ResNetLayer(Workload):
     def d2h(self):
         return [(self.y, self.yh)]
 
+    def e2e_path(self, args):
+        return (f"conv_fwd_host (pinned host tensors, chunks of {args.e2e_chunk} images: "
+                "copies overlap the convolution)")
+
     def host_step(self, args):
         # conv_fwd_host: x from pinned host memory, y back to it, in chunks of
         # images whose copies overlap the convolution
@@ -814,6 +818,43 @@ class ResNet50W(Workload):
             self.out = self.net.replay() if self.graph else self.net.forward(self.x)
         return [("resnet50_forward", run, self.net.flops(), 0, "tensor")]
 
+    def e2e_path(self, args):
+        if not self.graph:
+            return "copy in, the forward pass, logits out on one stream"
+        return ("each step's pinned host input copied on a copy stream into one of two "
+                "input buffers while the other buffer's graph runs; logits read back per step")
+
+    def host_step(self, args):
+        """End-to-end step with its input copied from pinned host memory: two input
+        buffers, each with its own graph, so the copy of step i+1's input (on a
+        copy stream) overlaps step i's forward pass; each step's logits are read
+        back after its forward pass."""
+        import torch
+        if not self.graph:
+            self.x.copy_(self.xh, non_blocking=True)
+            self.out = self.net.forward(self.x)
+            self.yh.copy_(self.out, non_blocking=True)
+            return
+        if not hasattr(self, "_pipe"):
+            x1 = torch.empty_like(self.x)
+            g1, o1 = self.net.capture_graph(x1)
+            self._pipe = dict(x=[self.x, x1], g=[None, g1], out=[None, o1],
+                              copy=torch.cuda.Stream(),
+                              done=[torch.cuda.Event(), torch.cuda.Event()],
+                              ready=[torch.cuda.Event(), torch.cuda.Event()], i=0)
+        p = self._pipe
+        s = p["i"] % 2
+        p["i"] += 1
+        cur = torch.cuda.current_stream()
+        with torch.cuda.stream(p["copy"]):
+            p["copy"].wait_event(p["done"][s])  # the graph that last read this buffer
+            p["x"][s].copy_(self.xh, non_blocking=True)
+            p["ready"][s].record(p["copy"])
+        cur.wait_event(p["ready"][s])
+        out = self.net.replay() if s == 0 else (p["g"][1].replay(), p["out"][1])[1]
+        p["done"][s].record(cur)
+        self.yh.copy_(out, non_blocking=True)
+
     def layer_breakdown(self, reps=5):
         """Per-layer device time from CUDA events between launch groups (median of
         `reps` forwards), with each conv's direct-equivalent TFLOP/s and algorithm."""
@@ -1174,9 +1215,7 @@ def main():
             "e2e": {"value": round(e2e_value, 3), "unit": wl.unit,
                     "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
                     "ms_per_step": round(e2e_ms, 4),
-                    "path": (f"conv_fwd_host (pinned host tensors, chunks of {args.e2e_chunk} "
-                             "images: copies overlap the convolution)"
-                             if hasattr(wl, "host_step") else
+                    "path": (wl.e2e_path(args) if hasattr(wl, "e2e_path") else
                              "copy in, the step's calls, copy out on one stream")},
             "gpu_launches": args.steps * count_launches(wl, groups),
             "roofline": roofline,

@@ -122,20 +122,27 @@ class ResNet50:
             self.algos[sp.name] = B.conv_algo_info(layer.desc, a)[1]
         self.tensors = {}
 
-    def capture(self, x_nchw: torch.Tensor) -> torch.Tensor:
-        """Record one forward pass of a fixed input buffer as a CUDA graph (the
-        library's calls only enqueue kernels: no allocation, no synchronization),
-        so each replay costs one graph launch instead of ~57 host-side launches.
-        Returns the output tensor that replay() refills."""
-        self._graph_x = x_nchw
+    def capture_graph(self, x_nchw: torch.Tensor):
+        """Record one forward pass of the fixed input buffer x_nchw as a CUDA
+        graph (the library's calls only enqueue kernels: no allocation, no
+        synchronization), so a replay costs one graph launch instead of ~57
+        host-side launches.  Returns (graph, output tensor a replay refills);
+        graphs over different input buffers are independent."""
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):  # warm the allocator outside the capture
-            self.forward(self._graph_x)
+            self.forward(x_nchw)
         torch.cuda.current_stream().wait_stream(side)
-        self._graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(self._graph):
-            self._graph_out = self.forward(self._graph_x)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            out = self.forward(x_nchw)
+        return graph, out
+
+    def capture(self, x_nchw: torch.Tensor) -> torch.Tensor:
+        """capture_graph() as this network's default graph; returns the output
+        tensor that replay() refills."""
+        self._graph_x = x_nchw
+        self._graph, self._graph_out = self.capture_graph(x_nchw)
         return self._graph_out
 
     def replay(self) -> torch.Tensor:
