@@ -1192,8 +1192,8 @@ def main():
         elif kname == "int8_igemm_mma":
             roofline["note"] = ("int8 runs on mma.sync (sm_103a has no tcgen05 int8 kind); the "
                                 "fraction is against the measured bf16 tensor peak")
-        cpu = None
-        if not args.no_cpu_baseline:
+        cpu = None  # the oracle's timing is a single-GPU figure: rank 0 at N = 1 only
+        if not args.no_cpu_baseline and world == 1:
             os.environ.setdefault("OMP_NUM_THREADS", str(cpu_cores()))
             cpu = cpu_baseline_sampled(wl, args)
         groups_out = {}
