@@ -74,4 +74,13 @@ def test_resnet50_cuda_graph_replay_matches_eager():
     got2 = net.replay()
     torch.cuda.synchronize()
     assert torch.equal(got2, eager2) and not torch.equal(got2, eager)
+    # a second, independent graph over another input buffer (the end-to-end
+    # bench alternates two): each replays its own buffer, back to back
+    xb = x.clone()
+    g2, out2 = net.capture_graph(xb)
+    net._graph_x.copy_(x2)
+    net.replay()
+    g2.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out2, eager) and torch.equal(net._graph_out, eager2)
     del out
