@@ -509,11 +509,11 @@ __global__ void __launch_bounds__(192, 1)
         // the low weight nibbles, then 64 against the high parts, all exact
         // integers in fp32; t = 16 * hi + lo + bias, requantised to int8 (the
         // MegEngine Beta report's native int8 epilogue)
-#pragma unroll 1
         // this group's 64 biases and scales, staged once in the warp's (here
         // unused) staging box and read back as broadcasts
         int32_t* sbi = reinterpret_cast<int32_t*>(sEpi + q * 2 * C::EPI_BOX);
         float* ssc = reinterpret_cast<float*>(sbi + 64);
+#pragma unroll 1
         for (int g = 0; g < width / 128; ++g) {
           const int k0 = (nt * BN + noff + g * 128) / 2;  // first output channel of the group
           if (k0 >= p.i8_kout) break;
