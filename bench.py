@@ -25,10 +25,13 @@ Other workloads (--workload):
 Timing: W >= 3 untimed warm-up steps, then K steps; before every step the L2
 (129 MB) is flushed by writing a 256 MB buffer, outside the CUDA-event window
 that brackets the step's launches on the launching stream.  `value` is the
-workload's metric over all ranks; `e2e` is the same metric through the same
-calls with the step's input copied from pinned host memory and its output
-copied back inside the timed region; `cpu_baseline` is the fp64 / exact-int8
-oracle on this host's cores over a bounded sample of the same workload.
+workload's metric over all ranks; `e2e` is the same metric with every step's
+input copied from pinned host memory and its output copied back inside the
+timed region (the headline layer through conv_fwd_host, whose chunked copies
+overlap the convolution; resnet50 with the next step's input copy overlapping
+the current forward pass; the others copy in, run, copy out on one stream);
+`cpu_baseline` is the fp64 / exact-int8 oracle on this host's cores over a
+bounded sample of the same workload, repeated to about 10 s (N = 1 only).
 
 --impl reference times the oracle itself (the reference arm of this metric).
 """
