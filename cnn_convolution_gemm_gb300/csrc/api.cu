@@ -440,6 +440,33 @@ static conv_status_t check_algo(const gbconv_desc_s& d, int algo) {
   return CONV_OK;
 }
 
+// Split-K for the bf16 implicit GEMMs (groups == 1): when the output tiles
+// (128 rows x the algorithm's BN columns) fill at most half the SMs and the
+// reduction has at least 16 k-steps, cut it into ranges of at least 4 k-steps,
+// as many as the idle SMs allow, each written as fp32 partial products, then
+// summed with the epilogue by a second kernel.  The plan depends only on the
+// layer and the device, so the workspace size and the forward call agree;
+// a forward given less workspace than the plan needs runs unsplit.
+struct IgemmSplitPlan {
+  int ksplit = 1, kchunk = 0;
+  size_t bytes = 0;
+};
+static IgemmSplitPlan igemm_split_plan(const gbconv_desc_s& d, int a) {
+  IgemmSplitPlan pl;
+  if (d.groups != 1 || d.dtype != CONV_BF16 || d.x_cstride || d.y_kstride) return pl;
+  const long long M = (long long)d.N * d.OH * d.OW;
+  const long long tiles = gb_ceil_div_ll(M, 128) * gb_ceil_div(d.K, igemm_block_n(a));
+  const int kiters = igemm_kiters(d);
+  const int sms = gb_num_sms();
+  if (kiters < 16 || tiles * 2 > sms) return pl;
+  const int ks = (int)std::min<long long>(sms / tiles, kiters / 4);
+  if (ks < 2) return pl;
+  pl.kchunk = gb_ceil_div(kiters, ks);
+  pl.ksplit = gb_ceil_div(kiters, pl.kchunk);
+  pl.bytes = (size_t)pl.ksplit * M * d.K * 4;
+  return pl;
+}
+
 extern "C" conv_status_t conv_workspace_size(conv_desc_t d, conv_algo_t algo, size_t* bytes) {
   if (!d || !bytes) return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
   const int a = resolve(*d, algo);
@@ -453,6 +480,8 @@ extern "C" conv_status_t conv_workspace_size(conv_desc_t d, conv_algo_t algo, si
   if (a == CONV_ALGO_STEM_S2D) *bytes = stem_s2d_workspace_bytes(*d);
   if (a == CONV_ALGO_STEM_S2D4) *bytes = stem_s2d4_workspace_bytes(*d);
   if (a == CONV_ALGO_INT8_WINO_F2) *bytes = int8_wino_workspace_bytes(*d);
+  if (a == CONV_ALGO_IGEMM_N64 || a == CONV_ALGO_IGEMM_N128 || a == CONV_ALGO_IGEMM_N256)
+    *bytes = igemm_split_plan(*d, a).bytes;
   return ok_status();
 }
 
@@ -554,6 +583,19 @@ static conv_status_t fwd_impl(const gbconv_desc_s& d, const void* x, const void*
     case CONV_ALGO_IGEMM_N64:
     case CONV_ALGO_IGEMM_N128:
     case CONV_ALGO_IGEMM_N256: {  // one launch per group over strided channel views
+      const IgemmSplitPlan pl = igemm_split_plan(d, a);
+      if (pl.ksplit > 1 && ws && ws_bytes >= pl.bytes && aligned16(ws)) {
+        IgemmSplit sp;
+        sp.ksplit = pl.ksplit;
+        sp.kchunk = pl.kchunk;
+        sp.part = static_cast<float*>(ws);
+        e = launch_igemm_bf16(d, igemm_block_n(a), x, wpack, nullptr, nullptr, y, err, wait_ns, s,
+                              sp);
+        if (e == cudaSuccess)
+          e = launch_splitk_reduce_bf16(d, pl.ksplit, ws, static_cast<const float*>(bias), res, y,
+                                        s);
+        break;
+      }
       const gbconv_desc_s v = group_view(d);
       const size_t wg = igemm_group_packed_bytes(v);
       for (int g = 0; g < d.groups && e == cudaSuccess; ++g)

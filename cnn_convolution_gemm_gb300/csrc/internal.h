@@ -92,6 +92,12 @@ struct IgemmSplit {
   int s2d4_k = 0;
 };
 int igemm_kiters(const gbconv_desc_s& d);
+// Sums part[ksplit][N*OH*OW][K] (fp32, the split-K GEMM's products) and applies
+// d's epilogue (+ bias, + residual, act) into bf16 NHWC y.  K % 8 == 0; part, res
+// and y 16-byte aligned.
+cudaError_t launch_splitk_reduce_bf16(const gbconv_desc_s& d, int ksplit, const void* part,
+                                      const float* bias, const void* res, void* y,
+                                      cudaStream_t st);
 cudaError_t launch_igemm_bf16(const gbconv_desc_s& d, int block_n, const void* x,
                               const void* wpack, const float* bias, const void* res, void* y,
                               int* err, unsigned long long wait_ns, cudaStream_t st,

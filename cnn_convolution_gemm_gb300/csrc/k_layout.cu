@@ -50,6 +50,45 @@ __global__ void nchw_f32_to_nhwc_bf16_kernel(const float* __restrict__ x,
   }
 }
 
+// Four consecutive pixels per thread when rows hold a multiple of four pixels
+// and both tensors are 16-byte aligned: one 16-byte load per input plane
+// (coalesced across the warp), C_OUT * 8 contiguous bytes stored as 16-byte
+// vectors.  Grid-stride over the pixel quads, so every SM keeps several
+// thousand bytes of loads in flight; the rounding is the same as above.
+template <int C_OUT>
+__global__ void nchw_f32_to_nhwc_bf16_quad_kernel(const float* __restrict__ x,
+                                                  __nv_bfloat16* __restrict__ y, int C,
+                                                  long long hw, long long quads) {
+  for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < quads;
+       q += (long long)gridDim.x * blockDim.x) {
+    const long long p = q * 4;
+    const long long n = p / hw;
+    const float* src = x + n * C * hw + (p - n * hw);
+    float v[C_OUT][4];
+#pragma unroll
+    for (int c = 0; c < C_OUT; ++c) {
+      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c < C) f = __ldg(reinterpret_cast<const float4*>(src + c * hw));
+      v[c][0] = f.x;
+      v[c][1] = f.y;
+      v[c][2] = f.z;
+      v[c][3] = f.w;
+    }
+    uint32_t o[2 * C_OUT];  // pixel-major, channel pairs
+#pragma unroll
+    for (int px = 0; px < 4; ++px)
+#pragma unroll
+      for (int c = 0; c < C_OUT; c += 2) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(v[c][px], v[c + 1][px]);
+        o[(px * C_OUT + c) / 2] = *reinterpret_cast<uint32_t*>(&b);
+      }
+    uint4* dst = reinterpret_cast<uint4*>(y + p * C_OUT);
+#pragma unroll
+    for (int i = 0; i < C_OUT / 2; ++i)
+      dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+  }
+}
+
 __global__ void nhwc_bf16_to_nchw_f32_kernel(const __nv_bfloat16* __restrict__ x,
                                              float* __restrict__ y, int N, int C, int H, int W,
                                              int C_in) {
@@ -105,18 +144,64 @@ __global__ void maxpool_nhwc_bf16_kernel(const __nv_bfloat16* __restrict__ x,
   }
 }
 
-// Global average pooling: one thread per (n, 8-channel vector), fp32 sum.
-__global__ void avgpool_nhwc_bf16_kernel(const __nv_bfloat16* __restrict__ x,
-                                         __nv_bfloat16* __restrict__ y, int N, int C, int HW) {
+// 3x3 max pooling (ResNet's 3x3 / stride 2), same thread mapping as above with
+// the window unrolled: the nine 16-byte loads of a thread are issued together
+// (taps outside the image read as -inf), and the maximum is taken on the bf16
+// pairs directly (a maximum of bf16 values is one of them, so no widening).
+__global__ void maxpool3_nhwc_bf16_kernel(const __nv_bfloat16* __restrict__ x,
+                                          __nv_bfloat16* __restrict__ y, int N, int C, int H,
+                                          int W, int stride, int pad, int OH, int OW) {
   const int cv = C / 8;
-  const long long total = (long long)N * cv;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int c8 = (int)(i % cv);
-    const long long n = i / cv;
-    float s[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int p = 0; p < HW; ++p) {
-      const uint4 v = *reinterpret_cast<const uint4*>(x + (n * HW + p) * C + c8 * 8);
+  const int item = blockIdx.x * blockDim.x + threadIdx.x;
+  if (item >= OW * cv) return;
+  const int ow = item / cv, c8 = item - ow * cv;
+  const uint4 ninf = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+  for (int row = blockIdx.y; row < N * OH; row += gridDim.y) {
+    const int n = row / OH, oh = row - n * OH;
+    uint4 v[9];
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+      const int ih = oh * stride - pad + r;
+#pragma unroll
+      for (int s = 0; s < 3; ++s) {
+        const int iw = ow * stride - pad + s;
+        v[r * 3 + s] = ninf;
+        if (ih >= 0 && ih < H && iw >= 0 && iw < W)
+          v[r * 3 + s] = __ldg(reinterpret_cast<const uint4*>(
+              x + (((long long)n * H + ih) * W + iw) * C + c8 * 8));
+      }
+    }
+    uint4 m = v[0];
+    __nv_bfloat162* mb = reinterpret_cast<__nv_bfloat162*>(&m);
+#pragma unroll
+    for (int t = 1; t < 9; ++t) {
+      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v[t]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mb[j] = __hmax2(mb[j], b[j]);
+    }
+    reinterpret_cast<uint4*>(y)[(long long)row * OW * cv + item] = m;
+  }
+}
+
+// Global average pooling.  A block covers one image and 32 consecutive
+// 8-channel vectors; its 8 warps take every 8th pixel (a warp reads 512
+// contiguous bytes per pixel), each thread keeps fp32 sums of its 8 channels,
+// and the 8 partial sums meet in shared memory, added in warp order.
+constexpr int kPoolParts = 8;
+__global__ void __launch_bounds__(32 * kPoolParts)
+    avgpool_nhwc_bf16_kernel(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ y,
+                             int C, int HW, int groups_per_image) {
+  __shared__ float4 part[kPoolParts][32][2];
+  const int cv = C / 8;
+  const int n = blockIdx.x / groups_per_image;
+  const int c8 = (blockIdx.x - n * groups_per_image) * 32 + (threadIdx.x & 31);
+  const int slice = threadIdx.x >> 5;
+  float s[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (c8 < cv) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (long long)n * HW * C) + c8;
+#pragma unroll 4
+    for (int p = slice; p < HW; p += kPoolParts) {
+      const uint4 v = __ldg(src + (long long)p * cv);
       const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -125,13 +210,23 @@ __global__ void avgpool_nhwc_bf16_kernel(const __nv_bfloat16* __restrict__ x,
         s[2 * j + 1] += f.y;
       }
     }
-    const float inv = 1.0f / (float)HW;
-    uint4 o;
-    __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) ob[j] = __floats2bfloat162_rn(s[2 * j] * inv, s[2 * j + 1] * inv);
-    *reinterpret_cast<uint4*>(y + n * C + c8 * 8) = o;
   }
+  part[slice][threadIdx.x & 31][0] = make_float4(s[0], s[1], s[2], s[3]);
+  part[slice][threadIdx.x & 31][1] = make_float4(s[4], s[5], s[6], s[7]);
+  __syncthreads();
+  if (slice != 0 || c8 >= cv) return;
+  float t[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int q = 0; q < kPoolParts; ++q) {
+    const float4 a = part[q][threadIdx.x][0], b = part[q][threadIdx.x][1];
+    t[0] += a.x; t[1] += a.y; t[2] += a.z; t[3] += a.w;
+    t[4] += b.x; t[5] += b.y; t[6] += b.z; t[7] += b.w;
+  }
+  const float inv = 1.0f / (float)HW;
+  uint4 o;
+  __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) ob[j] = __floats2bfloat162_rn(t[2 * j] * inv, t[2 * j + 1] * inv);
+  *reinterpret_cast<uint4*>(y + (long long)n * C + c8 * 8) = o;
 }
 
 __device__ __forceinline__ uint32_t hash32(uint32_t v) {
@@ -163,6 +258,20 @@ __global__ void fill_random_kernel(uint8_t* p, long long n, int elem_bytes, uint
 
 cudaError_t launch_nchw_f32_to_nhwc_bf16(const float* x, void* y, int N, int C, int H, int W,
                                          int C_out, cudaStream_t st) {
+  const long long hw = (long long)H * W;
+  if (W % 4 == 0 && C <= C_out && (C_out == 4 || C_out == 8) &&
+      ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15) == 0) {
+    const long long quads = (long long)N * hw / 4;
+    const int grid = (int)std::min<long long>(gb_ceil_div_ll(quads, kBlock), 8LL * gb_num_sms());
+    if (C_out == 4)
+      nchw_f32_to_nhwc_bf16_quad_kernel<4><<<grid, kBlock, 0, st>>>(
+          x, static_cast<__nv_bfloat16*>(y), C, hw, quads);
+    else
+      nchw_f32_to_nhwc_bf16_quad_kernel<8><<<grid, kBlock, 0, st>>>(
+          x, static_cast<__nv_bfloat16*>(y), C, hw, quads);
+    gb_count_launch();
+    return cudaGetLastError();
+  }
   if ((long long)N * H >= (1LL << 31)) return cudaErrorInvalidValue;
   const dim3 grid((unsigned)gb_ceil_div(W, 128), (unsigned)std::min(N * H, 65535));
   nchw_f32_to_nhwc_bf16_kernel<<<grid, 128, 0, st>>>(x, static_cast<__nv_bfloat16*>(y), N, C, H,
@@ -185,17 +294,25 @@ cudaError_t launch_maxpool_nhwc_bf16(const void* x, void* y, int N, int C, int H
   if ((long long)N * OH >= (1LL << 31) || (long long)OW * (C / 8) >= (1LL << 31))
     return cudaErrorInvalidValue;
   const dim3 grid((unsigned)gb_ceil_div(OW * (C / 8), kBlock), (unsigned)std::min(N * OH, 65535));
-  maxpool_nhwc_bf16_kernel<<<grid, kBlock, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), N, C, H, W, k, stride,
-      pad, OH, OW);
+  if (k == 3)
+    maxpool3_nhwc_bf16_kernel<<<grid, kBlock, 0, st>>>(static_cast<const __nv_bfloat16*>(x),
+                                                       static_cast<__nv_bfloat16*>(y), N, C, H, W,
+                                                       stride, pad, OH, OW);
+  else
+    maxpool_nhwc_bf16_kernel<<<grid, kBlock, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), N, C, H, W, k,
+        stride, pad, OH, OW);
   gb_count_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_avgpool_nhwc_bf16(const void* x, void* y, int N, int C, int H, int W,
                                      cudaStream_t st) {
-  avgpool_nhwc_bf16_kernel<<<grid_for((long long)N * (C / 8)), kBlock, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), N, C, H * W);
+  const int groups = gb_ceil_div(C / 8, 32);
+  if ((long long)N * groups >= (1LL << 31) || (long long)H * W >= (1LL << 31))
+    return cudaErrorInvalidValue;
+  avgpool_nhwc_bf16_kernel<<<N * groups, 32 * kPoolParts, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), C, H * W, groups);
   gb_count_launch();
   return cudaGetLastError();
 }

@@ -100,10 +100,13 @@ def test_layout_conversion_bit_exact():
     assert np.array_equal(back.cpu().numpy(), ol.round_bf16(x))
 
 
-@pytest.mark.parametrize("C,C_out,W", [(3, 4, 224), (3, 4, 130), (4, 4, 9), (3, 8, 300)])
+@pytest.mark.parametrize("C,C_out,W", [(3, 4, 224), (3, 4, 130), (4, 4, 9), (3, 8, 300),
+                                        (1, 4, 16), (8, 8, 12), (5, 8, 6)])
 def test_layout_conversion_image_channels(C, C_out, W):
     """An RGB image padded to 4 (the 4x4 space-to-depth stem's input) or 8
-    channels, rows wider than one 128-thread block included."""
+    channels, rows wider than one 128-thread block included; row widths that
+    are multiples of 4 take the four-pixels-per-thread path, the others the
+    pixel-per-thread one."""
     torch = need_gpu()
     from cnn_convolution_gemm_gb300 import binding as B
     dev = torch.device("cuda:0")
@@ -142,3 +145,40 @@ def test_pooling():
     assert np.array_equal(y2.double().cpu().numpy(), ref2)
     aref = ol.global_avgpool(nhwc_to_nchw(x.double().numpy()))
     np.testing.assert_allclose(a.double().cpu().numpy(), aref, rtol=1e-2, atol=1e-2)
+
+
+@pytest.mark.parametrize("k,stride,pad,H,W", [(3, 2, 1, 13, 11), (3, 1, 1, 9, 10), (3, 2, 0, 12, 12),
+                                              (2, 2, 0, 12, 10), (2, 1, 1, 7, 5), (5, 3, 2, 17, 13)])
+def test_maxpool_window_shapes(k, stride, pad, H, W):
+    """The unrolled 3x3 window (any stride and padding) and the generic loop
+    (other window sizes) against the oracle, with taps off every edge."""
+    torch = need_gpu()
+    from cnn_convolution_gemm_gb300 import binding as B
+    dev = torch.device("cuda:0")
+    g = np.random.default_rng(k * 100 + stride * 10 + pad)
+    x = torch.from_numpy(g.standard_normal((2, H, W, 24)).astype(np.float32)).to(torch.bfloat16)
+    OH, OW = (H + 2 * pad - k) // stride + 1, (W + 2 * pad - k) // stride + 1
+    y = torch.empty((2, OH, OW, 24), dtype=torch.bfloat16, device=dev)
+    B.conv_maxpool2d_nhwc_bf16(x.to(dev).data_ptr(), y.data_ptr(), 2, 24, H, W, k, stride, pad,
+                               None)
+    torch.cuda.synchronize()
+    ref = nchw_to_nhwc(ol.maxpool2d(nhwc_to_nchw(x.double().numpy()), k, stride, pad))
+    assert np.array_equal(y.double().cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("N,C,H,W", [(4, 2048, 7, 7), (3, 264, 5, 9), (2, 8, 1, 1),
+                                     (1, 64, 31, 17)])
+def test_global_avgpool_shapes(N, C, H, W):
+    """ResNet-50's 7x7 x 2048 pool, a channel count that leaves a partial group
+    of 32 vectors, a single pixel, and more pixels than the 8 slices x 4."""
+    torch = need_gpu()
+    from cnn_convolution_gemm_gb300 import binding as B
+    dev = torch.device("cuda:0")
+    g = np.random.default_rng(N * 1000 + C)
+    x = torch.from_numpy(g.standard_normal((N, H, W, C)).astype(np.float32)).to(torch.bfloat16)
+    a = torch.full((N, C), 9.0, dtype=torch.bfloat16, device=dev)
+    B.conv_global_avgpool_nhwc_bf16(x.to(dev).data_ptr(), a.data_ptr(), N, C, H, W, None)
+    torch.cuda.synchronize()
+    ref = ol.global_avgpool(nhwc_to_nchw(x.double().numpy()))
+    # fp32 sums of bf16 values, one bf16 rounding of the mean
+    np.testing.assert_allclose(a.double().cpu().numpy(), ref, rtol=8e-3, atol=1e-3)
