@@ -141,7 +141,15 @@ conv_status_t conv_algo_info(conv_desc_t desc, int i, conv_algo_t* algo, const c
                              int* applicable);
 /* The algorithm CONV_ALGO_AUTO resolves to (Fast-Run map, else heuristic). */
 conv_status_t conv_algo_resolve(conv_desc_t desc, conv_algo_t* algo);
-/* Bytes of device workspace conv_fwd needs for (desc, algo); 0 if none. */
+/* Bytes of device workspace conv_fwd needs for (desc, algo); 0 if none.
+ * For the implicit-GEMM algorithms (CONV_ALGO_IGEMM_N64/128/256, groups 1) this
+ * is the split-K buffer: when the layer's output tiles (128 rows x the tile
+ * width) fill at most half the device's SMs and its reduction has 16 or more
+ * k-steps, the reduction is cut into ranges whose fp32 partial products
+ * (ksplit x N*OH*OW x K floats) are summed by a second kernel with the bias,
+ * residual and activation ([MegEngine] "Im2col+MatMul", the reduction axis of
+ * the product split).  There the workspace is optional: a conv_fwd given less
+ * runs the same algorithm unsplit.  The size depends on the device's SM count. */
 conv_status_t conv_workspace_size(conv_desc_t desc, conv_algo_t algo, size_t* bytes);
 /* Bytes of the packed weight buffer for (desc, algo). */
 conv_status_t conv_weights_packed_size(conv_desc_t desc, conv_algo_t algo, size_t* bytes);
