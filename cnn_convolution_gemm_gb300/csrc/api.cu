@@ -240,7 +240,7 @@ static const char* const kAlgoNames[CONV_ALGO_COUNT] = {
     "direct", "igemm_tc_n64", "igemm_tc_n128", "igemm_tc_n256",
     "winograd_f2x2_3x3", "winograd_f6x6_3x3", "depthwise3x3", "int8_igemm_mma",
     "int8_igemm_tc", "im2col_gemm", "stem_s2d_igemm", "igemm_tf32",
-    "int8_winograd_f2x2_3x3", "stem_s2d4_igemm"};
+    "int8_winograd_f2x2_3x3", "stem_s2d4_igemm", "igemm_tc_2sm_n256"};
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -256,6 +256,10 @@ static bool applicable(const gbconv_desc_s& d, int algo, const char** why) {
     case CONV_ALGO_DIRECT:
       if (d.dtype == CONV_INT8 && !d.scale) return *why = "int8 needs a requant scale", false;
       return true;
+    case CONV_ALGO_IGEMM_2SM:
+      if (d.groups != 1) return *why = "needs groups == 1", false;
+      if (d.C == 8) return *why = "8-channel inputs take the narrow tile mode", false;
+      [[fallthrough]];
     case CONV_ALGO_IGEMM_N64:
     case CONV_ALGO_IGEMM_N128:
     case CONV_ALGO_IGEMM_N256: {
@@ -515,6 +519,7 @@ extern "C" conv_status_t conv_weights_packed_size(conv_desc_t d, conv_algo_t alg
     case CONV_ALGO_IGEMM_N64:
     case CONV_ALGO_IGEMM_N128:
     case CONV_ALGO_IGEMM_N256:
+    case CONV_ALGO_IGEMM_2SM:
       *bytes = igemm_group_packed_bytes(group_view(*d)) * d->groups;
       break;
     case CONV_ALGO_INT8_MMA: *bytes = (size_t)d->K * d->R * d->S * Cp64; break;
@@ -543,7 +548,8 @@ extern "C" conv_status_t conv_weights_prepack(conv_desc_t d, conv_algo_t algo, c
   switch (a) {
     case CONV_ALGO_IGEMM_N64:
     case CONV_ALGO_IGEMM_N128:
-    case CONV_ALGO_IGEMM_N256: {  // per group: weights [Kg][R][S][Cg] -> the group's slice
+    case CONV_ALGO_IGEMM_N256:
+    case CONV_ALGO_IGEMM_2SM: {  // per group: weights [Kg][R][S][Cg] -> the group's slice
       const gbconv_desc_s v = group_view(*d);
       const size_t in_g = (size_t)v.K * v.R * v.S * v.C * 2, out_g = igemm_group_packed_bytes(v);
       for (int g = 0; g < d->groups && e == cudaSuccess; ++g)
@@ -607,6 +613,10 @@ static conv_status_t fwd_impl(const gbconv_desc_s& d, const void* x, const void*
             static_cast<__nv_bfloat16*>(y) + (size_t)g * v.K, err, wait_ns, s);
       break;
     }
+    case CONV_ALGO_IGEMM_2SM:
+      e = launch_igemm_bf16_pair(d, x, wpack, static_cast<const float*>(bias), res, y, err,
+                                 wait_ns, s);
+      break;
     case CONV_ALGO_DEPTHWISE:
       e = launch_dwconv3x3(d, x, wpack, static_cast<const float*>(bias), res, y, err, wait_ns, s);
       break;
@@ -1252,6 +1262,7 @@ static bool implemented(int algo) {
     case CONV_ALGO_IGEMM_N64:
     case CONV_ALGO_IGEMM_N128:
     case CONV_ALGO_IGEMM_N256:
+    case CONV_ALGO_IGEMM_2SM:
     case CONV_ALGO_DEPTHWISE:
     case CONV_ALGO_WINO_F2:
     case CONV_ALGO_WINO_F6:

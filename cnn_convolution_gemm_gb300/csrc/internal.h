@@ -92,6 +92,12 @@ struct IgemmSplit {
   int s2d4_k = 0;
 };
 int igemm_kiters(const gbconv_desc_s& d);
+// The 256 x 256-tile implicit GEMM over clusters of two CTAs (tcgen05
+// cta_group::2): bf16 NHWC, groups 1, C != 8; same packed weights as the
+// single-SM tiles.
+cudaError_t launch_igemm_bf16_pair(const gbconv_desc_s& d, const void* x, const void* wpack,
+                                   const float* bias, const void* res, void* y, int* err,
+                                   unsigned long long wait_ns, cudaStream_t st);
 // Sums part[ksplit][N*OH*OW][K] (fp32, the split-K GEMM's products) and applies
 // d's epilogue (+ bias, + residual, act) into bf16 NHWC y.  K % 8 == 0; part, res
 // and y 16-byte aligned.

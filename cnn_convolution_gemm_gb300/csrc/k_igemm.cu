@@ -26,6 +26,16 @@
 //               box) moves in full 128-byte lines
 // The accumulator is double-buffered in TMEM (2 x BN columns) so the
 // epilogue of tile i overlaps the MMAs of tile i+1.
+//
+// Pair mode (PAIR, BN = 256): the grid is made of clusters of two CTAs on two
+// SMs, and each work unit is a 256-row x 256-column tile.  Each CTA loads its
+// own 128 rows of A and one half (128 rows) of B, so every SM moves and its
+// tensor core reads 32 KB of shared memory per 64-wide k-step instead of 48 KB
+// (a single SM's 128 x 256 MMA needs more shared-memory bandwidth than the SM
+// has).  The even CTA's MMA thread issues tcgen05.mma.cta_group::2 (M = 256)
+// over both CTAs' operands; its commits are multicast to both CTAs' barriers;
+// both CTAs' loads complete on the even CTA's stage barrier; each CTA's
+// epilogue drains the accumulator rows of its own A half from its own TMEM.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -83,13 +93,14 @@ enum { MODE_CONV = 0, MODE_BATCHED = 1 };
 
 // LIGHT: a shallow ring (for short reductions) so two CTAs fit on one SM and
 // the epilogue, which bounds memory-bound layers, gets twice the warps.
-template <int BN, bool LIGHT = false>
+// PAIR: each CTA holds half of B (see the pair mode above).
+template <int BN, bool LIGHT = false, bool PAIR = false>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES =
-      LIGHT ? (BN >= 128 ? 2 : 3) : ((BN >= 256) ? 4 : (BN >= 128 ? 6 : 8));
+      PAIR ? 6 : (LIGHT ? (BN >= 128 ? 2 : 3) : ((BN >= 256) ? 4 : (BN >= 128 ? 6 : 8)));
   static constexpr uint32_t TMEM_COLS = 2 * BN;  // double-buffered fp32 accumulator
   // epilogue staging: per epilogue warp two 32-row x 64-column bf16 boxes
   // (128-byte swizzle), written by the warp and stored by TMA
@@ -179,13 +190,14 @@ __device__ __forceinline__ float act_apply(float v, int act) {
 
 // TF32: fp32 NHWC tensors, kind::tf32 MMAs; a 128-byte swizzle row then holds
 // 32 channels (BKE) instead of 64 and each MMA still advances 32 bytes of K.
-template <int BN, int MODE, bool LIGHT = false, bool TF32 = false>
+template <int BN, int MODE, bool LIGHT = false, bool TF32 = false, bool PAIR = false>
 __global__ void __launch_bounds__(192, 1)
     igemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                          const __grid_constant__ CUtensorMap tm_w,
                          const __grid_constant__ CUtensorMap tm_y,
                          const __grid_constant__ CUtensorMap tm_r, const IgemmParams p) {
-  using C = Cfg<BN, LIGHT>;
+  using C = Cfg<BN, LIGHT, PAIR>;
+  static_assert(!PAIR || (BN == 256 && MODE == MODE_CONV && !LIGHT && !TF32), "pair mode");
   constexpr int BKE = TF32 ? 32 : BK;  // channels per k-step (one 128-byte row)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -204,6 +216,11 @@ __global__ void __launch_bounds__(192, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // pair mode: this CTA's rank in its pair (0 issues the MMAs), and the CTA's
+  // work-unit stride over the clusters
+  const uint32_t rank = PAIR ? gb::cluster_ctarank() : 0u;
+  const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int ustep = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -212,7 +229,8 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int b = 0; b < 2; ++b) {
       gb::mbar_init(&tfull[b], 1);
-      gb::mbar_init(&tempty[b], 128);
+      // pair mode: one arrival per epilogue warp of each CTA (on the even CTA's)
+      gb::mbar_init(&tempty[b], PAIR ? 8 : 128);
     }
     gb::mbar_init(mma_done, 1);
     for (int i = 0; i < 8; ++i) gb::mbar_init(&rbar[i], 1);
@@ -223,11 +241,18 @@ __global__ void __launch_bounds__(192, 1)
     if (MODE == MODE_CONV && p.res) gb::tma_prefetch_desc(&tm_r);
   }
   if (warp == 0) {
-    gb::tmem_alloc(tmem_slot, C::TMEM_COLS);
-    gb::tmem_relinquish();
+    if constexpr (PAIR) {
+      gb::tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+      gb::tmem_relinquish_pair();
+    } else {
+      gb::tmem_alloc(tmem_slot, C::TMEM_COLS);
+      gb::tmem_relinquish();
+    }
   }
   gb::tc_fence_before();
   __syncthreads();
+  // pair mode: both CTAs' barriers are initialised before either signals the other's
+  if constexpr (PAIR) gb::cluster_sync();
   gb::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // Programmatic dependent launch: the next kernel on the stream may start its
@@ -242,6 +267,11 @@ __global__ void __launch_bounds__(192, 1)
   // work unit u -> tile t, first output column offset within the tile, width
   const int num_units =
       p.tail_start < num_tiles ? p.tail_start + 2 * (num_tiles - p.tail_start) : num_tiles;
+  // the 128-row M tile this CTA covers in tile tt of a batch (pair mode: the
+  // unit's 256 rows are two M tiles, the even CTA's first)
+  auto m_tile = [&](int tt) {
+    return PAIR ? (tt / p.n_tiles) * 2 + (int)rank : tt / p.n_tiles;
+  };
   auto decode = [&](int u, int& t, int& noff, int& width) {
     if (u < p.tail_start) {
       t = u;
@@ -262,12 +292,14 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t phase = 0;
       long long issued = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      // pair mode: the even CTA's stage barriers, where both CTAs' loads complete
+      const uint32_t full_pair = PAIR ? gb::mapa_shared(gb::smem_u32(full), 0) : 0u;
+      for (int u = unit0; u < num_units && ok; u += ustep) {
         int t, noff, width;
         decode(u, t, noff, width);
         const int bt = t / tiles_per_batch;
         const int tt = t % tiles_per_batch;
-        const int mt = tt / p.n_tiles, nt = tt % p.n_tiles;
+        const int mt = m_tile(tt), nt = tt % p.n_tiles;
         const int m0 = mt * BM;  // M < 2^31 (checked on the host): 32-bit index math
         int img = 0, h0 = 0, w0 = 0;
         if (MODE == MODE_CONV) {
@@ -285,6 +317,20 @@ __global__ void __launch_bounds__(192, 1)
             ok = false;
             break;
           }
+          if constexpr (PAIR) {
+            // both CTAs' A tiles and B halves (width / 2 rows each) land on the even
+            // CTA's barrier, which alone expects their bytes
+            if (rank == 0)
+              gb::mbar_arrive_expect_tx(&full[stage], 2 * C::A_BYTES + width * BK * 2);
+            const uint32_t fb = full_pair + stage * 8;
+            gb::tma_load_im2col_4d_pair(sA + stage * C::A_BYTES, &tm_x, fb, cb * BKE, w0, h0, img,
+                                        (uint16_t)(s * p.dil), (uint16_t)(r * p.dil));
+            const int kcol = (r * p.S + s) * p.cblocks * BKE + cb * BKE;
+            const int n0 = nt * BN + noff + (int)rank * (width / 2);
+            for (int b = 0; b < width / 128; ++b)  // 64-row boxes
+              gb::tma_load_2d_pair(sB + stage * C::B_BYTES + b * 64 * 128, &tm_w, fb, kcol,
+                                   n0 + b * 64);
+          } else {
           gb::mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
           if (MODE == MODE_CONV && p.narrow) {
 #pragma unroll 1
@@ -307,6 +353,7 @@ __global__ void __launch_bounds__(192, 1)
             gb::tma_load_3d(sA + stage * C::A_BYTES, &tm_x, &full[stage], cb * BK, (int)m0, bt);
             gb::tma_load_3d(sB + stage * C::B_BYTES, &tm_w, &full[stage], cb * BK, nt * BN, bt);
           }
+          }
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -322,8 +369,11 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       // Drain: wait until the last loads this thread issued have landed, so no
-      // copy into shared memory is in flight when the block exits.
+      // copy into shared memory is in flight when the block exits (pair mode:
+      // the even CTA's barriers count both CTAs' bytes, so it drains for both,
+      // before the cluster barrier that precedes either CTA's exit).
       long long pending = issued < C::STAGES ? issued : C::STAGES;
+      if (PAIR && rank != 0) pending = 0;
       int st = stage;
       uint32_t ph = phase;
       for (long long i = 0; i < pending; ++i) {
@@ -335,18 +385,19 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       // ---------------- MMA issuer ----------------
-      const uint32_t IDESC = gb::idesc_f16(BM, BN, TF32 ? 2 : (MODE == MODE_CONV ? 1 : p.ab_type));
+      constexpr int MM = PAIR ? 2 * BM : BM;  // pair: M spans both CTAs' A tiles
+      const uint32_t IDESC = gb::idesc_f16(MM, BN, TF32 ? 2 : (MODE == MODE_CONV ? 1 : p.ab_type));
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      for (int u = unit0; u < num_units && ok; u += ustep) {
         int t, noff, width;
         decode(u, t, noff, width);
-        const uint32_t idesc_u = width == BN ? IDESC : gb::idesc_f16(BM, BN / 2, TF32 ? 2 : 1);
+        const uint32_t idesc_u = width == BN ? IDESC : gb::idesc_f16(MM, BN / 2, TF32 ? 2 : 1);
         if (!gb::mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, p.wait_ns, p.err)) break;
         gb::tc_fence_after();
         const uint32_t d = tmem_base + acc * BN;
@@ -372,25 +423,37 @@ __global__ void __launch_bounds__(192, 1)
             if constexpr (TF32)
               gb::tc_mma_tf32(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), idesc_u,
                               (it > kbeg || k > 0) ? 1u : 0u);
+            else if constexpr (PAIR)
+              gb::tc_mma_f16_pair(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), idesc_u,
+                                  (it > kbeg || k > 0) ? 1u : 0u);
             else
               gb::tc_mma_f16(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), idesc_u,
                              (it > kbeg || k > 0) ? 1u : 0u);
           }
-          gb::tc_commit(&empty[stage]);
+          if constexpr (PAIR)
+            gb::tc_commit_pair_multicast(&empty[stage], 0x3);  // both CTAs' stage is free
+          else
+            gb::tc_commit(&empty[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        gb::tc_commit(&tfull[acc]);
+        if constexpr (PAIR)
+          gb::tc_commit_pair_multicast(&tfull[acc], 0x3);
+        else
+          gb::tc_commit(&tfull[acc]);
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1;
         }
       }
       // All MMAs issued by this thread have completed once mma_done fires.
-      gb::tc_commit(mma_done);
+      if constexpr (PAIR)
+        gb::tc_commit_pair_multicast(mma_done, 0x1);
+      else
+        gb::tc_commit(mma_done);
       gb::mbar_wait_bounded(mma_done, 0, p.wait_ns, p.err);
     }
   } else {
@@ -414,7 +477,7 @@ __global__ void __launch_bounds__(192, 1)
       int t, noff, width;
       decode(u, t, noff, width);
       const int tt = t % tiles_per_batch;
-      const int mt2 = tt / p.n_tiles, nt2 = tt % p.n_tiles;
+      const int mt2 = m_tile(tt), nt2 = tt % p.n_tiles;
       uint64_t* bar = &rbar[q * 2 + b];
       gb::mbar_arrive_expect_tx(bar, C::EPI_BOX);
       asm volatile(
@@ -438,19 +501,21 @@ __global__ void __launch_bounds__(192, 1)
       return bv;
     };
     float2 bias_next = make_float2(0.f, 0.f);
-    if (!TF32 && MODE == MODE_CONV && !p.i8_y && !p.part && (int)blockIdx.x < num_units)
-      bias_next = bias_pair(blockIdx.x, 0);
+    if (!TF32 && MODE == MODE_CONV && !p.i8_y && !p.part && unit0 < num_units)
+      bias_next = bias_pair(unit0, 0);
     int pending = -1;  // box with a residual load not yet waited for
-    if (has_res && (int)blockIdx.x < num_units) {
-      if (lane == 0) fetch_res(blockIdx.x, 0, 0);
+    if (has_res && unit0 < num_units) {
+      if (lane == 0) fetch_res(unit0, 0, 0);
       pending = 0;
     }
-    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+    // pair mode: the even CTA's accumulator-free barriers
+    const uint32_t tempty_pair = PAIR ? gb::mapa_shared(gb::smem_u32(tempty), 0) : 0u;
+    for (int u = unit0; u < num_units; u += ustep) {
       int t, noff, width;
       decode(u, t, noff, width);
       const int bt = t / tiles_per_batch;
       const int tt = t % tiles_per_batch;
-      const int mt = tt / p.n_tiles, nt = tt % p.n_tiles;
+      const int mt = m_tile(tt), nt = tt % p.n_tiles;
       if (!gb::mbar_wait_bounded(&tfull[acc], acc_phase, p.wait_ns, p.err)) break;
       gb::tc_fence_after();
       const long long m = (long long)mt * BM + q * 32 + lane;
@@ -597,7 +662,7 @@ __global__ void __launch_bounds__(192, 1)
             // store that last read that box is done with it
             int tn = u, jn = j + 1;
             if (jn >= ns) {
-              tn = u + gridDim.x;
+              tn = u + ustep;
               jn = 0;
             }
             if (tn < num_units) {
@@ -627,7 +692,7 @@ __global__ void __launch_bounds__(192, 1)
           {
             int tn = u, jn = j + 1;
             if (jn >= ns) {
-              tn = u + gridDim.x;
+              tn = u + ustep;
               jn = 0;
             }
             if (tn < num_units) bias_next = bias_pair(tn, jn);
@@ -666,7 +731,17 @@ __global__ void __launch_bounds__(192, 1)
         (void)row_ok;
       }
       gb::tc_fence_before();
-      gb::mbar_arrive(&tempty[acc]);
+      if constexpr (PAIR) {
+        __syncwarp();  // every lane's accumulator reads are complete
+        if (lane == 0) {
+          if (rank == 0)
+            gb::mbar_arrive(&tempty[acc]);
+          else
+            gb::mbar_arrive_cluster(tempty_pair + acc * 8);
+        }
+      } else {
+        gb::mbar_arrive(&tempty[acc]);
+      }
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1;
@@ -682,9 +757,15 @@ __global__ void __launch_bounds__(192, 1)
 
   gb::tc_fence_before();
   __syncthreads();
+  // pair mode: neither CTA frees its TMEM or exits while the even CTA's MMAs,
+  // commits or drain may still touch the other's shared memory or TMEM
+  if constexpr (PAIR) gb::cluster_sync();
   if (warp == 0) {
     gb::tc_fence_after();
-    gb::tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if constexpr (PAIR)
+      gb::tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else
+      gb::tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
@@ -703,11 +784,39 @@ __global__ void pack_igemm_weights_kernel(const __nv_bfloat16* __restrict__ w,
   }
 }
 
-template <int BN, bool LIGHT, bool TF32 = false>
+// Clusters of two CTAs of the pair-mode kernel that fit on the device at once
+// (a cluster needs two SMs of one GPU processing cluster); 0 if none.
+template <int BN>
+int pair_max_clusters(int smem) {
+  static int cached[8] = {-1, -1, -1, -1, -1, -1, -1, -1};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 8) return 0;
+  if (cached[dev] >= 0) return cached[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(gb_num_sms() & ~1));
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(
+          &n, igemm_bf16_tc_kernel<BN, MODE_CONV, false, false, true>, &cfg) != cudaSuccess)
+    n = 0;
+  cudaGetLastError();  // clear a failed query
+  cached[dev] = n;
+  return n;
+}
+
+template <int BN, bool LIGHT, bool TF32 = false, bool PAIR = false>
 cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, const float* bias,
                       const void* res, void* y, int* err, unsigned long long wait_ns,
                       cudaStream_t st, const IgemmSplit& split) {
-  using Cf = Cfg<BN, LIGHT>;
+  using Cf = Cfg<BN, LIGHT, PAIR>;
   constexpr int BKE = TF32 ? 32 : BK;  // channels per k-step
   constexpr int ES = TF32 ? 4 : 2;     // element bytes
   const CUtensorMapDataType DT =
@@ -732,6 +841,7 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   p.Kw = narrow ? p.kiters * BK : d.R * d.S * Cp;
   p.M = (long long)d.N * d.OH * d.OW;
   p.m_tiles = (int)gb_ceil_div_ll(p.M, BM);
+  if (PAIR) p.m_tiles = gb_ceil_div(p.m_tiles, 2);  // 256-row units
   p.n_tiles = gb_ceil_div(d.K, BN);
   p.act = d.act;
   p.bias = bias;
@@ -755,6 +865,7 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   if (p.s2d4_k && (TF32 || res || p.i8_y || p.ksplit != 1 || p.s2d4_k != 64 ||
                    d.K != 4 * p.s2d4_k || d.OW % 8))
     return cudaErrorInvalidValue;
+  if (PAIR && (narrow || p.ksplit != 1 || p.part || p.i8_y || p.s2d4_k)) return cudaErrorInvalidValue;
 
   CUtensorMap tmx, tmw;
   {
@@ -776,7 +887,7 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   {
     cuuint64_t dims[2] = {(cuuint64_t)p.Kw, (cuuint64_t)d.K};
     cuuint64_t strides[1] = {(cuuint64_t)p.Kw * ES};
-    cuuint32_t box[2] = {BKE, BN};
+    cuuint32_t box[2] = {BKE, PAIR ? 64u : (cuuint32_t)BN};  // pair: 64-row pieces of a B half
     cuuint32_t estr[2] = {1, 1};
     CUresult r = gb_encode_tiled(&tmw, DT, 2, const_cast<void*>(wpack), dims, strides, box, estr,
                                  CU_TENSOR_MAP_SWIZZLE_128B);
@@ -826,11 +937,16 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
                         strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = gb_set_smem_once(
-      reinterpret_cast<const void*>(igemm_bf16_tc_kernel<BN, MODE_CONV, LIGHT, TF32>), Cf::SMEM);
+  auto* kern = igemm_bf16_tc_kernel<BN, MODE_CONV, LIGHT, TF32, PAIR>;
+  cudaError_t e = gb_set_smem_once(reinterpret_cast<const void*>(kern), Cf::SMEM);
   if (e != cudaSuccess) return e;
   const int tiles = p.m_tiles * p.n_tiles * p.ksplit;
-  const int slots = gb_num_sms() * (LIGHT ? 2 : 1);
+  // persistent grid: one work unit per CTA (pair mode: per cluster of two) at a time
+  int slots = gb_num_sms() * (LIGHT ? 2 : 1);
+  if constexpr (PAIR) {
+    slots = pair_max_clusters<BN>(Cf::SMEM);
+    if (slots <= 0) return cudaErrorInvalidConfiguration;
+  }
   const int grid = tiles < slots ? tiles : slots;
   // a last wave that would leave most SMs idle runs as half-width units (at
   // least 64 columns: the epilogue's sub-block; the exact int8 path needs a whole
@@ -841,17 +957,20 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
     if (rem > 0 && rem <= grid / 2) p.tail_start = tiles - rem;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
+  cfg.gridDim = dim3((unsigned)(PAIR ? 2 * grid : grid));
   cfg.blockDim = dim3(192);
   cfg.dynamicSmemBytes = Cf::SMEM;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t le = cudaLaunchKernelEx(&cfg, igemm_bf16_tc_kernel<BN, MODE_CONV, LIGHT, TF32>, tmx,
-                                      tmw, tmy, tmr, p);
+  cfg.numAttrs = PAIR ? 2 : 1;
+  cudaError_t le = cudaLaunchKernelEx(&cfg, kern, tmx, tmw, tmy, tmr, p);
   if (le != cudaSuccess) return le;
   gb_count_launch();
   return cudaGetLastError();
@@ -925,6 +1044,7 @@ int igemm_block_n(int algo) {
     case CONV_ALGO_IGEMM_N64: return 64;
     case CONV_ALGO_IGEMM_N128: return 128;
     case CONV_ALGO_IGEMM_N256: return 256;
+    case CONV_ALGO_IGEMM_2SM: return 256;
     default: return 0;
   }
 }
@@ -968,6 +1088,15 @@ cudaError_t launch_igemm_bf16(const gbconv_desc_s& d, int block_n, const void* x
     case 256: return launch_bn<256, false>(d, x, wpack, bias, res, y, err, wait_ns, st, split);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_igemm_bf16_pair(const gbconv_desc_s& d, const void* x, const void* wpack,
+                                   const float* bias, const void* res, void* y, int* err,
+                                   unsigned long long wait_ns, cudaStream_t st) {
+  if (d.dtype != CONV_BF16 || d.C == 8 || d.x_cstride || d.y_kstride)
+    return cudaErrorInvalidValue;
+  return launch_bn<256, false, false, true>(d, x, wpack, bias, res, y, err, wait_ns, st,
+                                            IgemmSplit());
 }
 
 int igemm_kiters(const gbconv_desc_s& d) {

@@ -90,7 +90,9 @@ typedef int conv_algo_t;
                                       space-to-depth + implicit GEMM whose columns are
                                       the 2x2 output pixels of each block (K == 64;
                                       workspace)                                         */
-#define CONV_ALGO_COUNT 14
+#define CONV_ALGO_IGEMM_2SM 14     /* implicit GEMM with 256 x 256 tiles split over a pair
+                                      of SMs (tcgen05 cta_group::2; groups 1, C != 8)   */
+#define CONV_ALGO_COUNT 15
 
 /* ---- descriptor --------------------------------------------------------- */
 

@@ -8,7 +8,7 @@ from tests.gpu_util import need_gpu, oracle_conv_nhwc, run_bf16_layer
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-2
-ALGOS = [1, 2, 3]  # CONV_ALGO_IGEMM_N64 / N128 / N256
+ALGOS = [1, 2, 3, 14]  # CONV_ALGO_IGEMM_N64 / N128 / N256 / 2SM (256 x 256 over an SM pair)
 
 CASES = [
     # N, C, H, W, K, R, S, stride, pad, dil
@@ -25,8 +25,8 @@ CASES = [
 ]
 
 
-def _applies(algo, K):
-    return {1: True, 2: K > 64, 3: K > 128}[algo]
+def _applies(algo, K, C=64):
+    return {1: True, 2: K > 64, 3: K > 128, 14: K > 128 and C != 8}[algo]
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c)))
@@ -34,7 +34,7 @@ def _applies(algo, K):
 def test_igemm_matches_oracle(case, algo):
     torch = need_gpu()
     N, C, H, W, K, R, S, st, pad, dil = case
-    if not _applies(algo, K):
+    if not _applies(algo, K, C):
         pytest.skip("tile wider than K")
     y, ref = run_bf16_layer(torch, algo, N, C, H, W, K, R, S, st, pad, dil, act=0, seed=11)
     err = ol.normalized_max_error(y, ref)
@@ -84,13 +84,15 @@ def test_igemm_full_resnet_layer_sampled():
 
 
 @pytest.mark.parametrize("residual", [False, True])
-def test_igemm_tail_wave_half_width_units(residual):
-    """196 full-width tiles on a 152-SM grid: the last partial wave runs as
-    half-width (128-column) work units; with a residual, its prefetch crosses
-    from full to half units."""
+@pytest.mark.parametrize("algo", [3, 14])
+def test_igemm_tail_wave_half_width_units(residual, algo):
+    """196 full-width tiles on a 152-SM grid (the SM-pair algorithm: 98
+    256-row units on 76 clusters): the last partial wave runs as half-width
+    (128-column) work units; with a residual, its prefetch crosses from full
+    to half units."""
     torch = need_gpu()
-    y, ref = run_bf16_layer(torch, 3, 8, 64, 56, 56, 256, 3, 3, 1, 1, act=1, residual=residual,
-                            seed=9)
+    y, ref = run_bf16_layer(torch, algo, 8, 64, 56, 56, 256, 3, 3, 1, 1, act=1,
+                            residual=residual, seed=9)
     assert ol.normalized_max_error(y, ref) <= TOL
 
 

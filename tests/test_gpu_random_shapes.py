@@ -11,7 +11,7 @@ from tests.gpu_util import need_gpu, oracle_conv_nhwc
 pytestmark = pytest.mark.gpu
 
 TOL = {5: 3e-2}  # Winograd F(6,3); everything else 1e-2
-BF16_ALGOS = [0, 1, 2, 3, 4, 5, 6, 9, 10, 13]
+BF16_ALGOS = [0, 1, 2, 3, 4, 5, 6, 9, 10, 13, 14]
 
 
 def _shapes(n, seed=2024):
