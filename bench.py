@@ -399,7 +399,7 @@ class ShuffleDepthwise(Workload):
 class GroupedConv(Workload):
     """ShuffleNet v1 (g = 3) grouped 1x1 convolution, 240 -> 240 channels
     (80 per group) at 28x28, batch 64: one implicit GEMM per group over
-    strided channel views (memory-bound: judged against HBM)."""
+    strided channel views (memory-bound: measured against the HBM roofline)."""
     name = "shufflenet_gconv1x1_c240_g3_28x28_n64_bf16_nhwc"
     metric = "conv TFLOP/s (direct-equivalent), grouped 1x1 240->240 g=3 @28x28, batch 64"
 
