@@ -116,6 +116,31 @@ def test_algo_table_and_applicability(B):
         B.conv_desc_destroy(h)
 
 
+def test_sm_pair_tile_applicability(B):
+    """The 256 x 256 SM-pair implicit GEMM: bf16 NHWC, groups 1, C != 8 (the
+    8-channel narrow mode stays single-SM), K > 128; same packed weights and no
+    workspace."""
+    def ok(*args, groups=1, dtype=None):
+        d = B.conv_desc_create(*args, 1, groups, B.CONV_BF16 if dtype is None else dtype)
+        try:
+            r = B.conv_algo_info(d, B.CONV_ALGO_IGEMM_2SM)
+            assert r[1] == "igemm_tc_2sm_n256"
+            return r[2]
+        finally:
+            B.conv_desc_destroy(d)
+    assert ok(32, 256, 56, 56, 256, 3, 3, 1, 1)
+    assert ok(2, 64, 9, 9, 136, 1, 1, 2, 0)             # K just above one 128-wide tile
+    assert not ok(2, 64, 9, 9, 128, 3, 3, 1, 1)         # K <= 128: a narrower tile
+    assert not ok(2, 512, 7, 7, 512, 3, 3, 1, 1, groups=2)
+    assert not ok(2, 8, 32, 32, 256, 7, 7, 2, 3)        # 8-channel stem input
+    assert not ok(2, 64, 9, 9, 256, 3, 3, 1, 1, dtype=B.CONV_INT8)
+    d = B.conv_desc_create(4, 256, 14, 14, 512, 3, 3, 1, 1, 1, 1, B.CONV_BF16)
+    assert B.conv_weights_packed_size(d, B.CONV_ALGO_IGEMM_2SM) == B.conv_weights_packed_size(
+        d, B.CONV_ALGO_IGEMM_N256)
+    assert B.conv_workspace_size(d, B.CONV_ALGO_IGEMM_2SM) == 0
+    B.conv_desc_destroy(d)
+
+
 def test_fwd_argument_errors(B):
     d = B.conv_desc_create(1, 64, 8, 8, 64, 3, 3, 1, 1, 1, 1, B.CONV_BF16)
     with pytest.raises(B.GbconvError) as e:
