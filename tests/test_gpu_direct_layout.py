@@ -13,11 +13,25 @@ pytestmark = pytest.mark.gpu
     (2, 16, 9, 7, 12, 3, 3, 1, 1, 1, 1),
     (1, 8, 10, 10, 8, 3, 3, 2, 1, 1, 8),      # depthwise through the direct loop
     (2, 12, 8, 8, 6, 3, 3, 1, 2, 2, 3),       # groups 3, dilation 2
+    (1, 1, 5, 5, 1, 3, 3, 1, 1, 1, 1),        # C = K = 1
+    (2, 3, 1, 1, 5, 3, 3, 1, 1, 1, 1),        # 1x1 image, only the centre tap inside
+    (1, 2, 4, 4, 3, 3, 3, 1, 3, 1, 1),        # padding past the kernel's reach: all-pad windows
+    (1, 5, 7, 3, 2, 5, 5, 3, 2, 1, 1),        # odd sizes, stride 3
 ])
 def test_direct_bf16(case):
     torch = need_gpu()
     N, C, H, W, K, R, S, st, pad, dil, g = case
     y, ref = run_bf16_layer(torch, 0, N, C, H, W, K, R, S, st, pad, dil, g, act=1, seed=3)
+    assert ol.normalized_max_error(y, ref) <= 1e-2
+
+
+@pytest.mark.parametrize("algo", [1, 2])
+def test_narrow_igemm_one_pixel_images(algo):
+    """8-channel input (the narrow tile mode) on 1x1 images: one output pixel
+    per image, a GEMM of a handful of rows in one ragged tile."""
+    torch = need_gpu()
+    y, ref = run_bf16_layer(torch, algo, 3, 8, 1, 1, 72 if algo == 1 else 136, 1, 1, 1, 0,
+                            act=2, seed=4)
     assert ol.normalized_max_error(y, ref) <= 1e-2
 
 
