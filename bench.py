@@ -33,6 +33,13 @@ the current forward pass; the others copy in, run, copy out on one stream);
 `cpu_baseline` is the fp64 / exact-int8 oracle on this host's cores over a
 bounded sample of the same workload, repeated to about 10 s (N = 1 only).
 
+The default run (the headline workload with Fast-Run) then times the other
+configurations the library is measured on -- single_layer, mbv2_block,
+int8_stages and resnet50 -- with fewer steps each, in the same regime (L2
+flush, CUDA events, clocks, roofline, e2e, a shorter CPU baseline), and adds
+them to the same JSON line under "workloads"; the top-level keys stay the
+headline's.  --no-extra-workloads times the headline alone.
+
 --impl reference times the oracle itself (the reference arm of this metric).
 """
 from __future__ import annotations
@@ -62,6 +69,12 @@ NCU_TRAFFIC = {
     ("resnet3x3", "igemm_tc_2sm_n256"): (52_630_784 + 8_501_248, "25142bcfa3cd0459"),
     ("mbv2_block", "mbv2_fused"): (9_710_592 + 0, "60565c380d276d7a"),
 }
+# the ncu figure is DRAM traffic while the kernel runs: output lines still dirty
+# in L2 when it ends are written back later, so it can sit below the algorithmic
+# bytes without any saving
+TRAFFIC_NOTE = ("dram__bytes_read.sum + dram__bytes_write.sum while the kernel runs (ncu): "
+                "output still dirty in L2 at kernel end is written back afterwards and is not "
+                "counted, so this can be below the algorithmic bytes")
 KERNEL_SOURCE = {"igemm_tc_n64": "k_igemm.cu", "igemm_tc_n128": "k_igemm.cu",
                  "igemm_tc_n256": "k_igemm.cu", "igemm_tc_2sm_n256": "k_igemm.cu",
                  "winograd_f2x2_3x3": "k_winograd.cu",
@@ -1024,6 +1037,183 @@ def count_launches(wl, groups):
     return B.conv_launch_count() - c0
 
 
+def measure(wl, args, dev, pg, world, rank, sampler, steps, warmup, cpu_seconds):
+    """Warm up, then time `steps` steps of the workload (L2 flushed before each,
+    outside the event window), its end-to-end step, its clocks, roofline and CPU
+    baseline.  Returns the workload's JSON fields on rank 0 (None elsewhere)."""
+    import torch
+    from cnn_convolution_gemm_gb300 import binding as B
+    groups = wl.groups()
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        for g in groups:
+            g[1]()
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    B.conv_sync_status(sh)
+
+    ng = len(groups)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(ng + 1)] for _ in range(steps)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        for j, g in enumerate(groups):
+            g[1]()
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    t_wall1 = time.time()
+    B.conv_sync_status(sh)
+    per_step = [e[0].elapsed_time(e[ng]) for e in ev]
+    per_group = [[e[j].elapsed_time(e[j + 1]) for e in ev] for j in range(ng)]
+    dev_ms = sum(per_step)
+
+    # end-to-end: the step's input host -> device, the step, its result -> host
+    e2e_steps = max(3, min(steps, 50))
+
+    def e2e_step():
+        if hasattr(wl, "host_step"):  # the library's host-tensor entry point
+            wl.host_step(args)
+            return
+        for hsrc, ddst in wl.h2d():
+            ddst.copy_(hsrc, non_blocking=True)
+        step()
+        for dsrc, hdst in wl.d2h():
+            hdst.copy_(dsrc, non_blocking=True)
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    time.sleep(0.25)
+    clocks = sampler.summary(t_wall0 - 0.15, t_wall1 + 0.15)
+
+    # replicas: every rank ran its own batch; the job's rate is all ranks' work
+    # over the slowest rank's time
+    dev_ms, e2e_ms = max_over_ranks([dev_ms, e2e_ms], pg, dev)
+    step_ms = dev_ms / steps
+    value = wl.value(step_ms) * world
+    e2e_value = wl.value(e2e_ms) * world
+    if rank != 0:
+        return None
+
+    peaks, peak_src = load_peaks()
+    tot = [sum(t) for t in per_group]
+    k = max(range(ng), key=lambda j: tot[j])  # dominant launch group
+    label, _, work, nbytes, bound = groups[k]
+    avg_ms = tot[k] / steps
+    kname = label.split(":")[-1]
+    if bound == "tensor":
+        achieved = wl.kernel_work(kname, work) / (avg_ms * 1e-3) / 1e12
+        peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        unit = "TFLOP/s"
+    elif bound == "tf32":
+        # tf32 peak = the measured bf16 peak x the nominal tf32 / bf16 ratio (1.1 / 2.25)
+        achieved = wl.kernel_work(kname, work) / (avg_ms * 1e-3) / 1e12
+        peak = round(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) * 1.1 / 2.25, 1)
+        unit = "TFLOP/s"
+    elif bound == "alu":
+        # CUDA-core fp32 FMA peak: SMs x 128 lanes x 2 FLOP x the maximum SM clock
+        achieved = wl.kernel_work(kname, work) / (avg_ms * 1e-3) / 1e12
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        mhz = peaks.get("sm_max_mhz", 2070.0)
+        peak = round(sms * 128 * 2 * mhz * 1e6 / 1e12, 2)
+        unit = "TFLOP/s"
+    else:
+        achieved = nbytes / (avg_ms * 1e-3) / 1e9
+        peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+        unit = "GB/s"
+    traffic = None
+    key = (next(n for n, c in WORKLOADS.items() if c.name == wl.name), kname)
+    if key in NCU_TRAFFIC and KERNEL_SOURCE.get(kname):
+        tb, h = NCU_TRAFFIC[key]
+        if h == src_hash(KERNEL_SOURCE[kname]):
+            traffic = tb
+    kind = "bf16 burst" if bound == "tensor" else "HBM copy"
+    psrc = (f"measured {kind} (MEASURED_PEAKS.json)" if peak_src == "measured"
+            else "fallback")
+    if bound == "tf32":
+        psrc = ("measured bf16 burst (MEASURED_PEAKS.json) x nominal tf32/bf16 1.1/2.25"
+                if peak_src == "measured" else "fallback bf16 x 1.1/2.25")
+        bound = "tensor"
+    if bound == "alu":
+        psrc = ("derived: SMs x 128 fp32 lanes x 2 FLOP x max SM clock "
+                f"({'MEASURED_PEAKS.json sm_max_mhz' if peak_src == 'measured' else 'fallback'})")
+    roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": psrc,
+                "kernel": label,
+                "algorithmic_work_per_launch": wl.kernel_work(kname, work),
+                "algorithmic_bytes_per_launch": nbytes}
+    if traffic is not None:
+        roofline["traffic_note"] = TRAFFIC_NOTE
+    if kname == "int8_igemm_tc":
+        roofline["note"] = ("int8 runs exactly on the bf16 tcgen05 pipe (sm_103a has no "
+                            "tcgen05 int8 kind; int8 values are exact in bf16 and fp32 sums of "
+                            "their products stay exact below 2^24): the fraction is against "
+                            "the measured bf16 tensor peak")
+    elif kname == "int8_igemm_mma":
+        roofline["note"] = ("int8 runs on mma.sync (sm_103a has no tcgen05 int8 kind); the "
+                            "fraction is against the measured bf16 tensor peak")
+    cpu = None  # the oracle's timing is a single-GPU figure: rank 0 at N = 1 only
+    if not args.no_cpu_baseline and world == 1:
+        os.environ.setdefault("OMP_NUM_THREADS", str(cpu_cores()))
+        cpu = cpu_baseline_sampled(wl, args, min_seconds=cpu_seconds)
+    groups_out = {}
+    for j, g in enumerate(groups):
+        ms = tot[j] / steps
+        groups_out[g[0]] = {"ms": round(ms, 5), "work": g[2], "bytes": g[3],
+                            "tflops": round(g[2] / (ms * 1e-3) / 1e12, 2),
+                            "gbs": round(g[3] / (ms * 1e-3) / 1e9, 1)}
+    h2d_bytes = sum(h.numel() * h.element_size() for h, _ in wl.h2d())
+    d2h_bytes = sum(d.numel() * d.element_size() for d, _ in wl.d2h())
+    out = {
+        "metric": wl.metric, "value": round(value, 3), "unit": wl.unit,
+        "steps": steps, "warmup": warmup, "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True, "dtype": wl.dtype,
+        "config": {"workload": wl.name, "algo": wl.algo_name,
+                   "l2": "flushed between steps (256 MB write outside the event window)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "e2e": {"value": round(e2e_value, 3), "unit": wl.unit,
+                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+                "ms_per_step": round(e2e_ms, 4),
+                "path": (wl.e2e_path(args) if hasattr(wl, "e2e_path") else
+                         "copy in, the step's calls, copy out on one stream")},
+        "gpu_launches": steps * count_launches(wl, groups),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "groups": groups_out,
+        "fastrun_ms": wl.fastrun_ms,
+        "step_ms_min_median": [round(min(per_step), 5), round(statistics.median(per_step), 5)],
+    }
+    if hasattr(wl, "algo_counts"):
+        out["config"]["algos"] = wl.algo_counts
+    if hasattr(wl, "layer_breakdown"):
+        out["layers"] = wl.layer_breakdown()
+    return out
+
+
+# the other configurations timed by the default run, after the headline, each
+# under the line's "workloads" key: (workload, steps, warm-up)
+EXTRA_WORKLOADS = [("single_layer", 100, 10), ("mbv2_block", 50, 5), ("int8_stages", 50, 5),
+                   ("resnet50", 30, 5)]
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1037,6 +1227,8 @@ def main():
                     help="load the Fast-Run map from this file if it exists (skipping "
                          "selection), else select and save it there")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-workloads", action="store_true",
+                    help="the default workload alone (no 'workloads' key)")
     ap.add_argument("--no-graph", action="store_true",
                     help="resnet50, int8_stages, single_layer: launch call by call instead of "
                          "replaying CUDA graphs")
@@ -1065,176 +1257,46 @@ def main():
     had_map = bool(args.fastrun_file and os.path.exists(args.fastrun_file))
     if had_map:
         B.conv_fastrun_load(args.fastrun_file)
-    wl = WORKLOADS[args.workload]()
-    wl.setup(dev, rank, args)
-    if args.fastrun_file and not had_map and rank == 0:
-        B.conv_fastrun_save(args.fastrun_file)
-    groups = wl.groups()
-    stream = torch.cuda.current_stream()
-    sh = stream.cuda_stream
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-
-    def step():
-        for g in groups:
-            g[1]()
-
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    B.conv_sync_status(sh)
-
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    ng = len(groups)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(ng + 1)]
-          for _ in range(args.steps)]
-    if pg:
-        pg.barrier()
-    torch.cuda.synchronize()
-    t_wall0 = time.time()
-    for i in range(args.steps):
-        flush.zero_()
-        ev[i][0].record(stream)
-        for j, g in enumerate(groups):
-            g[1]()
-            ev[i][j + 1].record(stream)
-    torch.cuda.synchronize()
-    if pg:
-        pg.barrier()
-    t_wall1 = time.time()
-    B.conv_sync_status(sh)
-    per_step = [e[0].elapsed_time(e[ng]) for e in ev]
-    per_group = [[e[j].elapsed_time(e[j + 1]) for e in ev] for j in range(ng)]
-    dev_ms = sum(per_step)
+    wl = WORKLOADS[args.workload]()
+    wl.setup(dev, rank, args)
+    line = measure(wl, args, dev, pg, world, rank, sampler, args.steps, args.warmup, 10.0)
 
-    # end-to-end: the step's input host -> device, the step, its result -> host
-    e2e_steps = max(3, min(args.steps, 50))
-
-    def e2e_step():
-        if hasattr(wl, "host_step"):  # the library's host-tensor entry point
-            wl.host_step(args)
-            return
-        for hsrc, ddst in wl.h2d():
-            ddst.copy_(hsrc, non_blocking=True)
-        step()
-        for dsrc, hdst in wl.d2h():
-            hdst.copy_(dsrc, non_blocking=True)
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    time.sleep(0.2)
+    # the default run also times the other configurations (each in the same
+    # regime, with fewer steps), reusing the process's Fast-Run map
+    extra = {}
+    if (args.workload == "resnet3x3" and args.algo == "fastrun" and
+            not args.no_extra_workloads):
+        del wl
+        torch.cuda.empty_cache()
+        for name, steps, warm in EXTRA_WORKLOADS:
+            w2 = WORKLOADS[name]()
+            w2.setup(dev, rank, args)
+            r = measure(w2, args, dev, pg, world, rank, sampler, steps, warm, 3.0)
+            if r is not None:
+                extra[name] = r
+            del w2
+            torch.cuda.empty_cache()
+    if args.fastrun_file and not had_map and rank == 0:
+        B.conv_fastrun_save(args.fastrun_file)
     sampler.stop()
-    clocks = sampler.summary(t_wall0 - 0.15, t_wall1 + 0.15)
-
-    # replicas: every rank ran its own batch; the job's rate is all ranks' work
-    # over the slowest rank's time
-    dev_ms, e2e_ms = max_over_ranks([dev_ms, e2e_ms], pg, dev)
-    step_ms = dev_ms / args.steps
-    value = wl.value(step_ms) * world
-    e2e_value = wl.value(e2e_ms) * world
 
     if rank == 0:
-        peaks, peak_src = load_peaks()
-        tot = [sum(t) for t in per_group]
-        k = max(range(ng), key=lambda j: tot[j])  # dominant launch group
-        label, _, work, nbytes, bound = groups[k]
-        avg_ms = tot[k] / args.steps
-        kname = label.split(":")[-1]
-        if bound == "tensor":
-            achieved = wl.kernel_work(kname, work) / (avg_ms * 1e-3) / 1e12
-            peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-            unit = "TFLOP/s"
-        elif bound == "tf32":
-            # tf32 peak = the measured bf16 peak x the nominal tf32 / bf16 ratio (1.1 / 2.25)
-            achieved = wl.kernel_work(kname, work) / (avg_ms * 1e-3) / 1e12
-            peak = round(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) * 1.1 / 2.25, 1)
-            unit = "TFLOP/s"
-        elif bound == "alu":
-            # CUDA-core fp32 FMA peak: SMs x 128 lanes x 2 FLOP x the maximum SM clock
-            achieved = wl.kernel_work(kname, work) / (avg_ms * 1e-3) / 1e12
-            sms = torch.cuda.get_device_properties(dev).multi_processor_count
-            mhz = peaks.get("sm_max_mhz", 2070.0)
-            peak = round(sms * 128 * 2 * mhz * 1e6 / 1e12, 2)
-            unit = "TFLOP/s"
-        else:
-            achieved = nbytes / (avg_ms * 1e-3) / 1e9
-            peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-            unit = "GB/s"
-        traffic = None
-        key = (args.workload, kname)
-        if key in NCU_TRAFFIC and KERNEL_SOURCE.get(kname):
-            tb, h = NCU_TRAFFIC[key]
-            if h == src_hash(KERNEL_SOURCE[kname]):
-                traffic = tb
-        kind = "bf16 burst" if bound == "tensor" else "HBM copy"
-        psrc = (f"measured {kind} (MEASURED_PEAKS.json)" if peak_src == "measured"
-                else "fallback")
-        if bound == "tf32":
-            psrc = ("measured bf16 burst (MEASURED_PEAKS.json) x nominal tf32/bf16 1.1/2.25"
-                    if peak_src == "measured" else "fallback bf16 x 1.1/2.25")
-            bound = "tensor"
-        if bound == "alu":
-            psrc = ("derived: SMs x 128 fp32 lanes x 2 FLOP x max SM clock "
-                    f"({'MEASURED_PEAKS.json sm_max_mhz' if peak_src == 'measured' else 'fallback'})")
-        roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-                    "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": psrc,
-                    "kernel": label,
-                    "algorithmic_work_per_launch": wl.kernel_work(kname, work),
-                    "algorithmic_bytes_per_launch": nbytes}
-        if kname == "int8_igemm_tc":
-            roofline["note"] = ("int8 runs exactly on the bf16 tcgen05 pipe (sm_103a has no "
-                                "tcgen05 int8 kind; int8 values are exact in bf16 and chunks of "
-                                "<= 1024 products are exact in fp32): the fraction is against "
-                                "the measured bf16 tensor peak")
-        elif kname == "int8_igemm_mma":
-            roofline["note"] = ("int8 runs on mma.sync (sm_103a has no tcgen05 int8 kind); the "
-                                "fraction is against the measured bf16 tensor peak")
-        cpu = None  # the oracle's timing is a single-GPU figure: rank 0 at N = 1 only
-        if not args.no_cpu_baseline and world == 1:
-            os.environ.setdefault("OMP_NUM_THREADS", str(cpu_cores()))
-            cpu = cpu_baseline_sampled(wl, args)
-        groups_out = {}
-        for j, g in enumerate(groups):
-            ms = tot[j] / args.steps
-            groups_out[g[0]] = {"ms": round(ms, 5), "work": g[2], "bytes": g[3],
-                                "tflops": round(g[2] / (ms * 1e-3) / 1e12, 2),
-                                "gbs": round(g[3] / (ms * 1e-3) / 1e9, 1)}
-        h2d_bytes = sum(h.numel() * h.element_size() for h, _ in wl.h2d())
-        d2h_bytes = sum(d.numel() * d.element_size() for d, _ in wl.d2h())
-        line = {
-            "metric": wl.metric, "value": round(value, 3), "unit": wl.unit, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        head = {
+            "metric": line["metric"], "value": line["value"], "unit": line["unit"],
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": line["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": line["dtype"],
             "data": "synthetic (seeded; N(0,1)/U activations, Kaiming weights)",
-            "config": {"workload": wl.name, "algo": wl.algo_name,
-                       "l2": "flushed between steps (256 MB write outside the event window)",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-            "e2e": {"value": round(e2e_value, 3), "unit": wl.unit,
-                    "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
-                    "ms_per_step": round(e2e_ms, 4),
-                    "path": (wl.e2e_path(args) if hasattr(wl, "e2e_path") else
-                             "copy in, the step's calls, copy out on one stream")},
-            "gpu_launches": args.steps * count_launches(wl, groups),
-            "roofline": roofline,
-            "cpu_baseline": cpu,
-            "clocks": clocks,
-            "groups": groups_out,
-            "fastrun_ms": wl.fastrun_ms,
-            "step_ms_min_median": [round(min(per_step), 5), round(statistics.median(per_step), 5)],
         }
-        if hasattr(wl, "algo_counts"):
-            line["config"]["algos"] = wl.algo_counts
-        if hasattr(wl, "layer_breakdown"):
-            line["layers"] = wl.layer_breakdown()
-        print(json.dumps(line), flush=True)
+        for k, v in line.items():
+            if k not in head and k not in ("steps", "warmup"):
+                head[k] = v
+        if extra:
+            head["workloads"] = extra
+        print(json.dumps(head), flush=True)
     if pg:
         pg.barrier()
         pg.destroy_process_group()

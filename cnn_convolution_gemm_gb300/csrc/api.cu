@@ -31,10 +31,12 @@ conv_status_t gb_fail(conv_status_t st, const char* fmt, ...) {
   return st;
 }
 
-static conv_status_t ok_status() {
+conv_status_t gb_ok() {
   g_detail[0] = 0;
   return CONV_OK;
 }
+
+static conv_status_t ok_status() { return gb_ok(); }
 
 static conv_status_t cuda_fail(cudaError_t e, const char* what) {
   return gb_fail(CONV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -412,8 +414,12 @@ static int lookup_map(const gbconv_desc_s& d) {
   return it == g_fastrun.end() ? -1 : it->second;
 }
 
+static void fastrun_autoload();
+static bool log_enabled();
+
 static int resolve(const gbconv_desc_s& d, int algo) {
   if (algo != CONV_ALGO_AUTO) return algo;
+  fastrun_autoload();
   const int a = lookup_map(d);
   if (a >= 0 && implemented(a) && applicable(d, a, nullptr)) return a;
   return heuristic(d);
@@ -422,6 +428,11 @@ static int resolve(const gbconv_desc_s& d, int algo) {
 extern "C" conv_status_t conv_algo_resolve(conv_desc_t d, conv_algo_t* algo) {
   if (!d || !algo) return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
   *algo = resolve(*d, CONV_ALGO_AUTO);
+  if (log_enabled()) {
+    const int m = lookup_map(*d);
+    fprintf(stderr, "[gbconv] resolve %s -> %s (%s)\n", desc_key(*d).c_str(), kAlgoNames[*algo],
+            m == *algo ? "fastrun map" : "heuristic");
+  }
   return ok_status();
 }
 
@@ -443,6 +454,8 @@ static conv_status_t check_algo(const gbconv_desc_s& d, int algo) {
     return gb_fail(CONV_ERR_UNSUPPORTED, "%s does not apply: %s", kAlgoNames[algo], why);
   return CONV_OK;
 }
+
+conv_status_t gb_check_algo(const gbconv_desc_s& d, int algo) { return check_algo(d, algo); }
 
 // Split-K for the bf16 implicit GEMMs (groups == 1): when the output tiles
 // (128 rows x the algorithm's BN columns) fill at most half the SMs and the
@@ -936,35 +949,101 @@ extern "C" conv_status_t conv_mbv2_block_fwd(int N, int H, int W, int C_in, int 
 
 // ---------------------------------------------------------------------------
 // Fast-Run selection: time every applicable algorithm on scratch tensors.
+//
+// The MegEngine report's Fast-Run searches every implemented operator on the
+// target device and keeps the best in a map.  Here each candidate is measured
+// the way the layer runs in a network pass: its output is first checked
+// against the direct kernel's (so a candidate that computes something else
+// cannot win), then every timed run starts with the L2 flushed (a 256 MB write
+// outside the timed events: a layer's input in a network arrives from HBM, and
+// a warm 129 MB L2 would favour memory-bound candidates), and the candidates
+// take turns round-robin across the repetitions so a slow drift of the clocks
+// lands on all of them alike.  The minimum median wins; an exact tie goes to
+// the lower id.
 
 namespace {
 struct DevBuf {
   void* p = nullptr;
+  DevBuf() = default;
+  DevBuf(const DevBuf&) = delete;
+  DevBuf& operator=(const DevBuf&) = delete;
+  DevBuf(DevBuf&& o) noexcept : p(o.p) { o.p = nullptr; }
   ~DevBuf() {
     if (p) cudaFree(p);
   }
   cudaError_t alloc(size_t n) { return cudaMalloc(&p, n ? n : 16); }
 };
+
+constexpr size_t kFastRunFlushBytes = 256ull << 20;  // twice the L2
+constexpr int kFastRunReps = 21;
+
+// normalized max error a candidate may show against the direct kernel: the
+// parity bars of the library's tests (int8: exact)
+float fastrun_tolerance(const gbconv_desc_s& d, int a) {
+  if (d.dtype == CONV_INT8) return 0.f;
+  if (d.dtype == CONV_F32) return 5e-3f;
+  return a == CONV_ALGO_WINO_F6 ? 3e-2f : 1e-2f;
+}
 }  // namespace
+
+// GBCONV_LOG=1: Fast-Run decisions, map loads and AUTO resolutions on stderr.
+static bool log_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("GBCONV_LOG");
+    return e && *e && strcmp(e, "0") != 0;
+  }();
+  return on;
+}
+
+// GBCONV_FASTRUN_FILE=path: the map is loaded from path (if it exists) before
+// the first lookup, and saved there after every selection.
+static const char* fastrun_file() {
+  static const char* f = [] {
+    const char* e = getenv("GBCONV_FASTRUN_FILE");
+    return (e && *e) ? e : nullptr;
+  }();
+  return f;
+}
+
+static void fastrun_autoload() {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    const char* f = fastrun_file();
+    if (!f) return;
+    FILE* t = fopen(f, "r");
+    if (!t) return;  // not written yet
+    fclose(t);
+    const conv_status_t st = conv_fastrun_load(f);
+    if (log_enabled())
+      fprintf(stderr, "[gbconv] fastrun map %s: %s\n", f,
+              st == CONV_OK ? "loaded" : conv_last_error_detail());
+  });
+}
 
 extern "C" conv_status_t conv_fastrun_select(conv_desc_t d, void* stream, conv_algo_t* best,
                                              float* times_ms) {
   if (!d || !best) return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
+  fastrun_autoload();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t eb = elem_bytes(d->dtype);
   const size_t xb = (size_t)d->N * d->C * d->H * d->W * eb;
-  const size_t yb = (size_t)d->N * d->K * d->OH * d->OW * eb;
+  const long long ny = (long long)d->N * d->K * d->OH * d->OW;
+  const size_t yb = (size_t)ny * eb;
   const size_t bb = (size_t)d->K * 4;
-  DevBuf x, y, res, bias, w, scale;
+  DevBuf x, y, yref, res, bias, w, scale, flush, cmp;
   cudaError_t e;
   if ((e = x.alloc(xb)) != cudaSuccess || (e = y.alloc(yb)) != cudaSuccess ||
-      (e = bias.alloc(bb)) != cudaSuccess || (e = w.alloc(user_weight_bytes(*d))) != cudaSuccess)
+      (e = yref.alloc(yb)) != cudaSuccess || (e = bias.alloc(bb)) != cudaSuccess ||
+      (e = w.alloc(user_weight_bytes(*d))) != cudaSuccess ||
+      (e = flush.alloc(kFastRunFlushBytes)) != cudaSuccess ||
+      (e = cmp.alloc(3 * sizeof(unsigned))) != cudaSuccess)
     return cuda_fail(e, "fastrun scratch");
   if (d->has_residual && (e = res.alloc(yb)) != cudaSuccess) return cuda_fail(e, "fastrun");
   gbconv_desc_s dd = *d;
+  std::vector<float> sc;
   if (d->dtype == CONV_INT8) {
     if ((e = scale.alloc((size_t)d->K * 4)) != cudaSuccess) return cuda_fail(e, "fastrun");
-    std::vector<float> sc(d->K, 1e-4f);
+    sc.assign(d->K, 1e-4f);
     cudaMemcpyAsync(scale.p, sc.data(), sc.size() * 4, cudaMemcpyHostToDevice, s);
     dd.scale = static_cast<const float*>(scale.p);
   }
@@ -973,69 +1052,119 @@ extern "C" conv_status_t conv_fastrun_select(conv_desc_t d, void* stream, conv_a
   launch_fill_random(w.p, user_weight_bytes(*d), esz, 2u, s);
   cudaMemsetAsync(bias.p, 0, bb, s);
   if (res.p) launch_fill_random(res.p, yb, esz, 3u, s);
+  auto flush_l2 = [&] { return cudaMemsetAsync(flush.p, 0, kFastRunFlushBytes, s); };
 
   float tms[CONV_ALGO_COUNT];
-  for (int a = 0; a < CONV_ALGO_COUNT; ++a) tms[a] = -1.f;
-  int best_a = -1;
-  float best_t = 0.f;
-  cudaEvent_t e0, e1;
-  cudaEventCreate(&e0);
-  cudaEventCreate(&e1);
-  // The heuristic's choice is timed first so that a clearly slower candidate
-  // can be measured with a single run instead of the full repetition count.
-  std::vector<int> order{heuristic(dd)};
-  for (int a = 0; a < CONV_ALGO_COUNT; ++a)
-    if (a != order[0]) order.push_back(a);
-  auto time_once = [&](int a, void* wp, void* wsp, size_t wsb, float* ms) {
-    cudaEventRecord(e0, s);
-    const bool ok = fwd_impl(dd, x.p, wp, bias.p, res.p, y.p, a, wsp, wsb, s) == CONV_OK;
-    cudaEventRecord(e1, s);
-    cudaEventSynchronize(e1);
-    cudaEventElapsedTime(ms, e0, e1);
-    return ok;
-  };
-  for (int a : order) {
-    if (!implemented(a) || !applicable(dd, a, nullptr)) continue;
-    size_t pb = 0, wsb = 0;
-    if (conv_weights_packed_size(&dd, a, &pb) != CONV_OK) continue;
-    if (conv_workspace_size(&dd, a, &wsb) != CONV_OK) continue;
+  float err_of[CONV_ALGO_COUNT];
+  for (int a = 0; a < CONV_ALGO_COUNT; ++a) tms[a] = -1.f, err_of[a] = -1.f;
+
+  // the reference output: the direct kernel (applies to every descriptor)
+  bool have_ref = false;
+  {
+    DevBuf wp;
+    size_t pb = 0;
+    if (applicable(dd, CONV_ALGO_DIRECT, nullptr) &&
+        conv_weights_packed_size(&dd, CONV_ALGO_DIRECT, &pb) == CONV_OK &&
+        wp.alloc(pb) == cudaSuccess &&
+        conv_weights_prepack(&dd, CONV_ALGO_DIRECT, w.p, wp.p, s) == CONV_OK &&
+        fwd_impl(dd, x.p, wp.p, bias.p, res.p, yref.p, CONV_ALGO_DIRECT, nullptr, 0, s) == CONV_OK)
+      have_ref = cudaStreamSynchronize(s) == cudaSuccess;
+    cudaGetLastError();
+  }
+
+  struct Cand {
+    int a;
     DevBuf wp, ws;
-    if (wp.alloc(pb) != cudaSuccess || ws.alloc(wsb) != cudaSuccess) {
+    size_t wsb = 0;
+    std::vector<float> t;
+  };
+  std::vector<Cand> cands;
+  for (int a = 0; a < CONV_ALGO_COUNT; ++a) {
+    if (!implemented(a) || !applicable(dd, a, nullptr)) continue;
+    Cand c;
+    c.a = a;
+    size_t pb = 0;
+    if (conv_weights_packed_size(&dd, a, &pb) != CONV_OK) continue;
+    if (conv_workspace_size(&dd, a, &c.wsb) != CONV_OK) continue;
+    if (c.wp.alloc(pb) != cudaSuccess || c.ws.alloc(c.wsb) != cudaSuccess) {
       cudaGetLastError();
       continue;
     }
-    if (conv_weights_prepack(&dd, a, w.p, wp.p, s) != CONV_OK) continue;
-    float probe = 0.f;
-    if (fwd_impl(dd, x.p, wp.p, bias.p, res.p, y.p, a, ws.p, wsb, s) != CONV_OK) continue;
-    if (!time_once(a, wp.p, ws.p, wsb, &probe)) continue;
-    if (best_a >= 0 && probe > 5.f * best_t) {  // far slower: one measurement is enough
-      tms[a] = probe;
-      continue;
+    if (conv_weights_prepack(&dd, a, w.p, c.wp.p, s) != CONV_OK) continue;
+    // first run: loads the kernels and produces the output that is checked
+    if (fwd_impl(dd, x.p, c.wp.p, bias.p, res.p, y.p, a, c.ws.p, c.wsb, s) != CONV_OK) continue;
+    if (have_ref && a != CONV_ALGO_DIRECT) {
+      unsigned h[3] = {0, 0, 0};
+      if (launch_compare_outputs(y.p, yref.p, ny, (int)dd.dtype, static_cast<unsigned*>(cmp.p),
+                                 s) != cudaSuccess ||
+          cudaMemcpyAsync(h, cmp.p, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+          cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        continue;
+      }
+      float md, mb;
+      memcpy(&md, &h[0], 4);
+      memcpy(&mb, &h[1], 4);
+      const float rel = mb > 0.f ? md / mb : md;
+      err_of[a] = rel;
+      const float tol = fastrun_tolerance(dd, a);
+      if (h[2] != 0 || !(rel <= tol)) {
+        tms[a] = -2.f;  // rejected: its output disagrees with the direct kernel's
+        if (log_enabled())
+          fprintf(stderr, "[gbconv] fastrun %s: %s rejected (error %.3g > %.3g, %u bad)\n",
+                  desc_key(*d).c_str(), kAlgoNames[a], rel, tol, h[2]);
+        continue;
+      }
     }
-    bool ok = true;
-    for (int i = 0; i < 2 && ok; ++i)
-      ok = fwd_impl(dd, x.p, wp.p, bias.p, res.p, y.p, a, ws.p, wsb, s) == CONV_OK;
-    std::vector<float> t;
-    const int reps = 15;
-    for (int i = 0; i < reps && ok; ++i) {
+    cands.push_back(std::move(c));
+  }
+
+  cudaEvent_t e0, e1;
+  cudaEventCreate(&e0);
+  cudaEventCreate(&e1);
+  auto time_once = [&](Cand& c, float* ms) {
+    if (flush_l2() != cudaSuccess) return false;
+    cudaEventRecord(e0, s);
+    const bool ok = fwd_impl(dd, x.p, c.wp.p, bias.p, res.p, y.p, c.a, c.ws.p, c.wsb, s) == CONV_OK;
+    cudaEventRecord(e1, s);
+    if (cudaEventSynchronize(e1) != cudaSuccess) return false;
+    cudaEventElapsedTime(ms, e0, e1);
+    return ok;
+  };
+  // one probe each; a candidate over 5x the fastest probe keeps that one figure
+  std::vector<float> probe(cands.size(), -1.f);
+  float best_probe = 0.f;
+  for (size_t i = 0; i < cands.size(); ++i)
+    if (time_once(cands[i], &probe[i]) && (best_probe == 0.f || probe[i] < best_probe))
+      best_probe = probe[i];
+  std::vector<size_t> live;
+  for (size_t i = 0; i < cands.size(); ++i) {
+    if (probe[i] < 0.f) continue;
+    if (probe[i] > 5.f * best_probe)
+      tms[cands[i].a] = probe[i];
+    else
+      live.push_back(i);
+  }
+  // repetitions, interleaved: rep r starts at candidate r mod count
+  bool ok = true;
+  for (int r = 0; r < kFastRunReps && ok && !live.empty(); ++r)
+    for (size_t j = 0; j < live.size() && ok; ++j) {
+      Cand& c = cands[live[(j + r) % live.size()]];
       float ms = 0.f;
-      ok = time_once(a, wp.p, ws.p, wsb, &ms);
-      t.push_back(ms);
+      ok = time_once(c, &ms);
+      c.t.push_back(ms);
     }
-    if (!ok || cudaStreamSynchronize(s) != cudaSuccess) continue;
-    std::sort(t.begin(), t.end());
-    tms[a] = t[t.size() / 2];
-  }
-  // Fastest median wins; within 1% the lower id is kept (deterministic ties).
-  for (int a = 0; a < CONV_ALGO_COUNT; ++a) {
-    if (tms[a] < 0.f) continue;
-    if (best_a < 0 || tms[a] < best_t * 0.99f) {
-      best_a = a;
-      best_t = tms[a];
-    }
-  }
   cudaEventDestroy(e0);
   cudaEventDestroy(e1);
+  if (ok)
+    for (size_t i : live) {
+      std::vector<float> t = cands[i].t;
+      std::sort(t.begin(), t.end());
+      tms[cands[i].a] = t[t.size() / 2];
+    }
+  int best_a = -1;
+  for (int a = 0; a < CONV_ALGO_COUNT; ++a)
+    if (tms[a] >= 0.f && (best_a < 0 || tms[a] < tms[best_a])) best_a = a;
   int* err = gb_device_error_word();
   int code = 0;
   if (err) {
@@ -1044,10 +1173,30 @@ extern "C" conv_status_t conv_fastrun_select(conv_desc_t d, void* stream, conv_a
   }
   if (code) return gb_fail(code == DEV_ERR_TIMEOUT ? CONV_ERR_TIMEOUT : CONV_ERR_INTERNAL,
                            "device error during Fast-Run timing");
+  if (!ok) return gb_fail(CONV_ERR_CUDA, "Fast-Run timing failed");
   if (best_a < 0) return gb_fail(CONV_ERR_UNSUPPORTED, "no applicable algorithm ran");
   {
     std::lock_guard<std::mutex> lk(g_map_mu);
     g_fastrun[desc_key(*d)] = best_a;
+  }
+  if (log_enabled()) {
+    std::string line = "[gbconv] fastrun " + desc_key(*d) + ":";
+    char buf[160];
+    for (int a = 0; a < CONV_ALGO_COUNT; ++a) {
+      if (tms[a] == -1.f) continue;
+      if (tms[a] == -2.f)
+        snprintf(buf, sizeof(buf), " %s=rejected", kAlgoNames[a]);
+      else if (err_of[a] >= 0.f)
+        snprintf(buf, sizeof(buf), " %s=%.4fms(err %.1e)", kAlgoNames[a], tms[a], err_of[a]);
+      else
+        snprintf(buf, sizeof(buf), " %s=%.4fms", kAlgoNames[a], tms[a]);
+      line += buf;
+    }
+    fprintf(stderr, "%s -> %s\n", line.c_str(), kAlgoNames[best_a]);
+  }
+  if (const char* f = fastrun_file()) {
+    const conv_status_t st = conv_fastrun_save(f);
+    if (st != CONV_OK) return st;
   }
   *best = best_a;
   if (times_ms) memcpy(times_ms, tms, sizeof(tms));
@@ -1056,6 +1205,7 @@ extern "C" conv_status_t conv_fastrun_select(conv_desc_t d, void* stream, conv_a
 
 extern "C" conv_status_t conv_fastrun_lookup(conv_desc_t d, conv_algo_t* algo) {
   if (!d || !algo) return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
+  fastrun_autoload();
   const int a = lookup_map(*d);
   if (a < 0) return gb_fail(CONV_ERR_NOT_FOUND, "no Fast-Run entry");
   *algo = a;
@@ -1124,6 +1274,9 @@ extern "C" conv_status_t conv_fastrun_load(const char* path) {
     return gb_fail(CONV_ERR_FASTRUN_FILE, "corrupt Fast-Run file %s", path);
   std::lock_guard<std::mutex> lk(g_map_mu);
   for (auto& kv : fresh) g_fastrun[kv.first] = kv.second;
+  if (log_enabled())
+    fprintf(stderr, "[gbconv] fastrun load %s: %zu entries for %s, %zu skipped (other device or "
+            "version)\n", path, fresh.size(), tag.c_str(), entries - fresh.size());
   return ok_status();
 }
 

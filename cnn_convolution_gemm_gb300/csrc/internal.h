@@ -28,6 +28,12 @@ enum : int { DEV_ERR_NONE = 0, DEV_ERR_TIMEOUT = 1, DEV_ERR_INTERNAL = 2 };
 
 // Thread-local error detail; returns st for convenience.
 conv_status_t gb_fail(conv_status_t st, const char* fmt, ...);
+// Clears the thread-local error detail and returns CONV_OK (every entry point's
+// success return).
+conv_status_t gb_ok();
+// CONV_OK if algorithm `algo` is built and applies to d (the check conv_fwd
+// makes), else CONV_ERR_BAD_PARAM / CONV_ERR_UNSUPPORTED with the reason.
+conv_status_t gb_check_algo(const gbconv_desc_s& d, int algo);
 // Device error word of the current device (a __device__ int, address cached).
 int* gb_device_error_word();
 // Number of SMs of the current device (cached).
@@ -168,6 +174,11 @@ cudaError_t launch_maxpool_nhwc_bf16(const void* x, void* y, int N, int C, int H
                                      int stride, int pad, cudaStream_t st);
 cudaError_t launch_avgpool_nhwc_bf16(const void* x, void* y, int N, int C, int H, int W,
                                      cudaStream_t st);
+// Compare two outputs of n elements of dtype (conv_dtype_t): out3[0] = max |a - b|,
+// out3[1] = max |b| (fp32 bit patterns), out3[2] = non-finite elements of a
+// (int8: also elements that differ).  out3: device, 3 unsigned, zeroed here.
+cudaError_t launch_compare_outputs(const void* a, const void* b, long long n, int dtype,
+                                   unsigned* out3, cudaStream_t st);
 // Fill a buffer with deterministic pseudo-random values (Fast-Run scratch).
 cudaError_t launch_fill_random(void* p, size_t bytes, int elem_bytes, uint32_t seed,
                                cudaStream_t st);

@@ -327,6 +327,49 @@ cudaError_t launch_fill_random(void* p, size_t bytes, int elem_bytes, uint32_t s
 }
 
 namespace {
+// Agreement of two outputs of the same convolution (Fast-Run's check of a
+// candidate against the reference algorithm).  out[0] = max |a - b| and
+// out[1] = max |b| as fp32 bit patterns (non-negative floats order like their
+// bits, so an unsigned max is a float max); out[2] = elements of a that are
+// not finite or, for int8, differ from b.
+__global__ void compare_outputs_kernel(const void* __restrict__ a, const void* __restrict__ b,
+                                       long long n, int dtype, unsigned* __restrict__ out) {
+  unsigned md = 0, mb = 0, bad = 0;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    float va, vb;
+    if (dtype == CONV_BF16) {
+      va = __bfloat162float(static_cast<const __nv_bfloat16*>(a)[i]);
+      vb = __bfloat162float(static_cast<const __nv_bfloat16*>(b)[i]);
+    } else if (dtype == CONV_F32) {
+      va = static_cast<const float*>(a)[i];
+      vb = static_cast<const float*>(b)[i];
+    } else {
+      va = (float)static_cast<const int8_t*>(a)[i];
+      vb = (float)static_cast<const int8_t*>(b)[i];
+      if (va != vb) ++bad;
+    }
+    const float dv = fabsf(va - vb);
+    if (!(dv <= 3.0e38f)) {  // NaN or infinity
+      ++bad;
+      continue;
+    }
+    md = max(md, __float_as_uint(dv));
+    if (fabsf(vb) <= 3.0e38f) mb = max(mb, __float_as_uint(fabsf(vb)));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    md = max(md, __shfl_xor_sync(0xffffffffu, md, o));
+    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+    bad += __shfl_xor_sync(0xffffffffu, bad, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    atomicMax(out, md);
+    atomicMax(out + 1, mb);
+    if (bad) atomicAdd(out + 2, bad);
+  }
+}
+
 // NCHW int8 [N][C][H][W] <-> NC32HW32 int8 [N][ceil(C/32)][H][W][32]; one byte
 // per thread, indexed by the NC32HW32 element (channels past C read as 0 going
 // in, are skipped going out)
@@ -379,6 +422,15 @@ __global__ void selftest_wait_timeout_kernel(int* err, unsigned long long limit_
 
 cudaError_t launch_selftest_wait_timeout(int* err, unsigned long long limit_ns, cudaStream_t st) {
   selftest_wait_timeout_kernel<<<1, 32, 0, st>>>(err, limit_ns);
+  gb_count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compare_outputs(const void* a, const void* b, long long n, int dtype,
+                                   unsigned* out3, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(out3, 0, 3 * sizeof(unsigned), st);
+  if (e != cudaSuccess) return e;
+  compare_outputs_kernel<<<grid_for(n), kBlock, 0, st>>>(a, b, n, dtype, out3);
   gb_count_launch();
   return cudaGetLastError();
 }

@@ -11,8 +11,10 @@
 // inputs and outputs.
 //
 // Limits and sharing:
-//   * the scratch array is kNoAllocScratchBytes (24 MiB) per GPU that loads the
-//     library and is held until the process exits;
+//   * the scratch array is kNoAllocScratchBytes (24 MiB) per GPU; it comes into
+//     being when this file's module is loaded on the device (under lazy module
+//     loading, the CUDA default, at the first call there) and is held until
+//     the process exits;
 //   * the batch is processed in slices of as many images as fit in it; a shape
 //     whose single image needs more is rejected with CONV_ERR_WORKSPACE before
 //     anything is launched;
@@ -65,11 +67,9 @@ extern "C" conv_status_t conv_fwd_noalloc(conv_desc_t d, const void* x, const vo
   if (!d || !x || !wpack || !y) return gb_fail(CONV_ERR_BAD_PARAM, "NULL tensor argument");
   if (algo != CONV_ALGO_WINO_F2 && algo != CONV_ALGO_WINO_F6)
     return gb_fail(CONV_ERR_UNSUPPORTED, "conv_fwd_noalloc runs the Winograd algorithms only");
-  if (d->dtype != CONV_BF16 || d->layout != CONV_NHWC || d->R != 3 || d->S != 3 ||
-      d->stride != 1 || d->dil != 1 || d->groups != 1 || d->C % 8 || d->K % 8)
-    return gb_fail(CONV_ERR_UNSUPPORTED,
-                   "Winograd needs bf16 NHWC, 3x3, stride 1, dilation 1, groups 1, C and K "
-                   "multiples of 8");
+  // the same applicability rules as conv_fwd (shape, dtype, layout, input shuffle)
+  conv_status_t st = gb_check_algo(*d, algo);
+  if (st != CONV_OK) return st;
   if (d->has_residual != (residual != nullptr))
     return gb_fail(CONV_ERR_BAD_PARAM, "residual must be given exactly when the descriptor has one");
   if (!aligned16(x) || !aligned16(y) || !aligned16(wpack) || (residual && !aligned16(residual)) ||
@@ -77,23 +77,33 @@ extern "C" conv_status_t conv_fwd_noalloc(conv_desc_t d, const void* x, const vo
     return gb_fail(CONV_ERR_ALIGNMENT, "tensors must be 16-byte aligned (bias 4-byte)");
   const int m = algo == CONV_ALGO_WINO_F2 ? 2 : 6;
 
-  // images per slice that fit in the fixed scratch
+  // Images per slice: the largest count whose scratch fits the fixed array.  The
+  // scratch a batch needs never decreases as the batch grows (its chunk size
+  // only grows with the batch), so the fitting counts form a prefix of [1, N]:
+  // binary search.  Every slice, the last and shorter one included, then fits.
   gbconv_desc_s sub = *d;
-  sub.N = 1;
-  const size_t one = winograd_workspace_bytes(sub, m);
-  if (one > kNoAllocScratchBytes)
+  auto fits = [&](int nb) {
+    sub.N = nb;
+    return winograd_workspace_bytes(sub, m) <= kNoAllocScratchBytes;
+  };
+  if (!fits(1)) {
+    sub.N = 1;
     return gb_fail(CONV_ERR_WORKSPACE,
                    "one image needs %zu bytes of Winograd scratch; the static scratch holds %zu",
-                   one, kNoAllocScratchBytes);
-  int nb = 1;
-  while (nb < d->N) {
-    sub.N = nb + 1;
-    if (winograd_workspace_bytes(sub, m) > kNoAllocScratchBytes) break;
-    ++nb;
+                   winograd_workspace_bytes(sub, m), kNoAllocScratchBytes);
   }
+  int lo = 1, hi = d->N;  // fits(lo) holds; find the largest such count
+  while (lo < hi) {
+    const int mid = lo + (hi - lo + 1) / 2;
+    if (fits(mid))
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int nb = lo;
 
   void* scratch = nullptr;
-  conv_status_t st = scratch_address(&scratch);
+  st = scratch_address(&scratch);
   if (st != CONV_OK) return st;
   int* err = gb_device_error_word();
   const unsigned long long wait_ns = gb_wait_limit_ns();
@@ -109,5 +119,5 @@ extern "C" conv_status_t conv_fwd_noalloc(conv_desc_t d, const void* x, const vo
     if (e != cudaSuccess)
       return gb_fail(CONV_ERR_CUDA, "conv_fwd_noalloc: %s", cudaGetErrorString(e));
   }
-  return CONV_OK;
+  return gb_ok();
 }

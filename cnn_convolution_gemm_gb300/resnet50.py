@@ -12,9 +12,15 @@ a fully connected layer is a convolution whose kernel covers the input).
 53 convolutions + the FC.  Batch norm is folded into each conv's bias.
 
 Layout: NHWC bf16 on the device; the NCHW fp32 input is converted (and its 3
-channels padded to 8 for 16-byte rows) by the library's layout kernel.
+channels padded to 4, the input of the 4x4 space-to-depth stem, whose
+64-channel blocks are 128-byte rows) by the library's layout kernel.
 Every conv's bias and ReLU are fused in its epilogue; the residual add + ReLU
 are fused into the block's last 1x1 conv.
+
+Each layer's launches sit inside an NVTX range named after the layer (and
+"layout", "maxpool", "avgpool" for the glue), so a profiler's timeline shows
+the network layer by layer.  NVTX ranges are host-side markers: a CUDA graph
+captured from forward() replays without them.
 """
 from __future__ import annotations
 
@@ -157,35 +163,44 @@ class ResNet50:
         `timer(name)` (optional) is called before each launch group for per-layer timing."""
         N, sh = self.N, current_stream_handle()
         t = {} if not self.keep else self.tensors
+        nvtx = torch.cuda.nvtx
         if timer:
             timer("layout")
+        nvtx.range_push("layout")
         x0 = torch.empty((N, self.H, self.W, STEM_CHANNELS), dtype=torch.bfloat16,
                          device=self.device)
         B.conv_nchw_f32_to_nhwc_bf16(x_nchw.data_ptr(), x0.data_ptr(), N, 3, self.H, self.W,
                                      STEM_CHANNELS, sh)
+        nvtx.range_pop()
         t["input"] = x0
         for sp in self.specs:
             if sp.name == "fc":
                 if timer:
                     timer("avgpool")
+                nvtx.range_push("avgpool")
                 src = t[self.specs[-2].dst]
                 pooled = torch.empty((N, 1, 1, 2048), dtype=torch.bfloat16, device=self.device)
                 B.conv_global_avgpool_nhwc_bf16(src.data_ptr(), pooled.data_ptr(), N, 2048,
                                                 src.shape[1], src.shape[2], sh)
+                nvtx.range_pop()
                 t["pool5"] = pooled
             if timer:
                 timer(sp.name)
+            nvtx.range_push(sp.name)
             layer = self.layers[sp.name]
             out = layer(t[sp.src], self.biases[sp.name],
                         t[sp.residual] if sp.residual else None, stream=sh)
+            nvtx.range_pop()
             t[sp.dst] = out
             if sp.name == "conv1":
                 if timer:
                     timer("maxpool")
+                nvtx.range_push("maxpool")
                 _, oh, ow, c = out.shape
                 ph, pw = (oh + 2 - 3) // 2 + 1, (ow + 2 - 3) // 2 + 1
                 pooled = torch.empty((N, ph, pw, c), dtype=torch.bfloat16, device=self.device)
                 B.conv_maxpool2d_nhwc_bf16(out.data_ptr(), pooled.data_ptr(), N, c, oh, ow, 3, 2,
                                            1, sh)
+                nvtx.range_pop()
                 t["pool1"] = pooled
         return t["logits"].view(N, 1000)

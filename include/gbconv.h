@@ -187,14 +187,19 @@ conv_status_t conv_fwd(conv_desc_t desc, const void* x, const void* wpack, const
  * whose memory budget is fixed at load time.  They pass inputs and outputs only
  * (same meaning, layout and alignment rules as conv_fwd; wpack from
  * conv_weights_prepack with the same algo).
- * Scratch: a fixed 24 MiB array in device global memory, held by every GPU
- * that loads the library until the process exits.  The batch is processed in
- * slices of as many images as fit; if a single image needs more, the call
- * returns CONV_ERR_WORKSPACE before launching anything.  All calls on a device
- * share the array: calls that can overlap on the GPU race on it, so order them
- * (one stream, or events).  The first call on a device looks up the array's
- * device address with that device current; make it before any stream capture.
- * Other algorithms return CONV_ERR_UNSUPPORTED.  Stream-ordered. */
+ * Scratch: a fixed 24 MiB array in device global memory.  It is created on a
+ * device when the library's module holding it is loaded there: under CUDA's
+ * default lazy module loading that is the first conv_fwd_noalloc call on that
+ * device (with CUDA_MODULE_LOADING=EAGER, when the library initialises its
+ * modules on the device); from then on it stays until the process exits.  The
+ * batch is processed in slices of as many images as fit; if a single image
+ * needs more, the call returns CONV_ERR_WORKSPACE before launching anything.
+ * All calls on a device share the array: calls that can overlap on the GPU
+ * race on it, so order them (one stream, or events).  The first call on a
+ * device looks up the array's device address with that device current; make
+ * it before any stream capture.  The descriptor must admit the algorithm under
+ * conv_fwd's rules (an input shuffle, for one, does not); other algorithms
+ * and descriptors return CONV_ERR_UNSUPPORTED.  Stream-ordered. */
 conv_status_t conv_fwd_noalloc(conv_desc_t desc, const void* x, const void* wpack,
                                const void* bias, const void* residual, void* y,
                                conv_algo_t algo, void* stream);
@@ -270,9 +275,23 @@ conv_status_t conv_mbv2_block_fwd(int N, int H, int W, int C_in, int E, int C_ou
 /* Selection phase: time every applicable algorithm for this descriptor on the
  * current device (scratch buffers allocated and freed inside the call;
  * synchronizes the stream), keep the fastest in the process-wide map under
- * the descriptor's key, and return it.  times_ms (optional, CONV_ALGO_COUNT
- * entries) receives each algorithm's median time, or -1 where not applicable.
- * Execution phase: CONV_ALGO_AUTO looks the map up. */
+ * the descriptor's key, and return it.  How candidates are measured:
+ *   - each one's output on seeded random inputs is first compared with the
+ *     direct kernel's; one whose normalized max error exceeds the library's
+ *     parity bar (bf16 1e-2, Winograd F(6x6,3x3) 3e-2, fp32 5e-3; int8: any
+ *     difference) is rejected and cannot win;
+ *   - before every timed run the L2 is flushed by a 256 MB write outside the
+ *     timed events (as a layer's input arrives from HBM inside a network);
+ *   - candidates are timed round-robin over 21 repetitions (one probe first;
+ *     a candidate over 5x the fastest probe keeps that single figure);
+ *   - the minimum median wins; an exact tie goes to the lower algorithm id.
+ * times_ms (optional, CONV_ALGO_COUNT entries) receives each algorithm's median
+ * time in ms, -1 where not applicable, -2 where the output check rejected it.
+ * Execution phase: CONV_ALGO_AUTO looks the map up.
+ * Environment: GBCONV_LOG=1 prints every candidate's time and the decision
+ * (and each map load and conv_algo_resolve) on stderr; GBCONV_FASTRUN_FILE=path
+ * loads the map from path, if present, before the first lookup and saves the
+ * map there after every selection. */
 conv_status_t conv_fastrun_select(conv_desc_t desc, void* stream, conv_algo_t* best,
                                   float* times_ms);
 /* Map lookup only; CONV_ERR_NOT_FOUND if the descriptor was never selected. */

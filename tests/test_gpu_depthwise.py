@@ -27,3 +27,30 @@ def test_depthwise_matches_oracle(case):
     y, ref = run_bf16_layer(torch, DW, N, C, H, W, C, 3, 3, st, 1, 1, C, act=act, residual=res,
                             seed=21)
     assert ol.normalized_max_error(y, ref) <= 1e-2
+
+
+def test_depthwise_full_mbv2_batch_sampled_images():
+    """The MobileNetV2 block's depthwise at full size (64 x 56 x 56 x 144, ReLU6,
+    bias), launched exactly as the benchmark launches it (one conv_fwd over the
+    whole batch: 1,792 row strips over the persistent CTAs, so every CTA's
+    buffer ring wraps several times); the first, a middle and the last image
+    are compared with the oracle element by element."""
+    torch = need_gpu()
+    import numpy as np
+    from cnn_convolution_gemm_gb300 import binding as B
+    from cnn_convolution_gemm_gb300 import synth
+    from cnn_convolution_gemm_gb300.layer import ConvLayer
+    from tests.gpu_util import oracle_conv_nhwc
+    dev = torch.device("cuda:0")
+    N, C, H = 64, 144, 56
+    x = torch.from_numpy(synth.normal((N, H, H, C), 1.0, 31)).to(torch.bfloat16)
+    w = torch.from_numpy(synth.kaiming((C, 3, 3, 1), 32)).to(torch.bfloat16)
+    b = synth.uniform((C,), -0.1, 0.1, 33)
+    layer = ConvLayer(N, C, H, H, C, 3, 3, 1, 1, groups=C, act=B.CONV_ACT_RELU6)
+    layer.prepack(w.to(dev), DW)
+    y = layer(x.to(dev), torch.from_numpy(b).to(dev))
+    B.conv_sync_status(torch.cuda.current_stream().cuda_stream)
+    for n in (0, N // 2 - 1, N - 1):
+        ref = oracle_conv_nhwc(x[n:n + 1].double().numpy(), w.double().numpy(),
+                               b.astype(np.float64), 1, 1, 1, C, None, B.CONV_ACT_RELU6)
+        assert ol.normalized_max_error(y[n:n + 1].double().cpu().numpy(), ref) <= 1e-2, n

@@ -280,3 +280,41 @@ def test_fastrun_file_roundtrip_and_corruption(B, tmp_path):
         B.conv_fastrun_lookup(d)
     assert e.value.status_name == "CONV_ERR_NOT_FOUND"
     B.conv_desc_destroy(d)
+
+
+def test_fastrun_log_and_map_file_environment(B, tmp_path):
+    """GBCONV_FASTRUN_FILE loads the map before the first lookup and GBCONV_LOG=1
+    reports the load and each resolution on stderr (a fresh process: both
+    variables are read once)."""
+    import subprocess
+    import sys
+    import textwrap
+    from cnn_convolution_gemm_gb300 import binding
+    version = binding.conv_version()
+    key = "N1_C64_H8_W8_K64_R3_S3_st1_p1_d1_g1_t0_l0_a0_r0_q0"
+    p = tmp_path / "map.txt"
+    p.write_text(f"version {version}\nentry nodevice {key} direct\nend 1\n")
+    code = textwrap.dedent(f"""
+        import sys
+        sys.path.insert(0, {ROOT!r})
+        from cnn_convolution_gemm_gb300 import binding as B
+        d = B.conv_desc_create(1, 64, 8, 8, 64, 3, 3, 1, 1, 1, 1, B.CONV_BF16)
+        print(B.conv_algo_resolve(d))
+        d2 = B.conv_desc_create(1, 64, 8, 8, 128, 3, 3, 1, 1, 1, 1, B.CONV_BF16)
+        print(B.conv_algo_resolve(d2))
+    """)
+    env = dict(os.environ, GBCONV_LOG="1", GBCONV_FASTRUN_FILE=str(p))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       timeout=120)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stderr.splitlines() if ln.startswith("[gbconv]")]
+    load = [ln for ln in lines if "fastrun load" in ln]
+    assert len(load) == 1 and str(p) in load[0], lines
+    resolved = [ln for ln in lines if ln.startswith("[gbconv] resolve")]
+    assert len(resolved) == 2, lines
+    if "1 entries for nodevice" in load[0]:  # no GPU: the entry is this machine's
+        assert resolved[0] == f"[gbconv] resolve {key} -> direct (fastrun map)"
+        assert r.stdout.split()[0] == str(B.CONV_ALGO_DIRECT)
+    else:  # an entry for another device is skipped
+        assert "(heuristic)" in resolved[0]
+    assert resolved[1].endswith("-> igemm_tc_n128 (heuristic)"), resolved
