@@ -916,13 +916,13 @@ class ResNet50W(Workload):
     def cpu_baseline(self, args):
         import numpy as np
         from cnn_convolution_gemm_gb300 import synth
-        from cnn_convolution_gemm_gb300.resnet50 import conv_specs
+        from cnn_convolution_gemm_gb300.resnet50 import STEM_CHANNELS, conv_specs
         from oracle import lib as ol
         specs = conv_specs()
         t0 = time.perf_counter()
         flops = 0
         x = synth.normal((1, 3, 224, 224), 1.0, 100).astype(np.float64)
-        t = {"input": np.concatenate([x, np.zeros((1, 5, 224, 224))], axis=1)}
+        t = {"input": np.concatenate([x, np.zeros((1, STEM_CHANNELS - 3, 224, 224))], axis=1)}
         for i, sp in enumerate(specs):
             if sp.name == "fc":
                 t["pool5"] = ol.global_avgpool(t[specs[-2].dst]).reshape(1, 2048, 1, 1)

@@ -91,6 +91,13 @@ struct IgemmSplit {
   int i8_kout = 0;
   int i8_relu = 0;
   int i8_nc32 = 0;  // int8 output in NC32HW32 (else NHWC)
+  // Chunked exact int8 (i8_nch >= 1; 0 selects the lo/hi split weights above):
+  // the GEMM's N = i8_kout columns over plain weights; every i8_kch k-steps
+  // (64 products each, at most 16: 1024 * 128 * 128 = 2^24) the MMAs start a
+  // new TMEM accumulator block, ceil(kiters / i8_kch) == i8_nch blocks in all,
+  // and the epilogue sums the blocks' exact integer partial sums in int32.
+  int i8_nch = 0;
+  int i8_kch = 0;
   // space-to-depth-by-4 stem: the GEMM runs over the 4x4-block grid and its
   // 4K columns are (py, px, k) of the 2x2 output pixels of each block; the
   // epilogue writes them to the stride-2 conv's NHWC output [N][2BH][2BW][K]

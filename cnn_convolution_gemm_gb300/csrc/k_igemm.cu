@@ -81,6 +81,13 @@ struct IgemmParams {
   const int32_t* i8_bias;
   const float* i8_scale;
   int i8_kout, i8_relu, i8_nc32;
+  // chunked accumulation (exact int8): every kch k-steps the MMAs start a new
+  // BN-column accumulator block, i8_nch blocks per tile (0: lo/hi split weights)
+  int i8_nch;
+  int kch;        // k-steps per accumulator block (the whole reduction otherwise)
+  int acc_cols;   // TMEM columns per tile accumulator (BN, or i8_nch * BN)
+  int nacc;       // tile accumulators in TMEM (2: the epilogue overlaps the next tile)
+  uint32_t tmem_cols;  // columns allocated (a power of two >= 32)
   // tf32 mode: fp32 residual [M][K] (the fp32 output goes through tm_y)
   const float* res_f32;
   // space-to-depth-by-4 stem output (see IgemmSplit): column c of the GEMM is
@@ -245,7 +252,7 @@ __global__ void __launch_bounds__(192, 1)
       gb::tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
       gb::tmem_relinquish_pair();
     } else {
-      gb::tmem_alloc(tmem_slot, C::TMEM_COLS);
+      gb::tmem_alloc(tmem_slot, p.tmem_cols);
       gb::tmem_relinquish();
     }
   }
@@ -400,11 +407,16 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t idesc_u = width == BN ? IDESC : gb::idesc_f16(MM, BN / 2, TF32 ? 2 : 1);
         if (!gb::mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, p.wait_ns, p.err)) break;
         gb::tc_fence_after();
-        const uint32_t d = tmem_base + acc * BN;
+        uint32_t d = tmem_base + acc * p.acc_cols;
         const int bt = t / tiles_per_batch;
         const int kbeg = MODE == MODE_CONV ? bt * p.kchunk : 0;
         const int kend = MODE == MODE_CONV ? min(p.kiters, kbeg + p.kchunk) : p.kiters;
+        int kin = 0;  // k-steps into the current accumulator block
         for (int it = kbeg; it < kend; ++it) {
+          if (kin == p.kch) {  // chunked accumulation: the next BN-column block
+            kin = 0;
+            d += BN;
+          }
           if (!gb::mbar_wait_bounded(&full[stage], phase, p.wait_ns, p.err)) {
             ok = false;
             break;
@@ -420,16 +432,15 @@ __global__ void __launch_bounds__(192, 1)
                 (MODE == MODE_CONV && p.narrow)
                     ? gb::noswz_kmajor_desc(a0 + k * 2 * (BM * 16), BM * 16, 128)
                     : gb::sw128_kmajor_desc(a0 + k * 32);
+            const uint32_t accum = (kin > 0 || k > 0) ? 1u : 0u;
             if constexpr (TF32)
-              gb::tc_mma_tf32(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), idesc_u,
-                              (it > kbeg || k > 0) ? 1u : 0u);
+              gb::tc_mma_tf32(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), idesc_u, accum);
             else if constexpr (PAIR)
-              gb::tc_mma_f16_pair(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), idesc_u,
-                                  (it > kbeg || k > 0) ? 1u : 0u);
+              gb::tc_mma_f16_pair(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), idesc_u, accum);
             else
-              gb::tc_mma_f16(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), idesc_u,
-                             (it > kbeg || k > 0) ? 1u : 0u);
+              gb::tc_mma_f16(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), idesc_u, accum);
           }
+          ++kin;
           if constexpr (PAIR)
             gb::tc_commit_pair_multicast(&empty[stage], 0x3);  // both CTAs' stage is free
           else
@@ -444,7 +455,7 @@ __global__ void __launch_bounds__(192, 1)
           gb::tc_commit_pair_multicast(&tfull[acc], 0x3);
         else
           gb::tc_commit(&tfull[acc]);
-        if (++acc == 2) {
+        if (++acc == p.nacc) {
           acc = 0;
           acc_phase ^= 1;
         }
@@ -520,7 +531,7 @@ __global__ void __launch_bounds__(192, 1)
       gb::tc_fence_after();
       const long long m = (long long)mt * BM + q * 32 + lane;
       const bool row_ok = m < p.M;
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * p.acc_cols;
       if constexpr (TF32) {
         // fp32 NHWC output: 32-column sub-blocks -> + bias (+ residual) ->
         // activation -> a 128-byte-swizzled 32 x 32 fp32 box per warp -> TMA store
@@ -568,6 +579,62 @@ __global__ void __launch_bounds__(192, 1)
             gb::bulk_commit();
           }
           ++epi_count;
+        }
+      } else if (MODE == MODE_CONV && p.i8_y && p.i8_nch > 0) {
+        // exact int8, chunked accumulation: output channel column j of the unit
+        // has i8_nch partial sums, one per BN-column accumulator block, each an
+        // exact integer in fp32 (at most 1024 products of int8 values); their
+        // int32 sum + bias is requantised to int8 (the MegEngine Beta report's
+        // native int8 epilogue).  This group's 64 biases and scales are staged in
+        // the warp's (here unused) staging box and read back as broadcasts.
+        int32_t* sbi = reinterpret_cast<int32_t*>(sEpi + q * 2 * C::EPI_BOX);
+        float* ssc = reinterpret_cast<float*>(sbi + 64);
+#pragma unroll 1
+        for (int g = 0; g < width / 64; ++g) {
+          const int k0 = nt * BN + noff + g * 64;  // first output channel of the group
+          if (k0 >= p.i8_kout) break;
+          __syncwarp();  // the previous group's reads of the slice are done
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int kk = k0 + h * 32 + lane;
+            const bool in = kk < p.i8_kout;
+            sbi[h * 32 + lane] = (in && p.i8_bias) ? __ldg(p.i8_bias + kk) : 0;
+            ssc[h * 32 + lane] = in ? __ldg(p.i8_scale + kk) : 0.f;
+          }
+          __syncwarp();
+#pragma unroll 1
+          for (int c16 = 0; c16 < 4; ++c16) {
+            const int kb = k0 + c16 * 16;
+            if (kb >= p.i8_kout) break;  // i8_kout % 16 == 0
+            int tv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) tv[i] = sbi[c16 * 16 + i];
+#pragma unroll 1
+            for (int c = 0; c < p.i8_nch; ++c) {
+              uint32_t v[16];
+              gb::tmem_ld_x16(tbase + c * BN + g * 64 + c16 * 16, v);
+              gb::tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) tv[i] += __float2int_rn(__uint_as_float(v[i]));
+            }
+            uint32_t pk[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              int qv = __float2int_rn(__fmul_rn(__int2float_rn(tv[i]), ssc[c16 * 16 + i]));
+              qv = qv > 127 ? 127 : (qv < -128 ? -128 : qv);
+              if (p.i8_relu && qv < 0) qv = 0;
+              pk[i >> 2] |= (uint32_t)(qv & 0xff) << (8 * (i & 3));
+            }
+            if (row_ok) {
+              // NHWC: row m, channel kb; NC32HW32: block kb/32 of image m / (OH*OW)
+              long long off = m * p.i8_kout + kb;
+              if (p.i8_nc32) {
+                const long long ohw = (long long)p.OH * p.OW, img = m / ohw;
+                off = ((img * (p.i8_kout / 32) + kb / 32) * ohw + (m - img * ohw)) * 32 + (kb & 31);
+              }
+              *reinterpret_cast<uint4*>(p.i8_y + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+          }
         }
       } else if (MODE == MODE_CONV && p.i8_y) {
         // exact int8: each 128-column group of the tile holds 64 sums against
@@ -742,7 +809,7 @@ __global__ void __launch_bounds__(192, 1)
       } else {
         gb::mbar_arrive(&tempty[acc]);
       }
-      if (++acc == 2) {
+      if (++acc == p.nacc) {
         acc = 0;
         acc_phase ^= 1;
       }
@@ -765,7 +832,7 @@ __global__ void __launch_bounds__(192, 1)
     if constexpr (PAIR)
       gb::tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
     else
-      gb::tmem_dealloc(tmem_base, C::TMEM_COLS);
+      gb::tmem_dealloc(tmem_base, p.tmem_cols);
   }
 }
 
@@ -859,8 +926,27 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   p.i8_kout = split.i8_kout;
   p.i8_relu = split.i8_relu;
   p.i8_nc32 = split.i8_nc32;
-  if (p.i8_y && (BN % 128 != 0 || p.ksplit != 1 || p.i8_kout * 2 != d.K || p.i8_kout % 16))
-    return cudaErrorInvalidValue;
+  // accumulator layout: one BN-column block per tile, or split.i8_nch blocks of
+  // at most i8_kch k-steps each (exact int8, chunked); two tile accumulators
+  // when they fit so the epilogue overlaps the next tile's MMAs.  A CTA never
+  // takes more than its share of the SM's 512 TMEM columns (LIGHT: two CTAs).
+  p.i8_nch = p.i8_y ? split.i8_nch : 0;
+  p.kch = p.i8_nch > 0 ? split.i8_kch : (1 << 30);
+  if (p.i8_y) {
+    if (p.ksplit != 1 || p.i8_kout % 16) return cudaErrorInvalidValue;
+    if (p.i8_nch == 0 && (BN % 128 != 0 || p.i8_kout * 2 != d.K)) return cudaErrorInvalidValue;
+    if (p.i8_nch > 0 && (p.i8_kout != d.K || p.kch < 1 || gb_ceil_div(p.kiters, p.kch) != p.i8_nch))
+      return cudaErrorInvalidValue;
+  }
+  p.acc_cols = p.i8_nch > 0 ? p.i8_nch * BN : BN;
+  {
+    const int budget = LIGHT ? 256 : 512;
+    p.nacc = 2 * p.acc_cols <= budget ? 2 : 1;
+    if (p.nacc * p.acc_cols > budget) return cudaErrorInvalidValue;
+    uint32_t cols = 32;
+    while (cols < (uint32_t)(p.nacc * p.acc_cols)) cols <<= 1;
+    p.tmem_cols = cols;
+  }
   p.s2d4_k = split.s2d4_k;
   if (p.s2d4_k && (TF32 || res || p.i8_y || p.ksplit != 1 || p.s2d4_k != 64 ||
                    d.K != 4 * p.s2d4_k || d.OW % 8))
@@ -952,7 +1038,7 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   // least 64 columns: the epilogue's sub-block; the exact int8 path needs a whole
   // 128-column lo/hi group per unit)
   p.tail_start = tiles;
-  if ((BN == 256 || (BN == 128 && !p.i8_y)) && p.ksplit == 1 && tiles > grid) {
+  if ((BN == 256 || (BN == 128 && !(p.i8_y && p.i8_nch == 0))) && p.ksplit == 1 && tiles > grid) {
     const int rem = tiles % grid;
     if (rem > 0 && rem <= grid / 2) p.tail_start = tiles - rem;
   }
@@ -996,6 +1082,10 @@ cudaError_t launch_batched_bn(int batch, int M, int N, int Kred, const void* A, 
   p.wait_ns = wait_ns;
   p.OH = p.OW = 1;
   p.tail_start = 1 << 30;
+  p.kch = 1 << 30;
+  p.acc_cols = BN;
+  p.nacc = 2;
+  p.tmem_cols = 2 * BN;
   const CUtensorMapDataType dt =
       ab_type ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap tma, tmb;

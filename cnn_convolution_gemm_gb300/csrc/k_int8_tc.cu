@@ -3,26 +3,27 @@
 // sm_103a's tcgen05.mma has no int8 kind.  Every int8 value (|v| <= 128) is
 // exact in bf16 and every product of two of them (|p| <= 16384) is exact in the
 // fp32 accumulator, and a sum of integers stays exact in fp32 while its
-// magnitude is below 2^24.  So the reduction is cut into chunks of at most
-// 1024 products per output (16 k-steps of 64 channels: 1024 * 127^2 < 2^24),
-// each chunk runs on the bf16 tcgen05 pipeline (split-K mode of the implicit
-// GEMM kernel) and writes its exact fp32 partial sums, and a final pass sums the
-// chunks in int32 and applies the int8 epilogue of the MegEngine Beta report's
-// native int8 inference: + int32 bias, fp32 requantisation
+// magnitude is at most 2^24.  So the reduction is cut into chunks of at most
+// 1024 products per output (16 k-steps of 64 channels: |sum| <= 1024 * 128^2 =
+// 2^24), each chunk's sums are accumulated on the bf16 tcgen05 pipeline, and the
+// chunks are added in int32 before the int8 epilogue of the MegEngine Beta
+// report's native int8 inference: + int32 bias, fp32 requantisation
 // q = clamp(rne(fp32(acc + bias) * scale[k]), -128, 127), ReLU.
 //
-// Steps per call: int8 -> bf16 copy of the activations (workspace), split-K
-// implicit GEMM into fp32 partials (workspace), reduction + requant -> int8.
+// Steps per call: int8 -> bf16 copy of the activations (workspace), then one of
 //
-// Split-weight path (used whenever K % 64 == 0 and R*S*C <= 8704): each weight
-// is cut at prepack into w = 16 * wh + wl, wl = w & 15 in [0, 15] and wh in
-// [-8, 7].  Products x * wl are at most 128 * 15 = 1920 and x * wh at most
-// 128 * 8 = 1024 in magnitude, so an fp32 accumulator stays exact over
-// 8704 products (8704 * 1920 < 2^24): every ResNet int8 layer (at most 4608)
-// needs no split at all.  One implicit GEMM over 2K columns (per 64 output
-// channels: 64 low-part columns, 64 high-part columns) then finishes in its
-// own epilogue — t = 16 * hi + lo + bias, requant, ReLU, int8 store — so the
-// fp32 partials and the reduction pass disappear, at twice the tensor work.
+// Chunked accumulation (when the layer's tiles fill at least half the SMs): one
+// implicit GEMM over the plain bf16 weights whose MMAs start a fresh TMEM
+// accumulator block every kch <= 16 k-steps (at most 1024 products, so each
+// block's sums are exact integers in fp32); its epilogue converts the blocks
+// to int32, adds them and the bias, requantises and stores int8.  The tensor
+// cores do exactly the direct-equivalent work and nothing goes to memory but
+// the int8 output.  A reduction of at most 16 k-steps (ResNet-50's 64-channel
+// 3x3 stage: 9) is a single block.
+//
+// Split-K (smaller grids): the GEMM's split-K mode writes each chunk's exact
+// fp32 partial sums to the workspace and a reduction pass sums them in int32
+// and requantises, so the chunks also spread over otherwise idle SMs.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -33,17 +34,38 @@
 namespace {
 
 constexpr int KCHUNK_MAX = 16;  // k-steps of 64 products per exact fp32 chunk
-constexpr int SPLITW_MAX = 8704;  // products per output that stay exact with split weights
 
-// the split-weight path applies (see the file comment) and its unsplit tile
-// grid fills at least half the SMs; smaller grids keep split-K, which spreads the
-// reduction (measured on the ResNet-50 stage shapes at batch 32: 256@14 with 98
-// tiles runs faster split-weight, 512@7 with 52 tiles faster split-K)
-bool split_weights(const gbconv_desc_s& d) {
-  if (d.K % 64 || (long long)d.R * d.S * (gb_ceil_div(d.C, 64) * 64) > SPLITW_MAX) return false;
-  const long long m_tiles = gb_ceil_div_ll((long long)d.N * d.OH * d.OW, 128);
-  const int n_tiles = d.K == 64 ? 1 : 2 * d.K / 256;
-  return 2 * m_tiles * n_tiles >= gb_num_sms();
+// Chunked accumulation inside one GEMM (see the file comment): the reduction's
+// k-steps are cut into nch blocks of kch <= 16, each accumulated in its own
+// TMEM block of BN columns.  BN is the widest tile (up to what K needs) whose
+// nch blocks fit TMEM twice (so the epilogue overlaps the next tile), else once.
+struct Chunked {
+  int block_n = 0, nch = 0, kch = 0;
+  long long tiles = 0;
+};
+
+Chunked chunked_plan(const gbconv_desc_s& d) {
+  Chunked c;
+  const int kiters = igemm_kiters(d);
+  c.nch = gb_ceil_div(kiters, KCHUNK_MAX);
+  c.kch = gb_ceil_div(kiters, c.nch);
+  c.nch = gb_ceil_div(kiters, c.kch);
+  const int widest = d.K > 128 ? 256 : (d.K > 64 ? 128 : 64);
+  int bn = widest;
+  while (bn > 64 && 2 * c.nch * bn > 512) bn /= 2;
+  if (c.nch * bn > 512) return Chunked{};  // more than 8 blocks: not this path
+  c.block_n = bn;
+  c.tiles = gb_ceil_div_ll((long long)d.N * d.OH * d.OW, 128) * gb_ceil_div(d.K, bn);
+  return c;
+}
+
+// The chunked GEMM applies (K a multiple of 16, at most 8 accumulator blocks)
+// and its tile grid fills at least half the SMs; smaller grids keep split-K,
+// which spreads the reduction over more CTAs.
+bool use_chunked(const gbconv_desc_s& d) {
+  if (d.K % 16) return false;
+  const Chunked c = chunked_plan(d);
+  return c.block_n > 0 && 2 * c.tiles >= gb_num_sms();
 }
 
 // bf16 has 8 significant bits: every int8 value converts exactly.  Output NHWC
@@ -83,31 +105,6 @@ __global__ void pack_int8_as_bf16_kernel(const int8_t* __restrict__ w,
     const int c = (int)(i % Cp);
     const long long krs = i / Cp;
     wp[i] = __float2bfloat16_rn(c < C ? (float)w[krs * C + c] : 0.f);
-  }
-}
-
-// int8 [K][RS][C] -> bf16 [2K][RS][Cp]: per 64 output channels, 64 rows of low
-// nibbles (w & 15) then 64 rows of high parts ((w - (w & 15)) / 16), zero
-// padded channels
-__global__ void pack_int8_split_kernel(const int8_t* __restrict__ w,
-                                       __nv_bfloat16* __restrict__ wp, int K, int RS, int C,
-                                       int Cp) {
-  const long long total = (long long)2 * K * RS * Cp;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int c = (int)(i % Cp);
-    const long long rowrs = i / Cp;
-    const int rs = (int)(rowrs % RS);
-    const int row = (int)(rowrs / RS);
-    const int k = (row >> 7) * 64 + (row & 63);  // output channel of this row
-    const bool high = (row & 64) != 0;
-    float v = 0.f;
-    if (c < C) {
-      const int wv = w[((long long)k * RS + rs) * C + c];
-      const int lo = wv & 15;
-      v = high ? (float)((wv - lo) / 16) : (float)lo;
-    }
-    wp[i] = __float2bfloat16_rn(v);  // |v| <= 15: exact
   }
 }
 
@@ -175,24 +172,16 @@ int grid_for(long long n) { return (int)std::min<long long>(gb_ceil_div_ll(n, 25
 
 size_t int8_tc_workspace_bytes(const gbconv_desc_s& d) {
   const Plan p = make_plan(d);
-  return split_weights(d) ? p.x_bytes : p.x_bytes + p.part_bytes;
+  return use_chunked(d) ? p.x_bytes : p.x_bytes + p.part_bytes;
 }
 
 size_t int8_tc_packed_bytes(const gbconv_desc_s& d) {
-  return (size_t)(split_weights(d) ? 2 : 1) * d.K * d.R * d.S * gb_ceil_div(d.C, 64) * 64 * 2;
+  return (size_t)d.K * d.R * d.S * gb_ceil_div(d.C, 64) * 64 * 2;
 }
 
 cudaError_t launch_pack_int8_tc_weights(const gbconv_desc_s& d, const void* w, void* wpack,
                                         cudaStream_t st) {
   const int Cp = gb_ceil_div(d.C, 64) * 64;
-  if (split_weights(d)) {
-    const long long total = (long long)2 * d.K * d.R * d.S * Cp;
-    pack_int8_split_kernel<<<grid_for(total), 256, 0, st>>>(
-        static_cast<const int8_t*>(w), static_cast<__nv_bfloat16*>(wpack), d.K, d.R * d.S, d.C,
-        Cp);
-    gb_count_launch();
-    return cudaGetLastError();
-  }
   const long long total = (long long)d.K * d.R * d.S * Cp;
   pack_int8_as_bf16_kernel<<<grid_for(total), 256, 0, st>>>(
       static_cast<const int8_t*>(w), static_cast<__nv_bfloat16*>(wpack), d.K, d.R * d.S, d.C, Cp);
@@ -217,8 +206,8 @@ cudaError_t launch_int8_tc(const gbconv_desc_s& d, const void* x, const void* wp
   db.dtype = CONV_BF16;
   db.act = CONV_ACT_NONE;
   db.has_residual = 0;
-  if (split_weights(d)) {  // one GEMM over 2K columns, int8 written by its epilogue
-    db.K = 2 * d.K;
+  if (use_chunked(d)) {  // one GEMM, int8 written by its epilogue
+    const Chunked c = chunked_plan(d);
     IgemmSplit sp;
     sp.i8_y = static_cast<int8_t*>(y);
     sp.i8_bias = bias;
@@ -226,8 +215,10 @@ cudaError_t launch_int8_tc(const gbconv_desc_s& d, const void* x, const void* wp
     sp.i8_kout = d.K;
     sp.i8_relu = d.act == CONV_ACT_RELU ? 1 : 0;
     sp.i8_nc32 = nc32;
-    return launch_igemm_bf16(db, d.K == 64 ? 128 : 256, xb, wpack, nullptr, nullptr, y, err,
-                             wait_ns, st, sp);
+    sp.i8_nch = c.nch;
+    sp.i8_kch = c.kch;
+    return launch_igemm_bf16(db, c.block_n, xb, wpack, nullptr, nullptr, y, err, wait_ns, st,
+                             sp);
   }
   IgemmSplit sp;
   sp.ksplit = pl.ksplit;

@@ -1,5 +1,6 @@
-"""Bit-exact parity of the int8 implicit GEMM (mma.sync s8, exact int32
-accumulate, fp32 requant, ReLU) with the oracle."""
+"""Bit-exact parity of the int8 convolutions (mma.sync s8 with exact int32
+accumulate; the tcgen05 path with exact fp32 chunks on the bf16 pipe; the
+exact int8 Winograd) with the oracle: fp32 requant, ReLU."""
 import numpy as np
 import pytest
 
@@ -49,7 +50,7 @@ def test_int8_resnet_stage_shapes_full_batch(C, HW, algo):
     (3, 32, 10, 10, 16, 3, 2, 1, False, True),   # stride 2, no ReLU
     (2, 96, 6, 6, 80, 1, 1, 0, True, False),     # 1x1, no bias, C not a 64 multiple
     (1, 64, 5, 5, 256, 3, 1, 2, True, True),     # pad 2 (many fully padded taps)
-    (1, 1024, 4, 5, 64, 3, 1, 1, True, True),    # 9216 products > the split-weight bound: chunked
+    (1, 1024, 4, 5, 64, 3, 1, 1, True, True),    # 9216 products: 9 exact chunks
 ])
 @pytest.mark.parametrize("algo", ALGOS)
 def test_int8_edge_cases(case, algo):
@@ -84,33 +85,35 @@ def test_int8_saturation_extremes(algo):
 
 
 @pytest.mark.parametrize("N", [2, 200])
-def test_int8_split_weight_bound_extremes(N):
-    """The largest exact sums: x = -128 everywhere and w alternating 127 / -128
-    over C = 512 (4608 products per output), so on the split-weight path the
-    low-nibble sums reach -128 * 15 * 4608 and the high-part sums -128 * 7 * 4608
-    (and +128 * 8 * 4608 for w = -128); requant into saturation both ways.
-    N = 200 (77 tiles of 128 pixels) takes the split-weight path, N = 2 (one
-    tile) the chunked split-K path; every image is the same, so the oracle
-    computes one and each image is compared with it."""
+@pytest.mark.parametrize("C,R", [(512, 3), (1024, 1)])
+def test_int8_chunk_bound_extremes(N, C, R):
+    """The largest exact sums: x = -128 everywhere and w alternating 127 / -128,
+    so every product is -16256 or +16384.  C = 512, 3x3: 72 k-steps of 64
+    products in five accumulator blocks of at most 15 k-steps (|block sum| <=
+    960 * 2^14); C = 1024, 1x1: a single block of 16 k-steps whose sums reach
+    exactly 2^24 = 1024 * 128 * 128 for the w = -128 channels.  N = 200 (77 tiles
+    of 128 pixels) takes the chunked GEMM, N = 2 (one tile) split-K; every image
+    is the same, so the oracle computes one and each image is compared with it."""
     torch = need_gpu()
     from cnn_convolution_gemm_gb300 import binding as B
     from cnn_convolution_gemm_gb300.layer import ConvLayer
     dev = torch.device("cuda:0")
-    C, H, K = 512, 7, 64
+    H, K = 7, 64
+    pad = R // 2
     x = np.full((N, H, H, C), -128, np.int8)
     w = np.where(np.arange(K)[:, None, None, None] % 2 == 0, 127, -128).astype(np.int8) * np.ones(
-        (K, 3, 3, C), np.int8)
+        (K, R, R, C), np.int8)
     scale = np.full(K, 1e-5, np.float32)
-    layer = ConvLayer(N, C, H, H, K, 3, 3, 1, 1, dtype=B.CONV_INT8,
+    layer = ConvLayer(N, C, H, H, K, R, R, 1, pad, dtype=B.CONV_INT8,
                       scale=torch.from_numpy(scale).to(dev))
     layer.prepack(torch.from_numpy(w).to(dev), INT8_TC)
-    # the split-weight path needs no fp32 partials: its workspace is the bf16 copy alone
+    # the chunked GEMM needs no fp32 partials: its workspace is the bf16 copy alone
     bf16_copy = (N * H * H * C * 2 + 255) // 256 * 256
-    split_weight = B.conv_workspace_size(layer.desc, INT8_TC) == bf16_copy
-    assert split_weight == (N == 200)
+    chunked = B.conv_workspace_size(layer.desc, INT8_TC) == bf16_copy
+    assert chunked == (N == 200)
     y = layer(torch.from_numpy(x).to(dev))
     B.conv_sync_status(torch.cuda.current_stream().cuda_stream)
-    ref = nchw_to_nhwc(ol.conv2d_i8(nhwc_to_nchw(x[:1]), nhwc_to_nchw(w), None, scale, pad=1,
+    ref = nchw_to_nhwc(ol.conv2d_i8(nhwc_to_nchw(x[:1]), nhwc_to_nchw(w), None, scale, pad=pad,
                                     relu=False))
     yn = y.cpu().numpy()
     for n in range(N):
@@ -146,8 +149,8 @@ def test_nc32hw32_conversion_roundtrip():
 
 
 @pytest.mark.parametrize("case", [
-    # N, C, H, W, K, algo — tcgen05 split-weight path (grid >= half the SMs), its split-K
-    # fallback (K not a multiple of 64), and the direct kernel
+    # N, C, H, W, K, algo — tcgen05 chunked GEMM (grid >= half the SMs), its split-K
+    # fallback (a one-tile grid, K not a multiple of 64), and the direct kernel
     (32, 64, 28, 28, 64, INT8_TC),
     (2, 64, 14, 14, 96, INT8_TC),
     (2, 32, 6, 5, 64, 0),
