@@ -242,7 +242,7 @@ static const char* const kAlgoNames[CONV_ALGO_COUNT] = {
     "direct", "igemm_tc_n64", "igemm_tc_n128", "igemm_tc_n256",
     "winograd_f2x2_3x3", "winograd_f6x6_3x3", "depthwise3x3", "int8_igemm_mma",
     "int8_igemm_tc", "im2col_gemm", "stem_s2d_igemm", "igemm_tf32",
-    "int8_winograd_f2x2_3x3", "stem_s2d4_igemm", "igemm_tc_2sm_n256"};
+    "int8_winograd_f2x2_3x3", "stem_s2d4_igemm", "igemm_tc_2sm_n256", "int8_igemm_tc_chunked"};
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -303,6 +303,7 @@ static bool applicable(const gbconv_desc_s& d, int algo, const char** why) {
       if (d.C % 16 || d.K % 16) return *why = "needs C and K multiples of 16", false;
       return true;
     case CONV_ALGO_INT8_TC:
+    case CONV_ALGO_INT8_TC_CHUNK:
       if (d.dtype != CONV_INT8 || !(nhwc || d.layout == CONV_NC32HW32))
         return *why = "needs int8 NHWC or NC32HW32", false;
       if (!d.scale) return *why = "int8 needs a requant scale", false;
@@ -492,7 +493,7 @@ extern "C" conv_status_t conv_workspace_size(conv_desc_t d, conv_algo_t algo, si
   *bytes = 0;
   if (a == CONV_ALGO_WINO_F2 || a == CONV_ALGO_WINO_F6)
     *bytes = winograd_workspace_bytes(*d, a == CONV_ALGO_WINO_F2 ? 2 : 6);
-  if (a == CONV_ALGO_INT8_TC) *bytes = int8_tc_workspace_bytes(*d);
+  if (a == CONV_ALGO_INT8_TC || a == CONV_ALGO_INT8_TC_CHUNK) *bytes = int8_tc_workspace_bytes(*d, a);
   if (a == CONV_ALGO_IM2COL_GEMM) *bytes = im2col_workspace_bytes(*d);
   if (a == CONV_ALGO_STEM_S2D) *bytes = stem_s2d_workspace_bytes(*d);
   if (a == CONV_ALGO_STEM_S2D4) *bytes = stem_s2d4_workspace_bytes(*d);
@@ -536,7 +537,8 @@ extern "C" conv_status_t conv_weights_packed_size(conv_desc_t d, conv_algo_t alg
       *bytes = igemm_group_packed_bytes(group_view(*d)) * d->groups;
       break;
     case CONV_ALGO_INT8_MMA: *bytes = (size_t)d->K * d->R * d->S * Cp64; break;
-    case CONV_ALGO_INT8_TC: *bytes = int8_tc_packed_bytes(*d); break;
+    case CONV_ALGO_INT8_TC:
+    case CONV_ALGO_INT8_TC_CHUNK: *bytes = int8_tc_packed_bytes(*d, a); break;
     case CONV_ALGO_IM2COL_GEMM: *bytes = im2col_packed_bytes(*d); break;
     case CONV_ALGO_STEM_S2D: *bytes = stem_s2d_packed_bytes(*d); break;
     case CONV_ALGO_STEM_S2D4: *bytes = stem_s2d4_packed_bytes(*d); break;
@@ -571,7 +573,8 @@ extern "C" conv_status_t conv_weights_prepack(conv_desc_t d, conv_algo_t algo, c
       break;
     }
     case CONV_ALGO_INT8_MMA: e = launch_pack_int8_weights(*d, w, wpack, s); break;
-    case CONV_ALGO_INT8_TC: e = launch_pack_int8_tc_weights(*d, w, wpack, s); break;
+    case CONV_ALGO_INT8_TC:
+    case CONV_ALGO_INT8_TC_CHUNK: e = launch_pack_int8_tc_weights(*d, a, w, wpack, s); break;
     case CONV_ALGO_IM2COL_GEMM: e = launch_pack_im2col_weights(*d, w, wpack, s); break;
     case CONV_ALGO_STEM_S2D: e = launch_pack_stem_weights(*d, w, wpack, s); break;
     case CONV_ALGO_STEM_S2D4: e = launch_pack_stem4_weights(*d, w, wpack, s); break;
@@ -679,13 +682,15 @@ static conv_status_t fwd_impl(const gbconv_desc_s& d, const void* x, const void*
       e = launch_stem_s2d4(d, x, wpack, static_cast<const float*>(bias), y, ws, err, wait_ns, s);
       break;
     }
-    case CONV_ALGO_INT8_TC: {
-      const size_t need = int8_tc_workspace_bytes(d);
+    case CONV_ALGO_INT8_TC:
+    case CONV_ALGO_INT8_TC_CHUNK: {
+      const size_t need = int8_tc_workspace_bytes(d, a);
       if (!ws || ws_bytes < need)
         return gb_fail(CONV_ERR_WORKSPACE, "workspace of %zu bytes needed", need);
       if (reinterpret_cast<uintptr_t>(ws) & 255u)
         return gb_fail(CONV_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
-      e = launch_int8_tc(d, x, wpack, static_cast<const int32_t*>(bias), y, ws, err, wait_ns, s);
+      e = launch_int8_tc(d, a, x, wpack, static_cast<const int32_t*>(bias), y, ws, err, wait_ns,
+                         s);
       break;
     }
     case CONV_ALGO_WINO_F2:
@@ -1426,6 +1431,7 @@ static bool implemented(int algo) {
     case CONV_ALGO_STEM_S2D4:
     case CONV_ALGO_IGEMM_TF32:
     case CONV_ALGO_INT8_WINO_F2:
+    case CONV_ALGO_INT8_TC_CHUNK:
       return true;
     default:
       return false;

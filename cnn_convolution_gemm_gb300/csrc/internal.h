@@ -146,11 +146,13 @@ cudaError_t launch_pack_int8_weights(const gbconv_desc_s& d, const void* w, void
 
 // int8 on tcgen05 with bf16 as the carrier (exact split-K, see k_int8_tc.cu).
 // wpack: [K][R*S][Cp] bf16.
-size_t int8_tc_workspace_bytes(const gbconv_desc_s& d);
-size_t int8_tc_packed_bytes(const gbconv_desc_s& d);
-cudaError_t launch_pack_int8_tc_weights(const gbconv_desc_s& d, const void* w, void* wpack,
-                                        cudaStream_t st);
-cudaError_t launch_int8_tc(const gbconv_desc_s& d, const void* x, const void* wpack,
+// algo: CONV_ALGO_INT8_TC (split weights, else split-K) or CONV_ALGO_INT8_TC_CHUNK
+// (chunked accumulation, else split-K).
+size_t int8_tc_workspace_bytes(const gbconv_desc_s& d, int algo);
+size_t int8_tc_packed_bytes(const gbconv_desc_s& d, int algo);
+cudaError_t launch_pack_int8_tc_weights(const gbconv_desc_s& d, int algo, const void* w,
+                                        void* wpack, cudaStream_t st);
+cudaError_t launch_int8_tc(const gbconv_desc_s& d, int algo, const void* x, const void* wpack,
                            const int32_t* bias, void* y, void* ws, int* err,
                            unsigned long long wait_ns, cudaStream_t st);
 

@@ -603,24 +603,30 @@ __global__ void __launch_bounds__(192, 1)
           }
           __syncwarp();
 #pragma unroll 1
-          for (int c16 = 0; c16 < 4; ++c16) {
-            const int kb = k0 + c16 * 16;
+          for (int c8 = 0; c8 < 8; ++c8) {
+            const int kb = k0 + c8 * 8;
             if (kb >= p.i8_kout) break;  // i8_kout % 16 == 0
-            int tv[16];
+            int tv[8];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) tv[i] = sbi[c16 * 16 + i];
+            for (int i = 0; i < 8; ++i) tv[i] = sbi[c8 * 8 + i];
+            // two blocks' loads in flight per wait (the block count is
+            // warp-uniform, so every lane takes the same loads)
 #pragma unroll 1
-            for (int c = 0; c < p.i8_nch; ++c) {
-              uint32_t v[16];
-              gb::tmem_ld_x16(tbase + c * BN + g * 64 + c16 * 16, v);
+            for (int c0 = 0; c0 < p.i8_nch; c0 += 2) {
+              uint32_t v0[8], v1[8];
+              const bool two = c0 + 1 < p.i8_nch;
+              gb::tmem_ld_x8(tbase + c0 * BN + g * 64 + c8 * 8, v0);
+              if (two) gb::tmem_ld_x8(tbase + (c0 + 1) * BN + g * 64 + c8 * 8, v1);
               gb::tmem_ld_wait();
 #pragma unroll
-              for (int i = 0; i < 16; ++i) tv[i] += __float2int_rn(__uint_as_float(v[i]));
+              for (int i = 0; i < 8; ++i)
+                tv[i] += __float2int_rn(__uint_as_float(v0[i])) +
+                         (two ? __float2int_rn(__uint_as_float(v1[i])) : 0);
             }
-            uint32_t pk[4] = {0u, 0u, 0u, 0u};
+            uint32_t pk[2] = {0u, 0u};
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              int qv = __float2int_rn(__fmul_rn(__int2float_rn(tv[i]), ssc[c16 * 16 + i]));
+            for (int i = 0; i < 8; ++i) {
+              int qv = __float2int_rn(__fmul_rn(__int2float_rn(tv[i]), ssc[c8 * 8 + i]));
               qv = qv > 127 ? 127 : (qv < -128 ? -128 : qv);
               if (p.i8_relu && qv < 0) qv = 0;
               pk[i >> 2] |= (uint32_t)(qv & 0xff) << (8 * (i & 3));
@@ -632,7 +638,7 @@ __global__ void __launch_bounds__(192, 1)
                 const long long ohw = (long long)p.OH * p.OW, img = m / ohw;
                 off = ((img * (p.i8_kout / 32) + kb / 32) * ohw + (m - img * ohw)) * 32 + (kb & 31);
               }
-              *reinterpret_cast<uint4*>(p.i8_y + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              *reinterpret_cast<uint2*>(p.i8_y + off) = make_uint2(pk[0], pk[1]);
             }
           }
         }

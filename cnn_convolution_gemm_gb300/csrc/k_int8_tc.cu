@@ -10,20 +10,35 @@
 // report's native int8 inference: + int32 bias, fp32 requantisation
 // q = clamp(rne(fp32(acc + bias) * scale[k]), -128, 127), ReLU.
 //
-// Steps per call: int8 -> bf16 copy of the activations (workspace), then one of
+// Steps per call: int8 -> bf16 copy of the activations (workspace), then one
+// of three plans.  Two algorithm ids share this file and Fast-Run times both:
+// int8_igemm_tc (split weights, else split-K) and int8_igemm_tc_chunked
+// (chunked accumulation, else split-K).
 //
-// Chunked accumulation (when the layer's tiles fill at least half the SMs): one
-// implicit GEMM over the plain bf16 weights whose MMAs start a fresh TMEM
-// accumulator block every kch <= 16 k-steps (at most 1024 products, so each
-// block's sums are exact integers in fp32); its epilogue converts the blocks
-// to int32, adds them and the bias, requantises and stores int8.  The tensor
-// cores do exactly the direct-equivalent work and nothing goes to memory but
-// the int8 output.  A reduction of at most 16 k-steps (ResNet-50's 64-channel
-// 3x3 stage: 9) is a single block.
+// Split weights (int8_igemm_tc, when K % 64 == 0, R*S*C <= 8704 and the grid
+// fills at least half the SMs): each weight is cut at prepack into
+// w = 16 * wh + wl, wl = w & 15 in [0, 15] and wh in [-8, 7].  Products x * wl
+// are at most 128 * 15 = 1920 and x * wh at most 128 * 8 = 1024 in magnitude,
+// so an fp32 accumulator stays exact over 8704 products (8704 * 1920 < 2^24):
+// every ResNet int8 layer (at most 4608) needs no split of the reduction.  One
+// implicit GEMM over 2K columns (per 64 output channels: 64 low-part columns,
+// 64 high-part columns) finishes in its own epilogue -- t = 16 * hi + lo +
+// bias, requant, ReLU, int8 store -- at twice the tensor work, with wide
+// (256-column) tiles that read each activation tile once per 128 channels.
 //
-// Split-K (smaller grids): the GEMM's split-K mode writes each chunk's exact
-// fp32 partial sums to the workspace and a reduction pass sums them in int32
-// and requantises, so the chunks also spread over otherwise idle SMs.
+// Chunked accumulation (int8_igemm_tc_chunked, when K % 16 == 0 and the grid
+// fills at least half the SMs): one implicit GEMM over the plain bf16 weights
+// whose MMAs start a fresh TMEM accumulator block every kch <= 16 k-steps (at
+// most 1024 products, so each block's sums are exact integers in fp32); its
+// epilogue converts the blocks to int32, adds them and the bias, requantises
+// and stores int8.  The tensor cores do exactly the direct-equivalent work,
+// but the blocks share the SM's 512 TMEM columns, so deep reductions get
+// narrower tiles.  A reduction of at most 16 k-steps is a single block.
+//
+// Split-K (smaller grids, either id): the GEMM's split-K mode writes each
+// chunk's exact fp32 partial sums to the workspace and a reduction pass sums
+// them in int32 and requantises, so the chunks also spread over otherwise idle
+// SMs.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -68,6 +83,19 @@ bool use_chunked(const gbconv_desc_s& d) {
   return c.block_n > 0 && 2 * c.tiles >= gb_num_sms();
 }
 
+constexpr int SPLITW_MAX = 8704;  // products per output that stay exact with split weights
+
+// the split-weight path applies (see the file comment) and its unsplit tile
+// grid fills at least half the SMs; smaller grids keep split-K, which spreads the
+// reduction (measured on the ResNet-50 stage shapes at batch 32: 256@14 with 98
+// tiles runs faster split-weight, 512@7 with 52 tiles faster split-K)
+bool split_weights(const gbconv_desc_s& d) {
+  if (d.K % 64 || (long long)d.R * d.S * (gb_ceil_div(d.C, 64) * 64) > SPLITW_MAX) return false;
+  const long long m_tiles = gb_ceil_div_ll((long long)d.N * d.OH * d.OW, 128);
+  const int n_tiles = d.K == 64 ? 1 : 2 * d.K / 256;
+  return 2 * m_tiles * n_tiles >= gb_num_sms();
+}
+
 // bf16 has 8 significant bits: every int8 value converts exactly.  Output NHWC
 // bf16, 16 channels per thread; the int8 input is NHWC, or NC32HW32 (nc32 = 1:
 // the same 16 channels are one 16-byte half of a 32-channel block vector).
@@ -105,6 +133,31 @@ __global__ void pack_int8_as_bf16_kernel(const int8_t* __restrict__ w,
     const int c = (int)(i % Cp);
     const long long krs = i / Cp;
     wp[i] = __float2bfloat16_rn(c < C ? (float)w[krs * C + c] : 0.f);
+  }
+}
+
+// int8 [K][RS][C] -> bf16 [2K][RS][Cp]: per 64 output channels, 64 rows of low
+// nibbles (w & 15) then 64 rows of high parts ((w - (w & 15)) / 16), zero
+// padded channels
+__global__ void pack_int8_split_kernel(const int8_t* __restrict__ w,
+                                       __nv_bfloat16* __restrict__ wp, int K, int RS, int C,
+                                       int Cp) {
+  const long long total = (long long)2 * K * RS * Cp;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int c = (int)(i % Cp);
+    const long long rowrs = i / Cp;
+    const int rs = (int)(rowrs % RS);
+    const int row = (int)(rowrs / RS);
+    const int k = (row >> 7) * 64 + (row & 63);  // output channel of this row
+    const bool high = (row & 64) != 0;
+    float v = 0.f;
+    if (c < C) {
+      const int wv = w[((long long)k * RS + rs) * C + c];
+      const int lo = wv & 15;
+      v = high ? (float)((wv - lo) / 16) : (float)lo;
+    }
+    wp[i] = __float2bfloat16_rn(v);  // |v| <= 15: exact
   }
 }
 
@@ -168,20 +221,37 @@ Plan make_plan(const gbconv_desc_s& d) {
 
 int grid_for(long long n) { return (int)std::min<long long>(gb_ceil_div_ll(n, 256), 148LL * 32); }
 
+// the plan algorithm `algo` (int8_igemm_tc or its chunked variant) runs on d
+enum class I8Plan { SplitWeights, Chunked, SplitK };
+
+I8Plan plan_for(const gbconv_desc_s& d, int algo) {
+  if (algo == CONV_ALGO_INT8_TC_CHUNK) return use_chunked(d) ? I8Plan::Chunked : I8Plan::SplitK;
+  return split_weights(d) ? I8Plan::SplitWeights : I8Plan::SplitK;
+}
+
 }  // namespace
 
-size_t int8_tc_workspace_bytes(const gbconv_desc_s& d) {
+size_t int8_tc_workspace_bytes(const gbconv_desc_s& d, int algo) {
   const Plan p = make_plan(d);
-  return use_chunked(d) ? p.x_bytes : p.x_bytes + p.part_bytes;
+  return plan_for(d, algo) == I8Plan::SplitK ? p.x_bytes + p.part_bytes : p.x_bytes;
 }
 
-size_t int8_tc_packed_bytes(const gbconv_desc_s& d) {
-  return (size_t)d.K * d.R * d.S * gb_ceil_div(d.C, 64) * 64 * 2;
+size_t int8_tc_packed_bytes(const gbconv_desc_s& d, int algo) {
+  return (size_t)(plan_for(d, algo) == I8Plan::SplitWeights ? 2 : 1) * d.K * d.R * d.S *
+         gb_ceil_div(d.C, 64) * 64 * 2;
 }
 
-cudaError_t launch_pack_int8_tc_weights(const gbconv_desc_s& d, const void* w, void* wpack,
-                                        cudaStream_t st) {
+cudaError_t launch_pack_int8_tc_weights(const gbconv_desc_s& d, int algo, const void* w,
+                                        void* wpack, cudaStream_t st) {
   const int Cp = gb_ceil_div(d.C, 64) * 64;
+  if (plan_for(d, algo) == I8Plan::SplitWeights) {
+    const long long total = (long long)2 * d.K * d.R * d.S * Cp;
+    pack_int8_split_kernel<<<grid_for(total), 256, 0, st>>>(
+        static_cast<const int8_t*>(w), static_cast<__nv_bfloat16*>(wpack), d.K, d.R * d.S, d.C,
+        Cp);
+    gb_count_launch();
+    return cudaGetLastError();
+  }
   const long long total = (long long)d.K * d.R * d.S * Cp;
   pack_int8_as_bf16_kernel<<<grid_for(total), 256, 0, st>>>(
       static_cast<const int8_t*>(w), static_cast<__nv_bfloat16*>(wpack), d.K, d.R * d.S, d.C, Cp);
@@ -189,10 +259,11 @@ cudaError_t launch_pack_int8_tc_weights(const gbconv_desc_s& d, const void* w, v
   return cudaGetLastError();
 }
 
-cudaError_t launch_int8_tc(const gbconv_desc_s& d, const void* x, const void* wpack,
+cudaError_t launch_int8_tc(const gbconv_desc_s& d, int algo, const void* x, const void* wpack,
                            const int32_t* bias, void* y, void* ws, int* err,
                            unsigned long long wait_ns, cudaStream_t st) {
   const Plan pl = make_plan(d);
+  const I8Plan plan = plan_for(d, algo);
   __nv_bfloat16* xb = static_cast<__nv_bfloat16*>(ws);
   float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.x_bytes);
   const long long n16 = (long long)d.N * d.H * d.W * d.C / 16;
@@ -206,8 +277,7 @@ cudaError_t launch_int8_tc(const gbconv_desc_s& d, const void* x, const void* wp
   db.dtype = CONV_BF16;
   db.act = CONV_ACT_NONE;
   db.has_residual = 0;
-  if (use_chunked(d)) {  // one GEMM, int8 written by its epilogue
-    const Chunked c = chunked_plan(d);
+  if (plan != I8Plan::SplitK) {  // one GEMM, int8 written by its epilogue
     IgemmSplit sp;
     sp.i8_y = static_cast<int8_t*>(y);
     sp.i8_bias = bias;
@@ -215,6 +285,12 @@ cudaError_t launch_int8_tc(const gbconv_desc_s& d, const void* x, const void* wp
     sp.i8_kout = d.K;
     sp.i8_relu = d.act == CONV_ACT_RELU ? 1 : 0;
     sp.i8_nc32 = nc32;
+    if (plan == I8Plan::SplitWeights) {  // 2K columns: low and high weight parts
+      db.K = 2 * d.K;
+      return launch_igemm_bf16(db, d.K == 64 ? 128 : 256, xb, wpack, nullptr, nullptr, y, err,
+                               wait_ns, st, sp);
+    }
+    const Chunked c = chunked_plan(d);
     sp.i8_nch = c.nch;
     sp.i8_kch = c.kch;
     return launch_igemm_bf16(db, c.block_n, xb, wpack, nullptr, nullptr, y, err, wait_ns, st,

@@ -77,7 +77,8 @@ typedef int conv_algo_t;
 #define CONV_ALGO_WINO_F6 5        /* Winograd F(6x6,3x3)                               */
 #define CONV_ALGO_DEPTHWISE 6      /* depthwise 3x3 (groups == C == K)                  */
 #define CONV_ALGO_INT8_MMA 7       /* int8 implicit GEMM on mma.sync, exact int32 acc.  */
-#define CONV_ALGO_INT8_TC 8        /* int8 on tcgen05 via exact bf16 chunks (workspace) */
+#define CONV_ALGO_INT8_TC 8        /* int8 on tcgen05, exact: weights split into 4-bit
+                                      parts over 2K GEMM columns (workspace)            */
 #define CONV_ALGO_IM2COL_GEMM 9    /* materialised im2col matrix + GEMM (workspace)     */
 #define CONV_ALGO_STEM_S2D 10      /* stride-2 conv over 8 channels (the image stem) as
                                       space-to-depth + stride-1 implicit GEMM (workspace) */
@@ -92,7 +93,11 @@ typedef int conv_algo_t;
                                       workspace)                                         */
 #define CONV_ALGO_IGEMM_2SM 14     /* implicit GEMM with 256 x 256 tiles split over a pair
                                       of SMs (tcgen05 cta_group::2; groups 1, C != 8)   */
-#define CONV_ALGO_COUNT 15
+#define CONV_ALGO_INT8_TC_CHUNK 15 /* int8 on tcgen05, exact by chunked accumulation: a
+                                      fresh TMEM accumulator every <= 16 k-steps, the
+                                      blocks summed in int32 by the epilogue (1x the
+                                      tensor work; workspace)                           */
+#define CONV_ALGO_COUNT 16
 
 /* ---- descriptor --------------------------------------------------------- */
 

@@ -9,8 +9,9 @@ from tests.gpu_util import need_gpu, nchw_to_nhwc, nhwc_to_nchw
 
 pytestmark = pytest.mark.gpu
 INT8_MMA = 7
-INT8_TC = 8
-ALGOS = [INT8_MMA, INT8_TC]
+INT8_TC = 8          # split weights (else split-K)
+INT8_TC_CHUNK = 15   # chunked accumulation (else split-K)
+ALGOS = [INT8_MMA, INT8_TC, INT8_TC_CHUNK]
 
 
 def _run(torch, N, C, H, W, K, R, stride, pad, relu=True, bias=True, seed=0, algo=INT8_MMA):
@@ -106,14 +107,49 @@ def test_int8_chunk_bound_extremes(N, C, R):
     scale = np.full(K, 1e-5, np.float32)
     layer = ConvLayer(N, C, H, H, K, R, R, 1, pad, dtype=B.CONV_INT8,
                       scale=torch.from_numpy(scale).to(dev))
-    layer.prepack(torch.from_numpy(w).to(dev), INT8_TC)
+    layer.prepack(torch.from_numpy(w).to(dev), INT8_TC_CHUNK)
     # the chunked GEMM needs no fp32 partials: its workspace is the bf16 copy alone
     bf16_copy = (N * H * H * C * 2 + 255) // 256 * 256
-    chunked = B.conv_workspace_size(layer.desc, INT8_TC) == bf16_copy
+    chunked = B.conv_workspace_size(layer.desc, INT8_TC_CHUNK) == bf16_copy
     assert chunked == (N == 200)
     y = layer(torch.from_numpy(x).to(dev))
     B.conv_sync_status(torch.cuda.current_stream().cuda_stream)
     ref = nchw_to_nhwc(ol.conv2d_i8(nhwc_to_nchw(x[:1]), nhwc_to_nchw(w), None, scale, pad=pad,
+                                    relu=False))
+    yn = y.cpu().numpy()
+    for n in range(N):
+        assert np.array_equal(yn[n:n + 1], ref), n
+    assert (ref == -128).any() and (ref == 127).any()
+
+
+@pytest.mark.parametrize("N", [2, 200])
+def test_int8_split_weight_bound_extremes(N):
+    """The largest exact sums of the split-weight GEMM: x = -128 everywhere and w
+    alternating 127 / -128 over C = 512 (4608 products per output), so the
+    low-nibble sums reach -128 * 15 * 4608 and the high-part sums -128 * 7 * 4608
+    (and +128 * 8 * 4608 for w = -128); requant into saturation both ways.
+    N = 200 (77 tiles of 128 pixels) takes the split-weight path, N = 2 (one
+    tile) split-K; every image is the same, so the oracle computes one and each
+    image is compared with it."""
+    torch = need_gpu()
+    from cnn_convolution_gemm_gb300 import binding as B
+    from cnn_convolution_gemm_gb300.layer import ConvLayer
+    dev = torch.device("cuda:0")
+    C, H, K = 512, 7, 64
+    x = np.full((N, H, H, C), -128, np.int8)
+    w = np.where(np.arange(K)[:, None, None, None] % 2 == 0, 127, -128).astype(np.int8) * np.ones(
+        (K, 3, 3, C), np.int8)
+    scale = np.full(K, 1e-5, np.float32)
+    layer = ConvLayer(N, C, H, H, K, 3, 3, 1, 1, dtype=B.CONV_INT8,
+                      scale=torch.from_numpy(scale).to(dev))
+    layer.prepack(torch.from_numpy(w).to(dev), INT8_TC)
+    # the split-weight path needs no fp32 partials: its workspace is the bf16 copy alone
+    bf16_copy = (N * H * H * C * 2 + 255) // 256 * 256
+    split_weight = B.conv_workspace_size(layer.desc, INT8_TC) == bf16_copy
+    assert split_weight == (N == 200)
+    y = layer(torch.from_numpy(x).to(dev))
+    B.conv_sync_status(torch.cuda.current_stream().cuda_stream)
+    ref = nchw_to_nhwc(ol.conv2d_i8(nhwc_to_nchw(x[:1]), nhwc_to_nchw(w), None, scale, pad=1,
                                     relu=False))
     yn = y.cpu().numpy()
     for n in range(N):
@@ -149,10 +185,13 @@ def test_nc32hw32_conversion_roundtrip():
 
 
 @pytest.mark.parametrize("case", [
-    # N, C, H, W, K, algo — tcgen05 chunked GEMM (grid >= half the SMs), its split-K
-    # fallback (a one-tile grid, K not a multiple of 64), and the direct kernel
+    # N, C, H, W, K, algo — tcgen05 split-weight and chunked GEMMs (grid >= half
+    # the SMs), their split-K fallback (a small grid, K not a multiple of 64),
+    # and the direct kernel
     (32, 64, 28, 28, 64, INT8_TC),
+    (32, 128, 28, 28, 128, INT8_TC_CHUNK),
     (2, 64, 14, 14, 96, INT8_TC),
+    (2, 64, 14, 14, 96, INT8_TC_CHUNK),
     (2, 32, 6, 5, 64, 0),
 ])
 def test_int8_nc32hw32_layout(case):

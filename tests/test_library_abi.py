@@ -187,7 +187,8 @@ def test_nc32hw32_layout_validation(B):
     B.conv_desc_set_layout(i64, B.CONV_NC32HW32)
     B.conv_desc_set_requant(i64, 0x1000)  # a device address stand-in: no call runs here
     ok = {n: a for _, n, a in (B.conv_algo_info(i64, i) for i in range(B.CONV_ALGO_COUNT))}
-    assert ok["int8_igemm_tc"] and ok["direct"] and not ok["int8_igemm_mma"]
+    assert ok["int8_igemm_tc"] and ok["int8_igemm_tc_chunked"] and ok["direct"]
+    assert not ok["int8_igemm_mma"]
     for h in (bf, i48, i64):
         B.conv_desc_destroy(h)
 
