@@ -317,6 +317,288 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// ---- F(2x2,3x3): the batched GEMM with the output transform in its epilogue ----
+//
+// One CTA work unit: 128 consecutive Winograd tiles (rows of V) x 64 output
+// channels.  Its 16 products M_xi,nu = V_xi,nu . U_xi,nu^T (128 x 64 each, fp32,
+// reduced over C) are computed in four groups, one per row xi of the 4 x 4
+// transformed tile.  A group's four accumulators take 4 x 64 TMEM columns; two
+// groups alternate in the 512 columns, so the epilogue drains one while the
+// MMAs fill the other.  The epilogue adds every product into the 2 x 2 outputs
+// of its tiles (the output transform Y = A^T M A, term by term):
+//   Y[i][j] += AT[i][xi] * AT[j][nu] * M_xi,nu
+// in registers, and after the fourth group adds bias and residual, applies the
+// activation and writes bf16 y.  The fp32 products never leave the SM, which
+// is the MegEngine report's point (section "Winograd"): the transformed data
+// of a block of tiles is consumed on chip, without a re-pack through memory.
+//
+// Warps: 0 TMA producer, 1 MMA issuer (one thread each), 2..9 epilogue.  An
+// epilogue warp reads TMEM lane quarter (warp % 4) -- 32 tiles -- and one half
+// (32) of the unit's 64 channels: 2 x 2 x 32 fp32 accumulators per thread.
+namespace wf {
+constexpr int BM = 128;                       // tiles per unit (TMEM lanes)
+constexpr int BN = 64;                        // output channels per unit
+constexpr int BK = 64;                        // channels per k-step (128-byte rows)
+constexpr int A_BYTES = BM * BK * 2;          // V tile, 16 KB
+constexpr int B_BYTES = BN * BK * 2;          // U tile, 8 KB
+constexpr int STAGE = A_BYTES + B_BYTES;
+constexpr int STAGES = 8;
+constexpr int GROUP_COLS = 4 * BN;            // one row xi: four 64-column products
+constexpr int TMEM_COLS = 2 * GROUP_COLS;     // two groups in flight
+constexpr int THREADS = 320;
+constexpr int SMEM = STAGES * STAGE + 256 + 1024;
+}  // namespace wf
+
+struct Wino2Params {
+  int C, K, OH, OW, th, tw, act;
+  int n0;        // first image of the chunk
+  int T;         // tiles in the chunk (rows of V)
+  int cblocks;   // k-steps per product: ceil(C / 64)
+  int m_tiles, n_tiles;
+  const float* bias;
+  const __nv_bfloat16* res;
+  __nv_bfloat16* y;
+  int* err;
+  unsigned long long wait_ns;
+};
+
+__global__ void __launch_bounds__(wf::THREADS, 1)
+    wino2_fused_kernel(const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_u, const Wino2Params p) {
+  using TT = F2T;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + wf::STAGES * wf::A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + wf::STAGES * wf::STAGE);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + wf::STAGES;
+  uint64_t* tfull = bars + 2 * wf::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < wf::STAGES; ++s) {
+      gb::mbar_init(&full[s], 1);
+      gb::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      gb::mbar_init(&tfull[b], 1);
+      gb::mbar_init(&tempty[b], 8);  // one arrival per epilogue warp
+    }
+    gb::mbar_init(mma_done, 1);
+    gb::fence_barrier_init();
+    gb::tma_prefetch_desc(&tm_v);
+    gb::tma_prefetch_desc(&tm_u);
+  }
+  if (warp == 0) {
+    gb::tmem_alloc(tmem_slot, wf::TMEM_COLS);
+    gb::tmem_relinquish();
+  }
+  gb::tc_fence_before();
+  __syncthreads();
+  gb::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int units = p.m_tiles * p.n_tiles;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- producer: for each product, its V tile and U tile per k-step ----
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const int mt = u / p.n_tiles, nt = u % p.n_tiles;
+        for (int a = 0; a < 16 && ok; ++a)
+          for (int cb = 0; cb < p.cblocks; ++cb) {
+            if (!gb::mbar_wait_bounded(&empty[stage], phase ^ 1, p.wait_ns, p.err)) {
+              ok = false;
+              break;
+            }
+            gb::mbar_arrive_expect_tx(&full[stage], wf::STAGE);
+            gb::tma_load_3d(sA + stage * wf::A_BYTES, &tm_v, &full[stage], cb * wf::BK,
+                            mt * wf::BM, a);
+            gb::tma_load_3d(sB + stage * wf::B_BYTES, &tm_u, &full[stage], cb * wf::BK,
+                            nt * wf::BN, a);
+            ++issued;
+            if (++stage == wf::STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+      }
+      // no copy into shared memory may be in flight when the block exits
+      long long pending = issued < wf::STAGES ? issued : wf::STAGES;
+      int st = stage;
+      uint32_t ph = phase;
+      for (long long i = 0; i < pending; ++i) {
+        if (--st < 0) {
+          st = wf::STAGES - 1;
+          ph ^= 1;
+        }
+        gb::mbar_wait_bounded(&full[st], ph, p.wait_ns, p.err);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer: group xi's four products into one TMEM group ----
+      constexpr uint32_t IDESC = gb::idesc_f16(wf::BM, wf::BN, 1);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t grp = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        for (int xi = 0; xi < 4 && ok; ++xi, ++grp) {
+          const uint32_t buf = grp & 1, gph = (grp >> 1) & 1;
+          if (!gb::mbar_wait_bounded(&tempty[buf], gph ^ 1, p.wait_ns, p.err)) {
+            ok = false;
+            break;
+          }
+          gb::tc_fence_after();
+          for (int nu = 0; nu < 4 && ok; ++nu) {
+            const uint32_t d = tmem_base + buf * wf::GROUP_COLS + nu * wf::BN;
+            for (int cb = 0; cb < p.cblocks; ++cb) {
+              if (!gb::mbar_wait_bounded(&full[stage], phase, p.wait_ns, p.err)) {
+                ok = false;
+                break;
+              }
+              gb::tc_fence_after();
+              const uint32_t a0 = gb::smem_u32(sA + stage * wf::A_BYTES);
+              const uint32_t b0 = gb::smem_u32(sB + stage * wf::B_BYTES);
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                gb::tc_mma_f16(d, gb::sw128_kmajor_desc(a0 + k * 32),
+                               gb::sw128_kmajor_desc(b0 + k * 32), IDESC,
+                               (cb > 0 || k > 0) ? 1u : 0u);
+              gb::tc_commit(&empty[stage]);
+              if (++stage == wf::STAGES) {
+                stage = 0;
+                phase ^= 1;
+              }
+            }
+          }
+          if (ok) gb::tc_commit(&tfull[buf]);
+        }
+      }
+      gb::tc_commit(mma_done);
+      gb::mbar_wait_bounded(mma_done, 0, p.wait_ns, p.err);
+    }
+  } else {
+    // ---- epilogue: output transform, bias, residual, activation, bf16 ----
+    const int q = warp & 3;          // TMEM lane quarter this warp may read
+    const int h = (warp - 2) >> 2;   // which 32 of the unit's 64 channels
+    uint32_t grp = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const int mt = u / p.n_tiles, nt = u % p.n_tiles;
+      float Y[4][32];  // [i * 2 + j][channel]
+#pragma unroll
+      for (int o = 0; o < 4; ++o)
+#pragma unroll
+        for (int c = 0; c < 32; ++c) Y[o][c] = 0.f;
+#pragma unroll
+      for (int xi = 0; xi < 4; ++xi) {
+        const uint32_t buf = grp & 1, gph = (grp >> 1) & 1;
+        ++grp;
+        if (!ok || !gb::mbar_wait_bounded(&tfull[buf], gph, p.wait_ns, p.err)) {
+          ok = false;
+          continue;
+        }
+        gb::tc_fence_after();
+        const uint32_t tcol =
+            tmem_base + ((uint32_t)(q * 32) << 16) + buf * wf::GROUP_COLS + h * 32;
+#pragma unroll
+        for (int piece = 0; piece < 4; ++piece) {
+          uint32_t v[4][8];
+#pragma unroll
+          for (int nu = 0; nu < 4; ++nu) gb::tmem_ld_x8(tcol + nu * wf::BN + piece * 8, v[nu]);
+          gb::tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            // Z_j = sum_nu AT[j][nu] M_xi,nu, then Y[i][j] += AT[i][xi] Z_j
+            float z[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              float a = 0.f;
+#pragma unroll
+              for (int nu = 0; nu < 4; ++nu) a = madd(a, TT::AT(j, nu), __uint_as_float(v[nu][e]));
+              z[j] = a;
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+              for (int j = 0; j < 2; ++j)
+                Y[i * 2 + j][piece * 8 + e] = madd(Y[i * 2 + j][piece * 8 + e], TT::AT(i, xi), z[j]);
+          }
+        }
+        gb::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) gb::mbar_arrive(&tempty[buf]);  // this group's columns are free
+      }
+      if (!ok) break;
+      // outputs of tile t: pixels (2 ti + i, 2 tj + j) of image n, channels kb..kb+31
+      const int t = mt * wf::BM + q * 32 + lane;
+      if (t >= p.T) continue;
+      const int tj = t % p.tw, ti = (t / p.tw) % p.th;
+      const int n = p.n0 + t / (p.tw * p.th);
+      const int kb = nt * wf::BN + h * 32;
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int oh = 2 * ti + i, ow = 2 * tj + j;
+          if (oh >= p.OH || ow >= p.OW) continue;
+          const size_t pix = (((size_t)n * p.OH + oh) * p.OW + ow) * p.K;
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8) {
+            const int k = kb + c8 * 8;
+            if (k >= p.K) break;  // K % 8 == 0
+            float o8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              o8[e] = Y[i * 2 + j][c8 * 8 + e] + (p.bias ? __ldg(p.bias + k + e) : 0.f);
+            if (p.res) {
+              const uint4 r = __ldg(reinterpret_cast<const uint4*>(p.res + pix + k));
+              const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rw[e]));
+                o8[2 * e] += f.x;
+                o8[2 * e + 1] += f.y;
+              }
+            }
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float a0 = o8[2 * e], a1 = o8[2 * e + 1];
+              if (p.act >= 1) {
+                a0 = fmaxf(a0, 0.f);
+                a1 = fmaxf(a1, 0.f);
+              }
+              if (p.act == 2) {
+                a0 = fminf(a0, 6.f);
+                a1 = fminf(a1, 6.f);
+              }
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(a0, a1);
+              pk[e] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            *reinterpret_cast<uint4*>(p.y + pix + k) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+        }
+    }
+  }
+  gb::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    gb::tc_fence_after();
+    gb::tmem_dealloc(tmem_base, wf::TMEM_COLS);
+  }
+}
+
 constexpr size_t kChunkBudget = 64ull << 20;  // V + M bytes per chunk (L2-resident)
 
 int tiles_h(const gbconv_desc_s& d, int m) { return gb_ceil_div(d.OH, m); }
@@ -347,6 +629,120 @@ int images_per_chunk(const gbconv_desc_s& d, int m) {
     }
   }
   return (int)best;
+}
+
+// ---- F(2x2,3x3) fused: input transform into an L2-resident V chunk, then the
+// GEMM with the output transform in its epilogue (no M buffer) -------------------
+
+constexpr size_t kVBudget = 48ull << 20;  // V bytes per chunk (L2-resident)
+
+size_t v_bytes_per_image(const gbconv_desc_s& d) {
+  return (size_t)16 * tiles_h(d, 2) * tiles_w(d, 2) * d.C * 2;
+}
+
+// Images per chunk: among counts whose V fits the budget, the one with the
+// fewest GEMM waves per image (a chunk's units = 128-tile rows x 64-channel
+// columns, over the SMs; ties: the larger chunk), capped at the batch.  The
+// count is min(constant, N), so a batch's scratch never shrinks as it grows.
+int images_per_chunk_fused(const gbconv_desc_s& d) {
+  const size_t per = v_bytes_per_image(d);
+  long long nbmax = per ? (long long)(kVBudget / per) : 1;
+  if (nbmax < 1) nbmax = 1;
+  nbmax = std::min<long long>(nbmax, 4096);
+  const long long tiles_img = (long long)tiles_h(d, 2) * tiles_w(d, 2);
+  const long long n_tiles = gb_ceil_div(d.K, wf::BN), sms = gb_num_sms();
+  long long best = 1;
+  double best_cost = 1e300;
+  for (long long nb = 1; nb <= nbmax; ++nb) {
+    const long long units = gb_ceil_div_ll(nb * tiles_img, wf::BM) * n_tiles;
+    const double cost = (double)gb_ceil_div_ll(units, sms) / (double)nb;
+    if (cost <= best_cost * (1 + 1e-12)) {
+      best_cost = cost;
+      best = nb;
+    }
+  }
+  return (int)std::min<long long>(best, d.N);
+}
+
+cudaError_t run_winograd2_fused(const gbconv_desc_s& d, const void* x, const void* wpack,
+                                const float* bias, const void* res, void* y, void* ws, int* err,
+                                unsigned long long wait_ns, cudaStream_t st) {
+  using TT = F2T;
+  WinoParams p{d.N, d.C, d.H, d.W, d.K, d.OH, d.OW, d.pad, tiles_h(d, 2), tiles_w(d, 2), d.act,
+               0, 0};
+  const int nb_max = images_per_chunk_fused(d);
+  CUtensorMap tmx;  // input strips, as for the unfused transform
+  {
+    cuuint64_t dims[4] = {(cuuint64_t)d.C, (cuuint64_t)d.W, (cuuint64_t)d.H, (cuuint64_t)d.N};
+    cuuint64_t strides[3] = {(cuuint64_t)d.C * 2, (cuuint64_t)d.W * d.C * 2,
+                             (cuuint64_t)d.H * d.W * d.C * 2};
+    cuuint32_t box[4] = {WCB, (cuuint32_t)InCfg<TT>::IW, (cuuint32_t)TT::a, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (gb_encode_tiled(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims,
+                        strides, box, estr, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  CUtensorMap tmu;  // U [16][K][C]: 64-channel x 64-row boxes
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)d.C, (cuuint64_t)d.K, 16};
+    cuuint64_t strides[2] = {(cuuint64_t)d.C * 2, (cuuint64_t)d.K * d.C * 2};
+    cuuint32_t box[3] = {wf::BK, wf::BN, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (gb_encode_tiled(&tmu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(wpack), dims,
+                        strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  cudaError_t e = gb_set_smem_once(reinterpret_cast<const void*>(input_transform_kernel<TT, false>),
+                                   InCfg<TT>::SMEM);
+  if (e != cudaSuccess) return e;
+  e = gb_set_smem_once(reinterpret_cast<const void*>(wino2_fused_kernel), wf::SMEM);
+  if (e != cudaSuccess) return e;
+  for (int n0 = 0; n0 < d.N; n0 += nb_max) {
+    p.n0 = n0;
+    p.nb = std::min(nb_max, d.N - n0);
+    const long long T = (long long)p.nb * p.th * p.tw;
+    const int strips = p.nb * p.th * gb_ceil_div(p.tw, TWC) * gb_ceil_div(d.C, WCB);
+    input_transform_kernel<TT, false><<<strips, 256, InCfg<TT>::SMEM, st>>>(tmx, p, ws, err,
+                                                                            wait_ns);
+    gb_count_launch();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    CUtensorMap tmv;  // V [16][T][C] of this chunk: 64-channel x 128-tile boxes
+    {
+      cuuint64_t dims[3] = {(cuuint64_t)d.C, (cuuint64_t)T, 16};
+      cuuint64_t strides[2] = {(cuuint64_t)d.C * 2, (cuuint64_t)T * d.C * 2};
+      cuuint32_t box[3] = {wf::BK, wf::BM, 1};
+      cuuint32_t estr[3] = {1, 1, 1};
+      if (gb_encode_tiled(&tmv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ws, dims, strides, box, estr,
+                          CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    }
+    Wino2Params q{};
+    q.C = d.C;
+    q.K = d.K;
+    q.OH = d.OH;
+    q.OW = d.OW;
+    q.th = p.th;
+    q.tw = p.tw;
+    q.act = d.act;
+    q.n0 = n0;
+    q.T = (int)T;
+    q.cblocks = gb_ceil_div(d.C, wf::BK);
+    q.m_tiles = (int)gb_ceil_div_ll(T, wf::BM);
+    q.n_tiles = gb_ceil_div(d.K, wf::BN);
+    q.bias = bias;
+    q.res = static_cast<const __nv_bfloat16*>(res);
+    q.y = static_cast<__nv_bfloat16*>(y);
+    q.err = err;
+    q.wait_ns = wait_ns;
+    const int units = q.m_tiles * q.n_tiles;
+    const int grid = std::min(units, gb_num_sms());
+    wino2_fused_kernel<<<grid, wf::THREADS, wf::SMEM, st>>>(tmv, tmu, q);
+    gb_count_launch();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 template <typename TT, bool F16>
@@ -407,6 +803,7 @@ size_t winograd_packed_bytes(const gbconv_desc_s& d, int m) {
 }
 
 size_t winograd_workspace_bytes(const gbconv_desc_s& d, int m) {
+  if (m == 2) return (size_t)images_per_chunk_fused(d) * v_bytes_per_image(d);
   const int A = m + 2;
   const long long Tmax = (long long)images_per_chunk(d, m) * tiles_h(d, m) * tiles_w(d, m);
   const size_t v = ((size_t)A * A * Tmax * d.C * 2 + 255) / 256 * 256;
@@ -429,6 +826,6 @@ cudaError_t launch_winograd_filter_transform(const gbconv_desc_s& d, int m, cons
 cudaError_t launch_winograd(const gbconv_desc_s& d, int m, const void* x, const void* wpack,
                             const float* bias, const void* res, void* y, void* ws, int* err,
                             unsigned long long wait_ns, cudaStream_t st) {
-  if (m == 2) return run_winograd<F2T, false>(d, x, wpack, bias, res, y, ws, err, wait_ns, st);
+  if (m == 2) return run_winograd2_fused(d, x, wpack, bias, res, y, ws, err, wait_ns, st);
   return run_winograd<F6T, true>(d, x, wpack, bias, res, y, ws, err, wait_ns, st);
 }
