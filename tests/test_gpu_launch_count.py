@@ -26,7 +26,8 @@ def _layer_and_inputs(torch, algo, N, C, H, K, R, stride, pad, groups=1):
     (1, (2, 96, 10, 96, 1, 1, 0, 3), 3),     # grouped implicit GEMM: one kernel per group
     (6, (2, 64, 12, 64, 3, 1, 1, 64), 1),    # depthwise: one kernel
     (10, (2, 8, 32, 64, 7, 2, 3, 1), 2),     # stem: space-to-depth + implicit GEMM
-    (4, (2, 64, 16, 64, 3, 1, 1, 1), 3),     # Winograd F(2,3): input, GEMM, output
+    (4, (2, 64, 16, 64, 3, 1, 1, 1), 2),     # Winograd F(2,3): input transform, GEMM + output
+    (5, (2, 64, 16, 64, 3, 1, 1, 1), 3),     # Winograd F(6,3): input, GEMM, output
 ])
 def test_launch_count_per_forward(algo, shape, expect):
     torch = need_gpu()
