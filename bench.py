@@ -469,7 +469,8 @@ class GroupedConv(Workload):
 class Stem7x7(Workload):
     """ResNet-50's stem alone: 7x7 / 2, pad 3, 3 -> 64 channels + ReLU on a batch
     of 64 224x224 images (NHWC bf16, the RGB channels padded to 4 for the 4x4
-    space-to-depth algorithm); FLOPs counted over the 3 real channels."""
+    space-to-depth algorithm, or to 8 with --stem-channels 8, where the 2x2
+    space-to-depth algorithm applies too); FLOPs counted over the 3 real channels."""
     name = "resnet50_stem_conv7x7s2_c3_k64_224x224_n64_bf16_nhwc"
     metric = "conv TFLOP/s (direct-equivalent), ResNet-50 stem 7x7/2 3->64 @224x224, batch 64"
 
@@ -479,7 +480,8 @@ class Stem7x7(Workload):
         from cnn_convolution_gemm_gb300 import synth
         from cnn_convolution_gemm_gb300.layer import ConvLayer
         from cnn_convolution_gemm_gb300.workload import ConvShape
-        N, C, H, K = 64, 4, 224, 64
+        N, C, H, K = 64, getattr(args, "stem_channels", 4), 224, 64
+        self.C = C
         self.shape = ConvShape(N, 3, H, H, K, 7, 7, 2, 3)
         x = synth.normal((N, H, H, C), 1.0, rank)
         x[..., 3:] = 0.0
@@ -499,7 +501,8 @@ class Stem7x7(Workload):
 
     def groups(self):
         # algorithmic bytes: the 4-channel input, the output, weights and bias
-        nbytes = 64 * 224 * 224 * 4 * 2 + 64 * 112 * 112 * 64 * 2 + 64 * 49 * 4 * 2 + 64 * 4
+        C = self.C
+        nbytes = 64 * 224 * 224 * C * 2 + 64 * 112 * 112 * 64 * 2 + 64 * 49 * C * 2 + 64 * 4
         return [(self.algo_name, lambda: self.layer.forward(self.x, self.b, out=self.y,
                                                             stream=self.sh),
                  self.shape.flops(), nbytes, "tensor")]
@@ -1232,6 +1235,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true",
                     help="resnet50, int8_stages, single_layer: launch call by call instead of "
                          "replaying CUDA graphs")
+    ap.add_argument("--stem-channels", type=int, default=4, choices=[4, 8],
+                    help="stem7x7: channels the RGB input is padded to")
     ap.add_argument("--cpu-images", type=int, default=32)
     ap.add_argument("--e2e-chunk", type=int, default=4,
                     help="images per chunk of the host-tensor forward pass (e2e of resnet3x3)")

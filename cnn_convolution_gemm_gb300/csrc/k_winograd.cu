@@ -335,16 +335,6 @@ __global__ void __launch_bounds__(256)
 // Warps: 0 TMA producer, 1 MMA issuer (one thread each), 2..9 epilogue.  An
 // epilogue warp reads TMEM lane quarter (warp % 4) -- 32 tiles -- and one half
 // (32) of the unit's 64 channels: 2 x 2 x 32 fp32 accumulators per thread.
-//
-// Clusters: the CTAs of a cluster of 2 or 4 take the same 128 tiles and
-// consecutive 64-channel blocks, so they read the same V tiles.  Rank 0 loads
-// each V tile once and multicasts it into every CTA's stage (and completes it
-// on each CTA's stage barrier); each CTA loads its own U tile.  Rank 0 may
-// refill a stage only when every CTA's MMAs are done with it: each MMA thread
-// also commits to rank 0's cluster-wide "stage free" barrier.  V is four times
-// the input's size (16 transformed values per 2 x 2 outputs), so its tile
-// loads are most of the kernel's L2 -> SM traffic; the multicast divides them
-// by the cluster size.
 namespace wf {
 constexpr int BM = 128;                       // tiles per unit (TMEM lanes)
 constexpr int BN = 64;                        // output channels per unit
@@ -356,7 +346,7 @@ constexpr int STAGES = 8;
 constexpr int GROUP_COLS = 4 * BN;            // one row xi: four 64-column products
 constexpr int TMEM_COLS = 2 * GROUP_COLS;     // two groups in flight
 constexpr int THREADS = 320;
-constexpr int SMEM = STAGES * STAGE + 512 + 1024;
+constexpr int SMEM = STAGES * STAGE + 256 + 1024;
 }  // namespace wf
 
 struct Wino2Params {
@@ -387,21 +377,13 @@ __global__ void __launch_bounds__(wf::THREADS, 1)
   uint64_t* tfull = bars + 2 * wf::STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* mma_done = tempty + 2;
-  uint64_t* cempty = mma_done + 1;  // [STAGES] rank 0: the stage is free in every CTA
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cempty + wf::STAGES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // cluster: its CTAs share the V tiles of a unit's 128 tiles (see above)
-  const uint32_t crank = gb::cluster_ctarank();
-  const uint32_t csize = gb::cluster_nctarank();
-  const int cid = (int)(blockIdx.x / csize), ncl = (int)(gridDim.x / csize);
-  const int ngroups = p.n_tiles / (int)csize;  // n_tiles % csize == 0 (host)
-  const int units = p.m_tiles * ngroups;       // per cluster: (m tile, block of csize n tiles)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < wf::STAGES; ++s) {
       gb::mbar_init(&full[s], 1);
       gb::mbar_init(&empty[s], 1);
-      gb::mbar_init(&cempty[s], csize);
     }
     for (int b = 0; b < 2; ++b) {
       gb::mbar_init(&tfull[b], 1);
@@ -418,14 +400,9 @@ __global__ void __launch_bounds__(wf::THREADS, 1)
   }
   gb::tc_fence_before();
   __syncthreads();
-  // every CTA's barriers are initialised before any is signalled from another
-  if (csize > 1) gb::cluster_sync();
   gb::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  auto unit_tiles = [&](int v, int& mt, int& nt) {
-    mt = v / ngroups;
-    nt = (v % ngroups) * (int)csize + (int)crank;
-  };
+  const int units = p.m_tiles * p.n_tiles;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -434,10 +411,8 @@ __global__ void __launch_bounds__(wf::THREADS, 1)
       uint32_t phase = 0;
       long long issued = 0;
       bool ok = true;
-      const uint16_t all = (uint16_t)((1u << csize) - 1);
-      for (int v = cid; v < units && ok; v += ncl) {
-        int mt, nt;
-        unit_tiles(v, mt, nt);
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const int mt = u / p.n_tiles, nt = u % p.n_tiles;
         for (int a = 0; a < 16 && ok; ++a)
           for (int cb = 0; cb < p.cblocks; ++cb) {
             if (!gb::mbar_wait_bounded(&empty[stage], phase ^ 1, p.wait_ns, p.err)) {
@@ -445,20 +420,10 @@ __global__ void __launch_bounds__(wf::THREADS, 1)
               break;
             }
             gb::mbar_arrive_expect_tx(&full[stage], wf::STAGE);
+            gb::tma_load_3d(sA + stage * wf::A_BYTES, &tm_v, &full[stage], cb * wf::BK,
+                            mt * wf::BM, a);
             gb::tma_load_3d(sB + stage * wf::B_BYTES, &tm_u, &full[stage], cb * wf::BK,
                             nt * wf::BN, a);
-            if (csize == 1) {
-              gb::tma_load_3d(sA + stage * wf::A_BYTES, &tm_v, &full[stage], cb * wf::BK,
-                              mt * wf::BM, a);
-            } else if (crank == 0) {
-              // the stage is free in every CTA of the cluster: refill its V tile in all
-              if (!gb::mbar_wait_bounded(&cempty[stage], phase ^ 1, p.wait_ns, p.err)) {
-                ok = false;
-                break;
-              }
-              gb::tma_load_3d_multicast(sA + stage * wf::A_BYTES, &tm_v, &full[stage],
-                                        cb * wf::BK, mt * wf::BM, a, all);
-            }
             ++issued;
             if (++stage == wf::STAGES) {
               stage = 0;
@@ -486,7 +451,7 @@ __global__ void __launch_bounds__(wf::THREADS, 1)
       uint32_t phase = 0;
       uint32_t grp = 0;
       bool ok = true;
-      for (int v = cid; v < units && ok; v += ncl) {
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         for (int xi = 0; xi < 4 && ok; ++xi, ++grp) {
           const uint32_t buf = grp & 1, gph = (grp >> 1) & 1;
           if (!gb::mbar_wait_bounded(&tempty[buf], gph ^ 1, p.wait_ns, p.err)) {
@@ -510,7 +475,6 @@ __global__ void __launch_bounds__(wf::THREADS, 1)
                                gb::sw128_kmajor_desc(b0 + k * 32), IDESC,
                                (cb > 0 || k > 0) ? 1u : 0u);
               gb::tc_commit(&empty[stage]);
-              if (csize > 1) gb::tc_commit_multicast(&cempty[stage], 0x1);  // rank 0's
               if (++stage == wf::STAGES) {
                 stage = 0;
                 phase ^= 1;
@@ -529,9 +493,8 @@ __global__ void __launch_bounds__(wf::THREADS, 1)
     const int h = (warp - 2) >> 2;   // which 32 of the unit's 64 channels
     uint32_t grp = 0;
     bool ok = true;
-    for (int v = cid; v < units && ok; v += ncl) {
-      int mt, nt;
-      unit_tiles(v, mt, nt);
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const int mt = u / p.n_tiles, nt = u % p.n_tiles;
       float Y[4][32];  // [i * 2 + j][channel]
 #pragma unroll
       for (int o = 0; o < 4; ++o)
@@ -630,8 +593,6 @@ __global__ void __launch_bounds__(wf::THREADS, 1)
   }
   gb::tc_fence_before();
   __syncthreads();
-  // no CTA exits while a peer's MMA commits may still reach rank 0's barriers
-  if (csize > 1) gb::cluster_sync();
   if (warp == 0) {
     gb::tc_fence_after();
     gb::tmem_dealloc(tmem_base, wf::TMEM_COLS);
@@ -701,58 +662,6 @@ int images_per_chunk_fused(const gbconv_desc_s& d) {
     }
   }
   return (int)std::min<long long>(best, d.N);
-}
-
-// Clusters of the fused kernel that fit on the device at once (a cluster needs
-// cs SMs of one GPU processing cluster); cached per (device, size).
-int wino2_max_clusters(int cs) {
-  static int cached[8][3] = {{-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1},
-                             {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 8) return 0;
-  const int ci = cs == 1 ? 0 : (cs == 2 ? 1 : 2);
-  if (cached[dev][ci] >= 0) return cached[dev][ci];
-  int n = 0;
-  if (cs == 1) {
-    n = gb_num_sms();
-  } else if (gb_set_smem_once(reinterpret_cast<const void*>(wino2_fused_kernel), wf::SMEM) ==
-             cudaSuccess) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(gb_num_sms() / cs * cs));
-    cfg.blockDim = dim3(wf::THREADS);
-    cfg.dynamicSmemBytes = wf::SMEM;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, wino2_fused_kernel, &cfg) != cudaSuccess) n = 0;
-  }
-  cudaGetLastError();  // clear a failed query
-  cached[dev][ci] = n;
-  return n;
-}
-
-// Cluster size for a layer with n_tiles 64-channel blocks: each candidate size
-// (dividing n_tiles) is weighed by the SMs its clusters can occupy against the
-// L2 -> SM bytes of a unit (a V tile of 16 KB shared by the cluster, a U tile of
-// 8 KB per CTA): estimated time ~ (16 / cs + 8) / (SMs in use).
-int wino2_cluster_size(int n_tiles) {
-  int best = 1;
-  double best_t = 1e300;
-  for (int cs : {1, 2, 4}) {
-    if (n_tiles % cs) continue;
-    const int sms = wino2_max_clusters(cs) * cs;
-    if (sms <= 0) continue;
-    const double t = (16.0 / cs + 8.0) / sms;
-    if (t < best_t * (1 - 1e-9)) {
-      best_t = t;
-      best = cs;
-    }
-  }
-  return best;
 }
 
 cudaError_t run_winograd2_fused(const gbconv_desc_s& d, const void* x, const void* wpack,
@@ -826,24 +735,9 @@ cudaError_t run_winograd2_fused(const gbconv_desc_s& d, const void* x, const voi
     q.y = static_cast<__nv_bfloat16*>(y);
     q.err = err;
     q.wait_ns = wait_ns;
-    const int cs = wino2_cluster_size(q.n_tiles);
-    const int cunits = q.m_tiles * (q.n_tiles / cs);
-    const int grid = std::min(cunits, wino2_max_clusters(cs)) * cs;
-    if (grid <= 0) return cudaErrorInvalidConfiguration;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(wf::THREADS);
-    cfg.dynamicSmemBytes = wf::SMEM;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, wino2_fused_kernel, tmv, tmu, q);
-    if (e != cudaSuccess) return e;
+    const int units = q.m_tiles * q.n_tiles;
+    const int grid = std::min(units, gb_num_sms());
+    wino2_fused_kernel<<<grid, wf::THREADS, wf::SMEM, st>>>(tmv, tmu, q);
     gb_count_launch();
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

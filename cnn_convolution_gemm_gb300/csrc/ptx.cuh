@@ -205,27 +205,6 @@ __device__ __forceinline__ void tma_load_im2col_4d_pair(void* smem, const void* 
       : "memory");
 }
 
-// Number of CTAs in this CTA's cluster.
-__device__ __forceinline__ uint32_t cluster_nctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-
-// 3-D tiled load multicast to the cluster's CTAs in cta_mask: the box lands at
-// the same shared-memory offset in each of them and completes on the mbarrier
-// at bar's offset in each (this GPU's own memory only).
-__device__ __forceinline__ void tma_load_3d_multicast(void* smem, const void* map, uint64_t* bar,
-                                                      int c0, int c1, int c2,
-                                                      uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(smem)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
 // ---- tcgen05 ------------------------------------------------------------------
 
 // Allocate ncols TMEM columns (power of two >= 32); the base address is written
@@ -313,16 +292,6 @@ __device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t a_desc
 __device__ __forceinline__ void tc_commit_pair_multicast(uint64_t* bar, uint16_t cta_mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
-// Arrive on the mbarrier at bar's offset in every CTA of cta_mask once all
-// tcgen05 operations this thread issued before have completed (cta_group::1).
-__device__ __forceinline__ void tc_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
       " [%0], %1;" ::"r"(smem_u32(bar)),
       "h"(cta_mask)
       : "memory");
