@@ -979,7 +979,13 @@ int pair_max_clusters(int smem) {
   static int cached[8] = {-1, -1, -1, -1, -1, -1, -1, -1};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 8) return 0;
-  if (cached[dev] >= 0) return cached[dev];
+  if (cached[dev] > 0) return cached[dev];
+  // the query needs the kernel's dynamic shared-memory limit raised first
+  auto* kern = igemm_bf16_tc_kernel<BN, MODE_CONV, false, false, true>;
+  if (gb_set_smem_once(reinterpret_cast<const void*>(kern), smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(gb_num_sms() & ~1));
   cfg.blockDim = dim3(192);
@@ -992,11 +998,9 @@ int pair_max_clusters(int smem) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(
-          &n, igemm_bf16_tc_kernel<BN, MODE_CONV, false, false, true>, &cfg) != cudaSuccess)
-    n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
   cudaGetLastError();  // clear a failed query
-  cached[dev] = n;
+  if (n > 0) cached[dev] = n;  // a failure is not remembered
   return n;
 }
 
