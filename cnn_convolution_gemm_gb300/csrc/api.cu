@@ -485,14 +485,6 @@ static IgemmSplitPlan igemm_split_plan(const gbconv_desc_s& d, int a) {
   return pl;
 }
 
-// Stream-K schedule of the 256-column implicit GEMMs (when the split-K plan
-// does not apply): its workspace bytes, 0 when it does not apply.
-static size_t streamk_bytes(const gbconv_desc_s& d, int a) {
-  if (a == CONV_ALGO_IGEMM_N256 && igemm_split_plan(d, a).ksplit > 1) return 0;
-  if (a != CONV_ALGO_IGEMM_N256 && a != CONV_ALGO_IGEMM_2SM) return 0;
-  return igemm_streamk_bytes(d, a == CONV_ALGO_IGEMM_2SM);
-}
-
 extern "C" conv_status_t conv_workspace_size(conv_desc_t d, conv_algo_t algo, size_t* bytes) {
   if (!d || !bytes) return gb_fail(CONV_ERR_BAD_PARAM, "NULL argument");
   const int a = resolve(*d, algo);
@@ -508,8 +500,6 @@ extern "C" conv_status_t conv_workspace_size(conv_desc_t d, conv_algo_t algo, si
   if (a == CONV_ALGO_INT8_WINO_F2) *bytes = int8_wino_workspace_bytes(*d);
   if (a == CONV_ALGO_IGEMM_N64 || a == CONV_ALGO_IGEMM_N128 || a == CONV_ALGO_IGEMM_N256)
     *bytes = igemm_split_plan(*d, a).bytes;
-  if (a == CONV_ALGO_IGEMM_N256 || a == CONV_ALGO_IGEMM_2SM)
-    *bytes = std::max(*bytes, streamk_bytes(*d, a));
   return ok_status();
 }
 
@@ -628,14 +618,6 @@ static conv_status_t fwd_impl(const gbconv_desc_s& d, const void* x, const void*
                                         s);
         break;
       }
-      const size_t skb = streamk_bytes(d, a);
-      if (skb && ws && ws_bytes >= skb && aligned16(ws)) {  // stream-K schedule
-        IgemmSplit sp;
-        sp.sk_part = static_cast<float*>(ws);
-        e = launch_igemm_bf16(d, igemm_block_n(a), x, wpack, static_cast<const float*>(bias),
-                              res, y, err, wait_ns, s, sp);
-        break;
-      }
       const gbconv_desc_s v = group_view(d);
       const size_t wg = igemm_group_packed_bytes(v);
       for (int g = 0; g < d.groups && e == cudaSuccess; ++g)
@@ -647,15 +629,10 @@ static conv_status_t fwd_impl(const gbconv_desc_s& d, const void* x, const void*
             static_cast<__nv_bfloat16*>(y) + (size_t)g * v.K, err, wait_ns, s);
       break;
     }
-    case CONV_ALGO_IGEMM_2SM: {
-      const size_t skb = streamk_bytes(d, a);
+    case CONV_ALGO_IGEMM_2SM:
       e = launch_igemm_bf16_pair(d, x, wpack, static_cast<const float*>(bias), res, y, err,
-                                 wait_ns, s,
-                                 (skb && ws && ws_bytes >= skb && aligned16(ws))
-                                     ? static_cast<float*>(ws)
-                                     : nullptr);
+                                 wait_ns, s);
       break;
-    }
     case CONV_ALGO_DEPTHWISE:
       e = launch_dwconv3x3(d, x, wpack, static_cast<const float*>(bias), res, y, err, wait_ns, s);
       break;

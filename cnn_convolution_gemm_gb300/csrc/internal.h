@@ -98,9 +98,6 @@ struct IgemmSplit {
   // and the epilogue sums the blocks' exact integer partial sums in int32.
   int i8_nch = 0;
   int i8_kch = 0;
-  // Stream-K (sk_part set; see igemm_streamk_bytes): partial sums and flags in
-  // the caller's workspace, laid out as igemm_streamk_bytes describes.
-  float* sk_part = nullptr;
   // space-to-depth-by-4 stem: the GEMM runs over the 4x4-block grid and its
   // 4K columns are (py, px, k) of the 2x2 output pixels of each block; the
   // epilogue writes them to the stride-2 conv's NHWC output [N][2BH][2BW][K]
@@ -108,22 +105,12 @@ struct IgemmSplit {
   int s2d4_k = 0;
 };
 int igemm_kiters(const gbconv_desc_s& d);
-// Stream-K schedule of the 256-column implicit GEMM (pair: the SM-pair tile):
-// the tiles' k-steps are split evenly over the persistent CTAs (clusters) so
-// no last partial wave leaves SMs idle.  Applies to groups-1 bf16 layers
-// without a residual whose tile count exceeds the CTA (cluster) count and is
-// not a multiple of it.  Returns the workspace bytes it needs -- per CTA one
-// 128 x 256 fp32 partial-sum slot, then four int flags per CTA -- or 0 when it
-// does not apply.
-size_t igemm_streamk_bytes(const gbconv_desc_s& d, bool pair);
 // The 256 x 256-tile implicit GEMM over clusters of two CTAs (tcgen05
 // cta_group::2): bf16 NHWC, groups 1, C != 8; same packed weights as the
 // single-SM tiles.
-// sk_part: stream-K workspace (igemm_streamk_bytes(d, true) bytes) or NULL.
 cudaError_t launch_igemm_bf16_pair(const gbconv_desc_s& d, const void* x, const void* wpack,
                                    const float* bias, const void* res, void* y, int* err,
-                                   unsigned long long wait_ns, cudaStream_t st,
-                                   float* sk_part = nullptr);
+                                   unsigned long long wait_ns, cudaStream_t st);
 // Sums part[ksplit][N*OH*OW][K] (fp32, the split-K GEMM's products) and applies
 // d's epilogue (+ bias, + residual, act) into bf16 NHWC y.  K % 8 == 0; part, res
 // and y 16-byte aligned.

@@ -88,19 +88,6 @@ struct IgemmParams {
   int acc_cols;   // TMEM columns per tile accumulator (BN, or i8_nch * BN)
   int nacc;       // tile accumulators in TMEM (2: the epilogue overlaps the next tile)
   uint32_t tmem_cols;  // columns allocated (a power of two >= 32)
-  // stream-K (conv mode, no residual): the tiles' k-steps, laid end to end, are
-  // cut into one equal range per CTA (pair mode: per cluster).  A range starts
-  // and ends inside tiles, so a tile is shared by at most two CTAs: the one
-  // whose range ends in it computes the first k-steps (it reaches that tile
-  // last and writes the output); the one whose range starts in it computes the
-  // rest first, stores its fp32 partial sums in its slot of sk_part
-  // ([slot][128][BN]) and raises its flag (sk_flag[slot][4], one per epilogue
-  // warp); the owner waits for the flag, adds the partial in its epilogue and
-  // lowers the flag again.  Slot = blockIdx.x.
-  int sk;
-  long long sk_total;  // tiles x kiters
-  float* sk_part;
-  int* sk_flag;
   // tf32 mode: fp32 residual [M][K] (the fp32 output goes through tm_y)
   const float* res_f32;
   // space-to-depth-by-4 stem output (see IgemmSplit): column c of the GEMM is
@@ -218,9 +205,6 @@ __global__ void __launch_bounds__(192, 1)
                          const __grid_constant__ CUtensorMap tm_r, const IgemmParams p) {
   using C = Cfg<BN, LIGHT, PAIR>;
   static_assert(!PAIR || (BN == 256 && MODE == MODE_CONV && !LIGHT && !TF32), "pair mode");
-  // stream-K code is compiled only where it can run (keeps the other
-  // instantiations' register count, which LIGHT's two CTAs per SM depend on)
-  constexpr bool SK = BN == 256 && MODE == MODE_CONV && !LIGHT && !TF32;
   constexpr int BKE = TF32 ? 32 : BK;  // channels per k-step (one 128-byte row)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -295,25 +279,8 @@ __global__ void __launch_bounds__(192, 1)
   auto m_tile = [&](int tt) {
     return PAIR ? (tt / p.n_tiles) * 2 + (int)rank : tt / p.n_tiles;
   };
-  // stream-K: this CTA's (cluster's) k-step range and the tiles it touches;
-  // work item u is then the u-th tile of the range
-  long long sk_beg = 0, sk_end = 0;
-  int sk_t0 = 0;
-  if (p.sk) {
-    sk_beg = (long long)unit0 * p.sk_total / ustep;
-    sk_end = (long long)(unit0 + 1) * p.sk_total / ustep;
-    sk_t0 = (int)(sk_beg / p.kiters);
-  }
-  const int ubeg = p.sk ? 0 : unit0;
-  const int uend = p.sk ? (sk_end > sk_beg ? (int)((sk_end - 1) / p.kiters) - sk_t0 + 1 : 0)
-                        : num_units;
-  const int ust = p.sk ? 1 : ustep;
   auto decode = [&](int u, int& t, int& noff, int& width) {
-    if (p.sk) {
-      t = sk_t0 + u;
-      noff = 0;
-      width = BN;
-    } else if (u < p.tail_start) {
+    if (u < p.tail_start) {
       t = u;
       noff = 0;
       width = BN;
@@ -322,21 +289,6 @@ __global__ void __launch_bounds__(192, 1)
       t = p.tail_start + (h >> 1);
       noff = (h & 1) * (BN / 2);
       width = BN / 2;
-    }
-  };
-  // k-steps [kb, ke) of work item u (tile t): a split-K range, the whole
-  // reduction, or this CTA's part of a stream-K tile
-  auto krange = [&](int u, int t, int& kb, int& ke) {
-    if (p.sk) {
-      const long long t0k = (long long)t * p.kiters;
-      kb = u == 0 ? (int)(sk_beg - t0k) : 0;
-      ke = (int)((sk_end < t0k + p.kiters ? sk_end : t0k + p.kiters) - t0k);
-    } else if (MODE == MODE_CONV) {
-      kb = (t / tiles_per_batch) * p.kchunk;
-      ke = min(p.kiters, kb + p.kchunk);
-    } else {
-      kb = 0;
-      ke = p.kiters;
     }
   };
 
@@ -349,7 +301,7 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       // pair mode: the even CTA's stage barriers, where both CTAs' loads complete
       const uint32_t full_pair = PAIR ? gb::mapa_shared(gb::smem_u32(full), 0) : 0u;
-      for (int u = ubeg; u < uend && ok; u += ust) {
+      for (int u = unit0; u < num_units && ok; u += ustep) {
         int t, noff, width;
         decode(u, t, noff, width);
         const int bt = t / tiles_per_batch;
@@ -364,8 +316,8 @@ __global__ void __launch_bounds__(192, 1)
           h0 = oh * p.stride - p.pad;
           w0 = (rem - oh * p.OW) * p.stride - p.pad;
         }
-        int kbeg, kend;
-        krange(u, t, kbeg, kend);
+        const int kbeg = MODE == MODE_CONV ? bt * p.kchunk : 0;
+        const int kend = MODE == MODE_CONV ? min(p.kiters, kbeg + p.kchunk) : p.kiters;
         int cb = kbeg % p.cblocks, s = (kbeg / p.cblocks) % p.S, r = (kbeg / p.cblocks) / p.S;
         for (int it = kbeg; it < kend; ++it) {
           if (!gb::mbar_wait_bounded(&empty[stage], phase ^ 1, p.wait_ns, p.err)) {
@@ -449,15 +401,16 @@ __global__ void __launch_bounds__(192, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int u = ubeg; u < uend && ok; u += ust) {
+      for (int u = unit0; u < num_units && ok; u += ustep) {
         int t, noff, width;
         decode(u, t, noff, width);
         const uint32_t idesc_u = width == BN ? IDESC : gb::idesc_f16(MM, BN / 2, TF32 ? 2 : 1);
         if (!gb::mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, p.wait_ns, p.err)) break;
         gb::tc_fence_after();
         uint32_t d = tmem_base + acc * p.acc_cols;
-        int kbeg, kend;
-        krange(u, t, kbeg, kend);
+        const int bt = t / tiles_per_batch;
+        const int kbeg = MODE == MODE_CONV ? bt * p.kchunk : 0;
+        const int kend = MODE == MODE_CONV ? min(p.kiters, kbeg + p.kchunk) : p.kiters;
         int kin = 0;  // k-steps into the current accumulator block
         for (int it = kbeg; it < kend; ++it) {
           if (kin == p.kch) {  // chunked accumulation: the next BN-column block
@@ -559,22 +512,16 @@ __global__ void __launch_bounds__(192, 1)
       return bv;
     };
     float2 bias_next = make_float2(0.f, 0.f);
-    if (!TF32 && MODE == MODE_CONV && !p.i8_y && !p.part && ubeg < uend)
-      bias_next = bias_pair(ubeg, 0);
+    if (!TF32 && MODE == MODE_CONV && !p.i8_y && !p.part && unit0 < num_units)
+      bias_next = bias_pair(unit0, 0);
     int pending = -1;  // box with a residual load not yet waited for
-    if (has_res && ubeg < uend) {
-      if (lane == 0) fetch_res(ubeg, 0, 0);
+    if (has_res && unit0 < num_units) {
+      if (lane == 0) fetch_res(unit0, 0, 0);
       pending = 0;
-    }
-    // stream-K: this CTA's flag starts lowered (this warp's own slot entry)
-    if (SK && p.sk && lane == 0) {
-      asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p.sk_flag + blockIdx.x * 4 + q),
-                   "r"(0)
-                   : "memory");
     }
     // pair mode: the even CTA's accumulator-free barriers
     const uint32_t tempty_pair = PAIR ? gb::mapa_shared(gb::smem_u32(tempty), 0) : 0u;
-    for (int u = ubeg; u < uend; u += ust) {
+    for (int u = unit0; u < num_units; u += ustep) {
       int t, noff, width;
       decode(u, t, noff, width);
       const int bt = t / tiles_per_batch;
@@ -778,29 +725,6 @@ __global__ void __launch_bounds__(192, 1)
         // swizzled staging box in shared memory -> TMA store of 32 rows x 64 cols
         const long long m_warp = (long long)mt * BM + q * 32;
         const int ns = nsub(u);
-        // stream-K part of this tile: 0 whole tile, 1 later part (partial sums
-        // out, flag up), 2 first part (wait for the partial of CTA sk_src)
-        int sk_kind = 0, sk_src = 0;
-        if (SK && p.sk) {
-          int kb, ke;
-          krange(u, t, kb, ke);
-          sk_kind = kb > 0 ? 1 : (ke < p.kiters ? 2 : 0);
-          sk_src = (int)blockIdx.x + (PAIR ? 2 : 1);
-          if (sk_kind == 2 && lane == 0) {
-            const int* f = p.sk_flag + sk_src * 4 + q;
-            const uint64_t t0 = gb::global_timer_ns();
-            while (true) {
-              int v;
-              asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
-              if (v != 0) break;
-              if (gb::global_timer_ns() - t0 > p.wait_ns) {
-                gb::record_error(p.err, DEV_ERR_TIMEOUT);
-                break;
-              }
-            }
-          }
-          __syncwarp();
-        }
 #pragma unroll 1
         for (int j = 0; j < ns; ++j) {
           const int cur = epi_count & 1;
@@ -811,10 +735,10 @@ __global__ void __launch_bounds__(192, 1)
             // store that last read that box is done with it
             int tn = u, jn = j + 1;
             if (jn >= ns) {
-              tn = u + ust;
+              tn = u + ustep;
               jn = 0;
             }
-            if (tn < uend) {
+            if (tn < num_units) {
               if (lane == 0) {
                 gb::bulk_wait_read<0>();
                 fetch_res(tn, jn, cur ^ 1);
@@ -823,7 +747,7 @@ __global__ void __launch_bounds__(192, 1)
             if (!gb::mbar_wait_bounded(&rbar[q * 2 + cur], (rphase >> cur) & 1, p.wait_ns, p.err))
               break;
             rphase ^= 1u << cur;
-            pending = tn < uend ? (cur ^ 1) : -1;
+            pending = tn < num_units ? (cur ^ 1) : -1;
           } else {
             if (lane == 0) gb::bulk_wait_read<1>();  // the store that last used this box
             __syncwarp();
@@ -841,37 +765,13 @@ __global__ void __launch_bounds__(192, 1)
           {
             int tn = u, jn = j + 1;
             if (jn >= ns) {
-              tn = u + ust;
+              tn = u + ustep;
               jn = 0;
             }
-            if (tn < uend) bias_next = bias_pair(tn, jn);
+            if (tn < num_units) bias_next = bias_pair(tn, jn);
           }
           __syncwarp();
           gb::tmem_ld_wait();
-          if (SK && sk_kind == 1) {
-            // stream-K, later part of the tile: this row's 64 fp32 partial sums
-            // to this CTA's slot; the owner adds them (no bf16 output here)
-            float4* dst = reinterpret_cast<float4*>(
-                p.sk_part + ((size_t)blockIdx.x * BM + q * 32 + lane) * BN + j * 64);
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                   __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
-            continue;
-          }
-          if (SK && sk_kind == 2) {
-            // stream-K, first part: add the other CTA's partial sums of this row
-            const float4* src = reinterpret_cast<const float4*>(
-                p.sk_part + ((size_t)sk_src * BM + q * 32 + lane) * BN + j * 64);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float4 v = __ldcg(src + i);
-              r[4 * i] = __float_as_uint(__uint_as_float(r[4 * i]) + v.x);
-              r[4 * i + 1] = __float_as_uint(__uint_as_float(r[4 * i + 1]) + v.y);
-              r[4 * i + 2] = __float_as_uint(__uint_as_float(r[4 * i + 2]) + v.z);
-              r[4 * i + 3] = __float_as_uint(__uint_as_float(r[4 * i + 3]) + v.w);
-            }
-          }
           if (p.act == 0)
             epi_bf16_subblock<0>(r, sbias, box, lane, has_res);
           else if (p.act == 1)
@@ -900,21 +800,6 @@ __global__ void __launch_bounds__(192, 1)
             gb::bulk_commit();
           }
           ++epi_count;
-        }
-        if (SK && sk_kind == 1) {
-          // the partial sums are visible device-wide before the flag goes up
-          __threadfence();
-          __syncwarp();
-          if (lane == 0)
-            asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.sk_flag + blockIdx.x * 4 + q),
-                         "r"(1)
-                         : "memory");
-        } else if (SK && sk_kind == 2) {
-          __syncwarp();  // every lane has read the partial
-          if (lane == 0)
-            asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p.sk_flag + sk_src * 4 + q),
-                         "r"(0)
-                         : "memory");
         }
         (void)row_ok;
       }
@@ -1073,10 +958,6 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
     p.tmem_cols = cols;
   }
   p.s2d4_k = split.s2d4_k;
-  p.sk = split.sk_part ? 1 : 0;
-  if (p.sk && (BN != 256 || LIGHT || TF32 || narrow || res || p.ksplit != 1 || p.i8_y ||
-               split.s2d4_k || d.x_cstride || d.y_kstride))
-    return cudaErrorInvalidValue;
   if (p.s2d4_k && (TF32 || res || p.i8_y || p.ksplit != 1 || p.s2d4_k != 64 ||
                    d.K != 4 * p.s2d4_k || d.OW % 8))
     return cudaErrorInvalidValue;
@@ -1171,13 +1052,6 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
     const int rem = tiles % grid;
     if (rem > 0 && rem <= grid / 2) p.tail_start = tiles - rem;
   }
-  if (p.sk) {  // stream-K replaces the tail units; its plan guarantees tiles > grid
-    if (tiles <= grid) return cudaErrorInvalidValue;
-    p.tail_start = tiles;
-    p.sk_total = (long long)tiles * p.kiters;
-    p.sk_part = split.sk_part;
-    p.sk_flag = reinterpret_cast<int*>(split.sk_part + (size_t)(PAIR ? 2 * grid : grid) * BM * BN);
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(PAIR ? 2 * grid : grid));
   cfg.blockDim = dim3(192);
@@ -1192,33 +1066,6 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = PAIR ? 2 : 1;
-  if (p.sk) {
-    // the CTAs of a stream-K launch wait on one another's partial sums: a
-    // cooperative launch guarantees they are all resident at once; where the
-    // runtime refuses it, the same GEMM runs with its ordinary schedule
-    cudaLaunchAttribute attr_sk[3] = {attr[0], attr[1], {}};
-    attr_sk[2].id = cudaLaunchAttributeCooperative;
-    attr_sk[2].val.cooperative = 1;
-    cudaLaunchConfig_t cfg_sk = cfg;
-    if (PAIR) {
-      cfg_sk.attrs = attr_sk;
-      cfg_sk.numAttrs = 3;
-    } else {
-      attr_sk[1] = attr_sk[2];
-      cfg_sk.attrs = attr_sk;
-      cfg_sk.numAttrs = 2;
-    }
-    cudaError_t le = cudaLaunchKernelEx(&cfg_sk, kern, tmx, tmw, tmy, tmr, p);
-    if (le == cudaSuccess) {
-      gb_count_launch();
-      return cudaGetLastError();
-    }
-    cudaGetLastError();  // clear the refusal
-    p.sk = 0;
-    p.tail_start = tiles;
-    const int rem = tiles % grid;
-    if (rem > 0 && rem <= grid / 2) p.tail_start = tiles - rem;
-  }
   cudaError_t le = cudaLaunchKernelEx(&cfg, kern, tmx, tmw, tmy, tmr, p);
   if (le != cudaSuccess) return le;
   gb_count_launch();
@@ -1345,12 +1192,11 @@ cudaError_t launch_igemm_bf16(const gbconv_desc_s& d, int block_n, const void* x
 
 cudaError_t launch_igemm_bf16_pair(const gbconv_desc_s& d, const void* x, const void* wpack,
                                    const float* bias, const void* res, void* y, int* err,
-                                   unsigned long long wait_ns, cudaStream_t st, float* sk_part) {
+                                   unsigned long long wait_ns, cudaStream_t st) {
   if (d.dtype != CONV_BF16 || d.C == 8 || d.x_cstride || d.y_kstride)
     return cudaErrorInvalidValue;
-  IgemmSplit sp;
-  sp.sk_part = sk_part;
-  return launch_bn<256, false, false, true>(d, x, wpack, bias, res, y, err, wait_ns, st, sp);
+  return launch_bn<256, false, false, true>(d, x, wpack, bias, res, y, err, wait_ns, st,
+                                            IgemmSplit());
 }
 
 int igemm_kiters(const gbconv_desc_s& d) {
@@ -1422,20 +1268,4 @@ cudaError_t launch_pack_igemm_weights(const gbconv_desc_s& d, const void* w, voi
                                                     d.R * d.S, d.C, Cp, d.R * d.S);
   gb_count_launch();
   return cudaGetLastError();
-}
-
-size_t igemm_streamk_bytes(const gbconv_desc_s& d, bool pair) {
-  if (d.dtype != CONV_BF16 || d.groups != 1 || d.has_residual || d.C == 8 || d.x_cstride ||
-      d.y_kstride)
-    return 0;
-  const long long m_tiles = gb_ceil_div_ll((long long)d.N * d.OH * d.OW, BM);
-  const long long tiles = (pair ? gb_ceil_div_ll(m_tiles, 2) : m_tiles) * gb_ceil_div(d.K, 256);
-  int slots = gb_num_sms();
-  if (pair) {
-    slots = pair_max_clusters<256>(Cfg<256, false, true>::SMEM);
-    if (slots <= 0) return 0;
-  }
-  if (tiles <= slots || tiles % slots == 0) return 0;
-  const size_t ctas = (size_t)(pair ? 2 * slots : slots);
-  return ctas * BM * 256 * 4 + ctas * 4 * sizeof(int);
 }
