@@ -156,18 +156,7 @@ conv_status_t conv_algo_resolve(conv_desc_t desc, conv_algo_t* algo);
  * (ksplit x N*OH*OW x K floats) are summed by a second kernel with the bias,
  * residual and activation ([MegEngine] "Im2col+MatMul", the reduction axis of
  * the product split).  There the workspace is optional: a conv_fwd given less
- * runs the same algorithm unsplit.  For CONV_ALGO_IGEMM_N256 and
- * CONV_ALGO_IGEMM_2SM without a residual, when the layer has more tiles than
- * the device runs at once and they do not divide evenly, the workspace holds
- * the stream-K schedule instead: the tiles' k-steps are split evenly over the
- * persistent CTAs (so no last partial wave leaves SMs idle), a tile shared by
- * two CTAs is completed from the other's fp32 partial sums, and per CTA the
- * workspace holds one 128 x 256 fp32 partial and four int flags.  The flags
- * are zeroed by the call itself and lowered again before it completes, so the
- * workspace needs no initialisation; calls that can overlap on the GPU must
- * not share it.  This workspace is optional too: without it the same
- * algorithm runs its ordinary schedule.  The size depends on the device's SM
- * count. */
+ * runs the same algorithm unsplit.  The size depends on the device's SM count. */
 conv_status_t conv_workspace_size(conv_desc_t desc, conv_algo_t algo, size_t* bytes);
 /* Bytes of the packed weight buffer for (desc, algo). */
 conv_status_t conv_weights_packed_size(conv_desc_t desc, conv_algo_t algo, size_t* bytes);
