@@ -40,7 +40,8 @@ CONV_ALGO_INT8_WINO_F2 = 12
 CONV_ALGO_STEM_S2D4 = 13
 CONV_ALGO_IGEMM_2SM = 14
 CONV_ALGO_INT8_TC_CHUNK = 15
-CONV_ALGO_COUNT = 16
+CONV_ALGO_IGEMM_STRIP = 16
+CONV_ALGO_COUNT = 17
 
 STATUS_NAMES = {
     0: "CONV_OK", 1: "CONV_ERR_BAD_PARAM", 2: "CONV_ERR_UNSUPPORTED", 3: "CONV_ERR_ALIGNMENT",

@@ -242,7 +242,8 @@ static const char* const kAlgoNames[CONV_ALGO_COUNT] = {
     "direct", "igemm_tc_n64", "igemm_tc_n128", "igemm_tc_n256",
     "winograd_f2x2_3x3", "winograd_f6x6_3x3", "depthwise3x3", "int8_igemm_mma",
     "int8_igemm_tc", "im2col_gemm", "stem_s2d_igemm", "igemm_tf32",
-    "int8_winograd_f2x2_3x3", "stem_s2d4_igemm", "igemm_tc_2sm_n256", "int8_igemm_tc_chunked"};
+    "int8_winograd_f2x2_3x3", "stem_s2d4_igemm", "igemm_tc_2sm_n256", "int8_igemm_tc_chunked",
+    "igemm_tc_strip_n64"};
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -280,6 +281,9 @@ static bool applicable(const gbconv_desc_s& d, int algo, const char** why) {
       if (bn == 128 && Kg <= 64) return *why = "K/groups <= 64: use a narrower tile", false;
       return true;
     }
+    case CONV_ALGO_IGEMM_STRIP:
+      if ((long long)d.N * d.OH * d.OW >= (1LL << 31)) return *why = "N*OH*OW >= 2^31", false;
+      return igemm_strip_applicable(d, why);
     case CONV_ALGO_WINO_F2:
     case CONV_ALGO_WINO_F6:
       if (d.dtype != CONV_BF16 || !nhwc) return *why = "needs bf16 NHWC", false;
@@ -534,6 +538,7 @@ extern "C" conv_status_t conv_weights_packed_size(conv_desc_t d, conv_algo_t alg
     case CONV_ALGO_IGEMM_N128:
     case CONV_ALGO_IGEMM_N256:
     case CONV_ALGO_IGEMM_2SM:
+    case CONV_ALGO_IGEMM_STRIP:
       *bytes = igemm_group_packed_bytes(group_view(*d)) * d->groups;
       break;
     case CONV_ALGO_INT8_MMA: *bytes = (size_t)d->K * d->R * d->S * Cp64; break;
@@ -564,7 +569,8 @@ extern "C" conv_status_t conv_weights_prepack(conv_desc_t d, conv_algo_t algo, c
     case CONV_ALGO_IGEMM_N64:
     case CONV_ALGO_IGEMM_N128:
     case CONV_ALGO_IGEMM_N256:
-    case CONV_ALGO_IGEMM_2SM: {  // per group: weights [Kg][R][S][Cg] -> the group's slice
+    case CONV_ALGO_IGEMM_2SM:
+    case CONV_ALGO_IGEMM_STRIP: {  // per group: weights [Kg][R][S][Cg] -> the group's slice
       const gbconv_desc_s v = group_view(*d);
       const size_t in_g = (size_t)v.K * v.R * v.S * v.C * 2, out_g = igemm_group_packed_bytes(v);
       for (int g = 0; g < d->groups && e == cudaSuccess; ++g)
@@ -632,6 +638,9 @@ static conv_status_t fwd_impl(const gbconv_desc_s& d, const void* x, const void*
     case CONV_ALGO_IGEMM_2SM:
       e = launch_igemm_bf16_pair(d, x, wpack, static_cast<const float*>(bias), res, y, err,
                                  wait_ns, s);
+      break;
+    case CONV_ALGO_IGEMM_STRIP:
+      e = launch_igemm_strip(d, x, wpack, static_cast<const float*>(bias), y, err, wait_ns, s);
       break;
     case CONV_ALGO_DEPTHWISE:
       e = launch_dwconv3x3(d, x, wpack, static_cast<const float*>(bias), res, y, err, wait_ns, s);
@@ -1432,6 +1441,7 @@ static bool implemented(int algo) {
     case CONV_ALGO_IGEMM_TF32:
     case CONV_ALGO_INT8_WINO_F2:
     case CONV_ALGO_INT8_TC_CHUNK:
+    case CONV_ALGO_IGEMM_STRIP:
       return true;
     default:
       return false;

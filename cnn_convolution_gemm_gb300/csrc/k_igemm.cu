@@ -842,6 +842,222 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
+// ---- row-strip implicit GEMM (one input strip per tile, taps by descriptor offset) ----
+//
+// For stride-1 convolutions over at most 64 channels into at most 64 output
+// channels (ResNet-50's 56x56 stage), the im2col loads of the general kernel
+// fetch every input pixel once per filter tap.  Here an output row is padded
+// to a "virtual" row of Wv pixels (the smallest power of two >= OW + S - 1),
+// a 128-row tile is RT = 128 / Wv whole output rows, and ONE tiled TMA load
+// brings the RT + R - 1 input rows the tile needs (Wv pixels each, starting at
+// column -pad, zeros outside the image) into shared memory with the 128-byte
+// swizzle.  Output pixel (i, x) of the tile under filter tap (r, s) reads strip
+// row (r + i) * Wv + x + s = m + r * Wv + s for tile row m = i * Wv + x: the A
+// operand of tap (r, s) is the strip itself, its start moved by r * Wv + s
+// rows (the tensor core applies the 128-byte swizzle to absolute shared-memory
+// addresses, so any 128-byte row is a valid start).  Virtual pixels x >= OW
+// are computed and dropped by the output map's bounds.  The R*S weight tiles
+// (64 output channels x 64 input channels each) stay resident for the whole
+// launch.  L2 -> SM bytes per tile: one strip instead of R*S im2col boxes.
+namespace strip {
+constexpr int STAGES = 3;
+constexpr int SLOT = 32 * 1024;          // strip bytes (Wv x rows x 128 B) at most
+constexpr int MAXTAPS = 9;
+constexpr int W_BYTES = MAXTAPS * 64 * 128;
+constexpr int EPI_BOX = 32 * 128;
+constexpr int SMEM = W_BYTES + STAGES * SLOT + 4 * 2 * EPI_BOX + 4 * 256 + 256 + 1024;
+}  // namespace strip
+
+struct StripParams {
+  int OH, OW, K, S, taps, Wv, RT, tiles_per_img, m_tiles, strip_bytes, act;
+  const float* bias;
+  int* err;
+  unsigned long long wait_ns;
+};
+
+template <int ACT>
+__global__ void __launch_bounds__(192, 1)
+    igemm_strip_kernel(const __grid_constant__ CUtensorMap tm_x,
+                       const __grid_constant__ CUtensorMap tm_w,
+                       const __grid_constant__ CUtensorMap tm_y, const StripParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sW = smem;
+  uint8_t* sS = smem + strip::W_BYTES;
+  uint8_t* sEpi = sS + strip::STAGES * strip::SLOT;
+  float* sBias = reinterpret_cast<float*>(sEpi + 4 * 2 * strip::EPI_BOX);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sBias + 4 * 64);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + strip::STAGES;
+  uint64_t* tfull = bars + 2 * strip::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* wbar = tempty + 2;
+  uint64_t* mma_done = wbar + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < strip::STAGES; ++s) {
+      gb::mbar_init(&full[s], 1);
+      gb::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      gb::mbar_init(&tfull[b], 1);
+      gb::mbar_init(&tempty[b], 128);
+    }
+    gb::mbar_init(wbar, 1);
+    gb::mbar_init(mma_done, 1);
+    gb::fence_barrier_init();
+    gb::tma_prefetch_desc(&tm_x);
+    gb::tma_prefetch_desc(&tm_w);
+    gb::tma_prefetch_desc(&tm_y);
+  }
+  if (warp == 0) {
+    gb::tmem_alloc(tmem_slot, 128);  // two 64-column accumulators
+    gb::tmem_relinquish();
+  }
+  gb::tc_fence_before();
+  __syncthreads();
+  gb::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // tile t: image t / tiles_per_img, output rows oh0 .. oh0 + RT - 1
+  auto tile_pos = [&](int t, int& n, int& oh0) {
+    n = t / p.tiles_per_img;
+    oh0 = (t - n * p.tiles_per_img) * p.RT;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- producer: the weight tiles once, then one input strip per tile ----
+      gb::mbar_arrive_expect_tx(wbar, p.taps * 64 * 128);
+      for (int tap = 0; tap < p.taps; ++tap)
+        gb::tma_load_2d(sW + tap * 64 * 128, &tm_w, wbar, tap * 64, 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      const int pad = (p.S - 1) / 2;
+      for (int t = blockIdx.x; t < p.m_tiles; t += gridDim.x) {
+        if (!gb::mbar_wait_bounded(&empty[stage], phase ^ 1, p.wait_ns, p.err)) break;
+        int n, oh0;
+        tile_pos(t, n, oh0);
+        gb::mbar_arrive_expect_tx(&full[stage], p.strip_bytes);
+        gb::tma_load_4d(sS + stage * strip::SLOT, &tm_x, &full[stage], 0, -pad, oh0 - pad, n);
+        ++issued;
+        if (++stage == strip::STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      // no copy into shared memory may be in flight when the block exits
+      gb::mbar_wait_bounded(wbar, 0, p.wait_ns, p.err);
+      long long pending = issued < strip::STAGES ? issued : strip::STAGES;
+      int st = stage;
+      uint32_t ph = phase;
+      for (long long i = 0; i < pending; ++i) {
+        if (--st < 0) {
+          st = strip::STAGES - 1;
+          ph ^= 1;
+        }
+        gb::mbar_wait_bounded(&full[st], ph, p.wait_ns, p.err);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer: per tile, every tap's product from the one strip ----
+      constexpr uint32_t IDESC = gb::idesc_f16(128, 64, 1);
+      bool ok = gb::mbar_wait_bounded(wbar, 0, p.wait_ns, p.err);
+      gb::tc_fence_after();
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      const uint32_t w0 = gb::smem_u32(sW);
+      for (int t = blockIdx.x; t < p.m_tiles && ok; t += gridDim.x) {
+        if (!gb::mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, p.wait_ns, p.err)) break;
+        if (!gb::mbar_wait_bounded(&full[stage], phase, p.wait_ns, p.err)) break;
+        gb::tc_fence_after();
+        const uint32_t d = tmem_base + acc * 64;
+        const uint32_t s0 = gb::smem_u32(sS + stage * strip::SLOT);
+        for (int tap = 0; tap < p.taps; ++tap) {
+          const int r = tap / p.S, sx = tap - r * p.S;
+          const uint32_t a0 = s0 + (uint32_t)((r * p.Wv + sx) * 128);
+          const uint32_t b0 = w0 + tap * 64 * 128;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            gb::tc_mma_f16(d, gb::sw128_kmajor_desc(a0 + k * 32),
+                           gb::sw128_kmajor_desc(b0 + k * 32), IDESC,
+                           (tap > 0 || k > 0) ? 1u : 0u);
+        }
+        gb::tc_commit(&empty[stage]);
+        gb::tc_commit(&tfull[acc]);
+        if (++stage == strip::STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      gb::tc_commit(mma_done);
+      gb::mbar_wait_bounded(mma_done, 0, p.wait_ns, p.err);
+    }
+  } else {
+    // ---- epilogue: bias, activation, bf16, 4-D TMA store (virtual pixels clipped) ----
+    const int q = warp & 3;
+    float* sbias = sBias + q * 64;
+    {
+      const int c = 2 * lane;  // the 64 biases (channels >= K read as 0)
+      sbias[c] = (p.bias && c < p.K) ? __ldg(p.bias + c) : 0.f;
+      sbias[c + 1] = (p.bias && c + 1 < p.K) ? __ldg(p.bias + c + 1) : 0.f;
+      __syncwarp();
+    }
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    uint32_t epi_count = 0;
+    for (int t = blockIdx.x; t < p.m_tiles; t += gridDim.x) {
+      if (!gb::mbar_wait_bounded(&tfull[acc], acc_phase, p.wait_ns, p.err)) break;
+      gb::tc_fence_after();
+      uint8_t* box = sEpi + (q * 2 + (epi_count & 1)) * strip::EPI_BOX;
+      if (lane == 0) gb::bulk_wait_read<1>();  // the store that last used this box
+      __syncwarp();
+      uint32_t r[64];
+      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + acc * 64;
+#pragma unroll
+      for (int c16 = 0; c16 < 4; ++c16)
+        gb::tmem_ld_x16(tb + c16 * 16, *reinterpret_cast<uint32_t(*)[16]>(&r[c16 * 16]));
+      gb::tmem_ld_wait();
+      gb::tc_fence_before();
+      gb::mbar_arrive(&tempty[acc]);
+      epi_bf16_subblock<ACT>(r, sbias, box, lane, false);
+      gb::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        int n, oh0;
+        tile_pos(t, n, oh0);
+        const int row = q * 32;  // this warp's first tile row
+        gb::tma_store_4d(&tm_y, box, 0, row % p.Wv, oh0 + row / p.Wv, n);
+        gb::bulk_commit();
+      }
+      ++epi_count;
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+    if (lane == 0) gb::bulk_wait_all();
+  }
+  gb::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    gb::tc_fence_after();
+    gb::tmem_dealloc(tmem_base, 128);
+  }
+}
+
 // wp[k][rs][c] (rs < RS, c < Cp) = w[k][rs][c] for rs < RS_valid and c < C, else 0
 __global__ void pack_igemm_weights_kernel(const __nv_bfloat16* __restrict__ w,
                                           __nv_bfloat16* __restrict__ wp, int K, int RS, int C,
@@ -1266,6 +1482,114 @@ cudaError_t launch_pack_igemm_weights(const gbconv_desc_s& d, const void* w, voi
   pack_igemm_weights_kernel<<<grid, block, 0, st>>>(static_cast<const __nv_bfloat16*>(w),
                                                     static_cast<__nv_bfloat16*>(wpack), d.K,
                                                     d.R * d.S, d.C, Cp, d.R * d.S);
+  gb_count_launch();
+  return cudaGetLastError();
+}
+
+// The row-strip geometry of d: virtual row width Wv and rows per tile RT (0 when
+// the strip kernel does not apply).
+static void strip_geometry(const gbconv_desc_s& d, int& Wv, int& RT) {
+  Wv = RT = 0;
+  const int need = d.OW + d.S - 1;
+  int w = 8;
+  while (w < need) w *= 2;
+  if (w > 128) return;
+  const int rows = 128 / w + d.R - 1;
+  if ((long long)w * rows * 128 > strip::SLOT) return;
+  Wv = w;
+  RT = 128 / w;
+}
+
+bool igemm_strip_applicable(const gbconv_desc_s& d, const char** why) {
+  const char* dummy;
+  if (!why) why = &dummy;
+  if (d.dtype != CONV_BF16 || d.layout != CONV_NHWC) return *why = "needs bf16 NHWC", false;
+  if (d.groups != 1 || d.stride != 1 || d.dil != 1)
+    return *why = "needs groups 1, stride 1, dilation 1", false;
+  if (d.C < 16 || d.C > 64 || d.C % 8 || d.K > 64 || d.K % 8)
+    return *why = "needs 16 <= C <= 64 and K <= 64, multiples of 8", false;
+  if (d.R * d.S > strip::MAXTAPS || d.R % 2 == 0 || d.S % 2 == 0 || d.pad != (d.S - 1) / 2 ||
+      d.pad != (d.R - 1) / 2)
+    return *why = "needs an odd R x S <= 9 taps with 'same' padding", false;
+  if (d.has_residual) return *why = "no residual", false;
+  int Wv, RT;
+  strip_geometry(d, Wv, RT);
+  if (!Wv) return *why = "output row too wide for one strip", false;
+  return true;
+}
+
+cudaError_t launch_igemm_strip(const gbconv_desc_s& d, const void* x, const void* wpack,
+                               const float* bias, void* y, int* err, unsigned long long wait_ns,
+                               cudaStream_t st) {
+  int Wv, RT;
+  strip_geometry(d, Wv, RT);
+  if (!Wv || !igemm_strip_applicable(d, nullptr)) return cudaErrorInvalidValue;
+  StripParams p{};
+  p.OH = d.OH;
+  p.OW = d.OW;
+  p.K = d.K;
+  p.S = d.S;
+  p.taps = d.R * d.S;
+  p.Wv = Wv;
+  p.RT = RT;
+  p.tiles_per_img = gb_ceil_div(d.OH, RT);
+  p.m_tiles = d.N * p.tiles_per_img;
+  const int rows = RT + d.R - 1;
+  p.strip_bytes = Wv * rows * 128;
+  p.act = d.act;
+  p.bias = bias;
+  p.err = err;
+  p.wait_ns = wait_ns;
+  CUtensorMap tmx, tmw, tmy;
+  {  // x: (C, W, H, N), box {64 channels, Wv pixels, rows, 1}
+    cuuint64_t dims[4] = {(cuuint64_t)d.C, (cuuint64_t)d.W, (cuuint64_t)d.H, (cuuint64_t)d.N};
+    cuuint64_t strides[3] = {(cuuint64_t)d.C * 2, (cuuint64_t)d.W * d.C * 2,
+                             (cuuint64_t)d.H * d.W * d.C * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)Wv, (cuuint32_t)rows, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (gb_encode_tiled(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims,
+                        strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {  // packed weights [K][taps][64]: one {64, 64} box per tap
+    const int Kw = d.R * d.S * 64;
+    cuuint64_t dims[2] = {(cuuint64_t)Kw, (cuuint64_t)d.K};
+    cuuint64_t strides[1] = {(cuuint64_t)Kw * 2};
+    cuuint32_t box[2] = {64, 64};
+    cuuint32_t estr[2] = {1, 1};
+    if (gb_encode_tiled(&tmw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(wpack), dims,
+                        strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {  // y: (K, OW, OH, N); a warp's 32 tile rows are min(Wv, 32) pixels of
+     // max(1, 32 / Wv) output rows
+    cuuint64_t dims[4] = {(cuuint64_t)d.K, (cuuint64_t)d.OW, (cuuint64_t)d.OH, (cuuint64_t)d.N};
+    cuuint64_t strides[3] = {(cuuint64_t)d.K * 2, (cuuint64_t)d.OW * d.K * 2,
+                             (cuuint64_t)d.OH * d.OW * d.K * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)(Wv < 32 ? Wv : 32), (cuuint32_t)(Wv < 32 ? 32 / Wv : 1),
+                         1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (gb_encode_tiled(&tmy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, y, dims, strides, box, estr,
+                        CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  auto* kern = d.act == 0 ? igemm_strip_kernel<0>
+                          : (d.act == 1 ? igemm_strip_kernel<1> : igemm_strip_kernel<2>);
+  cudaError_t e = gb_set_smem_once(reinterpret_cast<const void*>(kern), strip::SMEM);
+  if (e != cudaSuccess) return e;
+  const int grid = std::min(p.m_tiles, gb_num_sms());
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = strip::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, tmx, tmw, tmy, p);
+  if (e != cudaSuccess) return e;
   gb_count_launch();
   return cudaGetLastError();
 }

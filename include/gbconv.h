@@ -97,7 +97,13 @@ typedef int conv_algo_t;
                                       fresh TMEM accumulator every <= 16 k-steps, the
                                       blocks summed in int32 by the epilogue (1x the
                                       tensor work; workspace)                           */
-#define CONV_ALGO_COUNT 16
+#define CONV_ALGO_IGEMM_STRIP 16   /* implicit GEMM for stride-1 layers over <= 64 channels
+                                      into <= 64 (odd R x S <= 9, 'same' padding, no
+                                      residual): each 128-row tile loads ONE input-row
+                                      strip and takes every filter tap from it by a
+                                      shared-memory offset ([MegEngine] "Im2col+MatMul":
+                                      the unrolled rows are never fetched twice)        */
+#define CONV_ALGO_COUNT 17
 
 /* ---- descriptor --------------------------------------------------------- */
 
