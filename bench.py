@@ -10,6 +10,7 @@ Other workloads (--workload):
   single_layer  1 x 32 x 28 x 28 fp32 NCHW, 32 filters 3x3: boundary
                 conversion to NHWC bf16, conv, conversion back
   resnet3x3_tf32  the headline layer with fp32 NHWC tensors on the tf32 path
+  resnet50_s1_3x3  ResNet-50's stage-1 3x3 alone (64 -> 64, 56x56, batch 64, ReLU)
   gconv_g3      ShuffleNet v1 grouped 1x1 conv (240 -> 240, g = 3, 28x28, batch 64)
   shuffle_dw    ShuffleNet v1 depthwise (240 ch, 28x28, batch 64) reading its
                 input channel-shuffled (g = 3), the shuffle fused into the kernel
@@ -306,6 +307,56 @@ class ResNetLayer(Workload):
         return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": threads(), "kind": "oracle",
                 "sample": f"{n} of 32 images, all 256 output channels ({f / 1e9:.1f} GFLOP)",
                 "seconds": round(dt, 3)}
+
+
+class ResNetStage1Layer(ResNetLayer):
+    """ResNet-50's stage-1 3x3 conv alone: 64 -> 64 channels at 56x56, batch 64,
+    bf16 NHWC, bias + ReLU (the network's 64-channel layer shape)."""
+    name = "resnet50_stage1_conv3x3_c64_k64_56x56_n64_bf16_nhwc"
+    metric = "conv TFLOP/s (direct-equivalent), ResNet-50 stage-1 3x3 64->64 @56x56, batch 64"
+
+    def setup(self, dev, rank, args):
+        import torch
+        from cnn_convolution_gemm_gb300 import binding as B
+        from cnn_convolution_gemm_gb300 import synth
+        from cnn_convolution_gemm_gb300.layer import ConvLayer
+        from cnn_convolution_gemm_gb300.workload import ConvShape
+        N, C = 64, 64
+        self.shape = ConvShape(N, C, 56, 56, C, 3, 3, 1, 1)
+        x, w, b = synth.resnet_3x3_layer(seed=rank, N=N, C=C, K=C)
+        self.xh = torch.from_numpy(x).to(torch.bfloat16).pin_memory()
+        self.x = self.xh.to(dev)
+        self.b = torch.from_numpy(b).to(dev)
+        self.layer = ConvLayer(N, C, 56, 56, C, 3, 3, 1, 1, act=B.CONV_ACT_RELU)
+        self.sh = torch.cuda.current_stream().cuda_stream
+        a, self.fastrun_ms = fastrun_pick(self.layer, self.sh, args, B)
+        self.layer.prepack(torch.from_numpy(w).to(torch.bfloat16).to(dev), a)
+        self.algo_name = B.conv_algo_info(self.layer.desc, a)[1]
+        self.y = torch.empty(self.layer.output_shape, dtype=torch.bfloat16, device=dev)
+        self.yh = torch.empty(self.layer.output_shape, dtype=torch.bfloat16).pin_memory()
+
+    def e2e_path(self, args):
+        return "copy in, the layer, copy out on one stream"
+
+    def host_step(self, args):
+        self.x.copy_(self.xh, non_blocking=True)
+        self.layer.forward(self.x, self.b, out=self.y, stream=self.sh)
+        self.yh.copy_(self.y, non_blocking=True)
+
+    def cpu_baseline(self, args):
+        import numpy as np
+        from cnn_convolution_gemm_gb300 import synth
+        from oracle import lib as ol
+        n = 2
+        x, w, b = synth.resnet_3x3_layer(seed=0, N=n, C=64, K=64)
+        t0 = time.perf_counter()
+        ol.conv2d_f64(np.ascontiguousarray(x.transpose(0, 3, 1, 2), dtype=np.float64),
+                      np.ascontiguousarray(w.transpose(0, 3, 1, 2), dtype=np.float64),
+                      b.astype(np.float64), pad=1, act=1)
+        dt = time.perf_counter() - t0
+        f = 2 * n * 56 * 56 * 64 * 64 * 9
+        return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": threads(), "kind": "oracle",
+                "sample": f"{n} of 64 images", "seconds": round(dt, 3)}
 
 
 class ResNetLayerTF32(ResNetLayer):
@@ -946,6 +997,7 @@ class ResNet50W(Workload):
 
 
 WORKLOADS = {"resnet3x3": ResNetLayer, "resnet3x3_tf32": ResNetLayerTF32,
+             "resnet50_s1_3x3": ResNetStage1Layer,
              "shuffle_dw": ShuffleDepthwise, "gconv_g3": GroupedConv,
              "single_layer": SingleLayer, "mbv2_block": MBv2Block,
              "int8_stages": Int8Stages, "resnet50": ResNet50W, "stem7x7": Stem7x7}
