@@ -39,6 +39,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -74,8 +75,9 @@ struct IgemmParams {
   int ksplit, kchunk;
   float* part;
   // tail rebalancing: work units from tail_start on cover the last partial
-  // wave's tiles as two half-width (BN/2) units each
+  // wave's tiles as 2^tail_shift narrower (BN >> tail_shift column) units each
   int tail_start;
+  int tail_shift;  // 1 or 2 (a shift, not a divisor: decode runs in every role's loop)
   // exact int8 output (see IgemmSplit): y8[M][i8_kout]
   int8_t* i8_y;
   const int32_t* i8_bias;
@@ -273,7 +275,8 @@ __global__ void __launch_bounds__(192, 1)
   const int ohow = p.OH * p.OW;
   // work unit u -> tile t, first output column offset within the tile, width
   const int num_units =
-      p.tail_start < num_tiles ? p.tail_start + 2 * (num_tiles - p.tail_start) : num_tiles;
+      p.tail_start < num_tiles ? p.tail_start + ((num_tiles - p.tail_start) << p.tail_shift)
+                               : num_tiles;
   // the 128-row M tile this CTA covers in tile tt of a batch (pair mode: the
   // unit's 256 rows are two M tiles, the even CTA's first)
   auto m_tile = [&](int tt) {
@@ -286,9 +289,9 @@ __global__ void __launch_bounds__(192, 1)
       width = BN;
     } else {
       const int h = u - p.tail_start;
-      t = p.tail_start + (h >> 1);
-      noff = (h & 1) * (BN / 2);
-      width = BN / 2;
+      t = p.tail_start + (h >> p.tail_shift);
+      width = BN >> p.tail_shift;
+      noff = (h & ((1 << p.tail_shift) - 1)) * width;
     }
   };
 
@@ -319,24 +322,29 @@ __global__ void __launch_bounds__(192, 1)
         const int kbeg = MODE == MODE_CONV ? bt * p.kchunk : 0;
         const int kend = MODE == MODE_CONV ? min(p.kiters, kbeg + p.kchunk) : p.kiters;
         int cb = kbeg % p.cblocks, s = (kbeg / p.cblocks) % p.S, r = (kbeg / p.cblocks) / p.S;
+        // pair mode: both CTAs' A tiles and B halves land on the even CTA's
+        // barrier, which alone expects their bytes; a B half is one box of BN / 2
+        // rows, of which a narrower tail unit uses the first width / 2
+        const int n0 = nt * BN + noff + (PAIR ? (int)rank * (width / 2) : 0);
         for (int it = kbeg; it < kend; ++it) {
+          // Everything the copies need is computed before the wait, so they go
+          // out as soon as the stage is free: with the operands in L2 the ring's
+          // depth only just covers the load latency, and a delay here is a
+          // delay of the MMAs.  The B column of k-step it is it * BKE (taps,
+          // then channel blocks, in packed-weight order).
+          const int xc = cb * BKE, kcol = it * BKE;
+          const uint16_t offw = (uint16_t)(s * p.dil), offh = (uint16_t)(r * p.dil);
+          uint8_t* const a_dst = sA + stage * C::A_BYTES;
+          uint8_t* const b_dst = sB + stage * C::B_BYTES;
           if (!gb::mbar_wait_bounded(&empty[stage], phase ^ 1, p.wait_ns, p.err)) {
             ok = false;
             break;
           }
           if constexpr (PAIR) {
-            // both CTAs' A tiles and B halves (width / 2 rows each) land on the even
-            // CTA's barrier, which alone expects their bytes
-            if (rank == 0)
-              gb::mbar_arrive_expect_tx(&full[stage], 2 * C::A_BYTES + width * BK * 2);
+            if (rank == 0) gb::mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
             const uint32_t fb = full_pair + stage * 8;
-            gb::tma_load_im2col_4d_pair(sA + stage * C::A_BYTES, &tm_x, fb, cb * BKE, w0, h0, img,
-                                        (uint16_t)(s * p.dil), (uint16_t)(r * p.dil));
-            const int kcol = (r * p.S + s) * p.cblocks * BKE + cb * BKE;
-            const int n0 = nt * BN + noff + (int)rank * (width / 2);
-            for (int b = 0; b < width / 128; ++b)  // 64-row boxes
-              gb::tma_load_2d_pair(sB + stage * C::B_BYTES + b * 64 * 128, &tm_w, fb, kcol,
-                                   n0 + b * 64);
+            gb::tma_load_im2col_4d_pair(a_dst, &tm_x, fb, xc, w0, h0, img, offw, offh);
+            gb::tma_load_2d_pair(b_dst, &tm_w, fb, kcol, n0);
           } else {
           gb::mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
           if (MODE == MODE_CONV && p.narrow) {
@@ -352,10 +360,8 @@ __global__ void __launch_bounds__(192, 1)
             gb::tma_load_2d(sB + stage * C::B_BYTES, &tm_w, &full[stage], it * BK,
                             nt * BN + noff);
           } else if (MODE == MODE_CONV) {
-            gb::tma_load_im2col_4d(sA + stage * C::A_BYTES, &tm_x, &full[stage], cb * BKE, w0,
-                                   h0, img, (uint16_t)(s * p.dil), (uint16_t)(r * p.dil));
-            gb::tma_load_2d(sB + stage * C::B_BYTES, &tm_w, &full[stage],
-                            (r * p.S + s) * p.cblocks * BKE + cb * BKE, nt * BN + noff);
+            gb::tma_load_im2col_4d(a_dst, &tm_x, &full[stage], xc, w0, h0, img, offw, offh);
+            gb::tma_load_2d(b_dst, &tm_w, &full[stage], kcol, n0);
           } else {
             gb::tma_load_3d(sA + stage * C::A_BYTES, &tm_x, &full[stage], cb * BK, (int)m0, bt);
             gb::tma_load_3d(sB + stage * C::B_BYTES, &tm_w, &full[stage], cb * BK, nt * BN, bt);
@@ -366,13 +372,16 @@ __global__ void __launch_bounds__(192, 1)
             stage = 0;
             phase ^= 1;
           }
-          if (++cb == p.cblocks) {
-            cb = 0;
-            if (++s == p.S) {
-              s = 0;
-              ++r;
-            }
-          }
+          // next (channel block, filter column, filter row), without branches:
+          // nested data-dependent branches here measured 4% slower on the
+          // 256-column SM-pair layer
+          ++cb;
+          const bool wrap_c = cb == p.cblocks;
+          cb = wrap_c ? 0 : cb;
+          s += wrap_c ? 1 : 0;
+          const bool wrap_s = s == p.S;
+          s = wrap_s ? 0 : s;
+          r += wrap_s ? 1 : 0;
         }
       }
       // Drain: wait until the last loads this thread issued have landed, so no
@@ -394,71 +403,82 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ---------------- MMA issuer ----------------
+      // The loop is compiled once per (narrow-channel, chunked-accumulation)
+      // combination and chosen once: a run-time choice made per MMA between two
+      // descriptor forms measured 4% slower on the 256-column SM-pair layer.
       constexpr int MM = PAIR ? 2 * BM : BM;  // pair: M spans both CTAs' A tiles
       const uint32_t IDESC = gb::idesc_f16(MM, BN, TF32 ? 2 : (MODE == MODE_CONV ? 1 : p.ab_type));
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
-      bool ok = true;
-      for (int u = unit0; u < num_units && ok; u += ustep) {
-        int t, noff, width;
-        decode(u, t, noff, width);
-        const uint32_t idesc_u = width == BN ? IDESC : gb::idesc_f16(MM, BN / 2, TF32 ? 2 : 1);
-        if (!gb::mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, p.wait_ns, p.err)) break;
-        gb::tc_fence_after();
-        uint32_t d = tmem_base + acc * p.acc_cols;
-        const int bt = t / tiles_per_batch;
-        const int kbeg = MODE == MODE_CONV ? bt * p.kchunk : 0;
-        const int kend = MODE == MODE_CONV ? min(p.kiters, kbeg + p.kchunk) : p.kiters;
-        int kin = 0;  // k-steps into the current accumulator block
-        for (int it = kbeg; it < kend; ++it) {
-          if (kin == p.kch) {  // chunked accumulation: the next BN-column block
-            kin = 0;
-            d += BN;
-          }
-          if (!gb::mbar_wait_bounded(&full[stage], phase, p.wait_ns, p.err)) {
-            ok = false;
-            break;
-          }
+      auto issue = [&](auto narrow_tag, auto chunked_tag) {
+        constexpr bool NARROW = MODE == MODE_CONV && decltype(narrow_tag)::value;
+        constexpr bool CHUNKED = decltype(chunked_tag)::value;
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int u = unit0; u < num_units; u += ustep) {
+          int t, noff, width;
+          decode(u, t, noff, width);
+          const uint32_t idesc_u = width == BN ? IDESC : gb::idesc_f16(MM, width, TF32 ? 2 : 1);
+          if (!gb::mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, p.wait_ns, p.err)) return;
           gb::tc_fence_after();
-          const uint32_t a0 = gb::smem_u32(sA + stage * C::A_BYTES);
-          const uint32_t b0 = gb::smem_u32(sB + stage * C::B_BYTES);
+          uint32_t d = tmem_base + acc * p.acc_cols;
+          const int bt = t / tiles_per_batch;
+          const int kbeg = MODE == MODE_CONV ? bt * p.kchunk : 0;
+          const int kend = MODE == MODE_CONV ? min(p.kiters, kbeg + p.kchunk) : p.kiters;
+          int kin = 0;  // k-steps into the current accumulator block
+          for (int it = kbeg; it < kend; ++it) {
+            if (CHUNKED && kin == p.kch) {  // chunked accumulation: the next BN-column block
+              kin = 0;
+              d += BN;
+            }
+            const uint32_t a0 = gb::smem_u32(sA + stage * C::A_BYTES);
+            const uint32_t b0 = gb::smem_u32(sB + stage * C::B_BYTES);
+            if (!gb::mbar_wait_bounded(&full[stage], phase, p.wait_ns, p.err)) return;
+            gb::tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {  // 4 MMAs of 32 bytes of K per 128-byte row
-            // narrow mode: two taps (2 x 2 KB boxes) per 16-wide k; core matrices
-            // are 128 bytes apart along M and one box (2 KB) apart along K
-            const uint64_t adesc =
-                (MODE == MODE_CONV && p.narrow)
-                    ? gb::noswz_kmajor_desc(a0 + k * 2 * (BM * 16), BM * 16, 128)
-                    : gb::sw128_kmajor_desc(a0 + k * 32);
-            const uint32_t accum = (kin > 0 || k > 0) ? 1u : 0u;
-            if constexpr (TF32)
-              gb::tc_mma_tf32(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), idesc_u, accum);
-            else if constexpr (PAIR)
-              gb::tc_mma_f16_pair(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), idesc_u, accum);
+            for (int k = 0; k < 4; ++k) {  // 4 MMAs of 32 bytes of K per 128-byte row
+              // narrow mode: two taps (2 x 2 KB boxes) per 16-wide k; core matrices
+              // are 128 bytes apart along M and one box (2 KB) apart along K
+              const uint64_t adesc = NARROW
+                                         ? gb::noswz_kmajor_desc(a0 + k * 2 * (BM * 16), BM * 16, 128)
+                                         : gb::sw128_kmajor_desc(a0 + k * 32);
+              const uint32_t accum = (kin > 0 || k > 0) ? 1u : 0u;
+              if constexpr (TF32)
+                gb::tc_mma_tf32(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), idesc_u, accum);
+              else if constexpr (PAIR)
+                gb::tc_mma_f16_pair(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), idesc_u, accum);
+              else
+                gb::tc_mma_f16(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), idesc_u, accum);
+            }
+            ++kin;
+            if constexpr (PAIR)
+              gb::tc_commit_pair_multicast(&empty[stage], 0x3);  // both CTAs' stage is free
             else
-              gb::tc_mma_f16(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), idesc_u, accum);
+              gb::tc_commit(&empty[stage]);
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
-          ++kin;
           if constexpr (PAIR)
-            gb::tc_commit_pair_multicast(&empty[stage], 0x3);  // both CTAs' stage is free
+            gb::tc_commit_pair_multicast(&tfull[acc], 0x3);
           else
-            gb::tc_commit(&empty[stage]);
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1;
+            gb::tc_commit(&tfull[acc]);
+          if (++acc == p.nacc) {
+            acc = 0;
+            acc_phase ^= 1;
           }
         }
-        if (!ok) break;
-        if constexpr (PAIR)
-          gb::tc_commit_pair_multicast(&tfull[acc], 0x3);
-        else
-          gb::tc_commit(&tfull[acc]);
-        if (++acc == p.nacc) {
-          acc = 0;
-          acc_phase ^= 1;
-        }
+      };
+      using T = std::true_type;
+      using F = std::false_type;
+      const bool chunked = p.kch < p.kiters;
+      if (MODE == MODE_CONV && p.narrow) {
+        if (chunked) issue(T{}, T{});
+        else issue(T{}, F{});
+      } else {
+        if (chunked) issue(F{}, T{});
+        else issue(F{}, F{});
       }
       // All MMAs issued by this thread have completed once mma_done fires.
       if constexpr (PAIR)
@@ -981,15 +1001,18 @@ __global__ void __launch_bounds__(192, 1)
         gb::tc_fence_after();
         const uint32_t d = tmem_base + acc * 64;
         const uint32_t s0 = gb::smem_u32(sS + stage * strip::SLOT);
-        for (int tap = 0; tap < p.taps; ++tap) {
-          const int r = tap / p.S, sx = tap - r * p.S;
-          const uint32_t a0 = s0 + (uint32_t)((r * p.Wv + sx) * 128);
-          const uint32_t b0 = w0 + tap * 64 * 128;
+        // taps in filter order: row r of the strip is r * Wv pixels (128 bytes
+        // each) down, column sx one pixel along; each tap's weights are 64 rows
+        uint32_t b0 = w0;
+        for (int r = 0; r < p.taps / p.S; ++r) {
+          uint32_t a0 = s0 + (uint32_t)(r * p.Wv * 128);
+          for (int sx = 0; sx < p.S; ++sx, a0 += 128, b0 += 64 * 128) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            gb::tc_mma_f16(d, gb::sw128_kmajor_desc(a0 + k * 32),
-                           gb::sw128_kmajor_desc(b0 + k * 32), IDESC,
-                           (tap > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < 4; ++k)
+              gb::tc_mma_f16(d, gb::sw128_kmajor_desc(a0 + k * 32),
+                             gb::sw128_kmajor_desc(b0 + k * 32), IDESC,
+                             (b0 != w0 || k > 0) ? 1u : 0u);
+          }
         }
         gb::tc_commit(&empty[stage]);
         gb::tc_commit(&tfull[acc]);
@@ -1199,7 +1222,7 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   {
     cuuint64_t dims[2] = {(cuuint64_t)p.Kw, (cuuint64_t)d.K};
     cuuint64_t strides[1] = {(cuuint64_t)p.Kw * ES};
-    cuuint32_t box[2] = {BKE, PAIR ? 64u : (cuuint32_t)BN};  // pair: 64-row pieces of a B half
+    cuuint32_t box[2] = {BKE, PAIR ? (cuuint32_t)(BN / 2) : (cuuint32_t)BN};  // pair: a B half
     cuuint32_t estr[2] = {1, 1};
     CUresult r = gb_encode_tiled(&tmw, DT, 2, const_cast<void*>(wpack), dims, strides, box, estr,
                                  CU_TENSOR_MAP_SWIZZLE_128B);
@@ -1260,13 +1283,22 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
     if (slots <= 0) return cudaErrorInvalidConfiguration;
   }
   const int grid = tiles < slots ? tiles : slots;
-  // a last wave that would leave most SMs idle runs as half-width units (at
-  // least 64 columns: the epilogue's sub-block; the exact int8 path needs a whole
-  // 128-column lo/hi group per unit)
+  // a last wave that would leave most SMs idle runs as units of a half or a
+  // quarter of the tile's width, the narrowest whose count still fits one wave
+  // (at least 64 columns: the epilogue's sub-block; the exact int8 lo/hi path
+  // needs a whole 128-column group per unit)
   p.tail_start = tiles;
-  if ((BN == 256 || (BN == 128 && !(p.i8_y && p.i8_nch == 0))) && p.ksplit == 1 && tiles > grid) {
+  p.tail_shift = 1;
+  if (p.ksplit == 1 && tiles > grid) {
     const int rem = tiles % grid;
-    if (rem > 0 && rem <= grid / 2) p.tail_start = tiles - rem;
+    const int min_width = (p.i8_y && p.i8_nch == 0) ? 128 : 64;
+    for (int sh = (BN / min_width >= 4) ? 2 : 1; sh >= 1 && (BN / min_width) >= 2 && rem > 0; --sh) {
+      if ((rem << sh) <= grid) {
+        p.tail_start = tiles - rem;
+        p.tail_shift = sh;
+        break;
+      }
+    }
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(PAIR ? 2 * grid : grid));

@@ -96,6 +96,19 @@ def test_igemm_tail_wave_half_width_units(residual, algo):
     assert ol.normalized_max_error(y, ref) <= TOL
 
 
+@pytest.mark.parametrize("residual", [False, True])
+@pytest.mark.parametrize("algo", [2, 3, 14])
+def test_igemm_tail_wave_quarter_width_units(residual, algo):
+    """80 images of 16x16 (two 128-row tiles each): 160 full-width tiles on
+    152 SMs (the SM-pair algorithm: 80 units on 76 clusters) leave a last wave
+    of 8 (4) tiles, which runs as the narrowest units that fit one wave: 64
+    columns (a quarter of a 256-column tile, half of a 128-column one)."""
+    torch = need_gpu()
+    y, ref = run_bf16_layer(torch, algo, 80, 64, 16, 16, 256, 3, 3, 1, 1, act=1,
+                            residual=residual, seed=21)
+    assert ol.normalized_max_error(y, ref) <= TOL
+
+
 @pytest.mark.parametrize("case", [
     # N, C, H, R, pad, residual: 128-column tiles whose last partial wave runs as
     # 64-column units

@@ -9,7 +9,7 @@ rounding of x and w to bf16; the tf32 implicit GEMM reads the fp32 tensors in
 NHWC; the direct kernel runs on the NCHW fp32 tensors as given.
 
 Tolerances (normalized max error, max|y - y_ref| / max|y_ref|): 1e-2 for the
-bf16 implicit GEMM, the im2col comparator, the direct bf16 loop and Winograd
+bf16 implicit GEMMs (64-column tiles and the row-strip form), the im2col comparator, the direct bf16 loop and Winograd
 F(2x2,3x3); 3e-2 for Winograd F(6x6,3x3) (fp16 operands in the transformed
 domain); 5e-3 for tf32; 1e-5 for the fp32 direct loop."""
 import pytest
@@ -23,6 +23,7 @@ N, C, H, W, K = 1, 32, 28, 28, 32
 BF16_ALGOS = {  # algorithm name -> tolerance
     "direct": 1e-2,
     "igemm_tc_n64": 1e-2,
+    "igemm_tc_strip_n64": 1e-2,
     "im2col_gemm": 1e-2,
     "winograd_f2x2_3x3": 1e-2,
     "winograd_f6x6_3x3": 3e-2,
