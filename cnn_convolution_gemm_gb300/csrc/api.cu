@@ -50,6 +50,7 @@ static constexpr int kMaxDevices = 64;
 static std::mutex g_dev_mu;
 static int* g_err_ptr[kMaxDevices];
 static int g_num_sms[kMaxDevices];
+static long long g_l2_bytes[kMaxDevices];
 
 static int current_device() {
   int dev = 0;
@@ -79,6 +80,18 @@ int gb_num_sms() {
     g_num_sms[dev] = n > 0 ? n : 1;
   }
   return g_num_sms[dev];
+}
+
+long long gb_l2_bytes() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_l2_bytes[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev);
+    g_l2_bytes[dev] = n > 0 ? n : 1;
+  }
+  return g_l2_bytes[dev];
 }
 
 cudaError_t gb_set_smem_once(const void* func, int bytes) {

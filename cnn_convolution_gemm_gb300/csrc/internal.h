@@ -38,6 +38,8 @@ conv_status_t gb_check_algo(const gbconv_desc_s& d, int algo);
 int* gb_device_error_word();
 // Number of SMs of the current device (cached).
 int gb_num_sms();
+// L2 size of the current device in bytes (cached).
+long long gb_l2_bytes();
 // Called after each kernel launch: counts the kernels the library enqueues.
 void gb_count_launch();
 // Diagnostic: a kernel whose bounded wait on an mbarrier nothing arrives at runs

@@ -92,6 +92,13 @@ struct IgemmParams {
   uint32_t tmem_cols;  // columns allocated (a power of two >= 32)
   // tf32 mode: fp32 residual [M][K] (the fp32 output goes through tm_y)
   const float* res_f32;
+  // L2 warm-up (conv mode): while a unit's epilogue runs, each epilogue lane
+  // touches the input pixel under the middle filter tap of its output pixel in
+  // the unit this CTA takes after the next one (pf_x null: off)
+  const uint8_t* pf_x;
+  long long pf_pix;  // bytes between pixels of x
+  int pf_row;        // bytes of a pixel's channels
+  int pf_dh, pf_dw;  // middle tap offset, rows and columns (times the dilation)
   // space-to-depth-by-4 stem output (see IgemmSplit): column c of the GEMM is
   // channel c % s2d4_k of output pixel (2 bh + py, 2 bw + px), (py, px) = the
   // bits of c / s2d4_k; stored through the 5-D map in the tm_y slot
@@ -549,6 +556,31 @@ __global__ void __launch_bounds__(192, 1)
       const int mt = m_tile(tt), nt = tt % p.n_tiles;
       if (!gb::mbar_wait_bounded(&tfull[acc], acc_phase, p.wait_ns, p.err)) break;
       gb::tc_fence_after();
+      if (MODE == MODE_CONV && !LIGHT && p.pf_x != nullptr && u + 2 * ustep < num_units) {
+        // The first k-steps of a unit read its pixels from DRAM (later taps hit
+        // L2), and a wave's units all start at once: touching them a unit ahead
+        // spreads those reads over the previous unit.  Plain prefetches from
+        // these warps leave the TMA unit and the producer thread alone.  Not in
+        // the shallow two-CTA kernels: their epilogue is the bound (ResNet-50
+        // measured 4 % slower with it there).
+        int t2, n2, w2;
+        decode(u + 2 * ustep, t2, n2, w2);
+        const int tt2 = t2 % tiles_per_batch;
+        if (n2 == 0 && tt2 % p.n_tiles == 0) {  // other column units share the rows
+          const long long m2 = (long long)m_tile(tt2) * BM + q * 32 + lane;
+          if (m2 < p.M) {
+            const int img2 = (int)(m2 / ohow);
+            const int rem2 = (int)(m2 - (long long)img2 * ohow);
+            const int oh2 = rem2 / p.OW, ow2 = rem2 - oh2 * p.OW;
+            const int ih = oh2 * p.stride - p.pad + p.pf_dh, iw = ow2 * p.stride - p.pad + p.pf_dw;
+            if (ih >= 0 && ih < p.H && iw >= 0 && iw < p.W) {
+              const uint8_t* a = p.pf_x + (((long long)img2 * p.H + ih) * p.W + iw) * p.pf_pix;
+              for (int l = 0; l < p.pf_row; l += 128)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(a + l));
+            }
+          }
+        }
+      }
       const long long m = (long long)mt * BM + q * 32 + lane;
       const bool row_ok = m < p.M;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * p.acc_cols;
@@ -1142,6 +1174,18 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   IgemmParams p{};
   p.narrow = narrow ? 1 : 0;
   p.taps = d.R * d.S;
+  {
+    const long long xcs_pf = d.x_cstride ? d.x_cstride : d.C;
+    // only for an input of a quarter of L2 or more: a smaller one (the
+    // previous layer's output, say) is most likely still in L2 (ResNet-50
+    // measured 1 % slower with the prefetch on its 3-13 MB inputs)
+    const bool big = (long long)d.N * d.H * d.W * xcs_pf * ES >= gb_l2_bytes() / 4;
+    p.pf_x = (narrow || !big) ? nullptr : static_cast<const uint8_t*>(x);  // off for split-K below
+    p.pf_pix = xcs_pf * ES;
+    p.pf_row = d.C * ES;
+    p.pf_dh = (d.R / 2) * d.dil;
+    p.pf_dw = (d.S / 2) * d.dil;
+  }
   p.H = d.H;
   p.W = d.W;
   p.C = d.C;
@@ -1168,6 +1212,7 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   p.wait_ns = wait_ns;
   p.ksplit = split.ksplit > 1 ? split.ksplit : 1;
   p.kchunk = split.ksplit > 1 ? split.kchunk : p.kiters;
+  if (p.ksplit > 1) p.pf_x = nullptr;  // a range of the channels only
   p.part = split.part;
   p.i8_y = split.i8_y;
   p.i8_bias = split.i8_bias;
