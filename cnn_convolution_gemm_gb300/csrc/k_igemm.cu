@@ -78,6 +78,15 @@ struct IgemmParams {
   // wave's tiles as 2^tail_shift narrower (BN >> tail_shift column) units each
   int tail_start;
   int tail_shift;  // 1 or 2 (a shift, not a divisor: decode runs in every role's loop)
+  // k-steps whose MMAs the issuing thread starts after one round of waits, with
+  // one commit for the group (1 or 2; 2 needs a ring of at least 6 stages, an
+  // even number of them, and even k-step counts).  Each barrier wait in that
+  // thread costs about 200 cycles that the tensor pipe sees as idle time
+  // whenever a k-step's MMAs are short: 4 MMAs of N = 64 or 128 took 506
+  // cycles per k-step with a wait each, 380 in pairs (N = 256: 512 either way,
+  // the MMAs' own time).  A 4-stage ring in pairs is only two loads deep: the
+  // 256-column single-CTA layer ran 13 % slower so.
+  int kgroup;
   // exact int8 output (see IgemmSplit): y8[M][i8_kout]
   int8_t* i8_y;
   const int32_t* i8_bias;
@@ -125,6 +134,10 @@ struct Cfg {
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES + 1024;
 };
+
+// rings whose k-steps may be consumed in pairs (see IgemmParams::kgroup)
+template <class C>
+constexpr bool kGroupable = C::STAGES % 2 == 0 && C::STAGES >= 6;
 
 // Two fp32 values in one 64-bit register pair (channels n, n + 1) for the packed
 // fp32 add of the bf16 epilogue.
@@ -206,10 +219,14 @@ __device__ __forceinline__ float act_apply(float v, int act) {
 
 // TF32: fp32 NHWC tensors, kind::tf32 MMAs; a 128-byte swizzle row then holds
 // 32 channels (BKE) instead of 64 and each MMA still advances 32 bytes of K.
+// tm_wt: the weights with a box as wide as a tail unit (its B rows only: a
+// narrow unit that loaded the whole tile's box ran at the load path's speed,
+// as slow as a full-width unit); tm_w again when there is no tail.
 template <int BN, int MODE, bool LIGHT = false, bool TF32 = false, bool PAIR = false>
 __global__ void __launch_bounds__(192, 1)
     igemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                          const __grid_constant__ CUtensorMap tm_w,
+                         const __grid_constant__ CUtensorMap tm_wt,
                          const __grid_constant__ CUtensorMap tm_y,
                          const __grid_constant__ CUtensorMap tm_r, const IgemmParams p) {
   using C = Cfg<BN, LIGHT, PAIR>;
@@ -253,6 +270,8 @@ __global__ void __launch_bounds__(192, 1)
     gb::fence_barrier_init();
     gb::tma_prefetch_desc(&tm_x);
     gb::tma_prefetch_desc(&tm_w);
+    if (MODE == MODE_CONV && p.tail_start < p.m_tiles * p.n_tiles * p.ksplit)
+      gb::tma_prefetch_desc(&tm_wt);
     if (MODE == MODE_CONV) gb::tma_prefetch_desc(&tm_y);
     if (MODE == MODE_CONV && p.res) gb::tma_prefetch_desc(&tm_r);
   }
@@ -311,6 +330,7 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       // pair mode: the even CTA's stage barriers, where both CTAs' loads complete
       const uint32_t full_pair = PAIR ? gb::mapa_shared(gb::smem_u32(full), 0) : 0u;
+      const int gmask = (kGroupable<C> && p.kgroup == 2) ? 1 : 0;
       for (int u = unit0; u < num_units && ok; u += ustep) {
         int t, noff, width;
         decode(u, t, noff, width);
@@ -330,9 +350,12 @@ __global__ void __launch_bounds__(192, 1)
         const int kend = MODE == MODE_CONV ? min(p.kiters, kbeg + p.kchunk) : p.kiters;
         int cb = kbeg % p.cblocks, s = (kbeg / p.cblocks) % p.S, r = (kbeg / p.cblocks) / p.S;
         // pair mode: both CTAs' A tiles and B halves land on the even CTA's
-        // barrier, which alone expects their bytes; a B half is one box of BN / 2
-        // rows, of which a narrower tail unit uses the first width / 2
+        // barrier, which alone expects their bytes; a B half is one box of
+        // width / 2 rows (BN / 2, or a tail unit's through tm_wt)
         const int n0 = nt * BN + noff + (PAIR ? (int)rank * (width / 2) : 0);
+        const CUtensorMap* const bmap = width == BN ? &tm_w : &tm_wt;
+        const uint32_t stage_tx =
+            (uint32_t)(C::A_BYTES + (PAIR ? width / 2 : width) * (BK * 2));  // 128-byte rows
         for (int it = kbeg; it < kend; ++it) {
           // Everything the copies need is computed before the wait, so they go
           // out as soon as the stage is free: with the operands in L2 the ring's
@@ -343,17 +366,19 @@ __global__ void __launch_bounds__(192, 1)
           const uint16_t offw = (uint16_t)(s * p.dil), offh = (uint16_t)(r * p.dil);
           uint8_t* const a_dst = sA + stage * C::A_BYTES;
           uint8_t* const b_dst = sB + stage * C::B_BYTES;
-          if (!gb::mbar_wait_bounded(&empty[stage], phase ^ 1, p.wait_ns, p.err)) {
+          // grouped k-steps: the commit of a group frees all its stages on the
+          // barrier of its last one
+          if (!gb::mbar_wait_bounded(&empty[stage | gmask], phase ^ 1, p.wait_ns, p.err)) {
             ok = false;
             break;
           }
           if constexpr (PAIR) {
-            if (rank == 0) gb::mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+            if (rank == 0) gb::mbar_arrive_expect_tx(&full[stage], 2 * stage_tx);
             const uint32_t fb = full_pair + stage * 8;
             gb::tma_load_im2col_4d_pair(a_dst, &tm_x, fb, xc, w0, h0, img, offw, offh);
-            gb::tma_load_2d_pair(b_dst, &tm_w, fb, kcol, n0);
+            gb::tma_load_2d_pair(b_dst, bmap, fb, kcol, n0);
           } else {
-          gb::mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+          gb::mbar_arrive_expect_tx(&full[stage], MODE == MODE_CONV ? stage_tx : C::STAGE_BYTES);
           if (MODE == MODE_CONV && p.narrow) {
 #pragma unroll 1
             for (int t = 0; t < 8; ++t) {
@@ -364,11 +389,11 @@ __global__ void __launch_bounds__(192, 1)
                                      0, w0, h0, img, (uint16_t)(ts * p.dil),
                                      (uint16_t)(tr * p.dil));
             }
-            gb::tma_load_2d(sB + stage * C::B_BYTES, &tm_w, &full[stage], it * BK,
+            gb::tma_load_2d(sB + stage * C::B_BYTES, bmap, &full[stage], it * BK,
                             nt * BN + noff);
           } else if (MODE == MODE_CONV) {
             gb::tma_load_im2col_4d(a_dst, &tm_x, &full[stage], xc, w0, h0, img, offw, offh);
-            gb::tma_load_2d(b_dst, &tm_w, &full[stage], kcol, n0);
+            gb::tma_load_2d(b_dst, bmap, &full[stage], kcol, n0);
           } else {
             gb::tma_load_3d(sA + stage * C::A_BYTES, &tm_x, &full[stage], cb * BK, (int)m0, bt);
             gb::tma_load_3d(sB + stage * C::B_BYTES, &tm_w, &full[stage], cb * BK, nt * BN, bt);
@@ -410,14 +435,16 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ---------------- MMA issuer ----------------
-      // The loop is compiled once per (narrow-channel, chunked-accumulation)
-      // combination and chosen once: a run-time choice made per MMA between two
-      // descriptor forms measured 4% slower on the 256-column SM-pair layer.
+      // The loop is compiled once per (narrow-channel, chunked-accumulation,
+      // k-step group) combination and chosen once: a run-time choice made per
+      // MMA between two descriptor forms measured 4% slower on the 256-column
+      // SM-pair layer.
       constexpr int MM = PAIR ? 2 * BM : BM;  // pair: M spans both CTAs' A tiles
       const uint32_t IDESC = gb::idesc_f16(MM, BN, TF32 ? 2 : (MODE == MODE_CONV ? 1 : p.ab_type));
-      auto issue = [&](auto narrow_tag, auto chunked_tag) {
+      auto issue = [&](auto narrow_tag, auto chunked_tag, auto group_tag) {
         constexpr bool NARROW = MODE == MODE_CONV && decltype(narrow_tag)::value;
         constexpr bool CHUNKED = decltype(chunked_tag)::value;
+        constexpr int G = decltype(group_tag)::value;  // stages per round of waits
         int stage = 0;
         uint32_t phase = 0;
         int acc = 0;
@@ -433,36 +460,50 @@ __global__ void __launch_bounds__(192, 1)
           const int kbeg = MODE == MODE_CONV ? bt * p.kchunk : 0;
           const int kend = MODE == MODE_CONV ? min(p.kiters, kbeg + p.kchunk) : p.kiters;
           int kin = 0;  // k-steps into the current accumulator block
-          for (int it = kbeg; it < kend; ++it) {
-            if (CHUNKED && kin == p.kch) {  // chunked accumulation: the next BN-column block
-              kin = 0;
-              d += BN;
+          for (int it = kbeg; it < kend; it += G) {
+            // G consecutive stages (a group starts on a stage that is a multiple
+            // of G, so it does not wrap): addresses, then one round of waits
+            uint32_t a0[G], b0[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              a0[g] = gb::smem_u32(sA + (stage + g) * C::A_BYTES);
+              b0[g] = gb::smem_u32(sB + (stage + g) * C::B_BYTES);
             }
-            const uint32_t a0 = gb::smem_u32(sA + stage * C::A_BYTES);
-            const uint32_t b0 = gb::smem_u32(sB + stage * C::B_BYTES);
-            if (!gb::mbar_wait_bounded(&full[stage], phase, p.wait_ns, p.err)) return;
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+              if (!gb::mbar_wait_bounded(&full[stage + g], phase, p.wait_ns, p.err)) return;
             gb::tc_fence_after();
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {  // 4 MMAs of 32 bytes of K per 128-byte row
-              // narrow mode: two taps (2 x 2 KB boxes) per 16-wide k; core matrices
-              // are 128 bytes apart along M and one box (2 KB) apart along K
-              const uint64_t adesc = NARROW
-                                         ? gb::noswz_kmajor_desc(a0 + k * 2 * (BM * 16), BM * 16, 128)
-                                         : gb::sw128_kmajor_desc(a0 + k * 32);
-              const uint32_t accum = (kin > 0 || k > 0) ? 1u : 0u;
-              if constexpr (TF32)
-                gb::tc_mma_tf32(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), idesc_u, accum);
-              else if constexpr (PAIR)
-                gb::tc_mma_f16_pair(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), idesc_u, accum);
-              else
-                gb::tc_mma_f16(d, adesc, gb::sw128_kmajor_desc(b0 + k * 32), idesc_u, accum);
+            for (int g = 0; g < G; ++g) {
+              if (CHUNKED && kin == p.kch) {  // chunked accumulation: the next BN-column block
+                kin = 0;
+                d += BN;
+              }
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {  // 4 MMAs of 32 bytes of K per 128-byte row
+                // narrow mode: two taps (2 x 2 KB boxes) per 16-wide k; core matrices
+                // are 128 bytes apart along M and one box (2 KB) apart along K
+                const uint64_t adesc =
+                    NARROW ? gb::noswz_kmajor_desc(a0[g] + k * 2 * (BM * 16), BM * 16, 128)
+                           : gb::sw128_kmajor_desc(a0[g] + k * 32);
+                const uint32_t accum = (kin > 0 || k > 0) ? 1u : 0u;
+                if constexpr (TF32)
+                  gb::tc_mma_tf32(d, adesc, gb::sw128_kmajor_desc(b0[g] + k * 32), idesc_u, accum);
+                else if constexpr (PAIR)
+                  gb::tc_mma_f16_pair(d, adesc, gb::sw128_kmajor_desc(b0[g] + k * 32), idesc_u, accum);
+                else
+                  gb::tc_mma_f16(d, adesc, gb::sw128_kmajor_desc(b0[g] + k * 32), idesc_u, accum);
+              }
+              ++kin;
             }
-            ++kin;
+            // the group's stages are free once its MMAs complete (the producer
+            // waits on the last stage's barrier for each of them)
             if constexpr (PAIR)
-              gb::tc_commit_pair_multicast(&empty[stage], 0x3);  // both CTAs' stage is free
+              gb::tc_commit_pair_multicast(&empty[stage + G - 1], 0x3);  // both CTAs' stages
             else
-              gb::tc_commit(&empty[stage]);
-            if (++stage == C::STAGES) {
+              gb::tc_commit(&empty[stage + G - 1]);
+            stage += G;
+            if (stage == C::STAGES) {
               stage = 0;
               phase ^= 1;
             }
@@ -479,13 +520,24 @@ __global__ void __launch_bounds__(192, 1)
       };
       using T = std::true_type;
       using F = std::false_type;
+      using G1 = std::integral_constant<int, 1>;
+      using G2 = std::integral_constant<int, 2>;
       const bool chunked = p.kch < p.kiters;
+      auto run_group = [&](auto narrow_tag, auto chunked_tag) {
+        if constexpr (kGroupable<C>) {
+          if (p.kgroup == 2) {
+            issue(narrow_tag, chunked_tag, G2{});
+            return;
+          }
+        }
+        issue(narrow_tag, chunked_tag, G1{});
+      };
       if (MODE == MODE_CONV && p.narrow) {
-        if (chunked) issue(T{}, T{});
-        else issue(T{}, F{});
+        if (chunked) run_group(T{}, T{});
+        else run_group(T{}, F{});
       } else {
-        if (chunked) issue(F{}, T{});
-        else issue(F{}, F{});
+        if (chunked) run_group(F{}, T{});
+        else run_group(F{}, F{});
       }
       // All MMAs issued by this thread have completed once mma_done fires.
       if constexpr (PAIR)
@@ -1226,6 +1278,8 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   // takes more than its share of the SM's 512 TMEM columns (LIGHT: two CTAs).
   p.i8_nch = p.i8_y ? split.i8_nch : 0;
   p.kch = p.i8_nch > 0 ? split.i8_kch : (1 << 30);
+  // k-step pairs: every unit's k-range (kiters, or kchunk-long ranges) even
+  p.kgroup = (kGroupable<Cf> && p.kiters % 2 == 0 && (p.ksplit == 1 || p.kchunk % 2 == 0)) ? 2 : 1;
   if (p.i8_y) {
     if (p.ksplit != 1 || p.i8_kout % 16) return cudaErrorInvalidValue;
     if (p.i8_nch == 0 && (BN % 128 != 0 || p.i8_kout * 2 != d.K)) return cudaErrorInvalidValue;
@@ -1345,6 +1399,17 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
       }
     }
   }
+  CUtensorMap tmwt = tmw;  // B boxes of a tail unit's width
+  if (p.tail_start < tiles) {
+    const int wt = BN >> p.tail_shift;
+    cuuint64_t dims[2] = {(cuuint64_t)p.Kw, (cuuint64_t)d.K};
+    cuuint64_t strides[1] = {(cuuint64_t)p.Kw * ES};
+    cuuint32_t box[2] = {BKE, (cuuint32_t)(PAIR ? wt / 2 : wt)};
+    cuuint32_t estr[2] = {1, 1};
+    if (gb_encode_tiled(&tmwt, DT, 2, const_cast<void*>(wpack), dims, strides, box, estr,
+                        CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(PAIR ? 2 * grid : grid));
   cfg.blockDim = dim3(192);
@@ -1359,7 +1424,7 @@ cudaError_t launch_bn(const gbconv_desc_s& d, const void* x, const void* wpack, 
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = PAIR ? 2 : 1;
-  cudaError_t le = cudaLaunchKernelEx(&cfg, kern, tmx, tmw, tmy, tmr, p);
+  cudaError_t le = cudaLaunchKernelEx(&cfg, kern, tmx, tmw, tmwt, tmy, tmr, p);
   if (le != cudaSuccess) return le;
   gb_count_launch();
   return cudaGetLastError();
@@ -1386,6 +1451,7 @@ cudaError_t launch_batched_bn(int batch, int M, int N, int Kred, const void* A, 
   p.OH = p.OW = 1;
   p.tail_start = 1 << 30;
   p.kch = 1 << 30;
+  p.kgroup = (kGroupable<Cf> && p.kiters % 2 == 0) ? 2 : 1;
   p.acc_cols = BN;
   p.nacc = 2;
   p.tmem_cols = 2 * BN;
@@ -1425,7 +1491,7 @@ cudaError_t launch_batched_bn(int batch, int M, int N, int Kred, const void* A, 
                         CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  igemm_bf16_tc_kernel<BN, MODE_BATCHED><<<grid, 192, Cf::SMEM, st>>>(tma, tmb, tma, tmo, p);
+  igemm_bf16_tc_kernel<BN, MODE_BATCHED><<<grid, 192, Cf::SMEM, st>>>(tma, tmb, tmb, tma, tmo, p);
   gb_count_launch();
   return cudaGetLastError();
 }
