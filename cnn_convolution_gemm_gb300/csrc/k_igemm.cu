@@ -1074,41 +1074,55 @@ __global__ void __launch_bounds__(192, 1)
       constexpr uint32_t IDESC = gb::idesc_f16(128, 64, 1);
       bool ok = gb::mbar_wait_bounded(wbar, 0, p.wait_ns, p.err);
       gb::tc_fence_after();
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
-      const uint32_t w0 = gb::smem_u32(sW);
-      for (int t = blockIdx.x; t < p.m_tiles && ok; t += gridDim.x) {
-        if (!gb::mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, p.wait_ns, p.err)) break;
-        if (!gb::mbar_wait_bounded(&full[stage], phase, p.wait_ns, p.err)) break;
-        gb::tc_fence_after();
-        const uint32_t d = tmem_base + acc * 64;
-        const uint32_t s0 = gb::smem_u32(sS + stage * strip::SLOT);
-        // taps in filter order: row r of the strip is r * Wv pixels (128 bytes
-        // each) down, column sx one pixel along; each tap's weights are 64 rows
-        uint32_t b0 = w0;
-        for (int r = 0; r < p.taps / p.S; ++r) {
-          uint32_t a0 = s0 + (uint32_t)(r * p.Wv * 128);
-          for (int sx = 0; sx < p.S; ++sx, a0 += 128, b0 += 64 * 128) {
+      // One tile's 36 (or fewer) MMAs are issued from fully unrolled tap loops,
+      // each descriptor its base plus a constant: with N = 64 an MMA takes 48
+      // cycles, and the issuing thread is the bound (run-time tap loops that
+      // built every descriptor measured 91 cycles per MMA, 3,290 per 3x3 tile).
+      const uint64_t bdesc0 = gb::sw128_kmajor_desc(gb::smem_u32(sW));
+      const uint32_t row_units = (uint32_t)p.Wv * 8;  // one strip row of Wv pixels, in 16-byte units
+      auto run = [&](auto r_tag, auto s_tag) {
+        constexpr int R = decltype(r_tag)::value, S = decltype(s_tag)::value;
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < p.m_tiles && ok; t += gridDim.x) {
+          const uint32_t d = tmem_base + acc * 64;
+          const uint64_t adesc0 = gb::sw128_kmajor_desc(gb::smem_u32(sS + stage * strip::SLOT));
+          if (!gb::mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, p.wait_ns, p.err)) break;
+          if (!gb::mbar_wait_bounded(&full[stage], phase, p.wait_ns, p.err)) break;
+          gb::tc_fence_after();
+          // taps in filter order: row r of the strip is r * Wv pixels (128 bytes
+          // each) down, column sx one pixel along; each tap's weights are 64
+          // rows; K advances 32 bytes per MMA (descriptor units of 16 bytes)
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              gb::tc_mma_f16(d, gb::sw128_kmajor_desc(a0 + k * 32),
-                             gb::sw128_kmajor_desc(b0 + k * 32), IDESC,
-                             (b0 != w0 || k > 0) ? 1u : 0u);
+          for (int r = 0; r < R; ++r) {
+            const uint64_t arow = adesc0 + (uint64_t)(r * row_units);
+#pragma unroll
+            for (int sx = 0; sx < S; ++sx)
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                gb::tc_mma_f16(d, arow + (uint64_t)(sx * 8 + k * 2),
+                               bdesc0 + (uint64_t)((r * S + sx) * 64 * 8 + k * 2), IDESC,
+                               (r | sx | k) ? 1u : 0u);
+          }
+          gb::tc_commit(&empty[stage]);
+          gb::tc_commit(&tfull[acc]);
+          if (++stage == strip::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+          if (++acc == 2) {
+            acc = 0;
+            acc_phase ^= 1;
           }
         }
-        gb::tc_commit(&empty[stage]);
-        gb::tc_commit(&tfull[acc]);
-        if (++stage == strip::STAGES) {
-          stage = 0;
-          phase ^= 1;
-        }
-        if (++acc == 2) {
-          acc = 0;
-          acc_phase ^= 1;
-        }
-      }
+      };
+      // a 3x3 or 1x1 filter (checked on the host)
+      using I1 = std::integral_constant<int, 1>;
+      using I3 = std::integral_constant<int, 3>;
+      if (p.taps == 9) run(I3{}, I3{});
+      else run(I1{}, I1{});
       gb::tc_commit(mma_done);
       gb::mbar_wait_bounded(mma_done, 0, p.wait_ns, p.err);
     }
@@ -1651,9 +1665,9 @@ bool igemm_strip_applicable(const gbconv_desc_s& d, const char** why) {
     return *why = "needs groups 1, stride 1, dilation 1", false;
   if (d.C < 16 || d.C > 64 || d.C % 8 || d.K > 64 || d.K % 8)
     return *why = "needs 16 <= C <= 64 and K <= 64, multiples of 8", false;
-  if (d.R * d.S > strip::MAXTAPS || d.R % 2 == 0 || d.S % 2 == 0 || d.pad != (d.S - 1) / 2 ||
-      d.pad != (d.R - 1) / 2)
-    return *why = "needs an odd R x S <= 9 taps with 'same' padding", false;
+  // (the kernel's tap loops are compiled for these two filter sizes)
+  if (!((d.R == 1 && d.S == 1) || (d.R == 3 && d.S == 3)) || d.pad != (d.S - 1) / 2)
+    return *why = "needs a 1x1 or 3x3 filter with 'same' padding", false;
   if (d.has_residual) return *why = "no residual", false;
   int Wv, RT;
   strip_geometry(d, Wv, RT);

@@ -98,7 +98,7 @@ typedef int conv_algo_t;
                                       blocks summed in int32 by the epilogue (1x the
                                       tensor work; workspace)                           */
 #define CONV_ALGO_IGEMM_STRIP 16   /* implicit GEMM for stride-1 layers over <= 64 channels
-                                      into <= 64 (odd R x S <= 9, 'same' padding, no
+                                      into <= 64 (1x1 or 3x3, 'same' padding, no
                                       residual): each 128-row tile loads ONE input-row
                                       strip and takes every filter tap from it by a
                                       shared-memory offset ([MegEngine] "Im2col+MatMul":
