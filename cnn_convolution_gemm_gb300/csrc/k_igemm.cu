@@ -463,11 +463,15 @@ __global__ void __launch_bounds__(192, 1)
           for (int it = kbeg; it < kend; it += G) {
             // G consecutive stages (a group starts on a stage that is a multiple
             // of G, so it does not wrap): addresses, then one round of waits
-            uint32_t a0[G], b0[G];
+            // the stages' descriptors, built once: an MMA's are these plus a
+            // constant (the start address counts 16-byte units), which keeps the
+            // issuing thread's work per MMA small (it bounds MMAs of N <= 128)
+            uint64_t ad[G], bd[G];
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-              a0[g] = gb::smem_u32(sA + (stage + g) * C::A_BYTES);
-              b0[g] = gb::smem_u32(sB + (stage + g) * C::B_BYTES);
+              const uint32_t a0 = gb::smem_u32(sA + (stage + g) * C::A_BYTES);
+              ad[g] = NARROW ? gb::noswz_kmajor_desc(a0, BM * 16, 128) : gb::sw128_kmajor_desc(a0);
+              bd[g] = gb::sw128_kmajor_desc(gb::smem_u32(sB + (stage + g) * C::B_BYTES));
             }
 #pragma unroll
             for (int g = 0; g < G; ++g)
@@ -483,16 +487,15 @@ __global__ void __launch_bounds__(192, 1)
               for (int k = 0; k < 4; ++k) {  // 4 MMAs of 32 bytes of K per 128-byte row
                 // narrow mode: two taps (2 x 2 KB boxes) per 16-wide k; core matrices
                 // are 128 bytes apart along M and one box (2 KB) apart along K
-                const uint64_t adesc =
-                    NARROW ? gb::noswz_kmajor_desc(a0[g] + k * 2 * (BM * 16), BM * 16, 128)
-                           : gb::sw128_kmajor_desc(a0[g] + k * 32);
+                const uint64_t adesc = ad[g] + (uint64_t)(NARROW ? k * 2 * (BM * 16) / 16 : k * 2);
+                const uint64_t bdesc = bd[g] + (uint64_t)(k * 2);
                 const uint32_t accum = (kin > 0 || k > 0) ? 1u : 0u;
                 if constexpr (TF32)
-                  gb::tc_mma_tf32(d, adesc, gb::sw128_kmajor_desc(b0[g] + k * 32), idesc_u, accum);
+                  gb::tc_mma_tf32(d, adesc, bdesc, idesc_u, accum);
                 else if constexpr (PAIR)
-                  gb::tc_mma_f16_pair(d, adesc, gb::sw128_kmajor_desc(b0[g] + k * 32), idesc_u, accum);
+                  gb::tc_mma_f16_pair(d, adesc, bdesc, idesc_u, accum);
                 else
-                  gb::tc_mma_f16(d, adesc, gb::sw128_kmajor_desc(b0[g] + k * 32), idesc_u, accum);
+                  gb::tc_mma_f16(d, adesc, bdesc, idesc_u, accum);
               }
               ++kin;
             }
