@@ -411,11 +411,14 @@ __global__ void __launch_bounds__(wf::THREADS, 1)
       uint32_t phase = 0;
       long long issued = 0;
       bool ok = true;
+      // k-step pairs (an even channel-block count): the MMA thread frees a
+      // pair of stages with one commit on the second one's barrier
+      const int gmask = (p.cblocks % 2 == 0) ? 1 : 0;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const int mt = u / p.n_tiles, nt = u % p.n_tiles;
         for (int a = 0; a < 16 && ok; ++a)
           for (int cb = 0; cb < p.cblocks; ++cb) {
-            if (!gb::mbar_wait_bounded(&empty[stage], phase ^ 1, p.wait_ns, p.err)) {
+            if (!gb::mbar_wait_bounded(&empty[stage | gmask], phase ^ 1, p.wait_ns, p.err)) {
               ok = false;
               break;
             }
@@ -447,6 +450,8 @@ __global__ void __launch_bounds__(wf::THREADS, 1)
     if (lane == 0) {
       // ---- MMA issuer: group xi's four products into one TMEM group ----
       constexpr uint32_t IDESC = gb::idesc_f16(wf::BM, wf::BN, 1);
+      static_assert(wf::STAGES % 2 == 0, "stage pairs");
+      const bool paired = p.cblocks % 2 == 0;  // the producer's rule
       int stage = 0;
       uint32_t phase = 0;
       uint32_t grp = 0;
@@ -461,18 +466,47 @@ __global__ void __launch_bounds__(wf::THREADS, 1)
           gb::tc_fence_after();
           for (int nu = 0; nu < 4 && ok; ++nu) {
             const uint32_t d = tmem_base + buf * wf::GROUP_COLS + nu * wf::BN;
+            if (paired) {
+              // two k-steps per round of waits and one commit: with N = 64 MMAs
+              // the issuing thread, not the tensor pipe, sets the pace
+              for (int cb = 0; cb < p.cblocks; cb += 2) {
+                const uint64_t ad0 = gb::sw128_kmajor_desc(gb::smem_u32(sA + stage * wf::A_BYTES));
+                const uint64_t bd0 = gb::sw128_kmajor_desc(gb::smem_u32(sB + stage * wf::B_BYTES));
+                const uint64_t ad1 = gb::sw128_kmajor_desc(gb::smem_u32(sA + (stage + 1) * wf::A_BYTES));
+                const uint64_t bd1 = gb::sw128_kmajor_desc(gb::smem_u32(sB + (stage + 1) * wf::B_BYTES));
+                if (!gb::mbar_wait_bounded(&full[stage], phase, p.wait_ns, p.err) ||
+                    !gb::mbar_wait_bounded(&full[stage + 1], phase, p.wait_ns, p.err)) {
+                  ok = false;
+                  break;
+                }
+                gb::tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 4; ++k)  // descriptors count 16-byte units
+                  gb::tc_mma_f16(d, ad0 + (uint64_t)(k * 2), bd0 + (uint64_t)(k * 2), IDESC,
+                                 (cb > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  gb::tc_mma_f16(d, ad1 + (uint64_t)(k * 2), bd1 + (uint64_t)(k * 2), IDESC, 1u);
+                gb::tc_commit(&empty[stage + 1]);  // frees both stages
+                stage += 2;
+                if (stage == wf::STAGES) {
+                  stage = 0;
+                  phase ^= 1;
+                }
+              }
+              continue;
+            }
             for (int cb = 0; cb < p.cblocks; ++cb) {
               if (!gb::mbar_wait_bounded(&full[stage], phase, p.wait_ns, p.err)) {
                 ok = false;
                 break;
               }
               gb::tc_fence_after();
-              const uint32_t a0 = gb::smem_u32(sA + stage * wf::A_BYTES);
-              const uint32_t b0 = gb::smem_u32(sB + stage * wf::B_BYTES);
+              const uint64_t ad = gb::sw128_kmajor_desc(gb::smem_u32(sA + stage * wf::A_BYTES));
+              const uint64_t bd = gb::sw128_kmajor_desc(gb::smem_u32(sB + stage * wf::B_BYTES));
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                gb::tc_mma_f16(d, gb::sw128_kmajor_desc(a0 + k * 32),
-                               gb::sw128_kmajor_desc(b0 + k * 32), IDESC,
+                gb::tc_mma_f16(d, ad + (uint64_t)(k * 2), bd + (uint64_t)(k * 2), IDESC,
                                (cb > 0 || k > 0) ? 1u : 0u);
               gb::tc_commit(&empty[stage]);
               if (++stage == wf::STAGES) {
