@@ -107,14 +107,16 @@ struct IgemmSplit {
   int s2d4_k = 0;
 };
 int igemm_kiters(const gbconv_desc_s& d);
-// Row-strip implicit GEMM (stride 1, C and K <= 64, odd R x S <= 9 with 'same'
-// padding, no residual): one tiled input strip per 128-row tile, the taps'
-// A operands by shared-memory offset, weights resident.  wpack: the implicit
-// GEMM's packed layout [K][R*S][64].
+// Row-strip implicit GEMM (stride 1, C and K <= 64, a 1x1 or 3x3 filter with
+// 'same' padding, no residual): one tiled input strip per 128-row tile, the
+// taps' A operands by shared-memory offset, weights resident.  wpack: the
+// implicit GEMM's packed layout [K][R*S][64].  i8 (optional): exact int8
+// output instead of y (its i8_y, i8_bias, i8_scale, i8_relu, i8_nc32; K % 16,
+// and K % 32 for NC32HW32), over the bf16 copy of an int8 input.
 bool igemm_strip_applicable(const gbconv_desc_s& d, const char** why);
 cudaError_t launch_igemm_strip(const gbconv_desc_s& d, const void* x, const void* wpack,
                                const float* bias, void* y, int* err, unsigned long long wait_ns,
-                               cudaStream_t st);
+                               cudaStream_t st, const IgemmSplit* i8 = nullptr);
 // The 256 x 256-tile implicit GEMM over clusters of two CTAs (tcgen05
 // cta_group::2): bf16 NHWC, groups 1, C != 8; same packed weights as the
 // single-SM tiles.

@@ -980,6 +980,14 @@ struct StripParams {
   const float* bias;
   int* err;
   unsigned long long wait_ns;
+  // exact int8 output (i8_y set; bias / act above unused): the sums are exact
+  // integers (at most 9 x 64 products of int8 values, below 2^24 in size);
+  // + i8_bias in int32, requantised with i8_scale (fp32, round to nearest
+  // even), clamped to int8, optional ReLU, stored NHWC or NC32HW32
+  int8_t* i8_y;
+  const int32_t* i8_bias;
+  const float* i8_scale;
+  int i8_relu, i8_nc32;
 };
 
 template <int ACT>
@@ -1139,6 +1147,17 @@ __global__ void __launch_bounds__(192, 1)
       sbias[c + 1] = (p.bias && c + 1 < p.K) ? __ldg(p.bias + c + 1) : 0.f;
       __syncwarp();
     }
+    // int8 output: the 64 int32 biases and fp32 scales, in this warp's (then
+    // unused) staging boxes, read back as broadcasts
+    int32_t* sbi = reinterpret_cast<int32_t*>(sEpi + q * 2 * strip::EPI_BOX);
+    float* ssc = reinterpret_cast<float*>(sbi + 64);
+    if (p.i8_y) {
+      for (int c = lane; c < 64; c += 32) {
+        sbi[c] = (p.i8_bias && c < p.K) ? __ldg(p.i8_bias + c) : 0;
+        ssc[c] = c < p.K ? __ldg(p.i8_scale + c) : 0.f;
+      }
+      __syncwarp();
+    }
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t epi_count = 0;
@@ -1146,8 +1165,10 @@ __global__ void __launch_bounds__(192, 1)
       if (!gb::mbar_wait_bounded(&tfull[acc], acc_phase, p.wait_ns, p.err)) break;
       gb::tc_fence_after();
       uint8_t* box = sEpi + (q * 2 + (epi_count & 1)) * strip::EPI_BOX;
-      if (lane == 0) gb::bulk_wait_read<1>();  // the store that last used this box
-      __syncwarp();
+      if (!p.i8_y) {
+        if (lane == 0) gb::bulk_wait_read<1>();  // the store that last used this box
+        __syncwarp();
+      }
       uint32_t r[64];
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + acc * 64;
 #pragma unroll
@@ -1156,15 +1177,47 @@ __global__ void __launch_bounds__(192, 1)
       gb::tmem_ld_wait();
       gb::tc_fence_before();
       gb::mbar_arrive(&tempty[acc]);
-      epi_bf16_subblock<ACT>(r, sbias, box, lane, false);
-      gb::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
+      if (p.i8_y) {
+        // this lane's output pixel (tile row q * 32 + lane); virtual pixels
+        // (ow >= OW) and rows past the image are dropped
         int n, oh0;
         tile_pos(t, n, oh0);
-        const int row = q * 32;  // this warp's first tile row
-        gb::tma_store_4d(&tm_y, box, 0, row % p.Wv, oh0 + row / p.Wv, n);
-        gb::bulk_commit();
+        const int row = q * 32 + lane, rr = row / p.Wv;
+        const int oh = oh0 + rr, ow = row - rr * p.Wv;
+        if (ow < p.OW && oh < p.OH) {
+          const long long pix = ((long long)n * p.OH + oh) * p.OW + ow;
+#pragma unroll
+          for (int c16 = 0; c16 < 4; ++c16) {
+            if (c16 * 16 >= p.K) break;  // K % 16 == 0
+            uint32_t pk[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int c = c16 * 16 + i;
+              const int tv = __float2int_rn(__uint_as_float(r[c])) + sbi[c];
+              int qv = __float2int_rn(__fmul_rn(__int2float_rn(tv), ssc[c]));
+              qv = qv > 127 ? 127 : (qv < -128 ? -128 : qv);
+              if (p.i8_relu && qv < 0) qv = 0;
+              pk[i >> 2] |= (uint32_t)(qv & 0xff) << (8 * (i & 3));
+            }
+            // NHWC: pixel-major; NC32HW32: 32-channel blocks of the image
+            const long long off =
+                p.i8_nc32 ? (((long long)n * (p.K / 32) + c16 / 2) * p.OH * p.OW +
+                             (long long)oh * p.OW + ow) * 32 + (c16 & 1) * 16
+                          : pix * p.K + c16 * 16;
+            *reinterpret_cast<uint4*>(p.i8_y + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+        }
+      } else {
+        epi_bf16_subblock<ACT>(r, sbias, box, lane, false);
+        gb::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          int n, oh0;
+          tile_pos(t, n, oh0);
+          const int row = q * 32;  // this warp's first tile row
+          gb::tma_store_4d(&tm_y, box, 0, row % p.Wv, oh0 + row / p.Wv, n);
+          gb::bulk_commit();
+        }
       }
       ++epi_count;
       if (++acc == 2) {
@@ -1680,7 +1733,7 @@ bool igemm_strip_applicable(const gbconv_desc_s& d, const char** why) {
 
 cudaError_t launch_igemm_strip(const gbconv_desc_s& d, const void* x, const void* wpack,
                                const float* bias, void* y, int* err, unsigned long long wait_ns,
-                               cudaStream_t st) {
+                               cudaStream_t st, const IgemmSplit* i8) {
   int Wv, RT;
   strip_geometry(d, Wv, RT);
   if (!Wv || !igemm_strip_applicable(d, nullptr)) return cudaErrorInvalidValue;
@@ -1700,6 +1753,16 @@ cudaError_t launch_igemm_strip(const gbconv_desc_s& d, const void* x, const void
   p.bias = bias;
   p.err = err;
   p.wait_ns = wait_ns;
+  if (i8) {  // exact int8 output (see StripParams)
+    if (!i8->i8_y || !i8->i8_scale || d.K % 16 || (i8->i8_nc32 && d.K % 32))
+      return cudaErrorInvalidValue;
+    p.i8_y = i8->i8_y;
+    p.i8_bias = i8->i8_bias;
+    p.i8_scale = i8->i8_scale;
+    p.i8_relu = i8->i8_relu;
+    p.i8_nc32 = i8->i8_nc32;
+    p.act = 0;
+  }
   CUtensorMap tmx, tmw, tmy;
   {  // x: (C, W, H, N), box {64 channels, Wv pixels, rows, 1}
     cuuint64_t dims[4] = {(cuuint64_t)d.C, (cuuint64_t)d.W, (cuuint64_t)d.H, (cuuint64_t)d.N};
@@ -1721,7 +1784,9 @@ cudaError_t launch_igemm_strip(const gbconv_desc_s& d, const void* x, const void
                         strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  {  // y: (K, OW, OH, N); a warp's 32 tile rows are min(Wv, 32) pixels of
+  if (i8) {
+    tmy = tmx;  // int8 output: plain stores, the bf16 output map is not used
+  } else {  // y: (K, OW, OH, N); a warp's 32 tile rows are min(Wv, 32) pixels of
      // max(1, 32 / Wv) output rows
     cuuint64_t dims[4] = {(cuuint64_t)d.K, (cuuint64_t)d.OW, (cuuint64_t)d.OH, (cuuint64_t)d.N};
     cuuint64_t strides[3] = {(cuuint64_t)d.K * 2, (cuuint64_t)d.OW * d.K * 2,
@@ -1733,8 +1798,8 @@ cudaError_t launch_igemm_strip(const gbconv_desc_s& d, const void* x, const void
                         CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  auto* kern = d.act == 0 ? igemm_strip_kernel<0>
-                          : (d.act == 1 ? igemm_strip_kernel<1> : igemm_strip_kernel<2>);
+  auto* kern = p.act == 0 ? igemm_strip_kernel<0>
+                          : (p.act == 1 ? igemm_strip_kernel<1> : igemm_strip_kernel<2>);
   cudaError_t e = gb_set_smem_once(reinterpret_cast<const void*>(kern), strip::SMEM);
   if (e != cudaSuccess) return e;
   const int grid = std::min(p.m_tiles, gb_num_sms());

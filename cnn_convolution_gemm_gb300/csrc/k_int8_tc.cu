@@ -293,6 +293,13 @@ cudaError_t launch_int8_tc(const gbconv_desc_s& d, int algo, const void* x, cons
     const Chunked c = chunked_plan(d);
     sp.i8_nch = c.nch;
     sp.i8_kch = c.kch;
+    // one accumulator block over at most 64 channels into at most 64, stride 1,
+    // a 1x1 or 3x3 filter: the row-strip kernel (one input strip per tile, the
+    // taps by shared-memory offset) over the NHWC bf16 copy, same packed weights
+    gbconv_desc_s ds = db;
+    ds.layout = CONV_NHWC;
+    if (c.nch == 1 && igemm_strip_applicable(ds, nullptr))
+      return launch_igemm_strip(ds, xb, wpack, nullptr, nullptr, err, wait_ns, st, &sp);
     return launch_igemm_bf16(db, c.block_n, xb, wpack, nullptr, nullptr, y, err, wait_ns, st,
                              sp);
   }
