@@ -261,3 +261,43 @@ def test_int8_winograd_exactness_bound_extremes():
     B.conv_sync_status(torch.cuda.current_stream().cuda_stream)
     ref = ol.conv2d_i8(nhwc_to_nchw(x), nhwc_to_nchw(w), None, scale, pad=1, relu=False)
     assert np.array_equal(y.cpu().numpy(), nchw_to_nhwc(ref))
+
+
+@pytest.mark.parametrize("case", [
+    # N, C, H, W, K, R, pad, relu, bias, nc32 — chunked int8 layers of one
+    # accumulator block over <= 64 channels into <= 64 at stride 1 (enough
+    # tiles for the chunked plan): the row-strip kernel with the int8 epilogue
+    (4, 32, 56, 56, 48, 3, 1, True, True, False),    # K < 64, Wv 64 (two rows a tile)
+    (8, 64, 40, 60, 64, 1, 0, False, True, True),    # 1x1, NC32HW32 output, no ReLU
+    (6, 64, 57, 30, 32, 3, 1, True, False, True),    # Wv 32, ragged last tile, no bias
+    (3, 16, 40, 100, 64, 1, 0, True, True, False),   # 16 channels, 1x1, Wv 128 (one row a tile)
+])
+def test_int8_row_strip_path(case):
+    """Bit-exact against the oracle through the int8 row-strip path, and equal to
+    the split-weight GEMM (another exact path) on the same inputs."""
+    torch = need_gpu()
+    from cnn_convolution_gemm_gb300 import binding as B
+    from cnn_convolution_gemm_gb300 import synth
+    from cnn_convolution_gemm_gb300.layer import ConvLayer
+    N, C, H, W, K, R, pad, relu, bias, nc32 = case
+    dev = torch.device("cuda:0")
+    x = synth.int8_uniform((N, C, H, W), 31)  # NCHW
+    w = synth.int8_uniform((K, R, R, C), 32)
+    scale = synth.uniform((K,), 1e-4, 1e-3, 33)
+    b = synth.int32_uniform((K,), 34) if bias else None
+    act = B.CONV_ACT_RELU if relu else B.CONV_ACT_NONE
+    outs = []
+    for algo in (INT8_TC_CHUNK, INT8_TC):
+        layout = B.CONV_NC32HW32 if nc32 else B.CONV_NHWC
+        layer = ConvLayer(N, C, H, W, K, R, R, 1, pad, dtype=B.CONV_INT8, layout=layout, act=act,
+                          scale=torch.from_numpy(scale).to(dev))
+        layer.prepack(torch.from_numpy(w).to(dev), algo)
+        xin = _to_nc32(x) if nc32 else nchw_to_nhwc(x)
+        y = layer(torch.from_numpy(np.ascontiguousarray(xin)).to(dev),
+                  None if b is None else torch.from_numpy(b).to(dev))
+        B.conv_sync_status(torch.cuda.current_stream().cuda_stream)
+        outs.append(y.cpu().numpy())
+    ref = ol.conv2d_i8(x, nhwc_to_nchw(w), b, scale, pad=pad, relu=relu)
+    ref = _to_nc32(ref) if nc32 else nchw_to_nhwc(ref)
+    assert np.array_equal(outs[0], ref), int((outs[0] != ref).sum())
+    assert np.array_equal(outs[1], ref), int((outs[1] != ref).sum())
