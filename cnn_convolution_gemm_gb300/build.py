@@ -34,20 +34,20 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _deps_hash(src: str) -> str:
+def _deps_hash(src: str, extra: list[str]) -> str:
     h = hashlib.sha256()
     for p in [src] + sorted(glob.glob(os.path.join(CSRC, "*.h")) +
                             glob.glob(os.path.join(CSRC, "*.cuh")) +
                             glob.glob(os.path.join(INCLUDE, "*.h"))):
         with open(p, "rb") as f:
             h.update(f.read())
-    h.update(" ".join(ARCH + NVCC_FLAGS).encode())
+    h.update(" ".join(ARCH + NVCC_FLAGS + extra).encode())
     return h.hexdigest()[:16]
 
 
 def _compile(src: str, extra: list[str]) -> str:
     name = os.path.splitext(os.path.basename(src))[0]
-    obj = os.path.join(BUILD, f"{name}-{_deps_hash(src)}.o")
+    obj = os.path.join(BUILD, f"{name}-{_deps_hash(src, extra)}.o")
     if not os.path.exists(obj):
         tmp = obj + f".tmp{os.getpid()}"
         cmd = [nvcc()] + ARCH + NVCC_FLAGS + extra + ["-c", src, "-o", tmp]
@@ -75,6 +75,14 @@ def build(verbose: bool = False, extra: list[str] | None = None) -> str:
         os.replace(tmp, LIB)
         with open(stamp, "w") as f:
             f.write(key)
+    # objects of earlier sources or flags are not linked again: drop them
+    keep = set(objs)
+    for old in glob.glob(os.path.join(BUILD, "*.o")):
+        if old not in keep:
+            try:
+                os.remove(old)
+            except OSError:
+                pass
     if verbose:
         print(f"built {LIB}")
     return LIB
