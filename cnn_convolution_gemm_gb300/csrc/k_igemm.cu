@@ -462,10 +462,11 @@ __global__ void __launch_bounds__(192, 1)
           int kin = 0;  // k-steps into the current accumulator block
           for (int it = kbeg; it < kend; it += G) {
             // G consecutive stages (a group starts on a stage that is a multiple
-            // of G, so it does not wrap): addresses, then one round of waits
-            // the stages' descriptors, built once: an MMA's are these plus a
-            // constant (the start address counts 16-byte units), which keeps the
-            // issuing thread's work per MMA small (it bounds MMAs of N <= 128)
+            // of G, so it does not wrap): their descriptors, then one round of
+            // waits.  The descriptors are built once per stage and an MMA's are
+            // these plus a constant (the start address counts 16-byte units),
+            // which keeps the issuing thread's work per MMA small (it bounds
+            // MMAs of N <= 128)
             uint64_t ad[G], bd[G];
 #pragma unroll
             for (int g = 0; g < G; ++g) {
