@@ -291,10 +291,13 @@ __global__ void __launch_bounds__(192, 1)
   gb::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // Programmatic dependent launch: the next kernel on the stream may start its
-  // own set-up (this one's above) while this grid drains, and this grid reads
-  // or writes global memory only once the kernel before it has completed.
+  // own set-up (this one's above) while this grid drains.  This grid touches
+  // global memory only after the kernel before it has completed: the producer
+  // waits for it before its first unit's k-steps (the unit's coordinates,
+  // integer divisions on one thread, go before the wait), the epilogue warps
+  // before their first load or store; the MMA thread touches shared memory and
+  // TMEM only.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const int tiles_per_batch = p.m_tiles * p.n_tiles;
   const int num_tiles = tiles_per_batch * (MODE == MODE_BATCHED ? p.batch : p.ksplit);
@@ -356,6 +359,7 @@ __global__ void __launch_bounds__(192, 1)
         const CUtensorMap* const bmap = width == BN ? &tm_w : &tm_wt;
         const uint32_t stage_tx =
             (uint32_t)(C::A_BYTES + (PAIR ? width / 2 : width) * (BK * 2));  // 128-byte rows
+        if (u == unit0) asm volatile("griddepcontrol.wait;" ::: "memory");  // once, see above
         for (int it = kbeg; it < kend; ++it) {
           // Everything the copies need is computed before the wait, so they go
           // out as soon as the stage is free: with the operands in L2 the ring's
@@ -566,40 +570,47 @@ __global__ void __launch_bounds__(192, 1)
       const int s64 = rem > 0 ? (rem + 63) / 64 : 0;
       return s64 < width / 64 ? s64 : width / 64;
     };
-    // residual box (64 columns x 32 rows) for sub-block j of work unit u -> box b
-    auto fetch_res = [&](int u, int j, int b) {
-      int t, noff, width;
-      decode(u, t, noff, width);
-      const int tt = t % tiles_per_batch;
-      const int mt2 = m_tile(tt), nt2 = tt % p.n_tiles;
+    // work unit uu's first output column and this warp's first row in it: the
+    // decode's divisions cost hundreds of cycles on this one warp, so the bf16
+    // path takes them once per unit, for the next unit, before the accumulator
+    // wait (not once per 64-column sub-block)
+    auto unit_pos = [&](int uu, int& ncol, int& mrow) {
+      int t2, noff2, w2;
+      decode(uu, t2, noff2, w2);
+      const int tt2 = t2 % tiles_per_batch;
+      ncol = (tt2 % p.n_tiles) * BN + noff2;
+      mrow = m_tile(tt2) * BM + q * 32;
+    };
+    // residual box (64 columns x 32 rows) of sub-block j of the unit at (ncol, mrow) -> box b
+    auto fetch_res = [&](int ncol, int mrow, int j, int b) {
       uint64_t* bar = &rbar[q * 2 + b];
       gb::mbar_arrive_expect_tx(bar, C::EPI_BOX);
       asm volatile(
           "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
           " [%0], [%1, {%2, %3}], [%4];" ::"r"(gb::smem_u32(sEpi + (q * 2 + b) * C::EPI_BOX)),
-          "l"(reinterpret_cast<uint64_t>(&tm_r)), "r"(nt2 * BN + noff + j * 64),
-          "r"(mt2 * BM + q * 32), "r"(gb::smem_u32(bar))
+          "l"(reinterpret_cast<uint64_t>(&tm_r)), "r"(ncol + j * 64), "r"(mrow),
+          "r"(gb::smem_u32(bar))
           : "memory");
     };
     const bool has_res = MODE == MODE_CONV && p.res != nullptr && p.part == nullptr;
-    // bias of output columns (2 lane, 2 lane + 1) of sub-block j of work unit u
-    // (bf16 epilogue; s2d4: bias of channel c % K)
-    auto bias_pair = [&](int uu, int j) {
-      int t2, noff2, width2;
-      decode(uu, t2, noff2, width2);
-      const int nt2 = (t2 % tiles_per_batch) % p.n_tiles;
-      const int nc = nt2 * BN + noff2 + j * 64 + 2 * lane;
+    // bias of output columns (2 lane, 2 lane + 1) of sub-block j of the unit
+    // whose first column is ncol (bf16 epilogue; s2d4: bias of channel c % K)
+    auto bias_pair = [&](int ncol, int j) {
+      const int nc = ncol + j * 64 + 2 * lane;
       const int bc = p.s2d4_k ? nc % p.s2d4_k : nc;
       float2 bv = make_float2(0.f, 0.f);
       if (p.bias && nc < p.K) bv = make_float2(__ldg(p.bias + bc), __ldg(p.bias + bc + 1));
       return bv;
     };
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // see the producer
+    int ncol_n = 0, mrow_n = 0;  // the next unit's position (here: the first unit's)
+    if (unit0 < num_units) unit_pos(unit0, ncol_n, mrow_n);
     float2 bias_next = make_float2(0.f, 0.f);
     if (!TF32 && MODE == MODE_CONV && !p.i8_y && !p.part && unit0 < num_units)
-      bias_next = bias_pair(unit0, 0);
+      bias_next = bias_pair(ncol_n, 0);
     int pending = -1;  // box with a residual load not yet waited for
     if (has_res && unit0 < num_units) {
-      if (lane == 0) fetch_res(unit0, 0, 0);
+      if (lane == 0) fetch_res(ncol_n, mrow_n, 0, 0);
       pending = 0;
     }
     // pair mode: the even CTA's accumulator-free barriers
@@ -610,6 +621,9 @@ __global__ void __launch_bounds__(192, 1)
       const int bt = t / tiles_per_batch;
       const int tt = t % tiles_per_batch;
       const int mt = m_tile(tt), nt = tt % p.n_tiles;
+      const int ncol = ncol_n, mrow = mrow_n;  // this unit's position
+      const int un = u + ustep;                // the next unit
+      if (un < num_units) unit_pos(un, ncol_n, mrow_n);
       if (!gb::mbar_wait_bounded(&tfull[acc], acc_phase, p.wait_ns, p.err)) break;
       gb::tc_fence_after();
       if (MODE == MODE_CONV && !LIGHT && p.pf_x != nullptr && u + 2 * ustep < num_units) {
@@ -837,25 +851,22 @@ __global__ void __launch_bounds__(192, 1)
         for (int j = 0; j < ns; ++j) {
           const int cur = epi_count & 1;
           uint8_t* box = sEpi + (q * 2 + cur) * C::EPI_BOX;
-          const int nb0 = nt * BN + noff + j * 64;
+          const int nb0 = ncol + j * 64;
+          // the sub-block after this one: (this unit, j + 1) or (the next unit, 0)
+          const bool same = j + 1 < ns;
+          const bool has_nx = same || un < num_units;
+          const int ncol_x = same ? ncol : ncol_n, jx = same ? j + 1 : 0;
           if (has_res) {
             // prefetch the next sub-block's residual into the other box once the
             // store that last read that box is done with it
-            int tn = u, jn = j + 1;
-            if (jn >= ns) {
-              tn = u + ustep;
-              jn = 0;
-            }
-            if (tn < num_units) {
-              if (lane == 0) {
-                gb::bulk_wait_read<0>();
-                fetch_res(tn, jn, cur ^ 1);
-              }
+            if (has_nx && lane == 0) {
+              gb::bulk_wait_read<0>();
+              fetch_res(ncol_x, same ? mrow : mrow_n, jx, cur ^ 1);
             }
             if (!gb::mbar_wait_bounded(&rbar[q * 2 + cur], (rphase >> cur) & 1, p.wait_ns, p.err))
               break;
             rphase ^= 1u << cur;
-            pending = tn < num_units ? (cur ^ 1) : -1;
+            pending = has_nx ? (cur ^ 1) : -1;
           } else {
             if (lane == 0) gb::bulk_wait_read<1>();  // the store that last used this box
             __syncwarp();
@@ -870,14 +881,7 @@ __global__ void __launch_bounds__(192, 1)
           // lane) staged for broadcast reads; then the next sub-block's are loaded
           float* sbias = reinterpret_cast<float*>(sEpi + 4 * 2 * C::EPI_BOX + q * 256);
           reinterpret_cast<float2*>(sbias)[lane] = bias_next;
-          {
-            int tn = u, jn = j + 1;
-            if (jn >= ns) {
-              tn = u + ustep;
-              jn = 0;
-            }
-            if (tn < num_units) bias_next = bias_pair(tn, jn);
-          }
+          if (has_nx) bias_next = bias_pair(ncol_x, jx);
           __syncwarp();
           gb::tmem_ld_wait();
           if (p.act == 0)
