@@ -1041,8 +1041,10 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   gb::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // dependent launch as in the general kernel: the producer and the epilogue
+  // warps wait for the previous grid before their first global access, the
+  // MMA thread not at all
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   // tile t: image t / tiles_per_img, output rows oh0 .. oh0 + RT - 1
   auto tile_pos = [&](int t, int& n, int& oh0) {
     n = t / p.tiles_per_img;
@@ -1053,6 +1055,7 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       // ---- producer: the weight tiles once, then one input strip per tile ----
       gb::mbar_arrive_expect_tx(wbar, p.taps * 64 * 128);
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       for (int tap = 0; tap < p.taps; ++tap)
         gb::tma_load_2d(sW + tap * 64 * 128, &tm_w, wbar, tap * 64, 0);
       int stage = 0;
@@ -1146,6 +1149,7 @@ __global__ void __launch_bounds__(192, 1)
     // ---- epilogue: bias, activation, bf16, 4-D TMA store (virtual pixels clipped) ----
     const int q = warp & 3;
     float* sbias = sBias + q * 64;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     {
       const int c = 2 * lane;  // the 64 biases (channels >= K read as 0)
       sbias[c] = (p.bias && c < p.K) ? __ldg(p.bias + c) : 0.f;
