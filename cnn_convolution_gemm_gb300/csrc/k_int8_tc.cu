@@ -45,6 +45,7 @@
 #include <algorithm>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace {
 
@@ -101,6 +102,7 @@ bool split_weights(const gbconv_desc_s& d) {
 // the same 16 channels are one 16-byte half of a 32-channel block vector).
 __global__ void int8_to_bf16_kernel(const int8_t* __restrict__ x, __nv_bfloat16* __restrict__ y,
                                     long long n16, int C, long long HW, int nc32) {
+  gb::allow_dependents();  // the GEMM that reads y sets up meanwhile
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n16;
        i += (long long)gridDim.x * blockDim.x) {
     long long src = i;  // in 16-byte units

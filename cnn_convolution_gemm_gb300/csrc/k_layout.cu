@@ -59,6 +59,7 @@ template <int C_OUT>
 __global__ void nchw_f32_to_nhwc_bf16_quad_kernel(const float* __restrict__ x,
                                                   __nv_bfloat16* __restrict__ y, int C,
                                                   long long hw, long long quads) {
+  gb::allow_dependents();
   for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < quads;
        q += (long long)gridDim.x * blockDim.x) {
     const long long p = q * 4;
@@ -151,6 +152,7 @@ __global__ void maxpool_nhwc_bf16_kernel(const __nv_bfloat16* __restrict__ x,
 __global__ void maxpool3_nhwc_bf16_kernel(const __nv_bfloat16* __restrict__ x,
                                           __nv_bfloat16* __restrict__ y, int N, int C, int H,
                                           int W, int stride, int pad, int OH, int OW) {
+  gb::allow_dependents();
   const int cv = C / 8;
   const int item = blockIdx.x * blockDim.x + threadIdx.x;
   if (item >= OW * cv) return;
@@ -192,6 +194,7 @@ __global__ void __launch_bounds__(32 * kPoolParts)
     avgpool_nhwc_bf16_kernel(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ y,
                              int C, int HW, int groups_per_image) {
   __shared__ float4 part[kPoolParts][32][2];
+  gb::allow_dependents();
   const int cv = C / 8;
   const int n = blockIdx.x / groups_per_image;
   const int c8 = (blockIdx.x - n * groups_per_image) * 32 + (threadIdx.x & 31);

@@ -10,6 +10,7 @@
 #include <algorithm>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace {
 
@@ -23,6 +24,7 @@ __global__ void splitk_reduce_bf16_kernel(const float4* __restrict__ part, int k
                                           long long vecs, int K, const float* __restrict__ bias,
                                           const uint2* __restrict__ res, uint2* __restrict__ y,
                                           int act) {
+  gb::allow_dependents();  // the next layer's GEMM sets up meanwhile
   for (long long v = blockIdx.x * (long long)blockDim.x + threadIdx.x; v < vecs;
        v += (long long)gridDim.x * blockDim.x) {
     float4 a = __ldg(part + v);

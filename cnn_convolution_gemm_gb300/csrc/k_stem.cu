@@ -20,6 +20,7 @@
 #include <algorithm>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace {
 
@@ -149,6 +150,7 @@ gbconv_desc_s stem4_desc(const gbconv_desc_s& d) {
 // 4 C contiguous values, copied to channels dy * 4C .. of the block pixel
 __global__ void space_to_depth4_kernel(const uint4* __restrict__ x, uint4* __restrict__ x4,
                                        int N, int H, int W, int C) {
+  gb::allow_dependents();  // the block-grid GEMM sets up meanwhile
   const int BH = H / 4, BW = W / 4, v = C / 2;  // v: 16-byte vectors per 4 pixels
   const long long total = (long long)N * BH * BW * 4;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;

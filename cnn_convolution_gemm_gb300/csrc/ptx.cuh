@@ -21,6 +21,14 @@ __device__ __forceinline__ void record_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
 
+// Programmatic dependent launch: lets the next kernel on the stream, when it is
+// launched for it (the implicit GEMMs are), start its own set-up while this
+// grid runs.  That kernel still waits for this grid's completion, and for its
+// memory operations, before it touches global memory (griddepcontrol.wait).
+__device__ __forceinline__ void allow_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- mbarrier ---------------------------------------------------------------
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
